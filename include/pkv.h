@@ -1,0 +1,273 @@
+/*
+ * pkv.h -- C ABI of libpkv: decode attention over a paged KV cache on GB300.
+ *
+ * The cache keeps every sequence's keys and values in fixed 16-token
+ * physical blocks drawn from one shared pool; a per-sequence block table maps
+ * logical block i (tokens 16i .. 16i+15) to a physical block.  Blocks can be
+ * shared between sequences with reference counts and are copied on the first
+ * write to a shared block.  Decode attends one query token per sequence over
+ * its cached tokens, with grouped-query heads, optional FP8-E4M3 storage with
+ * per-token scales, optional sliding-window or sink + window keep-sets, and
+ * optional H2O accumulated-score output and keep-set selection.
+ *
+ * Sources (page title, section):
+ *   [LC] "长上下文优化：注意力稀疏化与 KV Cache 管理": KV bytes per token;
+ *        sliding-window mask; StreamingKVCache; H2OEviction; block-table
+ *        sketch; GQA head counts.
+ *   [PA] "KV Cache 与 PagedAttention：显存复用与长上下文推理": sections
+ *        PagedAttention 的设计, 物理布局示意, 三大运行时组件 (block allocator,
+ *        block table, reference count + copy-on-write), the Block/copy_on_write
+ *        sketch, 量化原理 (FP8 E4M3, per-token scaling), and the monitoring
+ *        note (free/used blocks).
+ *   [SO] "系统优化": 滑动窗口注意力 / StreamingLLM 详解 (sinks + window), KV
+ *        Cache 淘汰 (H2O), Flash Attention (tiled online softmax).
+ *
+ * Conventions
+ *   - Every call returns a pkv_status; nothing throws across the ABI.
+ *     pkv_last_error() gives a message for the calling thread's last failure.
+ *   - "device" pointers are CUDA device memory owned by the caller; the
+ *     library never frees them.  "host" pointers are ordinary host memory.
+ *     The library owns only its host-side allocator state and pinned staging
+ *     buffers.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Device work is enqueued asynchronously on it; host arrays
+ *     passed in are fully consumed before the call returns.
+ *   - A pool is used from one host thread at a time.
+ *   - Layouts (row-major, innermost last):
+ *       k_pool, v_pool  [num_blocks][n_kv_heads][16][head_dim]  kv dtype
+ *       k_scale,v_scale [num_blocks][n_kv_heads][16]            fp32 (FP8 only)
+ *       block_tables    [max_seqs][max_blocks_per_seq]          int32, -1 = none
+ *       q, out          [n_seqs][n_heads][head_dim]   fp32 (fp32 KV) else bf16
+ *       lse             [n_seqs][n_heads]                        fp32, natural log
+ *       logits          [n_seqs][n_kv_heads][logits_stride][G]   fp32
+ *     with G = n_heads / n_kv_heads; query head h reads kv head h / G.
+ *   - Device-side failures (a bounded wait that ran out, a table entry out of
+ *     range) set the pool's device status word; pkv_sync_status() reports
+ *     and clears them.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_BLOCK_SIZE 16
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,   /* bad argument; state unchanged */
+  PKV_ERR_UNSUPPORTED = 2,   /* valid but unsupported shape or dtype */
+  PKV_ERR_OUT_OF_BLOCKS = 3, /* the free pool cannot cover the request; state unchanged */
+  PKV_ERR_OUT_OF_SEQS = 4,   /* every sequence id is in use */
+  PKV_ERR_CUDA = 5,          /* a CUDA runtime call failed (message in pkv_last_error) */
+  PKV_ERR_TIMEOUT = 6,       /* a device-side bounded wait ran out */
+  PKV_ERR_DEVICE_ASSERT = 7, /* a device-side range check failed */
+  PKV_ERR_NO_DEVICE = 8,     /* device work requested on a host-only pool */
+  PKV_ERR_WORKSPACE = 9      /* workspace too small (see pkv_decode_workspace_size) */
+} pkv_status;
+
+typedef enum { PKV_KV_FP32 = 0, PKV_KV_BF16 = 1, PKV_KV_FP8_E4M3 = 2 } pkv_kv_dtype;
+
+/* Keep-sets for decode query position i = L - 1 over keys j in [0, L):
+ *   FULL         every key.
+ *   SLIDING      |i - j| <= window ([LC] sliding-window mask), i.e. the
+ *                window + 1 keys j >= L - 1 - window.
+ *   SINK_WINDOW  [LC] StreamingKVCache / [SO] StreamingLLM: when L exceeds
+ *                num_sinks + window, keys j < num_sinks and j >= L - window;
+ *                otherwise every key. */
+typedef enum { PKV_MASK_FULL = 0, PKV_MASK_SLIDING = 1, PKV_MASK_SINK_WINDOW = 2 } pkv_mask_mode;
+
+/* [PA] PagedAttention 的设计 / 三大运行时组件.  Shapes supported: block_size
+ * 16; head_dim 128 for BF16/FP8 and 64 or 128 for FP32; G in {1, 2, 4, 8}. */
+typedef struct {
+  int32_t num_blocks;         /* physical blocks in the pool */
+  int32_t block_size;         /* must be 16 */
+  int32_t n_heads;            /* query heads */
+  int32_t n_kv_heads;         /* KV heads (GQA: n_heads % n_kv_heads == 0) */
+  int32_t head_dim;
+  int32_t max_seqs;           /* rows of the block table */
+  int32_t max_blocks_per_seq; /* columns of the block table */
+  int32_t kv_dtype;           /* pkv_kv_dtype */
+  uint64_t alloc_seed;        /* initial free-pool order: Fisher-Yates shuffle of
+                                 [0, num_blocks) driven by splitmix64(alloc_seed);
+                                 0 = ascending order */
+  const int32_t* free_order;  /* host, optional: explicit initial free-pool order
+                                 (num_blocks distinct ids, front first); overrides
+                                 alloc_seed; copied during create */
+} pkv_pool_config;
+
+/* Device buffers of a pool, all allocated and owned by the caller. */
+typedef struct {
+  void* k_pool;          /* device, [num_blocks][n_kv_heads][16][head_dim] */
+  void* v_pool;          /* device, same shape */
+  float* k_scale;        /* device, [num_blocks][n_kv_heads][16] (FP8 only, else NULL) */
+  float* v_scale;        /* device, same (FP8 only, else NULL) */
+  int32_t* block_tables; /* device, [max_seqs][max_blocks_per_seq]; the library
+                            initialises it to -1 during create and keeps it in
+                            step with the host tables */
+  int32_t* status;       /* device, 4 int32: device error word, zeroed by create */
+} pkv_pool_buffers;
+
+typedef struct {
+  size_t k_pool, v_pool, k_scale, v_scale, block_tables, status; /* bytes */
+} pkv_buffer_sizes;
+
+typedef struct {
+  int64_t num_blocks, free_blocks, used_blocks;
+  int64_t shared_blocks; /* blocks with refcount > 1 */
+  int64_t active_seqs;
+  int64_t cow_copies;    /* copy-on-write block copies so far */
+  int64_t blocks_allocated, blocks_freed;
+} pkv_stats;
+
+typedef struct pkv_pool pkv_pool;
+
+/* ---- pool lifetime ------------------------------------------------------ */
+
+/* Bytes each device buffer of a pool with this config needs. */
+pkv_status pkv_pool_required_bytes(const pkv_pool_config* cfg, pkv_buffer_sizes* out);
+
+/* Creates a pool.  `buffers` NULL gives a host-only pool: the allocator calls
+ * work, device calls return PKV_ERR_NO_DEVICE.  With buffers, the current CUDA
+ * device must be the one that holds them; the block tables are set to -1 and
+ * the status word to 0 (synchronously). */
+pkv_status pkv_pool_create(const pkv_pool_config* cfg, const pkv_pool_buffers* buffers,
+                           pkv_pool** out);
+void pkv_pool_destroy(pkv_pool* pool);
+
+/* ---- sequences (host allocator, [PA] 三大运行时组件) ---------------------- */
+
+/* New empty sequence; the id is the smallest one not in use. */
+pkv_status pkv_seq_add(pkv_pool* pool, int32_t* seq_out);
+/* New sequence sharing every block of `src` (refcount + 1 each): parallel
+ * sampling / beam fork ([PA] 共享场景的价值). */
+pkv_status pkv_seq_fork(pkv_pool* pool, int32_t src, int32_t* dst_out);
+/* Drops every block reference (blocks reaching 0 return to the front of the
+ * free pool, in ascending logical order) and releases the id. */
+pkv_status pkv_seq_free(pkv_pool* pool, int32_t seq);
+/* Shortens a sequence to new_len tokens, dropping blocks past it (ascending).
+ * Refused if the new last block is partial and was evicted. */
+pkv_status pkv_seq_truncate(pkv_pool* pool, int32_t seq, int32_t new_len);
+/* StreamingLLM eviction ([LC] StreamingKVCache, [SO] StreamingLLM 详解): drops
+ * every block lying wholly outside [0, num_sinks) U [L - window, L); those
+ * table entries become -1.  No-op when L <= num_sinks + window.  window >= 1. */
+pkv_status pkv_seq_evict(pkv_pool* pool, int32_t seq, int32_t num_sinks, int32_t window);
+pkv_status pkv_seq_len(const pkv_pool* pool, int32_t seq, int32_t* len_out);
+/* Copies ceil(len/16) table entries of `seq` into host_out (capacity cap). */
+pkv_status pkv_get_block_table(const pkv_pool* pool, int32_t seq, int32_t* host_out, int32_t cap,
+                               int32_t* n_out);
+pkv_status pkv_pool_stats(const pkv_pool* pool, pkv_stats* out);
+
+/* Allocator step of an append ([PA] copy_on_write sketch), host side only.
+ * For each listed sequence in order, for each of T new tokens at position p:
+ * p % 16 == 0 takes the front block of the free pool; otherwise a shared last
+ * block (refcount > 1) is first copied to a fresh block (copy-on-write).
+ * Writes slots[i*T + t] = block * 16 + p % 16 (host, may be NULL) and the COW
+ * (src, dst) pairs (host [cow_cap][2], may be NULL).  All or nothing:
+ * PKV_ERR_OUT_OF_BLOCKS leaves the state unchanged.  On a device pool the
+ * block copies and table updates are queued and run at the start of the next
+ * call that takes a stream. */
+pkv_status pkv_reserve_slots(pkv_pool* pool, int32_t n_seqs, const int32_t* seq_ids, int32_t T,
+                             int64_t* slots_out, int32_t* cow_pairs_out, int32_t cow_cap,
+                             int32_t* n_cow_out);
+
+/* ---- device work -------------------------------------------------------- */
+
+/* Appends T tokens per sequence: pkv_reserve_slots, then on `stream` the
+ * queued COW block copies (whole blocks: K, V and scales of every kv head),
+ * the table updates and the scatter of the new rows into their slots.
+ * k_new, v_new: device [n_seqs][T][n_kv_heads][head_dim], fp32 for an FP32
+ * pool, bf16 otherwise.  FP8 pools quantise each (token, kv head) row:
+ * s = absmax / 448 in fp32 (1 when absmax is 0), code = E4M3(x / s) with
+ * round-to-nearest-even and saturation to +-448 ([PA] 量化原理). */
+pkv_status pkv_append(pkv_pool* pool, void* stream, int32_t n_seqs, const int32_t* seq_ids,
+                      int32_t T, const void* k_new, const void* v_new);
+
+/* Workspace bytes pkv_decode_attn needs for n_seqs sequences and the given
+ * num_splits (0 = automatic). */
+pkv_status pkv_decode_workspace_size(const pkv_pool* pool, int32_t n_seqs, int32_t num_splits,
+                                     size_t* bytes_out);
+
+/* Decode attention ([PA] decode loads KV block by block through the table;
+ * [SO] Flash Attention's tiled online softmax).  For each listed sequence b
+ * (context length L_b, the current token included) and query head h:
+ *   s_j = scale * q[b][h] . K_j   for kept keys j (FP8: K_j = code_j * s_j)
+ *   out[b][h] = sum_j softmax(s)_j V_j,   lse[b][h] = ln sum_j exp(s_j)
+ * Empty keep-set: out = 0, lse = -inf.
+ *   q, out      device [n_seqs][n_heads][head_dim] (fp32 for FP32 pools, else bf16)
+ *   lse         device [n_seqs][n_heads] fp32, or NULL
+ *   logits      device [n_seqs][n_kv_heads][logits_stride][G] fp32, or NULL:
+ *               receives s_j of every kept key (for pkv_h2o_scores); other
+ *               positions are left untouched.  logits_stride >= max L_b.
+ *   num_splits  0: the keys of all sequences are split evenly over the GPU's
+ *               warps; n > 0: each (sequence, kv head) range is cut into n
+ *               equal parts.  Partial results are merged by log-sum-exp.
+ *   workspace   device scratch of at least pkv_decode_workspace_size bytes;
+ *               it must not be in use by other work on the GPU meanwhile.
+ * Every block of the keep-set must be present (not evicted): else
+ * PKV_ERR_INVALID_ARG. */
+pkv_status pkv_decode_attn(pkv_pool* pool, void* stream, int32_t n_seqs, const int32_t* seq_ids,
+                           const void* q, float scale, int32_t mask_mode, int32_t num_sinks,
+                           int32_t window, int32_t num_splits, void* out, float* lse,
+                           float* logits, int64_t logits_stride, void* workspace,
+                           size_t workspace_bytes);
+
+/* H2O score update ([LC] H2OEviction.update_scores): for each listed sequence
+ * and each kept key j, acc[b][j] += (1/n_heads) * sum_h exp(s_hj - lse_h),
+ * the attention weight summed over the single decode query and averaged over
+ * all query heads.  logits/lse as written by pkv_decode_attn with the same
+ * sequences and keep-set.  acc: device [n_seqs][acc_stride] fp32. */
+pkv_status pkv_h2o_scores(pkv_pool* pool, void* stream, int32_t n_seqs, const int32_t* seq_ids,
+                          const float* logits, int64_t logits_stride, const float* lse,
+                          int32_t mask_mode, int32_t num_sinks, int32_t window, float* acc,
+                          int64_t acc_stride);
+
+/* H2O keep-set ([LC] H2OEviction.select, [SO] evict_tokens with recent = 0):
+ * with keep = budget - recent, the positions [L - recent, L) plus the keep
+ * highest acc values among [0, L - recent) (ties to the lower position), in
+ * ascending order; all of [0, L) when L <= budget.  lens: host [n_seqs].
+ * acc: device [n_seqs][acc_stride] fp32 (>= 0).  keep_idx: device
+ * [n_seqs][keep_stride] int32 (keep_stride >= budget); keep_count: device
+ * [n_seqs] int32.  0 <= recent <= budget. */
+pkv_status pkv_h2o_select(pkv_pool* pool, void* stream, int32_t n_seqs, const int32_t* lens,
+                          const float* acc, int64_t acc_stride, int32_t budget, int32_t recent,
+                          int32_t* keep_idx, int64_t keep_stride, int32_t* keep_count);
+
+/* Synchronises `stream`, then reports and clears the device status word:
+ * PKV_ERR_TIMEOUT, PKV_ERR_DEVICE_ASSERT or PKV_OK. */
+pkv_status pkv_sync_status(pkv_pool* pool, void* stream);
+
+/* ---- measurement -------------------------------------------------------- */
+
+typedef enum {
+  PKV_KERNEL_COW_COPY = 0,
+  PKV_KERNEL_APPEND = 1,
+  PKV_KERNEL_DECODE = 2,
+  PKV_KERNEL_COMBINE = 3,
+  PKV_KERNEL_H2O_SCORE = 4,
+  PKV_KERNEL_H2O_SELECT = 5,
+  PKV_KERNEL_TABLE_PATCH = 6,
+  PKV_KERNEL_COUNT = 7
+} pkv_kernel_id;
+
+/* When enabled, each kernel launch is bracketed by CUDA events on its stream. */
+pkv_status pkv_timing_enable(pkv_pool* pool, int32_t enable);
+/* Synchronises on the recorded events and returns, per kernel id, the summed
+ * device time (ms) and launch count since the last reset; then resets. */
+pkv_status pkv_timing_read(pkv_pool* pool, double* total_ms_out /* [PKV_KERNEL_COUNT] */,
+                           int64_t* launches_out /* [PKV_KERNEL_COUNT] */);
+/* Total kernel launches issued by this pool so far (all kernels). */
+pkv_status pkv_launch_count(const pkv_pool* pool, int64_t* out);
+
+const char* pkv_last_error(void);
+const char* pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

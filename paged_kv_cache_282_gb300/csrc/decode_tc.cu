@@ -1,0 +1,619 @@
+// decode_tc.cu -- decode attention over the paged KV cache, BF16 and FP8-E4M3
+// KV, head_dim 128, GQA group G in {1, 2, 4, 8}; sm_103a.
+//
+// What it computes (pages: "KV Cache 与 PagedAttention：显存复用与长上下文推理",
+// PagedAttention 的设计 -- decode loads KV block by block through the block
+// table; "系统优化", Flash Attention -- tiled online softmax; "长上下文优化：
+// 注意力稀疏化与 KV Cache 管理", GQA): for each (sequence, kv head) and the G
+// query heads that share it, softmax(scale * q K^T) V over the kept keys.
+//
+// GB300 design:
+//  - Work unit = one 16-token block of one kv head: a 4 KB (BF16) or 2 KB
+//    (FP8) K chunk plus the same for V, each contiguous in HBM.  The host cuts
+//    the concatenated units of all (sequence, kv head) pairs into equal
+//    contiguous runs, one per warp of a persistent grid (one CTA per SM), so
+//    ragged lengths balance exactly; partial results are merged by the
+//    log-sum-exp combine kernel.
+//  - Every warp owns a private ring of shared-memory stages filled by TMA
+//    (cp.async.bulk.tensor, 2-D tiles of 16 rows x 128 bytes with the 128-byte
+//    swizzle, so the fragment loads below are bank-conflict free) and
+//    completed through mbarrier transaction counts.  Lane 0 refills a stage as
+//    soon as the warp has consumed it; physical block ids for the next 32
+//    units are fetched one batch ahead.
+//  - Every K/V byte is read once per GQA group: the G query heads are the N
+//    dimension of m16n8k16 tensor-core MMAs (S = K Q^T, then O^T = V^T P),
+//    with fp32 accumulation.  The path is HBM-bound (4 flop/byte for BF16,
+//    G = 4); the MMAs only keep instruction issue far below the memory time.
+//  - FP8: codes are widened to fp16 in registers (exact); the per-token K
+//    scale multiplies the logit, and the per-token V scale is folded into the
+//    softmax weight through the exponent (b_j = a_j + log2 vs_j), so the fp16
+//    weights never exceed 1 and the running max stays consistent.
+//  - Every wait is bounded: after about 4 s the warp sets the status word,
+//    drains its own copies in flight (bounded again) and returns.
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr uint64_t kTimeoutNs = 4000000000ull;
+constexpr uint64_t kDrainTimeoutNs = 50000000ull;
+
+template <int KV>
+struct TC;
+template <>
+struct TC<1> {  // BF16
+  static constexpr int kWarps = 8, kStages = 3;
+  static constexpr int kStageBytes = 8192;  // K: 2 swizzled boxes of 2 KB, V: same
+  static constexpr int kScaleBytes = 0;
+  static constexpr uint32_t kTxBytes = 8192;
+};
+template <>
+struct TC<2> {  // FP8 E4M3
+  static constexpr int kWarps = 8, kStages = 5;
+  static constexpr int kStageBytes = 4096;  // K: one swizzled box of 2 KB, V: same
+  static constexpr int kScaleBytes = 128;   // 16 K scales + 16 V scales
+  static constexpr uint32_t kTxBytes = 4096 + 128;
+};
+
+template <int KV>
+constexpr size_t smem_bytes() {
+  return 1024 + (size_t)TC<KV>::kWarps * TC<KV>::kStages * (TC<KV>::kStageBytes + TC<KV>::kScaleBytes) +
+         (size_t)TC<KV>::kWarps * TC<KV>::kStages * 8;
+}
+
+// ---------------------------------------------------------------------------
+// PTX helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t global_timer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on phase `parity` of an mbarrier.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63) == 0 && global_timer() - t0 > limit_ns) return false;
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// two E4M3 codes (low byte first) -> two fp16 (low half first); exact
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xFFFFu), __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+__device__ __forceinline__ bool kept(int j, int L, int mode, int S, int W) {
+  if (j >= L) return false;
+  if (mode == 0) return true;
+  if (mode == 1) return (L - 1 - j) <= W;
+  if ((long long)L <= (long long)S + W) return true;
+  return j < S || j >= L - W;
+}
+
+// Walk a unit cursor (piece index, logical block) forward by n units.
+__device__ __forceinline__ void advance(const Piece* __restrict__ P, int pe, int& ip, int& il, int n) {
+  while (ip < pe) {
+    const int end = P[ip].lblk_end;
+    if (il + n < end) {
+      il += n;
+      return;
+    }
+    n -= end - il;
+    ++ip;
+    if (ip < pe) il = P[ip].lblk_begin;
+  }
+}
+
+// Row coordinate (block * Hk + kv_head) * 16 of the unit `lane` positions past
+// the cursor, or -1 past the end.
+__device__ __forceinline__ int unit_row(const DecodeTCParams& p, int pe, int ip, int il, int lane) {
+  advance(p.pieces, pe, ip, il, lane);
+  if (ip >= pe) return -1;
+  const Piece pc = p.pieces[ip];
+  int blk = p.tables[(size_t)pc.seq_slot * p.max_blocks + il];
+  if (blk < 0 || blk >= p.num_blocks) {
+    atomicOr(p.status, kStatusBadBlock);
+    p.status[1] = pc.seq_slot;
+    p.status[2] = il;
+    blk = 0;  // keep the copy in bounds; the status word reports the fault
+  }
+  return (blk * p.n_kv_heads + pc.kv_head) * kBlock;
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+
+template <int KV, int G>
+__global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const __grid_constant__ DecodeTCParams p) {
+  using C = TC<KV>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
+  const int gw = blockIdx.x * C::kWarps + wl;
+  if (gw >= p.total_warps) return;
+  const int pb = p.warp_begin[gw], pe = p.warp_begin[gw + 1];
+  if (pb >= pe) return;
+
+  const uint32_t data = smem_addr(base) + (uint32_t)(wl * S * C::kStageBytes);
+  const uint32_t scl = smem_addr(base) + (uint32_t)(C::kWarps * S * C::kStageBytes + wl * S * C::kScaleBytes);
+  const uint32_t bars =
+      smem_addr(base) + (uint32_t)(C::kWarps * S * (C::kStageBytes + C::kScaleBytes) + wl * S * 8);
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(bars + 8 * s, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncwarp();
+
+  const int r = lane >> 2, c = lane & 3;
+  const int Hk = p.n_kv_heads, H = p.n_heads;
+  const float sl2 = p.scale * kLog2e;
+
+  // total units of this warp
+  int n_units = 0;
+  for (int k = pb; k < pe; ++k) n_units += p.pieces[k].lblk_end - p.pieces[k].lblk_begin;
+
+  // issue side: rows of the current and the next batch of 32 units
+  int bip = pb, bil = p.pieces[pb].lblk_begin;  // cursor at the current batch start
+  int cur_rows = unit_row(p, pe, bip, bil, lane);
+  int nip = bip, nil = bil;
+  advance(p.pieces, pe, nip, nil, 32);
+  int next_rows = unit_row(p, pe, nip, nil, lane);
+  int batch_base = 0;
+  int issued = 0;
+
+  auto issue = [&](int v) {  // all lanes; lane 0 issues the copies of unit v
+    if (v - batch_base >= 32) {
+      batch_base += 32;
+      cur_rows = next_rows;
+      advance(p.pieces, pe, nip, nil, 32);
+      next_rows = unit_row(p, pe, nip, nil, lane);
+    }
+    const int row = __shfl_sync(kFull, cur_rows, v - batch_base);
+    if (lane == 0) {
+      const int st = v % S;
+      const uint32_t bar = bars + 8 * st;
+      const uint32_t dst = data + (uint32_t)(st * C::kStageBytes);
+      mbar_expect_tx(bar, C::kTxBytes);
+      if (KV == 1) {
+        tma_load_2d(dst, &p.tmap_k, 0, row, bar);
+        tma_load_2d(dst + 2048, &p.tmap_k, 64, row, bar);
+        tma_load_2d(dst + 4096, &p.tmap_v, 0, row, bar);
+        tma_load_2d(dst + 6144, &p.tmap_v, 64, row, bar);
+      } else {
+        tma_load_2d(dst, &p.tmap_k, 0, row, bar);
+        tma_load_2d(dst + 2048, &p.tmap_v, 0, row, bar);
+        const uint32_t sd = scl + (uint32_t)(st * C::kScaleBytes);
+        bulk_load(sd, p.k_scale + row, 64, bar);
+        bulk_load(sd + 64, p.v_scale + row, 64, bar);
+      }
+    }
+  };
+
+  for (; issued < n_units && issued < S; ++issued) issue(issued);
+
+  // per-lane fragment address pieces
+  const int mi = lane >> 3, rr = lane & 7;
+  // bf16 K (ldmatrix, non-transposed): matrices (tok 0-7|8-15) x (d lo|hi 8)
+  const uint32_t k_row_off = (uint32_t)((rr + ((mi & 1) << 3)) * 128);
+  const int k_hi = mi >> 1;
+  // bf16 V (ldmatrix, transposed): matrices (d lo|hi 8) x (tok 0-7|8-15)
+  const uint32_t v_row_off = (uint32_t)((rr + ((mi >> 1) << 3)) * 128);
+  const int v_hi = mi & 1;
+
+  uint32_t qf[8][2];
+  float o[8][4];
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  bool run_open = false;
+  int u = 0;
+
+  for (int pi = pb; pi < pe; ++pi) {
+    const Piece pc = p.pieces[pi];
+    const int g = pc.kv_head, L = pc.ctx_len;
+    if (!run_open) {
+      // Q^T fragments (B operand): rows k = head-dim slots, column n = query head r
+      const int h = g * G + r;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t b0 = 0, b1 = 0;
+        if (r < G) {
+          const __nv_bfloat16* qrow = reinterpret_cast<const __nv_bfloat16*>(p.q) + ((size_t)pc.q_row * H + h) * 128;
+          if (KV == 1) {
+            b0 = *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * c);
+            b1 = *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 8 + 2 * c);
+          } else {
+            // FP8 path: k-slot 2c+e <-> d = 32c + 4kk + e, slot 2c+8+e <-> d + 2
+            const uint2 raw = *reinterpret_cast<const uint2*>(qrow + 32 * c + 4 * kk);
+            const __nv_bfloat162 x01 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+            const __nv_bfloat162 x23 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+            b0 = pack_f16(__low2float(x01), __high2float(x01));
+            b1 = pack_f16(__low2float(x23), __high2float(x23));
+          }
+        }
+        qf[kk][0] = b0;
+        qf[kk][1] = b1;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+      m0 = m1 = -INFINITY;
+      l0 = l1 = 0.f;
+      run_open = true;
+    }
+
+    for (int lb = pc.lblk_begin; lb < pc.lblk_end; ++lb, ++u) {
+      const int st = u % S;
+      if (!mbar_wait(bars + 8 * st, (uint32_t)((u / S) & 1), kTimeoutNs)) {
+        if (lane == 0) {
+          atomicOr(p.status, kStatusTimeout);
+          p.status[1] = gw;
+        }
+        for (int v = u + 1; v < issued; ++v) mbar_wait(bars + 8 * (v % S), (uint32_t)((v / S) & 1), kDrainTimeoutNs);
+        return;
+      }
+      const uint32_t kb = data + (uint32_t)(st * C::kStageBytes);
+      const uint32_t vb = kb + (KV == 1 ? 4096u : 2048u);
+
+      // ---- S = K Q^T : rows = tokens, columns = query heads of the group
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      float ks_r = 1.f, ks_r8 = 1.f, lv_r = 0.f, lv_r8 = 0.f;
+      if (KV == 1) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int c16 = 2 * kk + k_hi;  // 16-byte chunk index across the 256-byte row
+          uint32_t a[4];
+          ldsm_x4(kb + (uint32_t)((c16 >> 3) * 2048) + k_row_off + (uint32_t)((((c16 & 7) ^ rr)) << 4), a);
+          if (kk & 1)
+            mma_bf16(sb, a, qf[kk][0], qf[kk][1]);
+          else
+            mma_bf16(sa, a, qf[kk][0], qf[kk][1]);
+        }
+      } else {
+        // tokens r and r + 8, codes d in [32c, 32c + 32)
+        const uint4 x0 = lds128(kb + (uint32_t)(r * 128) + (uint32_t)(((2 * c) ^ r) << 4));
+        const uint4 x1 = lds128(kb + (uint32_t)(r * 128) + (uint32_t)(((2 * c + 1) ^ r) << 4));
+        const uint4 y0 = lds128(kb + (uint32_t)((r + 8) * 128) + (uint32_t)(((2 * c) ^ r) << 4));
+        const uint4 y1 = lds128(kb + (uint32_t)((r + 8) * 128) + (uint32_t)(((2 * c + 1) ^ r) << 4));
+        const uint32_t tA[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        const uint32_t tB[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          uint32_t a[4];
+          a[0] = e4m3x2_to_f16x2(tA[kk]);
+          a[1] = e4m3x2_to_f16x2(tB[kk]);
+          a[2] = e4m3x2_to_f16x2(tA[kk] >> 16);
+          a[3] = e4m3x2_to_f16x2(tB[kk] >> 16);
+          if (kk & 1)
+            mma_f16(sb, a, qf[kk][0], qf[kk][1]);
+          else
+            mma_f16(sa, a, qf[kk][0], qf[kk][1]);
+        }
+        const uint32_t sc = scl + (uint32_t)(st * C::kScaleBytes);
+        ks_r = lds_f32(sc + 4 * r);
+        ks_r8 = lds_f32(sc + 4 * (r + 8));
+        lv_r = log2f(lds_f32(sc + 64 + 4 * r));
+        lv_r8 = log2f(lds_f32(sc + 64 + 4 * (r + 8)));
+      }
+      const float s0 = (sa[0] + sb[0]) * ks_r, s1 = (sa[1] + sb[1]) * ks_r;
+      const float s2 = (sa[2] + sb[2]) * ks_r8, s3 = (sa[3] + sb[3]) * ks_r8;
+
+      // ---- mask, logits out, online softmax (log2 units)
+      const int tok0 = lb * kBlock + r, tok1 = tok0 + 8;
+      const bool k0 = kept(tok0, L, p.mask_mode, p.num_sinks, p.window);
+      const bool k1 = kept(tok1, L, p.mask_mode, p.num_sinks, p.window);
+      const bool h0v = 2 * c < G, h1v = 2 * c + 1 < G;
+      if (p.logits != nullptr) {
+        float* lg = p.logits + ((size_t)pc.q_row * Hk + g) * p.logits_stride * G;
+        if (k0 && h0v) lg[(size_t)tok0 * G + 2 * c] = s0 * p.scale;
+        if (k0 && h1v) lg[(size_t)tok0 * G + 2 * c + 1] = s1 * p.scale;
+        if (k1 && h0v) lg[(size_t)tok1 * G + 2 * c] = s2 * p.scale;
+        if (k1 && h1v) lg[(size_t)tok1 * G + 2 * c + 1] = s3 * p.scale;
+      }
+      const float a0 = k0 ? s0 * sl2 : -INFINITY, a1 = k0 ? s1 * sl2 : -INFINITY;
+      const float a2 = k1 ? s2 * sl2 : -INFINITY, a3 = k1 ? s3 * sl2 : -INFINITY;
+      // b = a + log2(v scale): the exponent of the weight that multiplies V
+      const float e0 = a0 + lv_r, e1 = a1 + lv_r, e2 = a2 + lv_r8, e3 = a3 + lv_r8;
+      float bm0 = fmaxf(e0, e2), bm1 = fmaxf(e1, e3);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, off));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
+      }
+      const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+      const float z0 = mn0 == -INFINITY ? 0.f : mn0, z1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float al0 = exp2f(m0 - z0), al1 = exp2f(m1 - z1);
+      const float p0 = exp2f(e0 - z0), p1 = exp2f(e1 - z1), p2 = exp2f(e2 - z0), p3 = exp2f(e3 - z1);
+      if (KV == 1) {
+        l0 = l0 * al0 + (p0 + p2);
+        l1 = l1 * al1 + (p1 + p3);
+      } else {
+        l0 = l0 * al0 + (exp2f(a0 - z0) + exp2f(a2 - z0));
+        l1 = l1 * al1 + (exp2f(a1 - z1) + exp2f(a3 - z1));
+      }
+      m0 = mn0;
+      m1 = mn1;
+      if (__any_sync(kFull, (al0 != 1.f) || (al1 != 1.f))) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          o[i][0] *= al0;
+          o[i][1] *= al1;
+          o[i][2] *= al0;
+          o[i][3] *= al1;
+        }
+      }
+
+      // ---- O^T += V^T P : rows = head-dim, columns = query heads
+      const uint32_t pb0 = movmatrix_t(KV == 1 ? pack_bf16(p0, p1) : pack_f16(p0, p1));
+      const uint32_t pb1 = movmatrix_t(KV == 1 ? pack_bf16(p2, p3) : pack_f16(p2, p3));
+      if (KV == 1) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int c16 = 2 * i + v_hi;
+          uint32_t a[4];
+          ldsm_x4_t(vb + (uint32_t)((c16 >> 3) * 2048) + v_row_off + (uint32_t)((((c16 & 7) ^ rr)) << 4), a);
+          mma_bf16(o[i], a, pb0, pb1);
+        }
+      } else {
+        // tokens 2c, 2c+1, 2c+8, 2c+9; codes d in [16r, 16r + 16)
+        const uint4 va = lds128(vb + (uint32_t)((2 * c) * 128) + (uint32_t)((r ^ (2 * c)) << 4));
+        const uint4 vbb = lds128(vb + (uint32_t)((2 * c + 1) * 128) + (uint32_t)((r ^ (2 * c + 1)) << 4));
+        const uint4 vc = lds128(vb + (uint32_t)((2 * c + 8) * 128) + (uint32_t)((r ^ (2 * c)) << 4));
+        const uint4 vd = lds128(vb + (uint32_t)((2 * c + 9) * 128) + (uint32_t)((r ^ (2 * c + 1)) << 4));
+        const uint32_t A4[4] = {va.x, va.y, va.z, va.w}, B4[4] = {vbb.x, vbb.y, vbb.z, vbb.w};
+        const uint32_t C4[4] = {vc.x, vc.y, vc.z, vc.w}, D4[4] = {vd.x, vd.y, vd.z, vd.w};
+        uint32_t pab[16], pcd[16];  // (token pair) values at d = 16r + e
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t lo = __byte_perm(A4[w], B4[w], 0x5140), hi = __byte_perm(A4[w], B4[w], 0x7362);
+          pab[4 * w + 0] = e4m3x2_to_f16x2(lo);
+          pab[4 * w + 1] = e4m3x2_to_f16x2(lo >> 16);
+          pab[4 * w + 2] = e4m3x2_to_f16x2(hi);
+          pab[4 * w + 3] = e4m3x2_to_f16x2(hi >> 16);
+          const uint32_t lo2 = __byte_perm(C4[w], D4[w], 0x5140), hi2 = __byte_perm(C4[w], D4[w], 0x7362);
+          pcd[4 * w + 0] = e4m3x2_to_f16x2(lo2);
+          pcd[4 * w + 1] = e4m3x2_to_f16x2(lo2 >> 16);
+          pcd[4 * w + 2] = e4m3x2_to_f16x2(hi2);
+          pcd[4 * w + 3] = e4m3x2_to_f16x2(hi2 >> 16);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t a[4] = {pab[i], pab[8 + i], pcd[i], pcd[8 + i]};
+          mma_f16(o[i], a, pb0, pb1);
+        }
+      }
+      __syncwarp();
+      if (issued < n_units) {
+        issue(issued);
+        ++issued;
+      }
+    }
+
+    if (pc.flags & kPieceLastOfRun) {
+      // ---- finalise the run
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(kFull, l0, off);
+        l1 += __shfl_xor_sync(kFull, l1, off);
+      }
+      const int h0 = 2 * c, h1 = 2 * c + 1;
+      auto dpos = [&](int i, int half) { return KV == 1 ? 16 * i + 8 * half + r : 16 * r + 8 * half + i; };
+      if (pc.out_index < 0) {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+        const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+        const size_t row0 = ((size_t)pc.q_row * H + g * G + h0) * 128;
+        const size_t row1 = row0 + 128;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int d = dpos(i, half);
+            if (h0 < G) out[row0 + d] = __float2bfloat16(o[i][2 * half] * inv0);
+            if (h1 < G) out[row1 + d] = __float2bfloat16(o[i][2 * half + 1] * inv1);
+          }
+        if (r == 0 && p.lse != nullptr) {
+          const size_t li = (size_t)pc.q_row * H + g * G;
+          if (h0 < G) p.lse[li + h0] = l0 > 0.f ? (m0 + log2f(l0)) * kLn2 : -INFINITY;
+          if (h1 < G) p.lse[li + h1] = l1 > 0.f ? (m1 + log2f(l1)) * kLn2 : -INFINITY;
+        }
+      } else {
+        float* rec = p.partials + (size_t)pc.out_index * partial_floats(G, 128);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int d = dpos(i, half);
+            if (h0 < G) rec[h0 * 128 + d] = o[i][2 * half];
+            if (h1 < G) rec[h1 * 128 + d] = o[i][2 * half + 1];
+          }
+        if (r == 0) {
+          if (h0 < G) {
+            rec[G * 128 + h0] = m0;
+            rec[G * 128 + G + h0] = l0;
+          }
+          if (h1 < G) {
+            rec[G * 128 + h1] = m1;
+            rec[G * 128 + G + h1] = l1;
+          }
+        }
+      }
+      run_open = false;
+    }
+  }
+}
+
+template <int KV, int G>
+cudaError_t launch_t(const DecodeTCParams& p, int ctas, cudaStream_t st) {
+  decode_tc_kernel<KV, G><<<ctas, TC<KV>::kWarps * 32, smem_bytes<KV>(), st>>>(p);
+  return cudaGetLastError();
+}
+
+template <int KV>
+cudaError_t launch_kv(int G, const DecodeTCParams& p, int ctas, cudaStream_t st) {
+  switch (G) {
+    case 1: return launch_t<KV, 1>(p, ctas, st);
+    case 2: return launch_t<KV, 2>(p, ctas, st);
+    case 4: return launch_t<KV, 4>(p, ctas, st);
+    case 8: return launch_t<KV, 8>(p, ctas, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <int KV, int G>
+cudaError_t prepare_t() {
+  return cudaFuncSetAttribute(decode_tc_kernel<KV, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem_bytes<KV>());
+}
+
+template <int KV, int G>
+cudaError_t occupancy_t(int* n) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_tc_kernel<KV, G>, TC<KV>::kWarps * 32,
+                                                       smem_bytes<KV>());
+}
+
+template <int KV>
+cudaError_t dispatch_prepare(int G) {
+  switch (G) {
+    case 1: return prepare_t<KV, 1>();
+    case 2: return prepare_t<KV, 2>();
+    case 4: return prepare_t<KV, 4>();
+    case 8: return prepare_t<KV, 8>();
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <int KV>
+cudaError_t dispatch_occupancy(int G, int* n) {
+  switch (G) {
+    case 1: return occupancy_t<KV, 1>(n);
+    case 2: return occupancy_t<KV, 2>(n);
+    case 4: return occupancy_t<KV, 4>(n);
+    case 8: return occupancy_t<KV, 8>(n);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_decode_tc(int kv_dtype, int G, const DecodeTCParams& p, int ctas, cudaStream_t st) {
+  if (ctas <= 0) return cudaSuccess;
+  return kv_dtype == 2 ? launch_kv<2>(G, p, ctas, st) : launch_kv<1>(G, p, ctas, st);
+}
+
+int decode_tc_warps_per_cta(int kv_dtype) { return kv_dtype == 2 ? TC<2>::kWarps : TC<1>::kWarps; }
+
+size_t decode_tc_smem_bytes(int kv_dtype) { return kv_dtype == 2 ? smem_bytes<2>() : smem_bytes<1>(); }
+
+cudaError_t decode_tc_prepare(int kv_dtype, int G) {
+  return kv_dtype == 2 ? dispatch_prepare<2>(G) : dispatch_prepare<1>(G);
+}
+
+cudaError_t decode_tc_occupancy(int kv_dtype, int G, int* n) {
+  return kv_dtype == 2 ? dispatch_occupancy<2>(G, n) : dispatch_occupancy<1>(G, n);
+}
+
+}  // namespace pkv

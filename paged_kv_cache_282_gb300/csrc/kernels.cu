@@ -1,0 +1,431 @@
+// kernels.cu -- the HBM-bound helper kernels of libpkv (sm_103a):
+//   append / reshape_and_cache (+ FP8 E4M3 per-token quantisation),
+//   copy-on-write block copy, block-table patch, split-KV log-sum-exp combine,
+//   H2O score accumulation, H2O top-k keep-set selection, and the fp32
+//   CUDA-core decode used for fp32 pools.
+//
+// Pages (title, section): "KV Cache 与 PagedAttention：显存复用与长上下文推理"
+// (三大运行时组件, copy_on_write sketch, 量化原理); "长上下文优化：注意力稀疏化与
+// KV Cache 管理" (H2OEviction, StreamingKVCache, sliding-window mask);
+// "系统优化" (Flash Attention's online softmax; KV Cache 淘汰).
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <float.h>
+
+#include <algorithm>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// number of kept keys and the k-th kept position, in ascending order
+__device__ __forceinline__ int keep_count_of(int L, int mode, int S, int W) {
+  if (L <= 0) return 0;
+  if (mode == 0) return L;
+  if (mode == 1) return min(L, W + 1);
+  if ((long long)L <= (long long)S + W) return L;
+  return S + W;
+}
+__device__ __forceinline__ int keep_pos(int k, int L, int mode, int S, int W) {
+  if (mode == 0) return k;
+  if (mode == 1) return max(0, L - 1 - W) + k;
+  if ((long long)L <= (long long)S + W) return k;
+  return k < S ? k : L - W + (k - S);
+}
+
+// ---------------------------------------------------------------------------
+// append: scatter new rows into their slots (bf16 / fp32 copy)
+// ---------------------------------------------------------------------------
+
+__global__ void append_copy_kernel(const int64_t* __restrict__ slots, int n_tokens, int Hk, int row_chunks,
+                                   const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                                   uint4* __restrict__ k_pool, uint4* __restrict__ v_pool) {
+  const int64_t per_tok = (int64_t)Hk * row_chunks;
+  const int64_t total = (int64_t)n_tokens * per_tok;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < 2 * total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const bool is_v = i >= total;
+    const int64_t e = is_v ? i - total : i;
+    const int64_t t = e / per_tok;
+    const int64_t rem = e - t * per_tok;  // = g * row_chunks + chunk
+    const int64_t slot = slots[t];
+    const int64_t blk = slot >> 4, off = slot & 15;
+    const int64_t g = rem / row_chunks, ch = rem - g * row_chunks;
+    const int64_t dst = ((blk * Hk + g) * kBlock + off) * row_chunks + ch;
+    if (is_v)
+      v_pool[dst] = v_new[e];
+    else
+      k_pool[dst] = k_new[e];
+  }
+}
+
+// FP8: one warp per (token, kv head, K|V) row of 128 values.
+//   s = absmax / 448 (fp32, IEEE division; 1 when absmax is 0)
+//   code = E4M3(x / s), round to nearest even, saturate to +-448
+__global__ void append_fp8_kernel(const int64_t* __restrict__ slots, int n_tokens, int Hk,
+                                  const __nv_bfloat16* __restrict__ k_new, const __nv_bfloat16* __restrict__ v_new,
+                                  uint8_t* __restrict__ k_pool, uint8_t* __restrict__ v_pool,
+                                  float* __restrict__ k_scale, float* __restrict__ v_scale) {
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = (int64_t)n_tokens * Hk;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t w = blockIdx.x * (int64_t)(blockDim.x / 32) + (threadIdx.x >> 5); w < 2 * rows; w += warps) {
+    const bool is_v = w >= rows;
+    const int64_t row = is_v ? w - rows : w;  // = t * Hk + g
+    const int64_t t = row / Hk, g = row - t * Hk;
+    const __nv_bfloat16* src = (is_v ? v_new : k_new) + row * 128 + lane * 4;
+    const uint2 raw = *reinterpret_cast<const uint2*>(src);
+    const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+    const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+    float x[4] = {__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi)};
+    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+    const float s = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
+    uint32_t packed = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __nv_fp8_storage_t code = __nv_cvt_float_to_fp8(__fdiv_rn(x[k], s), __NV_SATFINITE, __NV_E4M3);
+      packed |= (uint32_t)code << (8 * k);
+    }
+    const int64_t slot = slots[t];
+    const int64_t blk = slot >> 4, off = slot & 15;
+    const int64_t srow = (blk * Hk + g) * kBlock + off;
+    uint8_t* dst = (is_v ? v_pool : k_pool) + srow * 128 + lane * 4;
+    *reinterpret_cast<uint32_t*>(dst) = packed;
+    if (lane == 0) (is_v ? v_scale : k_scale)[srow] = s;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// copy-on-write: copy whole physical blocks (K, V, and FP8 scales)
+// ---------------------------------------------------------------------------
+
+__global__ void cow_copy_kernel(const int32_t* __restrict__ pairs, uint4* __restrict__ k, uint4* __restrict__ v,
+                                int64_t chunks, float* __restrict__ ks, float* __restrict__ vs, int64_t sfloats) {
+  const int64_t src = pairs[2 * blockIdx.y], dst = pairs[2 * blockIdx.y + 1];
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < chunks; i += (int64_t)gridDim.x * blockDim.x) {
+    k[dst * chunks + i] = k[src * chunks + i];
+    v[dst * chunks + i] = v[src * chunks + i];
+  }
+  if (ks && blockIdx.x == 0)
+    for (int64_t i = threadIdx.x; i < sfloats; i += blockDim.x) {
+      ks[dst * sfloats + i] = ks[src * sfloats + i];
+      vs[dst * sfloats + i] = vs[src * sfloats + i];
+    }
+}
+
+__global__ void table_patch_kernel(const int32_t* __restrict__ patches, int n, int32_t* __restrict__ tables) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    tables[patches[2 * i]] = patches[2 * i + 1];
+}
+
+// ---------------------------------------------------------------------------
+// split-KV combine: merge partial (O, M, l) records by log-sum-exp.
+// M is in log2 units; O and l are relative to 2^M.
+// ---------------------------------------------------------------------------
+
+__global__ void combine_kernel(const CombineItem* __restrict__ items, const float* __restrict__ partials, int G,
+                               int D, int n_heads, int n_kv_heads, __nv_bfloat16* __restrict__ out,
+                               float* __restrict__ lse) {
+  const CombineItem it = items[blockIdx.x];
+  const int pf = G * D + 2 * G;
+  for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
+    const int h = e / D, d = e - h * D;
+    const size_t orow = ((size_t)it.q_row * n_heads + it.kv_head * G + h);
+    if (it.n_partials == 0) {
+      out[orow * D + d] = __float2bfloat16(0.0f);
+      if (d == 0 && lse) lse[orow] = -INFINITY;
+      continue;
+    }
+    float M = -INFINITY;
+    for (int k = 0; k < it.n_partials; ++k)
+      M = fmaxf(M, partials[(size_t)(it.first_partial + k) * pf + G * D + h]);
+    float acc = 0.0f, l = 0.0f;
+    for (int k = 0; k < it.n_partials; ++k) {
+      const float* rec = partials + (size_t)(it.first_partial + k) * pf;
+      const float Mk = rec[G * D + h];
+      const float w = Mk == -INFINITY ? 0.0f : exp2f(Mk - M);
+      acc += w * rec[h * D + d];
+      l += w * rec[G * D + G + h];
+    }
+    out[orow * D + d] = __float2bfloat16(l > 0.0f ? acc / l : 0.0f);
+    if (d == 0 && lse) lse[orow] = l > 0.0f ? (M + log2f(l)) * 0.6931471805599453f : -INFINITY;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// H2O score: acc[b][j] += mean over query heads of exp(s_hj - lse_h)
+// ---------------------------------------------------------------------------
+
+__global__ void h2o_score_kernel(const SeqRow* __restrict__ rows, int n_heads, int n_kv_heads,
+                                 const float* __restrict__ logits, int64_t stride, const float* __restrict__ lse,
+                                 int mode, int S, int W, float* __restrict__ acc, int64_t acc_stride) {
+  extern __shared__ float s_lse[];
+  const SeqRow row = rows[blockIdx.y];
+  const int b = row.q_row, L = row.ctx_len;
+  for (int h = threadIdx.x; h < n_heads; h += blockDim.x) s_lse[h] = lse[(size_t)b * n_heads + h];
+  __syncthreads();
+  const int nk = keep_count_of(L, mode, S, W);
+  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= nk) return;
+  const int j = keep_pos(k, L, mode, S, W);
+  const int G = n_heads / n_kv_heads;
+  float sum = 0.0f;
+  for (int g = 0; g < n_kv_heads; ++g) {
+    const float* lg = logits + (((size_t)b * n_kv_heads + g) * stride + j) * G;
+    for (int i = 0; i < G; ++i) sum += expf(lg[i] - s_lse[g * G + i]);
+  }
+  acc[(size_t)b * acc_stride + j] += sum / (float)n_heads;
+}
+
+// ---------------------------------------------------------------------------
+// H2O select: exact top-k by radix select on order-preserving keys, ties to
+// the lower position, output in ascending position order.
+// ---------------------------------------------------------------------------
+
+constexpr int kSelThreads = 1024;
+
+__device__ __forceinline__ uint32_t order_key(float x) {
+  uint32_t u = __float_as_uint(x);
+  if (u == 0x80000000u) u = 0;  // -0 ranks as +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// exclusive block scan of v (blockDim.x == kSelThreads); returns the total
+__device__ int block_excl_scan(int v, int* excl, int* s_warp) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int t = s_warp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, t, o);
+      if (lane >= o) t += y;
+    }
+    s_warp[lane] = t;  // inclusive prefix of warp totals
+  }
+  __syncthreads();
+  const int before = w ? s_warp[w - 1] : 0;
+  const int total = s_warp[31];
+  *excl = before + x - v;
+  __syncthreads();
+  return total;
+}
+
+__global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* __restrict__ rows,
+                                                                 const float* __restrict__ acc, int64_t acc_stride,
+                                                                 int budget, int recent, int32_t* __restrict__ keep_idx,
+                                                                 int64_t keep_stride, int32_t* __restrict__ keep_count) {
+  __shared__ uint32_t hist[256];
+  __shared__ int s_warp[32];
+  __shared__ uint32_t s_prefix, s_mask;
+  __shared__ int s_k;
+  const SeqRow row = rows[blockIdx.x];
+  const int b = row.q_row, L = row.ctx_len;
+  const float* a = acc + (size_t)b * acc_stride;
+  int32_t* out = keep_idx + (size_t)b * keep_stride;
+  if (L <= budget) {
+    for (int j = threadIdx.x; j < L; j += blockDim.x) out[j] = j;
+    if (threadIdx.x == 0) keep_count[b] = L;
+    return;
+  }
+  const int n = L - recent, keep = budget - recent;  // n > keep here
+  if (threadIdx.x == 0) {
+    s_prefix = 0;
+    s_mask = 0;
+    s_k = keep;
+  }
+  __syncthreads();
+  if (keep > 0) {
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+      __syncthreads();
+      const uint32_t prefix = s_prefix, mask = s_mask;
+      for (int j = threadIdx.x; j < n; j += blockDim.x) {
+        const uint32_t key = order_key(a[j]);
+        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        int k = s_k;
+        for (int dgt = 255; dgt >= 0; --dgt) {
+          const int c = (int)hist[dgt];
+          if (c >= k) {
+            s_prefix = prefix | ((uint32_t)dgt << shift);
+            s_mask = mask | (255u << shift);
+            break;
+          }
+          k -= c;
+        }
+        s_k = k;  // rank still needed among keys sharing the new prefix
+      }
+      __syncthreads();
+    }
+  }
+  const uint32_t T = s_prefix;
+  const int need_eq = s_k;  // equal-to-T keys to take, lowest positions first
+  int taken = 0, eq_seen = 0;
+  if (keep > 0) {
+    for (int base = 0; base < n; base += blockDim.x) {
+      const int j = base + threadIdx.x;
+      uint32_t key = 0;
+      if (j < n) key = order_key(a[j]);
+      const int gt = (j < n && key > T) ? 1 : 0;
+      const int eq = (j < n && key == T) ? 1 : 0;
+      int eq_excl;
+      const int eq_tot = block_excl_scan(eq, &eq_excl, s_warp);
+      const int sel = gt || (eq && eq_seen + eq_excl < need_eq);
+      int sel_excl;
+      const int sel_tot = block_excl_scan(sel, &sel_excl, s_warp);
+      if (sel) out[taken + sel_excl] = j;
+      taken += sel_tot;
+      eq_seen += eq_tot;
+    }
+  }
+  for (int i = threadIdx.x; i < recent; i += blockDim.x) out[keep + i] = n + i;
+  if (threadIdx.x == 0) keep_count[b] = budget;
+}
+
+// ---------------------------------------------------------------------------
+// fp32 decode on CUDA cores: one warp per query head, one CTA per
+// (sequence, kv head); online softmax over the kept keys in order.
+// ---------------------------------------------------------------------------
+
+template <int D>
+__global__ void decode_f32_kernel(const DecodeF32Params p) {
+  constexpr int E = D / 32;
+  const int lane = threadIdx.x & 31, i = threadIdx.x >> 5;
+  const SeqRow row = p.rows[blockIdx.x];
+  const int g = blockIdx.y, Hk = p.n_kv_heads, G = p.n_heads / Hk, h = g * G + i;
+  const int b = row.q_row, L = row.ctx_len;
+  float q[E], o[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    q[e] = p.q[((size_t)b * p.n_heads + h) * D + lane + 32 * e];
+    o[e] = 0.0f;
+  }
+  float m = -INFINITY, l = 0.0f;
+  const int nk = keep_count_of(L, p.mask_mode, p.num_sinks, p.window);
+  for (int k = 0; k < nk; ++k) {
+    const int j = keep_pos(k, L, p.mask_mode, p.num_sinks, p.window);
+    const int blk = p.tables[(size_t)row.seq_slot * p.max_blocks + j / kBlock];
+    if (blk < 0 || blk >= p.num_blocks) {
+      if (lane == 0) atomicOr(p.status, kStatusBadBlock);
+      continue;
+    }
+    const size_t r = ((size_t)blk * Hk + g) * kBlock + (j & 15);
+    const float* kr = p.k_pool + r * D;
+    const float* vr = p.v_pool + r * D;
+    float dot = 0.0f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) dot += q[e] * kr[lane + 32 * e];
+#pragma unroll
+    for (int off = 16; off; off >>= 1) dot += __shfl_xor_sync(kFull, dot, off);
+    const float s = dot * p.scale;
+    if (p.logits && lane == 0) p.logits[(((size_t)b * Hk + g) * p.logits_stride + j) * G + i] = s;
+    const float mn = fmaxf(m, s);
+    const float alpha = expf(m - mn);
+    const float pj = expf(s - mn);
+    l = l * alpha + pj;
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[e] = o[e] * alpha + pj * vr[lane + 32 * e];
+    m = mn;
+  }
+  const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) p.out[((size_t)b * p.n_heads + h) * D + lane + 32 * e] = o[e] * inv;
+  if (p.lse && lane == 0) p.lse[(size_t)b * p.n_heads + h] = l > 0.0f ? m + logf(l) : -INFINITY;
+}
+
+int grid_for(int64_t work, int threads) {
+  int64_t g = (work + threads - 1) / threads;
+  if (g > 65535LL * 32) g = 65535LL * 32;
+  return (int)(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+cudaError_t launch_append(int kv_dtype, const int64_t* slots, int n_tokens, int Hk, int D, const void* k_new,
+                          const void* v_new, void* k_pool, void* v_pool, float* k_scale, float* v_scale,
+                          cudaStream_t st) {
+  if (n_tokens <= 0) return cudaSuccess;
+  if (kv_dtype == 2) {
+    const int64_t warps = 2LL * n_tokens * Hk;
+    append_fp8_kernel<<<grid_for(warps * 32, 256), 256, 0, st>>>(
+        slots, n_tokens, Hk, (const __nv_bfloat16*)k_new, (const __nv_bfloat16*)v_new, (uint8_t*)k_pool,
+        (uint8_t*)v_pool, k_scale, v_scale);
+  } else {
+    const int row_chunks = D * (kv_dtype == 0 ? 4 : 2) / 16;
+    const int64_t work = 2LL * n_tokens * Hk * row_chunks;
+    append_copy_kernel<<<grid_for(work, 256), 256, 0, st>>>(slots, n_tokens, Hk, row_chunks, (const uint4*)k_new,
+                                                            (const uint4*)v_new, (uint4*)k_pool, (uint4*)v_pool);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cow_copy(const int32_t* pairs, int n_pairs, void* k_pool, void* v_pool, float* k_scale,
+                            float* v_scale, size_t block_bytes, size_t scale_floats, cudaStream_t st) {
+  if (n_pairs <= 0) return cudaSuccess;
+  const int64_t chunks = (int64_t)(block_bytes / 16);
+  dim3 grid((unsigned)std::min<int64_t>((chunks + 255) / 256, 64), (unsigned)n_pairs);
+  cow_copy_kernel<<<grid, 256, 0, st>>>(pairs, (uint4*)k_pool, (uint4*)v_pool, chunks, scale_floats ? k_scale : nullptr,
+                                        scale_floats ? v_scale : nullptr, (int64_t)scale_floats);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_table_patch(const int32_t* patches, int n, int32_t* tables, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  table_patch_kernel<<<std::min((n + 255) / 256, 1024), 256, 0, st>>>(patches, n, tables);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const CombineItem* items, int n_items, const float* partials, int G, int D, int n_heads,
+                           int /*out_bf16*/, void* out, float* lse, cudaStream_t st) {
+  if (n_items <= 0) return cudaSuccess;
+  combine_kernel<<<n_items, 256, 0, st>>>(items, partials, G, D, n_heads, n_heads / G, (__nv_bfloat16*)out, lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_h2o_score(const SeqRow* rows, int n_seqs, int n_heads, int n_kv_heads, const float* logits,
+                             int64_t stride, const float* lse, int mode, int S, int W, float* acc, int64_t acc_stride,
+                             int max_keep, cudaStream_t st) {
+  if (n_seqs <= 0 || max_keep <= 0) return cudaSuccess;
+  dim3 grid((unsigned)((max_keep + 255) / 256), (unsigned)n_seqs);
+  h2o_score_kernel<<<grid, 256, n_heads * sizeof(float), st>>>(rows, n_heads, n_kv_heads, logits, stride, lse, mode,
+                                                                S, W, acc, acc_stride);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_h2o_select(const SeqRow* rows, int n_seqs, const float* acc, int64_t acc_stride, int budget,
+                              int recent, int32_t* keep_idx, int64_t keep_stride, int32_t* keep_count,
+                              cudaStream_t st) {
+  if (n_seqs <= 0) return cudaSuccess;
+  h2o_select_kernel<<<n_seqs, kSelThreads, 0, st>>>(rows, acc, acc_stride, budget, recent, keep_idx, keep_stride,
+                                                     keep_count);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_f32(const DecodeF32Params& p, cudaStream_t st) {
+  if (p.n_seqs <= 0) return cudaSuccess;
+  dim3 grid((unsigned)p.n_seqs, (unsigned)p.n_kv_heads);
+  const int threads = 32 * (p.n_heads / p.n_kv_heads);
+  if (p.head_dim == 64)
+    decode_f32_kernel<64><<<grid, threads, 0, st>>>(p);
+  else
+    decode_f32_kernel<128><<<grid, threads, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,126 @@
+// pkv_internal.h -- structures shared by the host planner and the kernels of
+// libpkv.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+constexpr int kBlock = 16;   // tokens per physical block
+constexpr int kHeadDimTC = 128;  // head_dim of the tensor-core decode path
+
+// Device status word bits (pool status buffer, element 0).
+enum : int32_t { kStatusTimeout = 1, kStatusBadBlock = 2 };
+
+// One contiguous range of logical blocks of one (sequence, kv head), handled
+// by one warp of the decode kernel.  Consecutive pieces of the same
+// (sequence, kv head) inside one warp form a "run"; the run is finalised
+// after the piece that carries kPieceLastOfRun.
+enum : int32_t { kPieceLastOfRun = 1 };
+struct Piece {
+  int32_t seq_slot;    // block-table row
+  int32_t q_row;       // batch index into q / out / lse / logits
+  int32_t kv_head;
+  int32_t lblk_begin;  // logical block range [begin, end)
+  int32_t lblk_end;
+  int32_t ctx_len;     // L: context length, current token included
+  int32_t out_index;   // >= 0: partial record index; -1: write the final output
+  int32_t flags;
+};
+static_assert(sizeof(Piece) == 32, "Piece layout");
+
+// A (sequence, kv head) whose partial records must be merged, or whose
+// keep-set is empty (n_partials == 0: zeros and -inf).
+struct CombineItem {
+  int32_t q_row, kv_head, first_partial, n_partials;
+};
+
+// Per-sequence row for kernels that walk one sequence at a time.
+struct SeqRow {
+  int32_t seq_slot, q_row, ctx_len, pad;
+};
+
+// Floats per partial record: O[G][D] (unnormalised), then M[G] (log2 units),
+// then l[G].
+inline __host__ __device__ int partial_floats(int G, int D) { return G * D + 2 * G; }
+
+struct DecodeTCParams {
+  CUtensorMap tmap_k;  // 2-D view [num_blocks * Hk * 16][D] of the K pool, 128B swizzle
+  CUtensorMap tmap_v;
+  const float* k_scale;  // FP8 only
+  const float* v_scale;
+  const int32_t* tables;
+  int32_t max_blocks, num_blocks;
+  int32_t n_heads, n_kv_heads;
+  const void* q;
+  void* out;
+  float* lse;
+  float* logits;
+  int64_t logits_stride;
+  const Piece* pieces;
+  const int32_t* warp_begin;  // [total_warps + 1]
+  int32_t total_warps;
+  float* partials;
+  float scale;       // natural-unit softmax scale
+  int32_t mask_mode, num_sinks, window;
+  int32_t* status;
+};
+
+struct DecodeF32Params {
+  const float* k_pool;
+  const float* v_pool;
+  const int32_t* tables;
+  int32_t max_blocks, num_blocks;
+  int32_t n_heads, n_kv_heads, head_dim;
+  const SeqRow* rows;
+  int32_t n_seqs;
+  const float* q;
+  float* out;
+  float* lse;
+  float* logits;
+  int64_t logits_stride;
+  float scale;
+  int32_t mask_mode, num_sinks, window;
+  int32_t* status;
+};
+
+// ---- kernel launchers (defined in the .cu files) -------------------------
+
+// Tensor-core decode: kv_dtype 1 = bf16, 2 = FP8.  Returns the launch error.
+cudaError_t launch_decode_tc(int kv_dtype, int G, const DecodeTCParams& p, int grid_ctas,
+                             cudaStream_t stream);
+// Decode kernel geometry: warps per CTA and dynamic shared memory bytes.
+int decode_tc_warps_per_cta(int kv_dtype);
+size_t decode_tc_smem_bytes(int kv_dtype);
+cudaError_t decode_tc_prepare(int kv_dtype, int G);  // sets the smem attribute
+cudaError_t decode_tc_occupancy(int kv_dtype, int G, int* ctas_per_sm);
+
+cudaError_t launch_decode_f32(const DecodeF32Params& p, cudaStream_t stream);
+
+cudaError_t launch_combine(const CombineItem* items, int n_items, const float* partials, int G,
+                           int D, int n_heads, int kv_dtype_out_bf16, void* out, float* lse,
+                           cudaStream_t stream);
+
+cudaError_t launch_cow_copy(const int32_t* pairs, int n_pairs, void* k_pool, void* v_pool,
+                            float* k_scale, float* v_scale, size_t block_bytes,
+                            size_t scale_floats_per_block, cudaStream_t stream);
+
+cudaError_t launch_table_patch(const int32_t* patches, int n_patches, int32_t* tables,
+                               cudaStream_t stream);
+
+cudaError_t launch_append(int kv_dtype, const int64_t* slots, int n_tokens, int Hk, int D,
+                          const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                          float* k_scale, float* v_scale, cudaStream_t stream);
+
+cudaError_t launch_h2o_score(const SeqRow* rows, int n_seqs, int n_heads, int n_kv_heads,
+                             const float* logits, int64_t logits_stride, const float* lse,
+                             int mask_mode, int num_sinks, int window, float* acc,
+                             int64_t acc_stride, int max_keep, cudaStream_t stream);
+
+cudaError_t launch_h2o_select(const SeqRow* rows, int n_seqs, const float* acc, int64_t acc_stride,
+                              int budget, int recent, int32_t* keep_idx, int64_t keep_stride,
+                              int32_t* keep_count, cudaStream_t stream);
+
+}  // namespace pkv

@@ -1,0 +1,1139 @@
+// pool.cpp -- host side of libpkv: block allocator, decode planner, staging,
+// timing and every entry point of the C ABI declared in include/pkv.h.
+//
+// The allocator follows the runtime components of the PagedAttention page
+// ("KV Cache 与 PagedAttention：显存复用与长上下文推理", sections PagedAttention
+// 的设计, 三大运行时组件 and the copy_on_write sketch): a global free pool of
+// 16-token blocks, one block table per sequence, reference counts and a copy
+// on the first write to a shared block.  Its determinism rules (initial
+// order, front-of-pool reuse, smallest free sequence id, order of frees) are
+// fixed here so that tests can replay them exactly.
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <numeric>
+#include <set>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/pkv.h"
+#include "pkv_internal.h"
+
+using namespace pkv;
+
+// ---------------------------------------------------------------------------
+// errors
+// ---------------------------------------------------------------------------
+
+static thread_local std::string g_last_error;
+
+static pkv_status fail(pkv_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+#define PKV_CUDA(call)                                                                  \
+  do {                                                                                  \
+    cudaError_t e_ = (call);                                                            \
+    if (e_ != cudaSuccess)                                                              \
+      return fail(PKV_ERR_CUDA, "%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), \
+                  __FILE__, __LINE__);                                                  \
+  } while (0)
+
+// ---------------------------------------------------------------------------
+// keep-set geometry (which logical blocks a decode must read)
+// ---------------------------------------------------------------------------
+
+struct BlockRange {
+  int32_t lo, hi;  // logical blocks [lo, hi)
+};
+
+static int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+// Logical block ranges that intersect the keep-set of a decode query at
+// position L - 1 (mask semantics in include/pkv.h).
+static int keep_ranges(int L, int mode, int S, int W, BlockRange out[2]) {
+  if (L <= 0) return 0;
+  const int nblk = ceil_div(L, kBlock);
+  if (mode == PKV_MASK_FULL) {
+    out[0] = {0, nblk};
+    return 1;
+  }
+  if (mode == PKV_MASK_SLIDING) {
+    int lo_tok = std::max(0, L - 1 - W);
+    out[0] = {lo_tok / kBlock, nblk};
+    return 1;
+  }
+  // sink + window
+  if ((int64_t)L <= (int64_t)S + W) {
+    out[0] = {0, nblk};
+    return 1;
+  }
+  const int sink_hi = ceil_div(S, kBlock);  // blocks holding the sinks
+  const int win_lo = (L - W) / kBlock;      // first block holding the window
+  if (S > 0 && W > 0 && sink_hi >= win_lo) {
+    out[0] = {0, nblk};
+    return 1;
+  }
+  int n = 0;
+  if (S > 0) out[n++] = {0, sink_hi};
+  if (W > 0) out[n++] = {win_lo, nblk};
+  return n;
+}
+
+// ---------------------------------------------------------------------------
+// host block allocator
+// ---------------------------------------------------------------------------
+
+static uint64_t mix64(uint64_t& s) {  // splitmix64 (Steele, Lea & Flood 2014)
+  s += 0x9E3779B97F4A7C15ULL;
+  uint64_t z = s;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+  return z ^ (z >> 31);
+}
+
+struct TablePatch {
+  int32_t index, value;  // flat index into the device block table
+};
+
+struct HostAllocator {
+  int32_t NB = 0, max_seqs = 0, max_blocks = 0;
+  std::vector<int32_t> refcount;
+  std::vector<int32_t> free_blocks;  // back() is the front of the free pool
+  std::vector<std::vector<int32_t>> table;
+  std::vector<int32_t> len;
+  std::vector<uint8_t> live, holes;
+  std::set<int32_t> free_ids;
+  int64_t cow_count = 0, n_alloc = 0, n_freed = 0;
+  // queued device-side effects
+  std::vector<int32_t> pending_cow;  // (src, dst) pairs
+  std::vector<TablePatch> pending_patch;
+
+  void init(int32_t nb, int32_t ms, int32_t mb, uint64_t seed, const int32_t* order) {
+    NB = nb;
+    max_seqs = ms;
+    max_blocks = mb;
+    refcount.assign(nb, 0);
+    std::vector<int32_t> front_first(nb);
+    if (order) {
+      std::copy(order, order + nb, front_first.begin());
+    } else {
+      std::iota(front_first.begin(), front_first.end(), 0);
+      if (seed != 0) {
+        uint64_t st = seed;
+        for (int32_t i = nb - 1; i >= 1; --i) {
+          int32_t j = (int32_t)(mix64(st) % (uint64_t)(i + 1));
+          std::swap(front_first[i], front_first[j]);
+        }
+      }
+    }
+    free_blocks.assign(front_first.rbegin(), front_first.rend());
+    table.assign(ms, {});
+    len.assign(ms, 0);
+    live.assign(ms, 0);
+    holes.assign(ms, 0);
+    free_ids.clear();
+    for (int32_t s = 0; s < ms; ++s) free_ids.insert(s);
+  }
+
+  bool valid_seq(int32_t s) const { return s >= 0 && s < max_seqs && live[s]; }
+
+  int32_t take() {
+    int32_t b = free_blocks.back();
+    free_blocks.pop_back();
+    refcount[b] = 1;
+    ++n_alloc;
+    return b;
+  }
+  void release(int32_t b) {
+    if (--refcount[b] == 0) {
+      free_blocks.push_back(b);
+      ++n_freed;
+    }
+  }
+  void set_entry(int32_t s, int32_t lb, int32_t v) {
+    if ((int32_t)table[s].size() <= lb) table[s].resize(lb + 1, -1);
+    table[s][lb] = v;
+    pending_patch.push_back({s * max_blocks + lb, v});
+  }
+  void drop_from(int32_t s, int32_t first_lb) {
+    auto& t = table[s];
+    for (int32_t lb = first_lb; lb < (int32_t)t.size(); ++lb) {
+      if (t[lb] >= 0) release(t[lb]);
+      if (t[lb] != -1) pending_patch.push_back({s * max_blocks + lb, -1});
+    }
+    if ((int32_t)t.size() > first_lb) t.resize(first_lb);
+  }
+};
+
+// ---------------------------------------------------------------------------
+// staging: pinned host slots mirrored by device slots, reused round-robin
+// ---------------------------------------------------------------------------
+
+struct StagingSlot {
+  char* host = nullptr;
+  char* dev = nullptr;
+  size_t cap = 0;
+  cudaEvent_t done = nullptr;  // recorded after the last kernel reading `dev`
+  bool pending = false;
+};
+
+struct Staging {
+  static constexpr int kSlots = 4;
+  StagingSlot slot[kSlots];
+  int next = 0;
+
+  pkv_status acquire(size_t bytes, StagingSlot** out) {
+    StagingSlot& s = slot[next];
+    next = (next + 1) % kSlots;
+    if (s.pending) {
+      PKV_CUDA(cudaEventSynchronize(s.done));
+      s.pending = false;
+    }
+    if (s.cap < bytes) {
+      size_t cap = std::max<size_t>(bytes, size_t(1) << 20);
+      cap = (cap + 4095) & ~size_t(4095);
+      if (s.host) PKV_CUDA(cudaFreeHost(s.host));
+      if (s.dev) PKV_CUDA(cudaFree(s.dev));
+      s.host = nullptr;
+      s.dev = nullptr;
+      s.cap = 0;
+      PKV_CUDA(cudaHostAlloc((void**)&s.host, cap, cudaHostAllocDefault));
+      PKV_CUDA(cudaMalloc((void**)&s.dev, cap));
+      s.cap = cap;
+    }
+    if (!s.done) PKV_CUDA(cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming));
+    *out = &s;
+    return PKV_OK;
+  }
+  static pkv_status upload(StagingSlot* s, size_t bytes, cudaStream_t st) {
+    if (bytes) PKV_CUDA(cudaMemcpyAsync(s->dev, s->host, bytes, cudaMemcpyHostToDevice, st));
+    return PKV_OK;
+  }
+  static pkv_status release(StagingSlot* s, cudaStream_t st) {
+    PKV_CUDA(cudaEventRecord(s->done, st));
+    s->pending = true;
+    return PKV_OK;
+  }
+  void destroy() {
+    for (auto& s : slot) {
+      if (s.pending) cudaEventSynchronize(s.done);
+      if (s.host) cudaFreeHost(s.host);
+      if (s.dev) cudaFree(s.dev);
+      if (s.done) cudaEventDestroy(s.done);
+      s = StagingSlot{};
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// per-kernel event timing
+// ---------------------------------------------------------------------------
+
+struct Timing {
+  bool enabled = false;
+  std::vector<cudaEvent_t> spare;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> marks[PKV_KERNEL_COUNT];
+
+  cudaEvent_t get() {
+    if (!spare.empty()) {
+      cudaEvent_t e = spare.back();
+      spare.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+  void destroy() {
+    for (auto& v : marks)
+      for (auto& pr : v) {
+        cudaEventDestroy(pr.first);
+        cudaEventDestroy(pr.second);
+      }
+    for (auto e : spare) cudaEventDestroy(e);
+    spare.clear();
+    for (auto& v : marks) v.clear();
+  }
+};
+
+// ---------------------------------------------------------------------------
+// the pool
+// ---------------------------------------------------------------------------
+
+struct pkv_pool {
+  pkv_pool_config cfg{};
+  bool device = false;
+  pkv_pool_buffers buf{};
+  HostAllocator alloc;
+  Staging staging;
+  Timing timing;
+  int64_t launches = 0;
+  int device_id = 0, num_sms = 0;
+  int tc_warps_per_cta = 0, tc_ctas_per_sm = 0;
+  size_t tc_smem = 0;
+  CUtensorMap tmap_k{}, tmap_v{};
+  bool tc_path = false;
+  int G = 1;
+};
+
+namespace {
+
+template <class F>
+pkv_status launch(pkv_pool* p, int kernel, cudaStream_t st, F&& fn) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (p->timing.enabled) {
+    a = p->timing.get();
+    b = p->timing.get();
+    PKV_CUDA(cudaEventRecord(a, st));
+  }
+  cudaError_t e = fn();
+  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "kernel %d launch failed: %s", kernel, cudaGetErrorString(e));
+  ++p->launches;
+  if (p->timing.enabled) {
+    PKV_CUDA(cudaEventRecord(b, st));
+    p->timing.marks[kernel].push_back({a, b});
+  }
+  return PKV_OK;
+}
+
+int elem_bytes(int kv_dtype) { return kv_dtype == PKV_KV_FP32 ? 4 : kv_dtype == PKV_KV_BF16 ? 2 : 1; }
+
+pkv_status check_config(const pkv_pool_config* c) {
+  if (!c) return fail(PKV_ERR_INVALID_ARG, "config is NULL");
+  if (c->block_size != kBlock) return fail(PKV_ERR_UNSUPPORTED, "block_size must be 16");
+  if (c->num_blocks < 0 || c->max_seqs <= 0 || c->max_blocks_per_seq <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_blocks, max_seqs and max_blocks_per_seq must be positive");
+  if ((int64_t)c->max_seqs * c->max_blocks_per_seq >= (int64_t(1) << 31))
+    return fail(PKV_ERR_UNSUPPORTED, "block table larger than 2^31 entries");
+  if ((int64_t)c->max_blocks_per_seq * kBlock >= (int64_t(1) << 31))
+    return fail(PKV_ERR_UNSUPPORTED, "max_blocks_per_seq too large");
+  if (c->n_heads <= 0 || c->n_kv_heads <= 0 || c->n_heads % c->n_kv_heads)
+    return fail(PKV_ERR_INVALID_ARG, "n_heads must be a positive multiple of n_kv_heads");
+  int G = c->n_heads / c->n_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return fail(PKV_ERR_UNSUPPORTED, "group size %d not in {1,2,4,8}", G);
+  if (c->kv_dtype != PKV_KV_FP32 && c->kv_dtype != PKV_KV_BF16 && c->kv_dtype != PKV_KV_FP8_E4M3)
+    return fail(PKV_ERR_INVALID_ARG, "unknown kv_dtype %d", c->kv_dtype);
+  if (c->kv_dtype == PKV_KV_FP32 && c->head_dim != 64 && c->head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "fp32 pools support head_dim 64 or 128");
+  if (c->kv_dtype != PKV_KV_FP32 && c->head_dim != kHeadDimTC)
+    return fail(PKV_ERR_UNSUPPORTED, "bf16 / fp8 pools support head_dim 128");
+  if ((int64_t)c->num_blocks * c->n_kv_heads * kBlock >= (int64_t(1) << 31))
+    return fail(PKV_ERR_UNSUPPORTED, "pool too large for 32-bit row coordinates");
+  if (c->free_order) {
+    std::vector<uint8_t> seen(c->num_blocks, 0);
+    for (int32_t i = 0; i < c->num_blocks; ++i) {
+      int32_t b = c->free_order[i];
+      if (b < 0 || b >= c->num_blocks || seen[b]) return fail(PKV_ERR_INVALID_ARG, "free_order is not a permutation");
+      seen[b] = 1;
+    }
+  }
+  return PKV_OK;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+pkv_status make_tensor_map(CUtensorMap* m, void* base, const pkv_pool_config& c) {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    PKV_CUDA(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q));
+    if (q != cudaDriverEntryPointSuccess || !ptr) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    fn = (EncodeTiledFn)ptr;
+  }
+  const bool fp8 = c.kv_dtype == PKV_KV_FP8_E4M3;
+  const int es = fp8 ? 1 : 2;
+  // 2-D view: rows = (block, kv head, slot), columns = head_dim elements.
+  cuuint64_t dims[2] = {(cuuint64_t)c.head_dim, (cuuint64_t)c.num_blocks * c.n_kv_heads * kBlock};
+  cuuint64_t strides[1] = {(cuuint64_t)c.head_dim * es};
+  // one box = 16 rows x 128 bytes (64 bf16 or 128 FP8 values), 128-byte swizzle
+  cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)kBlock};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return PKV_OK;
+}
+
+pkv_status flush_pending(pkv_pool* p, cudaStream_t st) {
+  HostAllocator& A = p->alloc;
+  if (A.pending_cow.empty() && A.pending_patch.empty()) return PKV_OK;
+  const size_t ncow = A.pending_cow.size() / 2, npatch = A.pending_patch.size();
+  const size_t cow_bytes = ncow * 2 * sizeof(int32_t), patch_off = (cow_bytes + 255) & ~size_t(255);
+  const size_t bytes = patch_off + npatch * sizeof(TablePatch);
+  StagingSlot* s;
+  if (pkv_status r = p->staging.acquire(bytes, &s)) return r;
+  if (ncow) memcpy(s->host, A.pending_cow.data(), cow_bytes);
+  if (npatch) memcpy(s->host + patch_off, A.pending_patch.data(), npatch * sizeof(TablePatch));
+  if (pkv_status r = Staging::upload(s, bytes, st)) return r;
+  const auto& c = p->cfg;
+  if (ncow) {
+    const size_t blk_bytes = (size_t)c.n_kv_heads * kBlock * c.head_dim * elem_bytes(c.kv_dtype);
+    const size_t scl = c.kv_dtype == PKV_KV_FP8_E4M3 ? (size_t)c.n_kv_heads * kBlock : 0;
+    if (pkv_status r = launch(p, PKV_KERNEL_COW_COPY, st, [&] {
+          return launch_cow_copy((const int32_t*)s->dev, (int)ncow, p->buf.k_pool, p->buf.v_pool,
+                                 p->buf.k_scale, p->buf.v_scale, blk_bytes, scl, st);
+        }))
+      return r;
+  }
+  if (npatch) {
+    if (pkv_status r = launch(p, PKV_KERNEL_TABLE_PATCH, st, [&] {
+          return launch_table_patch((const int32_t*)(s->dev + patch_off), (int)npatch, p->buf.block_tables, st);
+        }))
+      return r;
+  }
+  if (pkv_status r = Staging::release(s, st)) return r;
+  A.pending_cow.clear();
+  A.pending_patch.clear();
+  return PKV_OK;
+}
+
+pkv_status check_seq_list(const pkv_pool* p, int32_t n, const int32_t* ids) {
+  if (n < 0) return fail(PKV_ERR_INVALID_ARG, "n_seqs < 0");
+  if (n > 0 && !ids) return fail(PKV_ERR_INVALID_ARG, "seq_ids is NULL");
+  for (int32_t i = 0; i < n; ++i)
+    if (!p->alloc.valid_seq(ids[i])) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", ids[i]);
+  return PKV_OK;
+}
+
+bool valid_mask(int mode, int S, int W) {
+  if (mode == PKV_MASK_FULL) return true;
+  if (mode == PKV_MASK_SLIDING) return W >= 0;
+  if (mode == PKV_MASK_SINK_WINDOW) return S >= 0 && W >= 0;
+  return false;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// decode planning
+// ---------------------------------------------------------------------------
+
+namespace {
+
+constexpr int kMinUnitsPerWarp = 4;
+
+struct Plan {
+  std::vector<int32_t> warp_begin;
+  std::vector<Piece> pieces;
+  std::vector<CombineItem> combine;
+  int total_warps = 0;
+  int n_partials = 0;
+};
+
+struct Seg {
+  int32_t b, g, lo, hi;  // batch index, kv head, logical blocks [lo, hi)
+};
+
+int max_total_warps(const pkv_pool* p) {
+  return std::max(1, p->num_sms * std::max(1, p->tc_ctas_per_sm) * std::max(1, p->tc_warps_per_cta));
+}
+
+size_t max_pieces(const pkv_pool* p, int32_t n_seqs, int32_t num_splits) {
+  const size_t nbg = (size_t)n_seqs * p->cfg.n_kv_heads;
+  const size_t a = 2 * nbg + (size_t)max_total_warps(p) + 1;
+  const size_t b = nbg * (size_t)std::max(1, num_splits) + nbg + 1;
+  return std::max(a, b);
+}
+
+void build_plan(const pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, int W, int num_splits,
+                Plan& plan) {
+  const int Hk = p->cfg.n_kv_heads;
+  const auto& A = p->alloc;
+  std::vector<Seg> segs;
+  std::vector<int64_t> bg_units((size_t)n * Hk, 0);
+  for (int32_t b = 0; b < n; ++b) {
+    BlockRange r[2];
+    const int nr = keep_ranges(A.len[ids[b]], mode, S, W, r);
+    for (int g = 0; g < Hk; ++g)
+      for (int k = 0; k < nr; ++k) {
+        segs.push_back({b, g, r[k].lo, r[k].hi});
+        bg_units[(size_t)b * Hk + g] += r[k].hi - r[k].lo;
+      }
+  }
+  plan.pieces.clear();
+  plan.combine.clear();
+  plan.warp_begin.clear();
+  const int TWmax = max_total_warps(p);
+  auto piece_of = [&](const Seg& s, int32_t lo, int32_t hi) {
+    Piece pc;
+    pc.seq_slot = ids[s.b];
+    pc.q_row = s.b;
+    pc.kv_head = s.g;
+    pc.lblk_begin = lo;
+    pc.lblk_end = hi;
+    pc.ctx_len = A.len[ids[s.b]];
+    pc.out_index = -1;
+    pc.flags = 0;
+    return pc;
+  };
+  std::vector<int32_t> piece_warp;  // warp of each piece
+  if (num_splits <= 0) {
+    int64_t U = 0;
+    for (auto& s : segs) U += s.hi - s.lo;
+    int TW = (int)std::min<int64_t>(TWmax, (U + kMinUnitsPerWarp - 1) / kMinUnitsPerWarp);
+    plan.total_warps = TW;
+    if (TW > 0) {
+      auto bound = [&](int w) { return (int64_t)((__int128)U * w / TW); };
+      int w = 0;
+      int64_t pos = 0;
+      for (auto& s : segs) {
+        int64_t start = pos, end = pos + (s.hi - s.lo);
+        while (start < end) {
+          while (bound(w + 1) <= start) ++w;
+          int64_t stop = std::min(end, bound(w + 1));
+          plan.pieces.push_back(piece_of(s, s.lo + (int32_t)(start - pos), s.lo + (int32_t)(stop - pos)));
+          piece_warp.push_back(w);
+          start = stop;
+        }
+        pos = end;
+      }
+    }
+  } else {
+    // exactly num_splits equal parts of each (sequence, kv head) unit list
+    struct Part {
+      size_t first_piece, n_pieces;
+    };
+    std::vector<Piece> parts_pieces;
+    std::vector<Part> parts;
+    size_t si = 0;
+    for (int32_t b = 0; b < n; ++b)
+      for (int g = 0; g < Hk; ++g) {
+        size_t s0 = si;
+        while (si < segs.size() && segs[si].b == b && segs[si].g == g) ++si;
+        const int64_t nu = bg_units[(size_t)b * Hk + g];
+        for (int k = 0; k < num_splits; ++k) {
+          int64_t u0 = nu * k / num_splits, u1 = nu * (k + 1) / num_splits;
+          if (u1 <= u0) continue;
+          Part pt{parts_pieces.size(), 0};
+          int64_t off = 0;
+          for (size_t j = s0; j < si; ++j) {
+            const Seg& s = segs[j];
+            int64_t a = std::max(u0, off), e = std::min(u1, off + (s.hi - s.lo));
+            if (a < e) {
+              parts_pieces.push_back(piece_of(s, s.lo + (int32_t)(a - off), s.lo + (int32_t)(e - off)));
+              ++pt.n_pieces;
+            }
+            off += s.hi - s.lo;
+          }
+          parts_pieces[parts_pieces.size() - 1].flags |= kPieceLastOfRun;
+          parts.push_back(pt);
+        }
+      }
+    const int64_t P = (int64_t)parts.size();
+    const int TW = (int)std::min<int64_t>(TWmax, P);
+    plan.total_warps = TW;
+    for (int w = 0; w < TW; ++w) {
+      const int64_t a = P * w / TW, e = P * (w + 1) / TW;
+      for (int64_t k = a; k < e; ++k)
+        for (size_t j = 0; j < parts[k].n_pieces; ++j) {
+          plan.pieces.push_back(parts_pieces[parts[k].first_piece + j]);
+          piece_warp.push_back(w);
+        }
+    }
+  }
+  // warp boundaries
+  plan.warp_begin.assign(plan.total_warps + 1, 0);
+  {
+    size_t k = 0;
+    for (int w = 0; w < plan.total_warps; ++w) {
+      plan.warp_begin[w] = (int32_t)k;
+      while (k < plan.pieces.size() && piece_warp[k] == w) ++k;
+    }
+    plan.warp_begin[plan.total_warps] = (int32_t)k;
+  }
+  // runs: consecutive pieces of one (b, g) inside one warp; explicit split
+  // parts already carry their own run ends
+  const size_t np = plan.pieces.size();
+  for (size_t k = 0; k < np; ++k) {
+    const bool end_of_warp = k + 1 == np || piece_warp[k + 1] != piece_warp[k];
+    const bool next_other = k + 1 == np || plan.pieces[k + 1].q_row != plan.pieces[k].q_row ||
+                            plan.pieces[k + 1].kv_head != plan.pieces[k].kv_head;
+    if (end_of_warp || next_other) plan.pieces[k].flags |= kPieceLastOfRun;
+  }
+  // partial indices: a run that covers all units of its (b, g) writes the
+  // final output; every other run gets a partial record
+  std::vector<int32_t> first_partial((size_t)n * Hk, -1), n_part((size_t)n * Hk, 0);
+  int next_partial = 0;
+  size_t run_start = 0;
+  for (size_t k = 0; k < np; ++k) {
+    if (!(plan.pieces[k].flags & kPieceLastOfRun)) continue;
+    const size_t bg = (size_t)plan.pieces[k].q_row * Hk + plan.pieces[k].kv_head;
+    int64_t units = 0;
+    for (size_t j = run_start; j <= k; ++j) units += plan.pieces[j].lblk_end - plan.pieces[j].lblk_begin;
+    int32_t idx = -1;
+    if (units != bg_units[bg]) {
+      idx = next_partial++;
+      if (first_partial[bg] < 0) first_partial[bg] = idx;
+      ++n_part[bg];
+    }
+    for (size_t j = run_start; j <= k; ++j) plan.pieces[j].out_index = idx;
+    run_start = k + 1;
+  }
+  plan.n_partials = next_partial;
+  for (int32_t b = 0; b < n; ++b)
+    for (int g = 0; g < Hk; ++g) {
+      const size_t bg = (size_t)b * Hk + g;
+      if (bg_units[bg] == 0) plan.combine.push_back({b, g, 0, 0});
+      else if (n_part[bg] > 0) plan.combine.push_back({b, g, first_partial[bg], n_part[bg]});
+    }
+}
+
+pkv_status check_keep_blocks_present(const pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, int W) {
+  const auto& A = p->alloc;
+  for (int32_t b = 0; b < n; ++b) {
+    const int32_t s = ids[b];
+    if (!A.holes[s]) continue;
+    BlockRange r[2];
+    const int nr = keep_ranges(A.len[s], mode, S, W, r);
+    for (int k = 0; k < nr; ++k)
+      for (int32_t lb = r[k].lo; lb < r[k].hi; ++lb)
+        if (A.table[s][lb] < 0)
+          return fail(PKV_ERR_INVALID_ARG, "sequence %d: block %d of the keep-set was evicted", s, lb);
+  }
+  return PKV_OK;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// C ABI
+// ---------------------------------------------------------------------------
+
+extern "C" {
+
+const char* pkv_last_error(void) { return g_last_error.c_str(); }
+const char* pkv_version(void) { return "pkv 0.1 (sm_103a)"; }
+
+pkv_status pkv_pool_required_bytes(const pkv_pool_config* cfg, pkv_buffer_sizes* out) {
+  if (pkv_status r = check_config(cfg)) return r;
+  if (!out) return fail(PKV_ERR_INVALID_ARG, "out is NULL");
+  const size_t rows = (size_t)cfg->num_blocks * cfg->n_kv_heads * kBlock;
+  out->k_pool = out->v_pool = rows * cfg->head_dim * elem_bytes(cfg->kv_dtype);
+  out->k_scale = out->v_scale = cfg->kv_dtype == PKV_KV_FP8_E4M3 ? rows * sizeof(float) : 0;
+  out->block_tables = (size_t)cfg->max_seqs * cfg->max_blocks_per_seq * sizeof(int32_t);
+  out->status = 4 * sizeof(int32_t);
+  return PKV_OK;
+}
+
+pkv_status pkv_pool_create(const pkv_pool_config* cfg, const pkv_pool_buffers* buffers, pkv_pool** out) {
+  if (!out) return fail(PKV_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (pkv_status r = check_config(cfg)) return r;
+  pkv_pool* p = new pkv_pool();
+  p->cfg = *cfg;
+  p->cfg.free_order = nullptr;
+  p->G = cfg->n_heads / cfg->n_kv_heads;
+  p->alloc.init(cfg->num_blocks, cfg->max_seqs, cfg->max_blocks_per_seq, cfg->alloc_seed, cfg->free_order);
+  if (buffers) {
+    const auto& b = *buffers;
+    const bool fp8 = cfg->kv_dtype == PKV_KV_FP8_E4M3;
+    if (!b.k_pool || !b.v_pool || !b.block_tables || !b.status || (fp8 && (!b.k_scale || !b.v_scale))) {
+      delete p;
+      return fail(PKV_ERR_INVALID_ARG, "a required device buffer is NULL");
+    }
+    if (((uintptr_t)b.k_pool | (uintptr_t)b.v_pool) & 127) {
+      delete p;
+      return fail(PKV_ERR_INVALID_ARG, "k_pool / v_pool must be 128-byte aligned");
+    }
+    if (fp8 && (((uintptr_t)b.k_scale | (uintptr_t)b.v_scale) & 15)) {
+      delete p;
+      return fail(PKV_ERR_INVALID_ARG, "k_scale / v_scale must be 16-byte aligned");
+    }
+    p->device = true;
+    p->buf = b;
+    auto fail_dev = [&](pkv_status r) {
+      p->staging.destroy();
+      delete p;
+      return r;
+    };
+    cudaError_t e = cudaGetDevice(&p->device_id);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device_id);
+    if (e != cudaSuccess) return fail_dev(fail(PKV_ERR_CUDA, "device query failed: %s", cudaGetErrorString(e)));
+    const size_t tbytes = (size_t)cfg->max_seqs * cfg->max_blocks_per_seq * sizeof(int32_t);
+    e = cudaMemset(b.block_tables, 0xFF, tbytes);
+    if (e == cudaSuccess) e = cudaMemset(b.status, 0, 4 * sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_dev(fail(PKV_ERR_CUDA, "buffer init failed: %s", cudaGetErrorString(e)));
+    if (cfg->kv_dtype != PKV_KV_FP32) {
+      p->tc_path = true;
+      if (pkv_status r = make_tensor_map(&p->tmap_k, b.k_pool, p->cfg)) return fail_dev(r);
+      if (pkv_status r = make_tensor_map(&p->tmap_v, b.v_pool, p->cfg)) return fail_dev(r);
+      e = decode_tc_prepare(cfg->kv_dtype, p->G);
+      int occ = 0;
+      if (e == cudaSuccess) e = decode_tc_occupancy(cfg->kv_dtype, p->G, &occ);
+      if (e != cudaSuccess) return fail_dev(fail(PKV_ERR_CUDA, "decode kernel setup failed: %s", cudaGetErrorString(e)));
+      p->tc_ctas_per_sm = std::max(1, occ);
+      p->tc_warps_per_cta = decode_tc_warps_per_cta(cfg->kv_dtype);
+      p->tc_smem = decode_tc_smem_bytes(cfg->kv_dtype);
+    }
+  }
+  *out = p;
+  return PKV_OK;
+}
+
+void pkv_pool_destroy(pkv_pool* p) {
+  if (!p) return;
+  if (p->device) {
+    p->staging.destroy();
+    p->timing.destroy();
+  }
+  delete p;
+}
+
+pkv_status pkv_seq_add(pkv_pool* p, int32_t* seq_out) {
+  if (!p || !seq_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  auto& A = p->alloc;
+  if (A.free_ids.empty()) return fail(PKV_ERR_OUT_OF_SEQS, "all %d sequence ids are in use", A.max_seqs);
+  int32_t s = *A.free_ids.begin();
+  A.free_ids.erase(A.free_ids.begin());
+  A.live[s] = 1;
+  A.holes[s] = 0;
+  A.len[s] = 0;
+  A.table[s].clear();
+  *seq_out = s;
+  return PKV_OK;
+}
+
+pkv_status pkv_seq_fork(pkv_pool* p, int32_t src, int32_t* dst_out) {
+  if (!p || !dst_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  auto& A = p->alloc;
+  if (!A.valid_seq(src)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", src);
+  int32_t d;
+  if (pkv_status r = pkv_seq_add(p, &d)) return r;
+  const int32_t nblk = ceil_div(A.len[src], kBlock);
+  for (int32_t lb = 0; lb < nblk; ++lb) {
+    const int32_t b = A.table[src][lb];
+    if (b >= 0) ++A.refcount[b];
+    A.set_entry(d, lb, b);
+  }
+  A.len[d] = A.len[src];
+  A.holes[d] = A.holes[src];
+  *dst_out = d;
+  return PKV_OK;
+}
+
+pkv_status pkv_seq_truncate(pkv_pool* p, int32_t s, int32_t new_len) {
+  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  auto& A = p->alloc;
+  if (!A.valid_seq(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", s);
+  if (new_len < 0 || new_len > A.len[s]) return fail(PKV_ERR_INVALID_ARG, "new_len %d outside [0, %d]", new_len, A.len[s]);
+  const int32_t keep_blk = ceil_div(new_len, kBlock);
+  if (new_len % kBlock && A.table[s][keep_blk - 1] < 0)
+    return fail(PKV_ERR_INVALID_ARG, "the new last block of sequence %d was evicted", s);
+  A.drop_from(s, keep_blk);
+  A.len[s] = new_len;
+  return PKV_OK;
+}
+
+pkv_status pkv_seq_free(pkv_pool* p, int32_t s) {
+  if (pkv_status r = pkv_seq_truncate(p, s, 0)) return r;
+  auto& A = p->alloc;
+  A.live[s] = 0;
+  A.holes[s] = 0;
+  A.free_ids.insert(s);
+  return PKV_OK;
+}
+
+pkv_status pkv_seq_evict(pkv_pool* p, int32_t s, int32_t S, int32_t W) {
+  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  auto& A = p->alloc;
+  if (!A.valid_seq(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", s);
+  if (S < 0 || W < 1) return fail(PKV_ERR_INVALID_ARG, "need num_sinks >= 0 and window >= 1");
+  const int32_t L = A.len[s];
+  if ((int64_t)L <= (int64_t)S + W) return PKV_OK;
+  const int32_t nblk = ceil_div(L, kBlock);
+  for (int32_t lb = 0; lb < nblk; ++lb) {
+    const int32_t b = A.table[s][lb];
+    if (b < 0) continue;
+    const int32_t lo = lb * kBlock, hi = std::min(L, lo + kBlock);  // tokens [lo, hi)
+    const bool touches_sinks = lo < S;
+    const bool touches_window = hi > L - W;
+    if (!touches_sinks && !touches_window) {
+      A.release(b);
+      A.set_entry(s, lb, -1);
+      A.holes[s] = 1;
+    }
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_seq_len(const pkv_pool* p, int32_t s, int32_t* len_out) {
+  if (!p || !len_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  if (!p->alloc.valid_seq(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", s);
+  *len_out = p->alloc.len[s];
+  return PKV_OK;
+}
+
+pkv_status pkv_get_block_table(const pkv_pool* p, int32_t s, int32_t* host_out, int32_t cap, int32_t* n_out) {
+  if (!p || !n_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  const auto& A = p->alloc;
+  if (!A.valid_seq(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", s);
+  const int32_t n = ceil_div(A.len[s], kBlock);
+  *n_out = n;
+  if (n > cap || (n > 0 && !host_out)) return fail(PKV_ERR_INVALID_ARG, "capacity %d < %d entries", cap, n);
+  for (int32_t i = 0; i < n; ++i) host_out[i] = A.table[s][i];
+  return PKV_OK;
+}
+
+pkv_status pkv_pool_stats(const pkv_pool* p, pkv_stats* out) {
+  if (!p || !out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  const auto& A = p->alloc;
+  out->num_blocks = A.NB;
+  out->free_blocks = (int64_t)A.free_blocks.size();
+  out->used_blocks = A.NB - out->free_blocks;
+  out->shared_blocks = 0;
+  for (int32_t r : A.refcount) out->shared_blocks += r > 1;
+  out->active_seqs = A.max_seqs - (int64_t)A.free_ids.size();
+  out->cow_copies = A.cow_count;
+  out->blocks_allocated = A.n_alloc;
+  out->blocks_freed = A.n_freed;
+  return PKV_OK;
+}
+
+pkv_status pkv_reserve_slots(pkv_pool* p, int32_t n, const int32_t* ids, int32_t T, int64_t* slots_out,
+                             int32_t* cow_out, int32_t cow_cap, int32_t* n_cow_out) {
+  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  if (T < 0) return fail(PKV_ERR_INVALID_ARG, "T < 0");
+  if (pkv_status r = check_seq_list(p, n, ids)) return r;
+  auto& A = p->alloc;
+  {
+    std::vector<int32_t> sorted(ids, ids + n);
+    std::sort(sorted.begin(), sorted.end());
+    if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end())
+      return fail(PKV_ERR_INVALID_ARG, "a sequence appears twice in one append");
+  }
+  // dry run: count the blocks needed, with the refcount drops earlier
+  // copies in this call cause
+  int64_t need = 0;
+  std::unordered_map<int32_t, int32_t> dropped;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t s = ids[i];
+    if ((int64_t)A.len[s] + T > (int64_t)A.max_blocks * kBlock)
+      return fail(PKV_ERR_INVALID_ARG, "sequence %d would exceed max_blocks_per_seq", s);
+    for (int32_t t = 0; t < T; ++t) {
+      const int32_t pos = A.len[s] + t;
+      if (pos % kBlock == 0) {
+        ++need;
+      } else if (t == 0) {
+        const int32_t b = A.table[s][pos / kBlock];
+        if (b < 0) return fail(PKV_ERR_INVALID_ARG, "sequence %d: last block was evicted", s);
+        if (A.refcount[b] - dropped[b] > 1) {
+          ++need;
+          ++dropped[b];
+        }
+      }
+    }
+  }
+  if (need > (int64_t)A.free_blocks.size())
+    return fail(PKV_ERR_OUT_OF_BLOCKS, "append needs %lld blocks, %zu free", (long long)need, A.free_blocks.size());
+  int32_t ncow = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t s = ids[i];
+    for (int32_t t = 0; t < T; ++t) {
+      const int32_t pos = A.len[s];
+      const int32_t lb = pos / kBlock;
+      if (pos % kBlock == 0) {
+        A.set_entry(s, lb, A.take());
+      } else if (A.refcount[A.table[s][lb]] > 1) {
+        const int32_t old = A.table[s][lb];
+        const int32_t fresh = A.take();
+        --A.refcount[old];
+        A.set_entry(s, lb, fresh);
+        if (p->device) {
+          A.pending_cow.push_back(old);
+          A.pending_cow.push_back(fresh);
+        }
+        if (cow_out && ncow < cow_cap) {
+          cow_out[2 * ncow] = old;
+          cow_out[2 * ncow + 1] = fresh;
+        }
+        ++ncow;
+        ++A.cow_count;
+      }
+      if (slots_out) slots_out[(size_t)i * T + t] = (int64_t)A.table[s][lb] * kBlock + pos % kBlock;
+      A.len[s] = pos + 1;
+    }
+  }
+  if (!p->device) A.pending_patch.clear();
+  if (n_cow_out) *n_cow_out = ncow;
+  return PKV_OK;
+}
+
+pkv_status pkv_append(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, int32_t T, const void* k_new,
+                      const void* v_new) {
+  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  if (!p->device) return fail(PKV_ERR_NO_DEVICE, "host-only pool");
+  if ((int64_t)n * T > 0 && (!k_new || !v_new)) return fail(PKV_ERR_INVALID_ARG, "k_new / v_new is NULL");
+  const size_t ntok = (size_t)n * (size_t)std::max(T, 0);
+  std::vector<int64_t> slots(ntok);
+  if (pkv_status r = pkv_reserve_slots(p, n, ids, T, slots.data(), nullptr, 0, nullptr)) return r;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (pkv_status r = flush_pending(p, st)) return r;
+  if (ntok == 0) return PKV_OK;
+  const auto& c = p->cfg;
+  const size_t row_bytes = (size_t)c.n_kv_heads * c.head_dim * (c.kv_dtype == PKV_KV_FP32 ? 4 : 2);
+  // large appends go through the staging ring in chunks of tokens
+  const size_t chunk = size_t(1) << 20;
+  for (size_t t0 = 0; t0 < ntok; t0 += chunk) {
+    const size_t nt = std::min(chunk, ntok - t0);
+    StagingSlot* s;
+    if (pkv_status r = p->staging.acquire(nt * sizeof(int64_t), &s)) return r;
+    memcpy(s->host, slots.data() + t0, nt * sizeof(int64_t));
+    if (pkv_status r = Staging::upload(s, nt * sizeof(int64_t), st)) return r;
+    if (pkv_status r = launch(p, PKV_KERNEL_APPEND, st, [&] {
+          return launch_append(c.kv_dtype, (const int64_t*)s->dev, (int)nt, c.n_kv_heads, c.head_dim,
+                               (const char*)k_new + t0 * row_bytes, (const char*)v_new + t0 * row_bytes,
+                               p->buf.k_pool, p->buf.v_pool, p->buf.k_scale, p->buf.v_scale, st);
+        }))
+      return r;
+    if (pkv_status r = Staging::release(s, st)) return r;
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_decode_workspace_size(const pkv_pool* p, int32_t n, int32_t num_splits, size_t* bytes_out) {
+  if (!p || !bytes_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  if (n < 0 || num_splits < 0) return fail(PKV_ERR_INVALID_ARG, "negative size");
+  if (p->cfg.kv_dtype == PKV_KV_FP32) {
+    *bytes_out = 0;
+    return PKV_OK;
+  }
+  *bytes_out = max_pieces(p, n, num_splits) * partial_floats(p->G, p->cfg.head_dim) * sizeof(float);
+  return PKV_OK;
+}
+
+pkv_status pkv_decode_attn(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, const void* q, float scale,
+                           int32_t mode, int32_t S, int32_t W, int32_t num_splits, void* out, float* lse,
+                           float* logits, int64_t logits_stride, void* workspace, size_t workspace_bytes) {
+  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  if (!p->device) return fail(PKV_ERR_NO_DEVICE, "host-only pool");
+  if (pkv_status r = check_seq_list(p, n, ids)) return r;
+  if (!valid_mask(mode, S, W)) return fail(PKV_ERR_INVALID_ARG, "invalid mask %d (%d, %d)", mode, S, W);
+  if (num_splits < 0) return fail(PKV_ERR_INVALID_ARG, "num_splits < 0");
+  if (n > 0 && (!q || !out)) return fail(PKV_ERR_INVALID_ARG, "q / out is NULL");
+  const auto& A = p->alloc;
+  int32_t maxlen = 0;
+  for (int32_t i = 0; i < n; ++i) maxlen = std::max(maxlen, A.len[ids[i]]);
+  if (logits && logits_stride < maxlen) return fail(PKV_ERR_INVALID_ARG, "logits_stride < max length");
+  if (pkv_status r = check_keep_blocks_present(p, n, ids, mode, S, W)) return r;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (pkv_status r = flush_pending(p, st)) return r;
+  if (n == 0) return PKV_OK;
+  const auto& c = p->cfg;
+
+  if (c.kv_dtype == PKV_KV_FP32) {
+    StagingSlot* s;
+    if (pkv_status r = p->staging.acquire(n * sizeof(SeqRow), &s)) return r;
+    SeqRow* rows = (SeqRow*)s->host;
+    for (int32_t i = 0; i < n; ++i) rows[i] = {ids[i], i, A.len[ids[i]], 0};
+    if (pkv_status r = Staging::upload(s, n * sizeof(SeqRow), st)) return r;
+    DecodeF32Params prm;
+    prm.k_pool = (const float*)p->buf.k_pool;
+    prm.v_pool = (const float*)p->buf.v_pool;
+    prm.tables = p->buf.block_tables;
+    prm.max_blocks = c.max_blocks_per_seq;
+    prm.num_blocks = c.num_blocks;
+    prm.n_heads = c.n_heads;
+    prm.n_kv_heads = c.n_kv_heads;
+    prm.head_dim = c.head_dim;
+    prm.rows = (const SeqRow*)s->dev;
+    prm.n_seqs = n;
+    prm.q = (const float*)q;
+    prm.out = (float*)out;
+    prm.lse = lse;
+    prm.logits = logits;
+    prm.logits_stride = logits_stride;
+    prm.scale = scale;
+    prm.mask_mode = mode;
+    prm.num_sinks = S;
+    prm.window = W;
+    prm.status = p->buf.status;
+    if (pkv_status r = launch(p, PKV_KERNEL_DECODE, st, [&] { return launch_decode_f32(prm, st); })) return r;
+    return Staging::release(s, st);
+  }
+
+  size_t need = 0;
+  pkv_decode_workspace_size(p, n, num_splits, &need);
+  Plan plan;
+  build_plan(p, n, ids, mode, S, W, num_splits, plan);
+  const size_t pf = (size_t)partial_floats(p->G, c.head_dim) * sizeof(float);
+  if (plan.n_partials > 0 && (!workspace || workspace_bytes < plan.n_partials * pf))
+    return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
+  if (plan.n_partials > 0 && ((uintptr_t)workspace & 15))
+    return fail(PKV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  const size_t wb_bytes = plan.warp_begin.size() * sizeof(int32_t);
+  const size_t pieces_off = (wb_bytes + 31) & ~size_t(31);
+  const size_t comb_off = pieces_off + plan.pieces.size() * sizeof(Piece);
+  const size_t bytes = comb_off + plan.combine.size() * sizeof(CombineItem);
+  StagingSlot* s;
+  if (pkv_status r = p->staging.acquire(bytes, &s)) return r;
+  memcpy(s->host, plan.warp_begin.data(), wb_bytes);
+  if (!plan.pieces.empty()) memcpy(s->host + pieces_off, plan.pieces.data(), plan.pieces.size() * sizeof(Piece));
+  if (!plan.combine.empty())
+    memcpy(s->host + comb_off, plan.combine.data(), plan.combine.size() * sizeof(CombineItem));
+  if (pkv_status r = Staging::upload(s, bytes, st)) return r;
+  if (plan.total_warps > 0) {
+    DecodeTCParams prm;
+    prm.tmap_k = p->tmap_k;
+    prm.tmap_v = p->tmap_v;
+    prm.k_scale = p->buf.k_scale;
+    prm.v_scale = p->buf.v_scale;
+    prm.tables = p->buf.block_tables;
+    prm.max_blocks = c.max_blocks_per_seq;
+    prm.num_blocks = c.num_blocks;
+    prm.n_heads = c.n_heads;
+    prm.n_kv_heads = c.n_kv_heads;
+    prm.q = q;
+    prm.out = out;
+    prm.lse = lse;
+    prm.logits = logits;
+    prm.logits_stride = logits_stride;
+    prm.pieces = (const Piece*)(s->dev + pieces_off);
+    prm.warp_begin = (const int32_t*)s->dev;
+    prm.total_warps = plan.total_warps;
+    prm.partials = (float*)workspace;
+    prm.scale = scale;
+    prm.mask_mode = mode;
+    prm.num_sinks = S;
+    prm.window = W;
+    prm.status = p->buf.status;
+    const int ctas = ceil_div(plan.total_warps, p->tc_warps_per_cta);
+    if (pkv_status r = launch(p, PKV_KERNEL_DECODE, st, [&] { return launch_decode_tc(c.kv_dtype, p->G, prm, ctas, st); }))
+      return r;
+  }
+  if (!plan.combine.empty()) {
+    if (pkv_status r = launch(p, PKV_KERNEL_COMBINE, st, [&] {
+          return launch_combine((const CombineItem*)(s->dev + comb_off), (int)plan.combine.size(),
+                                (const float*)workspace, p->G, c.head_dim, c.n_heads, 1, out, lse, st);
+        }))
+      return r;
+  }
+  return Staging::release(s, st);
+}
+
+pkv_status pkv_h2o_scores(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, const float* logits,
+                          int64_t logits_stride, const float* lse, int32_t mode, int32_t S, int32_t W, float* acc,
+                          int64_t acc_stride) {
+  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  if (!p->device) return fail(PKV_ERR_NO_DEVICE, "host-only pool");
+  if (pkv_status r = check_seq_list(p, n, ids)) return r;
+  if (!valid_mask(mode, S, W)) return fail(PKV_ERR_INVALID_ARG, "invalid mask");
+  if (n > 0 && (!logits || !lse || !acc)) return fail(PKV_ERR_INVALID_ARG, "NULL device array");
+  const auto& A = p->alloc;
+  int32_t maxlen = 0, max_keep = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t L = A.len[ids[i]];
+    maxlen = std::max(maxlen, L);
+    int32_t k = L;
+    if (mode == PKV_MASK_SLIDING) k = std::min(L, W + 1);
+    if (mode == PKV_MASK_SINK_WINDOW && (int64_t)L > (int64_t)S + W) k = S + W;
+    max_keep = std::max(max_keep, k);
+  }
+  if (logits_stride < maxlen || acc_stride < maxlen) return fail(PKV_ERR_INVALID_ARG, "stride < max length");
+  cudaStream_t st = (cudaStream_t)stream;
+  if (pkv_status r = flush_pending(p, st)) return r;
+  if (n == 0 || max_keep == 0) return PKV_OK;
+  StagingSlot* s;
+  if (pkv_status r = p->staging.acquire(n * sizeof(SeqRow), &s)) return r;
+  SeqRow* rows = (SeqRow*)s->host;
+  for (int32_t i = 0; i < n; ++i) rows[i] = {ids[i], i, A.len[ids[i]], 0};
+  if (pkv_status r = Staging::upload(s, n * sizeof(SeqRow), st)) return r;
+  const auto& c = p->cfg;
+  if (pkv_status r = launch(p, PKV_KERNEL_H2O_SCORE, st, [&] {
+        return launch_h2o_score((const SeqRow*)s->dev, n, c.n_heads, c.n_kv_heads, logits, logits_stride, lse, mode,
+                                S, W, acc, acc_stride, max_keep, st);
+      }))
+    return r;
+  return Staging::release(s, st);
+}
+
+pkv_status pkv_h2o_select(pkv_pool* p, void* stream, int32_t n, const int32_t* lens, const float* acc,
+                          int64_t acc_stride, int32_t budget, int32_t recent, int32_t* keep_idx, int64_t keep_stride,
+                          int32_t* keep_count) {
+  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  if (!p->device) return fail(PKV_ERR_NO_DEVICE, "host-only pool");
+  if (n < 0 || (n > 0 && !lens)) return fail(PKV_ERR_INVALID_ARG, "bad lens");
+  if (recent < 0 || budget < recent || budget < 1) return fail(PKV_ERR_INVALID_ARG, "need 0 <= recent <= budget, budget >= 1");
+  if (keep_stride < budget) return fail(PKV_ERR_INVALID_ARG, "keep_stride < budget");
+  if (n > 0 && (!acc || !keep_idx || !keep_count)) return fail(PKV_ERR_INVALID_ARG, "NULL device array");
+  for (int32_t i = 0; i < n; ++i)
+    if (lens[i] < 0 || lens[i] > acc_stride) return fail(PKV_ERR_INVALID_ARG, "length %d outside [0, acc_stride]", lens[i]);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (pkv_status r = flush_pending(p, st)) return r;
+  if (n == 0) return PKV_OK;
+  StagingSlot* s;
+  if (pkv_status r = p->staging.acquire(n * sizeof(SeqRow), &s)) return r;
+  SeqRow* rows = (SeqRow*)s->host;
+  for (int32_t i = 0; i < n; ++i) rows[i] = {-1, i, lens[i], 0};
+  if (pkv_status r = Staging::upload(s, n * sizeof(SeqRow), st)) return r;
+  if (pkv_status r = launch(p, PKV_KERNEL_H2O_SELECT, st, [&] {
+        return launch_h2o_select((const SeqRow*)s->dev, n, acc, acc_stride, budget, recent, keep_idx, keep_stride,
+                                 keep_count, st);
+      }))
+    return r;
+  return Staging::release(s, st);
+}
+
+pkv_status pkv_sync_status(pkv_pool* p, void* stream) {
+  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  if (!p->device) return fail(PKV_ERR_NO_DEVICE, "host-only pool");
+  cudaStream_t st = (cudaStream_t)stream;
+  PKV_CUDA(cudaStreamSynchronize(st));
+  int32_t w[4] = {0, 0, 0, 0};
+  PKV_CUDA(cudaMemcpy(w, p->buf.status, sizeof w, cudaMemcpyDeviceToHost));
+  if (w[0]) {
+    PKV_CUDA(cudaMemset(p->buf.status, 0, sizeof w));
+    PKV_CUDA(cudaDeviceSynchronize());
+    if (w[0] & kStatusTimeout) return fail(PKV_ERR_TIMEOUT, "a device wait timed out (info %d)", w[1]);
+    return fail(PKV_ERR_DEVICE_ASSERT, "device range check failed (info %d, %d)", w[1], w[2]);
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_timing_enable(pkv_pool* p, int32_t enable) {
+  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  p->timing.enabled = enable != 0 && p->device;
+  return PKV_OK;
+}
+
+pkv_status pkv_timing_read(pkv_pool* p, double* total_ms, int64_t* launches) {
+  if (!p || !total_ms || !launches) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  for (int k = 0; k < PKV_KERNEL_COUNT; ++k) {
+    double sum = 0;
+    for (auto& pr : p->timing.marks[k]) {
+      PKV_CUDA(cudaEventSynchronize(pr.second));
+      float ms = 0;
+      PKV_CUDA(cudaEventElapsedTime(&ms, pr.first, pr.second));
+      sum += ms;
+      p->timing.spare.push_back(pr.first);
+      p->timing.spare.push_back(pr.second);
+    }
+    total_ms[k] = sum;
+    launches[k] = (int64_t)p->timing.marks[k].size();
+    p->timing.marks[k].clear();
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_launch_count(const pkv_pool* p, int64_t* out) {
+  if (!p || !out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  *out = p->launches;
+  return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,190 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry point
+declared in include/pkv.h, and its host allocator replays bit-exactly
+against the oracle's allocator (same seeds, same operations)."""
+import os
+import random
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    from paged_kv_cache_282_gb300 import build
+    build.build()
+    import paged_kv_cache_282_gb300 as m
+    m.load()
+    return m
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(pkv):
+    names = _declared_functions()
+    assert len(names) >= 20
+    lib = pkv.load()
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(pkv._abi.SIGNATURES), "binding and header disagree"
+    assert b"sm_103a" in lib.pkv_version()
+
+
+def test_required_bytes(pkv):
+    import ctypes
+    from paged_kv_cache_282_gb300 import _abi
+    cfg = _abi.pkv_pool_config(100, 16, 32, 8, 128, 4, 64, 2, 0, None)
+    sz = _abi.pkv_buffer_sizes()
+    _abi.check(pkv.load().pkv_pool_required_bytes(ctypes.byref(cfg), ctypes.byref(sz)))
+    assert sz.k_pool == 100 * 8 * 16 * 128 and sz.k_scale == 100 * 8 * 16 * 4
+    assert sz.block_tables == 4 * 64 * 4 and sz.status == 16
+
+
+@pytest.mark.parametrize("bad", [dict(block_size=8), dict(n_heads=24, n_kv_heads=8),
+                                 dict(head_dim=96), dict(kv_dtype=7)])
+def test_config_rejected(pkv, bad):
+    import ctypes
+    from paged_kv_cache_282_gb300 import _abi
+    kw = dict(num_blocks=10, block_size=16, n_heads=32, n_kv_heads=8, head_dim=128, max_seqs=2,
+              max_blocks_per_seq=4, kv_dtype=1, alloc_seed=0, free_order=None)
+    kw.update(bad)
+    cfg = _abi.pkv_pool_config(**kw)
+    h = ctypes.c_void_p()
+    st = pkv.load().pkv_pool_create(ctypes.byref(cfg), None, ctypes.byref(h))
+    assert st in (1, 2)
+    assert pkv.load().pkv_last_error()
+
+
+def test_host_only_pool_refuses_device_work(pkv):
+    c = pkv.PagedKVCache(8, 4, 2, 64, 2, 4, kv_dtype="fp32", host_only=True)
+    s = c.seq_add()
+    with pytest.raises(pkv.PKVError) as e:
+        c.decode.__func__  # noqa: B018 (bound method exists)
+        import ctypes
+        ids = np.array([s], dtype=np.int32)
+        pkv._abi.check(c.lib.pkv_decode_attn(c.handle, None, 1, ids.ctypes.data_as(ctypes.c_void_p), None, 1.0,
+                                             0, 0, 0, 0, None, None, None, 0, None, 0))
+    assert e.value.status == 8
+
+
+def test_page_layout_example_via_library(pkv):
+    order = [7, 12, 3, 5, 8, 1, 2, 0, 9, 4, 6, 10, 11, 13, 14, 15]
+    c = pkv.PagedKVCache(16, 4, 2, 64, 4, 8, kv_dtype="fp32", free_order=order, host_only=True)
+    got = {}
+    for name, L in (("A", 35), ("B", 10), ("C", 70)):
+        s = c.seq_add()
+        c.reserve_slots([s], L)
+        got[name] = c.block_table(s).tolist()
+    assert got == {"A": [7, 12, 3], "B": [5], "C": [8, 1, 2, 0, 9]}
+
+
+def _replay(pkv, seed):
+    rng = random.Random(seed)
+    NB = rng.randint(8, 80)
+    aseed = rng.randint(0, 2 ** 63)
+    lib = pkv.PagedKVCache(NB, 4, 2, 64, 10, 48, kv_dtype="fp32", alloc_seed=aseed, host_only=True)
+    ora = oracle.OracleAllocator(NB, 10, 48, seed=aseed)
+    live = []
+    for op in range(150):
+        r = rng.random()
+        if r < 0.15 or not live:
+            try:
+                a = lib.seq_add()
+            except pkv.PKVError as e:
+                assert e.status == 4
+                with pytest.raises(RuntimeError):
+                    ora.seq_add()
+                continue
+            assert a == ora.seq_add()
+            live.append(a)
+        elif r < 0.65:
+            ids = rng.sample(live, rng.randint(1, len(live)))
+            T = rng.randint(1, 24)
+            try:
+                s1, c1 = lib.reserve_slots(ids, T)
+                ok = True
+            except pkv.PKVError as e:
+                ok = e.status
+            try:
+                s2, c2 = ora.append(ids, T)
+                ok2 = True
+            except MemoryError:
+                ok2 = 3
+            except ValueError:
+                ok2 = 1
+            assert ok == ok2
+            if ok is True:
+                assert np.array_equal(s1, s2) and np.array_equal(c1, c2)
+        elif r < 0.75:
+            s = rng.choice(live)
+            try:
+                d = lib.seq_fork(s)
+            except pkv.PKVError as e:
+                assert e.status == 4
+                with pytest.raises(ValueError):
+                    ora.fork(s)
+                continue
+            assert d == ora.fork(s)
+            live.append(d)
+        elif r < 0.85:
+            s = rng.choice(live)
+            lib.seq_free(s)
+            ora.free(s)
+            live.remove(s)
+        elif r < 0.93:
+            s = rng.choice(live)
+            S, W = rng.randint(0, 5), rng.randint(1, 40)
+            lib.seq_evict(s, S, W)
+            ora.evict(s, S, W)
+        else:
+            s = rng.choice(live)
+            n = rng.randint(0, lib.seq_len(s))
+            try:
+                lib.seq_truncate(s, n)
+                ok = True
+            except pkv.PKVError:
+                ok = False
+            try:
+                ora.truncate(s, n)
+                ok2 = True
+            except ValueError:
+                ok2 = False
+            assert ok == ok2
+        for s in live:
+            assert lib.seq_len(s) == ora.length(s)
+            assert np.array_equal(lib.block_table(s), ora.table(s)), (seed, op, s)
+        st = lib.stats()
+        assert st["free_blocks"] == ora.num_free()
+        assert st["shared_blocks"] == sum(1 for b in range(NB) if ora.refcount(b) > 1)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_allocator_matches_oracle_replay(pkv, seed):
+    _replay(pkv, seed)
+
+
+def test_workload_sized_pool_tables_match_oracle(pkv):
+    """The pool of the Llama-3-8B-shaped batch: a seeded permutation of a pool
+    sized to fit exactly; every table entry must agree with the oracle."""
+    import workloads
+    wl = workloads.llama3_8b_batch64()
+    nb = sum((L + 15) // 16 for L in wl.lens)
+    lib = pkv.PagedKVCache(nb, 32, 8, 128, 64, 512, kv_dtype="bf16", alloc_seed=wl.seed, host_only=True)
+    ora = oracle.OracleAllocator(nb, 64, 512, seed=wl.seed)
+    for L in wl.lens:
+        a, b = lib.seq_add(), ora.seq_add()
+        s1, _ = lib.reserve_slots([a], L)
+        s2, _ = ora.append([b], L)
+        assert np.array_equal(s1, s2)
+    assert lib.stats()["free_blocks"] == 0
+    with pytest.raises(pkv.PKVError) as e:
+        lib.reserve_slots([0], 16)
+    assert e.value.status == 3

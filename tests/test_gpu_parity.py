@@ -1,0 +1,232 @@
+"""GPU parity: libpkv (through the C ABI) against the CPU oracle on the same
+seeded inputs.  Bit-exact for block tables, slot placement, COW copies, FP8
+codes and scales, and H2O keep-sets on a given score array; attention output
+within max abs error 1e-2 (BF16 KV) / 2e-2 (FP8 KV) / 1e-4 (FP32 KV)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from harness import TOL, Twin, fill_sequences, lse_err, max_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _pool_bytes_equal(tw: Twin, ids):
+    """K/V bytes (and FP8 scales) of every written slot of every live sequence
+    equal the oracle's; unwritten slots hold whatever the memory held."""
+    c = tw.cache
+    NB, Hk = tw.pool.NB, tw.wl.n_kv_heads
+    dev = [c.k_pool, c.v_pool]
+    host = [tw.pool.k, tw.pool.v]
+    if tw.wl.kv_dtype == "fp8":
+        dev += [c.k_scale, c.v_scale]
+        host += [tw.pool.k_scale, tw.pool.v_scale]
+    for dt, ht in zip(dev, host):
+        d = dt.contiguous().view(torch.uint8).reshape(NB, Hk, 16, -1).cpu().numpy()
+        h = ht.view(np.uint8).reshape(NB, Hk, 16, -1)
+        for s in ids:
+            L = tw.alloc.length(s)
+            for lb, blk in enumerate(tw.alloc.table(s)):
+                if blk >= 0:
+                    n = min(16, L - 16 * lb)
+                    assert np.array_equal(d[blk, :, :n], h[blk, :, :n]), (s, lb, blk)
+
+
+# --------------------------------------------------------------------------
+# tiny configuration: fp32, 4/2/64, lengths 35, 10, 70 in a 16-block pool
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("placement", ["page_literal", "seeded"])
+def test_tiny_fp32(placement):
+    wl = workloads.tiny()
+    order = [7, 12, 3, 5, 8, 1, 2, 0, 9, 4, 6, 10, 11, 13, 14, 15] if placement == "page_literal" else None
+    tw = Twin(wl, 16, 3, 8, seed=wl.seed, free_order=order)
+    ids = fill_sequences(tw, wl.lens)
+    if placement == "page_literal":
+        assert [tw.cache.block_table(s).tolist() for s in ids] == [[7, 12, 3], [5], [8, 1, 2, 0, 9]]
+    for s in ids:
+        assert np.array_equal(tw.cache.block_table(s), tw.alloc.table(s))
+    _pool_bytes_equal(tw, ids)
+    q = workloads.queries(wl)
+    out, lse = tw.cache.decode(ids, q.cuda(), scale=wl.scale)
+    tw.cache.sync_status()
+    ref, ref_lse, _ = tw.oracle_decode(ids, q)
+    assert max_err(out, ref) <= TOL["fp32"]
+    assert lse_err(lse, ref_lse) <= 1e-4
+    test_tiny_fp32.outputs = getattr(test_tiny_fp32, "outputs", []) + [out.cpu()]
+    if len(test_tiny_fp32.outputs) == 2:  # both placements: identical bits
+        assert torch.equal(test_tiny_fp32.outputs[0], test_tiny_fp32.outputs[1])
+
+
+# --------------------------------------------------------------------------
+# small ragged cases across dtypes, group sizes, masks and split counts
+# --------------------------------------------------------------------------
+
+LENS = (1, 15, 16, 17, 33, 200, 517, 1000, 2049)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_small_full_mask(kv, G):
+    wl = workloads.small(kv, lens=LENS, n_heads=8 * G, n_kv_heads=8, seed=30 + G)
+    nb = sum((L + 15) // 16 for L in LENS) + 5
+    tw = Twin(wl, nb, len(LENS), 160, seed=123)
+    ids = fill_sequences(tw, LENS)
+    _pool_bytes_equal(tw, ids)
+    q = workloads.queries(wl)
+    ref, ref_lse, _ = tw.oracle_decode(ids, q)
+    outs = []
+    for splits in (0, 1, 3, 64):
+        out, lse = tw.cache.decode(ids, q.cuda(), scale=wl.scale, num_splits=splits)
+        tw.cache.sync_status()
+        assert max_err(out, ref) <= TOL[kv], (splits, max_err(out, ref))
+        assert lse_err(lse, ref_lse) <= 2e-3, splits
+        outs.append(out.float().cpu())
+    # split count changes only the merge order
+    for o in outs[1:]:
+        assert (o - outs[0]).abs().max() <= 8e-3
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("mask,S,W", [("sliding", 0, 0), ("sliding", 0, 37), ("sliding", 0, 600),
+                                      ("sink_window", 4, 100), ("sink_window", 0, 64), ("sink_window", 20, 3),
+                                      ("sink_window", 0, 0)])
+def test_small_masks(kv, mask, S, W):
+    wl = workloads.small(kv, lens=LENS, seed=50)
+    nb = sum((L + 15) // 16 for L in LENS)
+    tw = Twin(wl, nb, len(LENS), 160, seed=9)
+    ids = fill_sequences(tw, LENS)
+    q = workloads.queries(wl)
+    ref, ref_lse, _ = tw.oracle_decode(ids, q, mask, S, W)
+    for splits in (0, 2):
+        out, lse = tw.cache.decode(ids, q.cuda(), scale=wl.scale, mask=mask, num_sinks=S, window=W,
+                                   num_splits=splits)
+        tw.cache.sync_status()
+        assert max_err(out, ref) <= TOL[kv]
+        assert lse_err(lse, ref_lse) <= 2e-3
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_physical_placement_invariance(kv):
+    """The output depends only on logical order: two different physical
+    placements give bit-identical results."""
+    wl = workloads.small(kv, lens=LENS, seed=60)
+    nb = sum((L + 15) // 16 for L in LENS) + 40
+    q = workloads.queries(wl).cuda()
+    res = []
+    for seed in (1, 2):
+        tw = Twin(wl, nb, len(LENS), 160, seed=seed)
+        ids = fill_sequences(tw, LENS)
+        res.append(tw.cache.decode(ids, q, scale=wl.scale))
+        tables = [tw.cache.block_table(s).tolist() for s in ids]
+        res[-1] = res[-1] + (tables,)
+    assert res[0][2] != res[1][2]
+    assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
+
+
+def test_logits_match_oracle():
+    wl = workloads.small("bf16", lens=LENS, seed=61)
+    nb = sum((L + 15) // 16 for L in LENS)
+    tw = Twin(wl, nb, len(LENS), 160, seed=4)
+    ids = fill_sequences(tw, LENS)
+    q = workloads.queries(wl)
+    stride = max(LENS)
+    for mask, S, W in (("full", 0, 0), ("sink_window", 4, 300)):
+        logits = torch.full((len(LENS), wl.n_kv_heads, stride, wl.group), float("nan"), device="cuda")
+        tw.cache.decode(ids, q.cuda(), scale=wl.scale, mask=mask, num_sinks=S, window=W, logits=logits,
+                        logits_stride=stride)
+        _, _, ref = tw.oracle_decode(ids, q, mask, S, W, want_logits=True, logits_stride=stride)
+        got = logits.permute(0, 1, 3, 2).reshape(len(LENS), wl.n_heads, stride).cpu().numpy()
+        kept = ~np.isnan(ref)
+        assert np.array_equal(kept, ~np.isnan(got))
+        assert np.abs(got[kept] - ref[kept]).max() <= 2e-3
+
+
+def test_empty_and_zero_length():
+    wl = workloads.small("bf16", lens=(0, 5, 40), seed=62)
+    tw = Twin(wl, 8, 3, 8, seed=1)
+    ids = fill_sequences(tw, wl.lens)
+    q = workloads.queries(wl)
+    out, lse = tw.cache.decode(ids, q.cuda(), scale=wl.scale)
+    ref, ref_lse, _ = tw.oracle_decode(ids, q)
+    assert max_err(out, ref) <= TOL["bf16"] and lse_err(lse, ref_lse) <= 2e-3
+    assert torch.isneginf(lse[0]).all() and (out[0] == 0).all()
+    # sink + window with nothing kept
+    out, lse = tw.cache.decode(ids, q.cuda(), scale=wl.scale, mask="sink_window", num_sinks=0, window=0)
+    assert (out[1:] == 0).all() and torch.isneginf(lse[1:]).all()
+
+
+# --------------------------------------------------------------------------
+# copy-on-write and append bit-exactness
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_fork_append_cow(kv):
+    wl = workloads.small(kv, lens=(40, 64, 77), seed=70)
+    tw = Twin(wl, 64, 8, 16, seed=17)
+    ids = fill_sequences(tw, wl.lens)
+    kids = [tw.fork(s) for s in ids]
+    batch = [x for pair in zip(ids, kids) for x in pair]
+    for step in range(20):
+        k, v = workloads.new_tokens(wl, len(batch), step)
+        _, cow = tw.append(batch, k, v)
+        if step == 0:
+            # the parent of each pair with a partial, shared last block copies it
+            assert len(cow) == sum(1 for L in wl.lens if L % 16)
+    assert tw.cache.stats()["cow_copies"] == sum(1 for L in wl.lens if L % 16)
+    for s in batch:
+        assert np.array_equal(tw.cache.block_table(s), tw.alloc.table(s))
+    _pool_bytes_equal(tw, batch)
+    q = workloads.queries(wl, len(batch))
+    out, lse = tw.cache.decode(batch, q.cuda(), scale=wl.scale)
+    ref, ref_lse, _ = tw.oracle_decode(batch, q)
+    assert max_err(out, ref) <= TOL[kv] and lse_err(lse, ref_lse) <= 2e-3
+
+
+def test_evicted_block_in_keep_set_is_rejected():
+    wl = workloads.small("bf16", lens=(300,), seed=71)
+    tw = Twin(wl, 32, 2, 32, seed=3)
+    ids = fill_sequences(tw, wl.lens)
+    tw.evict(ids[0], 4, 64)
+    q = workloads.queries(wl).cuda()
+    with pytest.raises(Exception) as e:
+        tw.cache.decode(ids, q, scale=wl.scale)
+    assert getattr(e.value, "status", None) == 1
+    out, lse = tw.cache.decode(ids, q, scale=wl.scale, mask="sink_window", num_sinks=4, window=64)
+    ref, ref_lse, _ = tw.oracle_decode(ids, workloads.queries(wl), "sink_window", 4, 64)
+    assert max_err(out, ref) <= TOL["bf16"]
+
+
+def test_workspace_too_small_is_rejected():
+    wl = workloads.small("bf16", lens=(3000, 3000), seed=72)
+    tw = Twin(wl, 400, 2, 200, seed=3)
+    ids = fill_sequences(tw, wl.lens)
+    q = workloads.queries(wl).cuda()
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(Exception) as e:
+        tw.cache.decode(ids, q, scale=wl.scale, num_splits=8, workspace=ws)
+    assert getattr(e.value, "status", None) == 9
+
+
+# --------------------------------------------------------------------------
+# H2O select on its own: bit-exact keep-sets on given score arrays
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("budget,recent", [(2048, 512), (64, 0), (100, 100), (37, 5)])
+def test_h2o_select_bit_exact(budget, recent):
+    lens = [0, 1, 50, budget, budget + 1, 3000, 20000, 131072]
+    stride = max(lens)
+    acc = workloads.h2o_scores_input(len(lens), stride, seed=budget + recent)
+    wl = workloads.small("bf16", lens=(1,))
+    cache = Twin(wl, 4, 1, 4).cache
+    keep = torch.full((len(lens), budget), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros(len(lens), dtype=torch.int32, device="cuda")
+    cache.h2o_select(lens, acc.cuda(), stride, budget, recent, keep, budget, cnt)
+    cache.sync_status()
+    keep, cnt = keep.cpu().numpy(), cnt.cpu().numpy()
+    for b, L in enumerate(lens):
+        ref = oracle.h2o_select(L, budget, recent, acc[b, :L].double().numpy())
+        assert cnt[b] == ref.size
+        assert np.array_equal(keep[b, : cnt[b]], ref), (b, L)
