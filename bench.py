@@ -1,0 +1,529 @@
+"""Benchmark: paged decode attention on GB300 (one layer, one decode step).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl pkv|reference]
+
+A step is one pass of the hot path over one batch: the allocator places one
+new token per sequence and the append kernel scatters its K/V (plus the
+copy-on-write copies when a shared block is written), then decode attention
+runs over every sequence's full context (decode kernel + log-sum-exp combine;
+H2O score and keep-set selection too on the streaming workload).  After each
+step the appended token is rolled back on the host (the block table is
+truncated), so every timed step sees the same context lengths.
+
+Metric: algorithmic KV bytes read per second (each kept token's K and V bytes
+per (sequence, kv head) once, plus FP8 scales) and decode tokens per second
+(sequences / step time).  Inputs stay resident in HBM; the KV pool of the
+default workload (~1.1 GB) is far larger than L2, so no flush is needed.
+
+With --gpus N under torchrun every rank runs its own replica of the workload
+on its own GPU (no collective on the data path); the line reports the sum
+over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "paged decode KV GB/s (frac of HBM peak) and tokens/s, 1×GB300"
+FALLBACK_HBM_GBS = 6800.0
+BYTES = {"fp32": 4, "bf16": 2, "fp8": 1}
+
+
+# --------------------------------------------------------------------------
+# workload setup on the device
+# --------------------------------------------------------------------------
+
+def _kv_bytes_per_token(wl) -> int:
+    b = 2 * wl.n_kv_heads * wl.head_dim * BYTES[wl.kv_dtype]
+    if wl.kv_dtype == "fp8":
+        b += 2 * wl.n_kv_heads * 4  # per-token K and V scales
+    return b
+
+
+def _kept(L, wl) -> int:
+    if wl.mask == "sliding":
+        return min(L, wl.window + 1)
+    if wl.mask == "sink_window" and L > wl.num_sinks + wl.window:
+        return wl.num_sinks + wl.window
+    return L
+
+
+class Setup:
+    """Pool + sequences of one workload on one GPU, filled from the seeded
+    generator through the library's own append path."""
+
+    def __init__(self, wl, dev, headroom_blocks: int | None = None):
+        from paged_kv_cache_282_gb300 import PagedKVCache
+        self.wl, self.dev = wl, dev
+        self.extra = {}
+        name = wl.name
+        if name == "prefix_append":
+            self._setup_prefix(PagedKVCache)
+        elif name == "streaming_h2o":
+            self._setup_streaming(PagedKVCache)
+        else:
+            lens = list(wl.lens)
+            need = sum((L + 15) // 16 for L in lens)
+            hb = headroom_blocks if headroom_blocks is not None else len(lens) + 8
+            maxb = max((L + 15) // 16 for L in lens) + 4
+            self.cache = PagedKVCache(need + hb, wl.n_heads, wl.n_kv_heads, wl.head_dim, len(lens), maxb,
+                                      kv_dtype=wl.kv_dtype, alloc_seed=wl.seed, device=dev)
+            self.ids = []
+            for b, L in enumerate(lens):
+                s = self.cache.seq_add()
+                self.ids.append(s)
+                for t0 in range(0, L, 16384):
+                    n = min(16384, L - t0)
+                    k, v = workloads.kv_rows(wl, b, t0, n)
+                    self.cache.append([s], k[None].to(dev), v[None].to(dev))
+        torch.cuda.synchronize(dev)
+        self.lens = [self.cache.seq_len(s) for s in self.ids]
+
+    def _setup_prefix(self, PagedKVCache):
+        wl = self.wl
+        ex = wl.extra
+        groups, ppg, prefix = ex["groups"], ex["parents_per_group"], ex["prefix"]
+        need = groups * (prefix // 16) + sum((s + 15) // 16 + 1 for s in ex["suffix"]) * 2 + 64
+        maxb = max((L + 15) // 16 for L in wl.lens) + 4
+        n_seqs = 2 * groups * ppg + groups
+        self.cache = c = PagedKVCache(need, wl.n_heads, wl.n_kv_heads, wl.head_dim, n_seqs, maxb,
+                                      kv_dtype=wl.kv_dtype, alloc_seed=wl.seed, device=self.dev)
+        parents = []
+        for gi in range(groups):
+            holder = c.seq_add()
+            k, v = workloads.kv_rows(wl, 10_000 + gi, 0, prefix)
+            c.append([holder], k[None].to(self.dev), v[None].to(self.dev))
+            kids = [c.seq_fork(holder) for _ in range(ppg)]
+            c.seq_free(holder)
+            for j, s in enumerate(kids):
+                pidx = gi * ppg + j
+                k, v = workloads.kv_rows(wl, pidx, prefix, ex["suffix"][pidx])
+                c.append([s], k[None].to(self.dev), v[None].to(self.dev))
+            parents += kids
+        self.ids = sorted(parents + [c.seq_fork(p) for p in parents])
+
+    def _setup_streaming(self, PagedKVCache):
+        """Sequences of logical length L hold only the blocks that intersect
+        the sink + window keep-set: the middle is appended as zero filler in
+        chunks and evicted as it falls out of the window."""
+        wl = self.wl
+        S, W = wl.num_sinks, wl.window
+        chunk = 4096
+        per_seq = 1 + (W + 15) // 16 + 2 + chunk // 16 + 2
+        maxb = max((L + 15) // 16 for L in wl.lens) + 4
+        self.cache = c = PagedKVCache(len(wl.lens) * per_seq + 64, wl.n_heads, wl.n_kv_heads, wl.head_dim,
+                                      len(wl.lens), maxb, kv_dtype=wl.kv_dtype, alloc_seed=wl.seed,
+                                      device=self.dev)
+        zeros = torch.zeros((1, chunk, wl.n_kv_heads, wl.head_dim), dtype=torch.bfloat16, device=self.dev)
+        self.ids = []
+        for b, L in enumerate(wl.lens):
+            s = c.seq_add()
+            self.ids.append(s)
+            # first position of the first block that intersects the window
+            tail = (L - W) // 16 * 16 if L > S + W else 0
+            if tail < 32:  # the window reaches block 0 or 1: everything is real
+                k, v = workloads.kv_rows(wl, b, 0, L)
+                c.append([s], k[None].to(self.dev), v[None].to(self.dev))
+                continue
+            k, v = workloads.kv_rows(wl, b, 0, 16)  # block 0 holds the sinks
+            c.append([s], k[None].to(self.dev), v[None].to(self.dev))
+            pos = 16
+            while pos < tail:
+                n = min(chunk, tail - pos)
+                c.append([s], zeros[:, :n], zeros[:, :n])
+                pos += n
+                c.seq_evict(s, S, W)
+            k, v = workloads.kv_rows(wl, b, tail, L - tail)
+            c.append([s], k[None].to(self.dev), v[None].to(self.dev))
+            c.seq_evict(s, S, W)
+
+    def algorithmic_bytes(self, lens=None) -> int:
+        lens = self.lens if lens is None else lens
+        return sum(_kept(L, self.wl) for L in lens) * _kv_bytes_per_token(self.wl)
+
+
+# --------------------------------------------------------------------------
+# one step
+# --------------------------------------------------------------------------
+
+class Stepper:
+    def __init__(self, setup: Setup, num_splits: int):
+        wl, dev = setup.wl, setup.dev
+        self.s, self.wl, self.dev = setup, wl, dev
+        self.cache = setup.cache
+        self.ids = setup.ids
+        n = len(self.ids)
+        self.num_splits = num_splits
+        self.q = workloads.queries(wl, n).to(dev)
+        k, v = workloads.new_tokens(wl, n, 0)
+        self.k_new, self.v_new = k.to(dev), v.to(dev)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty((n, wl.n_heads), dtype=torch.float32, device=dev)
+        self.ws = self.cache.workspace(n, num_splits)
+        self.h2o = wl.budget > 0
+        if self.h2o:
+            self.stride = max(setup.lens) + 1
+            self.logits = torch.zeros((n, wl.n_kv_heads, self.stride, wl.group), dtype=torch.float32, device=dev)
+            self.acc = torch.zeros((n, self.stride), dtype=torch.float32, device=dev)
+            self.keep = torch.zeros((n, wl.budget), dtype=torch.int32, device=dev)
+            self.keep_n = torch.zeros(n, dtype=torch.int32, device=dev)
+
+    def step(self, q=None, k_new=None, v_new=None, out=None):
+        c, wl = self.cache, self.wl
+        c.append(self.ids, self.k_new if k_new is None else k_new, self.v_new if v_new is None else v_new)
+        o = self.out if out is None else out
+        if self.h2o:
+            c.decode(self.ids, self.q if q is None else q, scale=wl.scale, mask=wl.mask, num_sinks=wl.num_sinks,
+                     window=wl.window, num_splits=self.num_splits, out=o, lse=self.lse, logits=self.logits,
+                     logits_stride=self.stride, workspace=self.ws)
+            c.h2o_scores(self.ids, self.logits, self.stride, self.lse, self.acc, self.stride, mask=wl.mask,
+                         num_sinks=wl.num_sinks, window=wl.window)
+            lens = [L + 1 for L in self.s.lens]
+            c.h2o_select(lens, self.acc, self.stride, wl.budget, wl.recent, self.keep, wl.budget, self.keep_n)
+        else:
+            c.decode(self.ids, self.q if q is None else q, scale=wl.scale, mask=wl.mask, num_sinks=wl.num_sinks,
+                     window=wl.window, num_splits=self.num_splits, out=o, lse=self.lse, workspace=self.ws)
+        for s, L in zip(self.ids, self.s.lens):  # roll the appended token back (host only)
+            c.seq_truncate(s, L)
+
+
+# --------------------------------------------------------------------------
+# clocks
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [r for (t, r) in self.samples if t0 <= t <= t1] or [r for (_, r) in self.samples[-3:]]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[4:8]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------
+# helpers
+# --------------------------------------------------------------------------
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic(kernel_file: str, workload: str):
+    """DRAM bytes per launch recorded from an ncu capture in profiles/, valid
+    only while the kernel source is unchanged (sha256 recorded beside it)."""
+    path = os.path.join(ROOT, "profiles", f"decode_tc_{workload}.md")
+    src = os.path.join(ROOT, "paged_kv_cache_282_gb300", "csrc", kernel_file)
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+        m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+        if m_sha and m_tr and m_sha.group(1) == sha:
+            return float(m_tr.group(1))
+    except Exception:
+        pass
+    return None
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(x: float, ws: int, dev) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------
+# CPU baseline: the oracle, as it stands, on a bounded sample
+# --------------------------------------------------------------------------
+
+def oracle_baseline(wl, n_sample: int, repeats: int = 1):
+    import oracle
+    lens = list(wl.lens)[:n_sample]
+    nb = sum((L + 15) // 16 for L in lens)
+    kvd = {"fp32": oracle.KV_FP32, "bf16": oracle.KV_BF16, "fp8": oracle.KV_FP8}[wl.kv_dtype]
+    alloc = oracle.OracleAllocator(nb, len(lens), max((L + 15) // 16 for L in lens) + 1, seed=wl.seed)
+    pool = oracle.OraclePool(nb, wl.n_kv_heads, wl.head_dim, kvd)
+    ids = []
+    for b, L in enumerate(lens):
+        s = alloc.seq_add()
+        ids.append(s)
+        k, v = workloads.kv_rows(wl, b, 0, L)
+        slots, _ = alloc.append([s], L)
+        pool.write(slots, workloads.as_bits(k), workloads.as_bits(v))
+    q = workloads.as_bits(workloads.queries(wl, len(lens)))
+    tables = alloc.tables_matrix(ids)
+    qdt = oracle.KV_FP32 if wl.kv_dtype == "fp32" else oracle.KV_BF16
+    masks = {"full": oracle.MASK_FULL, "sliding": oracle.MASK_SLIDING, "sink_window": oracle.MASK_SINK_WINDOW}
+    cores = os.cpu_count() or 1
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        oracle.decode(pool, tables, lens, q, qdt, wl.n_heads, wl.scale, masks[wl.mask], wl.num_sinks, wl.window,
+                      n_threads=cores)
+        times.append(time.perf_counter() - t0)
+    t = min(times)
+    byts = sum(_kept(L, wl) for L in lens) * _kv_bytes_per_token(wl)
+    return {"value": byts / t / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(lens)} of {wl.batch} sequences of {wl.name} ({sum(lens)} tokens), fp64 oracle decode, "
+                      f"{t:.2f} s", "seconds": t, "tokens_per_s": len(lens) / t}
+
+
+# --------------------------------------------------------------------------
+# main
+# --------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--workload", default="llama3_8b_b64", choices=sorted(workloads.ALL))
+    ap.add_argument("--num-splits", type=int, default=None)
+    ap.add_argument("--cpu-sample", type=int, default=16, help="sequences in the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--profile-steps", type=int, default=0, help="run N untimed steps and exit (for ncu)")
+    args = ap.parse_args()
+
+    wl = workloads.ALL[args.workload]()
+    splits = wl.num_splits if args.num_splits is None else args.num_splits
+    ws, rank, local = dist_info()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        return run_reference(args, wl)
+
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import paged_kv_cache_282_gb300 as pkv
+    pkv.load()
+
+    setup = Setup(wl, dev)
+    st = Stepper(setup, splits)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        st.step()
+    setup.cache.sync_status()
+    if args.profile_steps:
+        for _ in range(args.profile_steps):
+            st.step()
+        torch.cuda.synchronize(dev)
+        print(json.dumps({"profile_steps": args.profile_steps, "workload": wl.name}))
+        return
+
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    time.sleep(0.3)
+    # ---- device-resident timed region (kernel timing events on) ----
+    setup.cache.timing_enable(True)
+    setup.cache.timing_read()
+    launches0 = setup.cache.launch_count()
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        st.step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    barrier(ws)
+    ms = e0.elapsed_time(e1)
+    launches = setup.cache.launch_count() - launches0
+    ktimes = setup.cache.timing_read()
+    setup.cache.timing_enable(False)
+    setup.cache.sync_status()
+    ms_max = reduce_max(ms, ws, dev)
+
+    # ---- end to end through host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        n = len(setup.ids)
+        q_h = st.q.cpu().pin_memory()
+        k_h, v_h = st.k_new.cpu().pin_memory(), st.v_new.cpu().pin_memory()
+        out_h = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+        q_d, k_d, v_d = torch.empty_like(st.q), torch.empty_like(st.k_new), torch.empty_like(st.v_new)
+        e2e_steps = max(10, args.steps // 4)
+        for _ in range(3):
+            q_d.copy_(q_h, non_blocking=True)
+            k_d.copy_(k_h, non_blocking=True)
+            v_d.copy_(v_h, non_blocking=True)
+            st.step(q=q_d, k_new=k_d, v_new=v_d)
+            out_h.copy_(st.out, non_blocking=True)
+        barrier(ws)
+        torch.cuda.synchronize(dev)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(e2e_steps):
+            q_d.copy_(q_h, non_blocking=True)
+            k_d.copy_(k_h, non_blocking=True)
+            v_d.copy_(v_h, non_blocking=True)
+            st.step(q=q_d, k_new=k_d, v_new=v_d)
+            out_h.copy_(st.out, non_blocking=True)
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(ws)
+        e2e_ms = reduce_max(a0.elapsed_time(a1), ws, dev) / e2e_steps
+        bi = (q_h.numel() * q_h.element_size() + k_h.numel() * k_h.element_size() +
+              v_h.numel() * v_h.element_size())
+        bo = out_h.numel() * out_h.element_size()
+        step_bytes = setup.algorithmic_bytes([L + 1 for L in setup.lens])
+        e2e = {"value": round(ws * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": round(e2e_ms, 5),
+               "tokens_per_s": round(ws * n / (e2e_ms * 1e-3), 1)}
+
+    if clocks:
+        clocks.stop()
+    if rank != 0:
+        return
+
+    lens_step = [L + 1 for L in setup.lens]
+    step_bytes = setup.algorithmic_bytes(lens_step)
+    ms_step = ms_max / args.steps
+    value = ws * step_bytes / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+    dec_ms, dec_n = ktimes["decode"]
+    dec_avg = dec_ms / max(dec_n, 1)
+    achieved = step_bytes / (dec_avg * 1e-3) / 1e9 if dec_n else None
+    traffic = profiled_traffic("decode_tc.cu", wl.name)
+    kernel_share = {k: round(v[0] / max(sum(x[0] for x in ktimes.values()), 1e-9), 4) for k, v in ktimes.items()
+                    if v[1]}
+    cpu = None
+    if not args.no_cpu_baseline and ws == 1:
+        cpu = oracle_baseline(wl, min(args.cpu_sample, wl.batch))
+    clk = clocks.summary(t_wall0, t_wall1) if clocks else None
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": wl.kv_dtype,
+        "data": "synthetic (seeded N(0,1) K/V/Q; seeded uniform lengths)",
+        "config": {"workload": wl.name, "batch": len(setup.ids), "n_heads": wl.n_heads,
+                   "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim, "kv_dtype": wl.kv_dtype,
+                   "mask": wl.mask, "num_splits": splits, "context_tokens": sum(lens_step),
+                   "kv_bytes_per_step": step_bytes, "l2": "KV pool larger than L2 (no flush needed)",
+                   "parallelism": f"replicas x{ws}"},
+        "tokens_per_s": round(ws * len(setup.ids) / (ms_step * 1e-3), 1),
+        "frac_of_hbm_peak": round(value / ws / peak, 4),
+        "roofline": {"bound": "hbm", "kernel": "decode_tc_kernel", "achieved": round(achieved, 2) if achieved else None,
+                     "peak": peak, "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4) if achieved else None, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": step_bytes, "avg_launch_ms": round(dec_avg, 5)},
+        "kernel_time_share": kernel_share,
+        "gpu_launches": launches,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "clocks": clk,
+    }
+    print(json.dumps(line))
+
+
+def run_reference(args, wl):
+    """The CPU oracle as it stands, timed on this machine's cores, each step a
+    bounded sample of the workload."""
+    n = min(args.cpu_sample, wl.batch)
+    res = [oracle_baseline(wl, n) for _ in range(max(1, args.warmup and 1))]  # warm-up (page in, threads)
+    times = []
+    for _ in range(args.steps):
+        r = oracle_baseline(wl, n)
+        times.append(r["seconds"])
+    t = sum(times) / len(times)
+    lens = list(wl.lens)[:n]
+    byts = sum(_kept(L, wl) for L in lens) * _kv_bytes_per_token(wl)
+    value = byts / t / 1e9
+    cores = os.cpu_count() or 1
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.batch, "sample_sequences": n},
+        "tokens_per_s": round(n / t, 3),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": res[0]["sample"]},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+if __name__ == "__main__":
+    main()

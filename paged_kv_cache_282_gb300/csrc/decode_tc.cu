@@ -416,8 +416,29 @@ __global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const
       }
       const float a0 = k0 ? s0 * sl2 : -INFINITY, a1 = k0 ? s1 * sl2 : -INFINITY;
       const float a2 = k1 ? s2 * sl2 : -INFINITY, a3 = k1 ? s3 * sl2 : -INFINITY;
-      // b = a + log2(v scale): the exponent of the weight that multiplies V
-      const float e0 = a0 + lv_r, e1 = a1 + lv_r, e2 = a2 + lv_r8, e3 = a3 + lv_r8;
+      // a + log2(v scale): the exponent of the weight that multiplies V.  Slots
+      // of masked tokens may hold anything (unwritten memory), so neither their
+      // scale nor their V row may reach the arithmetic.
+      const float e0 = k0 ? a0 + lv_r : -INFINITY, e1 = k0 ? a1 + lv_r : -INFINITY;
+      const float e2 = k1 ? a2 + lv_r8 : -INFINITY, e3 = k1 ? a3 + lv_r8 : -INFINITY;
+      if (__ballot_sync(kFull, !(k0 && k1))) {
+        // zero the V rows of masked tokens in this warp's stage (0 * NaN = NaN)
+        constexpr int kRowBytes = KV == 1 ? 256 : 128;
+        constexpr int kChunksPerRow = kRowBytes / 16;
+        constexpr int kRowsPerPass = 32 / kChunksPerRow;
+        const int ch = lane % kChunksPerRow;
+#pragma unroll
+        for (int t0 = 0; t0 < 16; t0 += kRowsPerPass) {
+          const int t = t0 + lane / kChunksPerRow;
+          if (!kept(lb * kBlock + t, L, p.mask_mode, p.num_sinks, p.window)) {
+            const uint32_t addr = vb + (uint32_t)((ch >> 3) * 2048 + t * 128 + (ch & 7) * 16);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
+          }
+        }
+        // order these generic-proxy writes before the TMA refill of this stage
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+      }
       float bm0 = fmaxf(e0, e2), bm1 = fmaxf(e1, e3);
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) {

@@ -379,9 +379,13 @@ cudaError_t launch_cow_copy(const int32_t* pairs, int n_pairs, void* k_pool, voi
                             float* v_scale, size_t block_bytes, size_t scale_floats, cudaStream_t st) {
   if (n_pairs <= 0) return cudaSuccess;
   const int64_t chunks = (int64_t)(block_bytes / 16);
-  dim3 grid((unsigned)std::min<int64_t>((chunks + 255) / 256, 64), (unsigned)n_pairs);
-  cow_copy_kernel<<<grid, 256, 0, st>>>(pairs, (uint4*)k_pool, (uint4*)v_pool, chunks, scale_floats ? k_scale : nullptr,
-                                        scale_floats ? v_scale : nullptr, (int64_t)scale_floats);
+  for (int first = 0; first < n_pairs; first += 65535) {
+    const int n = std::min(65535, n_pairs - first);
+    dim3 grid((unsigned)std::min<int64_t>((chunks + 255) / 256, 64), (unsigned)n);
+    cow_copy_kernel<<<grid, 256, 0, st>>>(pairs + 2 * first, (uint4*)k_pool, (uint4*)v_pool, chunks,
+                                          scale_floats ? k_scale : nullptr, scale_floats ? v_scale : nullptr,
+                                          (int64_t)scale_floats);
+  }
   return cudaGetLastError();
 }
 

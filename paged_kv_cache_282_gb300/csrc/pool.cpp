@@ -372,23 +372,54 @@ pkv_status make_tensor_map(CUtensorMap* m, void* base, const pkv_pool_config& c)
 pkv_status flush_pending(pkv_pool* p, cudaStream_t st) {
   HostAllocator& A = p->alloc;
   if (A.pending_cow.empty() && A.pending_patch.empty()) return PKV_OK;
-  const size_t ncow = A.pending_cow.size() / 2, npatch = A.pending_patch.size();
+  // Table patches: several changes to one entry collapse to the last one (the
+  // patch kernel applies its list in parallel).
+  std::vector<TablePatch> patches;
+  {
+    std::unordered_map<int32_t, size_t> last;
+    last.reserve(A.pending_patch.size() * 2);
+    for (size_t i = 0; i < A.pending_patch.size(); ++i) last[A.pending_patch[i].index] = i;
+    patches.reserve(last.size());
+    for (size_t i = 0; i < A.pending_patch.size(); ++i)
+      if (last[A.pending_patch[i].index] == i) patches.push_back(A.pending_patch[i]);
+  }
+  // COW copies: a copy whose source or destination is the destination of an
+  // earlier copy in the list must run after it, so the list is cut into waves
+  // of independent copies that run in order.
+  std::vector<size_t> wave_start{0};
+  {
+    std::set<int32_t> dsts;
+    for (size_t k = 0; k < A.pending_cow.size() / 2; ++k) {
+      const int32_t src = A.pending_cow[2 * k], dst = A.pending_cow[2 * k + 1];
+      if (dsts.count(src) || dsts.count(dst)) {
+        wave_start.push_back(k);
+        dsts.clear();
+      }
+      dsts.insert(dst);
+    }
+  }
+  const size_t ncow = A.pending_cow.size() / 2, npatch = patches.size();
+  wave_start.push_back(ncow);
   const size_t cow_bytes = ncow * 2 * sizeof(int32_t), patch_off = (cow_bytes + 255) & ~size_t(255);
   const size_t bytes = patch_off + npatch * sizeof(TablePatch);
   StagingSlot* s;
   if (pkv_status r = p->staging.acquire(bytes, &s)) return r;
   if (ncow) memcpy(s->host, A.pending_cow.data(), cow_bytes);
-  if (npatch) memcpy(s->host + patch_off, A.pending_patch.data(), npatch * sizeof(TablePatch));
+  if (npatch) memcpy(s->host + patch_off, patches.data(), npatch * sizeof(TablePatch));
   if (pkv_status r = Staging::upload(s, bytes, st)) return r;
   const auto& c = p->cfg;
   if (ncow) {
     const size_t blk_bytes = (size_t)c.n_kv_heads * kBlock * c.head_dim * elem_bytes(c.kv_dtype);
     const size_t scl = c.kv_dtype == PKV_KV_FP8_E4M3 ? (size_t)c.n_kv_heads * kBlock : 0;
-    if (pkv_status r = launch(p, PKV_KERNEL_COW_COPY, st, [&] {
-          return launch_cow_copy((const int32_t*)s->dev, (int)ncow, p->buf.k_pool, p->buf.v_pool,
-                                 p->buf.k_scale, p->buf.v_scale, blk_bytes, scl, st);
-        }))
-      return r;
+    for (size_t w = 0; w + 1 < wave_start.size(); ++w) {
+      const size_t k0 = wave_start[w], k1 = wave_start[w + 1];
+      if (k1 == k0) continue;
+      if (pkv_status r = launch(p, PKV_KERNEL_COW_COPY, st, [&] {
+            return launch_cow_copy((const int32_t*)s->dev + 2 * k0, (int)(k1 - k0), p->buf.k_pool, p->buf.v_pool,
+                                   p->buf.k_scale, p->buf.v_scale, blk_bytes, scl, st);
+          }))
+        return r;
+    }
   }
   if (npatch) {
     if (pkv_status r = launch(p, PKV_KERNEL_TABLE_PATCH, st, [&] {

@@ -97,5 +97,6 @@ def max_err(a: torch.Tensor, b: np.ndarray) -> float:
 def lse_err(a: torch.Tensor, b: np.ndarray) -> float:
     x = a.cpu().numpy().astype(np.float64)
     both_inf = np.isneginf(x) & np.isneginf(b)
-    d = np.where(both_inf, 0.0, np.abs(x - b))
+    with np.errstate(invalid="ignore"):
+        d = np.where(both_inf, 0.0, np.abs(x - b))
     return float(d.max()) if d.size else 0.0

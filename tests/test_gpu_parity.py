@@ -230,3 +230,40 @@ def test_h2o_select_bit_exact(budget, recent):
         ref = oracle.h2o_select(L, budget, recent, acc[b, :L].double().numpy())
         assert cnt[b] == ref.size
         assert np.array_equal(keep[b, : cnt[b]], ref), (b, L)
+
+
+def test_patches_and_cow_chains_in_one_flush():
+    """Several host-side changes queued before one device call: a table entry
+    set to -1 and back (truncate + re-append), and a copy-on-write whose source
+    is the destination of an earlier queued copy."""
+    wl = workloads.small("bf16", lens=(32, 20), seed=73)
+    tw = Twin(wl, 32, 8, 8, seed=5)
+    a, b = fill_sequences(tw, wl.lens)
+    k, v = workloads.new_tokens(wl, 1, 0)
+    for _ in range(3):  # truncate + re-append the block-opening token
+        tw.append([a], k, v)
+        tw.truncate(a, 32)
+    tw.append([a], k, v)
+    # chain: b's partial last block is shared, copied; the copy is shared and
+    # copied again, all before any device call
+    c1 = tw.fork(b)
+    s1, cow1 = tw.cache.reserve_slots([b], 1)
+    o1, ocow1 = tw.alloc.append([b], 1)
+    c2 = tw.fork(b)
+    s2, cow2 = tw.cache.reserve_slots([b], 1)
+    o2, ocow2 = tw.alloc.append([b], 1)
+    assert np.array_equal(cow1, ocow1) and np.array_equal(cow2, ocow2) and cow2[0, 0] == cow1[0, 1]
+    for src, dst in list(ocow1) + list(ocow2):
+        tw.pool.copy_block(int(src), int(dst))
+    q = workloads.queries(wl, 1)
+    out, lse = tw.cache.decode([a], q.cuda(), scale=wl.scale)  # flushes everything queued
+    tw.cache.sync_status()
+    ref, ref_lse, _ = tw.oracle_decode([a], q)
+    assert max_err(out, ref) <= TOL["bf16"]
+    assert np.array_equal(tw.cache.block_table(a), tw.alloc.table(a))
+    for s in (a, c1, c2):
+        assert np.array_equal(tw.cache.block_table(s), tw.alloc.table(s))
+    dst = int(cow2[0, 1])
+    # b's last block holds tokens 16..19 in slots 0..3 (the rest is unwritten)
+    d = tw.cache.k_pool.view(torch.int16)[dst, :, :4].cpu().numpy().view(np.uint16)
+    assert np.array_equal(d, tw.pool.k[dst, :, :4])
