@@ -216,6 +216,30 @@ pkv_status pkv_decode_attn(pkv_pool* pool, void* stream, int32_t n_seqs, const i
                            float* logits, int64_t logits_stride, void* workspace,
                            size_t workspace_bytes);
 
+/* Same computation and arguments as pkv_decode_attn, minus the workspace: the
+ * split-KV scratch lives in a fixed 32 MiB array compiled into the library
+ * (2 MiB for the per-call plan and queued block-table / copy-on-write updates,
+ * 30 MiB for partial records).  The pages describe nothing like it; it exists
+ * for callers that cannot allocate device memory on their own -- code running
+ * under a framework allocator that owns the whole device budget, or inside a
+ * latency-critical loop where cudaMalloc / cudaFree would synchronise the
+ * device.  It allocates no device or pinned memory (host-side planning uses
+ * ordinary heap memory) and copies its plan from pageable memory.
+ *   - bf16 and FP8 pools only (PKV_ERR_UNSUPPORTED for fp32); the pool's
+ *     device must be the current device.
+ *   - A call that needs more than the array holds fails with
+ *     PKV_ERR_WORKSPACE and a message giving both sizes; nothing is launched.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any
+ *     stream capture.
+ *   - Every device that runs this entry point keeps the 32 MiB until the
+ *     process exits.  All calls share the array: calls whose work overlaps on
+ *     the GPU (other streams, other pools on the same device) race on it. */
+pkv_status pkv_decode_attn_static(pkv_pool* pool, void* stream, int32_t n_seqs, const int32_t* seq_ids,
+                                  const void* q, float scale, int32_t mask_mode, int32_t num_sinks,
+                                  int32_t window, int32_t num_splits, void* out, float* lse, float* logits,
+                                  int64_t logits_stride);
+
 /* H2O score update ([LC] H2OEviction.update_scores): for each listed sequence
  * and each kept key j, acc[b][j] += (1/n_heads) * sum_h exp(s_hj - lse_h),
  * the attention weight summed over the single decode query and averaged over

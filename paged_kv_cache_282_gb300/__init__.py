@@ -199,6 +199,25 @@ class PagedKVCache:
             ws.data_ptr() if ws is not None else None, ws.numel() * ws.element_size() if ws is not None else 0))
         return out, lse
 
+    def decode_static(self, seq_ids, q, scale: float | None = None, mask: str = "full", num_sinks: int = 0,
+                      window: int = 0, num_splits: int = 0, out=None, lse=None, logits=None, logits_stride: int = 0,
+                      stream=None):
+        """pkv_decode_attn_static: decode whose scratch is the library's fixed
+        device array (no workspace argument); returns (out, lse)."""
+        import torch
+        ids = _i32_array(seq_ids)
+        if scale is None:
+            scale = 1.0 / math.sqrt(self.head_dim)
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty((ids.size, self.n_heads), dtype=torch.float32, device=q.device)
+        _abi.check(self.lib.pkv_decode_attn_static(
+            self._h, _stream_ptr(stream), ids.size, _ptr(ids), q.data_ptr(), float(scale), MASKS[mask], num_sinks,
+            window, num_splits, out.data_ptr(), lse.data_ptr(), logits.data_ptr() if logits is not None else None,
+            int(logits_stride)))
+        return out, lse
+
     def h2o_scores(self, seq_ids, logits, logits_stride: int, lse, acc, acc_stride: int, mask: str = "full",
                    num_sinks: int = 0, window: int = 0, stream=None) -> None:
         ids = _i32_array(seq_ids)

@@ -69,6 +69,8 @@ SIGNATURES = {
     "pkv_decode_workspace_size": [c_void_p, c_int32, c_int32, _P(c_size_t)],
     "pkv_decode_attn": [c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_float, c_int32, c_int32, c_int32,
                         c_int32, c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_size_t],
+    "pkv_decode_attn_static": [c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_float, c_int32, c_int32,
+                               c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_int64],
     "pkv_h2o_scores": [c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_int64, c_void_p, c_int32, c_int32,
                        c_int32, c_void_p, c_int64],
     "pkv_h2o_select": [c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_int64, c_int32, c_int32, c_void_p,

@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_objs")
 LIB = os.path.join(HERE, "libpkv.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["decode_tc.cu", "kernels.cu", "pool.cpp"]
+SOURCES = ["decode_tc.cu", "kernels.cu", "decode_static.cu", "pool.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

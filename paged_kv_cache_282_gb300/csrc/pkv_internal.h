@@ -124,3 +124,17 @@ cudaError_t launch_h2o_select(const SeqRow* rows, int n_seqs, const float* acc, 
                               int32_t* keep_count, cudaStream_t stream);
 
 }  // namespace pkv
+
+// ---- decode with caller-supplied device regions (no library allocation) ----
+struct pkv_pool;
+namespace pkv {
+// Sets the message pkv_last_error() returns on this thread.
+void set_error(const char* msg);
+// Runs the bf16 / FP8 decode of pkv_decode_attn, staging every host-built
+// array (queued copy-on-write pairs and table patches, the work plan) with
+// one pageable copy into `plan_dev` and keeping the split-KV partial records
+// in `partials_dev`.  Allocates no device or pinned memory.
+int decode_attn_into(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, const void* q, float scale,
+                     int32_t mode, int32_t S, int32_t W, int32_t num_splits, void* out, float* lse, float* logits,
+                     int64_t logits_stride, void* plan_dev, size_t plan_cap, void* partials_dev, size_t partials_cap);
+}  // namespace pkv

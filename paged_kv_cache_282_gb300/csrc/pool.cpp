@@ -40,6 +40,8 @@ static pkv_status fail(pkv_status s, const char* fmt, ...) {
   return s;
 }
 
+void pkv::set_error(const char* msg) { g_last_error = msg ? msg : ""; }
+
 #define PKV_CUDA(call)                                                                  \
   do {                                                                                  \
     cudaError_t e_ = (call);                                                            \
@@ -640,6 +642,144 @@ pkv_status check_keep_blocks_present(const pkv_pool* p, int32_t n, const int32_t
 }
 
 }  // namespace
+
+// ---------------------------------------------------------------------------
+// decode into caller-supplied device regions (used by the static-scratch
+// entry point); shares the planner and the launchers, allocates nothing
+// ---------------------------------------------------------------------------
+
+int pkv::decode_attn_into(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, const void* q, float scale,
+                          int32_t mode, int32_t S, int32_t W, int32_t num_splits, void* out, float* lse,
+                          float* logits, int64_t logits_stride, void* plan_dev, size_t plan_cap, void* partials_dev,
+                          size_t partials_cap) {
+  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  if (!p->device) return fail(PKV_ERR_NO_DEVICE, "host-only pool");
+  if (p->cfg.kv_dtype == PKV_KV_FP32) return fail(PKV_ERR_UNSUPPORTED, "static-scratch decode serves bf16 / fp8 pools");
+  {
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != p->device_id)
+      return fail(PKV_ERR_INVALID_ARG, "the pool's device (%d) is not the current device (%d)", p->device_id, cur);
+  }
+  if (pkv_status r = check_seq_list(p, n, ids)) return r;
+  if (!valid_mask(mode, S, W)) return fail(PKV_ERR_INVALID_ARG, "invalid mask %d (%d, %d)", mode, S, W);
+  if (num_splits < 0) return fail(PKV_ERR_INVALID_ARG, "num_splits < 0");
+  if (n > 0 && (!q || !out)) return fail(PKV_ERR_INVALID_ARG, "q / out is NULL");
+  HostAllocator& A = p->alloc;
+  int32_t maxlen = 0;
+  for (int32_t i = 0; i < n; ++i) maxlen = std::max(maxlen, A.len[ids[i]]);
+  if (logits && logits_stride < maxlen) return fail(PKV_ERR_INVALID_ARG, "logits_stride < max length");
+  if (pkv_status r = check_keep_blocks_present(p, n, ids, mode, S, W)) return r;
+  const auto& c = p->cfg;
+  cudaStream_t st = (cudaStream_t)stream;
+
+  // queued allocator effects: last value per table entry; copies in waves
+  std::vector<TablePatch> patches;
+  {
+    std::unordered_map<int32_t, size_t> last;
+    for (size_t i = 0; i < A.pending_patch.size(); ++i) last[A.pending_patch[i].index] = i;
+    for (size_t i = 0; i < A.pending_patch.size(); ++i)
+      if (last[A.pending_patch[i].index] == i) patches.push_back(A.pending_patch[i]);
+  }
+  const size_t ncow = A.pending_cow.size() / 2;
+  std::vector<size_t> waves{0};
+  {
+    std::set<int32_t> dsts;
+    for (size_t k = 0; k < ncow; ++k) {
+      if (dsts.count(A.pending_cow[2 * k]) || dsts.count(A.pending_cow[2 * k + 1])) {
+        waves.push_back(k);
+        dsts.clear();
+      }
+      dsts.insert(A.pending_cow[2 * k + 1]);
+    }
+    waves.push_back(ncow);
+  }
+  Plan plan;
+  if (n > 0) build_plan(p, n, ids, mode, S, W, num_splits, plan);
+  const size_t pf = (size_t)partial_floats(p->G, c.head_dim) * sizeof(float);
+  if ((size_t)plan.n_partials * pf > partials_cap)
+    return fail(PKV_ERR_WORKSPACE, "needs %zu bytes of partial records, the static scratch holds %zu",
+                (size_t)plan.n_partials * pf, partials_cap);
+
+  // one blob: [cow pairs][patches][warp_begin][pieces][combine]
+  auto up32 = [](size_t x) { return (x + 31) & ~size_t(31); };
+  const size_t cow_off = 0, patch_off = up32(ncow * 2 * sizeof(int32_t));
+  const size_t wb_off = up32(patch_off + patches.size() * sizeof(TablePatch));
+  const size_t pieces_off = up32(wb_off + plan.warp_begin.size() * sizeof(int32_t));
+  const size_t comb_off = pieces_off + plan.pieces.size() * sizeof(Piece);
+  const size_t bytes = comb_off + plan.combine.size() * sizeof(CombineItem);
+  if (bytes > plan_cap)
+    return fail(PKV_ERR_WORKSPACE, "needs %zu bytes of plan, the static scratch holds %zu", bytes, plan_cap);
+  std::vector<char> blob(bytes);
+  if (ncow) memcpy(blob.data() + cow_off, A.pending_cow.data(), ncow * 2 * sizeof(int32_t));
+  if (!patches.empty()) memcpy(blob.data() + patch_off, patches.data(), patches.size() * sizeof(TablePatch));
+  if (!plan.warp_begin.empty())
+    memcpy(blob.data() + wb_off, plan.warp_begin.data(), plan.warp_begin.size() * sizeof(int32_t));
+  if (!plan.pieces.empty()) memcpy(blob.data() + pieces_off, plan.pieces.data(), plan.pieces.size() * sizeof(Piece));
+  if (!plan.combine.empty())
+    memcpy(blob.data() + comb_off, plan.combine.data(), plan.combine.size() * sizeof(CombineItem));
+  char* dev = (char*)plan_dev;
+  if (bytes) PKV_CUDA(cudaMemcpyAsync(dev, blob.data(), bytes, cudaMemcpyHostToDevice, st));
+
+  if (ncow) {
+    const size_t blk_bytes = (size_t)c.n_kv_heads * kBlock * c.head_dim * elem_bytes(c.kv_dtype);
+    const size_t scl = c.kv_dtype == PKV_KV_FP8_E4M3 ? (size_t)c.n_kv_heads * kBlock : 0;
+    for (size_t w = 0; w + 1 < waves.size(); ++w) {
+      const size_t k0 = waves[w], k1 = waves[w + 1];
+      if (k1 == k0) continue;
+      if (pkv_status r = launch(p, PKV_KERNEL_COW_COPY, st, [&] {
+            return launch_cow_copy((const int32_t*)(dev + cow_off) + 2 * k0, (int)(k1 - k0), p->buf.k_pool,
+                                   p->buf.v_pool, p->buf.k_scale, p->buf.v_scale, blk_bytes, scl, st);
+          }))
+        return r;
+    }
+  }
+  if (!patches.empty()) {
+    if (pkv_status r = launch(p, PKV_KERNEL_TABLE_PATCH, st, [&] {
+          return launch_table_patch((const int32_t*)(dev + patch_off), (int)patches.size(), p->buf.block_tables, st);
+        }))
+      return r;
+  }
+  A.pending_cow.clear();
+  A.pending_patch.clear();
+  if (n == 0) return PKV_OK;
+  if (plan.total_warps > 0) {
+    DecodeTCParams prm;
+    prm.tmap_k = p->tmap_k;
+    prm.tmap_v = p->tmap_v;
+    prm.k_scale = p->buf.k_scale;
+    prm.v_scale = p->buf.v_scale;
+    prm.tables = p->buf.block_tables;
+    prm.max_blocks = c.max_blocks_per_seq;
+    prm.num_blocks = c.num_blocks;
+    prm.n_heads = c.n_heads;
+    prm.n_kv_heads = c.n_kv_heads;
+    prm.q = q;
+    prm.out = out;
+    prm.lse = lse;
+    prm.logits = logits;
+    prm.logits_stride = logits_stride;
+    prm.pieces = (const Piece*)(dev + pieces_off);
+    prm.warp_begin = (const int32_t*)(dev + wb_off);
+    prm.total_warps = plan.total_warps;
+    prm.partials = (float*)partials_dev;
+    prm.scale = scale;
+    prm.mask_mode = mode;
+    prm.num_sinks = S;
+    prm.window = W;
+    prm.status = p->buf.status;
+    const int ctas = ceil_div(plan.total_warps, p->tc_warps_per_cta);
+    if (pkv_status r = launch(p, PKV_KERNEL_DECODE, st, [&] { return launch_decode_tc(c.kv_dtype, p->G, prm, ctas, st); }))
+      return r;
+  }
+  if (!plan.combine.empty()) {
+    if (pkv_status r = launch(p, PKV_KERNEL_COMBINE, st, [&] {
+          return launch_combine((const CombineItem*)(dev + comb_off), (int)plan.combine.size(),
+                                (const float*)partials_dev, p->G, c.head_dim, c.n_heads, 1, out, lse, st);
+        }))
+      return r;
+  }
+  return PKV_OK;
+}
 
 // ---------------------------------------------------------------------------
 // C ABI
