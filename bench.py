@@ -158,6 +158,16 @@ class Setup:
         lens = self.lens if lens is None else lens
         return sum(_kept(L, self.wl) for L in lens) * _kv_bytes_per_token(self.wl)
 
+    def unique_bytes_per_step(self) -> int:
+        """KV bytes of distinct physical blocks the step reads (blocks shared
+        by several sequences count once), plus each sequence's new token."""
+        fill = {}
+        for s, L in zip(self.ids, self.lens):
+            for lb, blk in enumerate(self.cache.block_table(s)):
+                if blk >= 0:
+                    fill[int(blk)] = max(fill.get(int(blk), 0), min(16, L - 16 * lb))
+        return (sum(fill.values()) + len(self.ids)) * _kv_bytes_per_token(self.wl)
+
 
 # --------------------------------------------------------------------------
 # one step
@@ -200,8 +210,7 @@ class Stepper:
         else:
             c.decode(self.ids, self.q if q is None else q, scale=wl.scale, mask=wl.mask, num_sinks=wl.num_sinks,
                      window=wl.window, num_splits=self.num_splits, out=o, lse=self.lse, workspace=self.ws)
-        for s, L in zip(self.ids, self.s.lens):  # roll the appended token back (host only)
-            c.seq_truncate(s, L)
+        c.seq_truncate_many(self.ids, self.s.lens)  # roll the appended token back (host only)
 
 
 # --------------------------------------------------------------------------
@@ -379,8 +388,11 @@ def main():
         st.step()
     setup.cache.sync_status()
     if args.profile_steps:
+        torch.cuda.synchronize(dev)
+        torch.cuda.nvtx.range_push("profiled_steps")  # ncu --nvtx-include "profiled_steps/"
         for _ in range(args.profile_steps):
             st.step()
+        torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize(dev)
         print(json.dumps({"profile_steps": args.profile_steps, "workload": wl.name}))
         return
@@ -388,7 +400,7 @@ def main():
     clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     time.sleep(0.3)
     # ---- device-resident timed region (kernel timing events on) ----
-    setup.cache.timing_enable(True)
+    setup.cache.timing_enable(["decode"])
     setup.cache.timing_read()
     launches0 = setup.cache.launch_count()
     barrier(ws)
@@ -460,8 +472,8 @@ def main():
     dec_avg = dec_ms / max(dec_n, 1)
     achieved = step_bytes / (dec_avg * 1e-3) / 1e9 if dec_n else None
     traffic = profiled_traffic("decode_tc.cu", wl.name)
-    kernel_share = {k: round(v[0] / max(sum(x[0] for x in ktimes.values()), 1e-9), 4) for k, v in ktimes.items()
-                    if v[1]}
+    decode_share = round(dec_ms / max(ms, 1e-9), 4)
+    unique = setup.unique_bytes_per_step() if wl.name == "prefix_append" else None
     cpu = None
     if not args.no_cpu_baseline and ws == 1:
         cpu = oracle_baseline(wl, min(args.cpu_sample, wl.batch))
@@ -489,8 +501,11 @@ def main():
         "roofline": {"bound": "hbm", "kernel": "decode_tc_kernel", "achieved": round(achieved, 2) if achieved else None,
                      "peak": peak, "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s",
                      "frac": round(achieved / peak, 4) if achieved else None, "traffic": traffic,
+                     "achieved_unique": round(unique / (dec_avg * 1e-3) / 1e9, 2) if unique and dec_n else None,
                      "algorithmic_bytes_per_launch": step_bytes, "avg_launch_ms": round(dec_avg, 5)},
-        "kernel_time_share": kernel_share,
+        "decode_share_of_step": decode_share,
+        "unique_kv_bytes_per_step": unique,
+        "value_unique_gbs": round(ws * unique / (ms_step * 1e-3) / 1e9, 2) if unique else None,
         "gpu_launches": launches,
         "e2e": e2e,
         "cpu_baseline": cpu,

@@ -152,6 +152,9 @@ pkv_status pkv_seq_free(pkv_pool* pool, int32_t seq);
 /* Shortens a sequence to new_len tokens, dropping blocks past it (ascending).
  * Refused if the new last block is partial and was evicted. */
 pkv_status pkv_seq_truncate(pkv_pool* pool, int32_t seq, int32_t new_len);
+/* pkv_seq_truncate for n distinct sequences (host arrays ids[n], new_lens[n]),
+ * in the order given; every argument is checked before anything changes. */
+pkv_status pkv_seq_truncate_many(pkv_pool* pool, int32_t n, const int32_t* seq_ids, const int32_t* new_lens);
 /* StreamingLLM eviction ([LC] StreamingKVCache, [SO] StreamingLLM 详解): drops
  * every block lying wholly outside [0, num_sinks) U [L - window, L); those
  * table entries become -1.  No-op when L <= num_sinks + window.  window >= 1. */
@@ -271,15 +274,17 @@ typedef enum {
   PKV_KERNEL_COW_COPY = 0,
   PKV_KERNEL_APPEND = 1,
   PKV_KERNEL_DECODE = 2,
-  PKV_KERNEL_COMBINE = 3,
+  PKV_KERNEL_COMBINE = 3, /* the split-KV merge runs inside the decode kernel: no launches */
   PKV_KERNEL_H2O_SCORE = 4,
   PKV_KERNEL_H2O_SELECT = 5,
   PKV_KERNEL_TABLE_PATCH = 6,
   PKV_KERNEL_COUNT = 7
 } pkv_kernel_id;
 
-/* When enabled, each kernel launch is bracketed by CUDA events on its stream. */
-pkv_status pkv_timing_enable(pkv_pool* pool, int32_t enable);
+/* Bit k of kernel_mask (k a pkv_kernel_id) brackets every launch of kernel k
+ * with CUDA events on its stream; 0 turns timing off, -1 times every kernel.
+ * Events between launches can add small gaps: time only what you read. */
+pkv_status pkv_timing_enable(pkv_pool* pool, int32_t kernel_mask);
 /* Synchronises on the recorded events and returns, per kernel id, the summed
  * device time (ms) and launch count since the last reset; then resets. */
 pkv_status pkv_timing_read(pkv_pool* pool, double* total_ms_out /* [PKV_KERNEL_COUNT] */,

@@ -32,6 +32,7 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#include <unistd.h>
 
 #define ORACLE_BLOCK 16 /* [PA] PagedAttention design: fixed blocks of 16 tokens by default */
 
@@ -183,18 +184,56 @@ void oracle_scatter(void* pool, int Hk, int D, int elem_bytes, const int64_t* sl
 }
 
 /* FP8 variant: quantise each (token, kv_head) row of bf16 and scatter codes and
- * the per-token scale (scale pool layout [block][kv_head][slot]). */
-void oracle_quantize_scatter(uint8_t* pool, float* scale_pool, int Hk, int D,
-                             const int64_t* slots, int T, const uint16_t* src) {
+ * the per-token scale (scale pool layout [block][kv_head][slot]).  Tokens are
+ * independent (distinct slots), so they are spread over the host's cores. */
+typedef struct {
+  uint8_t* pool;
+  float* scale_pool;
+  int Hk, D, T, thread_id, n_threads;
+  const int64_t* slots;
+  const uint16_t* src;
+} quantize_job;
+
+static void* quantize_worker(void* arg) {
+  quantize_job* q = (quantize_job*)arg;
   int t, g;
-  for (t = 0; t < T; t++) {
-    int block = (int)(slots[t] / ORACLE_BLOCK), slot = (int)(slots[t] % ORACLE_BLOCK);
-    for (g = 0; g < Hk; g++) {
-      size_t di = pool_index(block, Hk, g, slot, D, 0);
-      size_t si = ((size_t)block * Hk + g) * ORACLE_BLOCK + slot;
-      oracle_quantize_row_bf16(src + ((size_t)t * Hk + g) * D, D, pool + di, scale_pool + si);
+  for (t = q->thread_id; t < q->T; t += q->n_threads) {
+    int block = (int)(q->slots[t] / ORACLE_BLOCK), slot = (int)(q->slots[t] % ORACLE_BLOCK);
+    for (g = 0; g < q->Hk; g++) {
+      size_t di = pool_index(block, q->Hk, g, slot, q->D, 0);
+      size_t si = ((size_t)block * q->Hk + g) * ORACLE_BLOCK + slot;
+      oracle_quantize_row_bf16(q->src + ((size_t)t * q->Hk + g) * q->D, q->D, q->pool + di,
+                               q->scale_pool + si);
     }
   }
+  return NULL;
+}
+
+void oracle_quantize_scatter(uint8_t* pool, float* scale_pool, int Hk, int D, const int64_t* slots, int T,
+                             const uint16_t* src) {
+  long ncpu = sysconf(_SC_NPROCESSORS_ONLN);
+  int n = (int)(ncpu > 0 ? ncpu : 1), i;
+  quantize_job* jobs;
+  pthread_t* th;
+  if (n > 64) n = 64;
+  if (T < 4096) n = 1;
+  jobs = (quantize_job*)malloc(sizeof(quantize_job) * n);
+  th = (pthread_t*)malloc(sizeof(pthread_t) * n);
+  for (i = 0; i < n; i++) {
+    jobs[i].pool = pool;
+    jobs[i].scale_pool = scale_pool;
+    jobs[i].Hk = Hk;
+    jobs[i].D = D;
+    jobs[i].T = T;
+    jobs[i].thread_id = i;
+    jobs[i].n_threads = n;
+    jobs[i].slots = slots;
+    jobs[i].src = src;
+    pthread_create(&th[i], NULL, quantize_worker, &jobs[i]);
+  }
+  for (i = 0; i < n; i++) pthread_join(th[i], NULL);
+  free(jobs);
+  free(th);
 }
 
 /* Copy one whole physical block (all kv heads, all slots, K, V and scales):

@@ -128,6 +128,11 @@ class PagedKVCache:
     def seq_truncate(self, seq: int, new_len: int) -> None:
         _abi.check(self.lib.pkv_seq_truncate(self._h, seq, new_len))
 
+    def seq_truncate_many(self, seq_ids, new_lens) -> None:
+        ids, lens = _i32_array(seq_ids), _i32_array(new_lens)
+        assert ids.size == lens.size
+        _abi.check(self.lib.pkv_seq_truncate_many(self._h, ids.size, _ptr(ids), _ptr(lens)))
+
     def seq_evict(self, seq: int, num_sinks: int, window: int) -> None:
         _abi.check(self.lib.pkv_seq_evict(self._h, seq, num_sinks, window))
 
@@ -236,8 +241,17 @@ class PagedKVCache:
         _abi.check(self.lib.pkv_sync_status(self._h, _stream_ptr(stream)))
 
     # ---- measurement ------------------------------------------------------
-    def timing_enable(self, on: bool = True) -> None:
-        _abi.check(self.lib.pkv_timing_enable(self._h, 1 if on else 0))
+    def timing_enable(self, on=True) -> None:
+        """on: True (every kernel), False, or an iterable of kernel names."""
+        if on is True:
+            mask = -1
+        elif not on:
+            mask = 0
+        else:
+            mask = 0
+            for name in on:
+                mask |= 1 << KERNELS.index(name)
+        _abi.check(self.lib.pkv_timing_enable(self._h, mask))
 
     def timing_read(self) -> dict:
         ms = np.zeros(len(KERNELS), dtype=np.float64)

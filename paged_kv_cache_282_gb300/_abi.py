@@ -60,6 +60,7 @@ SIGNATURES = {
     "pkv_seq_fork": [c_void_p, c_int32, _P(c_int32)],
     "pkv_seq_free": [c_void_p, c_int32],
     "pkv_seq_truncate": [c_void_p, c_int32, c_int32],
+    "pkv_seq_truncate_many": [c_void_p, c_int32, c_void_p, c_void_p],
     "pkv_seq_evict": [c_void_p, c_int32, c_int32, c_int32],
     "pkv_seq_len": [c_void_p, c_int32, _P(c_int32)],
     "pkv_get_block_table": [c_void_p, c_int32, c_void_p, c_int32, _P(c_int32)],

@@ -12,8 +12,10 @@
 //    (FP8) K chunk plus the same for V, each contiguous in HBM.  The host cuts
 //    the concatenated units of all (sequence, kv head) pairs into equal
 //    contiguous runs, one per warp of a persistent grid (one CTA per SM), so
-//    ragged lengths balance exactly; partial results are merged by the
-//    log-sum-exp combine kernel.
+//    ragged lengths balance exactly.  A run that covers only part of its
+//    (sequence, kv head) writes a partial record; the warp that writes the
+//    last record of a (sequence, kv head) -- counted with one atomic per item
+//    -- merges them by log-sum-exp, so no separate combine launch is needed.
 //  - Every warp owns a private ring of shared-memory stages filled by TMA
 //    (cp.async.bulk.tensor, 2-D tiles of 16 rows x 128 bytes with the 128-byte
 //    swizzle, so the fragment loads below are bank-conflict free) and
@@ -57,8 +59,8 @@ struct TC<1> {  // BF16
   static constexpr uint32_t kTxBytes = 8192;
 };
 template <>
-struct TC<2> {  // FP8 E4M3
-  static constexpr int kWarps = 8, kStages = 5;
+struct TC<2> {  // FP8 E4M3: half-size units, so twice the warps to keep enough in flight
+  static constexpr int kWarps = 16, kStages = 3;
   static constexpr int kStageBytes = 4096;  // K: one swizzled box of 2 KB, V: same
   static constexpr int kScaleBytes = 128;   // 16 K scales + 16 V scales
   static constexpr uint32_t kTxBytes = 4096 + 128;
@@ -179,10 +181,28 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// two E4M3 codes (low byte first) -> two fp16 (low half first); exact
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xFFFFu), __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// four E4M3 codes (byte 0 first) -> two f16x2 registers: lo = (byte 0, byte 1),
+// hi = (byte 2, byte 3), lower half first.  Exact: E4M3 is a subset of fp16.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t codes, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 c0, c1;\n\t"
+      "mov.b32 {c0, c1}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, c0;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, c1;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(codes));
+}
+
+// 2^x and log2(x) with the hardware approximations (relative error ~2^-22;
+// subnormal results flush to zero), used for softmax weights and exponents.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ bool kept(int j, int L, int mode, int S, int W) {
@@ -223,6 +243,69 @@ __device__ __forceinline__ int unit_row(const DecodeTCParams& p, int pe, int ip,
   return (blk * p.n_kv_heads + pc.kv_head) * kBlock;
 }
 
+// Log-sum-exp merge of the partial records of one (sequence, kv head) by one
+// warp (the last writer): M = max_p M_p, w_p = 2^(M_p - M),
+// out = sum_p w_p O_p / sum_p w_p l_p, lse = (M + log2 sum_p w_p l_p) ln 2.
+// Records are taken 32/G at a time: lane (j, h) = (lane / G, lane % G) owns
+// the scalars of record j, head h, so every head is merged at once and all
+// loads of a chunk are independent.  Records written by other SMs are read
+// through L2 (ld.global.cg).
+template <int G>
+__device__ void merge_partials(const DecodeTCParams& p, const CombineItem it, int lane) {
+  constexpr int PF = G * 128 + ((2 * G + 3) & ~3);
+  constexpr int RPC = 32 / G;  // records per chunk
+  const float* base = p.partials + (size_t)it.first_partial * PF;
+  const int hl = lane % G, jl = lane / G;
+  const int n = it.n_partials;
+  float M = -INFINITY;
+  for (int k0 = 0; k0 < n; k0 += RPC)
+    if (k0 + jl < n) M = fmaxf(M, __ldcg(base + (size_t)(k0 + jl) * PF + G * 128 + hl));
+#pragma unroll
+  for (int off = 16; off >= G; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+  float4 acc[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lsum = 0.f;
+  for (int k0 = 0; k0 < n; k0 += RPC) {
+    float w = 0.f;
+    if (k0 + jl < n) {
+      const float* rec = base + (size_t)(k0 + jl) * PF;
+      const float Mk = __ldcg(rec + G * 128 + hl);
+      w = Mk == -INFINITY ? 0.f : exp2f(Mk - M);
+      lsum += w * __ldcg(rec + G * 128 + G + hl);
+    }
+#pragma unroll
+    for (int j = 0; j < RPC; ++j) {
+      if (k0 + j >= n) break;
+      const float* rec = base + (size_t)(k0 + j) * PF;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float wj = __shfl_sync(kFull, w, j * G + h);
+        const float4 o = __ldcg(reinterpret_cast<const float4*>(rec + h * 128) + lane);
+        acc[h].x += wj * o.x;
+        acc[h].y += wj * o.y;
+        acc[h].z += wj * o.z;
+        acc[h].w += wj * o.w;
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off >= G; off >>= 1) lsum += __shfl_xor_sync(kFull, lsum, off);
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const float l = __shfl_sync(kFull, lsum, h);  // lane h holds head h's total
+    const float Mh = __shfl_sync(kFull, M, h);
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const size_t row = (size_t)it.q_row * p.n_heads + it.kv_head * G + h;
+    uint2 packed;
+    packed.x = pack_bf16(acc[h].x * inv, acc[h].y * inv);
+    packed.y = pack_bf16(acc[h].z * inv, acc[h].w * inv);
+    *reinterpret_cast<uint2*>(out + row * 128 + lane * 4) = packed;
+    if (lane == 0 && p.lse != nullptr) p.lse[row] = l > 0.f ? (Mh + log2f(l)) * kLn2 : -INFINITY;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
@@ -237,6 +320,16 @@ __global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
   const int gw = blockIdx.x * C::kWarps + wl;
   if (gw >= p.total_warps) return;
+  // (sequence, kv head) pairs with an empty keep-set: zeros and -inf
+  for (int e = gw; e < p.n_empty; e += p.total_warps) {
+    const EmptyItem it = p.empty[e];
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+    for (int h = 0; h < G; ++h) {
+      const size_t row = ((size_t)it.q_row * p.n_heads + it.kv_head * G + h);
+      *reinterpret_cast<uint2*>(out + row * 128 + lane * 4) = make_uint2(0u, 0u);
+      if (lane == 0 && p.lse != nullptr) p.lse[row] = -INFINITY;
+    }
+  }
   const int pb = p.warp_begin[gw], pe = p.warp_begin[gw + 1];
   if (pb >= pe) return;
 
@@ -384,10 +477,8 @@ __global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           uint32_t a[4];
-          a[0] = e4m3x2_to_f16x2(tA[kk]);
-          a[1] = e4m3x2_to_f16x2(tB[kk]);
-          a[2] = e4m3x2_to_f16x2(tA[kk] >> 16);
-          a[3] = e4m3x2_to_f16x2(tB[kk] >> 16);
+          e4m3x4_to_f16x2x2(tA[kk], a[0], a[2]);
+          e4m3x4_to_f16x2x2(tB[kk], a[1], a[3]);
           if (kk & 1)
             mma_f16(sb, a, qf[kk][0], qf[kk][1]);
           else
@@ -396,8 +487,8 @@ __global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const
         const uint32_t sc = scl + (uint32_t)(st * C::kScaleBytes);
         ks_r = lds_f32(sc + 4 * r);
         ks_r8 = lds_f32(sc + 4 * (r + 8));
-        lv_r = log2f(lds_f32(sc + 64 + 4 * r));
-        lv_r8 = log2f(lds_f32(sc + 64 + 4 * (r + 8)));
+        lv_r = fast_log2(lds_f32(sc + 64 + 4 * r));
+        lv_r8 = fast_log2(lds_f32(sc + 64 + 4 * (r + 8)));
       }
       const float s0 = (sa[0] + sb[0]) * ks_r, s1 = (sa[1] + sb[1]) * ks_r;
       const float s2 = (sa[2] + sb[2]) * ks_r8, s3 = (sa[3] + sb[3]) * ks_r8;
@@ -447,14 +538,14 @@ __global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const
       }
       const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
       const float z0 = mn0 == -INFINITY ? 0.f : mn0, z1 = mn1 == -INFINITY ? 0.f : mn1;
-      const float al0 = exp2f(m0 - z0), al1 = exp2f(m1 - z1);
-      const float p0 = exp2f(e0 - z0), p1 = exp2f(e1 - z1), p2 = exp2f(e2 - z0), p3 = exp2f(e3 - z1);
+      const float al0 = fast_exp2(m0 - z0), al1 = fast_exp2(m1 - z1);
+      const float p0 = fast_exp2(e0 - z0), p1 = fast_exp2(e1 - z1), p2 = fast_exp2(e2 - z0), p3 = fast_exp2(e3 - z1);
       if (KV == 1) {
         l0 = l0 * al0 + (p0 + p2);
         l1 = l1 * al1 + (p1 + p3);
       } else {
-        l0 = l0 * al0 + (exp2f(a0 - z0) + exp2f(a2 - z0));
-        l1 = l1 * al1 + (exp2f(a1 - z1) + exp2f(a3 - z1));
+        l0 = l0 * al0 + (fast_exp2(a0 - z0) + fast_exp2(a2 - z0));
+        l1 = l1 * al1 + (fast_exp2(a1 - z1) + fast_exp2(a3 - z1));
       }
       m0 = mn0;
       m1 = mn1;
@@ -491,15 +582,11 @@ __global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
           const uint32_t lo = __byte_perm(A4[w], B4[w], 0x5140), hi = __byte_perm(A4[w], B4[w], 0x7362);
-          pab[4 * w + 0] = e4m3x2_to_f16x2(lo);
-          pab[4 * w + 1] = e4m3x2_to_f16x2(lo >> 16);
-          pab[4 * w + 2] = e4m3x2_to_f16x2(hi);
-          pab[4 * w + 3] = e4m3x2_to_f16x2(hi >> 16);
+          e4m3x4_to_f16x2x2(lo, pab[4 * w + 0], pab[4 * w + 1]);
+          e4m3x4_to_f16x2x2(hi, pab[4 * w + 2], pab[4 * w + 3]);
           const uint32_t lo2 = __byte_perm(C4[w], D4[w], 0x5140), hi2 = __byte_perm(C4[w], D4[w], 0x7362);
-          pcd[4 * w + 0] = e4m3x2_to_f16x2(lo2);
-          pcd[4 * w + 1] = e4m3x2_to_f16x2(lo2 >> 16);
-          pcd[4 * w + 2] = e4m3x2_to_f16x2(hi2);
-          pcd[4 * w + 3] = e4m3x2_to_f16x2(hi2 >> 16);
+          e4m3x4_to_f16x2x2(lo2, pcd[4 * w + 0], pcd[4 * w + 1]);
+          e4m3x4_to_f16x2x2(hi2, pcd[4 * w + 2], pcd[4 * w + 3]);
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -560,6 +647,17 @@ __global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const
             rec[G * 128 + h1] = m1;
             rec[G * 128 + G + h1] = l1;
           }
+        }
+        // publish the record, count it, and merge if it was the last one
+        __threadfence();
+        __syncwarp();
+        const int ci = pc.flags >> 1;
+        int last = 0;
+        if (lane == 0) last = atomicAdd(p.counters + ci, 1) == p.combine[ci].n_partials - 1;
+        last = __shfl_sync(kFull, last, 0);
+        if (last) {
+          __threadfence();
+          merge_partials<G>(p, p.combine[ci], lane);
         }
       }
       run_open = false;

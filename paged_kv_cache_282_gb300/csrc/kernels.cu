@@ -1,6 +1,6 @@
 // kernels.cu -- the HBM-bound helper kernels of libpkv (sm_103a):
 //   append / reshape_and_cache (+ FP8 E4M3 per-token quantisation),
-//   copy-on-write block copy, block-table patch, split-KV log-sum-exp combine,
+//   copy-on-write block copy, block-table patch,
 //   H2O score accumulation, H2O top-k keep-set selection, and the fp32
 //   CUDA-core decode used for fp32 pools.
 //
@@ -38,24 +38,40 @@ __device__ __forceinline__ int keep_pos(int k, int L, int mode, int S, int W) {
 }
 
 // ---------------------------------------------------------------------------
-// append: scatter new rows into their slots (bf16 / fp32 copy)
+// append: scatter new rows into their slots (bf16 / fp32 copy, or FP8
+// quantisation), and apply the block-table patches queued with them
 // ---------------------------------------------------------------------------
 
-__global__ void append_copy_kernel(const int64_t* __restrict__ slots, int n_tokens, int Hk, int row_chunks,
-                                   const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
-                                   uint4* __restrict__ k_pool, uint4* __restrict__ v_pool) {
-  const int64_t per_tok = (int64_t)Hk * row_chunks;
-  const int64_t total = (int64_t)n_tokens * per_tok;
+__device__ __forceinline__ int64_t slot_of(const AppendArgs& a, int64_t t) {
+  return a.slots ? a.slots[t] : a.inline_slots[t];
+}
+
+__device__ __forceinline__ void apply_patches(const AppendArgs& a) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.n_patches; i += gridDim.x * blockDim.x) {
+    const int32_t idx = a.patches ? a.patches[2 * i] : a.inline_patches[2 * i];
+    const int32_t val = a.patches ? a.patches[2 * i + 1] : a.inline_patches[2 * i + 1];
+    a.tables[idx] = val;
+  }
+}
+
+__global__ void append_copy_kernel(const __grid_constant__ AppendArgs a, int row_chunks) {
+  apply_patches(a);
+  const uint4* k_new = static_cast<const uint4*>(a.k_new);
+  const uint4* v_new = static_cast<const uint4*>(a.v_new);
+  uint4* k_pool = static_cast<uint4*>(a.k_pool);
+  uint4* v_pool = static_cast<uint4*>(a.v_pool);
+  const int64_t per_tok = (int64_t)a.Hk * row_chunks;
+  const int64_t total = (int64_t)a.n_tokens * per_tok;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < 2 * total;
        i += (int64_t)gridDim.x * blockDim.x) {
     const bool is_v = i >= total;
     const int64_t e = is_v ? i - total : i;
     const int64_t t = e / per_tok;
     const int64_t rem = e - t * per_tok;  // = g * row_chunks + chunk
-    const int64_t slot = slots[t];
+    const int64_t slot = slot_of(a, t);
     const int64_t blk = slot >> 4, off = slot & 15;
     const int64_t g = rem / row_chunks, ch = rem - g * row_chunks;
-    const int64_t dst = ((blk * Hk + g) * kBlock + off) * row_chunks + ch;
+    const int64_t dst = ((blk * a.Hk + g) * kBlock + off) * row_chunks + ch;
     if (is_v)
       v_pool[dst] = v_new[e];
     else
@@ -66,18 +82,17 @@ __global__ void append_copy_kernel(const int64_t* __restrict__ slots, int n_toke
 // FP8: one warp per (token, kv head, K|V) row of 128 values.
 //   s = absmax / 448 (fp32, IEEE division; 1 when absmax is 0)
 //   code = E4M3(x / s), round to nearest even, saturate to +-448
-__global__ void append_fp8_kernel(const int64_t* __restrict__ slots, int n_tokens, int Hk,
-                                  const __nv_bfloat16* __restrict__ k_new, const __nv_bfloat16* __restrict__ v_new,
-                                  uint8_t* __restrict__ k_pool, uint8_t* __restrict__ v_pool,
-                                  float* __restrict__ k_scale, float* __restrict__ v_scale) {
+__global__ void append_fp8_kernel(const __grid_constant__ AppendArgs a) {
+  apply_patches(a);
   const int lane = threadIdx.x & 31;
-  const int64_t rows = (int64_t)n_tokens * Hk;
+  const int64_t rows = (int64_t)a.n_tokens * a.Hk;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
   for (int64_t w = blockIdx.x * (int64_t)(blockDim.x / 32) + (threadIdx.x >> 5); w < 2 * rows; w += warps) {
     const bool is_v = w >= rows;
     const int64_t row = is_v ? w - rows : w;  // = t * Hk + g
-    const int64_t t = row / Hk, g = row - t * Hk;
-    const __nv_bfloat16* src = (is_v ? v_new : k_new) + row * 128 + lane * 4;
+    const int64_t t = row / a.Hk, g = row - t * a.Hk;
+    const __nv_bfloat16* src =
+        static_cast<const __nv_bfloat16*>(is_v ? a.v_new : a.k_new) + row * 128 + lane * 4;
     const uint2 raw = *reinterpret_cast<const uint2*>(src);
     const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
     const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
@@ -92,12 +107,12 @@ __global__ void append_fp8_kernel(const int64_t* __restrict__ slots, int n_token
       const __nv_fp8_storage_t code = __nv_cvt_float_to_fp8(__fdiv_rn(x[k], s), __NV_SATFINITE, __NV_E4M3);
       packed |= (uint32_t)code << (8 * k);
     }
-    const int64_t slot = slots[t];
+    const int64_t slot = slot_of(a, t);
     const int64_t blk = slot >> 4, off = slot & 15;
-    const int64_t srow = (blk * Hk + g) * kBlock + off;
-    uint8_t* dst = (is_v ? v_pool : k_pool) + srow * 128 + lane * 4;
+    const int64_t srow = (blk * a.Hk + g) * kBlock + off;
+    uint8_t* dst = static_cast<uint8_t*>(is_v ? a.v_pool : a.k_pool) + srow * 128 + lane * 4;
     *reinterpret_cast<uint32_t*>(dst) = packed;
-    if (lane == 0) (is_v ? v_scale : k_scale)[srow] = s;
+    if (lane == 0) (is_v ? a.v_scale : a.k_scale)[srow] = s;
   }
 }
 
@@ -122,40 +137,6 @@ __global__ void cow_copy_kernel(const int32_t* __restrict__ pairs, uint4* __rest
 __global__ void table_patch_kernel(const int32_t* __restrict__ patches, int n, int32_t* __restrict__ tables) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
     tables[patches[2 * i]] = patches[2 * i + 1];
-}
-
-// ---------------------------------------------------------------------------
-// split-KV combine: merge partial (O, M, l) records by log-sum-exp.
-// M is in log2 units; O and l are relative to 2^M.
-// ---------------------------------------------------------------------------
-
-__global__ void combine_kernel(const CombineItem* __restrict__ items, const float* __restrict__ partials, int G,
-                               int D, int n_heads, int n_kv_heads, __nv_bfloat16* __restrict__ out,
-                               float* __restrict__ lse) {
-  const CombineItem it = items[blockIdx.x];
-  const int pf = G * D + 2 * G;
-  for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
-    const int h = e / D, d = e - h * D;
-    const size_t orow = ((size_t)it.q_row * n_heads + it.kv_head * G + h);
-    if (it.n_partials == 0) {
-      out[orow * D + d] = __float2bfloat16(0.0f);
-      if (d == 0 && lse) lse[orow] = -INFINITY;
-      continue;
-    }
-    float M = -INFINITY;
-    for (int k = 0; k < it.n_partials; ++k)
-      M = fmaxf(M, partials[(size_t)(it.first_partial + k) * pf + G * D + h]);
-    float acc = 0.0f, l = 0.0f;
-    for (int k = 0; k < it.n_partials; ++k) {
-      const float* rec = partials + (size_t)(it.first_partial + k) * pf;
-      const float Mk = rec[G * D + h];
-      const float w = Mk == -INFINITY ? 0.0f : exp2f(Mk - M);
-      acc += w * rec[h * D + d];
-      l += w * rec[G * D + G + h];
-    }
-    out[orow * D + d] = __float2bfloat16(l > 0.0f ? acc / l : 0.0f);
-    if (d == 0 && lse) lse[orow] = l > 0.0f ? (M + log2f(l)) * 0.6931471805599453f : -INFINITY;
-  }
 }
 
 // ---------------------------------------------------------------------------
@@ -228,6 +209,8 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
                                                                  const float* __restrict__ acc, int64_t acc_stride,
                                                                  int budget, int recent, int32_t* __restrict__ keep_idx,
                                                                  int64_t keep_stride, int32_t* __restrict__ keep_count) {
+  constexpr int kUnroll = 8;  // independent loads in flight per thread
+  constexpr int kPerThread = 4;  // contiguous keys per thread in the ordered pass
   __shared__ uint32_t hist[256];
   __shared__ int s_warp[32];
   __shared__ uint32_t s_prefix, s_mask;
@@ -242,6 +225,7 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
     return;
   }
   const int n = L - recent, keep = budget - recent;  // n > keep here
+  const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     s_prefix = 0;
     s_mask = 0;
@@ -253,9 +237,23 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
       for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
       __syncthreads();
       const uint32_t prefix = s_prefix, mask = s_mask;
-      for (int j = threadIdx.x; j < n; j += blockDim.x) {
-        const uint32_t key = order_key(a[j]);
-        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+      for (int base = 0; base < n; base += kUnroll * kSelThreads) {
+        uint32_t key[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int j = base + u * kSelThreads + threadIdx.x;
+          key[u] = j < n ? order_key(a[j]) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int j = base + u * kSelThreads + threadIdx.x;
+          const bool match = j < n && (key[u] & mask) == prefix;
+          // lanes with the same digit add their count once (scores are often
+          // equal, e.g. zero outside the keep-set, and would all hit one bin)
+          const uint32_t digit = match ? ((key[u] >> shift) & 255u) : 256u;
+          const unsigned same = __match_any_sync(kFull, digit);
+          if (match && lane == __ffs(same) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(same));
+        }
       }
       __syncthreads();
       if (threadIdx.x == 0) {
@@ -278,18 +276,36 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
   const int need_eq = s_k;  // equal-to-T keys to take, lowest positions first
   int taken = 0, eq_seen = 0;
   if (keep > 0) {
-    for (int base = 0; base < n; base += blockDim.x) {
-      const int j = base + threadIdx.x;
-      uint32_t key = 0;
-      if (j < n) key = order_key(a[j]);
-      const int gt = (j < n && key > T) ? 1 : 0;
-      const int eq = (j < n && key == T) ? 1 : 0;
+    for (int base = 0; base < n; base += kPerThread * kSelThreads) {
+      const int j0 = base + kPerThread * threadIdx.x;
+      uint32_t key[kPerThread];
+      int n_gt = 0, n_eq = 0;
+#pragma unroll
+      for (int u = 0; u < kPerThread; ++u) {
+        key[u] = j0 + u < n ? order_key(a[j0 + u]) : 0u;
+        n_gt += (j0 + u < n && key[u] > T);
+        n_eq += (j0 + u < n && key[u] == T);
+      }
       int eq_excl;
-      const int eq_tot = block_excl_scan(eq, &eq_excl, s_warp);
-      const int sel = gt || (eq && eq_seen + eq_excl < need_eq);
+      const int eq_tot = block_excl_scan(n_eq, &eq_excl, s_warp);
+      int rank = eq_seen + eq_excl, n_sel = n_gt;
+      bool sel[kPerThread];
+#pragma unroll
+      for (int u = 0; u < kPerThread; ++u) {
+        const bool valid = j0 + u < n;
+        const bool is_eq = valid && key[u] == T;
+        sel[u] = (valid && key[u] > T) || (is_eq && rank < need_eq);
+        if (is_eq) {
+          n_sel += rank < need_eq;
+          ++rank;
+        }
+      }
       int sel_excl;
-      const int sel_tot = block_excl_scan(sel, &sel_excl, s_warp);
-      if (sel) out[taken + sel_excl] = j;
+      const int sel_tot = block_excl_scan(n_sel, &sel_excl, s_warp);
+      int pos = taken + sel_excl;
+#pragma unroll
+      for (int u = 0; u < kPerThread; ++u)
+        if (sel[u]) out[pos++] = j0 + u;
       taken += sel_tot;
       eq_seen += eq_tot;
     }
@@ -357,20 +373,15 @@ int grid_for(int64_t work, int threads) {
 
 }  // namespace
 
-cudaError_t launch_append(int kv_dtype, const int64_t* slots, int n_tokens, int Hk, int D, const void* k_new,
-                          const void* v_new, void* k_pool, void* v_pool, float* k_scale, float* v_scale,
-                          cudaStream_t st) {
-  if (n_tokens <= 0) return cudaSuccess;
-  if (kv_dtype == 2) {
-    const int64_t warps = 2LL * n_tokens * Hk;
-    append_fp8_kernel<<<grid_for(warps * 32, 256), 256, 0, st>>>(
-        slots, n_tokens, Hk, (const __nv_bfloat16*)k_new, (const __nv_bfloat16*)v_new, (uint8_t*)k_pool,
-        (uint8_t*)v_pool, k_scale, v_scale);
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t st) {
+  if (a.n_tokens <= 0 && a.n_patches <= 0) return cudaSuccess;
+  if (a.kv_dtype == 2) {
+    const int64_t warps = 2LL * a.n_tokens * a.Hk;
+    append_fp8_kernel<<<grid_for(std::max<int64_t>(warps * 32, a.n_patches), 256), 256, 0, st>>>(a);
   } else {
-    const int row_chunks = D * (kv_dtype == 0 ? 4 : 2) / 16;
-    const int64_t work = 2LL * n_tokens * Hk * row_chunks;
-    append_copy_kernel<<<grid_for(work, 256), 256, 0, st>>>(slots, n_tokens, Hk, row_chunks, (const uint4*)k_new,
-                                                            (const uint4*)v_new, (uint4*)k_pool, (uint4*)v_pool);
+    const int row_chunks = a.D * (a.kv_dtype == 0 ? 4 : 2) / 16;
+    const int64_t work = 2LL * a.n_tokens * a.Hk * row_chunks;
+    append_copy_kernel<<<grid_for(std::max<int64_t>(work, a.n_patches), 256), 256, 0, st>>>(a, row_chunks);
   }
   return cudaGetLastError();
 }
@@ -392,13 +403,6 @@ cudaError_t launch_cow_copy(const int32_t* pairs, int n_pairs, void* k_pool, voi
 cudaError_t launch_table_patch(const int32_t* patches, int n, int32_t* tables, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
   table_patch_kernel<<<std::min((n + 255) / 256, 1024), 256, 0, st>>>(patches, n, tables);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_combine(const CombineItem* items, int n_items, const float* partials, int G, int D, int n_heads,
-                           int /*out_bf16*/, void* out, float* lse, cudaStream_t st) {
-  if (n_items <= 0) return cudaSuccess;
-  combine_kernel<<<n_items, 256, 0, st>>>(items, partials, G, D, n_heads, n_heads / G, (__nv_bfloat16*)out, lse);
   return cudaGetLastError();
 }
 

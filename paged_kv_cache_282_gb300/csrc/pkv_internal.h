@@ -17,7 +17,9 @@ enum : int32_t { kStatusTimeout = 1, kStatusBadBlock = 2 };
 // One contiguous range of logical blocks of one (sequence, kv head), handled
 // by one warp of the decode kernel.  Consecutive pieces of the same
 // (sequence, kv head) inside one warp form a "run"; the run is finalised
-// after the piece that carries kPieceLastOfRun.
+// after the piece whose flags carry kPieceLastOfRun.  A run that does not
+// cover its whole (sequence, kv head) writes a partial record; flags >> 1 is
+// then the index of the merge item that owns the record.
 enum : int32_t { kPieceLastOfRun = 1 };
 struct Piece {
   int32_t seq_slot;    // block-table row
@@ -27,14 +29,20 @@ struct Piece {
   int32_t lblk_end;
   int32_t ctx_len;     // L: context length, current token included
   int32_t out_index;   // >= 0: partial record index; -1: write the final output
-  int32_t flags;
+  int32_t flags;       // bit 0: last piece of its run; bits 31..1: merge item
 };
 static_assert(sizeof(Piece) == 32, "Piece layout");
 
-// A (sequence, kv head) whose partial records must be merged, or whose
-// keep-set is empty (n_partials == 0: zeros and -inf).
+// A (sequence, kv head) whose n_partials (>= 2) partial records, stored
+// consecutively from first_partial, are merged by log-sum-exp.  The warp that
+// writes the last of them (counted with an atomic per item) does the merge.
 struct CombineItem {
   int32_t q_row, kv_head, first_partial, n_partials;
+};
+
+// A (sequence, kv head) with an empty keep-set: out = 0, lse = -inf.
+struct EmptyItem {
+  int32_t q_row, kv_head;
 };
 
 // Per-sequence row for kernels that walk one sequence at a time.
@@ -42,9 +50,9 @@ struct SeqRow {
   int32_t seq_slot, q_row, ctx_len, pad;
 };
 
-// Floats per partial record: O[G][D] (unnormalised), then M[G] (log2 units),
-// then l[G].
-inline __host__ __device__ int partial_floats(int G, int D) { return G * D + 2 * G; }
+// Floats per partial record: O[G][D] (unnormalised), M[G] (log2 units),
+// l[G], padded so that every record starts on a 16-byte boundary.
+inline __host__ __device__ int partial_floats(int G, int D) { return G * D + ((2 * G + 3) & ~3); }
 
 struct DecodeTCParams {
   CUtensorMap tmap_k;  // 2-D view [num_blocks * Hk * 16][D] of the K pool, 128B swizzle
@@ -63,6 +71,10 @@ struct DecodeTCParams {
   const int32_t* warp_begin;  // [total_warps + 1]
   int32_t total_warps;
   float* partials;
+  const CombineItem* combine;  // merge items, with one arrival counter each
+  int32_t* counters;           // zero at launch
+  const EmptyItem* empty;
+  int32_t n_empty;
   float scale;       // natural-unit softmax scale
   int32_t mask_mode, num_sinks, window;
   int32_t* status;
@@ -99,10 +111,6 @@ cudaError_t decode_tc_occupancy(int kv_dtype, int G, int* ctas_per_sm);
 
 cudaError_t launch_decode_f32(const DecodeF32Params& p, cudaStream_t stream);
 
-cudaError_t launch_combine(const CombineItem* items, int n_items, const float* partials, int G,
-                           int D, int n_heads, int kv_dtype_out_bf16, void* out, float* lse,
-                           cudaStream_t stream);
-
 cudaError_t launch_cow_copy(const int32_t* pairs, int n_pairs, void* k_pool, void* v_pool,
                             float* k_scale, float* v_scale, size_t block_bytes,
                             size_t scale_floats_per_block, cudaStream_t stream);
@@ -110,9 +118,25 @@ cudaError_t launch_cow_copy(const int32_t* pairs, int n_pairs, void* k_pool, voi
 cudaError_t launch_table_patch(const int32_t* patches, int n_patches, int32_t* tables,
                                cudaStream_t stream);
 
-cudaError_t launch_append(int kv_dtype, const int64_t* slots, int n_tokens, int Hk, int D,
-                          const void* k_new, const void* v_new, void* k_pool, void* v_pool,
-                          float* k_scale, float* v_scale, cudaStream_t stream);
+// Append (scatter / FP8 quantise) of new rows, plus the block-table patches
+// queued with it.  Up to kInlineAppend slots and patches travel inside the
+// kernel parameters; larger lists come from device memory.
+constexpr int kInlineAppend = 256;
+struct AppendArgs {
+  int kv_dtype, n_tokens, n_patches, Hk, D;
+  const int64_t* slots;     // device, or nullptr: inline_slots
+  const int32_t* patches;   // device (index, value) pairs, or nullptr: inline_patches
+  const void* k_new;
+  const void* v_new;
+  void* k_pool;
+  void* v_pool;
+  float* k_scale;
+  float* v_scale;
+  int32_t* tables;
+  int64_t inline_slots[kInlineAppend];
+  int32_t inline_patches[2 * kInlineAppend];
+};
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 
 cudaError_t launch_h2o_score(const SeqRow* rows, int n_seqs, int n_heads, int n_kv_heads,
                              const float* logits, int64_t logits_stride, const float* lse,

@@ -242,7 +242,7 @@ struct Staging {
 // ---------------------------------------------------------------------------
 
 struct Timing {
-  bool enabled = false;
+  int32_t mask = 0;  // bit k: bracket launches of kernel id k with events
   std::vector<cudaEvent_t> spare;
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> marks[PKV_KERNEL_COUNT];
 
@@ -293,7 +293,8 @@ namespace {
 template <class F>
 pkv_status launch(pkv_pool* p, int kernel, cudaStream_t st, F&& fn) {
   cudaEvent_t a = nullptr, b = nullptr;
-  if (p->timing.enabled) {
+  const bool timed = (p->timing.mask >> kernel) & 1;
+  if (timed) {
     a = p->timing.get();
     b = p->timing.get();
     PKV_CUDA(cudaEventRecord(a, st));
@@ -301,7 +302,7 @@ pkv_status launch(pkv_pool* p, int kernel, cudaStream_t st, F&& fn) {
   cudaError_t e = fn();
   if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "kernel %d launch failed: %s", kernel, cudaGetErrorString(e));
   ++p->launches;
-  if (p->timing.enabled) {
+  if (timed) {
     PKV_CUDA(cudaEventRecord(b, st));
     p->timing.marks[kernel].push_back({a, b});
   }
@@ -371,20 +372,28 @@ pkv_status make_tensor_map(CUtensorMap* m, void* base, const pkv_pool_config& c)
   return PKV_OK;
 }
 
-pkv_status flush_pending(pkv_pool* p, cudaStream_t st) {
+// Several queued changes of one table entry collapse to the last one (the
+// kernels that apply patches do so in parallel).
+std::vector<TablePatch> dedup_patches(const std::vector<TablePatch>& q) {
+  std::unordered_map<int32_t, size_t> last;
+  last.reserve(q.size() * 2);
+  for (size_t i = 0; i < q.size(); ++i) last[q[i].index] = i;
+  std::vector<TablePatch> out;
+  out.reserve(last.size());
+  for (size_t i = 0; i < q.size(); ++i)
+    if (last[q[i].index] == i) out.push_back(q[i]);
+  return out;
+}
+
+// Flushes queued copy-on-write copies and, unless the caller applies them
+// itself (the append kernel does), the queued block-table patches.
+pkv_status flush_pending(pkv_pool* p, cudaStream_t st, bool with_patches = true) {
   HostAllocator& A = p->alloc;
-  if (A.pending_cow.empty() && A.pending_patch.empty()) return PKV_OK;
+  if (A.pending_cow.empty() && (A.pending_patch.empty() || !with_patches)) return PKV_OK;
   // Table patches: several changes to one entry collapse to the last one (the
   // patch kernel applies its list in parallel).
   std::vector<TablePatch> patches;
-  {
-    std::unordered_map<int32_t, size_t> last;
-    last.reserve(A.pending_patch.size() * 2);
-    for (size_t i = 0; i < A.pending_patch.size(); ++i) last[A.pending_patch[i].index] = i;
-    patches.reserve(last.size());
-    for (size_t i = 0; i < A.pending_patch.size(); ++i)
-      if (last[A.pending_patch[i].index] == i) patches.push_back(A.pending_patch[i]);
-  }
+  if (with_patches) patches = dedup_patches(A.pending_patch);
   // COW copies: a copy whose source or destination is the destination of an
   // earlier copy in the list must run after it, so the list is cut into waves
   // of independent copies that run in order.
@@ -431,7 +440,7 @@ pkv_status flush_pending(pkv_pool* p, cudaStream_t st) {
   }
   if (pkv_status r = Staging::release(s, st)) return r;
   A.pending_cow.clear();
-  A.pending_patch.clear();
+  if (with_patches) A.pending_patch.clear();
   return PKV_OK;
 }
 
@@ -461,10 +470,12 @@ namespace {
 constexpr int kMinUnitsPerWarp = 4;
 
 struct Plan {
-  std::vector<int32_t> warp_begin;
-  std::vector<Piece> pieces;
+  std::vector<int32_t> warp_begin;  // per physical warp slot (cta * warps_per_cta + warp)
+  std::vector<Piece> pieces;        // grouped by physical warp slot
   std::vector<CombineItem> combine;
-  int total_warps = 0;
+  std::vector<EmptyItem> empty;
+  int total_warps = 0;  // physical warp slots = ctas * warps_per_cta
+  int ctas = 0;
   int n_partials = 0;
 };
 
@@ -579,16 +590,6 @@ void build_plan(const pkv_pool* p, int32_t n, const int32_t* ids, int mode, int 
         }
     }
   }
-  // warp boundaries
-  plan.warp_begin.assign(plan.total_warps + 1, 0);
-  {
-    size_t k = 0;
-    for (int w = 0; w < plan.total_warps; ++w) {
-      plan.warp_begin[w] = (int32_t)k;
-      while (k < plan.pieces.size() && piece_warp[k] == w) ++k;
-    }
-    plan.warp_begin[plan.total_warps] = (int32_t)k;
-  }
   // runs: consecutive pieces of one (b, g) inside one warp; explicit split
   // parts already carry their own run ends
   const size_t np = plan.pieces.size();
@@ -618,12 +619,48 @@ void build_plan(const pkv_pool* p, int32_t n, const int32_t* ids, int mode, int 
     run_start = k + 1;
   }
   plan.n_partials = next_partial;
+  std::vector<int32_t> item_of((size_t)n * Hk, -1);
   for (int32_t b = 0; b < n; ++b)
     for (int g = 0; g < Hk; ++g) {
       const size_t bg = (size_t)b * Hk + g;
-      if (bg_units[bg] == 0) plan.combine.push_back({b, g, 0, 0});
-      else if (n_part[bg] > 0) plan.combine.push_back({b, g, first_partial[bg], n_part[bg]});
+      if (bg_units[bg] == 0) {
+        plan.empty.push_back({b, g});
+      } else if (n_part[bg] > 0) {
+        item_of[bg] = (int32_t)plan.combine.size();
+        plan.combine.push_back({b, g, first_partial[bg], n_part[bg]});
+      }
     }
+  for (auto& pc : plan.pieces)
+    if (pc.out_index >= 0) pc.flags |= item_of[(size_t)pc.q_row * Hk + pc.kv_head] << 1;
+
+  // Physical placement: virtual warp v runs in CTA v % C as its warp v / C,
+  // so that the work is spread over as many SMs as possible.
+  const int TW = plan.total_warps;
+  const int WPC = std::max(1, p->tc_warps_per_cta);
+  const int C = std::max(1, std::min(TW, max_total_warps(p) / WPC));
+  std::vector<size_t> vstart(TW + 1, 0);
+  {
+    size_t k = 0;
+    for (int v = 0; v < TW; ++v) {
+      vstart[v] = k;
+      while (k < np && piece_warp[k] == v) ++k;
+    }
+    vstart[TW] = k;
+  }
+  std::vector<Piece> ordered;
+  ordered.reserve(np);
+  const int slots = TW > 0 ? C * WPC : 0;
+  plan.warp_begin.assign(slots + 1, 0);
+  for (int phys = 0; phys < slots; ++phys) {
+    plan.warp_begin[phys] = (int32_t)ordered.size();
+    const int v = (phys % WPC) * C + phys / WPC;
+    if (v < TW)
+      for (size_t k = vstart[v]; k < vstart[v + 1]; ++k) ordered.push_back(plan.pieces[k]);
+  }
+  plan.warp_begin[slots] = (int32_t)ordered.size();
+  plan.pieces.swap(ordered);
+  plan.total_warps = slots;
+  plan.ctas = TW > 0 ? C : 0;
 }
 
 pkv_status check_keep_blocks_present(const pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, int W) {
@@ -639,6 +676,76 @@ pkv_status check_keep_blocks_present(const pkv_pool* p, int32_t n, const int32_t
           return fail(PKV_ERR_INVALID_ARG, "sequence %d: block %d of the keep-set was evicted", s, lb);
   }
   return PKV_OK;
+}
+
+// Byte layout of an uploaded decode plan: [warp_begin][pieces][merge items]
+// [merge counters, zero][empty items], each part 32-byte aligned.
+struct PlanLayout {
+  size_t wb = 0, pieces = 0, combine = 0, counters = 0, empty = 0, bytes = 0;
+};
+
+PlanLayout plan_layout(Plan& pl, int warps_per_cta, size_t base) {
+  if (pl.total_warps == 0 && !pl.empty.empty()) {  // only empty keep-sets: one CTA writes them
+    pl.ctas = 1;
+    pl.total_warps = warps_per_cta;
+    pl.warp_begin.assign(warps_per_cta + 1, 0);
+  }
+  auto up = [](size_t x) { return (x + 31) & ~size_t(31); };
+  PlanLayout L;
+  L.wb = up(base);
+  L.pieces = up(L.wb + pl.warp_begin.size() * sizeof(int32_t));
+  L.combine = up(L.pieces + pl.pieces.size() * sizeof(Piece));
+  L.counters = up(L.combine + pl.combine.size() * sizeof(CombineItem));
+  L.empty = up(L.counters + pl.combine.size() * sizeof(int32_t));
+  L.bytes = L.empty + pl.empty.size() * sizeof(EmptyItem);
+  return L;
+}
+
+void plan_write(const Plan& pl, const PlanLayout& L, char* host) {
+  if (!pl.warp_begin.empty()) memcpy(host + L.wb, pl.warp_begin.data(), pl.warp_begin.size() * sizeof(int32_t));
+  if (!pl.pieces.empty()) memcpy(host + L.pieces, pl.pieces.data(), pl.pieces.size() * sizeof(Piece));
+  if (!pl.combine.empty()) {
+    memcpy(host + L.combine, pl.combine.data(), pl.combine.size() * sizeof(CombineItem));
+    memset(host + L.counters, 0, pl.combine.size() * sizeof(int32_t));
+  }
+  if (!pl.empty.empty()) memcpy(host + L.empty, pl.empty.data(), pl.empty.size() * sizeof(EmptyItem));
+}
+
+// Launches the tensor-core decode (with its fused merge) over an uploaded plan.
+pkv_status launch_tc_plan(pkv_pool* p, cudaStream_t st, const Plan& pl, const PlanLayout& L, const char* dev,
+                          const void* q, float scale, int mode, int S, int W, void* out, float* lse, float* logits,
+                          int64_t logits_stride, void* partials) {
+  if (pl.total_warps == 0) return PKV_OK;
+  const auto& c = p->cfg;
+  DecodeTCParams prm;
+  prm.tmap_k = p->tmap_k;
+  prm.tmap_v = p->tmap_v;
+  prm.k_scale = p->buf.k_scale;
+  prm.v_scale = p->buf.v_scale;
+  prm.tables = p->buf.block_tables;
+  prm.max_blocks = c.max_blocks_per_seq;
+  prm.num_blocks = c.num_blocks;
+  prm.n_heads = c.n_heads;
+  prm.n_kv_heads = c.n_kv_heads;
+  prm.q = q;
+  prm.out = out;
+  prm.lse = lse;
+  prm.logits = logits;
+  prm.logits_stride = logits_stride;
+  prm.pieces = (const Piece*)(dev + L.pieces);
+  prm.warp_begin = (const int32_t*)(dev + L.wb);
+  prm.total_warps = pl.total_warps;
+  prm.partials = (float*)partials;
+  prm.combine = (const CombineItem*)(dev + L.combine);
+  prm.counters = (int32_t*)(dev + L.counters);
+  prm.empty = (const EmptyItem*)(dev + L.empty);
+  prm.n_empty = (int32_t)pl.empty.size();
+  prm.scale = scale;
+  prm.mask_mode = mode;
+  prm.num_sinks = S;
+  prm.window = W;
+  prm.status = p->buf.status;
+  return launch(p, PKV_KERNEL_DECODE, st, [&] { return launch_decode_tc(c.kv_dtype, p->G, prm, pl.ctas, st); });
 }
 
 }  // namespace
@@ -700,23 +807,17 @@ int pkv::decode_attn_into(pkv_pool* p, void* stream, int32_t n, const int32_t* i
     return fail(PKV_ERR_WORKSPACE, "needs %zu bytes of partial records, the static scratch holds %zu",
                 (size_t)plan.n_partials * pf, partials_cap);
 
-  // one blob: [cow pairs][patches][warp_begin][pieces][combine]
+  // one blob: [cow pairs][patches][plan]
   auto up32 = [](size_t x) { return (x + 31) & ~size_t(31); };
   const size_t cow_off = 0, patch_off = up32(ncow * 2 * sizeof(int32_t));
-  const size_t wb_off = up32(patch_off + patches.size() * sizeof(TablePatch));
-  const size_t pieces_off = up32(wb_off + plan.warp_begin.size() * sizeof(int32_t));
-  const size_t comb_off = pieces_off + plan.pieces.size() * sizeof(Piece);
-  const size_t bytes = comb_off + plan.combine.size() * sizeof(CombineItem);
+  const PlanLayout L = plan_layout(plan, p->tc_warps_per_cta, patch_off + patches.size() * sizeof(TablePatch));
+  const size_t bytes = L.bytes;
   if (bytes > plan_cap)
     return fail(PKV_ERR_WORKSPACE, "needs %zu bytes of plan, the static scratch holds %zu", bytes, plan_cap);
   std::vector<char> blob(bytes);
   if (ncow) memcpy(blob.data() + cow_off, A.pending_cow.data(), ncow * 2 * sizeof(int32_t));
   if (!patches.empty()) memcpy(blob.data() + patch_off, patches.data(), patches.size() * sizeof(TablePatch));
-  if (!plan.warp_begin.empty())
-    memcpy(blob.data() + wb_off, plan.warp_begin.data(), plan.warp_begin.size() * sizeof(int32_t));
-  if (!plan.pieces.empty()) memcpy(blob.data() + pieces_off, plan.pieces.data(), plan.pieces.size() * sizeof(Piece));
-  if (!plan.combine.empty())
-    memcpy(blob.data() + comb_off, plan.combine.data(), plan.combine.size() * sizeof(CombineItem));
+  plan_write(plan, L, blob.data());
   char* dev = (char*)plan_dev;
   if (bytes) PKV_CUDA(cudaMemcpyAsync(dev, blob.data(), bytes, cudaMemcpyHostToDevice, st));
 
@@ -742,43 +843,7 @@ int pkv::decode_attn_into(pkv_pool* p, void* stream, int32_t n, const int32_t* i
   A.pending_cow.clear();
   A.pending_patch.clear();
   if (n == 0) return PKV_OK;
-  if (plan.total_warps > 0) {
-    DecodeTCParams prm;
-    prm.tmap_k = p->tmap_k;
-    prm.tmap_v = p->tmap_v;
-    prm.k_scale = p->buf.k_scale;
-    prm.v_scale = p->buf.v_scale;
-    prm.tables = p->buf.block_tables;
-    prm.max_blocks = c.max_blocks_per_seq;
-    prm.num_blocks = c.num_blocks;
-    prm.n_heads = c.n_heads;
-    prm.n_kv_heads = c.n_kv_heads;
-    prm.q = q;
-    prm.out = out;
-    prm.lse = lse;
-    prm.logits = logits;
-    prm.logits_stride = logits_stride;
-    prm.pieces = (const Piece*)(dev + pieces_off);
-    prm.warp_begin = (const int32_t*)(dev + wb_off);
-    prm.total_warps = plan.total_warps;
-    prm.partials = (float*)partials_dev;
-    prm.scale = scale;
-    prm.mask_mode = mode;
-    prm.num_sinks = S;
-    prm.window = W;
-    prm.status = p->buf.status;
-    const int ctas = ceil_div(plan.total_warps, p->tc_warps_per_cta);
-    if (pkv_status r = launch(p, PKV_KERNEL_DECODE, st, [&] { return launch_decode_tc(c.kv_dtype, p->G, prm, ctas, st); }))
-      return r;
-  }
-  if (!plan.combine.empty()) {
-    if (pkv_status r = launch(p, PKV_KERNEL_COMBINE, st, [&] {
-          return launch_combine((const CombineItem*)(dev + comb_off), (int)plan.combine.size(),
-                                (const float*)partials_dev, p->G, c.head_dim, c.n_heads, 1, out, lse, st);
-        }))
-      return r;
-  }
-  return PKV_OK;
+  return launch_tc_plan(p, st, plan, L, dev, q, scale, mode, S, W, out, lse, logits, logits_stride, partials_dev);
 }
 
 // ---------------------------------------------------------------------------
@@ -908,6 +973,26 @@ pkv_status pkv_seq_truncate(pkv_pool* p, int32_t s, int32_t new_len) {
     return fail(PKV_ERR_INVALID_ARG, "the new last block of sequence %d was evicted", s);
   A.drop_from(s, keep_blk);
   A.len[s] = new_len;
+  return PKV_OK;
+}
+
+pkv_status pkv_seq_truncate_many(pkv_pool* p, int32_t n, const int32_t* ids, const int32_t* new_lens) {
+  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  if (n < 0 || (n > 0 && (!ids || !new_lens))) return fail(PKV_ERR_INVALID_ARG, "bad arrays");
+  auto& A = p->alloc;
+  for (int32_t i = 0; i < n; ++i) {  // validate everything before changing anything
+    const int32_t s = ids[i], L = new_lens[i];
+    if (!A.valid_seq(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", s);
+    if (L < 0 || L > A.len[s]) return fail(PKV_ERR_INVALID_ARG, "new_len %d outside [0, %d]", L, A.len[s]);
+    if (L % kBlock && A.table[s][ceil_div(L, kBlock) - 1] < 0)
+      return fail(PKV_ERR_INVALID_ARG, "the new last block of sequence %d was evicted", s);
+    for (int32_t j = 0; j < i; ++j)
+      if (ids[j] == s) return fail(PKV_ERR_INVALID_ARG, "sequence %d listed twice", s);
+  }
+  for (int32_t i = 0; i < n; ++i) {
+    A.drop_from(ids[i], ceil_div(new_lens[i], kBlock));
+    A.len[ids[i]] = new_lens[i];
+  }
   return PKV_OK;
 }
 
@@ -1054,26 +1139,60 @@ pkv_status pkv_append(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, 
   std::vector<int64_t> slots(ntok);
   if (pkv_status r = pkv_reserve_slots(p, n, ids, T, slots.data(), nullptr, 0, nullptr)) return r;
   cudaStream_t st = (cudaStream_t)stream;
-  if (pkv_status r = flush_pending(p, st)) return r;
-  if (ntok == 0) return PKV_OK;
+  // copies first: the new rows of a copied block land in the copy
+  if (pkv_status r = flush_pending(p, st, /*with_patches=*/false)) return r;
+  std::vector<TablePatch> patches = dedup_patches(p->alloc.pending_patch);
+  p->alloc.pending_patch.clear();
+  if (ntok == 0 && patches.empty()) return PKV_OK;
   const auto& c = p->cfg;
   const size_t row_bytes = (size_t)c.n_kv_heads * c.head_dim * (c.kv_dtype == PKV_KV_FP32 ? 4 : 2);
-  // large appends go through the staging ring in chunks of tokens
-  const size_t chunk = size_t(1) << 20;
-  for (size_t t0 = 0; t0 < ntok; t0 += chunk) {
-    const size_t nt = std::min(chunk, ntok - t0);
-    StagingSlot* s;
-    if (pkv_status r = p->staging.acquire(nt * sizeof(int64_t), &s)) return r;
-    memcpy(s->host, slots.data() + t0, nt * sizeof(int64_t));
-    if (pkv_status r = Staging::upload(s, nt * sizeof(int64_t), st)) return r;
-    if (pkv_status r = launch(p, PKV_KERNEL_APPEND, st, [&] {
-          return launch_append(c.kv_dtype, (const int64_t*)s->dev, (int)nt, c.n_kv_heads, c.head_dim,
-                               (const char*)k_new + t0 * row_bytes, (const char*)v_new + t0 * row_bytes,
-                               p->buf.k_pool, p->buf.v_pool, p->buf.k_scale, p->buf.v_scale, st);
-        }))
-      return r;
-    if (pkv_status r = Staging::release(s, st)) return r;
+  AppendArgs a;
+  a.kv_dtype = c.kv_dtype;
+  a.Hk = c.n_kv_heads;
+  a.D = c.head_dim;
+  a.k_pool = p->buf.k_pool;
+  a.v_pool = p->buf.v_pool;
+  a.k_scale = p->buf.k_scale;
+  a.v_scale = p->buf.v_scale;
+  a.tables = p->buf.block_tables;
+  if (ntok <= (size_t)kInlineAppend && patches.size() <= (size_t)kInlineAppend) {
+    // small (decode-step) append: slots and patches ride in the parameters
+    a.n_tokens = (int)ntok;
+    a.n_patches = (int)patches.size();
+    a.slots = nullptr;
+    a.patches = nullptr;
+    for (size_t i = 0; i < ntok; ++i) a.inline_slots[i] = slots[i];
+    for (size_t i = 0; i < patches.size(); ++i) {
+      a.inline_patches[2 * i] = patches[i].index;
+      a.inline_patches[2 * i + 1] = patches[i].value;
+    }
+    a.k_new = k_new;
+    a.v_new = v_new;
+    return launch(p, PKV_KERNEL_APPEND, st, [&] { return launch_append(a, st); });
   }
+  // large appends go through the staging ring in chunks of tokens; the first
+  // chunk carries the patches
+  const size_t chunk = size_t(1) << 20;
+  size_t t0 = 0;
+  do {
+    const size_t nt = std::min(chunk, ntok - t0);
+    const size_t np = t0 == 0 ? patches.size() : 0;
+    const size_t slot_off = (np * sizeof(TablePatch) + 255) & ~size_t(255);
+    StagingSlot* s;
+    if (pkv_status r = p->staging.acquire(slot_off + nt * sizeof(int64_t), &s)) return r;
+    if (np) memcpy(s->host, patches.data(), np * sizeof(TablePatch));
+    if (nt) memcpy(s->host + slot_off, slots.data() + t0, nt * sizeof(int64_t));
+    if (pkv_status r = Staging::upload(s, slot_off + nt * sizeof(int64_t), st)) return r;
+    a.n_tokens = (int)nt;
+    a.n_patches = (int)np;
+    a.patches = (const int32_t*)s->dev;
+    a.slots = (const int64_t*)(s->dev + slot_off);
+    a.k_new = (const char*)k_new + t0 * row_bytes;
+    a.v_new = (const char*)v_new + t0 * row_bytes;
+    if (pkv_status r = launch(p, PKV_KERNEL_APPEND, st, [&] { return launch_append(a, st); })) return r;
+    if (pkv_status r = Staging::release(s, st)) return r;
+    t0 += nt;
+  } while (t0 < ntok);
   return PKV_OK;
 }
 
@@ -1147,53 +1266,14 @@ pkv_status pkv_decode_attn(pkv_pool* p, void* stream, int32_t n, const int32_t* 
     return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
   if (plan.n_partials > 0 && ((uintptr_t)workspace & 15))
     return fail(PKV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
-  const size_t wb_bytes = plan.warp_begin.size() * sizeof(int32_t);
-  const size_t pieces_off = (wb_bytes + 31) & ~size_t(31);
-  const size_t comb_off = pieces_off + plan.pieces.size() * sizeof(Piece);
-  const size_t bytes = comb_off + plan.combine.size() * sizeof(CombineItem);
+  const PlanLayout L = plan_layout(plan, p->tc_warps_per_cta, 0);
   StagingSlot* s;
-  if (pkv_status r = p->staging.acquire(bytes, &s)) return r;
-  memcpy(s->host, plan.warp_begin.data(), wb_bytes);
-  if (!plan.pieces.empty()) memcpy(s->host + pieces_off, plan.pieces.data(), plan.pieces.size() * sizeof(Piece));
-  if (!plan.combine.empty())
-    memcpy(s->host + comb_off, plan.combine.data(), plan.combine.size() * sizeof(CombineItem));
-  if (pkv_status r = Staging::upload(s, bytes, st)) return r;
-  if (plan.total_warps > 0) {
-    DecodeTCParams prm;
-    prm.tmap_k = p->tmap_k;
-    prm.tmap_v = p->tmap_v;
-    prm.k_scale = p->buf.k_scale;
-    prm.v_scale = p->buf.v_scale;
-    prm.tables = p->buf.block_tables;
-    prm.max_blocks = c.max_blocks_per_seq;
-    prm.num_blocks = c.num_blocks;
-    prm.n_heads = c.n_heads;
-    prm.n_kv_heads = c.n_kv_heads;
-    prm.q = q;
-    prm.out = out;
-    prm.lse = lse;
-    prm.logits = logits;
-    prm.logits_stride = logits_stride;
-    prm.pieces = (const Piece*)(s->dev + pieces_off);
-    prm.warp_begin = (const int32_t*)s->dev;
-    prm.total_warps = plan.total_warps;
-    prm.partials = (float*)workspace;
-    prm.scale = scale;
-    prm.mask_mode = mode;
-    prm.num_sinks = S;
-    prm.window = W;
-    prm.status = p->buf.status;
-    const int ctas = ceil_div(plan.total_warps, p->tc_warps_per_cta);
-    if (pkv_status r = launch(p, PKV_KERNEL_DECODE, st, [&] { return launch_decode_tc(c.kv_dtype, p->G, prm, ctas, st); }))
-      return r;
-  }
-  if (!plan.combine.empty()) {
-    if (pkv_status r = launch(p, PKV_KERNEL_COMBINE, st, [&] {
-          return launch_combine((const CombineItem*)(s->dev + comb_off), (int)plan.combine.size(),
-                                (const float*)workspace, p->G, c.head_dim, c.n_heads, 1, out, lse, st);
-        }))
-      return r;
-  }
+  if (pkv_status r = p->staging.acquire(L.bytes, &s)) return r;
+  plan_write(plan, L, s->host);
+  if (pkv_status r = Staging::upload(s, L.bytes, st)) return r;
+  if (pkv_status r = launch_tc_plan(p, st, plan, L, s->dev, q, scale, mode, S, W, out, lse, logits, logits_stride,
+                                    workspace))
+    return r;
   return Staging::release(s, st);
 }
 
@@ -1276,9 +1356,9 @@ pkv_status pkv_sync_status(pkv_pool* p, void* stream) {
   return PKV_OK;
 }
 
-pkv_status pkv_timing_enable(pkv_pool* p, int32_t enable) {
+pkv_status pkv_timing_enable(pkv_pool* p, int32_t kernel_mask) {
   if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
-  p->timing.enabled = enable != 0 && p->device;
+  p->timing.mask = p->device ? kernel_mask : 0;
   return PKV_OK;
 }
 

@@ -100,3 +100,85 @@ def lse_err(a: torch.Tensor, b: np.ndarray) -> float:
     with np.errstate(invalid="ignore"):
         d = np.where(both_inf, 0.0, np.abs(x - b))
     return float(d.max()) if d.size else 0.0
+
+
+def pool_bytes_equal(tw: Twin, ids, every: int = 1):
+    """K/V bytes (and FP8 scales) of written slots equal the oracle's, for
+    every `every`-th block of each sequence."""
+    c = tw.cache
+    NB, Hk = tw.pool.NB, tw.wl.n_kv_heads
+    pairs = [(c.k_pool, tw.pool.k), (c.v_pool, tw.pool.v)]
+    if tw.wl.kv_dtype == "fp8":
+        pairs += [(c.k_scale, tw.pool.k_scale), (c.v_scale, tw.pool.v_scale)]
+    for dt, ht in pairs:
+        d = dt.view(torch.uint8).reshape(NB, Hk, 16, -1) if dt.dtype != torch.uint8 else dt.reshape(NB, Hk, 16, -1)
+        h = ht.view(np.uint8).reshape(NB, Hk, 16, -1)
+        for s in ids:
+            L = tw.alloc.length(s)
+            t = tw.alloc.table(s)
+            sel = [lb for lb in range(0, len(t), every) if t[lb] >= 0]
+            if not sel:
+                continue
+            blks = torch.tensor([int(t[lb]) for lb in sel], dtype=torch.long, device=d.device)
+            got = d.index_select(0, blks).cpu().numpy()
+            for i, lb in enumerate(sel):
+                n = min(16, L - 16 * lb)
+                assert np.array_equal(got[i, :, :n], h[t[lb], :, :n]), (s, lb, int(t[lb]))
+
+
+def build_streaming(wl: workloads.Workload, device="cuda", chunk: int = 4096):
+    """Sequences of logical length L that hold only the blocks intersecting
+    the sink + window keep-set: block 0 and the window are real seeded data,
+    the middle is zero filler appended in chunks and evicted as it leaves the
+    window (the oracle replays the same operations; filler is not mirrored)."""
+    S, W = wl.num_sinks, wl.window
+    per_seq = 1 + (W + 15) // 16 + 2 + chunk // 16 + 2
+    maxb = max((L + 15) // 16 for L in wl.lens) + 4
+    tw = Twin(wl, len(wl.lens) * per_seq + 64, len(wl.lens), maxb, seed=wl.seed, device=device)
+    zc = torch.zeros((1, chunk, wl.n_kv_heads, wl.head_dim), dtype=torch.bfloat16)
+    zd = zc.to(tw.dev)
+    ids = []
+    for b, L in enumerate(wl.lens):
+        s = tw.add()
+        ids.append(s)
+        tail = (L - W) // 16 * 16 if L > S + W else 0
+        if tail < 32:
+            k, v = workloads.kv_rows(wl, b, 0, L)
+            tw.append([s], k[None], v[None])
+            continue
+        k, v = workloads.kv_rows(wl, b, 0, 16)
+        tw.append([s], k[None], v[None])
+        pos = 16
+        while pos < tail:
+            n = min(chunk, tail - pos)
+            tw.append([s], zc[:, :n], zc[:, :n], k_dev=zd[:, :n], v_dev=zd[:, :n], mirror=False)
+            pos += n
+            tw.evict(s, S, W)
+        k, v = workloads.kv_rows(wl, b, tail, L - tail)
+        tw.append([s], k[None], v[None])
+        tw.evict(s, S, W)
+    return tw, ids
+
+
+def build_prefix(wl: workloads.Workload, device="cuda", fork_parents: bool = True):
+    """Groups sharing a 2048-token prefix through refcounted blocks; each
+    parent adds a private suffix and (by default) is forked once."""
+    ex = wl.extra
+    groups, ppg, prefix = ex["groups"], ex["parents_per_group"], ex["prefix"]
+    need = groups * (prefix // 16) + sum((s + 15) // 16 + 1 for s in ex["suffix"]) * 2 + 64
+    maxb = max((L + 15) // 16 for L in wl.lens) + 4
+    tw = Twin(wl, need, 2 * groups * ppg + groups, maxb, seed=wl.seed, device=device)
+    parents = []
+    for gi in range(groups):
+        holder = tw.add()
+        k, v = workloads.kv_rows(wl, 10_000 + gi, 0, prefix)
+        tw.append([holder], k[None], v[None])
+        kids = [tw.fork(holder) for _ in range(ppg)]
+        tw.free(holder)
+        for j, s in enumerate(kids):
+            pidx = gi * ppg + j
+            k, v = workloads.kv_rows(wl, pidx, prefix, ex["suffix"][pidx])
+            tw.append([s], k[None], v[None])
+        parents += kids
+    ids = sorted(parents + [tw.fork(p) for p in parents]) if fork_parents else sorted(parents)
+    return tw, ids

@@ -188,3 +188,27 @@ def test_workload_sized_pool_tables_match_oracle(pkv):
     with pytest.raises(pkv.PKVError) as e:
         lib.reserve_slots([0], 16)
     assert e.value.status == 3
+
+
+def test_truncate_many_matches_single_truncates(pkv):
+    rng = random.Random(77)
+    lib = pkv.PagedKVCache(200, 4, 2, 64, 8, 40, kv_dtype="fp32", alloc_seed=3, host_only=True)
+    ora = oracle.OracleAllocator(200, 8, 40, seed=3)
+    ids = [lib.seq_add() for _ in range(6)]
+    for s in ids:
+        assert ora.seq_add() == s
+        L = rng.randint(1, 300)
+        lib.reserve_slots([s], L)
+        ora.append([s], L)
+    ids.append(lib.seq_fork(ids[0]))
+    assert ora.fork(ids[0]) == ids[-1]
+    new = [rng.randint(0, lib.seq_len(s)) for s in ids]
+    lib.seq_truncate_many(ids, new)
+    for s, L in zip(ids, new):
+        ora.truncate(s, L)
+    for s in ids:
+        assert np.array_equal(lib.block_table(s), ora.table(s))
+    assert lib.stats()["free_blocks"] == ora.num_free()
+    with pytest.raises(pkv.PKVError):  # duplicates are refused before anything changes
+        lib.seq_truncate_many([ids[0], ids[0]], [0, 0])
+    assert lib.seq_len(ids[0]) == new[0]
