@@ -362,6 +362,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=0, help="run N untimed steps and exit (for ncu)")
+    ap.add_argument("--time-kernels", action="store_true",
+                    help="bracket every kernel (not only decode) with events; adds gaps to the step")
     args = ap.parse_args()
 
     wl = workloads.ALL[args.workload]()
@@ -400,7 +402,7 @@ def main():
     clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     time.sleep(0.3)
     # ---- device-resident timed region (kernel timing events on) ----
-    setup.cache.timing_enable(["decode"])
+    setup.cache.timing_enable(True if args.time_kernels else ["decode"])
     setup.cache.timing_read()
     launches0 = setup.cache.launch_count()
     barrier(ws)
@@ -504,6 +506,8 @@ def main():
                      "achieved_unique": round(unique / (dec_avg * 1e-3) / 1e9, 2) if unique and dec_n else None,
                      "algorithmic_bytes_per_launch": step_bytes, "avg_launch_ms": round(dec_avg, 5)},
         "decode_share_of_step": decode_share,
+        "kernel_ms_per_step": {k: round(v[0] / args.steps, 5) for k, v in ktimes.items() if v[1]}
+        if args.time_kernels else None,
         "unique_kv_bytes_per_step": unique,
         "value_unique_gbs": round(ws * unique / (ms_step * 1e-3) / 1e9, 2) if unique else None,
         "gpu_launches": launches,

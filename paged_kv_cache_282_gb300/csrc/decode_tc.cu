@@ -53,14 +53,14 @@ template <int KV>
 struct TC;
 template <>
 struct TC<1> {  // BF16
-  static constexpr int kWarps = 8, kStages = 3;
+  static constexpr int kWarps = 12, kStages = 2;
   static constexpr int kStageBytes = 8192;  // K: 2 swizzled boxes of 2 KB, V: same
   static constexpr int kScaleBytes = 0;
   static constexpr uint32_t kTxBytes = 8192;
 };
 template <>
 struct TC<2> {  // FP8 E4M3: half-size units, so twice the warps to keep enough in flight
-  static constexpr int kWarps = 16, kStages = 3;
+  static constexpr int kWarps = 16, kStages = 2;
   static constexpr int kStageBytes = 4096;  // K: one swizzled box of 2 KB, V: same
   static constexpr int kScaleBytes = 128;   // 16 K scales + 16 V scales
   static constexpr uint32_t kTxBytes = 4096 + 128;

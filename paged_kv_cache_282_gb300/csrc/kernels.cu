@@ -157,9 +157,20 @@ __global__ void h2o_score_kernel(const SeqRow* __restrict__ rows, int n_heads, i
   const int j = keep_pos(k, L, mode, S, W);
   const int G = n_heads / n_kv_heads;
   float sum = 0.0f;
-  for (int g = 0; g < n_kv_heads; ++g) {
-    const float* lg = logits + (((size_t)b * n_kv_heads + g) * stride + j) * G;
-    for (int i = 0; i < G; ++i) sum += expf(lg[i] - s_lse[g * G + i]);
+  if ((G & 3) == 0 && ((reinterpret_cast<uintptr_t>(logits) | (uintptr_t)(stride * G * 4)) & 15) == 0) {
+    for (int g = 0; g < n_kv_heads; ++g) {
+      const float4* lg = reinterpret_cast<const float4*>(logits + (((size_t)b * n_kv_heads + g) * stride + j) * G);
+      for (int i = 0; i < G / 4; ++i) {
+        const float4 x = lg[i];
+        const float* ls = s_lse + g * G + 4 * i;
+        sum += __expf(x.x - ls[0]) + __expf(x.y - ls[1]) + __expf(x.z - ls[2]) + __expf(x.w - ls[3]);
+      }
+    }
+  } else {
+    for (int g = 0; g < n_kv_heads; ++g) {
+      const float* lg = logits + (((size_t)b * n_kv_heads + g) * stride + j) * G;
+      for (int i = 0; i < G; ++i) sum += __expf(lg[i] - s_lse[g * G + i]);
+    }
   }
   acc[(size_t)b * acc_stride + j] += sum / (float)n_heads;
 }
@@ -209,8 +220,8 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
                                                                  const float* __restrict__ acc, int64_t acc_stride,
                                                                  int budget, int recent, int32_t* __restrict__ keep_idx,
                                                                  int64_t keep_stride, int32_t* __restrict__ keep_count) {
-  constexpr int kUnroll = 8;  // independent loads in flight per thread
-  constexpr int kPerThread = 4;  // contiguous keys per thread in the ordered pass
+  constexpr int kUnroll = 16;     // independent loads in flight per thread
+  constexpr int kPerThread = 16;  // contiguous keys per thread in the ordered pass
   __shared__ uint32_t hist[256];
   __shared__ int s_warp[32];
   __shared__ uint32_t s_prefix, s_mask;
@@ -225,7 +236,6 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
     return;
   }
   const int n = L - recent, keep = budget - recent;  // n > keep here
-  const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     s_prefix = 0;
     s_mask = 0;
@@ -237,6 +247,10 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
       for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
       __syncthreads();
       const uint32_t prefix = s_prefix, mask = s_mask;
+      // Each thread counts runs of equal digits and adds a run to the shared
+      // histogram only when its digit changes: scores are often equal (zero
+      // outside the keep-set), and one shared bin would serialise the atomics.
+      uint32_t run_digit = 256u, run = 0u;
       for (int base = 0; base < n; base += kUnroll * kSelThreads) {
         uint32_t key[kUnroll];
 #pragma unroll
@@ -247,14 +261,19 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
           const int j = base + u * kSelThreads + threadIdx.x;
-          const bool match = j < n && (key[u] & mask) == prefix;
-          // lanes with the same digit add their count once (scores are often
-          // equal, e.g. zero outside the keep-set, and would all hit one bin)
-          const uint32_t digit = match ? ((key[u] >> shift) & 255u) : 256u;
-          const unsigned same = __match_any_sync(kFull, digit);
-          if (match && lane == __ffs(same) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(same));
+          if (j < n && (key[u] & mask) == prefix) {
+            const uint32_t digit = (key[u] >> shift) & 255u;
+            if (digit == run_digit) {
+              ++run;
+            } else {
+              if (run) atomicAdd(&hist[run_digit], run);
+              run_digit = digit;
+              run = 1u;
+            }
+          }
         }
       }
+      if (run) atomicAdd(&hist[run_digit], run);
       __syncthreads();
       if (threadIdx.x == 0) {
         int k = s_k;

@@ -578,8 +578,10 @@ void build_plan(const pkv_pool* p, int32_t n, const int32_t* ids, int mode, int 
           parts.push_back(pt);
         }
       }
+    // every warp gets the same number of parts (rounds), or one fewer
     const int64_t P = (int64_t)parts.size();
-    const int TW = (int)std::min<int64_t>(TWmax, P);
+    const int64_t rounds = P > 0 ? (P + TWmax - 1) / TWmax : 0;
+    const int TW = rounds > 0 ? (int)((P + rounds - 1) / rounds) : 0;
     plan.total_warps = TW;
     for (int w = 0; w < TW; ++w) {
       const int64_t a = P * w / TW, e = P * (w + 1) / TW;
