@@ -216,16 +216,134 @@ __device__ int block_excl_scan(int v, int* excl, int* s_warp) {
   return total;
 }
 
+constexpr int kSelUnroll = 16;     // keys per thread per sweep (independent loads)
+constexpr int kSelCap = 16384;      // shared-memory candidates of the two-pass path
+
+struct SelShared {
+  uint32_t hist[256];
+  int warp[32];
+  uint32_t prefix, mask;
+  int k, n_cand, top;
+};
+
+// Histogram of digit (key >> shift) & 255 over the keys i < m whose bits under
+// `mask` equal `prefix`.  Each thread counts runs of equal digits and adds a
+// run to the shared histogram only when its digit changes: scores are often
+// equal (zero outside the keep-set), and one shared bin would serialise.
+template <class KeyAt>
+__device__ void digit_histogram(KeyAt key_at, int m, uint32_t prefix, uint32_t mask, int shift, SelShared& sh) {
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) sh.hist[i] = 0;
+  __syncthreads();
+  uint32_t run_digit = 256u, run = 0u;
+  for (int base = 0; base < m; base += kSelUnroll * kSelThreads) {
+    uint32_t key[kSelUnroll];
+#pragma unroll
+    for (int u = 0; u < kSelUnroll; ++u) {
+      const int i = base + u * kSelThreads + threadIdx.x;
+      key[u] = i < m ? key_at(i) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kSelUnroll; ++u) {
+      const int i = base + u * kSelThreads + threadIdx.x;
+      if (i < m && (key[u] & mask) == prefix) {
+        const uint32_t digit = (key[u] >> shift) & 255u;
+        if (digit == run_digit) {
+          ++run;
+        } else {
+          if (run) atomicAdd(&sh.hist[run_digit], run);
+          run_digit = digit;
+          run = 1u;
+        }
+      }
+    }
+  }
+  if (run) atomicAdd(&sh.hist[run_digit], run);
+  __syncthreads();
+}
+
+// Exact keep-th largest key among keys i < m (radix select, 8 bits a pass):
+// on return sh.prefix is that key and sh.k the number of keys equal to it
+// that belong to the selection (the lowest positions among them).
+template <class KeyAt>
+__device__ void radix_select(KeyAt key_at, int m, int keep, SelShared& sh) {
+  if (threadIdx.x == 0) {
+    sh.prefix = 0;
+    sh.mask = 0;
+    sh.k = keep;
+  }
+  __syncthreads();
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    const uint32_t prefix = sh.prefix, mask = sh.mask;
+    digit_histogram(key_at, m, prefix, mask, shift, sh);
+    if (threadIdx.x == 0) {
+      int k = sh.k;
+      for (int dgt = 255; dgt >= 0; --dgt) {
+        const int c = (int)sh.hist[dgt];
+        if (c >= k) {
+          sh.prefix = prefix | ((uint32_t)dgt << shift);
+          sh.mask = mask | (255u << shift);
+          break;
+        }
+        k -= c;
+      }
+      sh.k = k;
+    }
+    __syncthreads();
+  }
+}
+
+// Writes, in ascending order, the positions of the keys i < m that are above
+// T, plus the first need_eq keys equal to T; keys are visited in the order of
+// i, which must be the order of positions.
+template <class KeyAt, class PosAt>
+__device__ void ordered_emit(KeyAt key_at, PosAt pos_at, int m, uint32_t T, int need_eq, int32_t* out,
+                             SelShared& sh) {
+  int taken = 0, eq_seen = 0;
+  for (int base = 0; base < m; base += kSelUnroll * kSelThreads) {
+    const int i0 = base + kSelUnroll * threadIdx.x;
+    uint32_t key[kSelUnroll];
+    int n_gt = 0, n_eq = 0;
+#pragma unroll
+    for (int u = 0; u < kSelUnroll; ++u) {
+      key[u] = i0 + u < m ? key_at(i0 + u) : 0u;
+      n_gt += (i0 + u < m && key[u] > T);
+      n_eq += (i0 + u < m && key[u] == T);
+    }
+    int eq_excl;
+    const int eq_tot = block_excl_scan(n_eq, &eq_excl, sh.warp);
+    int rank = eq_seen + eq_excl, n_sel = n_gt;
+#pragma unroll
+    for (int u = 0; u < kSelUnroll; ++u)
+      if (i0 + u < m && key[u] == T) n_sel += rank++ < need_eq;
+    int sel_excl;
+    const int sel_tot = block_excl_scan(n_sel, &sel_excl, sh.warp);
+    int pos = taken + sel_excl;
+    rank = eq_seen + eq_excl;
+#pragma unroll
+    for (int u = 0; u < kSelUnroll; ++u) {
+      if (i0 + u >= m) continue;
+      const bool sel = key[u] > T || (key[u] == T && rank++ < need_eq);
+      if (sel) out[pos++] = pos_at(i0 + u);
+    }
+    taken += sel_tot;
+    eq_seen += eq_tot;
+  }
+}
+
+// One CTA per sequence.  Two passes over the scores in global memory: a
+// histogram of the top byte finds the smallest top-byte bucket that, with
+// the buckets above it, holds at least `keep` keys; those candidates are
+// gathered, in position order, into shared memory, where the exact radix
+// select and the ordered output run.  If the candidates do not fit, the
+// select and the output run over global memory instead.
 __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* __restrict__ rows,
                                                                  const float* __restrict__ acc, int64_t acc_stride,
                                                                  int budget, int recent, int32_t* __restrict__ keep_idx,
                                                                  int64_t keep_stride, int32_t* __restrict__ keep_count) {
-  constexpr int kUnroll = 16;     // independent loads in flight per thread
-  constexpr int kPerThread = 16;  // contiguous keys per thread in the ordered pass
-  __shared__ uint32_t hist[256];
-  __shared__ int s_warp[32];
-  __shared__ uint32_t s_prefix, s_mask;
-  __shared__ int s_k;
+  __shared__ SelShared sh;
+  extern __shared__ uint32_t cand[];  // kSelCap keys, then kSelCap positions
+  uint32_t* c_key = cand;
+  int32_t* c_pos = reinterpret_cast<int32_t*>(cand + kSelCap);
   const SeqRow row = rows[blockIdx.x];
   const int b = row.q_row, L = row.ctx_len;
   const float* a = acc + (size_t)b * acc_stride;
@@ -236,97 +354,62 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
     return;
   }
   const int n = L - recent, keep = budget - recent;  // n > keep here
-  if (threadIdx.x == 0) {
-    s_prefix = 0;
-    s_mask = 0;
-    s_k = keep;
-  }
-  __syncthreads();
   if (keep > 0) {
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
-      __syncthreads();
-      const uint32_t prefix = s_prefix, mask = s_mask;
-      // Each thread counts runs of equal digits and adds a run to the shared
-      // histogram only when its digit changes: scores are often equal (zero
-      // outside the keep-set), and one shared bin would serialise the atomics.
-      uint32_t run_digit = 256u, run = 0u;
-      for (int base = 0; base < n; base += kUnroll * kSelThreads) {
-        uint32_t key[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          const int j = base + u * kSelThreads + threadIdx.x;
-          key[u] = j < n ? order_key(a[j]) : 0u;
-        }
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          const int j = base + u * kSelThreads + threadIdx.x;
-          if (j < n && (key[u] & mask) == prefix) {
-            const uint32_t digit = (key[u] >> shift) & 255u;
-            if (digit == run_digit) {
-              ++run;
-            } else {
-              if (run) atomicAdd(&hist[run_digit], run);
-              run_digit = digit;
-              run = 1u;
-            }
-          }
+    auto global_key = [a](int i) { return order_key(a[i]); };
+    auto global_pos = [](int i) { return i; };
+    // pass 1: top-byte histogram and the candidate bucket
+    digit_histogram(global_key, n, 0u, 0u, 24, sh);
+    if (threadIdx.x == 0) {
+      int cum = 0, top = 0;
+      for (int dgt = 255; dgt >= 0; --dgt) {
+        cum += (int)sh.hist[dgt];
+        if (cum >= keep) {
+          top = dgt;
+          break;
         }
       }
-      if (run) atomicAdd(&hist[run_digit], run);
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        int k = s_k;
-        for (int dgt = 255; dgt >= 0; --dgt) {
-          const int c = (int)hist[dgt];
-          if (c >= k) {
-            s_prefix = prefix | ((uint32_t)dgt << shift);
-            s_mask = mask | (255u << shift);
-            break;
-          }
-          k -= c;
-        }
-        s_k = k;  // rank still needed among keys sharing the new prefix
-      }
-      __syncthreads();
+      sh.top = top;
+      sh.n_cand = cum;
     }
-  }
-  const uint32_t T = s_prefix;
-  const int need_eq = s_k;  // equal-to-T keys to take, lowest positions first
-  int taken = 0, eq_seen = 0;
-  if (keep > 0) {
-    for (int base = 0; base < n; base += kPerThread * kSelThreads) {
-      const int j0 = base + kPerThread * threadIdx.x;
-      uint32_t key[kPerThread];
-      int n_gt = 0, n_eq = 0;
+    __syncthreads();
+    const uint32_t lo_key = (uint32_t)sh.top << 24;
+    const int m = sh.n_cand;
+    if (m <= kSelCap) {
+      // pass 2: gather the candidates in position order
+      int filled = 0;
+      for (int base = 0; base < n; base += kSelUnroll * kSelThreads) {
+        const int j0 = base + kSelUnroll * threadIdx.x;
+        uint32_t key[kSelUnroll];
+        int c = 0;
 #pragma unroll
-      for (int u = 0; u < kPerThread; ++u) {
-        key[u] = j0 + u < n ? order_key(a[j0 + u]) : 0u;
-        n_gt += (j0 + u < n && key[u] > T);
-        n_eq += (j0 + u < n && key[u] == T);
-      }
-      int eq_excl;
-      const int eq_tot = block_excl_scan(n_eq, &eq_excl, s_warp);
-      int rank = eq_seen + eq_excl, n_sel = n_gt;
-      bool sel[kPerThread];
-#pragma unroll
-      for (int u = 0; u < kPerThread; ++u) {
-        const bool valid = j0 + u < n;
-        const bool is_eq = valid && key[u] == T;
-        sel[u] = (valid && key[u] > T) || (is_eq && rank < need_eq);
-        if (is_eq) {
-          n_sel += rank < need_eq;
-          ++rank;
+        for (int u = 0; u < kSelUnroll; ++u) {
+          key[u] = j0 + u < n ? order_key(a[j0 + u]) : 0u;
+          c += (j0 + u < n && key[u] >= lo_key);
         }
-      }
-      int sel_excl;
-      const int sel_tot = block_excl_scan(n_sel, &sel_excl, s_warp);
-      int pos = taken + sel_excl;
+        int excl;
+        const int tot = block_excl_scan(c, &excl, sh.warp);
+        int w = filled + excl;
 #pragma unroll
-      for (int u = 0; u < kPerThread; ++u)
-        if (sel[u]) out[pos++] = j0 + u;
-      taken += sel_tot;
-      eq_seen += eq_tot;
+        for (int u = 0; u < kSelUnroll; ++u)
+          if (j0 + u < n && key[u] >= lo_key) {
+            c_key[w] = key[u];
+            c_pos[w] = j0 + u;
+            ++w;
+          }
+        filled += tot;
+      }
+      __syncthreads();
+      auto smem_key = [c_key](int i) { return c_key[i]; };
+      auto smem_pos = [c_pos](int i) { return c_pos[i]; };
+      radix_select(smem_key, m, keep, sh);
+      const uint32_t T = sh.prefix;
+      const int need_eq = sh.k;
+      ordered_emit(smem_key, smem_pos, m, T, need_eq, out, sh);
+    } else {
+      radix_select(global_key, n, keep, sh);
+      const uint32_t T = sh.prefix;
+      const int need_eq = sh.k;
+      ordered_emit(global_key, global_pos, n, T, need_eq, out, sh);
     }
   }
   for (int i = threadIdx.x; i < recent; i += blockDim.x) out[keep + i] = n + i;
@@ -439,8 +522,15 @@ cudaError_t launch_h2o_select(const SeqRow* rows, int n_seqs, const float* acc, 
                               int recent, int32_t* keep_idx, int64_t keep_stride, int32_t* keep_count,
                               cudaStream_t st) {
   if (n_seqs <= 0) return cudaSuccess;
-  h2o_select_kernel<<<n_seqs, kSelThreads, 0, st>>>(rows, acc, acc_stride, budget, recent, keep_idx, keep_stride,
-                                                     keep_count);
+  static bool attr_set = false;
+  const int smem = kSelCap * 8;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(h2o_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  h2o_select_kernel<<<n_seqs, kSelThreads, smem, st>>>(rows, acc, acc_stride, budget, recent, keep_idx, keep_stride,
+                                                        keep_count);
   return cudaGetLastError();
 }
 
