@@ -296,12 +296,19 @@ def dist_info():
 
 
 def reduce_max(x: float, ws: int, dev) -> float:
+    """Maximum of x over the ranks (the slowest rank's time)."""
     if ws == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    on_cpu = dist.get_backend() == "gloo"
+    t = torch.tensor([x], dtype=torch.float64, device="cpu" if on_cpu else dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(ws: int, bytes_per_rank_step: int, ms_per_step_max: float) -> float:
+    """GB/s of the whole job: every rank's bytes over the slowest rank's time."""
+    return ws * bytes_per_rank_step / (ms_per_step_max * 1e-3) / 1e9
 
 
 def barrier(ws):
@@ -468,7 +475,7 @@ def main():
     lens_step = [L + 1 for L in setup.lens]
     step_bytes = setup.algorithmic_bytes(lens_step)
     ms_step = ms_max / args.steps
-    value = ws * step_bytes / (ms_step * 1e-3) / 1e9
+    value = whole_job_rate(ws, step_bytes, ms_step)
     peak, peak_kind = hbm_peak()
     dec_ms, dec_n = ktimes["decode"]
     dec_avg = dec_ms / max(dec_n, 1)

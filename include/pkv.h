@@ -289,6 +289,17 @@ pkv_status pkv_timing_enable(pkv_pool* pool, int32_t kernel_mask);
  * device time (ms) and launch count since the last reset; then resets. */
 pkv_status pkv_timing_read(pkv_pool* pool, double* total_ms_out /* [PKV_KERNEL_COUNT] */,
                            int64_t* launches_out /* [PKV_KERNEL_COUNT] */);
+/* Bound (ns, within [1 ms, 60 s]; default 4 s) of every wait of the decode
+ * kernel on its shared-memory stages.  A wait that runs out sets
+ * PKV_ERR_TIMEOUT in the status word; the warp then drains its own copies in
+ * flight (bounded again) and returns, leaving the context usable. */
+pkv_status pkv_set_wait_limit(pkv_pool* pool, int64_t wait_limit_ns);
+/* Test hook for the bound above: in the next decode on this pool, warp `warp`
+ * of the grid arms its first stage without issuing the copies, so that wait
+ * can only run out.  Outputs of that call are undefined; the status word
+ * reports PKV_ERR_TIMEOUT. */
+pkv_status pkv_test_starve_next_decode(pkv_pool* pool, int32_t warp);
+
 /* Total kernel launches issued by this pool so far (all kernels). */
 pkv_status pkv_launch_count(const pkv_pool* pool, int64_t* out);
 

@@ -55,7 +55,9 @@ def _load():
     with _lock:
         if _lib is not None:
             return _lib
-        lib = ctypes.CDLL(build())
+        # ORACLE_LIB points at another build of pkv_oracle.c (the mutation
+        # tests load deliberately broken copies to show the pins catch them)
+        lib = ctypes.CDLL(os.environ.get("ORACLE_LIB") or build())
         c_int, c_dbl, vp = ctypes.c_int, ctypes.c_double, ctypes.c_void_p
         lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
         lib.oracle_e4m3_decode.restype = c_dbl

@@ -46,7 +46,6 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr uint64_t kTimeoutNs = 4000000000ull;
 constexpr uint64_t kDrainTimeoutNs = 50000000ull;
 
 template <int KV>
@@ -374,6 +373,7 @@ __global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const
       const uint32_t bar = bars + 8 * st;
       const uint32_t dst = data + (uint32_t)(st * C::kStageBytes);
       mbar_expect_tx(bar, C::kTxBytes);
+      if (v == 0 && gw == p.starve_warp) return;  // test hook: this stage never completes
       if (KV == 1) {
         tma_load_2d(dst, &p.tmap_k, 0, row, bar);
         tma_load_2d(dst + 2048, &p.tmap_k, 64, row, bar);
@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const
 
     for (int lb = pc.lblk_begin; lb < pc.lblk_end; ++lb, ++u) {
       const int st = u % S;
-      if (!mbar_wait(bars + 8 * st, (uint32_t)((u / S) & 1), kTimeoutNs)) {
+      if (!mbar_wait(bars + 8 * st, (uint32_t)((u / S) & 1), p.wait_limit_ns)) {
         if (lane == 0) {
           atomicOr(p.status, kStatusTimeout);
           p.status[1] = gw;
@@ -495,8 +495,14 @@ __global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const
 
       // ---- mask, logits out, online softmax (log2 units)
       const int tok0 = lb * kBlock + r, tok1 = tok0 + 8;
-      const bool k0 = kept(tok0, L, p.mask_mode, p.num_sinks, p.window);
-      const bool k1 = kept(tok1, L, p.mask_mode, p.num_sinks, p.window);
+      // most units lie wholly inside the keep-set: their first and last
+      // token decide it, and the per-token test is skipped
+      const bool whole = kept(lb * kBlock, L, p.mask_mode, p.num_sinks, p.window) &&
+                         kept(lb * kBlock + kBlock - 1, L, p.mask_mode, p.num_sinks, p.window) &&
+                         (p.mask_mode != 2 || lb * kBlock + kBlock <= p.num_sinks ||
+                          lb * kBlock >= L - p.window || (long long)L <= (long long)p.num_sinks + p.window);
+      const bool k0 = whole || kept(tok0, L, p.mask_mode, p.num_sinks, p.window);
+      const bool k1 = whole || kept(tok1, L, p.mask_mode, p.num_sinks, p.window);
       const bool h0v = 2 * c < G, h1v = 2 * c + 1 < G;
       if (p.logits != nullptr) {
         float* lg = p.logits + ((size_t)pc.q_row * Hk + g) * p.logits_stride * G;
@@ -512,7 +518,7 @@ __global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const
       // scale nor their V row may reach the arithmetic.
       const float e0 = k0 ? a0 + lv_r : -INFINITY, e1 = k0 ? a1 + lv_r : -INFINITY;
       const float e2 = k1 ? a2 + lv_r8 : -INFINITY, e3 = k1 ? a3 + lv_r8 : -INFINITY;
-      if (__ballot_sync(kFull, !(k0 && k1))) {
+      if (!whole && __ballot_sync(kFull, !(k0 && k1))) {
         // zero the V rows of masked tokens in this warp's stage (0 * NaN = NaN)
         constexpr int kRowBytes = KV == 1 ? 256 : 128;
         constexpr int kChunksPerRow = kRowBytes / 16;

@@ -78,6 +78,8 @@ struct DecodeTCParams {
   float scale;       // natural-unit softmax scale
   int32_t mask_mode, num_sinks, window;
   int32_t* status;
+  uint64_t wait_limit_ns;  // bound of every mbarrier wait
+  int32_t starve_warp;     // >= 0: that warp arms its first stage but issues no copy (wait-expiry test)
 };
 
 struct DecodeF32Params {

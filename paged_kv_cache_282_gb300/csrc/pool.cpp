@@ -286,6 +286,8 @@ struct pkv_pool {
   CUtensorMap tmap_k{}, tmap_v{};
   bool tc_path = false;
   int G = 1;
+  uint64_t wait_limit_ns = 4000000000ull;  // bound of the decode kernel's waits
+  int32_t starve_warp = -1;                // one-shot wait-expiry test hook
 };
 
 namespace {
@@ -747,6 +749,9 @@ pkv_status launch_tc_plan(pkv_pool* p, cudaStream_t st, const Plan& pl, const Pl
   prm.num_sinks = S;
   prm.window = W;
   prm.status = p->buf.status;
+  prm.wait_limit_ns = p->wait_limit_ns;
+  prm.starve_warp = p->starve_warp;
+  p->starve_warp = -1;
   return launch(p, PKV_KERNEL_DECODE, st, [&] { return launch_decode_tc(c.kv_dtype, p->G, prm, pl.ctas, st); });
 }
 
@@ -1380,6 +1385,21 @@ pkv_status pkv_timing_read(pkv_pool* p, double* total_ms, int64_t* launches) {
     launches[k] = (int64_t)p->timing.marks[k].size();
     p->timing.marks[k].clear();
   }
+  return PKV_OK;
+}
+
+pkv_status pkv_set_wait_limit(pkv_pool* p, int64_t wait_limit_ns) {
+  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  if (wait_limit_ns < 1000000 || wait_limit_ns > 60000000000LL)
+    return fail(PKV_ERR_INVALID_ARG, "wait limit must lie in [1 ms, 60 s]");
+  p->wait_limit_ns = (uint64_t)wait_limit_ns;
+  return PKV_OK;
+}
+
+pkv_status pkv_test_starve_next_decode(pkv_pool* p, int32_t warp) {
+  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  if (warp < 0) return fail(PKV_ERR_INVALID_ARG, "warp < 0");
+  p->starve_warp = warp;
   return PKV_OK;
 }
 

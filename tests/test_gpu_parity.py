@@ -9,6 +9,7 @@ import torch
 import oracle
 import workloads
 from harness import TOL, Twin, fill_sequences, lse_err, max_err
+from paged_kv_cache_282_gb300 import _abi
 
 pytestmark = pytest.mark.gpu
 
@@ -267,3 +268,23 @@ def test_patches_and_cow_chains_in_one_flush():
     # b's last block holds tokens 16..19 in slots 0..3 (the rest is unwritten)
     d = tw.cache.k_pool.view(torch.int16)[dst, :, :4].cpu().numpy().view(np.uint16)
     assert np.array_equal(d, tw.pool.k[dst, :, :4])
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A stage whose copies are never issued makes its bounded wait run out:
+    the kernel returns, the status word reports the expiry, and the next
+    decode on the same context is correct."""
+    wl = workloads.small("bf16", lens=(300, 700), seed=80)
+    tw = Twin(wl, 80, 2, 64, seed=3)
+    ids = fill_sequences(tw, wl.lens)
+    q = workloads.queries(wl)
+    _abi.check(tw.cache.lib.pkv_set_wait_limit(tw.cache.handle, 50_000_000))  # 50 ms
+    _abi.check(tw.cache.lib.pkv_test_starve_next_decode(tw.cache.handle, 0))
+    tw.cache.decode(ids, q.cuda(), scale=wl.scale)
+    with pytest.raises(_abi.PKVError) as e:
+        tw.cache.sync_status()
+    assert e.value.status == 6
+    out, lse = tw.cache.decode(ids, q.cuda(), scale=wl.scale)
+    tw.cache.sync_status()
+    ref, ref_lse, _ = tw.oracle_decode(ids, q)
+    assert max_err(out, ref) <= TOL["bf16"] and lse_err(lse, ref_lse) <= 2e-3
