@@ -264,6 +264,29 @@ pkv_status pkv_h2o_select(pkv_pool* pool, void* stream, int32_t n_seqs, const in
                           const float* acc, int64_t acc_stride, int32_t budget, int32_t recent,
                           int32_t* keep_idx, int64_t keep_stride, int32_t* keep_count);
 
+/* H2O compaction ([LC] H2OEviction keeps only the selected positions; [PA]
+ * 剪枝/淘汰: memory goes from O(seq) to O(budget)).  For each listed sequence,
+ * the counts[i] tokens at positions keep_idx[i][0 .. counts[i]) (ascending,
+ * e.g. the output of pkv_h2o_select) become its whole contents, in that
+ * order, in freshly allocated blocks; the sequence's length becomes counts[i]
+ * and its old blocks are released.  Order: every sequence's fresh blocks are
+ * taken first (list order), then the old blocks are released (list order,
+ * ascending logical order).  acc (device [n_seqs][acc_stride] fp32, or NULL)
+ * is compacted alike: acc[i][j] = acc[i][keep_idx[i][j]] for j < counts[i],
+ * 0 from counts[i] up to the old length.
+ *   keep_idx  device [n_seqs][keep_stride] int32 (keep_stride >= max count)
+ *   counts    host [n_seqs]
+ * keep_idx must be ascending for acc's in-place compaction to be correct.
+ * A position outside [0, old length) or in an evicted block is not copied
+ * and sets the device status word (PKV_ERR_DEVICE_ASSERT at the next
+ * pkv_sync_status).  On a host-only pool only the allocator changes
+ * (keep_idx and acc unused).  PKV_ERR_INVALID_ARG (a sequence listed twice,
+ * a count above the length) or PKV_ERR_OUT_OF_BLOCKS (the fresh blocks do
+ * not fit) leave every state unchanged. */
+pkv_status pkv_seq_compact(pkv_pool* pool, void* stream, int32_t n_seqs, const int32_t* seq_ids,
+                           const int32_t* keep_idx, int64_t keep_stride, const int32_t* counts, float* acc,
+                           int64_t acc_stride);
+
 /* Synchronises `stream`, then reports and clears the device status word:
  * PKV_ERR_TIMEOUT, PKV_ERR_DEVICE_ASSERT or PKV_OK. */
 pkv_status pkv_sync_status(pkv_pool* pool, void* stream);

@@ -77,6 +77,8 @@ def _load():
                                           vp, c_int]
         lib.oracle_h2o_select.argtypes = [c_int, c_int, c_int, vp, vp]
         lib.oracle_h2o_select.restype = c_int
+        lib.oracle_policy_select.argtypes = [c_int, c_int, c_int, c_int, vp, vp]
+        lib.oracle_policy_select.restype = c_int
         lib.oracle_splitmix64.argtypes = [ctypes.c_uint64, c_int, vp]
         lib.oracle_alloc_create.argtypes = [c_int, c_int, c_int, ctypes.c_uint64, vp]
         lib.oracle_alloc_create.restype = vp
@@ -90,6 +92,9 @@ def _load():
             getattr(lib, name).restype = c_int
         lib.oracle_alloc_truncate.argtypes = [vp, c_int, c_int]
         lib.oracle_alloc_truncate.restype = c_int
+        lib.oracle_alloc_compact.argtypes = [vp, c_int, vp, vp, vp]
+        lib.oracle_alloc_compact.restype = c_int
+        lib.oracle_copy_rows.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, vp, vp, c_int]
         lib.oracle_alloc_evict.argtypes = [vp, c_int, c_int, c_int]
         lib.oracle_alloc_evict.restype = c_int
         lib.oracle_alloc_len.argtypes = [vp, c_int]
@@ -214,6 +219,12 @@ class OraclePool:
             lib.oracle_scatter(_ptr(self.k), self.Hk, self.D, es, _ptr(slots), T, _ptr(kb))
             lib.oracle_scatter(_ptr(self.v), self.Hk, self.D, es, _ptr(slots), T, _ptr(vb))
 
+    def copy_rows(self, src_slots, dst_slots) -> None:
+        es = {KV_FP32: 4, KV_BF16: 2, KV_FP8: 1}[self.kv_dtype]
+        src, dst = _c(src_slots, np.int64), _c(dst_slots, np.int64)
+        _load().oracle_copy_rows(_ptr(self.k), _ptr(self.v), _ptr(self.k_scale), _ptr(self.v_scale), self.Hk,
+                                 self.D, es, _ptr(src), _ptr(dst), src.size)
+
     def copy_block(self, src: int, dst: int) -> None:
         es = {KV_FP32: 4, KV_BF16: 2, KV_FP8: 1}[self.kv_dtype]
         _load().oracle_copy_block(_ptr(self.k), _ptr(self.v), _ptr(self.k_scale),
@@ -268,6 +279,15 @@ def h2o_update(acc: np.ndarray, lens: np.ndarray, logits: np.ndarray, lse: np.nd
     lib.oracle_h2o_update(n, H, _ptr(lens), _ptr(logits), lstride, _ptr(lse), mask_mode,
                           num_sinks, window, _ptr(acc), acc.shape[1])
     return acc
+
+
+def policy_select(L: int, sinks: int, window: int, heavy: int, scores: np.ndarray) -> np.ndarray:
+    """The combined sink + recent window + heavy-hitter keep-set (ascending)."""
+    lib = _load()
+    scores = _c(scores, np.float64)
+    out = np.empty(max(L, 1), dtype=np.int32)
+    n = lib.oracle_policy_select(L, sinks, window, heavy, _ptr(scores), _ptr(out))
+    return out[:n].copy()
 
 
 def h2o_select(L: int, budget: int, recent: int, scores: np.ndarray) -> np.ndarray:
@@ -341,6 +361,24 @@ class OracleAllocator:
     def evict(self, s: int, num_sinks: int, window: int) -> None:
         if self._lib.oracle_alloc_evict(self._h, s, num_sinks, window):
             raise ValueError("evict failed")
+
+    def compact(self, seq_ids, counts) -> list:
+        """H2O compaction of the allocator state; returns each sequence's
+        fresh blocks."""
+        ids, cnt = _c(seq_ids, np.int32), _c(counts, np.int32)
+        total = int(sum((int(c) + 15) // 16 for c in cnt))
+        out = np.empty(max(total, 1), dtype=np.int32)
+        r = self._lib.oracle_alloc_compact(self._h, ids.size, _ptr(ids), _ptr(cnt), _ptr(out))
+        if r == -1:
+            raise MemoryError("out of blocks")
+        if r != 0:
+            raise ValueError("invalid compaction")
+        res, pos = [], 0
+        for c in cnt:
+            nb = (int(c) + 15) // 16
+            res.append(out[pos: pos + nb].copy())
+            pos += nb
+        return res
 
     def length(self, s: int) -> int:
         return self._lib.oracle_alloc_len(self._h, s)

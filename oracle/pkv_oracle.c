@@ -236,8 +236,27 @@ void oracle_quantize_scatter(uint8_t* pool, float* scale_pool, int Hk, int D, co
   free(th);
 }
 
+/* Copy rows (all kv heads, K, V and scales) from slot src[t] to slot dst[t]. */
+void oracle_copy_rows(void* k_pool, void* v_pool, float* k_scale, float* v_scale, int Hk, int D, int elem_bytes,
+                      const int64_t* src, const int64_t* dst, int n) {
+  int t, g;
+  for (t = 0; t < n; t++) {
+    int sb = (int)(src[t] / ORACLE_BLOCK), so = (int)(src[t] % ORACLE_BLOCK);
+    int db = (int)(dst[t] / ORACLE_BLOCK), dso = (int)(dst[t] % ORACLE_BLOCK);
+    for (g = 0; g < Hk; g++) {
+      size_t si = pool_index(sb, Hk, g, so, D, 0), di = pool_index(db, Hk, g, dso, D, 0);
+      memcpy((char*)k_pool + di * elem_bytes, (char*)k_pool + si * elem_bytes, (size_t)D * elem_bytes);
+      memcpy((char*)v_pool + di * elem_bytes, (char*)v_pool + si * elem_bytes, (size_t)D * elem_bytes);
+      if (k_scale && v_scale) {
+        k_scale[((size_t)db * Hk + g) * ORACLE_BLOCK + dso] = k_scale[((size_t)sb * Hk + g) * ORACLE_BLOCK + so];
+        v_scale[((size_t)db * Hk + g) * ORACLE_BLOCK + dso] = v_scale[((size_t)sb * Hk + g) * ORACLE_BLOCK + so];
+      }
+    }
+  }
+}
+
 /* Copy one whole physical block (all kv heads, all slots, K, V and scales):
- * [PA] copy_on_write, "new.data.copy_(old.data)". */
+ * [PA] copy-on-write, where the fresh block receives the shared block's data. */
 void oracle_copy_block(void* k_pool, void* v_pool, float* k_scale, float* v_scale, int Hk,
                        int D, int elem_bytes, int src, int dst) {
   size_t blk = (size_t)Hk * ORACLE_BLOCK * D * elem_bytes;
@@ -468,6 +487,37 @@ int oracle_h2o_select(int L, int budget, int recent, const double* scores, int32
     if (chosen[j]) keep_out[n++] = j;
   free(c);
   free(chosen);
+  return n;
+}
+
+/* The combined cache rule ([PA] KV compression, the combination of initial
+ * tokens, a recent window and high-attention tokens, with sink 4, window 256
+ * and 512 - 4 - 256 heavy hitters): position p of a length-L sequence stays
+ * when p < sinks, when p is one of the last `window` positions, or when its
+ * accumulated score is among the `heavy` highest of ALL L positions.
+ * Readings: the ranking spans every position, as the printed rule ranks the
+ * whole score array, so a heavy hitter that is also a sink or recent counts
+ * once and the kept set can be smaller than sinks + window + heavy; ties go
+ * to the lower position.  Result ascending; returns its size. */
+int oracle_policy_select(int L, int sinks, int window, int heavy, const double* scores, int32_t* keep_out) {
+  unsigned char* heavy_hit;
+  scored_pos* c;
+  int j, n = 0;
+  if (L <= 0) return 0;
+  heavy_hit = (unsigned char*)calloc((size_t)L, 1);
+  c = (scored_pos*)malloc(sizeof(scored_pos) * (size_t)L);
+  for (j = 0; j < L; j++) {
+    c[j].score = scores[j];
+    c[j].pos = j;
+  }
+  qsort(c, (size_t)L, sizeof(scored_pos), cmp_desc_score_asc_pos);
+  for (j = 0; j < heavy && j < L; j++) heavy_hit[c[j].pos] = 1;
+  for (j = 0; j < L; j++) {
+    const int is_sink = j < sinks, is_recent = j >= L - window;
+    if (is_sink || is_recent || heavy_hit[j]) keep_out[n++] = j;
+  }
+  free(c);
+  free(heavy_hit);
   return n;
 }
 
@@ -727,6 +777,49 @@ int oracle_alloc_evict(oracle_alloc* a, int s, int num_sinks, int window) {
       *e = -1;
     }
   }
+  return 0;
+}
+
+/* H2O compaction (the cache keeps only the selected tokens): for each listed
+ * sequence, counts[i] fresh blocks' worth of slots are taken from the front
+ * of the free pool (all sequences first, in list order, blocks in logical
+ * order); then every old block of every listed sequence is released (list
+ * order, ascending logical order); the new table is the fresh blocks and the
+ * length is counts[i].  new_blocks receives the fresh ids, concatenated.
+ * Returns 0, -1 when out of blocks (state unchanged), -2 for invalid input. */
+int oracle_alloc_compact(oracle_alloc* a, int n, const int32_t* seq_ids, const int32_t* counts,
+                         int32_t* new_blocks) {
+  oracle_alloc* w;
+  int i, k, total = 0, pos = 0;
+  for (i = 0; i < n; i++) {
+    if (seq_ids[i] < 0 || seq_ids[i] >= a->max_seqs || !a->active[seq_ids[i]]) return -2;
+    if (counts[i] < 0 || counts[i] > a->lens[seq_ids[i]]) return -2;
+    for (k = 0; k < i; k++)
+      if (seq_ids[k] == seq_ids[i]) return -2;
+    total += (counts[i] + ORACLE_BLOCK - 1) / ORACLE_BLOCK;
+  }
+  if (total > a->free_top) return -1;
+  w = alloc_clone(a);
+  for (i = 0; i < n; i++) {
+    int nb = (counts[i] + ORACLE_BLOCK - 1) / ORACLE_BLOCK;
+    for (k = 0; k < nb; k++) new_blocks[pos++] = take_block(w);
+  }
+  for (i = 0; i < n; i++) {
+    int s = seq_ids[i], lb, nold = (w->lens[s] + ORACLE_BLOCK - 1) / ORACLE_BLOCK;
+    for (lb = 0; lb < nold; lb++) {
+      int32_t* e = w->tables + (size_t)s * w->max_blocks + lb;
+      if (*e >= 0) drop_block(w, *e);
+      *e = -1;
+    }
+  }
+  pos = 0;
+  for (i = 0; i < n; i++) {
+    int s = seq_ids[i], nb = (counts[i] + ORACLE_BLOCK - 1) / ORACLE_BLOCK;
+    for (k = 0; k < nb; k++) w->tables[(size_t)s * w->max_blocks + k] = new_blocks[pos++];
+    w->lens[s] = counts[i];
+  }
+  alloc_swap(a, w);
+  oracle_alloc_destroy(w);
   return 0;
 }
 

@@ -237,6 +237,16 @@ class PagedKVCache:
                                            int(acc_stride), budget, recent, keep_idx.data_ptr(), int(keep_stride),
                                            keep_count.data_ptr()))
 
+    def seq_compact(self, seq_ids, counts, keep_idx=None, keep_stride: int = 0, acc=None, acc_stride: int = 0,
+                    stream=None) -> None:
+        """H2O compaction: keep_idx device [n][keep_stride] int32 (ascending
+        positions), counts host; acc optional device scores to compact."""
+        ids, cnt = _i32_array(seq_ids), _i32_array(counts)
+        _abi.check(self.lib.pkv_seq_compact(
+            self._h, None if self.host_only else _stream_ptr(stream), ids.size, _ptr(ids),
+            keep_idx.data_ptr() if keep_idx is not None else None, int(keep_stride), _ptr(cnt),
+            acc.data_ptr() if acc is not None else None, int(acc_stride)))
+
     def sync_status(self, stream=None) -> None:
         _abi.check(self.lib.pkv_sync_status(self._h, _stream_ptr(stream)))
 

@@ -417,6 +417,70 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
 }
 
 // ---------------------------------------------------------------------------
+// H2O compaction: kept tokens move, in order, into fresh blocks (one warp per
+// (token, kv head) row: K, V and the FP8 scales); the score array follows.
+// ---------------------------------------------------------------------------
+
+__global__ void compact_gather_kernel(const CompactSeq* __restrict__ seqs, const int32_t* __restrict__ new_blocks,
+                                      const int32_t* __restrict__ tables, int max_blocks, int num_blocks,
+                                      const int32_t* __restrict__ keep_idx, int64_t keep_stride, int Hk, int row_bytes,
+                                      char* __restrict__ k_pool, char* __restrict__ v_pool,
+                                      float* __restrict__ k_scale, float* __restrict__ v_scale,
+                                      int32_t* __restrict__ status) {
+  const CompactSeq sq = seqs[blockIdx.y];
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = (int64_t)sq.count * Hk;
+  const int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (w >= rows) return;
+  const int i = (int)(w / Hk), g = (int)(w - (int64_t)i * Hk);
+  const int src = keep_idx[(size_t)sq.q_row * keep_stride + i];
+  const int sb = (src >= 0 && src < sq.old_len) ? tables[(size_t)sq.seq_slot * max_blocks + src / kBlock] : -1;
+  if (sb < 0 || sb >= num_blocks) {
+    if (lane == 0) atomicOr(status, kStatusBadBlock);
+    return;
+  }
+  const int db = new_blocks[sq.new_off + i / kBlock];
+  const size_t srow = ((size_t)sb * Hk + g) * kBlock + (src & 15);
+  const size_t drow = ((size_t)db * Hk + g) * kBlock + (i & 15);
+  for (int ch = lane; ch < row_bytes / 16; ch += 32) {
+    reinterpret_cast<uint4*>(k_pool + drow * row_bytes)[ch] = reinterpret_cast<const uint4*>(k_pool + srow * row_bytes)[ch];
+    reinterpret_cast<uint4*>(v_pool + drow * row_bytes)[ch] = reinterpret_cast<const uint4*>(v_pool + srow * row_bytes)[ch];
+  }
+  if (k_scale && lane == 0) {
+    k_scale[drow] = k_scale[srow];
+    v_scale[drow] = v_scale[srow];
+  }
+}
+
+// acc[b][i] = acc[b][keep_idx[i]] for i < count, zero for count <= i < old_len.
+// Kept positions are ascending, so keep_idx[i] >= i: a chunk reads only
+// positions no earlier chunk has written, and reads before it writes.
+__global__ void __launch_bounds__(1024) compact_scores_kernel(const CompactSeq* __restrict__ seqs,
+                                                              const int32_t* __restrict__ keep_idx, int64_t keep_stride,
+                                                              float* __restrict__ acc, int64_t acc_stride) {
+  constexpr int kChunk = 4096;
+  const CompactSeq sq = seqs[blockIdx.x];
+  float* a = acc + (size_t)sq.q_row * acc_stride;
+  const int32_t* k = keep_idx + (size_t)sq.q_row * keep_stride;
+  for (int base = 0; base < sq.count; base += kChunk) {
+    float v[kChunk / 1024];
+#pragma unroll
+    for (int u = 0; u < kChunk / 1024; ++u) {
+      const int i = base + u * 1024 + threadIdx.x;
+      v[u] = i < sq.count ? a[k[i]] : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kChunk / 1024; ++u) {
+      const int i = base + u * 1024 + threadIdx.x;
+      if (i < sq.count) a[i] = v[u];
+    }
+    __syncthreads();
+  }
+  for (int i = sq.count + threadIdx.x; i < sq.old_len; i += blockDim.x) a[i] = 0.0f;
+}
+
+// ---------------------------------------------------------------------------
 // fp32 decode on CUDA cores: one warp per query head, one CTA per
 // (sequence, kv head); online softmax over the kept keys in order.
 // ---------------------------------------------------------------------------
@@ -515,6 +579,29 @@ cudaError_t launch_h2o_score(const SeqRow* rows, int n_seqs, int n_heads, int n_
   dim3 grid((unsigned)((max_keep + 255) / 256), (unsigned)n_seqs);
   h2o_score_kernel<<<grid, 256, n_heads * sizeof(float), st>>>(rows, n_heads, n_kv_heads, logits, stride, lse, mode,
                                                                 S, W, acc, acc_stride);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compact_gather(const CompactSeq* seqs, int n, int max_count, const int32_t* new_blocks,
+                                  const int32_t* tables, int max_blocks, int num_blocks, const int32_t* keep_idx,
+                                  int64_t keep_stride, int Hk, int row_bytes, void* k_pool, void* v_pool, float* k_scale,
+                                  float* v_scale, int32_t* status, cudaStream_t st) {
+  if (n <= 0 || max_count <= 0) return cudaSuccess;
+  const int64_t rows = (int64_t)max_count * Hk;
+  for (int first = 0; first < n; first += 65535) {  // grid.y limit
+    dim3 grid((unsigned)((rows + 7) / 8), (unsigned)std::min(65535, n - first));
+    compact_gather_kernel<<<grid, 256, 0, st>>>(seqs + first, new_blocks, tables, max_blocks, num_blocks, keep_idx,
+                                                keep_stride, Hk, row_bytes, (char*)k_pool, (char*)v_pool, k_scale,
+                                                v_scale, status);
+    if (cudaError_t e = cudaGetLastError()) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_compact_scores(const CompactSeq* seqs, int n, const int32_t* keep_idx, int64_t keep_stride,
+                                  float* acc, int64_t acc_stride, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  compact_scores_kernel<<<n, 1024, 0, st>>>(seqs, keep_idx, keep_stride, acc, acc_stride);
   return cudaGetLastError();
 }
 

@@ -45,6 +45,12 @@ struct EmptyItem {
   int32_t q_row, kv_head;
 };
 
+// One sequence of an H2O compaction: its count kept tokens move, in order,
+// into the fresh blocks new_blocks[new_off ...].
+struct CompactSeq {
+  int32_t seq_slot, q_row, count, new_off, old_len, pad0, pad1, pad2;
+};
+
 // Per-sequence row for kernels that walk one sequence at a time.
 struct SeqRow {
   int32_t seq_slot, q_row, ctx_len, pad;
@@ -144,6 +150,13 @@ cudaError_t launch_h2o_score(const SeqRow* rows, int n_seqs, int n_heads, int n_
                              const float* logits, int64_t logits_stride, const float* lse,
                              int mask_mode, int num_sinks, int window, float* acc,
                              int64_t acc_stride, int max_keep, cudaStream_t stream);
+
+cudaError_t launch_compact_gather(const CompactSeq* seqs, int n, int max_count, const int32_t* new_blocks,
+                                  const int32_t* tables, int max_blocks, int num_blocks, const int32_t* keep_idx,
+                                  int64_t keep_stride, int Hk, int row_bytes, void* k_pool, void* v_pool, float* k_scale,
+                                  float* v_scale, int32_t* status, cudaStream_t stream);
+cudaError_t launch_compact_scores(const CompactSeq* seqs, int n, const int32_t* keep_idx, int64_t keep_stride,
+                                  float* acc, int64_t acc_stride, cudaStream_t stream);
 
 cudaError_t launch_h2o_select(const SeqRow* rows, int n_seqs, const float* acc, int64_t acc_stride,
                               int budget, int recent, int32_t* keep_idx, int64_t keep_stride,

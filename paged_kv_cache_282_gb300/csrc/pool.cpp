@@ -1203,6 +1203,81 @@ pkv_status pkv_append(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, 
   return PKV_OK;
 }
 
+pkv_status pkv_seq_compact(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, const int32_t* keep_idx,
+                           int64_t keep_stride, const int32_t* counts, float* acc, int64_t acc_stride) {
+  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  if (pkv_status r = check_seq_list(p, n, ids)) return r;
+  if (n > 0 && !counts) return fail(PKV_ERR_INVALID_ARG, "counts is NULL");
+  auto& A = p->alloc;
+  int64_t need = 0;
+  int32_t max_count = 0, max_len = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    for (int32_t j = 0; j < i; ++j)
+      if (ids[j] == ids[i]) return fail(PKV_ERR_INVALID_ARG, "sequence %d listed twice", ids[i]);
+    if (counts[i] < 0 || counts[i] > A.len[ids[i]])
+      return fail(PKV_ERR_INVALID_ARG, "count %d outside [0, %d]", counts[i], A.len[ids[i]]);
+    need += ceil_div(counts[i], kBlock);
+    max_count = std::max(max_count, counts[i]);
+    max_len = std::max(max_len, A.len[ids[i]]);
+  }
+  if (p->device) {
+    if (max_count > 0 && (!keep_idx || keep_stride < max_count))
+      return fail(PKV_ERR_INVALID_ARG, "keep_idx is NULL or keep_stride < largest count");
+    if (acc && acc_stride < max_len) return fail(PKV_ERR_INVALID_ARG, "acc_stride < length");
+  }
+  if (need > (int64_t)A.free_blocks.size())
+    return fail(PKV_ERR_OUT_OF_BLOCKS, "compaction needs %lld fresh blocks, %zu free", (long long)need,
+                A.free_blocks.size());
+  cudaStream_t st = (cudaStream_t)stream;
+  if (p->device)
+    if (pkv_status r = flush_pending(p, st)) return r;  // the gather reads the current device table
+  // fresh blocks for every sequence first, then release the old ones
+  std::vector<CompactSeq> seqs(n);
+  std::vector<int32_t> fresh;
+  fresh.reserve(need);
+  for (int32_t i = 0; i < n; ++i) {
+    seqs[i] = {ids[i], i, counts[i], (int32_t)fresh.size(), A.len[ids[i]], 0, 0, 0};
+    for (int32_t k = 0; k < ceil_div(counts[i], kBlock); ++k) fresh.push_back(A.take());
+  }
+  StagingSlot* s = nullptr;
+  if (p->device && n > 0) {
+    const size_t seq_bytes = n * sizeof(CompactSeq), off = (seq_bytes + 255) & ~size_t(255);
+    if (pkv_status r = p->staging.acquire(off + fresh.size() * sizeof(int32_t) + 4, &s)) return r;
+    memcpy(s->host, seqs.data(), seq_bytes);
+    if (!fresh.empty()) memcpy(s->host + off, fresh.data(), fresh.size() * sizeof(int32_t));
+    if (pkv_status r = Staging::upload(s, off + fresh.size() * sizeof(int32_t), st)) return r;
+    const auto& c = p->cfg;
+    const int row_bytes = c.head_dim * elem_bytes(c.kv_dtype);
+    const bool fp8 = c.kv_dtype == PKV_KV_FP8_E4M3;
+    if (pkv_status r = launch(p, PKV_KERNEL_COW_COPY, st, [&] {
+          return launch_compact_gather((const CompactSeq*)s->dev, n, max_count, (const int32_t*)(s->dev + off),
+                                       p->buf.block_tables, c.max_blocks_per_seq, c.num_blocks, keep_idx, keep_stride,
+                                       c.n_kv_heads, row_bytes, p->buf.k_pool, p->buf.v_pool,
+                                       fp8 ? p->buf.k_scale : nullptr, fp8 ? p->buf.v_scale : nullptr, p->buf.status,
+                                       st);
+        }))
+      return r;
+  }
+  size_t pos = 0;
+  for (int32_t i = 0; i < n; ++i) A.drop_from(ids[i], 0);  // old blocks, ascending, sequence by sequence
+  for (int32_t i = 0; i < n; ++i) {
+    for (int32_t k = 0; k < ceil_div(counts[i], kBlock); ++k) A.set_entry(ids[i], k, fresh[pos++]);
+    A.len[ids[i]] = counts[i];
+    A.holes[ids[i]] = 0;
+  }
+  if (!p->device) {
+    A.pending_patch.clear();
+    return PKV_OK;
+  }
+  if (pkv_status r = flush_pending(p, st)) return r;  // new tables, after the gather
+  if (acc && n > 0)
+    if (pkv_status r = launch(p, PKV_KERNEL_H2O_SCORE, st, [&] {
+          return launch_compact_scores((const CompactSeq*)s->dev, n, keep_idx, keep_stride, acc, acc_stride, st);
+        }))
+      return r;
+  return s ? Staging::release(s, st) : PKV_OK;
+}
+
 pkv_status pkv_decode_workspace_size(const pkv_pool* p, int32_t n, int32_t num_splits, size_t* bytes_out) {
   if (!p || !bytes_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
   if (n < 0 || num_splits < 0) return fail(PKV_ERR_INVALID_ARG, "negative size");

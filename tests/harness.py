@@ -65,6 +65,26 @@ class Twin:
                             workloads.as_bits(v.reshape(-1, *v.shape[2:])))
         return slots, cow
 
+    def compact(self, seq_ids, keeps, acc=None, acc_stride: int = 0):
+        """H2O compaction on both sides: keeps[i] (ascending positions) become
+        sequence seq_ids[i]'s whole contents.  The oracle moves the same rows
+        through its own allocator and row copy."""
+        seq_ids = list(seq_ids)
+        counts = [len(k) for k in keeps]
+        stride = max([1] + counts)
+        kd = torch.full((len(seq_ids), stride), -1, dtype=torch.int32)
+        for i, k in enumerate(keeps):
+            kd[i, : len(k)] = torch.as_tensor(np.asarray(k, dtype=np.int32))
+        self.cache.seq_compact(seq_ids, counts, kd.to(self.dev), stride, acc, acc_stride)
+        src = []
+        for s, k in zip(seq_ids, keeps):
+            t = self.alloc.table(s)
+            src += [int(t[p // 16]) * 16 + p % 16 for p in k]
+        fresh = self.alloc.compact(seq_ids, counts)
+        dst = [int(f[i // 16]) * 16 + i % 16 for f, c in zip(fresh, counts) for i in range(c)]
+        self.pool.copy_rows(src, dst)
+        return fresh
+
     def tables(self, seq_ids) -> np.ndarray:
         return self.alloc.tables_matrix(list(seq_ids))
 

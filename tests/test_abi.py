@@ -139,11 +139,25 @@ def _replay(pkv, seed):
             lib.seq_free(s)
             ora.free(s)
             live.remove(s)
-        elif r < 0.93:
+        elif r < 0.91:
             s = rng.choice(live)
             S, W = rng.randint(0, 5), rng.randint(1, 40)
             lib.seq_evict(s, S, W)
             ora.evict(s, S, W)
+        elif r < 0.96:
+            ids = rng.sample(live, rng.randint(1, len(live)))
+            counts = [rng.randint(0, lib.seq_len(s)) for s in ids]
+            try:
+                lib.seq_compact(ids, counts)
+                ok = True
+            except pkv.PKVError as e:
+                ok = e.status
+            try:
+                ora.compact(ids, counts)
+                ok2 = True
+            except MemoryError:
+                ok2 = 3
+            assert ok == ok2
         else:
             s = rng.choice(live)
             n = rng.randint(0, lib.seq_len(s))
@@ -168,6 +182,8 @@ def _replay(pkv, seed):
 
 @pytest.mark.parametrize("seed", range(12))
 def test_allocator_matches_oracle_replay(pkv, seed):
+    """Random adds, appends (with copy-on-write), forks, frees, evictions,
+    H2O compactions and truncations, the same on both sides."""
     _replay(pkv, seed)
 
 
@@ -212,3 +228,21 @@ def test_truncate_many_matches_single_truncates(pkv):
     with pytest.raises(pkv.PKVError):  # duplicates are refused before anything changes
         lib.seq_truncate_many([ids[0], ids[0]], [0, 0])
     assert lib.seq_len(ids[0]) == new[0]
+
+
+def test_compaction_refusals_leave_state_unchanged(pkv):
+    lib = pkv.PagedKVCache(10, 4, 2, 64, 4, 8, kv_dtype="fp32", alloc_seed=5, host_only=True)
+    a, b = lib.seq_add(), lib.seq_add()
+    lib.reserve_slots([a], 64)
+    lib.reserve_slots([b], 40)
+    before = (lib.block_table(a).tolist(), lib.block_table(b).tolist(), lib.stats()["free_blocks"])
+    for ids, counts, status in (([a, b], [64, 40], 3),   # 7 fresh blocks, 3 free
+                                ([a, a], [1, 1], 1),     # listed twice
+                                ([a], [65], 1),          # more than the length
+                                ([3], [0], 1)):          # not a live sequence
+        with pytest.raises(pkv.PKVError) as e:
+            lib.seq_compact(ids, counts)
+        assert e.value.status == status
+        assert (lib.block_table(a).tolist(), lib.block_table(b).tolist(), lib.stats()["free_blocks"]) == before
+    lib.seq_compact([b], [17])
+    assert lib.seq_len(b) == 17 and len(lib.block_table(b)) == 2

@@ -288,3 +288,64 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     tw.cache.sync_status()
     ref, ref_lse, _ = tw.oracle_decode(ids, q)
     assert max_err(out, ref) <= TOL["bf16"] and lse_err(lse, ref_lse) <= 2e-3
+
+
+# --------------------------------------------------------------------------
+# H2O compaction: the keep-set becomes the whole sequence
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_h2o_compaction(kv):
+    """Keep-sets from the oracle's selection on seeded scores; one sequence
+    shares its blocks with a fork, one keeps nothing, one keeps everything.
+    After compaction: tables and free counts equal the oracle's, every kept
+    row is byte-equal, the scores moved with their tokens, decode over the
+    compacted sequences matches the oracle, and appends continue after it."""
+    lens = (3000, 700, 1, 257, 40)
+    wl = workloads.small(kv, lens=lens, seed=81)
+    tw = Twin(wl, 800, 8, 220, seed=19)
+    ids = fill_sequences(tw, wl.lens)
+    twin_fork = tw.fork(ids[0])
+    stride = max(lens)
+    acc = workloads.h2o_scores_input(len(lens), stride, seed=81)
+    keeps = [oracle.h2o_select(L, 300, 64, acc[b, :L].double().numpy()) for b, L in enumerate(lens)]
+    keeps[2] = np.zeros(0, dtype=np.int32)
+    keeps[4] = np.arange(40, dtype=np.int32)
+    acc_dev = acc.cuda()
+    tw.compact(ids, keeps, acc_dev, stride)
+    tw.cache.sync_status()
+    for s in ids + [twin_fork]:
+        assert tw.cache.seq_len(s) == tw.alloc.length(s)
+        assert np.array_equal(tw.cache.block_table(s), tw.alloc.table(s))
+    assert tw.cache.stats()["free_blocks"] == tw.alloc.num_free()
+    _pool_bytes_equal(tw, ids + [twin_fork])
+    got = acc_dev.cpu().numpy()
+    for b, L in enumerate(lens):
+        n = len(keeps[b])
+        assert np.array_equal(got[b, :n], acc.numpy()[b, keeps[b]])
+        assert not got[b, n:L].any()
+        assert np.array_equal(got[b, L:], acc.numpy()[b, L:])
+    live = [s for s in ids if tw.alloc.length(s) > 0] + [twin_fork]
+    q = workloads.queries(wl, n=len(live)).cuda()
+    out, lse = tw.cache.decode(live, q, scale=wl.scale)
+    ref, ref_lse, _ = tw.oracle_decode(live, q.cpu())
+    assert max_err(out, ref) <= TOL[kv] and lse_err(lse, ref_lse) <= 1e-3
+    k, v = workloads.new_tokens(wl, len(live), 5)
+    tw.append(live, k, v)
+    out, _ = tw.cache.decode(live, q, scale=wl.scale)
+    ref, _, _ = tw.oracle_decode(live, q.cpu())
+    assert max_err(out, ref) <= TOL[kv]
+    _pool_bytes_equal(tw, live)
+
+
+def test_h2o_compaction_refuses_out_of_range_positions():
+    """A keep position at or past the sequence length is flagged by the
+    gather (status word) instead of reading another sequence's rows."""
+    wl = workloads.small("bf16", lens=(64,), seed=82)
+    tw = Twin(wl, 20, 2, 8, seed=1)
+    ids = fill_sequences(tw, wl.lens)
+    bad = torch.tensor([[0, 5, 64]], dtype=torch.int32, device="cuda")
+    tw.cache.seq_compact(ids, [3], bad, 3)
+    with pytest.raises(Exception) as e:
+        tw.cache.sync_status()
+    assert getattr(e.value, "status", None) == 7

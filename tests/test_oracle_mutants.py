@@ -28,6 +28,12 @@ MUTANTS = {
     "copy-on-write never fires": ("} else if (w->refcount[row[lb]] > 1) {", "} else if (w->refcount[row[lb]] > 2) {"),
     "fork does not take references": ("if (b >= 0) a->refcount[b] += 1;", "if (b >= 0) a->refcount[b] += 0;"),
     "splitmix64 increment": ("uint64_t z = (*state += 0x9E3779B97F4A7C15ULL);", "uint64_t z = (*state += 0x9E3779B97F4A7C17ULL);"),
+    "combined rule: window one short": ("const int is_sink = j < sinks, is_recent = j >= L - window;",
+                                        "const int is_sink = j < sinks, is_recent = j > L - window;"),
+    "combined rule: one heavy hitter short": ("for (j = 0; j < heavy && j < L; j++) heavy_hit[c[j].pos] = 1;",
+                                              "for (j = 0; j + 1 < heavy && j < L; j++) heavy_hit[c[j].pos] = 1;"),
+    "compaction keeps the old blocks": ("      if (*e >= 0) drop_block(w, *e);\n      *e = -1;",
+                                        "      *e = -1;"),
     "token slot shifted": ("    slot = j % ORACLE_BLOCK;\n    if (block < 0 || block >= jb->num_blocks) {",
                            "    slot = (j + 1) % ORACLE_BLOCK;\n    if (block < 0 || block >= jb->num_blocks) {"),
 }

@@ -248,6 +248,39 @@ def test_h2o_select_page_variant_without_recent():
     assert got.tolist() == sorted(np.argsort(-s, kind="stable")[:10].tolist())
 
 
+def test_policy_select_reduces_to_parts():
+    """The combined rule is the union of three independently pinned pieces:
+    the sinks, the recent window, and the plain top-k of all positions (the
+    select with recent = 0), and also numpy's stable ranking of all scores."""
+    rng = np.random.default_rng(8)
+    for L in (1, 3, 4, 5, 40, 260, 300, 700):
+        for sinks, window, heavy in ((4, 256, 252), (0, 0, 7), (2, 3, 0), (0, 5, 5), (6, 0, 1000)):
+            s = np.floor(rng.random(L) * 6)  # many ties
+            got = oracle.policy_select(L, sinks, window, heavy, s).tolist()
+            top = oracle.h2o_select(L, heavy, 0, s).tolist() if heavy else []
+            ranked = np.argsort(-s, kind="stable")[:heavy].tolist()
+            assert sorted(top) == sorted(ranked)
+            want = sorted(set(range(min(sinks, L))) | set(range(max(L - window, 0), L)) | set(top))
+            assert got == want, (L, sinks, window, heavy)
+
+
+def test_policy_select_printed_configuration():
+    """Sink 4, window 256, 512 - 4 - 256 = 252 heavy hitters.  Scores that
+    put the 252 largest strictly inside the middle keep exactly 512
+    positions; scores that put them in the window keep only 4 + 256."""
+    L = 2000
+    s = np.zeros(L)
+    mid = np.arange(100, 100 + 252 * 5, 5)
+    s[mid] = 1.0 + np.arange(252)
+    got = oracle.policy_select(L, 4, 256, 512 - 4 - 256, s)
+    assert got.size == 512
+    assert got.tolist() == sorted([0, 1, 2, 3] + mid.tolist() + list(range(L - 256, L)))
+    s = np.zeros(L)
+    s[L - 256:] = 5.0
+    got = oracle.policy_select(L, 4, 256, 252, s)
+    assert got.tolist() == [0, 1, 2, 3] + list(range(L - 256, L))
+
+
 def _accumulate_h2o(weights_per_step):
     """[LC] H2OEviction.update_scores restated: each step's weights [heads,
     q_len, kv_len] are reduced to one value per position (sum over queries,
@@ -490,8 +523,9 @@ def _check_invariants(a, live):
 
 
 def test_allocator_random_ops_invariants_and_contents():
-    """Random add/append/fork/free/evict/truncate; a content model (token ids
-    written through slots, COW pairs applied as whole-block copies) must give
+    """Random add/append/fork/free/evict/H2O-compact/truncate; a content
+    model (token ids written through slots, COW pairs applied as whole-block
+    copies, compaction as row moves into the returned fresh blocks) must give
     every sequence exactly its own history."""
     rng = random.Random(2024)
     for trial in range(30):
@@ -539,7 +573,7 @@ def test_allocator_random_ops_invariants_and_contents():
                 s = rng.choice(live)
                 a.free(s)
                 del hist[s]
-            elif r < 0.93:
+            elif r < 0.91:
                 s = rng.choice(live)
                 S, W = rng.randint(0, 5), rng.randint(1, 30)
                 a.evict(s, S, W)
@@ -550,6 +584,25 @@ def test_allocator_random_ops_invariants_and_contents():
                         if not any(j < S or j >= L - W for j in range(lo, hi)):
                             for j in range(lo, hi):
                                 hist[s][j] = None
+            elif r < 0.96:
+                ids = rng.sample(live, rng.randint(1, len(live)))
+                keeps = []
+                for s in ids:
+                    held = [j for j, lab in enumerate(hist[s]) if lab is not None]
+                    keeps.append(sorted(rng.sample(held, rng.randint(0, len(held)))))
+                src = [[int(a.table(s)[j // 16]) * 16 + j % 16 for j in k] for s, k in zip(ids, keeps)]
+                before = a.free_list().tolist()
+                try:
+                    fresh = a.compact(ids, [len(k) for k in keeps])
+                except MemoryError:
+                    assert a.free_list().tolist() == before
+                    continue
+                for s, k, sl, f in zip(ids, keeps, src, fresh):
+                    assert len(f) == (len(k) + 15) // 16 and set(f.tolist()) <= set(before)
+                    moved = [data[x // 16, x % 16] for x in sl]
+                    for i, lab in enumerate(moved):
+                        data[f[i // 16], i % 16] = lab
+                    hist[s] = [hist[s][j] for j in k]
             else:
                 s = rng.choice(live)
                 n = rng.randint(0, len(hist[s]))
