@@ -264,6 +264,21 @@ pkv_status pkv_h2o_select(pkv_pool* pool, void* stream, int32_t n_seqs, const in
                           const float* acc, int64_t acc_stride, int32_t budget, int32_t recent,
                           int32_t* keep_idx, int64_t keep_stride, int32_t* keep_count);
 
+/* The combined keep rule ([PA] KV compression: initial tokens + recent window
+ * + high-attention tokens, printed with sink 4, window 256 and 512 - 4 - 256
+ * heavy hitters): position p of a length-L sequence is kept when
+ * p < sink_size, when p >= L - window_size, or when acc[b][p] is among the
+ * h2o_size highest of all L positions (ties to the lower position).  The
+ * ranking spans every position, so a heavy hitter that is also a sink or
+ * recent is kept once and the set may be smaller than the three sizes'
+ * sum.  Output ascending in keep_idx (device [n_seqs][keep_stride], with
+ * keep_stride >= min(sink_size + window_size + h2o_size, largest length)),
+ * its size in keep_count (device [n_seqs]).  lens: host [n_seqs]; acc:
+ * device [n_seqs][acc_stride] fp32 (>= 0). */
+pkv_status pkv_policy_select(pkv_pool* pool, void* stream, int32_t n_seqs, const int32_t* lens,
+                             const float* acc, int64_t acc_stride, int32_t sink_size, int32_t window_size,
+                             int32_t h2o_size, int32_t* keep_idx, int64_t keep_stride, int32_t* keep_count);
+
 /* H2O compaction ([LC] H2OEviction keeps only the selected positions; [PA]
  * 剪枝/淘汰: memory goes from O(seq) to O(budget)).  For each listed sequence,
  * the counts[i] tokens at positions keep_idx[i][0 .. counts[i]) (ascending,

@@ -237,6 +237,15 @@ class PagedKVCache:
                                            int(acc_stride), budget, recent, keep_idx.data_ptr(), int(keep_stride),
                                            keep_count.data_ptr()))
 
+    def policy_select(self, lens, acc, acc_stride: int, sink_size: int, window_size: int, h2o_size: int, keep_idx,
+                      keep_stride: int, keep_count, stream=None) -> None:
+        """Combined keep rule: first sink_size positions, last window_size,
+        and the h2o_size highest scores over all positions."""
+        ln = _i32_array(lens)
+        _abi.check(self.lib.pkv_policy_select(self._h, _stream_ptr(stream), ln.size, _ptr(ln), acc.data_ptr(),
+                                              int(acc_stride), sink_size, window_size, h2o_size, keep_idx.data_ptr(),
+                                              int(keep_stride), keep_count.data_ptr()))
+
     def seq_compact(self, seq_ids, counts, keep_idx=None, keep_stride: int = 0, acc=None, acc_stride: int = 0,
                     stream=None) -> None:
         """H2O compaction: keep_idx device [n][keep_stride] int32 (ascending

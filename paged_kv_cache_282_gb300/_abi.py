@@ -76,6 +76,8 @@ SIGNATURES = {
                        c_int32, c_void_p, c_int64],
     "pkv_h2o_select": [c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_int64, c_int32, c_int32, c_void_p,
                        c_int64, c_void_p],
+    "pkv_policy_select": [c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_int64, c_int32, c_int32, c_int32,
+                          c_void_p, c_int64, c_void_p],
     "pkv_seq_compact": [c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_int64, c_void_p, c_void_p, c_int64],
     "pkv_sync_status": [c_void_p, c_void_p],
     "pkv_timing_enable": [c_void_p, c_int32],

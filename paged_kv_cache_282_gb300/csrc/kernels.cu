@@ -14,6 +14,7 @@
 #include <float.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "pkv_internal.h"
 
@@ -292,53 +293,62 @@ __device__ void radix_select(KeyAt key_at, int m, int keep, SelShared& sh) {
   }
 }
 
-// Writes, in ascending order, the positions of the keys i < m that are above
-// T, plus the first need_eq keys equal to T; keys are visited in the order of
-// i, which must be the order of positions.
+// Writes, in ascending order, the positions in [emit_lo, emit_hi) of the
+// selected keys among i < m: those above T, plus the first need_eq keys equal
+// to T (counted over all i, in or out of the range); keys are visited in the
+// order of i, which must be the order of positions.  Returns the number
+// written.
 template <class KeyAt, class PosAt>
-__device__ void ordered_emit(KeyAt key_at, PosAt pos_at, int m, uint32_t T, int need_eq, int32_t* out,
-                             SelShared& sh) {
+__device__ int ordered_emit(KeyAt key_at, PosAt pos_at, int m, uint32_t T, int need_eq, int emit_lo, int emit_hi,
+                            int32_t* out, SelShared& sh) {
   int taken = 0, eq_seen = 0;
   for (int base = 0; base < m; base += kSelUnroll * kSelThreads) {
     const int i0 = base + kSelUnroll * threadIdx.x;
     uint32_t key[kSelUnroll];
-    int n_gt = 0, n_eq = 0;
+    int n_eq = 0;
 #pragma unroll
     for (int u = 0; u < kSelUnroll; ++u) {
       key[u] = i0 + u < m ? key_at(i0 + u) : 0u;
-      n_gt += (i0 + u < m && key[u] > T);
       n_eq += (i0 + u < m && key[u] == T);
     }
     int eq_excl;
     const int eq_tot = block_excl_scan(n_eq, &eq_excl, sh.warp);
-    int rank = eq_seen + eq_excl, n_sel = n_gt;
-#pragma unroll
-    for (int u = 0; u < kSelUnroll; ++u)
-      if (i0 + u < m && key[u] == T) n_sel += rank++ < need_eq;
-    int sel_excl;
-    const int sel_tot = block_excl_scan(n_sel, &sel_excl, sh.warp);
-    int pos = taken + sel_excl;
-    rank = eq_seen + eq_excl;
+    int rank = eq_seen + eq_excl, n_sel = 0;
+    uint32_t take = 0;  // bit u: key u is selected and inside the range
 #pragma unroll
     for (int u = 0; u < kSelUnroll; ++u) {
       if (i0 + u >= m) continue;
       const bool sel = key[u] > T || (key[u] == T && rank++ < need_eq);
-      if (sel) out[pos++] = pos_at(i0 + u);
+      const int p = pos_at(i0 + u);
+      if (sel && p >= emit_lo && p < emit_hi) {
+        take |= 1u << u;
+        ++n_sel;
+      }
     }
+    int sel_excl;
+    const int sel_tot = block_excl_scan(n_sel, &sel_excl, sh.warp);
+    int pos = taken + sel_excl;
+#pragma unroll
+    for (int u = 0; u < kSelUnroll; ++u)
+      if (take >> u & 1u) out[pos++] = pos_at(i0 + u);
     taken += sel_tot;
     eq_seen += eq_tot;
   }
+  return taken;
 }
 
-// One CTA per sequence.  Two passes over the scores in global memory: a
-// histogram of the top byte finds the smallest top-byte bucket that, with
-// the buckets above it, holds at least `keep` keys; those candidates are
-// gathered, in position order, into shared memory, where the exact radix
-// select and the ordered output run.  If the candidates do not fit, the
-// select and the output run over global memory instead.
+// One CTA per sequence.  The kept set is [0, lo) (sinks), the selected
+// positions inside [lo, hi), and [hi, L) (the recent window), where the
+// selection is the `heavy` highest scores among the ranked positions [0, n).
+// Two passes over the scores in global memory: a histogram of the top byte
+// finds the smallest top-byte bucket that, with the buckets above it, holds
+// at least `keep` keys; those candidates are gathered, in position order,
+// into shared memory, where the exact radix select and the ordered output
+// run.  If the candidates do not fit, the select and the output run over
+// global memory instead.
 __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* __restrict__ rows,
                                                                  const float* __restrict__ acc, int64_t acc_stride,
-                                                                 int budget, int recent, int32_t* __restrict__ keep_idx,
+                                                                 SelPolicy pol, int32_t* __restrict__ keep_idx,
                                                                  int64_t keep_stride, int32_t* __restrict__ keep_count) {
   __shared__ SelShared sh;
   extern __shared__ uint32_t cand[];  // kSelCap keys, then kSelCap positions
@@ -348,12 +358,15 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
   const int b = row.q_row, L = row.ctx_len;
   const float* a = acc + (size_t)b * acc_stride;
   int32_t* out = keep_idx + (size_t)b * keep_stride;
-  if (L <= budget) {
+  const int hi = max(L - pol.window, 0), lo = min(pol.sinks, hi);
+  const int n = pol.rank_all ? L : hi, keep = pol.heavy;
+  if (hi <= lo || n <= keep) {  // every position is kept
     for (int j = threadIdx.x; j < L; j += blockDim.x) out[j] = j;
     if (threadIdx.x == 0) keep_count[b] = L;
     return;
   }
-  const int n = L - recent, keep = budget - recent;  // n > keep here
+  for (int j = threadIdx.x; j < lo; j += blockDim.x) out[j] = j;
+  int n_heavy = 0;
   if (keep > 0) {
     auto global_key = [a](int i) { return order_key(a[i]); };
     auto global_pos = [](int i) { return i; };
@@ -404,16 +417,16 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
       radix_select(smem_key, m, keep, sh);
       const uint32_t T = sh.prefix;
       const int need_eq = sh.k;
-      ordered_emit(smem_key, smem_pos, m, T, need_eq, out, sh);
+      n_heavy = ordered_emit(smem_key, smem_pos, m, T, need_eq, lo, hi, out + lo, sh);
     } else {
       radix_select(global_key, n, keep, sh);
       const uint32_t T = sh.prefix;
       const int need_eq = sh.k;
-      ordered_emit(global_key, global_pos, n, T, need_eq, out, sh);
+      n_heavy = ordered_emit(global_key, global_pos, n, T, need_eq, lo, hi, out + lo, sh);
     }
   }
-  for (int i = threadIdx.x; i < recent; i += blockDim.x) out[keep + i] = n + i;
-  if (threadIdx.x == 0) keep_count[b] = budget;
+  for (int i = threadIdx.x; i < L - hi; i += blockDim.x) out[lo + n_heavy + i] = hi + i;
+  if (threadIdx.x == 0) keep_count[b] = lo + n_heavy + (L - hi);
 }
 
 // ---------------------------------------------------------------------------
@@ -605,19 +618,21 @@ cudaError_t launch_compact_scores(const CompactSeq* seqs, int n, const int32_t* 
   return cudaGetLastError();
 }
 
-cudaError_t launch_h2o_select(const SeqRow* rows, int n_seqs, const float* acc, int64_t acc_stride, int budget,
-                              int recent, int32_t* keep_idx, int64_t keep_stride, int32_t* keep_count,
+cudaError_t launch_h2o_select(const SeqRow* rows, int n_seqs, const float* acc, int64_t acc_stride,
+                              const SelPolicy& pol, int32_t* keep_idx, int64_t keep_stride, int32_t* keep_count,
                               cudaStream_t st) {
   if (n_seqs <= 0) return cudaSuccess;
-  static bool attr_set = false;
+  static std::atomic<uint64_t> attr_set{0};  // one bit per device
   const int smem = kSelCap * 8;
-  if (!attr_set) {
+  int dev = 0;
+  if (cudaError_t e = cudaGetDevice(&dev)) return e;
+  const uint64_t bit = dev < 64 ? uint64_t(1) << dev : 0;
+  if (!(attr_set.load() & bit)) {
     const cudaError_t e = cudaFuncSetAttribute(h2o_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set.fetch_or(bit);
   }
-  h2o_select_kernel<<<n_seqs, kSelThreads, smem, st>>>(rows, acc, acc_stride, budget, recent, keep_idx, keep_stride,
-                                                        keep_count);
+  h2o_select_kernel<<<n_seqs, kSelThreads, smem, st>>>(rows, acc, acc_stride, pol, keep_idx, keep_stride, keep_count);
   return cudaGetLastError();
 }
 

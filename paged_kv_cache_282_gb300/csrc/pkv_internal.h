@@ -51,6 +51,13 @@ struct CompactSeq {
   int32_t seq_slot, q_row, count, new_off, old_len, pad0, pad1, pad2;
 };
 
+// A keep-set rule: the first `sinks` positions, the last `window` positions,
+// and the `heavy` highest scores among all positions (rank_all) or among the
+// positions before the window.
+struct SelPolicy {
+  int32_t sinks, window, heavy, rank_all;
+};
+
 // Per-sequence row for kernels that walk one sequence at a time.
 struct SeqRow {
   int32_t seq_slot, q_row, ctx_len, pad;
@@ -159,8 +166,8 @@ cudaError_t launch_compact_scores(const CompactSeq* seqs, int n, const int32_t* 
                                   float* acc, int64_t acc_stride, cudaStream_t stream);
 
 cudaError_t launch_h2o_select(const SeqRow* rows, int n_seqs, const float* acc, int64_t acc_stride,
-                              int budget, int recent, int32_t* keep_idx, int64_t keep_stride,
-                              int32_t* keep_count, cudaStream_t stream);
+                              const SelPolicy& pol, int32_t* keep_idx, int64_t keep_stride, int32_t* keep_count,
+                              cudaStream_t stream);
 
 }  // namespace pkv
 

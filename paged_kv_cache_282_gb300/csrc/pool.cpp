@@ -1395,17 +1395,22 @@ pkv_status pkv_h2o_scores(pkv_pool* p, void* stream, int32_t n, const int32_t* i
   return Staging::release(s, st);
 }
 
-pkv_status pkv_h2o_select(pkv_pool* p, void* stream, int32_t n, const int32_t* lens, const float* acc,
-                          int64_t acc_stride, int32_t budget, int32_t recent, int32_t* keep_idx, int64_t keep_stride,
-                          int32_t* keep_count) {
+namespace {
+
+pkv_status select_keep(pkv_pool* p, void* stream, int32_t n, const int32_t* lens, const float* acc,
+                       int64_t acc_stride, const SelPolicy& pol, int64_t max_keep, int32_t* keep_idx,
+                       int64_t keep_stride, int32_t* keep_count) {
   if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
   if (!p->device) return fail(PKV_ERR_NO_DEVICE, "host-only pool");
   if (n < 0 || (n > 0 && !lens)) return fail(PKV_ERR_INVALID_ARG, "bad lens");
-  if (recent < 0 || budget < recent || budget < 1) return fail(PKV_ERR_INVALID_ARG, "need 0 <= recent <= budget, budget >= 1");
-  if (keep_stride < budget) return fail(PKV_ERR_INVALID_ARG, "keep_stride < budget");
   if (n > 0 && (!acc || !keep_idx || !keep_count)) return fail(PKV_ERR_INVALID_ARG, "NULL device array");
-  for (int32_t i = 0; i < n; ++i)
+  int32_t max_len = 0;
+  for (int32_t i = 0; i < n; ++i) {
     if (lens[i] < 0 || lens[i] > acc_stride) return fail(PKV_ERR_INVALID_ARG, "length %d outside [0, acc_stride]", lens[i]);
+    max_len = std::max(max_len, lens[i]);
+  }
+  if (keep_stride < std::min<int64_t>(max_keep, max_len))
+    return fail(PKV_ERR_INVALID_ARG, "keep_stride %lld below the largest keep-set", (long long)keep_stride);
   cudaStream_t st = (cudaStream_t)stream;
   if (pkv_status r = flush_pending(p, st)) return r;
   if (n == 0) return PKV_OK;
@@ -1415,11 +1420,31 @@ pkv_status pkv_h2o_select(pkv_pool* p, void* stream, int32_t n, const int32_t* l
   for (int32_t i = 0; i < n; ++i) rows[i] = {-1, i, lens[i], 0};
   if (pkv_status r = Staging::upload(s, n * sizeof(SeqRow), st)) return r;
   if (pkv_status r = launch(p, PKV_KERNEL_H2O_SELECT, st, [&] {
-        return launch_h2o_select((const SeqRow*)s->dev, n, acc, acc_stride, budget, recent, keep_idx, keep_stride,
-                                 keep_count, st);
+        return launch_h2o_select((const SeqRow*)s->dev, n, acc, acc_stride, pol, keep_idx, keep_stride, keep_count,
+                                 st);
       }))
     return r;
   return Staging::release(s, st);
+}
+
+}  // namespace
+
+pkv_status pkv_h2o_select(pkv_pool* p, void* stream, int32_t n, const int32_t* lens, const float* acc,
+                          int64_t acc_stride, int32_t budget, int32_t recent, int32_t* keep_idx, int64_t keep_stride,
+                          int32_t* keep_count) {
+  if (recent < 0 || budget < recent || budget < 1) return fail(PKV_ERR_INVALID_ARG, "need 0 <= recent <= budget, budget >= 1");
+  if (keep_stride < budget) return fail(PKV_ERR_INVALID_ARG, "keep_stride < budget");
+  return select_keep(p, stream, n, lens, acc, acc_stride, SelPolicy{0, recent, budget - recent, 0}, budget, keep_idx,
+                     keep_stride, keep_count);
+}
+
+pkv_status pkv_policy_select(pkv_pool* p, void* stream, int32_t n, const int32_t* lens, const float* acc,
+                             int64_t acc_stride, int32_t sink_size, int32_t window_size, int32_t h2o_size,
+                             int32_t* keep_idx, int64_t keep_stride, int32_t* keep_count) {
+  if (sink_size < 0 || window_size < 0 || h2o_size < 0)
+    return fail(PKV_ERR_INVALID_ARG, "sink_size, window_size and h2o_size must be >= 0");
+  return select_keep(p, stream, n, lens, acc, acc_stride, SelPolicy{sink_size, window_size, h2o_size, 1},
+                     (int64_t)sink_size + window_size + h2o_size, keep_idx, keep_stride, keep_count);
 }
 
 pkv_status pkv_sync_status(pkv_pool* p, void* stream) {

@@ -233,6 +233,28 @@ def test_h2o_select_bit_exact(budget, recent):
         assert np.array_equal(keep[b, : cnt[b]], ref), (b, L)
 
 
+@pytest.mark.parametrize("sinks,window,heavy", [(4, 256, 252), (0, 0, 64), (2, 3, 0), (16, 1024, 1000),
+                                                (0, 512, 2048), (7, 0, 20000)])
+def test_policy_select_bit_exact(sinks, window, heavy):
+    """The combined sink + window + heavy-hitter rule on seeded score arrays
+    with many ties, every length regime: all kept, ranking smaller than the
+    heavy count, and long sequences whose candidates overflow shared memory."""
+    lens = [0, 1, 50, 259, 260, 261, 512, 513, 3000, 20000, 131072]
+    stride = max(lens)
+    acc = workloads.h2o_scores_input(len(lens), stride, seed=sinks + window + heavy)
+    cache = Twin(workloads.small("bf16", lens=(1,)), 4, 1, 4).cache
+    width = min(sinks + window + heavy, stride)
+    keep = torch.full((len(lens), width), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((len(lens),), -1, dtype=torch.int32, device="cuda")
+    cache.policy_select(lens, acc.cuda(), stride, sinks, window, heavy, keep, width, cnt)
+    cache.sync_status()
+    keep, cnt = keep.cpu().numpy(), cnt.cpu().numpy()
+    for b, L in enumerate(lens):
+        ref = oracle.policy_select(L, sinks, window, heavy, acc[b, :L].double().numpy())
+        assert cnt[b] == ref.size, (b, L)
+        assert np.array_equal(keep[b, : cnt[b]], ref), (b, L)
+
+
 def test_patches_and_cow_chains_in_one_flush():
     """Several host-side changes queued before one device call: a table entry
     set to -1 and back (truncate + re-append), and a copy-on-write whose source
@@ -349,3 +371,51 @@ def test_h2o_compaction_refuses_out_of_range_positions():
     with pytest.raises(Exception) as e:
         tw.cache.sync_status()
     assert getattr(e.value, "status", None) == 7
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_policy_scores_select_compact_chain(kv):
+    """Decode with logits, accumulate the heavy-hitter scores, keep 4 sinks +
+    256 recent + 252 heavy hitters, compact, decode again.  Each side runs
+    its own chain; the keep-sets may differ only where scores tie within
+    fp32 rounding, and both sides compact with the oracle's keep-set."""
+    lens = (3000, 700, 5000, 300, 520)
+    S, W, Hh = 4, 256, 252
+    wl = workloads.small(kv, lens=lens, seed=83)
+    tw = Twin(wl, 1000, 6, 340, seed=23)
+    ids = fill_sequences(tw, wl.lens)
+    stride = max(lens)
+    q = workloads.queries(wl)
+    logits = torch.zeros((len(ids), wl.n_kv_heads, stride, wl.group), device="cuda")
+    _, lse = tw.cache.decode(ids, q.cuda(), scale=wl.scale, logits=logits, logits_stride=stride)
+    acc = torch.zeros((len(ids), stride), device="cuda")
+    tw.cache.h2o_scores(ids, logits, stride, lse, acc, stride)
+    keep = torch.full((len(ids), S + W + Hh), -1, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros(len(ids), dtype=torch.int32, device="cuda")
+    tw.cache.policy_select(list(lens), acc, stride, S, W, Hh, keep, S + W + Hh, cnt)
+    tw.cache.sync_status()
+
+    _, ref_lse, ref_logits = tw.oracle_decode(ids, q, want_logits=True, logits_stride=stride)
+    ref_acc = np.zeros((len(ids), stride))
+    oracle.h2o_update(ref_acc, list(lens), ref_logits, ref_lse, oracle.MASK_FULL, 0, 0)
+    keeps = []
+    gk, gc = keep.cpu().numpy(), cnt.cpu().numpy()
+    for b, L in enumerate(lens):
+        want = oracle.policy_select(L, S, W, Hh, ref_acc[b, :L])
+        keeps.append(want)
+        got = set(gk[b, : gc[b]].tolist())
+        if L > Hh:
+            kth = np.sort(ref_acc[b, :L])[::-1][Hh - 1]
+            for j in got ^ set(want.tolist()):
+                assert abs(ref_acc[b, j] - kth) <= 1e-4 * kth + 1e-9, (b, j)
+        else:
+            assert got == set(range(L))
+    tw.compact(ids, keeps)
+    tw.cache.sync_status()
+    for s in ids:
+        assert np.array_equal(tw.cache.block_table(s), tw.alloc.table(s))
+    _pool_bytes_equal(tw, ids)
+    q2 = workloads.queries(wl, step=1)
+    out, lse = tw.cache.decode(ids, q2.cuda(), scale=wl.scale)
+    ref, ref_lse, _ = tw.oracle_decode(ids, q2)
+    assert max_err(out, ref) <= TOL[kv] and lse_err(lse, ref_lse) <= 2e-3
