@@ -332,6 +332,16 @@ pkv_status pkv_timing_read(pkv_pool* pool, double* total_ms_out /* [PKV_KERNEL_C
  * PKV_ERR_TIMEOUT in the status word; the warp then drains its own copies in
  * flight (bounded again) and returns, leaving the context usable. */
 pkv_status pkv_set_wait_limit(pkv_pool* pool, int64_t wait_limit_ns);
+/* Shared-prefix (cascade) decode, on by default ([PA] prefix sharing: a
+ * system prompt reused by many requests, parallel sampling).  In decode over
+ * whole keep-sets (PKV_MASK_FULL, num_splits = 0) the planner sorts the
+ * sequences by their block tables and pairs neighbours that share leading
+ * full blocks; such a pair's shared blocks are read once, by one warp that
+ * attends for both sequences, and each sequence's remainder is read alone.
+ * The results are merged by log-sum-exp like any split.  Pairing is skipped
+ * when it would save less than an eighth of the batch's block reads.
+ * enable = 0 turns it off (every sequence reads its blocks itself). */
+pkv_status pkv_set_cascade(pkv_pool* pool, int32_t enable);
 /* Test hook for the bound above: in the next decode on this pool, warp `warp`
  * of the grid arms its first stage without issuing the copies, so that wait
  * can only run out.  Outputs of that call are undefined; the status word

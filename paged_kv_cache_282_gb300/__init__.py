@@ -246,6 +246,10 @@ class PagedKVCache:
                                               int(acc_stride), sink_size, window_size, h2o_size, keep_idx.data_ptr(),
                                               int(keep_stride), keep_count.data_ptr()))
 
+    def set_cascade(self, enable: bool) -> None:
+        """Shared-prefix decode (pairs of sequences read shared blocks once)."""
+        _abi.check(self.lib.pkv_set_cascade(self._h, 1 if enable else 0))
+
     def seq_compact(self, seq_ids, counts, keep_idx=None, keep_stride: int = 0, acc=None, acc_stride: int = 0,
                     stream=None) -> None:
         """H2O compaction: keep_idx device [n][keep_stride] int32 (ascending

@@ -84,6 +84,7 @@ SIGNATURES = {
     "pkv_timing_read": [c_void_p, c_void_p, c_void_p],
     "pkv_launch_count": [c_void_p, _P(c_int64)],
     "pkv_set_wait_limit": [c_void_p, c_int64],
+    "pkv_set_cascade": [c_void_p, c_int32],
     "pkv_test_starve_next_decode": [c_void_p, c_int32],
     "pkv_last_error": [],
     "pkv_version": [],

@@ -48,27 +48,43 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint64_t kDrainTimeoutNs = 50000000ull;
 
-template <int KV>
+template <int KV, int NQ>
 struct TC;
 template <>
-struct TC<1> {  // BF16
+struct TC<1, 1> {  // BF16
   static constexpr int kWarps = 12, kStages = 2;
   static constexpr int kStageBytes = 8192;  // K: 2 swizzled boxes of 2 KB, V: same
   static constexpr int kScaleBytes = 0;
   static constexpr uint32_t kTxBytes = 8192;
 };
 template <>
-struct TC<2> {  // FP8 E4M3: half-size units, so twice the warps to keep enough in flight
+struct TC<2, 1> {  // FP8 E4M3: half-size units, so twice the warps to keep enough in flight
   static constexpr int kWarps = 16, kStages = 2;
   static constexpr int kStageBytes = 4096;  // K: one swizzled box of 2 KB, V: same
   static constexpr int kScaleBytes = 128;   // 16 K scales + 16 V scales
   static constexpr uint32_t kTxBytes = 4096 + 128;
 };
+// Two sequences per warp: twice the accumulators, so fewer warps (up to 255
+// registers a thread) with deeper rings.
+template <>
+struct TC<1, 2> {
+  static constexpr int kWarps = 8, kStages = 3;
+  static constexpr int kStageBytes = 8192;
+  static constexpr int kScaleBytes = 0;
+  static constexpr uint32_t kTxBytes = 8192;
+};
+template <>
+struct TC<2, 2> {
+  static constexpr int kWarps = 8, kStages = 4;
+  static constexpr int kStageBytes = 4096;
+  static constexpr int kScaleBytes = 128;
+  static constexpr uint32_t kTxBytes = 4096 + 128;
+};
 
-template <int KV>
+template <int KV, int NQ>
 constexpr size_t smem_bytes() {
-  return 1024 + (size_t)TC<KV>::kWarps * TC<KV>::kStages * (TC<KV>::kStageBytes + TC<KV>::kScaleBytes) +
-         (size_t)TC<KV>::kWarps * TC<KV>::kStages * 8;
+  using C = TC<KV, NQ>;
+  return 1024 + (size_t)C::kWarps * C::kStages * (C::kStageBytes + C::kScaleBytes) + (size_t)C::kWarps * C::kStages * 8;
 }
 
 // ---------------------------------------------------------------------------
@@ -309,9 +325,10 @@ __device__ void merge_partials(const DecodeTCParams& p, const CombineItem it, in
 // the kernel
 // ---------------------------------------------------------------------------
 
-template <int KV, int G>
-__global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const __grid_constant__ DecodeTCParams p) {
-  using C = TC<KV>;
+template <int KV, int G, int NQ>
+__global__ void __launch_bounds__(TC<KV, NQ>::kWarps * 32, 1)
+    decode_tc_kernel(const __grid_constant__ DecodeTCParams p) {
+  using C = TC<KV, NQ>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -400,42 +417,49 @@ __global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const
   const uint32_t v_row_off = (uint32_t)((rr + ((mi >> 1) << 3)) * 128);
   const int v_hi = mi & 1;
 
-  uint32_t qf[8][2];
-  float o[8][4];
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  bool run_open = false;
+  // Per sequence t of the piece (t = 1 only in the two-sequence variant):
+  // Q^T fragments, O^T accumulators and the softmax state of columns 2c, 2c+1.
+  uint32_t qf[NQ][8][2];
+  float o[NQ][8][4];
+  float m0[NQ], m1[NQ], l0[NQ], l1[NQ];
+  bool run_open = false, two = false;
   int u = 0;
 
   for (int pi = pb; pi < pe; ++pi) {
     const Piece pc = p.pieces[pi];
     const int g = pc.kv_head, L = pc.ctx_len;
     if (!run_open) {
+      two = NQ == 2 && pc.q_row1 >= 0;
       // Q^T fragments (B operand): rows k = head-dim slots, column n = query head r
       const int h = g * G + r;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        uint32_t b0 = 0, b1 = 0;
-        if (r < G) {
-          const __nv_bfloat16* qrow = reinterpret_cast<const __nv_bfloat16*>(p.q) + ((size_t)pc.q_row * H + h) * 128;
-          if (KV == 1) {
-            b0 = *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * c);
-            b1 = *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 8 + 2 * c);
-          } else {
-            // FP8 path: k-slot 2c+e <-> d = 32c + 4kk + e, slot 2c+8+e <-> d + 2
-            const uint2 raw = *reinterpret_cast<const uint2*>(qrow + 32 * c + 4 * kk);
-            const __nv_bfloat162 x01 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-            const __nv_bfloat162 x23 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-            b0 = pack_f16(__low2float(x01), __high2float(x01));
-            b1 = pack_f16(__low2float(x23), __high2float(x23));
-          }
-        }
-        qf[kk][0] = b0;
-        qf[kk][1] = b1;
-      }
+      for (int t = 0; t < NQ; ++t) {
+        const int qr = t == 0 ? pc.q_row : pc.q_row1;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-      m0 = m1 = -INFINITY;
-      l0 = l1 = 0.f;
+        for (int kk = 0; kk < 8; ++kk) {
+          uint32_t b0 = 0, b1 = 0;
+          if (r < G && qr >= 0) {
+            const __nv_bfloat16* qrow = reinterpret_cast<const __nv_bfloat16*>(p.q) + ((size_t)qr * H + h) * 128;
+            if (KV == 1) {
+              b0 = *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * c);
+              b1 = *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 8 + 2 * c);
+            } else {
+              // FP8 path: k-slot 2c+e <-> d = 32c + 4kk + e, slot 2c+8+e <-> d + 2
+              const uint2 raw = *reinterpret_cast<const uint2*>(qrow + 32 * c + 4 * kk);
+              const __nv_bfloat162 x01 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+              const __nv_bfloat162 x23 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+              b0 = pack_f16(__low2float(x01), __high2float(x01));
+              b1 = pack_f16(__low2float(x23), __high2float(x23));
+            }
+          }
+          qf[t][kk][0] = b0;
+          qf[t][kk][1] = b1;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[t][i][0] = o[t][i][1] = o[t][i][2] = o[t][i][3] = 0.f;
+        m0[t] = m1[t] = -INFINITY;
+        l0[t] = l1[t] = 0.f;
+      }
       run_open = true;
     }
 
@@ -453,7 +477,11 @@ __global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const
       const uint32_t vb = kb + (KV == 1 ? 4096u : 2048u);
 
       // ---- S = K Q^T : rows = tokens, columns = query heads of the group
-      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      float sa[NQ][4], sb[NQ][4];
+#pragma unroll
+      for (int t = 0; t < NQ; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sa[t][e] = sb[t][e] = 0.f;
       float ks_r = 1.f, ks_r8 = 1.f, lv_r = 0.f, lv_r8 = 0.f;
       if (KV == 1) {
 #pragma unroll
@@ -461,10 +489,14 @@ __global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const
           const int c16 = 2 * kk + k_hi;  // 16-byte chunk index across the 256-byte row
           uint32_t a[4];
           ldsm_x4(kb + (uint32_t)((c16 >> 3) * 2048) + k_row_off + (uint32_t)((((c16 & 7) ^ rr)) << 4), a);
-          if (kk & 1)
-            mma_bf16(sb, a, qf[kk][0], qf[kk][1]);
-          else
-            mma_bf16(sa, a, qf[kk][0], qf[kk][1]);
+#pragma unroll
+          for (int t = 0; t < NQ; ++t) {
+            if (t == 1 && !two) break;
+            if (kk & 1)
+              mma_bf16(sb[t], a, qf[t][kk][0], qf[t][kk][1]);
+            else
+              mma_bf16(sa[t], a, qf[t][kk][0], qf[t][kk][1]);
+          }
         }
       } else {
         // tokens r and r + 8, codes d in [32c, 32c + 32)
@@ -479,10 +511,14 @@ __global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const
           uint32_t a[4];
           e4m3x4_to_f16x2x2(tA[kk], a[0], a[2]);
           e4m3x4_to_f16x2x2(tB[kk], a[1], a[3]);
-          if (kk & 1)
-            mma_f16(sb, a, qf[kk][0], qf[kk][1]);
-          else
-            mma_f16(sa, a, qf[kk][0], qf[kk][1]);
+#pragma unroll
+          for (int t = 0; t < NQ; ++t) {
+            if (t == 1 && !two) break;
+            if (kk & 1)
+              mma_f16(sb[t], a, qf[t][kk][0], qf[t][kk][1]);
+            else
+              mma_f16(sa[t], a, qf[t][kk][0], qf[t][kk][1]);
+          }
         }
         const uint32_t sc = scl + (uint32_t)(st * C::kScaleBytes);
         ks_r = lds_f32(sc + 4 * r);
@@ -490,10 +526,9 @@ __global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const
         lv_r = fast_log2(lds_f32(sc + 64 + 4 * r));
         lv_r8 = fast_log2(lds_f32(sc + 64 + 4 * (r + 8)));
       }
-      const float s0 = (sa[0] + sb[0]) * ks_r, s1 = (sa[1] + sb[1]) * ks_r;
-      const float s2 = (sa[2] + sb[2]) * ks_r8, s3 = (sa[3] + sb[3]) * ks_r8;
 
-      // ---- mask, logits out, online softmax (log2 units)
+      // ---- mask (per token: the same for both sequences, whose shared
+      // blocks are whole), logits out, online softmax (log2 units)
       const int tok0 = lb * kBlock + r, tok1 = tok0 + 8;
       // most units lie wholly inside the keep-set: their first and last
       // token decide it, and the per-token test is skipped
@@ -504,20 +539,6 @@ __global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const
       const bool k0 = whole || kept(tok0, L, p.mask_mode, p.num_sinks, p.window);
       const bool k1 = whole || kept(tok1, L, p.mask_mode, p.num_sinks, p.window);
       const bool h0v = 2 * c < G, h1v = 2 * c + 1 < G;
-      if (p.logits != nullptr) {
-        float* lg = p.logits + ((size_t)pc.q_row * Hk + g) * p.logits_stride * G;
-        if (k0 && h0v) lg[(size_t)tok0 * G + 2 * c] = s0 * p.scale;
-        if (k0 && h1v) lg[(size_t)tok0 * G + 2 * c + 1] = s1 * p.scale;
-        if (k1 && h0v) lg[(size_t)tok1 * G + 2 * c] = s2 * p.scale;
-        if (k1 && h1v) lg[(size_t)tok1 * G + 2 * c + 1] = s3 * p.scale;
-      }
-      const float a0 = k0 ? s0 * sl2 : -INFINITY, a1 = k0 ? s1 * sl2 : -INFINITY;
-      const float a2 = k1 ? s2 * sl2 : -INFINITY, a3 = k1 ? s3 * sl2 : -INFINITY;
-      // a + log2(v scale): the exponent of the weight that multiplies V.  Slots
-      // of masked tokens may hold anything (unwritten memory), so neither their
-      // scale nor their V row may reach the arithmetic.
-      const float e0 = k0 ? a0 + lv_r : -INFINITY, e1 = k0 ? a1 + lv_r : -INFINITY;
-      const float e2 = k1 ? a2 + lv_r8 : -INFINITY, e3 = k1 ? a3 + lv_r8 : -INFINITY;
       if (!whole && __ballot_sync(kFull, !(k0 && k1))) {
         // zero the V rows of masked tokens in this warp's stage (0 * NaN = NaN)
         constexpr int kRowBytes = KV == 1 ? 256 : 128;
@@ -536,45 +557,72 @@ __global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
       }
-      float bm0 = fmaxf(e0, e2), bm1 = fmaxf(e1, e3);
+      uint32_t pb0[NQ], pb1[NQ];
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, off));
-        bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
-      }
-      const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-      const float z0 = mn0 == -INFINITY ? 0.f : mn0, z1 = mn1 == -INFINITY ? 0.f : mn1;
-      const float al0 = fast_exp2(m0 - z0), al1 = fast_exp2(m1 - z1);
-      const float p0 = fast_exp2(e0 - z0), p1 = fast_exp2(e1 - z1), p2 = fast_exp2(e2 - z0), p3 = fast_exp2(e3 - z1);
-      if (KV == 1) {
-        l0 = l0 * al0 + (p0 + p2);
-        l1 = l1 * al1 + (p1 + p3);
-      } else {
-        l0 = l0 * al0 + (fast_exp2(a0 - z0) + fast_exp2(a2 - z0));
-        l1 = l1 * al1 + (fast_exp2(a1 - z1) + fast_exp2(a3 - z1));
-      }
-      m0 = mn0;
-      m1 = mn1;
-      if (__any_sync(kFull, (al0 != 1.f) || (al1 != 1.f))) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          o[i][0] *= al0;
-          o[i][1] *= al1;
-          o[i][2] *= al0;
-          o[i][3] *= al1;
+      for (int t = 0; t < NQ; ++t) {
+        if (t == 1 && !two) break;
+        const float s0 = (sa[t][0] + sb[t][0]) * ks_r, s1 = (sa[t][1] + sb[t][1]) * ks_r;
+        const float s2 = (sa[t][2] + sb[t][2]) * ks_r8, s3 = (sa[t][3] + sb[t][3]) * ks_r8;
+        if (p.logits != nullptr) {
+          const int qr = t == 0 ? pc.q_row : pc.q_row1;
+          float* lg = p.logits + ((size_t)qr * Hk + g) * p.logits_stride * G;
+          if (k0 && h0v) lg[(size_t)tok0 * G + 2 * c] = s0 * p.scale;
+          if (k0 && h1v) lg[(size_t)tok0 * G + 2 * c + 1] = s1 * p.scale;
+          if (k1 && h0v) lg[(size_t)tok1 * G + 2 * c] = s2 * p.scale;
+          if (k1 && h1v) lg[(size_t)tok1 * G + 2 * c + 1] = s3 * p.scale;
         }
+        const float a0 = k0 ? s0 * sl2 : -INFINITY, a1 = k0 ? s1 * sl2 : -INFINITY;
+        const float a2 = k1 ? s2 * sl2 : -INFINITY, a3 = k1 ? s3 * sl2 : -INFINITY;
+        // a + log2(v scale): the exponent of the weight that multiplies V.  Slots
+        // of masked tokens may hold anything (unwritten memory), so neither their
+        // scale nor their V row may reach the arithmetic.
+        const float e0 = k0 ? a0 + lv_r : -INFINITY, e1 = k0 ? a1 + lv_r : -INFINITY;
+        const float e2 = k1 ? a2 + lv_r8 : -INFINITY, e3 = k1 ? a3 + lv_r8 : -INFINITY;
+        float bm0 = fmaxf(e0, e2), bm1 = fmaxf(e1, e3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, off));
+          bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
+        }
+        const float mn0 = fmaxf(m0[t], bm0), mn1 = fmaxf(m1[t], bm1);
+        const float z0 = mn0 == -INFINITY ? 0.f : mn0, z1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = fast_exp2(m0[t] - z0), al1 = fast_exp2(m1[t] - z1);
+        const float p0 = fast_exp2(e0 - z0), p1 = fast_exp2(e1 - z1), p2 = fast_exp2(e2 - z0),
+                    p3 = fast_exp2(e3 - z1);
+        if (KV == 1) {
+          l0[t] = l0[t] * al0 + (p0 + p2);
+          l1[t] = l1[t] * al1 + (p1 + p3);
+        } else {
+          l0[t] = l0[t] * al0 + (fast_exp2(a0 - z0) + fast_exp2(a2 - z0));
+          l1[t] = l1[t] * al1 + (fast_exp2(a1 - z1) + fast_exp2(a3 - z1));
+        }
+        m0[t] = mn0;
+        m1[t] = mn1;
+        if (__any_sync(kFull, (al0 != 1.f) || (al1 != 1.f))) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            o[t][i][0] *= al0;
+            o[t][i][1] *= al1;
+            o[t][i][2] *= al0;
+            o[t][i][3] *= al1;
+          }
+        }
+        pb0[t] = movmatrix_t(KV == 1 ? pack_bf16(p0, p1) : pack_f16(p0, p1));
+        pb1[t] = movmatrix_t(KV == 1 ? pack_bf16(p2, p3) : pack_f16(p2, p3));
       }
 
       // ---- O^T += V^T P : rows = head-dim, columns = query heads
-      const uint32_t pb0 = movmatrix_t(KV == 1 ? pack_bf16(p0, p1) : pack_f16(p0, p1));
-      const uint32_t pb1 = movmatrix_t(KV == 1 ? pack_bf16(p2, p3) : pack_f16(p2, p3));
       if (KV == 1) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int c16 = 2 * i + v_hi;
           uint32_t a[4];
           ldsm_x4_t(vb + (uint32_t)((c16 >> 3) * 2048) + v_row_off + (uint32_t)((((c16 & 7) ^ rr)) << 4), a);
-          mma_bf16(o[i], a, pb0, pb1);
+#pragma unroll
+          for (int t = 0; t < NQ; ++t) {
+            if (t == 1 && !two) break;
+            mma_bf16(o[t][i], a, pb0[t], pb1[t]);
+          }
         }
       } else {
         // tokens 2c, 2c+1, 2c+8, 2c+9; codes d in [16r, 16r + 16)
@@ -597,7 +645,11 @@ __global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const uint32_t a[4] = {pab[i], pab[8 + i], pcd[i], pcd[8 + i]};
-          mma_f16(o[i], a, pb0, pb1);
+#pragma unroll
+          for (int t = 0; t < NQ; ++t) {
+            if (t == 1 && !two) break;
+            mma_f16(o[t][i], a, pb0[t], pb1[t]);
+          }
         }
       }
       __syncwarp();
@@ -608,62 +660,69 @@ __global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const
     }
 
     if (pc.flags & kPieceLastOfRun) {
-      // ---- finalise the run
+      // ---- finalise the run: one output or partial record per sequence
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        l0 += __shfl_xor_sync(kFull, l0, off);
-        l1 += __shfl_xor_sync(kFull, l1, off);
-      }
-      const int h0 = 2 * c, h1 = 2 * c + 1;
-      auto dpos = [&](int i, int half) { return KV == 1 ? 16 * i + 8 * half + r : 16 * r + 8 * half + i; };
-      if (pc.out_index < 0) {
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-        const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-        const size_t row0 = ((size_t)pc.q_row * H + g * G + h0) * 128;
-        const size_t row1 = row0 + 128;
+      for (int t = 0; t < NQ; ++t) {
+        if (t == 1 && !two) break;
+        float L0 = l0[t], L1 = l1[t];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const int d = dpos(i, half);
-            if (h0 < G) out[row0 + d] = __float2bfloat16(o[i][2 * half] * inv0);
-            if (h1 < G) out[row1 + d] = __float2bfloat16(o[i][2 * half + 1] * inv1);
-          }
-        if (r == 0 && p.lse != nullptr) {
-          const size_t li = (size_t)pc.q_row * H + g * G;
-          if (h0 < G) p.lse[li + h0] = l0 > 0.f ? (m0 + log2f(l0)) * kLn2 : -INFINITY;
-          if (h1 < G) p.lse[li + h1] = l1 > 0.f ? (m1 + log2f(l1)) * kLn2 : -INFINITY;
+        for (int off = 4; off < 32; off <<= 1) {
+          L0 += __shfl_xor_sync(kFull, L0, off);
+          L1 += __shfl_xor_sync(kFull, L1, off);
         }
-      } else {
-        float* rec = p.partials + (size_t)pc.out_index * partial_floats(G, 128);
+        const int qr = t == 0 ? pc.q_row : pc.q_row1;
+        const int oi = t == 0 ? pc.out_index : pc.out_index1;
+        const int ci = t == 0 ? pc.flags >> 1 : pc.item1;
+        const int h0 = 2 * c, h1 = 2 * c + 1;
+        auto dpos = [&](int i, int half) { return KV == 1 ? 16 * i + 8 * half + r : 16 * r + 8 * half + i; };
+        if (oi < 0) {
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+          const float inv0 = L0 > 0.f ? 1.f / L0 : 0.f, inv1 = L1 > 0.f ? 1.f / L1 : 0.f;
+          const size_t row0 = ((size_t)qr * H + g * G + h0) * 128;
+          const size_t row1 = row0 + 128;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+          for (int i = 0; i < 8; ++i)
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const int d = dpos(i, half);
-            if (h0 < G) rec[h0 * 128 + d] = o[i][2 * half];
-            if (h1 < G) rec[h1 * 128 + d] = o[i][2 * half + 1];
+            for (int half = 0; half < 2; ++half) {
+              const int d = dpos(i, half);
+              if (h0 < G) out[row0 + d] = __float2bfloat16(o[t][i][2 * half] * inv0);
+              if (h1 < G) out[row1 + d] = __float2bfloat16(o[t][i][2 * half + 1] * inv1);
+            }
+          if (r == 0 && p.lse != nullptr) {
+            const size_t li = (size_t)qr * H + g * G;
+            if (h0 < G) p.lse[li + h0] = L0 > 0.f ? (m0[t] + log2f(L0)) * kLn2 : -INFINITY;
+            if (h1 < G) p.lse[li + h1] = L1 > 0.f ? (m1[t] + log2f(L1)) * kLn2 : -INFINITY;
           }
-        if (r == 0) {
-          if (h0 < G) {
-            rec[G * 128 + h0] = m0;
-            rec[G * 128 + G + h0] = l0;
+        } else {
+          float* rec = p.partials + (size_t)oi * partial_floats(G, 128);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const int d = dpos(i, half);
+              if (h0 < G) rec[h0 * 128 + d] = o[t][i][2 * half];
+              if (h1 < G) rec[h1 * 128 + d] = o[t][i][2 * half + 1];
+            }
+          if (r == 0) {
+            if (h0 < G) {
+              rec[G * 128 + h0] = m0[t];
+              rec[G * 128 + G + h0] = L0;
+            }
+            if (h1 < G) {
+              rec[G * 128 + h1] = m1[t];
+              rec[G * 128 + G + h1] = L1;
+            }
           }
-          if (h1 < G) {
-            rec[G * 128 + h1] = m1;
-            rec[G * 128 + G + h1] = l1;
-          }
-        }
-        // publish the record, count it, and merge if it was the last one
-        __threadfence();
-        __syncwarp();
-        const int ci = pc.flags >> 1;
-        int last = 0;
-        if (lane == 0) last = atomicAdd(p.counters + ci, 1) == p.combine[ci].n_partials - 1;
-        last = __shfl_sync(kFull, last, 0);
-        if (last) {
+          // publish the record, count it, and merge if it was the last one
           __threadfence();
-          merge_partials<G>(p, p.combine[ci], lane);
+          __syncwarp();
+          int last = 0;
+          if (lane == 0) last = atomicAdd(p.counters + ci, 1) == p.combine[ci].n_partials - 1;
+          last = __shfl_sync(kFull, last, 0);
+          if (last) {
+            __threadfence();
+            merge_partials<G>(p, p.combine[ci], lane);
+          }
         }
       }
       run_open = false;
@@ -671,74 +730,67 @@ __global__ void __launch_bounds__(TC<KV>::kWarps * 32, 1) decode_tc_kernel(const
   }
 }
 
-template <int KV, int G>
+template <int KV, int G, int NQ>
 cudaError_t launch_t(const DecodeTCParams& p, int ctas, cudaStream_t st) {
-  decode_tc_kernel<KV, G><<<ctas, TC<KV>::kWarps * 32, smem_bytes<KV>(), st>>>(p);
+  decode_tc_kernel<KV, G, NQ><<<ctas, TC<KV, NQ>::kWarps * 32, smem_bytes<KV, NQ>(), st>>>(p);
   return cudaGetLastError();
 }
 
-template <int KV>
-cudaError_t launch_kv(int G, const DecodeTCParams& p, int ctas, cudaStream_t st) {
-  switch (G) {
-    case 1: return launch_t<KV, 1>(p, ctas, st);
-    case 2: return launch_t<KV, 2>(p, ctas, st);
-    case 4: return launch_t<KV, 4>(p, ctas, st);
-    case 8: return launch_t<KV, 8>(p, ctas, st);
-  }
-  return cudaErrorInvalidValue;
-}
-
-template <int KV, int G>
+template <int KV, int G, int NQ>
 cudaError_t prepare_t() {
-  return cudaFuncSetAttribute(decode_tc_kernel<KV, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)smem_bytes<KV>());
+  return cudaFuncSetAttribute(decode_tc_kernel<KV, G, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem_bytes<KV, NQ>());
 }
 
-template <int KV, int G>
+template <int KV, int G, int NQ>
 cudaError_t occupancy_t(int* n) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_tc_kernel<KV, G>, TC<KV>::kWarps * 32,
-                                                       smem_bytes<KV>());
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_tc_kernel<KV, G, NQ>, TC<KV, NQ>::kWarps * 32,
+                                                       smem_bytes<KV, NQ>());
 }
 
-template <int KV>
-cudaError_t dispatch_prepare(int G) {
-  switch (G) {
-    case 1: return prepare_t<KV, 1>();
-    case 2: return prepare_t<KV, 2>();
-    case 4: return prepare_t<KV, 4>();
-    case 8: return prepare_t<KV, 8>();
-  }
-  return cudaErrorInvalidValue;
-}
-
-template <int KV>
-cudaError_t dispatch_occupancy(int G, int* n) {
-  switch (G) {
-    case 1: return occupancy_t<KV, 1>(n);
-    case 2: return occupancy_t<KV, 2>(n);
-    case 4: return occupancy_t<KV, 4>(n);
-    case 8: return occupancy_t<KV, 8>(n);
-  }
-  return cudaErrorInvalidValue;
-}
+// Expands X(KV, G, NQ) for every compiled variant, returning its result when
+// it matches the runtime (kv_dtype, G, nq).
+#define PKV_FOR_VARIANTS(X)                                                        \
+  X(1, 1, 1) X(1, 2, 1) X(1, 4, 1) X(1, 8, 1) X(2, 1, 1) X(2, 2, 1) X(2, 4, 1) X(2, 8, 1) \
+  X(1, 1, 2) X(1, 2, 2) X(1, 4, 2) X(1, 8, 2) X(2, 1, 2) X(2, 2, 2) X(2, 4, 2) X(2, 8, 2)
 
 }  // namespace
 
-cudaError_t launch_decode_tc(int kv_dtype, int G, const DecodeTCParams& p, int ctas, cudaStream_t st) {
+cudaError_t launch_decode_tc(int kv_dtype, int G, int nq, const DecodeTCParams& p, int ctas, cudaStream_t st) {
   if (ctas <= 0) return cudaSuccess;
-  return kv_dtype == 2 ? launch_kv<2>(G, p, ctas, st) : launch_kv<1>(G, p, ctas, st);
+#define X(KV, GG, NQ) \
+  if (kv_dtype == KV && G == GG && nq == NQ) return launch_t<KV, GG, NQ>(p, ctas, st);
+  PKV_FOR_VARIANTS(X)
+#undef X
+  return cudaErrorInvalidValue;
 }
 
-int decode_tc_warps_per_cta(int kv_dtype) { return kv_dtype == 2 ? TC<2>::kWarps : TC<1>::kWarps; }
-
-size_t decode_tc_smem_bytes(int kv_dtype) { return kv_dtype == 2 ? smem_bytes<2>() : smem_bytes<1>(); }
-
-cudaError_t decode_tc_prepare(int kv_dtype, int G) {
-  return kv_dtype == 2 ? dispatch_prepare<2>(G) : dispatch_prepare<1>(G);
+int decode_tc_warps_per_cta(int kv_dtype, int nq) {
+  if (kv_dtype == 2) return nq == 2 ? TC<2, 2>::kWarps : TC<2, 1>::kWarps;
+  return nq == 2 ? TC<1, 2>::kWarps : TC<1, 1>::kWarps;
 }
 
-cudaError_t decode_tc_occupancy(int kv_dtype, int G, int* n) {
-  return kv_dtype == 2 ? dispatch_occupancy<2>(G, n) : dispatch_occupancy<1>(G, n);
+size_t decode_tc_smem_bytes(int kv_dtype, int nq) {
+  if (kv_dtype == 2) return nq == 2 ? smem_bytes<2, 2>() : smem_bytes<2, 1>();
+  return nq == 2 ? smem_bytes<1, 2>() : smem_bytes<1, 1>();
 }
+
+cudaError_t decode_tc_prepare(int kv_dtype, int G, int nq) {
+#define X(KV, GG, NQ) \
+  if (kv_dtype == KV && G == GG && nq == NQ) return prepare_t<KV, GG, NQ>();
+  PKV_FOR_VARIANTS(X)
+#undef X
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t decode_tc_occupancy(int kv_dtype, int G, int nq, int* n) {
+#define X(KV, GG, NQ) \
+  if (kv_dtype == KV && G == GG && nq == NQ) return occupancy_t<KV, GG, NQ>(n);
+  PKV_FOR_VARIANTS(X)
+#undef X
+  return cudaErrorInvalidValue;
+}
+
+#undef PKV_FOR_VARIANTS
 
 }  // namespace pkv

@@ -30,8 +30,15 @@ struct Piece {
   int32_t ctx_len;     // L: context length, current token included
   int32_t out_index;   // >= 0: partial record index; -1: write the final output
   int32_t flags;       // bit 0: last piece of its run; bits 31..1: merge item
+  // A second sequence whose blocks [lblk_begin, lblk_end) are the same
+  // physical blocks (shared-prefix decode); q_row1 = -1: none.  Its run
+  // always ends in a partial record out_index1 of merge item item1.
+  int32_t q_row1;
+  int32_t out_index1;
+  int32_t item1;
+  int32_t pad;
 };
-static_assert(sizeof(Piece) == 32, "Piece layout");
+static_assert(sizeof(Piece) == 48, "Piece layout");
 
 // A (sequence, kv head) whose n_partials (>= 2) partial records, stored
 // consecutively from first_partial, are merged by log-sum-exp.  The warp that
@@ -115,14 +122,16 @@ struct DecodeF32Params {
 
 // ---- kernel launchers (defined in the .cu files) -------------------------
 
-// Tensor-core decode: kv_dtype 1 = bf16, 2 = FP8.  Returns the launch error.
-cudaError_t launch_decode_tc(int kv_dtype, int G, const DecodeTCParams& p, int grid_ctas,
+// Tensor-core decode: kv_dtype 1 = bf16, 2 = FP8; nq = 1, or 2 for the
+// variant whose pieces may carry a second sequence over shared blocks.
+// Returns the launch error.
+cudaError_t launch_decode_tc(int kv_dtype, int G, int nq, const DecodeTCParams& p, int grid_ctas,
                              cudaStream_t stream);
 // Decode kernel geometry: warps per CTA and dynamic shared memory bytes.
-int decode_tc_warps_per_cta(int kv_dtype);
-size_t decode_tc_smem_bytes(int kv_dtype);
-cudaError_t decode_tc_prepare(int kv_dtype, int G);  // sets the smem attribute
-cudaError_t decode_tc_occupancy(int kv_dtype, int G, int* ctas_per_sm);
+int decode_tc_warps_per_cta(int kv_dtype, int nq);
+size_t decode_tc_smem_bytes(int kv_dtype, int nq);
+cudaError_t decode_tc_prepare(int kv_dtype, int G, int nq);  // sets the smem attribute
+cudaError_t decode_tc_occupancy(int kv_dtype, int G, int nq, int* ctas_per_sm);
 
 cudaError_t launch_decode_f32(const DecodeF32Params& p, cudaStream_t stream);
 

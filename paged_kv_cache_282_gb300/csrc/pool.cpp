@@ -281,7 +281,9 @@ struct pkv_pool {
   Timing timing;
   int64_t launches = 0;
   int device_id = 0, num_sms = 0;
-  int tc_warps_per_cta = 0, tc_ctas_per_sm = 0;
+  int tc_warps_per_cta = 0, tc_ctas_per_sm = 0;    // one sequence per warp
+  int tc2_warps_per_cta = 0, tc2_ctas_per_sm = 0;  // up to two sequences over shared blocks
+  bool cascade = true;                              // read shared prefixes once per sequence pair
   size_t tc_smem = 0;
   CUtensorMap tmap_k{}, tmap_v{};
   bool tc_path = false;
@@ -479,21 +481,75 @@ struct Plan {
   int total_warps = 0;  // physical warp slots = ctas * warps_per_cta
   int ctas = 0;
   int n_partials = 0;
+  int nq = 1;  // 2: pieces may carry a second sequence (the two-sequence kernel)
 };
 
 struct Seg {
   int32_t b, g, lo, hi;  // batch index, kv head, logical blocks [lo, hi)
+  int32_t b1;            // >= 0: a second sequence over the same physical blocks
 };
 
-int max_total_warps(const pkv_pool* p) {
-  return std::max(1, p->num_sms * std::max(1, p->tc_ctas_per_sm) * std::max(1, p->tc_warps_per_cta));
+int warps_per_cta(const pkv_pool* p, int nq) {
+  return std::max(1, nq == 2 ? p->tc2_warps_per_cta : p->tc_warps_per_cta);
 }
 
+int max_total_warps(const pkv_pool* p, int nq = 1) {
+  const int ctas = nq == 2 ? p->tc2_ctas_per_sm : p->tc_ctas_per_sm;
+  return std::max(1, p->num_sms * std::max(1, ctas) * warps_per_cta(p, nq));
+}
+
+// Upper bound of partial records (and pieces) of one decode call.
 size_t max_pieces(const pkv_pool* p, int32_t n_seqs, int32_t num_splits) {
   const size_t nbg = (size_t)n_seqs * p->cfg.n_kv_heads;
   const size_t a = 2 * nbg + (size_t)max_total_warps(p) + 1;
   const size_t b = nbg * (size_t)std::max(1, num_splits) + nbg + 1;
-  return std::max(a, b);
+  // shared-prefix plans: 3 segments per sequence pair and kv head, and a
+  // record for each sequence of a run
+  const size_t c = 2 * (2 * nbg + (size_t)max_total_warps(p, 2)) + 2;
+  return std::max(std::max(a, b), c);
+}
+
+// Shared-prefix pairing for decode over whole keep-sets: sequences sorted by
+// their block tables, then adjacent ones paired while they share leading
+// blocks that are full in both (the same physical block at the same logical
+// index holds the same 16 tokens for both).  Returns (b0, b1, shared blocks)
+// triples, or nothing when the pairs would save less than an eighth of all
+// block reads.
+struct Pairing {
+  int32_t b0, b1, shared;
+};
+
+std::vector<Pairing> pair_shared_prefixes(const pkv_pool* p, int32_t n, const int32_t* ids) {
+  const auto& A = p->alloc;
+  std::vector<int32_t> order(n);
+  for (int32_t b = 0; b < n; ++b) order[b] = b;
+  auto nblk = [&](int32_t b) { return ceil_div(A.len[ids[b]], kBlock); };
+  auto entry = [&](int32_t b, int32_t lb) { return A.table[ids[b]][lb]; };
+  std::sort(order.begin(), order.end(), [&](int32_t x, int32_t y) {
+    const int32_t nx = nblk(x), ny = nblk(y);
+    for (int32_t lb = 0; lb < std::min(nx, ny); ++lb)
+      if (entry(x, lb) != entry(y, lb)) return entry(x, lb) < entry(y, lb);
+    if (nx != ny) return nx < ny;
+    return x < y;
+  });
+  std::vector<Pairing> pairs;
+  int64_t saved = 0, total = 0;
+  for (int32_t b = 0; b < n; ++b) total += nblk(b);
+  for (int32_t i = 0; i + 1 < n;) {
+    const int32_t x = order[i], y = order[i + 1];
+    const int32_t full = std::min(A.len[ids[x]], A.len[ids[y]]) / kBlock;
+    int32_t c = 0;
+    while (c < full && entry(x, c) >= 0 && entry(x, c) == entry(y, c)) ++c;
+    if (c > 0) {
+      pairs.push_back({std::min(x, y), std::max(x, y), c});
+      saved += c;
+      i += 2;
+    } else {
+      i += 1;
+    }
+  }
+  if (saved * 8 < total) pairs.clear();
+  return pairs;
 }
 
 void build_plan(const pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, int W, int num_splits,
@@ -502,19 +558,39 @@ void build_plan(const pkv_pool* p, int32_t n, const int32_t* ids, int mode, int 
   const auto& A = p->alloc;
   std::vector<Seg> segs;
   std::vector<int64_t> bg_units((size_t)n * Hk, 0);
-  for (int32_t b = 0; b < n; ++b) {
-    BlockRange r[2];
-    const int nr = keep_ranges(A.len[ids[b]], mode, S, W, r);
-    for (int g = 0; g < Hk; ++g)
-      for (int k = 0; k < nr; ++k) {
-        segs.push_back({b, g, r[k].lo, r[k].hi});
-        bg_units[(size_t)b * Hk + g] += r[k].hi - r[k].lo;
+  // whole keep-sets (no mask), automatic partition: shared prefixes are read
+  // once per sequence pair by the two-sequence kernel
+  std::vector<Pairing> pairs;
+  if (p->cascade && mode == 0 && num_splits <= 0 && n >= 2) pairs = pair_shared_prefixes(p, n, ids);
+  plan.nq = pairs.empty() ? 1 : 2;
+  if (!pairs.empty()) {
+    std::vector<int32_t> shared_of(n, 0);
+    for (const auto& pr : pairs) {
+      shared_of[pr.b0] = shared_of[pr.b1] = pr.shared;
+      for (int g = 0; g < Hk; ++g) segs.push_back({pr.b0, g, 0, pr.shared, pr.b1});
+    }
+    for (int32_t b = 0; b < n; ++b) {
+      const int32_t nb = ceil_div(A.len[ids[b]], kBlock);
+      for (int g = 0; g < Hk; ++g) {
+        if (shared_of[b] < nb) segs.push_back({b, g, shared_of[b], nb, -1});
+        bg_units[(size_t)b * Hk + g] = nb;
       }
+    }
+  } else {
+    for (int32_t b = 0; b < n; ++b) {
+      BlockRange r[2];
+      const int nr = keep_ranges(A.len[ids[b]], mode, S, W, r);
+      for (int g = 0; g < Hk; ++g)
+        for (int k = 0; k < nr; ++k) {
+          segs.push_back({b, g, r[k].lo, r[k].hi, -1});
+          bg_units[(size_t)b * Hk + g] += r[k].hi - r[k].lo;
+        }
+    }
   }
   plan.pieces.clear();
   plan.combine.clear();
   plan.warp_begin.clear();
-  const int TWmax = max_total_warps(p);
+  const int TWmax = max_total_warps(p, plan.nq);
   auto piece_of = [&](const Seg& s, int32_t lo, int32_t hi) {
     Piece pc;
     pc.seq_slot = ids[s.b];
@@ -525,6 +601,10 @@ void build_plan(const pkv_pool* p, int32_t n, const int32_t* ids, int mode, int 
     pc.ctx_len = A.len[ids[s.b]];
     pc.out_index = -1;
     pc.flags = 0;
+    pc.q_row1 = s.b1;
+    pc.out_index1 = -1;
+    pc.item1 = 0;
+    pc.pad = 0;
     return pc;
   };
   std::vector<int32_t> piece_warp;  // warp of each piece
@@ -594,34 +674,44 @@ void build_plan(const pkv_pool* p, int32_t n, const int32_t* ids, int mode, int 
         }
     }
   }
-  // runs: consecutive pieces of one (b, g) inside one warp; explicit split
-  // parts already carry their own run ends
+  // runs: consecutive pieces of one (b, g) -- or one sequence pair and g --
+  // inside one warp; explicit split parts already carry their own run ends
   const size_t np = plan.pieces.size();
   for (size_t k = 0; k < np; ++k) {
     const bool end_of_warp = k + 1 == np || piece_warp[k + 1] != piece_warp[k];
     const bool next_other = k + 1 == np || plan.pieces[k + 1].q_row != plan.pieces[k].q_row ||
-                            plan.pieces[k + 1].kv_head != plan.pieces[k].kv_head;
+                            plan.pieces[k + 1].kv_head != plan.pieces[k].kv_head ||
+                            plan.pieces[k + 1].q_row1 != plan.pieces[k].q_row1;
     if (end_of_warp || next_other) plan.pieces[k].flags |= kPieceLastOfRun;
   }
-  // partial indices: a run that covers all units of its (b, g) writes the
-  // final output; every other run gets a partial record
+  // partial records: a single-sequence run that covers all units of its
+  // (b, g) writes the final output; every other run writes one record per
+  // sequence.  Records of one (b, g) are consecutive: counted first, then
+  // numbered.
   std::vector<int32_t> first_partial((size_t)n * Hk, -1), n_part((size_t)n * Hk, 0);
-  int next_partial = 0;
+  auto run_units = [&](size_t k0, size_t k1) {
+    int64_t units = 0;
+    for (size_t j = k0; j <= k1; ++j) units += plan.pieces[j].lblk_end - plan.pieces[j].lblk_begin;
+    return units;
+  };
+  auto needs_record = [&](size_t k0, size_t k1) {
+    const Piece& pc = plan.pieces[k1];
+    return pc.q_row1 >= 0 || run_units(k0, k1) != bg_units[(size_t)pc.q_row * Hk + pc.kv_head];
+  };
   size_t run_start = 0;
   for (size_t k = 0; k < np; ++k) {
     if (!(plan.pieces[k].flags & kPieceLastOfRun)) continue;
-    const size_t bg = (size_t)plan.pieces[k].q_row * Hk + plan.pieces[k].kv_head;
-    int64_t units = 0;
-    for (size_t j = run_start; j <= k; ++j) units += plan.pieces[j].lblk_end - plan.pieces[j].lblk_begin;
-    int32_t idx = -1;
-    if (units != bg_units[bg]) {
-      idx = next_partial++;
-      if (first_partial[bg] < 0) first_partial[bg] = idx;
-      ++n_part[bg];
-    }
-    for (size_t j = run_start; j <= k; ++j) plan.pieces[j].out_index = idx;
+    const Piece& pc = plan.pieces[k];
+    if (needs_record(run_start, k)) ++n_part[(size_t)pc.q_row * Hk + pc.kv_head];
+    if (pc.q_row1 >= 0) ++n_part[(size_t)pc.q_row1 * Hk + pc.kv_head];
     run_start = k + 1;
   }
+  int next_partial = 0;
+  for (size_t bg = 0; bg < (size_t)n * Hk; ++bg)
+    if (n_part[bg] > 0) {
+      first_partial[bg] = next_partial;
+      next_partial += n_part[bg];
+    }
   plan.n_partials = next_partial;
   std::vector<int32_t> item_of((size_t)n * Hk, -1);
   for (int32_t b = 0; b < n; ++b)
@@ -634,14 +724,34 @@ void build_plan(const pkv_pool* p, int32_t n, const int32_t* ids, int mode, int 
         plan.combine.push_back({b, g, first_partial[bg], n_part[bg]});
       }
     }
-  for (auto& pc : plan.pieces)
-    if (pc.out_index >= 0) pc.flags |= item_of[(size_t)pc.q_row * Hk + pc.kv_head] << 1;
+  std::vector<int32_t> cursor(first_partial);
+  run_start = 0;
+  for (size_t k = 0; k < np; ++k) {
+    if (!(plan.pieces[k].flags & kPieceLastOfRun)) continue;
+    const Piece& pc = plan.pieces[k];
+    const size_t bg0 = (size_t)pc.q_row * Hk + pc.kv_head;
+    const int32_t idx0 = needs_record(run_start, k) ? cursor[bg0]++ : -1;
+    int32_t idx1 = -1, item1 = 0;
+    if (pc.q_row1 >= 0) {
+      const size_t bg1 = (size_t)pc.q_row1 * Hk + pc.kv_head;
+      idx1 = cursor[bg1]++;
+      item1 = item_of[bg1];
+    }
+    for (size_t j = run_start; j <= k; ++j) {
+      Piece& q = plan.pieces[j];
+      q.out_index = idx0;
+      if (idx0 >= 0) q.flags |= item_of[bg0] << 1;
+      q.out_index1 = idx1;
+      q.item1 = item1;
+    }
+    run_start = k + 1;
+  }
 
   // Physical placement: virtual warp v runs in CTA v % C as its warp v / C,
   // so that the work is spread over as many SMs as possible.
   const int TW = plan.total_warps;
-  const int WPC = std::max(1, p->tc_warps_per_cta);
-  const int C = std::max(1, std::min(TW, max_total_warps(p) / WPC));
+  const int WPC = warps_per_cta(p, plan.nq);
+  const int C = std::max(1, std::min(TW, max_total_warps(p, plan.nq) / WPC));
   std::vector<size_t> vstart(TW + 1, 0);
   {
     size_t k = 0;
@@ -688,11 +798,11 @@ struct PlanLayout {
   size_t wb = 0, pieces = 0, combine = 0, counters = 0, empty = 0, bytes = 0;
 };
 
-PlanLayout plan_layout(Plan& pl, int warps_per_cta, size_t base) {
+PlanLayout plan_layout(Plan& pl, int wpc, size_t base) {
   if (pl.total_warps == 0 && !pl.empty.empty()) {  // only empty keep-sets: one CTA writes them
     pl.ctas = 1;
-    pl.total_warps = warps_per_cta;
-    pl.warp_begin.assign(warps_per_cta + 1, 0);
+    pl.total_warps = wpc;
+    pl.warp_begin.assign(wpc + 1, 0);
   }
   auto up = [](size_t x) { return (x + 31) & ~size_t(31); };
   PlanLayout L;
@@ -752,7 +862,8 @@ pkv_status launch_tc_plan(pkv_pool* p, cudaStream_t st, const Plan& pl, const Pl
   prm.wait_limit_ns = p->wait_limit_ns;
   prm.starve_warp = p->starve_warp;
   p->starve_warp = -1;
-  return launch(p, PKV_KERNEL_DECODE, st, [&] { return launch_decode_tc(c.kv_dtype, p->G, prm, pl.ctas, st); });
+  return launch(p, PKV_KERNEL_DECODE, st,
+                [&] { return launch_decode_tc(c.kv_dtype, p->G, pl.nq, prm, pl.ctas, st); });
 }
 
 }  // namespace
@@ -817,7 +928,8 @@ int pkv::decode_attn_into(pkv_pool* p, void* stream, int32_t n, const int32_t* i
   // one blob: [cow pairs][patches][plan]
   auto up32 = [](size_t x) { return (x + 31) & ~size_t(31); };
   const size_t cow_off = 0, patch_off = up32(ncow * 2 * sizeof(int32_t));
-  const PlanLayout L = plan_layout(plan, p->tc_warps_per_cta, patch_off + patches.size() * sizeof(TablePatch));
+  const PlanLayout L =
+      plan_layout(plan, warps_per_cta(p, plan.nq), patch_off + patches.size() * sizeof(TablePatch));
   const size_t bytes = L.bytes;
   if (bytes > plan_cap)
     return fail(PKV_ERR_WORKSPACE, "needs %zu bytes of plan, the static scratch holds %zu", bytes, plan_cap);
@@ -916,13 +1028,17 @@ pkv_status pkv_pool_create(const pkv_pool_config* cfg, const pkv_pool_buffers* b
       p->tc_path = true;
       if (pkv_status r = make_tensor_map(&p->tmap_k, b.k_pool, p->cfg)) return fail_dev(r);
       if (pkv_status r = make_tensor_map(&p->tmap_v, b.v_pool, p->cfg)) return fail_dev(r);
-      e = decode_tc_prepare(cfg->kv_dtype, p->G);
-      int occ = 0;
-      if (e == cudaSuccess) e = decode_tc_occupancy(cfg->kv_dtype, p->G, &occ);
+      e = decode_tc_prepare(cfg->kv_dtype, p->G, 1);
+      if (e == cudaSuccess) e = decode_tc_prepare(cfg->kv_dtype, p->G, 2);
+      int occ = 0, occ2 = 0;
+      if (e == cudaSuccess) e = decode_tc_occupancy(cfg->kv_dtype, p->G, 1, &occ);
+      if (e == cudaSuccess) e = decode_tc_occupancy(cfg->kv_dtype, p->G, 2, &occ2);
       if (e != cudaSuccess) return fail_dev(fail(PKV_ERR_CUDA, "decode kernel setup failed: %s", cudaGetErrorString(e)));
       p->tc_ctas_per_sm = std::max(1, occ);
-      p->tc_warps_per_cta = decode_tc_warps_per_cta(cfg->kv_dtype);
-      p->tc_smem = decode_tc_smem_bytes(cfg->kv_dtype);
+      p->tc_warps_per_cta = decode_tc_warps_per_cta(cfg->kv_dtype, 1);
+      p->tc2_ctas_per_sm = std::max(1, occ2);
+      p->tc2_warps_per_cta = decode_tc_warps_per_cta(cfg->kv_dtype, 2);
+      p->tc_smem = decode_tc_smem_bytes(cfg->kv_dtype, 1);
     }
   }
   *out = p;
@@ -1348,7 +1464,7 @@ pkv_status pkv_decode_attn(pkv_pool* p, void* stream, int32_t n, const int32_t* 
     return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
   if (plan.n_partials > 0 && ((uintptr_t)workspace & 15))
     return fail(PKV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
-  const PlanLayout L = plan_layout(plan, p->tc_warps_per_cta, 0);
+  const PlanLayout L = plan_layout(plan, warps_per_cta(p, plan.nq), 0);
   StagingSlot* s;
   if (pkv_status r = p->staging.acquire(L.bytes, &s)) return r;
   plan_write(plan, L, s->host);
@@ -1493,6 +1609,12 @@ pkv_status pkv_set_wait_limit(pkv_pool* p, int64_t wait_limit_ns) {
   if (wait_limit_ns < 1000000 || wait_limit_ns > 60000000000LL)
     return fail(PKV_ERR_INVALID_ARG, "wait limit must lie in [1 ms, 60 s]");
   p->wait_limit_ns = (uint64_t)wait_limit_ns;
+  return PKV_OK;
+}
+
+pkv_status pkv_set_cascade(pkv_pool* p, int32_t enable) {
+  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  p->cascade = enable != 0;
   return PKV_OK;
 }
 
