@@ -369,6 +369,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=0, help="run N untimed steps and exit (for ncu)")
+    ap.add_argument("--no-cascade", action="store_true",
+                    help="every sequence reads its own blocks (no shared-prefix pairing)")
     ap.add_argument("--time-kernels", action="store_true",
                     help="bracket every kernel (not only decode) with events; adds gaps to the step")
     args = ap.parse_args()
@@ -391,6 +393,7 @@ def main():
     pkv.load()
 
     setup = Setup(wl, dev)
+    setup.cache.set_cascade(not args.no_cascade)
     st = Stepper(setup, splits)
     stream = torch.cuda.current_stream(dev)
     for _ in range(max(3, args.warmup)):
@@ -502,7 +505,8 @@ def main():
         "data": "synthetic (seeded N(0,1) K/V/Q; seeded uniform lengths)",
         "config": {"workload": wl.name, "batch": len(setup.ids), "n_heads": wl.n_heads,
                    "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim, "kv_dtype": wl.kv_dtype,
-                   "mask": wl.mask, "num_splits": splits, "context_tokens": sum(lens_step),
+                   "mask": wl.mask, "num_splits": splits, "cascade": not args.no_cascade,
+                   "context_tokens": sum(lens_step),
                    "kv_bytes_per_step": step_bytes, "l2": "KV pool larger than L2 (no flush needed)",
                    "parallelism": f"replicas x{ws}"},
         "tokens_per_s": round(ws * len(setup.ids) / (ms_step * 1e-3), 1),

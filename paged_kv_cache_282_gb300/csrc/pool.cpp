@@ -13,6 +13,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <memory>
 #include <numeric>
 #include <set>
 #include <string>
@@ -272,6 +273,14 @@ struct Timing {
 // the pool
 // ---------------------------------------------------------------------------
 
+namespace {
+struct PlanCache;  // the decode planner's reusable buffers
+void destroy_plan_cache(PlanCache* c);
+struct PlanCacheDeleter {
+  void operator()(PlanCache* c) const { destroy_plan_cache(c); }
+};
+}  // namespace
+
 struct pkv_pool {
   pkv_pool_config cfg{};
   bool device = false;
@@ -290,6 +299,9 @@ struct pkv_pool {
   int G = 1;
   uint64_t wait_limit_ns = 4000000000ull;  // bound of the decode kernel's waits
   int32_t starve_warp = -1;                // one-shot wait-expiry test hook
+  // Vectors reused by every decode plan: fresh ones each call would spend
+  // most of the planning time faulting in new pages.
+  std::unique_ptr<PlanCache, PlanCacheDeleter> plan_cache;
 };
 
 namespace {
@@ -489,6 +501,29 @@ struct Seg {
   int32_t b1;            // >= 0: a second sequence over the same physical blocks
 };
 
+struct PlanRun {
+  size_t begin, end;  // pieces [begin, end)
+  bool record0;       // the first sequence writes a partial record
+};
+
+struct PlanCache {
+  Plan plan;
+  std::vector<Seg> segs;
+  std::vector<int64_t> bg_units;
+  std::vector<int32_t> piece_warp, first_partial, n_part, item_of, cursor;
+  std::vector<PlanRun> runs;
+  std::vector<size_t> vstart;
+  std::vector<Piece> ordered;
+  std::vector<char> blob;
+};
+
+void destroy_plan_cache(PlanCache* c) { delete c; }
+
+PlanCache& plan_cache(pkv_pool* p) {
+  if (!p->plan_cache) p->plan_cache.reset(new PlanCache());
+  return *p->plan_cache;
+}
+
 int warps_per_cta(const pkv_pool* p, int nq) {
   return std::max(1, nq == 2 ? p->tc2_warps_per_cta : p->tc_warps_per_cta);
 }
@@ -509,71 +544,107 @@ size_t max_pieces(const pkv_pool* p, int32_t n_seqs, int32_t num_splits) {
   return std::max(std::max(a, b), c);
 }
 
-// Shared-prefix pairing for decode over whole keep-sets: sequences sorted by
-// their block tables, then adjacent ones paired while they share leading
-// blocks that are full in both (the same physical block at the same logical
-// index holds the same 16 tokens for both).  Returns (b0, b1, shared blocks)
-// triples, or nothing when the pairs would save less than an eighth of all
-// block reads.
+// Shared-prefix pairing for decode over whole keep-sets.  Blocks are shared
+// only through forks and replaced only at the tail (append, copy-on-write,
+// truncate) or all at once (compaction), so two sequences that hold the same
+// physical block at logical index k share every block before it as well.
+// Pairs are formed first among sequences whose last full blocks coincide
+// (they share every full block), then among the rest that share their first
+// block; the shared length is then measured entry by entry.  Returns
+// (b0, b1, shared blocks) triples, or nothing when the pairs would save less
+// than an eighth of the batch's block reads.
 struct Pairing {
   int32_t b0, b1, shared;
 };
 
 std::vector<Pairing> pair_shared_prefixes(const pkv_pool* p, int32_t n, const int32_t* ids) {
   const auto& A = p->alloc;
-  std::vector<int32_t> order(n);
-  for (int32_t b = 0; b < n; ++b) order[b] = b;
-  auto nblk = [&](int32_t b) { return ceil_div(A.len[ids[b]], kBlock); };
-  auto entry = [&](int32_t b, int32_t lb) { return A.table[ids[b]][lb]; };
-  std::sort(order.begin(), order.end(), [&](int32_t x, int32_t y) {
-    const int32_t nx = nblk(x), ny = nblk(y);
-    for (int32_t lb = 0; lb < std::min(nx, ny); ++lb)
-      if (entry(x, lb) != entry(y, lb)) return entry(x, lb) < entry(y, lb);
-    if (nx != ny) return nx < ny;
-    return x < y;
-  });
+  auto full = [&](int32_t b) { return A.len[ids[b]] / kBlock; };
+  auto row = [&](int32_t b) { return A.table[ids[b]].data(); };
   std::vector<Pairing> pairs;
-  int64_t saved = 0, total = 0;
-  for (int32_t b = 0; b < n; ++b) total += nblk(b);
-  for (int32_t i = 0; i + 1 < n;) {
-    const int32_t x = order[i], y = order[i + 1];
-    const int32_t full = std::min(A.len[ids[x]], A.len[ids[y]]) / kBlock;
-    int32_t c = 0;
-    while (c < full && entry(x, c) >= 0 && entry(x, c) == entry(y, c)) ++c;
-    if (c > 0) {
-      pairs.push_back({std::min(x, y), std::max(x, y), c});
-      saved += c;
-      i += 2;
-    } else {
-      i += 1;
+  std::vector<uint8_t> used(n, 0);
+  std::vector<std::pair<int64_t, int32_t>> keyed;
+  keyed.reserve(n);
+  auto pair_adjacent = [&]() {
+    std::sort(keyed.begin(), keyed.end());
+    for (size_t i = 0; i + 1 < keyed.size();) {
+      if (keyed[i].first != keyed[i + 1].first) {
+        ++i;
+        continue;
+      }
+      const int32_t x = keyed[i].second, y = keyed[i + 1].second;
+      const int32_t lim = std::min(full(x), full(y));
+      // shared blocks form a prefix: the last equal entry, by bisection
+      int32_t c = 0, hi = lim;
+      if (lim > 0 && row(x)[lim - 1] == row(y)[lim - 1]) {
+        c = lim;
+      } else {
+        while (c < hi) {  // invariant: entries below c equal, entry hi - 1 differs (or hi = lim)
+          const int32_t mid = (c + hi) / 2;
+          if (row(x)[mid] == row(y)[mid]) c = mid + 1; else hi = mid;
+        }
+      }
+      if (c > 0) {
+        pairs.push_back({std::min(x, y), std::max(x, y), c});
+        used[x] = used[y] = 1;
+        i += 2;
+      } else {
+        ++i;
+      }
     }
-  }
+  };
+  // (full-block count, last full block): identical full blocks
+  for (int32_t b = 0; b < n; ++b)
+    if (full(b) > 0 && row(b)[full(b) - 1] >= 0) keyed.push_back({((int64_t)full(b) << 32) | row(b)[full(b) - 1], b});
+  pair_adjacent();
+  // the rest: a common first block
+  keyed.clear();
+  for (int32_t b = 0; b < n; ++b)
+    if (!used[b] && full(b) > 0 && row(b)[0] >= 0) keyed.push_back({row(b)[0], b});
+  pair_adjacent();
+  int64_t saved = 0, total = 0;
+  for (int32_t b = 0; b < n; ++b) total += ceil_div(A.len[ids[b]], kBlock);
+  for (const auto& pr : pairs) saved += pr.shared;
   if (saved * 8 < total) pairs.clear();
   return pairs;
 }
 
-void build_plan(const pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, int W, int num_splits,
-                Plan& plan) {
+// Fills plan = the pool's cached plan; the returned reference stays valid
+// until the next call.
+Plan& build_plan(pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, int W, int num_splits) {
   const int Hk = p->cfg.n_kv_heads;
   const auto& A = p->alloc;
-  std::vector<Seg> segs;
-  std::vector<int64_t> bg_units((size_t)n * Hk, 0);
+  PlanCache& cache = plan_cache(p);
+  Plan& plan = cache.plan;
+  plan.empty.clear();
+  plan.total_warps = plan.ctas = plan.n_partials = 0;
+  std::vector<Seg>& segs = cache.segs;
+  segs.clear();
+  std::vector<int64_t>& bg_units = cache.bg_units;
+  bg_units.assign((size_t)n * Hk, 0);
   // whole keep-sets (no mask), automatic partition: shared prefixes are read
   // once per sequence pair by the two-sequence kernel
   std::vector<Pairing> pairs;
   if (p->cascade && mode == 0 && num_splits <= 0 && n >= 2) pairs = pair_shared_prefixes(p, n, ids);
   plan.nq = pairs.empty() ? 1 : 2;
   if (!pairs.empty()) {
-    std::vector<int32_t> shared_of(n, 0);
+    // each pair's shared segment is followed by the two remainders, so the
+    // short remainder runs (and the merges they end with) spread over all
+    // warps instead of piling up at the end of the unit list
+    std::vector<uint8_t> paired(n, 0);
+    auto nblk = [&](int32_t b) { return ceil_div(A.len[ids[b]], kBlock); };
     for (const auto& pr : pairs) {
-      shared_of[pr.b0] = shared_of[pr.b1] = pr.shared;
-      for (int g = 0; g < Hk; ++g) segs.push_back({pr.b0, g, 0, pr.shared, pr.b1});
+      paired[pr.b0] = paired[pr.b1] = 1;
+      for (int g = 0; g < Hk; ++g) {
+        segs.push_back({pr.b0, g, 0, pr.shared, pr.b1});
+        if (pr.shared < nblk(pr.b0)) segs.push_back({pr.b0, g, pr.shared, nblk(pr.b0), -1});
+        if (pr.shared < nblk(pr.b1)) segs.push_back({pr.b1, g, pr.shared, nblk(pr.b1), -1});
+      }
     }
     for (int32_t b = 0; b < n; ++b) {
-      const int32_t nb = ceil_div(A.len[ids[b]], kBlock);
       for (int g = 0; g < Hk; ++g) {
-        if (shared_of[b] < nb) segs.push_back({b, g, shared_of[b], nb, -1});
-        bg_units[(size_t)b * Hk + g] = nb;
+        if (!paired[b] && nblk(b) > 0) segs.push_back({b, g, 0, nblk(b), -1});
+        bg_units[(size_t)b * Hk + g] = nblk(b);
       }
     }
   } else {
@@ -607,21 +678,39 @@ void build_plan(const pkv_pool* p, int32_t n, const int32_t* ids, int mode, int 
     pc.pad = 0;
     return pc;
   };
-  std::vector<int32_t> piece_warp;  // warp of each piece
+  std::vector<int32_t>& piece_warp = cache.piece_warp;  // warp of each piece
+  piece_warp.clear();
   if (num_splits <= 0) {
     int64_t U = 0;
     for (auto& s : segs) U += s.hi - s.lo;
     int TW = (int)std::min<int64_t>(TWmax, (U + kMinUnitsPerWarp - 1) / kMinUnitsPerWarp);
     plan.total_warps = TW;
     if (TW > 0) {
-      auto bound = [&](int w) { return (int64_t)((__int128)U * w / TW); };
+      plan.pieces.reserve(segs.size() + TW);
+      piece_warp.reserve(segs.size() + TW);
+      // warp w takes units [floor(U w / TW), floor(U (w + 1) / TW)); the
+      // bounds advance by U / TW plus a carry of the remainder, no division
+      const int64_t q = U / TW, r = U % TW;
+      int64_t next = q + (r >= TW ? 1 : 0), carry = r;  // bound of warp 1
+      if (carry >= TW) carry -= TW;
+      auto step_bound = [&]() {
+        carry += r;
+        next += q;
+        if (carry >= TW) {
+          carry -= TW;
+          ++next;
+        }
+      };
       int w = 0;
       int64_t pos = 0;
       for (auto& s : segs) {
         int64_t start = pos, end = pos + (s.hi - s.lo);
         while (start < end) {
-          while (bound(w + 1) <= start) ++w;
-          int64_t stop = std::min(end, bound(w + 1));
+          while (next <= start) {
+            ++w;
+            step_bound();
+          }
+          const int64_t stop = std::min(end, next);
           plan.pieces.push_back(piece_of(s, s.lo + (int32_t)(start - pos), s.lo + (int32_t)(stop - pos)));
           piece_warp.push_back(w);
           start = stop;
@@ -688,23 +777,26 @@ void build_plan(const pkv_pool* p, int32_t n, const int32_t* ids, int mode, int 
   // (b, g) writes the final output; every other run writes one record per
   // sequence.  Records of one (b, g) are consecutive: counted first, then
   // numbered.
-  std::vector<int32_t> first_partial((size_t)n * Hk, -1), n_part((size_t)n * Hk, 0);
-  auto run_units = [&](size_t k0, size_t k1) {
+  std::vector<int32_t>& first_partial = cache.first_partial;
+  std::vector<int32_t>& n_part = cache.n_part;
+  first_partial.assign((size_t)n * Hk, -1);
+  n_part.assign((size_t)n * Hk, 0);
+  std::vector<PlanRun>& runs = cache.runs;
+  runs.clear();
+  {
+    size_t start = 0;
     int64_t units = 0;
-    for (size_t j = k0; j <= k1; ++j) units += plan.pieces[j].lblk_end - plan.pieces[j].lblk_begin;
-    return units;
-  };
-  auto needs_record = [&](size_t k0, size_t k1) {
-    const Piece& pc = plan.pieces[k1];
-    return pc.q_row1 >= 0 || run_units(k0, k1) != bg_units[(size_t)pc.q_row * Hk + pc.kv_head];
-  };
-  size_t run_start = 0;
-  for (size_t k = 0; k < np; ++k) {
-    if (!(plan.pieces[k].flags & kPieceLastOfRun)) continue;
-    const Piece& pc = plan.pieces[k];
-    if (needs_record(run_start, k)) ++n_part[(size_t)pc.q_row * Hk + pc.kv_head];
-    if (pc.q_row1 >= 0) ++n_part[(size_t)pc.q_row1 * Hk + pc.kv_head];
-    run_start = k + 1;
+    for (size_t k = 0; k < np; ++k) {
+      const Piece& pc = plan.pieces[k];
+      units += pc.lblk_end - pc.lblk_begin;
+      if (!(pc.flags & kPieceLastOfRun)) continue;
+      const bool rec0 = pc.q_row1 >= 0 || units != bg_units[(size_t)pc.q_row * Hk + pc.kv_head];
+      runs.push_back({start, k + 1, rec0});
+      if (rec0) ++n_part[(size_t)pc.q_row * Hk + pc.kv_head];
+      if (pc.q_row1 >= 0) ++n_part[(size_t)pc.q_row1 * Hk + pc.kv_head];
+      start = k + 1;
+      units = 0;
+    }
   }
   int next_partial = 0;
   for (size_t bg = 0; bg < (size_t)n * Hk; ++bg)
@@ -713,7 +805,8 @@ void build_plan(const pkv_pool* p, int32_t n, const int32_t* ids, int mode, int 
       next_partial += n_part[bg];
     }
   plan.n_partials = next_partial;
-  std::vector<int32_t> item_of((size_t)n * Hk, -1);
+  std::vector<int32_t>& item_of = cache.item_of;
+  item_of.assign((size_t)n * Hk, -1);
   for (int32_t b = 0; b < n; ++b)
     for (int g = 0; g < Hk; ++g) {
       const size_t bg = (size_t)b * Hk + g;
@@ -724,27 +817,25 @@ void build_plan(const pkv_pool* p, int32_t n, const int32_t* ids, int mode, int 
         plan.combine.push_back({b, g, first_partial[bg], n_part[bg]});
       }
     }
-  std::vector<int32_t> cursor(first_partial);
-  run_start = 0;
-  for (size_t k = 0; k < np; ++k) {
-    if (!(plan.pieces[k].flags & kPieceLastOfRun)) continue;
-    const Piece& pc = plan.pieces[k];
+  std::vector<int32_t>& cursor = cache.cursor;
+  cursor = first_partial;
+  for (const PlanRun& ru : runs) {
+    const Piece& pc = plan.pieces[ru.end - 1];
     const size_t bg0 = (size_t)pc.q_row * Hk + pc.kv_head;
-    const int32_t idx0 = needs_record(run_start, k) ? cursor[bg0]++ : -1;
+    const int32_t idx0 = ru.record0 ? cursor[bg0]++ : -1;
     int32_t idx1 = -1, item1 = 0;
     if (pc.q_row1 >= 0) {
       const size_t bg1 = (size_t)pc.q_row1 * Hk + pc.kv_head;
       idx1 = cursor[bg1]++;
       item1 = item_of[bg1];
     }
-    for (size_t j = run_start; j <= k; ++j) {
+    for (size_t j = ru.begin; j < ru.end; ++j) {
       Piece& q = plan.pieces[j];
       q.out_index = idx0;
       if (idx0 >= 0) q.flags |= item_of[bg0] << 1;
       q.out_index1 = idx1;
       q.item1 = item1;
     }
-    run_start = k + 1;
   }
 
   // Physical placement: virtual warp v runs in CTA v % C as its warp v / C,
@@ -752,7 +843,8 @@ void build_plan(const pkv_pool* p, int32_t n, const int32_t* ids, int mode, int 
   const int TW = plan.total_warps;
   const int WPC = warps_per_cta(p, plan.nq);
   const int C = std::max(1, std::min(TW, max_total_warps(p, plan.nq) / WPC));
-  std::vector<size_t> vstart(TW + 1, 0);
+  std::vector<size_t>& vstart = cache.vstart;
+  vstart.assign(TW + 1, 0);
   {
     size_t k = 0;
     for (int v = 0; v < TW; ++v) {
@@ -761,20 +853,24 @@ void build_plan(const pkv_pool* p, int32_t n, const int32_t* ids, int mode, int 
     }
     vstart[TW] = k;
   }
-  std::vector<Piece> ordered;
-  ordered.reserve(np);
+  std::vector<Piece>& ordered = cache.ordered;
+  ordered.resize(np);
   const int slots = TW > 0 ? C * WPC : 0;
   plan.warp_begin.assign(slots + 1, 0);
+  size_t filled = 0;
   for (int phys = 0; phys < slots; ++phys) {
-    plan.warp_begin[phys] = (int32_t)ordered.size();
+    plan.warp_begin[phys] = (int32_t)filled;
     const int v = (phys % WPC) * C + phys / WPC;
-    if (v < TW)
-      for (size_t k = vstart[v]; k < vstart[v + 1]; ++k) ordered.push_back(plan.pieces[k]);
+    if (v < TW) {
+      std::copy(plan.pieces.begin() + vstart[v], plan.pieces.begin() + vstart[v + 1], ordered.begin() + filled);
+      filled += vstart[v + 1] - vstart[v];
+    }
   }
-  plan.warp_begin[slots] = (int32_t)ordered.size();
+  plan.warp_begin[slots] = (int32_t)filled;
   plan.pieces.swap(ordered);
   plan.total_warps = slots;
   plan.ctas = TW > 0 ? C : 0;
+  return plan;
 }
 
 pkv_status check_keep_blocks_present(const pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, int W) {
@@ -918,8 +1014,8 @@ int pkv::decode_attn_into(pkv_pool* p, void* stream, int32_t n, const int32_t* i
     }
     waves.push_back(ncow);
   }
-  Plan plan;
-  if (n > 0) build_plan(p, n, ids, mode, S, W, num_splits, plan);
+  Plan empty_plan;
+  Plan& plan = n > 0 ? build_plan(p, n, ids, mode, S, W, num_splits) : empty_plan;
   const size_t pf = (size_t)partial_floats(p->G, c.head_dim) * sizeof(float);
   if ((size_t)plan.n_partials * pf > partials_cap)
     return fail(PKV_ERR_WORKSPACE, "needs %zu bytes of partial records, the static scratch holds %zu",
@@ -933,7 +1029,8 @@ int pkv::decode_attn_into(pkv_pool* p, void* stream, int32_t n, const int32_t* i
   const size_t bytes = L.bytes;
   if (bytes > plan_cap)
     return fail(PKV_ERR_WORKSPACE, "needs %zu bytes of plan, the static scratch holds %zu", bytes, plan_cap);
-  std::vector<char> blob(bytes);
+  std::vector<char>& blob = plan_cache(p).blob;
+  if (blob.size() < bytes) blob.resize(bytes);
   if (ncow) memcpy(blob.data() + cow_off, A.pending_cow.data(), ncow * 2 * sizeof(int32_t));
   if (!patches.empty()) memcpy(blob.data() + patch_off, patches.data(), patches.size() * sizeof(TablePatch));
   plan_write(plan, L, blob.data());
@@ -1457,8 +1554,7 @@ pkv_status pkv_decode_attn(pkv_pool* p, void* stream, int32_t n, const int32_t* 
 
   size_t need = 0;
   pkv_decode_workspace_size(p, n, num_splits, &need);
-  Plan plan;
-  build_plan(p, n, ids, mode, S, W, num_splits, plan);
+  Plan& plan = build_plan(p, n, ids, mode, S, W, num_splits);
   const size_t pf = (size_t)partial_floats(p->G, c.head_dim) * sizeof(float);
   if (plan.n_partials > 0 && (!workspace || workspace_bytes < plan.n_partials * pf))
     return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
