@@ -30,7 +30,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "pkv_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 
-KV_FP32, KV_BF16, KV_FP8 = 0, 1, 2
+KV_FP32, KV_BF16, KV_FP8, KV_INT8 = 0, 1, 2, 3
 MASK_FULL, MASK_SLIDING, MASK_SINK_WINDOW = 0, 1, 2
 BLOCK = 16
 
@@ -67,7 +67,10 @@ def _load():
         lib.oracle_keep.argtypes = [c_int] * 5
         lib.oracle_keep.restype = c_int
         lib.oracle_scatter.argtypes = [vp, c_int, c_int, c_int, vp, c_int, vp]
-        lib.oracle_quantize_scatter.argtypes = [vp, vp, c_int, c_int, vp, c_int, vp]
+        lib.oracle_quantize_scatter.argtypes = [vp, vp, c_int, c_int, vp, c_int, vp, c_int]
+        lib.oracle_int8_encode.argtypes = [ctypes.c_float]
+        lib.oracle_int8_encode.restype = ctypes.c_int8
+        lib.oracle_quantize_row_int8.argtypes = [vp, c_int, vp, vp]
         lib.oracle_copy_block.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int]
         lib.oracle_decode.argtypes = [c_int, c_int, c_int, c_int, c_int, vp, vp, vp, vp, c_int,
                                       vp, c_int, vp, c_int, vp, c_dbl, c_int, c_int, c_int,
@@ -159,6 +162,20 @@ def e4m3_encode_array(x: np.ndarray) -> np.ndarray:
                        count=flat.size).reshape(np.shape(x))
 
 
+def int8_encode(x: float) -> int:
+    return int(_load().oracle_int8_encode(float(x)))
+
+
+def quantize_row_int8(row_bits: np.ndarray):
+    """row_bits: uint16 bf16 bit patterns [D] -> (codes int8 [D], scale fp32)."""
+    lib = _load()
+    row_bits = _c(row_bits, np.uint16)
+    codes = np.empty(row_bits.size, dtype=np.int8)
+    scale = np.zeros(1, dtype=np.float32)
+    lib.oracle_quantize_row_int8(_ptr(row_bits), row_bits.size, _ptr(codes), _ptr(scale))
+    return codes, float(scale[0])
+
+
 def quantize_row_bf16(row_bits: np.ndarray):
     """row_bits: uint16 bf16 bit patterns [D] -> (codes uint8 [D], scale fp32)."""
     lib = _load()
@@ -190,11 +207,11 @@ class OraclePool:
 
     def __init__(self, num_blocks: int, n_kv_heads: int, head_dim: int, kv_dtype: int):
         self.NB, self.Hk, self.D, self.kv_dtype = num_blocks, n_kv_heads, head_dim, kv_dtype
-        dt = {KV_FP32: np.float32, KV_BF16: np.uint16, KV_FP8: np.uint8}[kv_dtype]
+        dt = {KV_FP32: np.float32, KV_BF16: np.uint16, KV_FP8: np.uint8, KV_INT8: np.int8}[kv_dtype]
         shape = (num_blocks, n_kv_heads, BLOCK, head_dim)
         self.k = np.zeros(shape, dtype=dt)
         self.v = np.zeros(shape, dtype=dt)
-        if kv_dtype == KV_FP8:
+        if kv_dtype in (KV_FP8, KV_INT8):
             self.k_scale = np.zeros(shape[:3], dtype=np.float32)
             self.v_scale = np.zeros(shape[:3], dtype=np.float32)
         else:
@@ -206,12 +223,12 @@ class OraclePool:
         lib = _load()
         slots = _c(slots, np.int64)
         T = slots.size
-        if self.kv_dtype == KV_FP8:
+        if self.kv_dtype in (KV_FP8, KV_INT8):
             kb, vb = _c(k_rows, np.uint16), _c(v_rows, np.uint16)
             lib.oracle_quantize_scatter(_ptr(self.k), _ptr(self.k_scale), self.Hk, self.D,
-                                        _ptr(slots), T, _ptr(kb))
+                                        _ptr(slots), T, _ptr(kb), self.kv_dtype)
             lib.oracle_quantize_scatter(_ptr(self.v), _ptr(self.v_scale), self.Hk, self.D,
-                                        _ptr(slots), T, _ptr(vb))
+                                        _ptr(slots), T, _ptr(vb), self.kv_dtype)
         else:
             dt = np.float32 if self.kv_dtype == KV_FP32 else np.uint16
             kb, vb = _c(k_rows, dt), _c(v_rows, dt)
@@ -220,13 +237,13 @@ class OraclePool:
             lib.oracle_scatter(_ptr(self.v), self.Hk, self.D, es, _ptr(slots), T, _ptr(vb))
 
     def copy_rows(self, src_slots, dst_slots) -> None:
-        es = {KV_FP32: 4, KV_BF16: 2, KV_FP8: 1}[self.kv_dtype]
+        es = {KV_FP32: 4, KV_BF16: 2, KV_FP8: 1, KV_INT8: 1}[self.kv_dtype]
         src, dst = _c(src_slots, np.int64), _c(dst_slots, np.int64)
         _load().oracle_copy_rows(_ptr(self.k), _ptr(self.v), _ptr(self.k_scale), _ptr(self.v_scale), self.Hk,
                                  self.D, es, _ptr(src), _ptr(dst), src.size)
 
     def copy_block(self, src: int, dst: int) -> None:
-        es = {KV_FP32: 4, KV_BF16: 2, KV_FP8: 1}[self.kv_dtype]
+        es = {KV_FP32: 4, KV_BF16: 2, KV_FP8: 1, KV_INT8: 1}[self.kv_dtype]
         _load().oracle_copy_block(_ptr(self.k), _ptr(self.v), _ptr(self.k_scale),
                                   _ptr(self.v_scale), self.Hk, self.D, es, src, dst)
 

@@ -36,7 +36,7 @@
 
 #define ORACLE_BLOCK 16 /* [PA] PagedAttention design: fixed blocks of 16 tokens by default */
 
-enum { KV_FP32 = 0, KV_BF16 = 1, KV_FP8 = 2 };
+enum { KV_FP32 = 0, KV_BF16 = 1, KV_FP8 = 2, KV_INT8 = 3 };
 enum { MASK_FULL = 0, MASK_SLIDING = 1, MASK_SINK_WINDOW = 2 };
 
 /* ------------------------------------------------------------------------- */
@@ -134,6 +134,37 @@ void oracle_quantize_row_bf16(const uint16_t* x, int D, uint8_t* codes, float* s
   *scale = s;
 }
 
+/* fp32 -> symmetric INT8: round to nearest, ties to even, then clamp to
+ * [-127, 127] (-128 is never produced, so the code range is symmetric). */
+int8_t oracle_int8_encode(float x) {
+  double a = fabs((double)x);
+  int n;
+  if (a != a) return 0;
+  if (a > 127.0) a = 127.0;
+  n = round_half_even(a);
+  if (n > 127) n = 127;
+  return (int8_t)(x < 0.0f ? -n : n);
+}
+
+/* Per-token INT8 quantisation of one (token, kv_head) row of D bf16 values
+ * ([PA] KV quantisation, FP16 -> INT8 with per-token scaling).  Reading
+ * adopted: symmetric, s = absmax / 127 in fp32 (s = 1 when absmax == 0),
+ * code_d = INT8(x_d / s) with the quotient rounded to fp32 first. */
+void oracle_quantize_row_int8(const uint16_t* x, int D, int8_t* codes, float* scale) {
+  float amax = 0.0f, s;
+  int d;
+  for (d = 0; d < D; d++) {
+    float v = fabsf(bf16_bits_to_float(x[d]));
+    if (v > amax) amax = v;
+  }
+  s = (amax == 0.0f) ? 1.0f : amax / 127.0f;
+  for (d = 0; d < D; d++) {
+    float q = bf16_bits_to_float(x[d]) / s;
+    codes[d] = oracle_int8_encode(q);
+  }
+  *scale = s;
+}
+
 /* ------------------------------------------------------------------------- */
 /* Keep-set predicates.                                                       */
 /*   FULL:         every j in [0, L).                                         */
@@ -183,13 +214,14 @@ void oracle_scatter(void* pool, int Hk, int D, int elem_bytes, const int64_t* sl
   }
 }
 
-/* FP8 variant: quantise each (token, kv_head) row of bf16 and scatter codes and
- * the per-token scale (scale pool layout [block][kv_head][slot]).  Tokens are
- * independent (distinct slots), so they are spread over the host's cores. */
+/* Quantised variants (FP8 E4M3 or INT8): quantise each (token, kv_head) row
+ * of bf16 and scatter codes and the per-token scale (scale pool layout
+ * [block][kv_head][slot]).  Tokens are independent (distinct slots), so they
+ * are spread over the host's cores. */
 typedef struct {
   uint8_t* pool;
   float* scale_pool;
-  int Hk, D, T, thread_id, n_threads;
+  int Hk, D, T, thread_id, n_threads, kv_dtype;
   const int64_t* slots;
   const uint16_t* src;
 } quantize_job;
@@ -202,15 +234,19 @@ static void* quantize_worker(void* arg) {
     for (g = 0; g < q->Hk; g++) {
       size_t di = pool_index(block, q->Hk, g, slot, q->D, 0);
       size_t si = ((size_t)block * q->Hk + g) * ORACLE_BLOCK + slot;
-      oracle_quantize_row_bf16(q->src + ((size_t)t * q->Hk + g) * q->D, q->D, q->pool + di,
-                               q->scale_pool + si);
+      if (q->kv_dtype == KV_INT8)
+        oracle_quantize_row_int8(q->src + ((size_t)t * q->Hk + g) * q->D, q->D, (int8_t*)(q->pool + di),
+                                 q->scale_pool + si);
+      else
+        oracle_quantize_row_bf16(q->src + ((size_t)t * q->Hk + g) * q->D, q->D, q->pool + di,
+                                 q->scale_pool + si);
     }
   }
   return NULL;
 }
 
 void oracle_quantize_scatter(uint8_t* pool, float* scale_pool, int Hk, int D, const int64_t* slots, int T,
-                             const uint16_t* src) {
+                             const uint16_t* src, int kv_dtype) {
   long ncpu = sysconf(_SC_NPROCESSORS_ONLN);
   int n = (int)(ncpu > 0 ? ncpu : 1), i;
   quantize_job* jobs;
@@ -229,6 +265,7 @@ void oracle_quantize_scatter(uint8_t* pool, float* scale_pool, int Hk, int D, co
     jobs[i].n_threads = n;
     jobs[i].slots = slots;
     jobs[i].src = src;
+    jobs[i].kv_dtype = kv_dtype;
     pthread_create(&th[i], NULL, quantize_worker, &jobs[i]);
   }
   for (i = 0; i < n; i++) pthread_join(th[i], NULL);
@@ -303,6 +340,7 @@ static double kv_value(const decode_job* jb, const void* pool, const float* scl,
   if (jb->kv_dtype == KV_BF16) return bf16_bits_to_double(((const uint16_t*)pool)[i]);
   {
     size_t si = ((size_t)block * jb->Hk + g) * ORACLE_BLOCK + slot;
+    if (jb->kv_dtype == KV_INT8) return (double)((const int8_t*)pool)[i] * (double)scl[si];
     return oracle_e4m3_decode(((const uint8_t*)pool)[i]) * (double)scl[si];
   }
 }

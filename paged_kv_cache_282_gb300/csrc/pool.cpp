@@ -584,6 +584,10 @@ std::vector<Pairing> pair_shared_prefixes(const pkv_pool* p, int32_t n, const in
           if (row(x)[mid] == row(y)[mid]) c = mid + 1; else hi = mid;
         }
       }
+      // the prefix property is what the tables guarantee; a mismatch inside
+      // the found prefix (never expected) falls back to the exact scan
+      if (c > 0 && memcmp(row(x), row(y), (size_t)c * sizeof(int32_t)) != 0)
+        c = (int32_t)(std::mismatch(row(x), row(x) + c, row(y)).first - row(x));
       if (c > 0) {
         pairs.push_back({std::min(x, y), std::max(x, y), c});
         used[x] = used[y] = 1;

@@ -34,6 +34,11 @@ MUTANTS = {
                                               "for (j = 0; j + 1 < heavy && j < L; j++) heavy_hit[c[j].pos] = 1;"),
     "compaction keeps the old blocks": ("      if (*e >= 0) drop_block(w, *e);\n      *e = -1;",
                                         "      *e = -1;"),
+    "int8 quantiser divides by 128": ("s = (amax == 0.0f) ? 1.0f : amax / 127.0f;",
+                                      "s = (amax == 0.0f) ? 1.0f : amax / 128.0f;"),
+    "int8 codes truncate": ("  n = round_half_even(a);\n  if (n > 127) n = 127;", "  n = (int)a;\n  if (n > 127) n = 127;"),
+    "int8 codes read unsigned": ("if (jb->kv_dtype == KV_INT8) return (double)((const int8_t*)pool)[i] * (double)scl[si];",
+                                 "if (jb->kv_dtype == KV_INT8) return (double)((const uint8_t*)pool)[i] * (double)scl[si];"),
     "token slot shifted": ("    slot = j % ORACLE_BLOCK;\n    if (block < 0 || block >= jb->num_blocks) {",
                            "    slot = (j + 1) % ORACLE_BLOCK;\n    if (block < 0 || block >= jb->num_blocks) {"),
 }

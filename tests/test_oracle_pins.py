@@ -168,6 +168,43 @@ def test_quantize_row_per_token_scale():
     assert s == 1.0 and not codes.any()
 
 
+def test_int8_encode_rounds_half_to_even_and_clamps():
+    for x, want in ((0.5, 0), (1.5, 2), (2.5, 2), (-2.5, -2), (-3.5, -4), (126.5, 126), (0.49999997, 0),
+                    (127.0, 127), (127.4, 127), (127.6, 127), (300.0, 127), (-1e9, -127), (float("inf"), 127),
+                    (-0.0, 0), (float("nan"), 0)):
+        assert oracle.int8_encode(x) == want, x
+
+
+def test_int8_encode_matches_numpy_rounding():
+    rng = np.random.default_rng(17)
+    x = (rng.standard_normal(100_000) * 60).astype(np.float32)
+    x[:2000] = np.round(x[:2000]) + 0.5  # exact ties
+    want = np.clip(np.rint(x.astype(np.float64)), -127, 127).astype(np.int8)
+    got = np.array([oracle.int8_encode(float(v)) for v in x], dtype=np.int8)
+    assert np.array_equal(got, want)
+
+
+def test_quantize_row_int8_per_token_scale():
+    rng = np.random.default_rng(4)
+    for trial in range(200):
+        D = 128 if trial % 2 else 64
+        x = torch.from_numpy(rng.standard_normal(D).astype(np.float32) * 10 ** rng.uniform(-3, 3))
+        bits = workloads.as_bits(x.to(torch.bfloat16))
+        xf = x.to(torch.bfloat16).float().numpy()
+        codes, s = oracle.quantize_row_int8(bits)
+        amax = float(np.max(np.abs(xf)))
+        i = int(np.argmax(np.abs(xf)))
+        # the largest magnitude lands on +-127; the scale is absmax / 127
+        assert codes[i] == (-127 if xf[i] < 0 else 127)
+        assert abs(s * 127.0 - amax) <= amax * 2 ** -22
+        # every code is numpy's half-to-even rounding of the fp32 quotient
+        q = (xf / np.float32(s)).astype(np.float32)
+        assert np.array_equal(codes, np.clip(np.rint(q), -127, 127).astype(np.int8))
+        # dequantisation error within half a step (plus the quotient's rounding)
+        assert np.all(np.abs(codes.astype(np.float64) * s - xf) <= s * (0.5 + 1e-5))
+    codes, s = oracle.quantize_row_int8(np.zeros(128, dtype=np.uint16))
+    assert s == 1.0 and not codes.any()
+
 # --------------------------------------------------------------------------
 # Keep-sets versus the pages' own snippets, re-run literally on tiny inputs.
 # --------------------------------------------------------------------------
@@ -309,7 +346,8 @@ def _build_oracle_cache(wl, lens, seed, order=None):
     nb = sum((L + 15) // 16 for L in lens) + 4
     alloc = oracle.OracleAllocator(nb, len(lens), max((L + 15) // 16 for L in lens) + 1, seed=seed,
                                    order=order)
-    kvd = {"fp32": oracle.KV_FP32, "bf16": oracle.KV_BF16, "fp8": oracle.KV_FP8}[wl.kv_dtype]
+    kvd = {"fp32": oracle.KV_FP32, "bf16": oracle.KV_BF16, "fp8": oracle.KV_FP8,
+           "int8": oracle.KV_INT8}[wl.kv_dtype]
     pool = oracle.OraclePool(nb, wl.n_kv_heads, wl.head_dim, kvd)
     ids = [alloc.seq_add() for _ in lens]
     dense = []
@@ -361,19 +399,24 @@ def _sdpa(q, K, V, G, keep_mask, scale):
 
 
 def _dequant_dense(wl, pool, alloc, sid, L):
-    """Dequantised dense [L][Hk][D] through torch's float8 decoder (library)."""
+    """Dequantised dense [L][Hk][D]: codes through torch's float8 decoder
+    (library) or as plain integers, times the per-token scales."""
     t = alloc.table(sid)
     ks, vs = [], []
     for j in range(L):
         b, o = t[j // 16], j % 16
-        kc = torch.from_numpy(pool.k[b, :, o, :].copy()).view(torch.float8_e4m3fn).double()
-        vc = torch.from_numpy(pool.v[b, :, o, :].copy()).view(torch.float8_e4m3fn).double()
+        if wl.kv_dtype == "int8":
+            kc = torch.from_numpy(pool.k[b, :, o, :].astype(np.float64))
+            vc = torch.from_numpy(pool.v[b, :, o, :].astype(np.float64))
+        else:
+            kc = torch.from_numpy(pool.k[b, :, o, :].copy()).view(torch.float8_e4m3fn).double()
+            vc = torch.from_numpy(pool.v[b, :, o, :].copy()).view(torch.float8_e4m3fn).double()
         ks.append(kc * torch.from_numpy(pool.k_scale[b, :, o].astype(np.float64))[:, None])
         vs.append(vc * torch.from_numpy(pool.v_scale[b, :, o].astype(np.float64))[:, None])
     return torch.stack(ks), torch.stack(vs)
 
 
-@pytest.mark.parametrize("kv", ["fp32", "bf16", "fp8"])
+@pytest.mark.parametrize("kv", ["fp32", "bf16", "fp8", "int8"])
 @pytest.mark.parametrize("mask", ["full", "sliding", "sink_window"])
 def test_decode_matches_library_attention(kv, mask):
     lens = (1, 16, 17, 50, 97)
@@ -388,7 +431,7 @@ def test_decode_matches_library_attention(kv, mask):
                                 oracle.KV_FP32 if kv == "fp32" else oracle.KV_BF16, wl.n_heads,
                                 wl.scale, mode, S, W)
     for b, L in enumerate(lens):
-        if kv == "fp8":
+        if kv in ("fp8", "int8"):
             K, V = _dequant_dense(wl, pool, alloc, ids[b], L)
         else:
             K, V = dense[b][0].double(), dense[b][1].double()

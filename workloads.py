@@ -31,7 +31,7 @@ class Workload:
     n_heads: int
     n_kv_heads: int
     head_dim: int
-    kv_dtype: str  # "fp32" | "bf16" | "fp8" (fp8 is quantised from bf16 rows)
+    kv_dtype: str  # "fp32" | "bf16" | "fp8" | "int8" (fp8 and int8 are quantised from bf16 rows)
     seed: int
     lens: tuple  # context length of each sequence (including the current token)
     mask: str = "full"  # "full" | "sliding" | "sink_window"
