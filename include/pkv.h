@@ -6,8 +6,9 @@
  * logical block i (tokens 16i .. 16i+15) to a physical block.  Blocks can be
  * shared between sequences with reference counts and are copied on the first
  * write to a shared block.  Decode attends one query token per sequence over
- * its cached tokens, with grouped-query heads, optional FP8-E4M3 storage with
- * per-token scales, optional sliding-window or sink + window keep-sets, and
+ * its cached tokens, with grouped-query heads, optional FP8-E4M3 or INT8
+ * storage with per-token scales, optional sliding-window or sink + window
+ * keep-sets, and
  * optional H2O accumulated-score output and keep-set selection.
  *
  * Sources (page title, section):
@@ -17,7 +18,7 @@
  *   [PA] "KV Cache 与 PagedAttention：显存复用与长上下文推理": sections
  *        PagedAttention 的设计, 物理布局示意, 三大运行时组件 (block allocator,
  *        block table, reference count + copy-on-write), the Block/copy_on_write
- *        sketch, 量化原理 (FP8 E4M3, per-token scaling), and the monitoring
+ *        sketch, 量化原理 (FP16 -> INT8 / FP8 E4M3, per-token scaling), and the monitoring
  *        note (free/used blocks).
  *   [SO] "系统优化": 滑动窗口注意力 / StreamingLLM 详解 (sinks + window), KV
  *        Cache 淘汰 (H2O), Flash Attention (tiled online softmax).
@@ -35,7 +36,7 @@
  *   - A pool is used from one host thread at a time.
  *   - Layouts (row-major, innermost last):
  *       k_pool, v_pool  [num_blocks][n_kv_heads][16][head_dim]  kv dtype
- *       k_scale,v_scale [num_blocks][n_kv_heads][16]            fp32 (FP8 only)
+ *       k_scale,v_scale [num_blocks][n_kv_heads][16]            fp32 (FP8 / INT8 only)
  *       block_tables    [max_seqs][max_blocks_per_seq]          int32, -1 = none
  *       q, out          [n_seqs][n_heads][head_dim]   fp32 (fp32 KV) else bf16
  *       lse             [n_seqs][n_heads]                        fp32, natural log
@@ -70,7 +71,7 @@ typedef enum {
   PKV_ERR_WORKSPACE = 9      /* workspace too small (see pkv_decode_workspace_size) */
 } pkv_status;
 
-typedef enum { PKV_KV_FP32 = 0, PKV_KV_BF16 = 1, PKV_KV_FP8_E4M3 = 2 } pkv_kv_dtype;
+typedef enum { PKV_KV_FP32 = 0, PKV_KV_BF16 = 1, PKV_KV_FP8_E4M3 = 2, PKV_KV_INT8 = 3 } pkv_kv_dtype;
 
 /* Keep-sets for decode query position i = L - 1 over keys j in [0, L):
  *   FULL         every key.
@@ -82,7 +83,7 @@ typedef enum { PKV_KV_FP32 = 0, PKV_KV_BF16 = 1, PKV_KV_FP8_E4M3 = 2 } pkv_kv_dt
 typedef enum { PKV_MASK_FULL = 0, PKV_MASK_SLIDING = 1, PKV_MASK_SINK_WINDOW = 2 } pkv_mask_mode;
 
 /* [PA] PagedAttention 的设计 / 三大运行时组件.  Shapes supported: block_size
- * 16; head_dim 128 for BF16/FP8 and 64 or 128 for FP32; G in {1, 2, 4, 8}. */
+ * 16; head_dim 128 for BF16/FP8/INT8 and 64 or 128 for FP32; G in {1, 2, 4, 8}. */
 typedef struct {
   int32_t num_blocks;         /* physical blocks in the pool */
   int32_t block_size;         /* must be 16 */
@@ -104,8 +105,8 @@ typedef struct {
 typedef struct {
   void* k_pool;          /* device, [num_blocks][n_kv_heads][16][head_dim] */
   void* v_pool;          /* device, same shape */
-  float* k_scale;        /* device, [num_blocks][n_kv_heads][16] (FP8 only, else NULL) */
-  float* v_scale;        /* device, same (FP8 only, else NULL) */
+  float* k_scale;        /* device, [num_blocks][n_kv_heads][16] (FP8 / INT8 only, else NULL) */
+  float* v_scale;        /* device, same (FP8 / INT8 only, else NULL) */
   int32_t* block_tables; /* device, [max_seqs][max_blocks_per_seq]; the library
                             initialises it to -1 during create and keeps it in
                             step with the host tables */
@@ -186,7 +187,9 @@ pkv_status pkv_reserve_slots(pkv_pool* pool, int32_t n_seqs, const int32_t* seq_
  * k_new, v_new: device [n_seqs][T][n_kv_heads][head_dim], fp32 for an FP32
  * pool, bf16 otherwise.  FP8 pools quantise each (token, kv head) row:
  * s = absmax / 448 in fp32 (1 when absmax is 0), code = E4M3(x / s) with
- * round-to-nearest-even and saturation to +-448 ([PA] 量化原理). */
+ * round-to-nearest-even and saturation to +-448 ([PA] 量化原理).  INT8 pools
+ * alike with s = absmax / 127 and code = x / s rounded to the nearest
+ * integer (ties to even), clamped to +-127. */
 pkv_status pkv_append(pkv_pool* pool, void* stream, int32_t n_seqs, const int32_t* seq_ids,
                       int32_t T, const void* k_new, const void* v_new);
 
@@ -198,7 +201,7 @@ pkv_status pkv_decode_workspace_size(const pkv_pool* pool, int32_t n_seqs, int32
 /* Decode attention ([PA] decode loads KV block by block through the table;
  * [SO] Flash Attention's tiled online softmax).  For each listed sequence b
  * (context length L_b, the current token included) and query head h:
- *   s_j = scale * q[b][h] . K_j   for kept keys j (FP8: K_j = code_j * s_j)
+ *   s_j = scale * q[b][h] . K_j   for kept keys j (FP8 / INT8: K_j = code_j * s_j)
  *   out[b][h] = sum_j softmax(s)_j V_j,   lse[b][h] = ln sum_j exp(s_j)
  * Empty keep-set: out = 0, lse = -inf.
  *   q, out      device [n_seqs][n_heads][head_dim] (fp32 for FP32 pools, else bf16)

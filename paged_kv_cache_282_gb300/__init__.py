@@ -52,7 +52,7 @@ class PagedKVCache:
     """One KV pool: device buffers (torch-allocated), the library handle, and
     methods that forward to the C ABI.
 
-    kv_dtype: "fp32" | "bf16" | "fp8".  host_only=True creates the allocator
+    kv_dtype: "fp32" | "bf16" | "fp8" | "int8".  host_only=True creates the allocator
     without device buffers (allocator calls only)."""
 
     def __init__(self, num_blocks: int, n_heads: int, n_kv_heads: int, head_dim: int, max_seqs: int,
@@ -77,12 +77,12 @@ class PagedKVCache:
         self.device = torch.device(device)
         sizes = _abi.pkv_buffer_sizes()
         _abi.check(self.lib.pkv_pool_required_bytes(ctypes.byref(self.cfg), ctypes.byref(sizes)))
-        dt = {"fp32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.uint8}[kv_dtype]
+        dt = {"fp32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.uint8, "int8": torch.int8}[kv_dtype]
         shape = (num_blocks, n_kv_heads, BLOCK_SIZE, head_dim)
         with torch.cuda.device(self.device):
             self.k_pool = torch.empty(shape, dtype=dt, device=self.device)
             self.v_pool = torch.empty(shape, dtype=dt, device=self.device)
-            if kv_dtype == "fp8":
+            if kv_dtype in ("fp8", "int8"):
                 self.k_scale = torch.empty(shape[:3], dtype=torch.float32, device=self.device)
                 self.v_scale = torch.empty(shape[:3], dtype=torch.float32, device=self.device)
             else:

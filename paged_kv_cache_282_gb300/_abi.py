@@ -17,7 +17,7 @@ STATUS_NAMES = {
     4: "PKV_ERR_OUT_OF_SEQS", 5: "PKV_ERR_CUDA", 6: "PKV_ERR_TIMEOUT", 7: "PKV_ERR_DEVICE_ASSERT",
     8: "PKV_ERR_NO_DEVICE", 9: "PKV_ERR_WORKSPACE",
 }
-KV_DTYPES = {"fp32": 0, "bf16": 1, "fp8": 2, "fp8_e4m3": 2}
+KV_DTYPES = {"fp32": 0, "bf16": 1, "fp8": 2, "fp8_e4m3": 2, "int8": 3}
 MASKS = {"full": 0, "sliding": 1, "sink_window": 2}
 KERNELS = ["cow_copy", "append", "decode", "combine", "h2o_score", "h2o_select", "table_patch"]
 

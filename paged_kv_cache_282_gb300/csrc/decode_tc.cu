@@ -1,5 +1,5 @@
-// decode_tc.cu -- decode attention over the paged KV cache, BF16 and FP8-E4M3
-// KV, head_dim 128, GQA group G in {1, 2, 4, 8}; sm_103a.
+// decode_tc.cu -- decode attention over the paged KV cache, BF16, FP8-E4M3
+// and INT8 KV, head_dim 128, GQA group G in {1, 2, 4, 8}; sm_103a.
 //
 // What it computes (pages: "KV Cache 与 PagedAttention：显存复用与长上下文推理",
 // PagedAttention 的设计 -- decode loads KV block by block through the block
@@ -26,7 +26,7 @@
 //    dimension of m16n8k16 tensor-core MMAs (S = K Q^T, then O^T = V^T P),
 //    with fp32 accumulation.  The path is HBM-bound (4 flop/byte for BF16,
 //    G = 4); the MMAs only keep instruction issue far below the memory time.
-//  - FP8: codes are widened to fp16 in registers (exact); the per-token K
+//  - FP8 / INT8: codes are widened to fp16 in registers (exact); the per-token K
 //    scale multiplies the logit, and the per-token V scale is folded into the
 //    softmax weight through the exponent (b_j = a_j + log2 vs_j), so the fp16
 //    weights never exceed 1 and the running max stays consistent.
@@ -80,6 +80,10 @@ struct TC<2, 2> {
   static constexpr int kScaleBytes = 128;
   static constexpr uint32_t kTxBytes = 4096 + 128;
 };
+
+// INT8 codes: the same geometry as FP8
+template <int NQ>
+struct TC<3, NQ> : TC<2, NQ> {};
 
 template <int KV, int NQ>
 constexpr size_t smem_bytes() {
@@ -205,6 +209,29 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t codes, uint32_t& lo, 
       "cvt.rn.f16x2.e4m3x2 %1, c1;\n\t}"
       : "=r"(lo), "=r"(hi)
       : "r"(codes));
+}
+
+// four INT8 codes (byte 0 first) -> two f16x2 registers, same layout as
+// above.  Exact: with u = c + 128 in [1, 255], the fp16 bit pattern
+// 0x6400 | u is 1024 + u (fp16 spacing is 1 on [1024, 2048)), and
+// subtracting 1152 leaves c.
+__device__ __forceinline__ void i8x4_to_f16x2x2(uint32_t codes, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = codes ^ 0x80808080u;
+  const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140), b = __byte_perm(u, 0x64646464u, 0x4342);
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+  const __half2 x = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+  const __half2 y = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+  lo = *reinterpret_cast<const uint32_t*>(&x);
+  hi = *reinterpret_cast<const uint32_t*>(&y);
+}
+
+// one-byte codes of the pool's type -> fp16 pairs
+template <int KV>
+__device__ __forceinline__ void codes4_to_f16x2x2(uint32_t codes, uint32_t& lo, uint32_t& hi) {
+  if (KV == 3)
+    i8x4_to_f16x2x2(codes, lo, hi);
+  else
+    e4m3x4_to_f16x2x2(codes, lo, hi);
 }
 
 // 2^x and log2(x) with the hardware approximations (relative error ~2^-22;
@@ -509,8 +536,8 @@ __global__ void __launch_bounds__(TC<KV, NQ>::kWarps * 32, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           uint32_t a[4];
-          e4m3x4_to_f16x2x2(tA[kk], a[0], a[2]);
-          e4m3x4_to_f16x2x2(tB[kk], a[1], a[3]);
+          codes4_to_f16x2x2<KV>(tA[kk], a[0], a[2]);
+          codes4_to_f16x2x2<KV>(tB[kk], a[1], a[3]);
 #pragma unroll
           for (int t = 0; t < NQ; ++t) {
             if (t == 1 && !two) break;
@@ -636,11 +663,11 @@ __global__ void __launch_bounds__(TC<KV, NQ>::kWarps * 32, 1)
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
           const uint32_t lo = __byte_perm(A4[w], B4[w], 0x5140), hi = __byte_perm(A4[w], B4[w], 0x7362);
-          e4m3x4_to_f16x2x2(lo, pab[4 * w + 0], pab[4 * w + 1]);
-          e4m3x4_to_f16x2x2(hi, pab[4 * w + 2], pab[4 * w + 3]);
+          codes4_to_f16x2x2<KV>(lo, pab[4 * w + 0], pab[4 * w + 1]);
+          codes4_to_f16x2x2<KV>(hi, pab[4 * w + 2], pab[4 * w + 3]);
           const uint32_t lo2 = __byte_perm(C4[w], D4[w], 0x5140), hi2 = __byte_perm(C4[w], D4[w], 0x7362);
-          e4m3x4_to_f16x2x2(lo2, pcd[4 * w + 0], pcd[4 * w + 1]);
-          e4m3x4_to_f16x2x2(hi2, pcd[4 * w + 2], pcd[4 * w + 3]);
+          codes4_to_f16x2x2<KV>(lo2, pcd[4 * w + 0], pcd[4 * w + 1]);
+          codes4_to_f16x2x2<KV>(hi2, pcd[4 * w + 2], pcd[4 * w + 3]);
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -750,9 +777,10 @@ cudaError_t occupancy_t(int* n) {
 
 // Expands X(KV, G, NQ) for every compiled variant, returning its result when
 // it matches the runtime (kv_dtype, G, nq).
-#define PKV_FOR_VARIANTS(X)                                                        \
-  X(1, 1, 1) X(1, 2, 1) X(1, 4, 1) X(1, 8, 1) X(2, 1, 1) X(2, 2, 1) X(2, 4, 1) X(2, 8, 1) \
-  X(1, 1, 2) X(1, 2, 2) X(1, 4, 2) X(1, 8, 2) X(2, 1, 2) X(2, 2, 2) X(2, 4, 2) X(2, 8, 2)
+#define PKV_FOR_VARIANTS(X)                                                                 \
+  X(1, 1, 1) X(1, 2, 1) X(1, 4, 1) X(1, 8, 1) X(2, 1, 1) X(2, 2, 1) X(2, 4, 1) X(2, 8, 1)          \
+  X(3, 1, 1) X(3, 2, 1) X(3, 4, 1) X(3, 8, 1) X(1, 1, 2) X(1, 2, 2) X(1, 4, 2) X(1, 8, 2)          \
+  X(2, 1, 2) X(2, 2, 2) X(2, 4, 2) X(2, 8, 2) X(3, 1, 2) X(3, 2, 2) X(3, 4, 2) X(3, 8, 2)
 
 }  // namespace
 
@@ -766,12 +794,12 @@ cudaError_t launch_decode_tc(int kv_dtype, int G, int nq, const DecodeTCParams& 
 }
 
 int decode_tc_warps_per_cta(int kv_dtype, int nq) {
-  if (kv_dtype == 2) return nq == 2 ? TC<2, 2>::kWarps : TC<2, 1>::kWarps;
+  if (kv_dtype == 2 || kv_dtype == 3) return nq == 2 ? TC<2, 2>::kWarps : TC<2, 1>::kWarps;
   return nq == 2 ? TC<1, 2>::kWarps : TC<1, 1>::kWarps;
 }
 
 size_t decode_tc_smem_bytes(int kv_dtype, int nq) {
-  if (kv_dtype == 2) return nq == 2 ? smem_bytes<2, 2>() : smem_bytes<2, 1>();
+  if (kv_dtype == 2 || kv_dtype == 3) return nq == 2 ? smem_bytes<2, 2>() : smem_bytes<2, 1>();
   return nq == 2 ? smem_bytes<1, 2>() : smem_bytes<1, 1>();
 }
 

@@ -80,10 +80,15 @@ __global__ void append_copy_kernel(const __grid_constant__ AppendArgs a, int row
   }
 }
 
-// FP8: one warp per (token, kv head, K|V) row of 128 values.
-//   s = absmax / 448 (fp32, IEEE division; 1 when absmax is 0)
-//   code = E4M3(x / s), round to nearest even, saturate to +-448
-__global__ void append_fp8_kernel(const __grid_constant__ AppendArgs a) {
+// FP8 / INT8: one warp per (token, kv head, K|V) row of 128 values.
+//   FP8:  s = absmax / 448, code = E4M3(x / s), round to nearest even,
+//         saturate to +-448
+//   INT8: s = absmax / 127, code = x / s rounded to the nearest integer
+//         (ties to even), clamped to +-127
+// (fp32, IEEE division; s = 1 when absmax is 0)
+template <int KV>
+__global__ void append_quant_kernel(const __grid_constant__ AppendArgs a) {
+  constexpr float kMaxCode = KV == 3 ? 127.0f : 448.0f;
   apply_patches(a);
   const int lane = threadIdx.x & 31;
   const int64_t rows = (int64_t)a.n_tokens * a.Hk;
@@ -101,12 +106,18 @@ __global__ void append_fp8_kernel(const __grid_constant__ AppendArgs a) {
     float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
     for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-    const float s = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
+    const float s = amax == 0.0f ? 1.0f : __fdiv_rn(amax, kMaxCode);
     uint32_t packed = 0;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const __nv_fp8_storage_t code = __nv_cvt_float_to_fp8(__fdiv_rn(x[k], s), __NV_SATFINITE, __NV_E4M3);
-      packed |= (uint32_t)code << (8 * k);
+      uint32_t code;
+      if (KV == 3) {
+        const int n = __float2int_rn(__fdiv_rn(x[k], s));
+        code = (uint32_t)(uint8_t)(int8_t)max(-127, min(127, n));
+      } else {
+        code = __nv_cvt_float_to_fp8(__fdiv_rn(x[k], s), __NV_SATFINITE, __NV_E4M3);
+      }
+      packed |= code << (8 * k);
     }
     const int64_t slot = slot_of(a, t);
     const int64_t blk = slot >> 4, off = slot & 15;
@@ -118,7 +129,7 @@ __global__ void append_fp8_kernel(const __grid_constant__ AppendArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// copy-on-write: copy whole physical blocks (K, V, and FP8 scales)
+// copy-on-write: copy whole physical blocks (K, V, and FP8 / INT8 scales)
 // ---------------------------------------------------------------------------
 
 __global__ void cow_copy_kernel(const int32_t* __restrict__ pairs, uint4* __restrict__ k, uint4* __restrict__ v,
@@ -431,7 +442,7 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
 
 // ---------------------------------------------------------------------------
 // H2O compaction: kept tokens move, in order, into fresh blocks (one warp per
-// (token, kv head) row: K, V and the FP8 scales); the score array follows.
+// (token, kv head) row: K, V and the FP8 / INT8 scales); the score array follows.
 // ---------------------------------------------------------------------------
 
 __global__ void compact_gather_kernel(const CompactSeq* __restrict__ seqs, const int32_t* __restrict__ new_blocks,
@@ -554,9 +565,13 @@ int grid_for(int64_t work, int threads) {
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t st) {
   if (a.n_tokens <= 0 && a.n_patches <= 0) return cudaSuccess;
-  if (a.kv_dtype == 2) {
+  if (a.kv_dtype == 2 || a.kv_dtype == 3) {
     const int64_t warps = 2LL * a.n_tokens * a.Hk;
-    append_fp8_kernel<<<grid_for(std::max<int64_t>(warps * 32, a.n_patches), 256), 256, 0, st>>>(a);
+    const int grid = grid_for(std::max<int64_t>(warps * 32, a.n_patches), 256);
+    if (a.kv_dtype == 3)
+      append_quant_kernel<3><<<grid, 256, 0, st>>>(a);
+    else
+      append_quant_kernel<2><<<grid, 256, 0, st>>>(a);
   } else {
     const int row_chunks = a.D * (a.kv_dtype == 0 ? 4 : 2) / 16;
     const int64_t work = 2LL * a.n_tokens * a.Hk * row_chunks;

@@ -326,6 +326,8 @@ pkv_status launch(pkv_pool* p, int kernel, cudaStream_t st, F&& fn) {
 }
 
 int elem_bytes(int kv_dtype) { return kv_dtype == PKV_KV_FP32 ? 4 : kv_dtype == PKV_KV_BF16 ? 2 : 1; }
+// FP8 and INT8 pools keep one fp32 scale per (token, kv head) for K and V
+bool has_scales(int kv_dtype) { return kv_dtype == PKV_KV_FP8_E4M3 || kv_dtype == PKV_KV_INT8; }
 
 pkv_status check_config(const pkv_pool_config* c) {
   if (!c) return fail(PKV_ERR_INVALID_ARG, "config is NULL");
@@ -340,12 +342,13 @@ pkv_status check_config(const pkv_pool_config* c) {
     return fail(PKV_ERR_INVALID_ARG, "n_heads must be a positive multiple of n_kv_heads");
   int G = c->n_heads / c->n_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return fail(PKV_ERR_UNSUPPORTED, "group size %d not in {1,2,4,8}", G);
-  if (c->kv_dtype != PKV_KV_FP32 && c->kv_dtype != PKV_KV_BF16 && c->kv_dtype != PKV_KV_FP8_E4M3)
+  if (c->kv_dtype != PKV_KV_FP32 && c->kv_dtype != PKV_KV_BF16 && c->kv_dtype != PKV_KV_FP8_E4M3 &&
+      c->kv_dtype != PKV_KV_INT8)
     return fail(PKV_ERR_INVALID_ARG, "unknown kv_dtype %d", c->kv_dtype);
   if (c->kv_dtype == PKV_KV_FP32 && c->head_dim != 64 && c->head_dim != 128)
     return fail(PKV_ERR_UNSUPPORTED, "fp32 pools support head_dim 64 or 128");
   if (c->kv_dtype != PKV_KV_FP32 && c->head_dim != kHeadDimTC)
-    return fail(PKV_ERR_UNSUPPORTED, "bf16 / fp8 pools support head_dim 128");
+    return fail(PKV_ERR_UNSUPPORTED, "bf16 / fp8 / int8 pools support head_dim 128");
   if ((int64_t)c->num_blocks * c->n_kv_heads * kBlock >= (int64_t(1) << 31))
     return fail(PKV_ERR_UNSUPPORTED, "pool too large for 32-bit row coordinates");
   if (c->free_order) {
@@ -373,12 +376,12 @@ pkv_status make_tensor_map(CUtensorMap* m, void* base, const pkv_pool_config& c)
     if (q != cudaDriverEntryPointSuccess || !ptr) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
     fn = (EncodeTiledFn)ptr;
   }
-  const bool fp8 = c.kv_dtype == PKV_KV_FP8_E4M3;
+  const bool fp8 = elem_bytes(c.kv_dtype) == 1;  // FP8 or INT8 codes
   const int es = fp8 ? 1 : 2;
   // 2-D view: rows = (block, kv head, slot), columns = head_dim elements.
   cuuint64_t dims[2] = {(cuuint64_t)c.head_dim, (cuuint64_t)c.num_blocks * c.n_kv_heads * kBlock};
   cuuint64_t strides[1] = {(cuuint64_t)c.head_dim * es};
-  // one box = 16 rows x 128 bytes (64 bf16 or 128 FP8 values), 128-byte swizzle
+  // one box = 16 rows x 128 bytes (64 bf16 or 128 one-byte codes), 128-byte swizzle
   cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)kBlock};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides,
@@ -437,7 +440,7 @@ pkv_status flush_pending(pkv_pool* p, cudaStream_t st, bool with_patches = true)
   const auto& c = p->cfg;
   if (ncow) {
     const size_t blk_bytes = (size_t)c.n_kv_heads * kBlock * c.head_dim * elem_bytes(c.kv_dtype);
-    const size_t scl = c.kv_dtype == PKV_KV_FP8_E4M3 ? (size_t)c.n_kv_heads * kBlock : 0;
+    const size_t scl = has_scales(c.kv_dtype) ? (size_t)c.n_kv_heads * kBlock : 0;
     for (size_t w = 0; w + 1 < wave_start.size(); ++w) {
       const size_t k0 = wave_start[w], k1 = wave_start[w + 1];
       if (k1 == k0) continue;
@@ -979,7 +982,8 @@ int pkv::decode_attn_into(pkv_pool* p, void* stream, int32_t n, const int32_t* i
                           size_t partials_cap) {
   if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
   if (!p->device) return fail(PKV_ERR_NO_DEVICE, "host-only pool");
-  if (p->cfg.kv_dtype == PKV_KV_FP32) return fail(PKV_ERR_UNSUPPORTED, "static-scratch decode serves bf16 / fp8 pools");
+  if (p->cfg.kv_dtype == PKV_KV_FP32)
+    return fail(PKV_ERR_UNSUPPORTED, "static-scratch decode serves bf16 / fp8 / int8 pools");
   {
     int cur = -1;
     if (cudaGetDevice(&cur) != cudaSuccess || cur != p->device_id)
@@ -1043,7 +1047,7 @@ int pkv::decode_attn_into(pkv_pool* p, void* stream, int32_t n, const int32_t* i
 
   if (ncow) {
     const size_t blk_bytes = (size_t)c.n_kv_heads * kBlock * c.head_dim * elem_bytes(c.kv_dtype);
-    const size_t scl = c.kv_dtype == PKV_KV_FP8_E4M3 ? (size_t)c.n_kv_heads * kBlock : 0;
+    const size_t scl = has_scales(c.kv_dtype) ? (size_t)c.n_kv_heads * kBlock : 0;
     for (size_t w = 0; w + 1 < waves.size(); ++w) {
       const size_t k0 = waves[w], k1 = waves[w + 1];
       if (k1 == k0) continue;
@@ -1080,7 +1084,7 @@ pkv_status pkv_pool_required_bytes(const pkv_pool_config* cfg, pkv_buffer_sizes*
   if (!out) return fail(PKV_ERR_INVALID_ARG, "out is NULL");
   const size_t rows = (size_t)cfg->num_blocks * cfg->n_kv_heads * kBlock;
   out->k_pool = out->v_pool = rows * cfg->head_dim * elem_bytes(cfg->kv_dtype);
-  out->k_scale = out->v_scale = cfg->kv_dtype == PKV_KV_FP8_E4M3 ? rows * sizeof(float) : 0;
+  out->k_scale = out->v_scale = has_scales(cfg->kv_dtype) ? rows * sizeof(float) : 0;
   out->block_tables = (size_t)cfg->max_seqs * cfg->max_blocks_per_seq * sizeof(int32_t);
   out->status = 4 * sizeof(int32_t);
   return PKV_OK;
@@ -1097,7 +1101,7 @@ pkv_status pkv_pool_create(const pkv_pool_config* cfg, const pkv_pool_buffers* b
   p->alloc.init(cfg->num_blocks, cfg->max_seqs, cfg->max_blocks_per_seq, cfg->alloc_seed, cfg->free_order);
   if (buffers) {
     const auto& b = *buffers;
-    const bool fp8 = cfg->kv_dtype == PKV_KV_FP8_E4M3;
+    const bool fp8 = has_scales(cfg->kv_dtype);
     if (!b.k_pool || !b.v_pool || !b.block_tables || !b.status || (fp8 && (!b.k_scale || !b.v_scale))) {
       delete p;
       return fail(PKV_ERR_INVALID_ARG, "a required device buffer is NULL");
@@ -1465,7 +1469,7 @@ pkv_status pkv_seq_compact(pkv_pool* p, void* stream, int32_t n, const int32_t* 
     if (pkv_status r = Staging::upload(s, off + fresh.size() * sizeof(int32_t), st)) return r;
     const auto& c = p->cfg;
     const int row_bytes = c.head_dim * elem_bytes(c.kv_dtype);
-    const bool fp8 = c.kv_dtype == PKV_KV_FP8_E4M3;
+    const bool fp8 = has_scales(c.kv_dtype);
     if (pkv_status r = launch(p, PKV_KERNEL_COW_COPY, st, [&] {
           return launch_compact_gather((const CompactSeq*)s->dev, n, max_count, (const int32_t*)(s->dev + off),
                                        p->buf.block_tables, c.max_blocks_per_seq, c.num_blocks, keep_idx, keep_stride,

@@ -11,9 +11,9 @@ import oracle
 import workloads
 from paged_kv_cache_282_gb300 import PagedKVCache
 
-KV_CODE = {"fp32": oracle.KV_FP32, "bf16": oracle.KV_BF16, "fp8": oracle.KV_FP8}
+KV_CODE = {"fp32": oracle.KV_FP32, "bf16": oracle.KV_BF16, "fp8": oracle.KV_FP8, "int8": oracle.KV_INT8}
 MASK_CODE = {"full": oracle.MASK_FULL, "sliding": oracle.MASK_SLIDING, "sink_window": oracle.MASK_SINK_WINDOW}
-TOL = {"fp32": 1e-4, "bf16": 1e-2, "fp8": 2e-2}  # max abs error on N(0,1) inputs
+TOL = {"fp32": 1e-4, "bf16": 1e-2, "fp8": 2e-2, "int8": 2e-2}  # max abs error on N(0,1) inputs
 
 
 class Twin:
@@ -128,7 +128,7 @@ def pool_bytes_equal(tw: Twin, ids, every: int = 1):
     c = tw.cache
     NB, Hk = tw.pool.NB, tw.wl.n_kv_heads
     pairs = [(c.k_pool, tw.pool.k), (c.v_pool, tw.pool.v)]
-    if tw.wl.kv_dtype == "fp8":
+    if tw.wl.kv_dtype in ("fp8", "int8"):
         pairs += [(c.k_scale, tw.pool.k_scale), (c.v_scale, tw.pool.v_scale)]
     for dt, ht in pairs:
         d = dt.view(torch.uint8).reshape(NB, Hk, 16, -1) if dt.dtype != torch.uint8 else dt.reshape(NB, Hk, 16, -1)

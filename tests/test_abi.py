@@ -48,6 +48,15 @@ def test_required_bytes(pkv):
     assert sz.block_tables == 4 * 64 * 4 and sz.status == 16
 
 
+def test_required_bytes_int8(pkv):
+    import ctypes
+    from paged_kv_cache_282_gb300 import _abi
+    cfg = _abi.pkv_pool_config(100, 16, 32, 8, 128, 4, 64, 3, 0, None)
+    sz = _abi.pkv_buffer_sizes()
+    _abi.check(pkv.load().pkv_pool_required_bytes(ctypes.byref(cfg), ctypes.byref(sz)))
+    assert sz.k_pool == 100 * 8 * 16 * 128 and sz.k_scale == 100 * 8 * 16 * 4
+
+
 @pytest.mark.parametrize("bad", [dict(block_size=8), dict(n_heads=24, n_kv_heads=8),
                                  dict(head_dim=96), dict(kv_dtype=7)])
 def test_config_rejected(pkv, bad):

@@ -74,7 +74,7 @@ def _decode_both(tw, wl, ids, cascade: bool, static: bool = False, logits: bool 
     return out
 
 
-@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8", "int8"])
 @pytest.mark.parametrize("n_heads", [64, 32, 16, 8])
 def test_cascade_matches_oracle(kv, n_heads):
     wl, tw, ids = _shared_batch(kv, n_heads, seed=90 + n_heads)

@@ -21,7 +21,7 @@ def _pool_bytes_equal(tw: Twin, ids):
     NB, Hk = tw.pool.NB, tw.wl.n_kv_heads
     dev = [c.k_pool, c.v_pool]
     host = [tw.pool.k, tw.pool.v]
-    if tw.wl.kv_dtype == "fp8":
+    if tw.wl.kv_dtype in ("fp8", "int8"):
         dev += [c.k_scale, c.v_scale]
         host += [tw.pool.k_scale, tw.pool.v_scale]
     for dt, ht in zip(dev, host):
@@ -68,7 +68,7 @@ def test_tiny_fp32(placement):
 LENS = (1, 15, 16, 17, 33, 200, 517, 1000, 2049)
 
 
-@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8", "int8"])
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
 def test_small_full_mask(kv, G):
     wl = workloads.small(kv, lens=LENS, n_heads=8 * G, n_kv_heads=8, seed=30 + G)
@@ -90,7 +90,7 @@ def test_small_full_mask(kv, G):
         assert (o - outs[0]).abs().max() <= 8e-3
 
 
-@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8", "int8"])
 @pytest.mark.parametrize("mask,S,W", [("sliding", 0, 0), ("sliding", 0, 37), ("sliding", 0, 600),
                                       ("sink_window", 4, 100), ("sink_window", 0, 64), ("sink_window", 20, 3),
                                       ("sink_window", 0, 0)])
@@ -109,7 +109,7 @@ def test_small_masks(kv, mask, S, W):
         assert lse_err(lse, ref_lse) <= 2e-3
 
 
-@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8", "int8"])
 def test_physical_placement_invariance(kv):
     """The output depends only on logical order: two different physical
     placements give bit-identical results."""
@@ -163,7 +163,7 @@ def test_empty_and_zero_length():
 # copy-on-write and append bit-exactness
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8", "int8"])
 def test_fork_append_cow(kv):
     wl = workloads.small(kv, lens=(40, 64, 77), seed=70)
     tw = Twin(wl, 64, 8, 16, seed=17)
@@ -316,7 +316,7 @@ def test_bounded_wait_reports_timeout_and_context_survives():
 # H2O compaction: the keep-set becomes the whole sequence
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8", "int8"])
 def test_h2o_compaction(kv):
     """Keep-sets from the oracle's selection on seeded scores; one sequence
     shares its blocks with a fork, one keeps nothing, one keeps everything.
@@ -373,7 +373,7 @@ def test_h2o_compaction_refuses_out_of_range_positions():
     assert getattr(e.value, "status", None) == 7
 
 
-@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8", "int8"])
 def test_policy_scores_select_compact_chain(kv):
     """Decode with logits, accumulate the heavy-hitter scores, keep 4 sinks +
     256 recent + 252 heavy hitters, compact, decode again.  Each side runs
