@@ -11,7 +11,8 @@ step the appended token is rolled back on the host (the block table is
 truncated), so every timed step sees the same context lengths.
 
 Metric: algorithmic KV bytes read per second (each kept token's K and V bytes
-per (sequence, kv head) once, plus FP8 scales) and decode tokens per second
+per (sequence, kv head) once, plus FP8 / INT8 scales; a physical block shared
+by several sequences counts once) and decode tokens per second
 (sequences / step time).  Inputs stay resident in HBM; the KV pool of the
 default workload (~1.1 GB) is far larger than L2, so no flush is needed.
 
@@ -43,7 +44,7 @@ import workloads  # noqa: E402
 
 METRIC = "paged decode KV GB/s (frac of HBM peak) and tokens/s, 1×GB300"
 FALLBACK_HBM_GBS = 6800.0
-BYTES = {"fp32": 4, "bf16": 2, "fp8": 1}
+BYTES = {"fp32": 4, "bf16": 2, "fp8": 1, "int8": 1}
 
 
 # --------------------------------------------------------------------------
@@ -52,7 +53,7 @@ BYTES = {"fp32": 4, "bf16": 2, "fp8": 1}
 
 def _kv_bytes_per_token(wl) -> int:
     b = 2 * wl.n_kv_heads * wl.head_dim * BYTES[wl.kv_dtype]
-    if wl.kv_dtype == "fp8":
+    if wl.kv_dtype in ("fp8", "int8"):
         b += 2 * wl.n_kv_heads * 4  # per-token K and V scales
     return b
 
@@ -157,6 +158,13 @@ class Setup:
     def algorithmic_bytes(self, lens=None) -> int:
         lens = self.lens if lens is None else lens
         return sum(_kept(L, self.wl) for L in lens) * _kv_bytes_per_token(self.wl)
+
+    def kv_bytes_read_per_step(self) -> int:
+        """KV bytes one step must read: each sequence's kept tokens, except
+        that a physical block shared by several sequences counts once."""
+        if self.wl.name != "prefix_append":
+            return self.algorithmic_bytes([L + 1 for L in self.lens])
+        return self.unique_bytes_per_step()
 
     def unique_bytes_per_step(self) -> int:
         """KV bytes of distinct physical blocks the step reads (blocks shared
@@ -325,7 +333,7 @@ def oracle_baseline(wl, n_sample: int, repeats: int = 1):
     import oracle
     lens = list(wl.lens)[:n_sample]
     nb = sum((L + 15) // 16 for L in lens)
-    kvd = {"fp32": oracle.KV_FP32, "bf16": oracle.KV_BF16, "fp8": oracle.KV_FP8}[wl.kv_dtype]
+    kvd = {"fp32": oracle.KV_FP32, "bf16": oracle.KV_BF16, "fp8": oracle.KV_FP8, "int8": oracle.KV_INT8}[wl.kv_dtype]
     alloc = oracle.OracleAllocator(nb, len(lens), max((L + 15) // 16 for L in lens) + 1, seed=wl.seed)
     pool = oracle.OraclePool(nb, wl.n_kv_heads, wl.head_dim, kvd)
     ids = []
@@ -369,6 +377,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=0, help="run N untimed steps and exit (for ncu)")
+    ap.add_argument("--kv-dtype", default=None, choices=["bf16", "fp8", "int8"],
+                    help="run the workload with another KV storage type")
     ap.add_argument("--no-cascade", action="store_true",
                     help="every sequence reads its own blocks (no shared-prefix pairing)")
     ap.add_argument("--time-kernels", action="store_true",
@@ -376,6 +386,11 @@ def main():
     args = ap.parse_args()
 
     wl = workloads.ALL[args.workload]()
+    label = wl.name
+    if args.kv_dtype and args.kv_dtype != wl.kv_dtype:
+        import dataclasses
+        wl = dataclasses.replace(wl, kv_dtype=args.kv_dtype)
+        label = f"{wl.name}_{args.kv_dtype}"
     splits = wl.num_splits if args.num_splits is None else args.num_splits
     ws, rank, local = dist_info()
 
@@ -465,7 +480,7 @@ def main():
         bi = (q_h.numel() * q_h.element_size() + k_h.numel() * k_h.element_size() +
               v_h.numel() * v_h.element_size())
         bo = out_h.numel() * out_h.element_size()
-        step_bytes = setup.algorithmic_bytes([L + 1 for L in setup.lens])
+        step_bytes = setup.kv_bytes_read_per_step()
         e2e = {"value": round(ws * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": round(e2e_ms, 5),
                "tokens_per_s": round(ws * n / (e2e_ms * 1e-3), 1)}
@@ -476,16 +491,16 @@ def main():
         return
 
     lens_step = [L + 1 for L in setup.lens]
-    step_bytes = setup.algorithmic_bytes(lens_step)
+    logical = setup.algorithmic_bytes(lens_step)
+    step_bytes = setup.kv_bytes_read_per_step()
     ms_step = ms_max / args.steps
     value = whole_job_rate(ws, step_bytes, ms_step)
     peak, peak_kind = hbm_peak()
     dec_ms, dec_n = ktimes["decode"]
     dec_avg = dec_ms / max(dec_n, 1)
     achieved = step_bytes / (dec_avg * 1e-3) / 1e9 if dec_n else None
-    traffic = profiled_traffic("decode_tc.cu", wl.name)
+    traffic = profiled_traffic("decode_tc.cu", label)
     decode_share = round(dec_ms / max(ms, 1e-9), 4)
-    unique = setup.unique_bytes_per_step() if wl.name == "prefix_append" else None
     cpu = None
     if not args.no_cpu_baseline and ws == 1:
         cpu = oracle_baseline(wl, min(args.cpu_sample, wl.batch))
@@ -503,7 +518,7 @@ def main():
         "vs_baseline": None,
         "dtype": wl.kv_dtype,
         "data": "synthetic (seeded N(0,1) K/V/Q; seeded uniform lengths)",
-        "config": {"workload": wl.name, "batch": len(setup.ids), "n_heads": wl.n_heads,
+        "config": {"workload": label, "batch": len(setup.ids), "n_heads": wl.n_heads,
                    "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim, "kv_dtype": wl.kv_dtype,
                    "mask": wl.mask, "num_splits": splits, "cascade": not args.no_cascade,
                    "context_tokens": sum(lens_step),
@@ -514,13 +529,12 @@ def main():
         "roofline": {"bound": "hbm", "kernel": "decode_tc_kernel", "achieved": round(achieved, 2) if achieved else None,
                      "peak": peak, "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s",
                      "frac": round(achieved / peak, 4) if achieved else None, "traffic": traffic,
-                     "achieved_unique": round(unique / (dec_avg * 1e-3) / 1e9, 2) if unique and dec_n else None,
                      "algorithmic_bytes_per_launch": step_bytes, "avg_launch_ms": round(dec_avg, 5)},
         "decode_share_of_step": decode_share,
         "kernel_ms_per_step": {k: round(v[0] / args.steps, 5) for k, v in ktimes.items() if v[1]}
         if args.time_kernels else None,
-        "unique_kv_bytes_per_step": unique,
-        "value_unique_gbs": round(ws * unique / (ms_step * 1e-3) / 1e9, 2) if unique else None,
+        "logical_kv_bytes_per_step": logical if logical != step_bytes else None,
+        "value_logical_gbs": round(ws * logical / (ms_step * 1e-3) / 1e9, 2) if logical != step_bytes else None,
         "gpu_launches": launches,
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -547,7 +561,7 @@ def run_reference(args, wl):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "batch": wl.batch, "sample_sequences": n},
+        "config": {"workload": label, "batch": wl.batch, "sample_sequences": n},
         "tokens_per_s": round(n / t, 3),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": res[0]["sample"]},
