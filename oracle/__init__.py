@@ -98,6 +98,21 @@ def _load():
         lib.oracle_alloc_compact.argtypes = [vp, c_int, vp, vp, vp]
         lib.oracle_alloc_compact.restype = c_int
         lib.oracle_copy_rows.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, vp, vp, c_int]
+        lib.oracle_alloc_set_swap_space.argtypes = [vp, c_int]
+        lib.oracle_alloc_set_swap_space.restype = c_int
+        lib.oracle_alloc_swap_out.argtypes = [vp, c_int, vp, vp]
+        lib.oracle_alloc_swap_out.restype = c_int
+        lib.oracle_alloc_swap_in.argtypes = [vp, c_int, vp, vp]
+        lib.oracle_alloc_swap_in.restype = c_int
+        lib.oracle_alloc_swapped.argtypes = [vp, c_int]
+        lib.oracle_alloc_swapped.restype = c_int
+        lib.oracle_alloc_host_refcount.argtypes = [vp, c_int]
+        lib.oracle_alloc_host_refcount.restype = c_int
+        lib.oracle_alloc_num_host_free.argtypes = [vp]
+        lib.oracle_alloc_num_host_free.restype = c_int
+        lib.oracle_alloc_host_table.argtypes = [vp, c_int, vp]
+        lib.oracle_alloc_host_table.restype = c_int
+        lib.oracle_copy_blocks_between.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, vp, c_int]
         lib.oracle_alloc_evict.argtypes = [vp, c_int, c_int, c_int]
         lib.oracle_alloc_evict.restype = c_int
         lib.oracle_alloc_len.argtypes = [vp, c_int]
@@ -242,6 +257,28 @@ class OraclePool:
         _load().oracle_copy_rows(_ptr(self.k), _ptr(self.v), _ptr(self.k_scale), _ptr(self.v_scale), self.Hk,
                                  self.D, es, _ptr(src), _ptr(dst), src.size)
 
+    def add_host_pool(self, num_host_blocks: int) -> None:
+        """Host-side swap space with the device pool's layout."""
+        self.NH = num_host_blocks
+        self.hk = np.zeros((num_host_blocks,) + self.k.shape[1:], dtype=self.k.dtype)
+        self.hv = np.zeros_like(self.hk)
+        if self.k_scale is not None:
+            self.hk_scale = np.zeros((num_host_blocks,) + self.k_scale.shape[1:], dtype=np.float32)
+            self.hv_scale = np.zeros_like(self.hk_scale)
+        else:
+            self.hk_scale = self.hv_scale = None
+
+    def swap_copy(self, pairs: np.ndarray, out: bool) -> None:
+        """Block copies device -> host (out) or host -> device."""
+        pairs = _c(pairs, np.int32)
+        es = {KV_FP32: 4, KV_BF16: 2, KV_FP8: 1, KV_INT8: 1}[self.kv_dtype]
+        src = (self.k, self.v, self.k_scale, self.v_scale)
+        dst = (self.hk, self.hv, self.hk_scale, self.hv_scale)
+        if not out:
+            src, dst = dst, src
+        _load().oracle_copy_blocks_between(*(_ptr(x) for x in src), *(_ptr(x) for x in dst), self.Hk, self.D, es,
+                                           _ptr(pairs), pairs.size // 2)
+
     def copy_block(self, src: int, dst: int) -> None:
         es = {KV_FP32: 4, KV_BF16: 2, KV_FP8: 1, KV_INT8: 1}[self.kv_dtype]
         _load().oracle_copy_block(_ptr(self.k), _ptr(self.v), _ptr(self.k_scale),
@@ -378,6 +415,43 @@ class OracleAllocator:
     def evict(self, s: int, num_sinks: int, window: int) -> None:
         if self._lib.oracle_alloc_evict(self._h, s, num_sinks, window):
             raise ValueError("evict failed")
+
+    def set_swap_space(self, num_host_blocks: int) -> None:
+        if self._lib.oracle_alloc_set_swap_space(self._h, num_host_blocks):
+            raise ValueError("swap space in use")
+        self.NH = num_host_blocks
+
+    def _swap(self, fn, seq_ids) -> np.ndarray:
+        ids = _c(seq_ids, np.int32)
+        out = np.empty((max(self.NB, getattr(self, "NH", 0), 1), 2), dtype=np.int32)
+        r = fn(self._h, ids.size, _ptr(ids), _ptr(out))
+        if r == -1:
+            raise MemoryError("out of blocks")
+        if r < 0:
+            raise ValueError("invalid swap")
+        return out[:r].copy()
+
+    def swap_out(self, seq_ids) -> np.ndarray:
+        """CPU swap-out; returns the (device block, host block) copies."""
+        return self._swap(self._lib.oracle_alloc_swap_out, seq_ids)
+
+    def swap_in(self, seq_ids) -> np.ndarray:
+        """CPU swap-in; returns the (host block, device block) copies."""
+        return self._swap(self._lib.oracle_alloc_swap_in, seq_ids)
+
+    def swapped(self, s: int) -> bool:
+        return bool(self._lib.oracle_alloc_swapped(self._h, s))
+
+    def host_refcount(self, b: int) -> int:
+        return self._lib.oracle_alloc_host_refcount(self._h, b)
+
+    def num_host_free(self) -> int:
+        return self._lib.oracle_alloc_num_host_free(self._h)
+
+    def host_table(self, s: int) -> np.ndarray:
+        out = np.empty(max(self.max_blocks, 1), dtype=np.int32)
+        n = self._lib.oracle_alloc_host_table(self._h, s, _ptr(out))
+        return out[:n].copy()
 
     def compact(self, seq_ids, counts) -> list:
         """H2O compaction of the allocator state; returns each sequence's

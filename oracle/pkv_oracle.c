@@ -590,6 +590,15 @@ typedef struct {
   int32_t* tables;
   int32_t* lens;
   unsigned char* active;
+  /* CPU swap space: NH host blocks with their own counts and free pool; a
+   * swapped-out sequence keeps its length, its device table row is empty
+   * and its blocks are named by host_tables. */
+  int NH;
+  int32_t* host_refcount;
+  int32_t* host_free_stack;
+  int host_free_top;
+  int32_t* host_tables;
+  unsigned char* swapped;
 } oracle_alloc;
 
 static uint64_t splitmix64_next(uint64_t* state) {
@@ -621,6 +630,13 @@ oracle_alloc* oracle_alloc_create(int NB, int max_seqs, int max_blocks, uint64_t
   a->lens = (int32_t*)calloc((size_t)max_seqs, sizeof(int32_t));
   a->active = (unsigned char*)calloc((size_t)max_seqs, 1);
   for (i = 0; i < max_seqs * max_blocks; i++) a->tables[i] = -1;
+  a->NH = 0;
+  a->host_refcount = (int32_t*)calloc(1, sizeof(int32_t));
+  a->host_free_stack = (int32_t*)calloc(1, sizeof(int32_t));
+  a->host_free_top = 0;
+  a->host_tables = (int32_t*)malloc(sizeof(int32_t) * (size_t)max_seqs * max_blocks);
+  for (i = 0; i < max_seqs * max_blocks; i++) a->host_tables[i] = -1;
+  a->swapped = (unsigned char*)calloc((size_t)max_seqs, 1);
   if (order) {
     for (i = 0; i < NB; i++) perm[i] = order[i];
   } else {
@@ -649,6 +665,10 @@ void oracle_alloc_destroy(oracle_alloc* a) {
   free(a->tables);
   free(a->lens);
   free(a->active);
+  free(a->host_refcount);
+  free(a->host_free_stack);
+  free(a->host_tables);
+  free(a->swapped);
   free(a);
 }
 
@@ -666,7 +686,24 @@ static oracle_alloc* alloc_clone(const oracle_alloc* a) {
   memcpy(c->tables, a->tables, sizeof(int32_t) * nt);
   memcpy(c->lens, a->lens, sizeof(int32_t) * (size_t)a->max_seqs);
   memcpy(c->active, a->active, (size_t)a->max_seqs);
+  {
+    size_t nh = (size_t)(a->NH > 0 ? a->NH : 1);
+    c->host_refcount = (int32_t*)malloc(sizeof(int32_t) * nh);
+    c->host_free_stack = (int32_t*)malloc(sizeof(int32_t) * nh);
+    c->host_tables = (int32_t*)malloc(sizeof(int32_t) * nt);
+    c->swapped = (unsigned char*)malloc((size_t)a->max_seqs);
+    memcpy(c->host_refcount, a->host_refcount, sizeof(int32_t) * nh);
+    memcpy(c->host_free_stack, a->host_free_stack, sizeof(int32_t) * nh);
+    memcpy(c->host_tables, a->host_tables, sizeof(int32_t) * nt);
+    memcpy(c->swapped, a->swapped, (size_t)a->max_seqs);
+  }
   return c;
+}
+
+/* A live sequence whose blocks are on the device (device-side operations
+ * refuse a swapped-out sequence). */
+static int dev_seq(const oracle_alloc* a, int s) {
+  return s >= 0 && s < a->max_seqs && a->active[s] && !a->swapped[s];
 }
 
 static void alloc_swap(oracle_alloc* a, oracle_alloc* c) {
@@ -709,7 +746,7 @@ int oracle_alloc_append(oracle_alloc* a, int n, const int32_t* seq_ids, int T, i
   int i, t, ncow = 0;
   for (i = 0; i < n; i++) {
     int k;
-    if (seq_ids[i] < 0 || seq_ids[i] >= a->max_seqs || !a->active[seq_ids[i]]) return -2;
+    if (!dev_seq(a, seq_ids[i])) return -2;
     for (k = 0; k < i; k++)
       if (seq_ids[k] == seq_ids[i]) return -2;
     if ((a->lens[seq_ids[i]] + T + ORACLE_BLOCK - 1) / ORACLE_BLOCK > a->max_blocks) return -2;
@@ -759,7 +796,7 @@ int oracle_alloc_append(oracle_alloc* a, int n, const int32_t* seq_ids, int T, i
 
 int oracle_alloc_fork(oracle_alloc* a, int src) {
   int dst, lb, nblk;
-  if (src < 0 || src >= a->max_seqs || !a->active[src]) return -2;
+  if (!dev_seq(a, src)) return -2;
   dst = oracle_alloc_seq_add(a);
   if (dst < 0) return -1;
   nblk = (a->lens[src] + ORACLE_BLOCK - 1) / ORACLE_BLOCK;
@@ -774,8 +811,7 @@ int oracle_alloc_fork(oracle_alloc* a, int src) {
 
 int oracle_alloc_truncate(oracle_alloc* a, int s, int new_len) {
   int lb, keep_blk, nblk;
-  if (s < 0 || s >= a->max_seqs || !a->active[s] || new_len < 0 || new_len > a->lens[s])
-    return -2;
+  if (!dev_seq(a, s) || new_len < 0 || new_len > a->lens[s]) return -2;
   keep_blk = (new_len + ORACLE_BLOCK - 1) / ORACLE_BLOCK;
   nblk = (a->lens[s] + ORACLE_BLOCK - 1) / ORACLE_BLOCK;
   /* a partial last block must still be present, or later appends would have
@@ -791,16 +827,181 @@ int oracle_alloc_truncate(oracle_alloc* a, int s, int new_len) {
   return 0;
 }
 
+static int take_host_block(oracle_alloc* a) {
+  int b;
+  if (a->host_free_top == 0) return -1;
+  b = a->host_free_stack[--a->host_free_top];
+  a->host_refcount[b] = 1;
+  return b;
+}
+
+static void drop_host_block(oracle_alloc* a, int b) {
+  a->host_refcount[b] -= 1;
+  if (a->host_refcount[b] == 0) a->host_free_stack[a->host_free_top++] = b;
+}
+
 int oracle_alloc_free(oracle_alloc* a, int s) {
-  int r = oracle_alloc_truncate(a, s, 0);
+  int r;
+  if (s >= 0 && s < a->max_seqs && a->active[s] && a->swapped[s]) {
+    /* a swapped-out sequence gives back its host blocks, ascending */
+    int lb, nblk = (a->lens[s] + ORACLE_BLOCK - 1) / ORACLE_BLOCK;
+    for (lb = 0; lb < nblk; lb++) {
+      int32_t* e = a->host_tables + (size_t)s * a->max_blocks + lb;
+      if (*e >= 0) drop_host_block(a, *e);
+      *e = -1;
+    }
+    a->swapped[s] = 0;
+    a->lens[s] = 0;
+    a->active[s] = 0;
+    return 0;
+  }
+  r = oracle_alloc_truncate(a, s, 0);
   if (r) return r;
   a->active[s] = 0;
   return 0;
 }
 
+/* CPU swap ([PA] the block allocator manages the pool in blocks and can swap
+ * them out to CPU RAM; [LC] CPU offloading keeps inactive requests' KV in host
+ * memory and loads it back when needed).  Readings adopted:
+ *  - the host pool holds NH blocks; it starts in ascending order, allocation
+ *    takes its front and a released host block goes back to the front;
+ *  - swap-out of a list of sequences: every listed sequence's blocks, in list
+ *    order and ascending logical order, get host blocks -- a device block that
+ *    several listed sequences share is copied once and its host block is
+ *    shared as many times; then every device block is released (same
+ *    order) and the device table rows become empty;
+ *  - swap-in is the mirror image: device blocks from the front of the device
+ *    pool (a host block shared by several listed sequences becomes one device
+ *    block shared as many times), then the host blocks are released;
+ *  - either call changes nothing when the destination pool lacks blocks
+ *    (returns -1), and refuses (-2) a sequence that is not live, already in
+ *    the requested place, or listed twice;
+ *  - a swapped-out sequence keeps its length; every device-side operation
+ *    refuses it; freeing it releases its host blocks. */
+int oracle_alloc_set_swap_space(oracle_alloc* a, int NH) {
+  int i;
+  for (i = 0; i < a->max_seqs; i++)
+    if (a->swapped[i]) return -2;
+  free(a->host_refcount);
+  free(a->host_free_stack);
+  a->NH = NH;
+  a->host_refcount = (int32_t*)calloc((size_t)(NH > 0 ? NH : 1), sizeof(int32_t));
+  a->host_free_stack = (int32_t*)malloc(sizeof(int32_t) * (size_t)(NH > 0 ? NH : 1));
+  a->host_free_top = 0;
+  for (i = NH - 1; i >= 0; i--) a->host_free_stack[a->host_free_top++] = i;
+  return 0;
+}
+
+/* pairs_out receives (device block, host block) copies (swap-out) or (host
+ * block, device block) copies (swap-in); returns the number of pairs. */
+static int swap_move(oracle_alloc* a, int n, const int32_t* seq_ids, int out, int32_t* pairs_out) {
+  int i, k, lb, npairs = 0, need = 0;
+  int32_t* map;
+  int src_n = out ? a->NB : a->NH;
+  for (i = 0; i < n; i++) {
+    int s = seq_ids[i];
+    if (s < 0 || s >= a->max_seqs || !a->active[s] || a->swapped[s] != (out ? 0 : 1)) return -2;
+    for (k = 0; k < i; k++)
+      if (seq_ids[k] == s) return -2;
+  }
+  map = (int32_t*)malloc(sizeof(int32_t) * (size_t)(src_n > 0 ? src_n : 1));
+  for (i = 0; i < src_n; i++) map[i] = -1;
+  for (i = 0; i < n; i++) {
+    int s = seq_ids[i], nblk = (a->lens[s] + ORACLE_BLOCK - 1) / ORACLE_BLOCK;
+    const int32_t* row = (out ? a->tables : a->host_tables) + (size_t)s * a->max_blocks;
+    for (lb = 0; lb < nblk; lb++)
+      if (row[lb] >= 0 && map[row[lb]] < 0) {
+        map[row[lb]] = 0;
+        need++;
+      }
+  }
+  if (need > (out ? a->host_free_top : a->free_top)) {
+    free(map);
+    return -1;
+  }
+  for (i = 0; i < src_n; i++) map[i] = -1;
+  for (i = 0; i < n; i++) {
+    int s = seq_ids[i], nblk = (a->lens[s] + ORACLE_BLOCK - 1) / ORACLE_BLOCK;
+    int32_t* from = (out ? a->tables : a->host_tables) + (size_t)s * a->max_blocks;
+    int32_t* to = (out ? a->host_tables : a->tables) + (size_t)s * a->max_blocks;
+    for (lb = 0; lb < nblk; lb++) {
+      int b = from[lb];
+      if (b < 0) {
+        to[lb] = -1;
+        continue;
+      }
+      if (map[b] < 0) {
+        map[b] = out ? take_host_block(a) : take_block(a);
+        pairs_out[2 * npairs] = b;
+        pairs_out[2 * npairs + 1] = map[b];
+        npairs++;
+      } else if (out) {
+        a->host_refcount[map[b]] += 1;
+      } else {
+        a->refcount[map[b]] += 1;
+      }
+      to[lb] = map[b];
+    }
+  }
+  for (i = 0; i < n; i++) {
+    int s = seq_ids[i], nblk = (a->lens[s] + ORACLE_BLOCK - 1) / ORACLE_BLOCK;
+    int32_t* from = (out ? a->tables : a->host_tables) + (size_t)s * a->max_blocks;
+    for (lb = 0; lb < nblk; lb++) {
+      if (from[lb] >= 0) {
+        if (out)
+          drop_block(a, from[lb]);
+        else
+          drop_host_block(a, from[lb]);
+      }
+      from[lb] = -1;
+    }
+    a->swapped[s] = out ? 1 : 0;
+  }
+  free(map);
+  return npairs;
+}
+
+int oracle_alloc_swap_out(oracle_alloc* a, int n, const int32_t* seq_ids, int32_t* pairs_out) {
+  return swap_move(a, n, seq_ids, 1, pairs_out);
+}
+
+int oracle_alloc_swap_in(oracle_alloc* a, int n, const int32_t* seq_ids, int32_t* pairs_out) {
+  return swap_move(a, n, seq_ids, 0, pairs_out);
+}
+
+int oracle_alloc_swapped(const oracle_alloc* a, int s) { return a->swapped[s]; }
+int oracle_alloc_host_refcount(const oracle_alloc* a, int b) { return a->host_refcount[b]; }
+int oracle_alloc_num_host_free(const oracle_alloc* a) { return a->host_free_top; }
+
+/* Copies the host table row of a swapped-out sequence (ceil(len/16) entries). */
+int oracle_alloc_host_table(const oracle_alloc* a, int s, int32_t* out) {
+  int nblk = (a->lens[s] + ORACLE_BLOCK - 1) / ORACLE_BLOCK, lb;
+  for (lb = 0; lb < nblk; lb++) out[lb] = a->host_tables[(size_t)s * a->max_blocks + lb];
+  return nblk;
+}
+
+/* Block copies between a device pool and a host pool of the same layout:
+ * pairs[2i] -> pairs[2i+1] (K, V and, when present, the scales). */
+void oracle_copy_blocks_between(const void* src_k, const void* src_v, const float* src_ks, const float* src_vs,
+                                void* dst_k, void* dst_v, float* dst_ks, float* dst_vs, int Hk, int D,
+                                int elem_bytes, const int32_t* pairs, int n) {
+  size_t blk = (size_t)Hk * ORACLE_BLOCK * D * elem_bytes, sb = (size_t)Hk * ORACLE_BLOCK;
+  int i;
+  for (i = 0; i < n; i++) {
+    size_t s = (size_t)pairs[2 * i], d = (size_t)pairs[2 * i + 1];
+    memcpy((char*)dst_k + d * blk, (const char*)src_k + s * blk, blk);
+    memcpy((char*)dst_v + d * blk, (const char*)src_v + s * blk, blk);
+    if (src_ks && dst_ks) {
+      memcpy(dst_ks + d * sb, src_ks + s * sb, sb * sizeof(float));
+      memcpy(dst_vs + d * sb, src_vs + s * sb, sb * sizeof(float));
+    }
+  }
+}
+
 int oracle_alloc_evict(oracle_alloc* a, int s, int num_sinks, int window) {
   int L, lb, nblk;
-  if (s < 0 || s >= a->max_seqs || !a->active[s] || num_sinks < 0 || window < 1) return -2;
+  if (!dev_seq(a, s) || num_sinks < 0 || window < 1) return -2;
   L = a->lens[s];
   if (L <= num_sinks + window) return 0;
   nblk = (L + ORACLE_BLOCK - 1) / ORACLE_BLOCK;
@@ -830,7 +1031,7 @@ int oracle_alloc_compact(oracle_alloc* a, int n, const int32_t* seq_ids, const i
   oracle_alloc* w;
   int i, k, total = 0, pos = 0;
   for (i = 0; i < n; i++) {
-    if (seq_ids[i] < 0 || seq_ids[i] >= a->max_seqs || !a->active[seq_ids[i]]) return -2;
+    if (!dev_seq(a, seq_ids[i])) return -2;
     if (counts[i] < 0 || counts[i] > a->lens[seq_ids[i]]) return -2;
     for (k = 0; k < i; k++)
       if (seq_ids[k] == seq_ids[i]) return -2;

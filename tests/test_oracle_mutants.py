@@ -39,6 +39,9 @@ MUTANTS = {
     "int8 codes truncate": ("  n = round_half_even(a);\n  if (n > 127) n = 127;", "  n = (int)a;\n  if (n > 127) n = 127;"),
     "int8 codes read unsigned": ("if (jb->kv_dtype == KV_INT8) return (double)((const int8_t*)pool)[i] * (double)scl[si];",
                                  "if (jb->kv_dtype == KV_INT8) return (double)((const uint8_t*)pool)[i] * (double)scl[si];"),
+    "swap-out shares no host block": ("      } else if (out) {\n        a->host_refcount[map[b]] += 1;",
+                                      "      } else if (0) {\n        a->host_refcount[map[b]] += 1;"),
+    "swap-in keeps the host blocks": ("        else\n          drop_host_block(a, from[lb]);", "        else\n          (void)0;"),
     "token slot shifted": ("    slot = j % ORACLE_BLOCK;\n    if (block < 0 || block >= jb->num_blocks) {",
                            "    slot = (j + 1) % ORACLE_BLOCK;\n    if (block < 0 || block >= jb->num_blocks) {"),
 }

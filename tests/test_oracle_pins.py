@@ -550,13 +550,22 @@ def test_free_pool_initial_order():
 
 def _check_invariants(a, live):
     NB = a.NB
-    held = {}
+    held, host_held = {}, {}
     for s in live:
         t = a.table(s)
         assert t.size == (a.length(s) + 15) // 16
+        if getattr(a, "NH", 0) and a.swapped(s):
+            assert not (t >= 0).any()  # a swapped-out sequence holds no device block
+            for hb in a.host_table(s):
+                if hb >= 0:
+                    host_held[hb] = host_held.get(hb, 0) + 1
         for blk in t:
             if blk >= 0:
                 held[blk] = held.get(blk, 0) + 1
+    if getattr(a, "NH", 0):
+        assert a.num_host_free() + len(host_held) == a.NH
+        for hb in range(a.NH):
+            assert a.host_refcount(hb) == host_held.get(hb, 0)
     free = a.free_list().tolist()
     assert len(set(free)) == len(free)
     assert set(free).isdisjoint(held)
@@ -566,20 +575,55 @@ def _check_invariants(a, live):
 
 
 def test_allocator_random_ops_invariants_and_contents():
-    """Random add/append/fork/free/evict/H2O-compact/truncate; a content
-    model (token ids written through slots, COW pairs applied as whole-block
-    copies, compaction as row moves into the returned fresh blocks) must give
-    every sequence exactly its own history."""
+    """Random add/append/fork/free/evict/H2O-compact/truncate/CPU swap; a
+    content model (token ids written through slots, COW pairs applied as
+    whole-block copies, compaction as row moves into the returned fresh
+    blocks, swaps as block copies between the device and host pools) must
+    give every sequence exactly its own history."""
     rng = random.Random(2024)
     for trial in range(30):
         NB = rng.randint(8, 60)
         a = oracle.OracleAllocator(NB, 12, 40, seed=rng.randint(0, 10 ** 9))
+        NH = rng.randint(4, 60)
+        a.set_swap_space(NH)
         data = np.full((NB, 16), -1, dtype=np.int64)  # physical content: token labels
+        hdata = np.full((NH, 16), -1, dtype=np.int64)  # host swap space content
         hist = {}  # seq -> list of labels (or None for evicted positions)
         label = 0
         for op in range(120):
-            live = list(hist)
             r = rng.random()
+            if r < 0.1 and hist:
+                # CPU swap: move some sequences out or back in
+                out = rng.random() < 0.5
+                cand = [s for s in hist if a.swapped(s) != out]
+                if cand:
+                    ids = rng.sample(cand, rng.randint(1, len(cand)))
+                    before = (a.free_list().tolist(), a.num_host_free())
+                    try:
+                        pairs = a.swap_out(ids) if out else a.swap_in(ids)
+                    except MemoryError:
+                        assert (a.free_list().tolist(), a.num_host_free()) == before
+                        continue
+                    for src, dst in pairs:
+                        if out:
+                            hdata[dst] = data[src]
+                        else:
+                            data[dst] = hdata[src]
+                    with pytest.raises(ValueError):  # not twice to the same place
+                        a.swap_out(ids[:1]) if out else a.swap_in(ids[:1])
+                    if out:  # device-side operations refuse a swapped-out sequence
+                        with pytest.raises(ValueError):
+                            a.append(ids[:1], 1)
+                        with pytest.raises(ValueError):
+                            a.fork(ids[0])
+                        with pytest.raises(ValueError):
+                            a.truncate(ids[0], 0)
+                _check_invariants(a, list(hist))
+                continue
+            live = [s for s in hist if not a.swapped(s)]
+            r = rng.random()
+            if r >= 0.15 and not live:
+                continue
             if r < 0.15 or not live:
                 try:
                     s = a.seq_add()
@@ -613,7 +657,7 @@ def test_allocator_random_ops_invariants_and_contents():
                     continue
                 hist[d] = list(hist[s])
             elif r < 0.85:
-                s = rng.choice(live)
+                s = rng.choice(list(hist))  # swapped-out sequences can be freed too
                 a.free(s)
                 del hist[s]
             elif r < 0.91:
@@ -657,12 +701,14 @@ def test_allocator_random_ops_invariants_and_contents():
                 hist[s] = hist[s][:n]
             _check_invariants(a, list(hist))
             for s, h in hist.items():
-                t = a.table(s)
+                swapped = a.swapped(s)
+                t = a.host_table(s) if swapped else a.table(s)
+                mem = hdata if swapped else data
                 for j, lab in enumerate(h):
                     if lab is None:
                         assert t[j // 16] == -1
                     else:
-                        assert data[t[j // 16], j % 16] == lab, (trial, op, s, j)
+                        assert mem[t[j // 16], j % 16] == lab, (trial, op, s, j)
 
 
 def test_cow_fires_once_per_shared_partial_block():
