@@ -305,6 +305,51 @@ pkv_status pkv_seq_compact(pkv_pool* pool, void* stream, int32_t n_seqs, const i
                            const int32_t* keep_idx, int64_t keep_stride, const int32_t* counts, float* acc,
                            int64_t acc_stride);
 
+/* ---- CPU swap space ------------------------------------------------------ */
+
+/* CPU swap ([PA] three runtime components: the block allocator manages the
+ * pool in blocks and can swap them out to CPU RAM; [LC] CPU offloading keeps
+ * inactive requests' KV in host memory and loads it back when needed).
+ *
+ * pkv_swap_space_create gives the pool a host pool of num_host_blocks
+ * blocks with the device pool's layout:
+ *   host_k, host_v            [num_host_blocks][n_kv_heads][16][head_dim]
+ *   host_k_scale, host_v_scale [num_host_blocks][n_kv_heads][16] fp32
+ *                              (FP8 / INT8 pools only, else NULL)
+ * On a device pool they must be page-locked host memory the device can
+ * address (cudaHostAlloc, or cudaHostRegister with mapping); the copies run
+ * as one kernel per call that reads or writes them directly.  On a host-only
+ * pool they must be NULL (the allocator alone is tracked).  The host pool
+ * starts in ascending order; allocation takes its front and a released host
+ * block goes back to the front.  Refused while a sequence is swapped out.
+ *
+ * pkv_swap_out: every listed sequence's blocks, in list order and ascending
+ * logical order, get host blocks (a device block shared by several listed
+ * sequences is copied once and its host block shared as many times); the
+ * copies are enqueued on `stream`; then every device block is released (same
+ * order) and the device table rows become -1.  A swapped-out sequence keeps
+ * its length; append, fork, truncate, evict, compaction and decode refuse it;
+ * pkv_seq_free releases its host blocks.
+ * pkv_swap_in mirrors it: device blocks from the front of the device pool (a
+ * host block shared by several listed sequences becomes one shared device
+ * block), copies on `stream`, then the host blocks are released.
+ * Both: PKV_ERR_OUT_OF_BLOCKS when the destination pool is short (state
+ * unchanged); PKV_ERR_INVALID_ARG for a sequence that is not live, already in
+ * the requested place, or listed twice.  Host memory the copies touch may be
+ * read by the caller only after `stream` has passed them. */
+pkv_status pkv_swap_space_create(pkv_pool* pool, int64_t num_host_blocks, void* host_k, void* host_v,
+                                 float* host_k_scale, float* host_v_scale);
+pkv_status pkv_swap_out(pkv_pool* pool, void* stream, int32_t n_seqs, const int32_t* seq_ids);
+pkv_status pkv_swap_in(pkv_pool* pool, void* stream, int32_t n_seqs, const int32_t* seq_ids);
+/* 1 if the sequence is swapped out, else 0. */
+pkv_status pkv_seq_swapped(const pkv_pool* pool, int32_t seq, int32_t* swapped_out);
+/* Host block table of a swapped-out sequence (ceil(len / 16) entries, -1 for
+ * blocks it did not hold); like pkv_get_block_table. */
+pkv_status pkv_get_host_block_table(const pkv_pool* pool, int32_t seq, int32_t* host_out, int32_t cap,
+                                    int32_t* n_out);
+/* Free blocks of the host pool. */
+pkv_status pkv_host_free_blocks(const pkv_pool* pool, int64_t* n_out);
+
 /* Synchronises `stream`, then reports and clears the device status word:
  * PKV_ERR_TIMEOUT, PKV_ERR_DEVICE_ASSERT or PKV_OK. */
 pkv_status pkv_sync_status(pkv_pool* pool, void* stream);
@@ -319,7 +364,9 @@ typedef enum {
   PKV_KERNEL_H2O_SCORE = 4,
   PKV_KERNEL_H2O_SELECT = 5,
   PKV_KERNEL_TABLE_PATCH = 6,
-  PKV_KERNEL_COUNT = 7
+  PKV_KERNEL_SWAP_COPY = 7, /* CPU swap-out / swap-in block copies */
+  PKV_KERNEL_COMPACT = 8,   /* H2O compaction: row gather and score compaction */
+  PKV_KERNEL_COUNT = 9
 } pkv_kernel_id;
 
 /* Bit k of kernel_mask (k a pkv_kernel_id) brackets every launch of kernel k

@@ -147,6 +147,55 @@ class PagedKVCache:
         _abi.check(self.lib.pkv_get_block_table(self._h, seq, _ptr(out), out.size, ctypes.byref(n)))
         return out[: n.value].copy()
 
+    # ---- CPU swap space ---------------------------------------------------
+    def swap_space(self, num_host_blocks: int) -> None:
+        """Gives the pool a host swap pool of num_host_blocks blocks in pinned
+        host memory (allocator only on a host-only pool)."""
+        import torch
+        self.num_host_blocks = num_host_blocks
+        if self.host_only:
+            _abi.check(self.lib.pkv_swap_space_create(self._h, num_host_blocks, None, None, None, None))
+            return
+        shape = (num_host_blocks, self.n_kv_heads, BLOCK_SIZE, self.head_dim)
+        self.host_k = torch.empty(shape, dtype=self.k_pool.dtype, pin_memory=True)
+        self.host_v = torch.empty(shape, dtype=self.k_pool.dtype, pin_memory=True)
+        if self.k_scale is not None:
+            self.host_k_scale = torch.empty(shape[:3], dtype=torch.float32, pin_memory=True)
+            self.host_v_scale = torch.empty(shape[:3], dtype=torch.float32, pin_memory=True)
+        else:
+            self.host_k_scale = self.host_v_scale = None
+        with torch.cuda.device(self.device):
+            _abi.check(self.lib.pkv_swap_space_create(
+                self._h, num_host_blocks, self.host_k.data_ptr(), self.host_v.data_ptr(),
+                self.host_k_scale.data_ptr() if self.host_k_scale is not None else None,
+                self.host_v_scale.data_ptr() if self.host_v_scale is not None else None))
+
+    def swap_out(self, seq_ids, stream=None) -> None:
+        ids = _i32_array(seq_ids)
+        _abi.check(self.lib.pkv_swap_out(self._h, None if self.host_only else _stream_ptr(stream), ids.size,
+                                         _ptr(ids)))
+
+    def swap_in(self, seq_ids, stream=None) -> None:
+        ids = _i32_array(seq_ids)
+        _abi.check(self.lib.pkv_swap_in(self._h, None if self.host_only else _stream_ptr(stream), ids.size,
+                                        _ptr(ids)))
+
+    def swapped(self, seq: int) -> bool:
+        v = ctypes.c_int32()
+        _abi.check(self.lib.pkv_seq_swapped(self._h, seq, ctypes.byref(v)))
+        return bool(v.value)
+
+    def host_block_table(self, seq: int) -> np.ndarray:
+        out = np.empty(self.max_blocks_per_seq, dtype=np.int32)
+        n = ctypes.c_int32()
+        _abi.check(self.lib.pkv_get_host_block_table(self._h, seq, _ptr(out), out.size, ctypes.byref(n)))
+        return out[: n.value].copy()
+
+    def host_free_blocks(self) -> int:
+        v = ctypes.c_int64()
+        _abi.check(self.lib.pkv_host_free_blocks(self._h, ctypes.byref(v)))
+        return int(v.value)
+
     def stats(self) -> dict:
         st = _abi.pkv_stats()
         _abi.check(self.lib.pkv_pool_stats(self._h, ctypes.byref(st)))

@@ -19,7 +19,8 @@ STATUS_NAMES = {
 }
 KV_DTYPES = {"fp32": 0, "bf16": 1, "fp8": 2, "fp8_e4m3": 2, "int8": 3}
 MASKS = {"full": 0, "sliding": 1, "sink_window": 2}
-KERNELS = ["cow_copy", "append", "decode", "combine", "h2o_score", "h2o_select", "table_patch"]
+KERNELS = ["cow_copy", "append", "decode", "combine", "h2o_score", "h2o_select", "table_patch", "swap_copy",
+           "compact"]
 
 
 class PKVError(RuntimeError):
@@ -85,6 +86,12 @@ SIGNATURES = {
     "pkv_launch_count": [c_void_p, _P(c_int64)],
     "pkv_set_wait_limit": [c_void_p, c_int64],
     "pkv_set_cascade": [c_void_p, c_int32],
+    "pkv_swap_space_create": [c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_void_p],
+    "pkv_swap_out": [c_void_p, c_void_p, c_int32, c_void_p],
+    "pkv_swap_in": [c_void_p, c_void_p, c_int32, c_void_p],
+    "pkv_seq_swapped": [c_void_p, c_int32, c_void_p],
+    "pkv_get_host_block_table": [c_void_p, c_int32, c_void_p, c_int32, c_void_p],
+    "pkv_host_free_blocks": [c_void_p, c_void_p],
     "pkv_test_starve_next_decode": [c_void_p, c_int32],
     "pkv_last_error": [],
     "pkv_version": [],

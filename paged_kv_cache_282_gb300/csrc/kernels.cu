@@ -129,20 +129,25 @@ __global__ void append_quant_kernel(const __grid_constant__ AppendArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// copy-on-write: copy whole physical blocks (K, V, and FP8 / INT8 scales)
+// copy-on-write and CPU swap: copy whole physical blocks (K, V, and FP8 /
+// INT8 scales)
 // ---------------------------------------------------------------------------
 
-__global__ void cow_copy_kernel(const int32_t* __restrict__ pairs, uint4* __restrict__ k, uint4* __restrict__ v,
-                                int64_t chunks, float* __restrict__ ks, float* __restrict__ vs, int64_t sfloats) {
+// Whole-block copies pairs[2i] -> pairs[2i+1] from one pool to another (the
+// same pool for copy-on-write; device <-> pinned host pool for CPU swap, the
+// host side reached through its device-mapped address).
+__global__ void block_copy_kernel(const int32_t* __restrict__ pairs, const uint4* src_k, const uint4* src_v,
+                                  uint4* dst_k, uint4* dst_v, int64_t chunks, const float* src_ks,
+                                  const float* src_vs, float* dst_ks, float* dst_vs, int64_t sfloats) {
   const int64_t src = pairs[2 * blockIdx.y], dst = pairs[2 * blockIdx.y + 1];
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < chunks; i += (int64_t)gridDim.x * blockDim.x) {
-    k[dst * chunks + i] = k[src * chunks + i];
-    v[dst * chunks + i] = v[src * chunks + i];
+    dst_k[dst * chunks + i] = src_k[src * chunks + i];
+    dst_v[dst * chunks + i] = src_v[src * chunks + i];
   }
-  if (ks && blockIdx.x == 0)
+  if (src_ks && blockIdx.x == 0)
     for (int64_t i = threadIdx.x; i < sfloats; i += blockDim.x) {
-      ks[dst * sfloats + i] = ks[src * sfloats + i];
-      vs[dst * sfloats + i] = vs[src * sfloats + i];
+      dst_ks[dst * sfloats + i] = src_ks[src * sfloats + i];
+      dst_vs[dst * sfloats + i] = src_vs[src * sfloats + i];
     }
 }
 
@@ -580,18 +585,26 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_cow_copy(const int32_t* pairs, int n_pairs, void* k_pool, void* v_pool, float* k_scale,
-                            float* v_scale, size_t block_bytes, size_t scale_floats, cudaStream_t st) {
+cudaError_t launch_block_copy(const int32_t* pairs, int n_pairs, const void* src_k, const void* src_v,
+                              const float* src_ks, const float* src_vs, void* dst_k, void* dst_v, float* dst_ks,
+                              float* dst_vs, size_t block_bytes, size_t scale_floats, cudaStream_t st) {
   if (n_pairs <= 0) return cudaSuccess;
   const int64_t chunks = (int64_t)(block_bytes / 16);
   for (int first = 0; first < n_pairs; first += 65535) {
     const int n = std::min(65535, n_pairs - first);
     dim3 grid((unsigned)std::min<int64_t>((chunks + 255) / 256, 64), (unsigned)n);
-    cow_copy_kernel<<<grid, 256, 0, st>>>(pairs + 2 * first, (uint4*)k_pool, (uint4*)v_pool, chunks,
-                                          scale_floats ? k_scale : nullptr, scale_floats ? v_scale : nullptr,
-                                          (int64_t)scale_floats);
+    block_copy_kernel<<<grid, 256, 0, st>>>(pairs + 2 * first, (const uint4*)src_k, (const uint4*)src_v,
+                                            (uint4*)dst_k, (uint4*)dst_v, chunks, scale_floats ? src_ks : nullptr,
+                                            scale_floats ? src_vs : nullptr, dst_ks, dst_vs, (int64_t)scale_floats);
+    if (cudaError_t e = cudaGetLastError()) return e;
   }
-  return cudaGetLastError();
+  return cudaSuccess;
+}
+
+cudaError_t launch_cow_copy(const int32_t* pairs, int n_pairs, void* k_pool, void* v_pool, float* k_scale,
+                            float* v_scale, size_t block_bytes, size_t scale_floats, cudaStream_t st) {
+  return launch_block_copy(pairs, n_pairs, k_pool, v_pool, k_scale, v_scale, k_pool, v_pool, k_scale, v_scale,
+                           block_bytes, scale_floats, st);
 }
 
 cudaError_t launch_table_patch(const int32_t* patches, int n, int32_t* tables, cudaStream_t st) {

@@ -135,6 +135,9 @@ cudaError_t decode_tc_occupancy(int kv_dtype, int G, int nq, int* ctas_per_sm);
 
 cudaError_t launch_decode_f32(const DecodeF32Params& p, cudaStream_t stream);
 
+cudaError_t launch_block_copy(const int32_t* pairs, int n_pairs, const void* src_k, const void* src_v,
+                              const float* src_ks, const float* src_vs, void* dst_k, void* dst_v, float* dst_ks,
+                              float* dst_vs, size_t block_bytes, size_t scale_floats, cudaStream_t stream);
 cudaError_t launch_cow_copy(const int32_t* pairs, int n_pairs, void* k_pool, void* v_pool,
                             float* k_scale, float* v_scale, size_t block_bytes,
                             size_t scale_floats_per_block, cudaStream_t stream);

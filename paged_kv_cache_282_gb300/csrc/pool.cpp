@@ -144,11 +144,36 @@ struct HostAllocator {
     len.assign(ms, 0);
     live.assign(ms, 0);
     holes.assign(ms, 0);
+    swapped.assign(ms, 0);
+    host_table.assign(ms, {});
     free_ids.clear();
     for (int32_t s = 0; s < ms; ++s) free_ids.insert(s);
   }
 
   bool valid_seq(int32_t s) const { return s >= 0 && s < max_seqs && live[s]; }
+  // live and with its blocks on the device (not swapped out)
+  bool on_device(int32_t s) const { return valid_seq(s) && !swapped[s]; }
+
+  // CPU swap space: host blocks with their own counts and free pool
+  int32_t NH = 0;
+  std::vector<int32_t> host_refcount, host_free;  // host_free.back() is the front
+  std::vector<std::vector<int32_t>> host_table;
+  std::vector<uint8_t> swapped;
+  void set_swap_space(int32_t nh) {
+    NH = nh;
+    host_refcount.assign(nh, 0);
+    host_free.resize(nh);
+    for (int32_t i = 0; i < nh; ++i) host_free[i] = nh - 1 - i;
+  }
+  int32_t take_host() {
+    const int32_t b = host_free.back();
+    host_free.pop_back();
+    host_refcount[b] = 1;
+    return b;
+  }
+  void release_host(int32_t b) {
+    if (--host_refcount[b] == 0) host_free.push_back(b);
+  }
 
   int32_t take() {
     int32_t b = free_blocks.back();
@@ -302,6 +327,12 @@ struct pkv_pool {
   // Vectors reused by every decode plan: fresh ones each call would spend
   // most of the planning time faulting in new pages.
   std::unique_ptr<PlanCache, PlanCacheDeleter> plan_cache;
+  // CPU swap space (host pointers and their device-mapped addresses)
+  bool swap_space = false;
+  void *host_k = nullptr, *host_v = nullptr;
+  float *host_ks = nullptr, *host_vs = nullptr;
+  void *host_k_dev = nullptr, *host_v_dev = nullptr;
+  float *host_ks_dev = nullptr, *host_vs_dev = nullptr;
 };
 
 namespace {
@@ -467,7 +498,8 @@ pkv_status check_seq_list(const pkv_pool* p, int32_t n, const int32_t* ids) {
   if (n < 0) return fail(PKV_ERR_INVALID_ARG, "n_seqs < 0");
   if (n > 0 && !ids) return fail(PKV_ERR_INVALID_ARG, "seq_ids is NULL");
   for (int32_t i = 0; i < n; ++i)
-    if (!p->alloc.valid_seq(ids[i])) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", ids[i]);
+    if (!p->alloc.on_device(ids[i]))
+      return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live or is swapped out", ids[i]);
   return PKV_OK;
 }
 
@@ -1074,6 +1106,122 @@ int pkv::decode_attn_into(pkv_pool* p, void* stream, int32_t n, const int32_t* i
 // C ABI
 // ---------------------------------------------------------------------------
 
+// ---------------------------------------------------------------------------
+// CPU swap space
+// ---------------------------------------------------------------------------
+
+namespace {
+
+pkv_status map_host(void* h, void** dev, const char* what) {
+  *dev = nullptr;
+  if (!h) return PKV_OK;
+  if ((uintptr_t)h & 15) return fail(PKV_ERR_INVALID_ARG, "%s must be 16-byte aligned", what);
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, h) != cudaSuccess || at.type != cudaMemoryTypeHost) {
+    cudaGetLastError();
+    return fail(PKV_ERR_UNSUPPORTED, "%s is not page-locked host memory", what);
+  }
+  if (cudaHostGetDevicePointer(dev, h, 0) != cudaSuccess || !*dev) {
+    cudaGetLastError();
+    return fail(PKV_ERR_UNSUPPORTED, "%s has no device-mapped address", what);
+  }
+  return PKV_OK;
+}
+
+// Swap-out (out) or swap-in of the listed sequences: allocator moves, then the
+// block copies on `stream`.
+pkv_status swap_move(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, bool out) {
+  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  if (!p->swap_space) return fail(PKV_ERR_INVALID_ARG, "the pool has no swap space");
+  if (n < 0 || (n > 0 && !ids)) return fail(PKV_ERR_INVALID_ARG, "bad sequence list");
+  auto& A = p->alloc;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t s = ids[i];
+    if (!A.valid_seq(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", s);
+    if (A.swapped[s] != (out ? 0 : 1))
+      return fail(PKV_ERR_INVALID_ARG, "sequence %d is already %s", s, out ? "swapped out" : "on the device");
+    for (int32_t j = 0; j < i; ++j)
+      if (ids[j] == s) return fail(PKV_ERR_INVALID_ARG, "sequence %d listed twice", s);
+  }
+  std::unordered_map<int32_t, int32_t> moved;  // source block -> destination block
+  for (int32_t i = 0; i < n; ++i)
+    for (int32_t b : out ? A.table[ids[i]] : A.host_table[ids[i]])
+      if (b >= 0) moved.emplace(b, -1);
+  const size_t avail = out ? A.host_free.size() : A.free_blocks.size();
+  if (moved.size() > avail)
+    return fail(PKV_ERR_OUT_OF_BLOCKS, "swap-%s needs %zu blocks, %zu free", out ? "out" : "in", moved.size(), avail);
+  cudaStream_t st = (cudaStream_t)stream;
+  // queued copies first: a pending copy-on-write must land before its blocks move
+  if (p->device)
+    if (pkv_status r = flush_pending(p, st)) return r;
+  std::vector<int32_t> pairs;
+  pairs.reserve(2 * moved.size());
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t s = ids[i], nb = ceil_div(A.len[s], kBlock);
+    std::vector<int32_t> row(nb, -1);
+    const std::vector<int32_t>& from = out ? A.table[s] : A.host_table[s];
+    for (int32_t lb = 0; lb < nb && lb < (int32_t)from.size(); ++lb) {
+      const int32_t b = from[lb];
+      if (b < 0) continue;
+      int32_t& m = moved[b];
+      if (m < 0) {
+        m = out ? A.take_host() : A.take();
+        pairs.push_back(b);
+        pairs.push_back(m);
+      } else if (out) {
+        ++A.host_refcount[m];
+      } else {
+        ++A.refcount[m];
+      }
+      row[lb] = m;
+    }
+    if (out) {
+      A.host_table[s] = row;
+    } else {
+      for (int32_t lb = 0; lb < nb; ++lb) A.set_entry(s, lb, row[lb]);
+    }
+  }
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t s = ids[i], nb = ceil_div(A.len[s], kBlock);
+    if (out) {
+      A.drop_from(s, 0);  // releases the device blocks, ascending; rows become -1
+      A.table[s].assign(nb, -1);
+      A.swapped[s] = 1;
+    } else {
+      for (int32_t hb : A.host_table[s])
+        if (hb >= 0) A.release_host(hb);
+      A.host_table[s].clear();
+      A.swapped[s] = 0;
+    }
+  }
+  if (!p->device) {
+    A.pending_patch.clear();
+    return PKV_OK;
+  }
+  const int npairs = (int)(pairs.size() / 2);
+  if (npairs == 0) return PKV_OK;
+  const auto& c = p->cfg;
+  const size_t blk_bytes = (size_t)c.n_kv_heads * kBlock * c.head_dim * elem_bytes(c.kv_dtype);
+  const size_t scl = has_scales(c.kv_dtype) ? (size_t)c.n_kv_heads * kBlock : 0;
+  StagingSlot* sl;
+  if (pkv_status r = p->staging.acquire(pairs.size() * sizeof(int32_t), &sl)) return r;
+  memcpy(sl->host, pairs.data(), pairs.size() * sizeof(int32_t));
+  if (pkv_status r = Staging::upload(sl, pairs.size() * sizeof(int32_t), st)) return r;
+  if (pkv_status r = launch(p, PKV_KERNEL_SWAP_COPY, st, [&] {
+        if (out)
+          return launch_block_copy((const int32_t*)sl->dev, npairs, p->buf.k_pool, p->buf.v_pool, p->buf.k_scale,
+                                   p->buf.v_scale, p->host_k_dev, p->host_v_dev, p->host_ks_dev, p->host_vs_dev,
+                                   blk_bytes, scl, st);
+        return launch_block_copy((const int32_t*)sl->dev, npairs, p->host_k_dev, p->host_v_dev, p->host_ks_dev,
+                                 p->host_vs_dev, p->buf.k_pool, p->buf.v_pool, p->buf.k_scale, p->buf.v_scale,
+                                 blk_bytes, scl, st);
+      }))
+    return r;
+  return Staging::release(sl, st);
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* pkv_last_error(void) { return g_last_error.c_str(); }
@@ -1176,7 +1324,7 @@ pkv_status pkv_seq_add(pkv_pool* p, int32_t* seq_out) {
 pkv_status pkv_seq_fork(pkv_pool* p, int32_t src, int32_t* dst_out) {
   if (!p || !dst_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
   auto& A = p->alloc;
-  if (!A.valid_seq(src)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", src);
+  if (!A.on_device(src)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live or is swapped out", src);
   int32_t d;
   if (pkv_status r = pkv_seq_add(p, &d)) return r;
   const int32_t nblk = ceil_div(A.len[src], kBlock);
@@ -1194,7 +1342,7 @@ pkv_status pkv_seq_fork(pkv_pool* p, int32_t src, int32_t* dst_out) {
 pkv_status pkv_seq_truncate(pkv_pool* p, int32_t s, int32_t new_len) {
   if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
   auto& A = p->alloc;
-  if (!A.valid_seq(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", s);
+  if (!A.on_device(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live or is swapped out", s);
   if (new_len < 0 || new_len > A.len[s]) return fail(PKV_ERR_INVALID_ARG, "new_len %d outside [0, %d]", new_len, A.len[s]);
   const int32_t keep_blk = ceil_div(new_len, kBlock);
   if (new_len % kBlock && A.table[s][keep_blk - 1] < 0)
@@ -1210,7 +1358,7 @@ pkv_status pkv_seq_truncate_many(pkv_pool* p, int32_t n, const int32_t* ids, con
   auto& A = p->alloc;
   for (int32_t i = 0; i < n; ++i) {  // validate everything before changing anything
     const int32_t s = ids[i], L = new_lens[i];
-    if (!A.valid_seq(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", s);
+    if (!A.on_device(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live or is swapped out", s);
     if (L < 0 || L > A.len[s]) return fail(PKV_ERR_INVALID_ARG, "new_len %d outside [0, %d]", L, A.len[s]);
     if (L % kBlock && A.table[s][ceil_div(L, kBlock) - 1] < 0)
       return fail(PKV_ERR_INVALID_ARG, "the new last block of sequence %d was evicted", s);
@@ -1225,8 +1373,18 @@ pkv_status pkv_seq_truncate_many(pkv_pool* p, int32_t n, const int32_t* ids, con
 }
 
 pkv_status pkv_seq_free(pkv_pool* p, int32_t s) {
-  if (pkv_status r = pkv_seq_truncate(p, s, 0)) return r;
+  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
   auto& A = p->alloc;
+  if (A.valid_seq(s) && A.swapped[s]) {  // give back the host blocks, ascending
+    for (int32_t hb : A.host_table[s])
+      if (hb >= 0) A.release_host(hb);
+    A.host_table[s].clear();
+    A.table[s].clear();
+    A.swapped[s] = 0;
+    A.len[s] = 0;
+  } else if (pkv_status r = pkv_seq_truncate(p, s, 0)) {
+    return r;
+  }
   A.live[s] = 0;
   A.holes[s] = 0;
   A.free_ids.insert(s);
@@ -1238,6 +1396,7 @@ pkv_status pkv_seq_evict(pkv_pool* p, int32_t s, int32_t S, int32_t W) {
   auto& A = p->alloc;
   if (!A.valid_seq(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", s);
   if (S < 0 || W < 1) return fail(PKV_ERR_INVALID_ARG, "need num_sinks >= 0 and window >= 1");
+  if (A.swapped[s]) return fail(PKV_ERR_INVALID_ARG, "sequence %d is swapped out", s);
   const int32_t L = A.len[s];
   if ((int64_t)L <= (int64_t)S + W) return PKV_OK;
   const int32_t nblk = ceil_div(L, kBlock);
@@ -1470,7 +1629,7 @@ pkv_status pkv_seq_compact(pkv_pool* p, void* stream, int32_t n, const int32_t* 
     const auto& c = p->cfg;
     const int row_bytes = c.head_dim * elem_bytes(c.kv_dtype);
     const bool fp8 = has_scales(c.kv_dtype);
-    if (pkv_status r = launch(p, PKV_KERNEL_COW_COPY, st, [&] {
+    if (pkv_status r = launch(p, PKV_KERNEL_COMPACT, st, [&] {
           return launch_compact_gather((const CompactSeq*)s->dev, n, max_count, (const int32_t*)(s->dev + off),
                                        p->buf.block_tables, c.max_blocks_per_seq, c.num_blocks, keep_idx, keep_stride,
                                        c.n_kv_heads, row_bytes, p->buf.k_pool, p->buf.v_pool,
@@ -1492,11 +1651,76 @@ pkv_status pkv_seq_compact(pkv_pool* p, void* stream, int32_t n, const int32_t* 
   }
   if (pkv_status r = flush_pending(p, st)) return r;  // new tables, after the gather
   if (acc && n > 0)
-    if (pkv_status r = launch(p, PKV_KERNEL_H2O_SCORE, st, [&] {
+    if (pkv_status r = launch(p, PKV_KERNEL_COMPACT, st, [&] {
           return launch_compact_scores((const CompactSeq*)s->dev, n, keep_idx, keep_stride, acc, acc_stride, st);
         }))
       return r;
   return s ? Staging::release(s, st) : PKV_OK;
+}
+
+pkv_status pkv_swap_space_create(pkv_pool* p, int64_t nh, void* hk, void* hv, float* hks, float* hvs) {
+  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  auto& A = p->alloc;
+  if (nh < 0 || nh > INT32_MAX) return fail(PKV_ERR_INVALID_ARG, "num_host_blocks %lld out of range", (long long)nh);
+  for (int32_t s = 0; s < A.max_seqs; ++s)
+    if (A.swapped[s]) return fail(PKV_ERR_INVALID_ARG, "sequence %d is swapped out", s);
+  const bool scaled = has_scales(p->cfg.kv_dtype);
+  void *kd = nullptr, *vd = nullptr, *ksd = nullptr, *vsd = nullptr;
+  if (p->device) {
+    if (nh > 0 && (!hk || !hv || (scaled && (!hks || !hvs))))
+      return fail(PKV_ERR_INVALID_ARG, "a host buffer of the swap space is NULL");
+    if (pkv_status r = map_host(hk, &kd, "host_k")) return r;
+    if (pkv_status r = map_host(hv, &vd, "host_v")) return r;
+    if (scaled) {
+      if (pkv_status r = map_host(hks, &ksd, "host_k_scale")) return r;
+      if (pkv_status r = map_host(hvs, &vsd, "host_v_scale")) return r;
+    }
+  } else if (hk || hv || hks || hvs) {
+    return fail(PKV_ERR_INVALID_ARG, "a host-only pool takes no swap buffers");
+  }
+  p->host_k = hk;
+  p->host_v = hv;
+  p->host_ks = scaled ? hks : nullptr;
+  p->host_vs = scaled ? hvs : nullptr;
+  p->host_k_dev = kd;
+  p->host_v_dev = vd;
+  p->host_ks_dev = (float*)ksd;
+  p->host_vs_dev = (float*)vsd;
+  A.set_swap_space((int32_t)nh);
+  p->swap_space = true;
+  return PKV_OK;
+}
+
+pkv_status pkv_swap_out(pkv_pool* p, void* stream, int32_t n, const int32_t* ids) {
+  return swap_move(p, stream, n, ids, true);
+}
+
+pkv_status pkv_swap_in(pkv_pool* p, void* stream, int32_t n, const int32_t* ids) {
+  return swap_move(p, stream, n, ids, false);
+}
+
+pkv_status pkv_seq_swapped(const pkv_pool* p, int32_t s, int32_t* swapped_out) {
+  if (!p || !swapped_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  if (!p->alloc.valid_seq(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", s);
+  *swapped_out = p->alloc.swapped[s];
+  return PKV_OK;
+}
+
+pkv_status pkv_get_host_block_table(const pkv_pool* p, int32_t s, int32_t* host_out, int32_t cap, int32_t* n_out) {
+  if (!p || !n_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  const auto& A = p->alloc;
+  if (!A.valid_seq(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", s);
+  const int32_t n = A.swapped[s] ? ceil_div(A.len[s], kBlock) : 0;
+  *n_out = n;
+  if (n > cap || (n > 0 && !host_out)) return fail(PKV_ERR_INVALID_ARG, "capacity %d < %d entries", cap, n);
+  for (int32_t i = 0; i < n; ++i) host_out[i] = A.host_table[s][i];
+  return PKV_OK;
+}
+
+pkv_status pkv_host_free_blocks(const pkv_pool* p, int64_t* n_out) {
+  if (!p || !n_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  *n_out = (int64_t)p->alloc.host_free.size();
+  return PKV_OK;
 }
 
 pkv_status pkv_decode_workspace_size(const pkv_pool* p, int32_t n, int32_t num_splits, size_t* bytes_out) {

@@ -85,6 +85,23 @@ class Twin:
         self.pool.copy_rows(src, dst)
         return fresh
 
+    def swap_space(self, num_host_blocks: int) -> None:
+        self.cache.swap_space(num_host_blocks)
+        self.alloc.set_swap_space(num_host_blocks)
+        self.pool.add_host_pool(num_host_blocks)
+
+    def swap_out(self, seq_ids) -> np.ndarray:
+        self.cache.swap_out(list(seq_ids))
+        pairs = self.alloc.swap_out(list(seq_ids))
+        self.pool.swap_copy(pairs, out=True)
+        return pairs
+
+    def swap_in(self, seq_ids) -> np.ndarray:
+        self.cache.swap_in(list(seq_ids))
+        pairs = self.alloc.swap_in(list(seq_ids))
+        self.pool.swap_copy(pairs, out=False)
+        return pairs
+
     def tables(self, seq_ids) -> np.ndarray:
         return self.alloc.tables_matrix(list(seq_ids))
 

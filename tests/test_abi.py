@@ -101,8 +101,36 @@ def _replay(pkv, seed):
     aseed = rng.randint(0, 2 ** 63)
     lib = pkv.PagedKVCache(NB, 4, 2, 64, 10, 48, kv_dtype="fp32", alloc_seed=aseed, host_only=True)
     ora = oracle.OracleAllocator(NB, 10, 48, seed=aseed)
-    live = []
+    NH = rng.randint(4, 80)
+    lib.swap_space(NH)
+    ora.set_swap_space(NH)
+    seqs = []  # every live sequence, swapped out or not
     for op in range(150):
+        if seqs and rng.random() < 0.12:
+            out = rng.random() < 0.5
+            cand = [s for s in seqs if ora.swapped(s) != out]
+            if cand:
+                ids = rng.sample(cand, rng.randint(1, len(cand)))
+                try:
+                    (lib.swap_out if out else lib.swap_in)(ids)
+                    ok = True
+                except pkv.PKVError as e:
+                    ok = e.status
+                try:
+                    ora.swap_out(ids) if out else ora.swap_in(ids)
+                    ok2 = True
+                except MemoryError:
+                    ok2 = 3
+                assert ok == ok2
+                if out and ok is True:  # device-side operations refuse it
+                    for call in (lambda: lib.reserve_slots(ids[:1], 1), lambda: lib.seq_fork(ids[0]),
+                                 lambda: lib.seq_truncate(ids[0], 0), lambda: lib.seq_evict(ids[0], 1, 4),
+                                 lambda: lib.seq_compact(ids[:1], [0])):
+                        with pytest.raises(pkv.PKVError) as e:
+                            call()
+                        assert e.value.status == 1
+            continue
+        live = [s for s in seqs if not ora.swapped(s)]
         r = rng.random()
         if r < 0.15 or not live:
             try:
@@ -113,7 +141,7 @@ def _replay(pkv, seed):
                     ora.seq_add()
                 continue
             assert a == ora.seq_add()
-            live.append(a)
+            seqs.append(a)
         elif r < 0.65:
             ids = rng.sample(live, rng.randint(1, len(live)))
             T = rng.randint(1, 24)
@@ -142,12 +170,12 @@ def _replay(pkv, seed):
                     ora.fork(s)
                 continue
             assert d == ora.fork(s)
-            live.append(d)
+            seqs.append(d)
         elif r < 0.85:
-            s = rng.choice(live)
+            s = rng.choice(seqs)  # swapped-out sequences can be freed too
             lib.seq_free(s)
             ora.free(s)
-            live.remove(s)
+            seqs.remove(s)
         elif r < 0.91:
             s = rng.choice(live)
             S, W = rng.randint(0, 5), rng.randint(1, 40)
@@ -181,18 +209,22 @@ def _replay(pkv, seed):
             except ValueError:
                 ok2 = False
             assert ok == ok2
-        for s in live:
+        for s in seqs:
             assert lib.seq_len(s) == ora.length(s)
             assert np.array_equal(lib.block_table(s), ora.table(s)), (seed, op, s)
+            assert lib.swapped(s) == ora.swapped(s)
+            if ora.swapped(s):
+                assert np.array_equal(lib.host_block_table(s), ora.host_table(s)), (seed, op, s)
         st = lib.stats()
         assert st["free_blocks"] == ora.num_free()
+        assert lib.host_free_blocks() == ora.num_host_free()
         assert st["shared_blocks"] == sum(1 for b in range(NB) if ora.refcount(b) > 1)
 
 
 @pytest.mark.parametrize("seed", range(12))
 def test_allocator_matches_oracle_replay(pkv, seed):
     """Random adds, appends (with copy-on-write), forks, frees, evictions,
-    H2O compactions and truncations, the same on both sides."""
+    H2O compactions, truncations and CPU swaps, the same on both sides."""
     _replay(pkv, seed)
 
 
