@@ -211,7 +211,8 @@ struct StagingSlot {
   char* host = nullptr;
   char* dev = nullptr;
   size_t cap = 0;
-  cudaEvent_t done = nullptr;  // recorded after the last kernel reading `dev`
+  cudaEvent_t done = nullptr;    // recorded after the last kernel reading `dev`
+  cudaEvent_t copied = nullptr;  // recorded after an upload on the copy stream
   bool pending = false;
 };
 
@@ -247,19 +248,37 @@ struct Staging {
     if (bytes) PKV_CUDA(cudaMemcpyAsync(s->dev, s->host, bytes, cudaMemcpyHostToDevice, st));
     return PKV_OK;
   }
+  // The same copy on the pool's own copy stream, with `st` waiting for it: the
+  // copy then overlaps whatever `st` is still running (a decode plan upload
+  // overlaps the append kernel before it).  The slot's previous readers have
+  // finished (acquire waited for them), so nothing on `st` is overtaken.
+  cudaStream_t copy_stream = nullptr;
+  pkv_status upload_overlapped(StagingSlot* s, size_t bytes, cudaStream_t st) {
+    if (!bytes) return PKV_OK;
+    if (!copy_stream) PKV_CUDA(cudaStreamCreateWithFlags(&copy_stream, cudaStreamNonBlocking));
+    if (!s->copied) PKV_CUDA(cudaEventCreateWithFlags(&s->copied, cudaEventDisableTiming));
+    PKV_CUDA(cudaMemcpyAsync(s->dev, s->host, bytes, cudaMemcpyHostToDevice, copy_stream));
+    PKV_CUDA(cudaEventRecord(s->copied, copy_stream));
+    PKV_CUDA(cudaStreamWaitEvent(st, s->copied, 0));
+    return PKV_OK;
+  }
   static pkv_status release(StagingSlot* s, cudaStream_t st) {
     PKV_CUDA(cudaEventRecord(s->done, st));
     s->pending = true;
     return PKV_OK;
   }
   void destroy() {
+    if (copy_stream) cudaStreamSynchronize(copy_stream);
     for (auto& s : slot) {
       if (s.pending) cudaEventSynchronize(s.done);
       if (s.host) cudaFreeHost(s.host);
       if (s.dev) cudaFree(s.dev);
       if (s.done) cudaEventDestroy(s.done);
+      if (s.copied) cudaEventDestroy(s.copied);
       s = StagingSlot{};
     }
+    if (copy_stream) cudaStreamDestroy(copy_stream);
+    copy_stream = nullptr;
   }
 };
 
@@ -1796,7 +1815,7 @@ pkv_status pkv_decode_attn(pkv_pool* p, void* stream, int32_t n, const int32_t* 
   StagingSlot* s;
   if (pkv_status r = p->staging.acquire(L.bytes, &s)) return r;
   plan_write(plan, L, s->host);
-  if (pkv_status r = Staging::upload(s, L.bytes, st)) return r;
+  if (pkv_status r = p->staging.upload_overlapped(s, L.bytes, st)) return r;
   if (pkv_status r = launch_tc_plan(p, st, plan, L, s->dev, q, scale, mode, S, W, out, lse, logits, logits_stride,
                                     workspace))
     return r;
