@@ -244,14 +244,15 @@ struct SelShared {
 };
 
 // Histogram of digit (key >> shift) & 255 over the keys i < m whose bits under
-// `mask` equal `prefix`.  Each thread counts runs of equal digits and adds a
-// run to the shared histogram only when its digit changes: scores are often
-// equal (zero outside the keep-set), and one shared bin would serialise.
+// `mask` equal `prefix`.  Scores are often equal (zero outside the keep-set,
+// or of one magnitude), so lanes of a warp holding the same digit are
+// grouped (match.any) and their leader adds the group's count: one shared
+// atomic per distinct digit per warp step instead of one per key.
 template <class KeyAt>
 __device__ void digit_histogram(KeyAt key_at, int m, uint32_t prefix, uint32_t mask, int shift, SelShared& sh) {
   for (int i = threadIdx.x; i < 256; i += blockDim.x) sh.hist[i] = 0;
   __syncthreads();
-  uint32_t run_digit = 256u, run = 0u;
+  const int lane = threadIdx.x & 31;
   for (int base = 0; base < m; base += kSelUnroll * kSelThreads) {
     uint32_t key[kSelUnroll];
 #pragma unroll
@@ -262,19 +263,43 @@ __device__ void digit_histogram(KeyAt key_at, int m, uint32_t prefix, uint32_t m
 #pragma unroll
     for (int u = 0; u < kSelUnroll; ++u) {
       const int i = base + u * kSelThreads + threadIdx.x;
-      if (i < m && (key[u] & mask) == prefix) {
-        const uint32_t digit = (key[u] >> shift) & 255u;
-        if (digit == run_digit) {
-          ++run;
-        } else {
-          if (run) atomicAdd(&sh.hist[run_digit], run);
-          run_digit = digit;
-          run = 1u;
-        }
-      }
+      const bool in = i < m && (key[u] & mask) == prefix;
+      if (!__any_sync(0xffffffffu, in)) continue;
+      const uint32_t digit = in ? (key[u] >> shift) & 255u : 256u;
+      const uint32_t peers = __match_any_sync(0xffffffffu, digit);
+      if (in && lane == __ffs(peers) - 1) atomicAdd(&sh.hist[digit], (uint32_t)__popc(peers));
     }
   }
-  if (run) atomicAdd(&sh.hist[run_digit], run);
+  __syncthreads();
+}
+
+// Finds, in parallel over the 256 bins, the digit d whose bin holds the k-th
+// largest key: (keys in bins above d) < k <= (keys in bins d and above).
+// Writes d to *digit_out and k minus the keys above it to *k_out, and the
+// keys in bins d and above to *count_out (when not NULL).  Called by the
+// whole block; ends with a barrier.
+__device__ void find_digit(SelShared& sh, int k, int* digit_out, int* k_out, int* count_out) {
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  // bins in descending digit order: position j holds digit 255 - j
+  int c = t < 256 ? (int)sh.hist[255 - t] : 0;
+  int incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (t < 256 && lane == 31) sh.warp[w] = incl;
+  __syncthreads();
+  if (t < 256) {
+    int before = 0;
+    for (int i = 0; i < w; ++i) before += sh.warp[i];
+    const int above = before + incl - c, upto = before + incl;
+    if (above < k && k <= upto) {
+      *digit_out = 255 - t;
+      *k_out = k - above;
+      if (count_out) *count_out = upto;
+    }
+  }
   __syncthreads();
 }
 
@@ -291,19 +316,14 @@ __device__ void radix_select(KeyAt key_at, int m, int keep, SelShared& sh) {
   __syncthreads();
   for (int shift = 24; shift >= 0; shift -= 8) {
     const uint32_t prefix = sh.prefix, mask = sh.mask;
+    const int k = sh.k;
     digit_histogram(key_at, m, prefix, mask, shift, sh);
+    __shared__ int s_digit, s_k;
+    find_digit(sh, k, &s_digit, &s_k, nullptr);
     if (threadIdx.x == 0) {
-      int k = sh.k;
-      for (int dgt = 255; dgt >= 0; --dgt) {
-        const int c = (int)sh.hist[dgt];
-        if (c >= k) {
-          sh.prefix = prefix | ((uint32_t)dgt << shift);
-          sh.mask = mask | (255u << shift);
-          break;
-        }
-        k -= c;
-      }
-      sh.k = k;
+      sh.prefix = prefix | ((uint32_t)s_digit << shift);
+      sh.mask = mask | (255u << shift);
+      sh.k = s_k;
     }
     __syncthreads();
   }
@@ -388,19 +408,15 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
     auto global_pos = [](int i) { return i; };
     // pass 1: top-byte histogram and the candidate bucket
     digit_histogram(global_key, n, 0u, 0u, 24, sh);
-    if (threadIdx.x == 0) {
-      int cum = 0, top = 0;
-      for (int dgt = 255; dgt >= 0; --dgt) {
-        cum += (int)sh.hist[dgt];
-        if (cum >= keep) {
-          top = dgt;
-          break;
-        }
+    {
+      __shared__ int s_top, s_rest, s_cnt;
+      find_digit(sh, keep, &s_top, &s_rest, &s_cnt);
+      if (threadIdx.x == 0) {
+        sh.top = s_top;
+        sh.n_cand = s_cnt;
       }
-      sh.top = top;
-      sh.n_cand = cum;
+      __syncthreads();
     }
-    __syncthreads();
     const uint32_t lo_key = (uint32_t)sh.top << 24;
     const int m = sh.n_cand;
     if (m <= kSelCap) {
