@@ -380,7 +380,9 @@ def main():
     ap.add_argument("--kv-dtype", default=None, choices=["bf16", "fp8", "int8"],
                     help="run the workload with another KV storage type")
     ap.add_argument("--no-cascade", action="store_true",
-                    help="every sequence reads its own blocks (no shared-prefix pairing)")
+                    help="every sequence reads its own blocks (no shared-prefix decode)")
+    ap.add_argument("--cascade", type=int, default=1, choices=[0, 1, 2],
+                    help="shared-prefix decode: 0 off, 1 sequence pairs, 2 group prefixes (multi-query kernel)")
     ap.add_argument("--time-kernels", action="store_true",
                     help="bracket every kernel (not only decode) with events; adds gaps to the step")
     args = ap.parse_args()
@@ -408,7 +410,8 @@ def main():
     pkv.load()
 
     setup = Setup(wl, dev)
-    setup.cache.set_cascade(not args.no_cascade)
+    cascade = 0 if args.no_cascade else args.cascade
+    setup.cache.set_cascade(cascade)
     st = Stepper(setup, splits)
     stream = torch.cuda.current_stream(dev)
     for _ in range(max(3, args.warmup)):
@@ -427,7 +430,7 @@ def main():
     clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     time.sleep(0.3)
     # ---- device-resident timed region (kernel timing events on) ----
-    setup.cache.timing_enable(True if args.time_kernels else ["decode"])
+    setup.cache.timing_enable(True if args.time_kernels else ["decode", "prefix_decode"])
     setup.cache.timing_read()
     launches0 = setup.cache.launch_count()
     barrier(ws)
@@ -496,7 +499,10 @@ def main():
     ms_step = ms_max / args.steps
     value = whole_job_rate(ws, step_bytes, ms_step)
     peak, peak_kind = hbm_peak()
+    # decode time per step: the main decode kernel plus, with shared-prefix
+    # groups, the multi-query kernel that runs before it
     dec_ms, dec_n = ktimes["decode"]
+    dec_ms += ktimes["prefix_decode"][0]
     dec_avg = dec_ms / max(dec_n, 1)
     achieved = step_bytes / (dec_avg * 1e-3) / 1e9 if dec_n else None
     traffic = profiled_traffic("decode_tc.cu", label)
@@ -520,13 +526,14 @@ def main():
         "data": "synthetic (seeded N(0,1) K/V/Q; seeded uniform lengths)",
         "config": {"workload": label, "batch": len(setup.ids), "n_heads": wl.n_heads,
                    "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim, "kv_dtype": wl.kv_dtype,
-                   "mask": wl.mask, "num_splits": splits, "cascade": not args.no_cascade,
+                   "mask": wl.mask, "num_splits": splits, "cascade": cascade,
                    "context_tokens": sum(lens_step),
                    "kv_bytes_per_step": step_bytes, "l2": "KV pool larger than L2 (no flush needed)",
                    "parallelism": f"replicas x{ws}"},
         "tokens_per_s": round(ws * len(setup.ids) / (ms_step * 1e-3), 1),
         "frac_of_hbm_peak": round(value / ws / peak, 4),
-        "roofline": {"bound": "hbm", "kernel": "decode_tc_kernel", "achieved": round(achieved, 2) if achieved else None,
+        "roofline": {"bound": "hbm",
+                     "kernel": "decode_tc_kernel" + (" + prefix_decode_kernel" if ktimes["prefix_decode"][1] else ""), "achieved": round(achieved, 2) if achieved else None,
                      "peak": peak, "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s",
                      "frac": round(achieved / peak, 4) if achieved else None, "traffic": traffic,
                      "algorithmic_bytes_per_launch": step_bytes, "avg_launch_ms": round(dec_avg, 5)},

@@ -366,7 +366,8 @@ typedef enum {
   PKV_KERNEL_TABLE_PATCH = 6,
   PKV_KERNEL_SWAP_COPY = 7, /* CPU swap-out / swap-in block copies */
   PKV_KERNEL_COMPACT = 8,   /* H2O compaction: row gather and score compaction */
-  PKV_KERNEL_COUNT = 9
+  PKV_KERNEL_PREFIX = 9,    /* shared-prefix multi-query decode */
+  PKV_KERNEL_COUNT = 10
 } pkv_kernel_id;
 
 /* Bit k of kernel_mask (k a pkv_kernel_id) brackets every launch of kernel k
@@ -382,16 +383,22 @@ pkv_status pkv_timing_read(pkv_pool* pool, double* total_ms_out /* [PKV_KERNEL_C
  * PKV_ERR_TIMEOUT in the status word; the warp then drains its own copies in
  * flight (bounded again) and returns, leaving the context usable. */
 pkv_status pkv_set_wait_limit(pkv_pool* pool, int64_t wait_limit_ns);
-/* Shared-prefix (cascade) decode, on by default ([PA] prefix sharing: a
- * system prompt reused by many requests, parallel sampling).  In decode over
- * whole keep-sets (PKV_MASK_FULL, num_splits = 0) the planner sorts the
- * sequences by their block tables and pairs neighbours that share leading
- * full blocks; such a pair's shared blocks are read once, by one warp that
- * attends for both sequences, and each sequence's remainder is read alone.
- * The results are merged by log-sum-exp like any split.  Pairing is skipped
- * when it would save less than an eighth of the batch's block reads.
- * enable = 0 turns it off (every sequence reads its blocks itself). */
-pkv_status pkv_set_cascade(pkv_pool* pool, int32_t enable);
+/* Shared-prefix (cascade) decode ([PA] prefix sharing: a system prompt
+ * reused by many requests, parallel sampling).  In decode over whole
+ * keep-sets (PKV_MASK_FULL, num_splits = 0):
+ *   - mode 1 (default): the planner pairs sequences that share leading full
+ *     blocks; a pair's shared blocks are read once, by one warp attending
+ *     for both (skipped when it would save under an eighth of the batch's
+ *     block reads); each sequence's remaining blocks are read alone;
+ *   - mode 2 (BF16 pools): sequences whose first block is the same physical
+ *     block form groups (at least 4 sequences sharing at least 8 full
+ *     blocks); a group's common prefix is read once per CTA of a multi-query
+ *     kernel that attends for up to 128 query rows at once, and the rest of
+ *     every sequence is read alone (no pairs); without groups, mode 2 pairs
+ *     like mode 1;
+ *   - mode 0: every sequence reads its own blocks.
+ * All parts are merged by log-sum-exp like any split. */
+pkv_status pkv_set_cascade(pkv_pool* pool, int32_t mode);
 /* Test hook for the bound above: in the next decode on this pool, warp `warp`
  * of the grid arms its first stage without issuing the copies, so that wait
  * can only run out.  Outputs of that call are undefined; the status word

@@ -295,9 +295,11 @@ class PagedKVCache:
                                               int(acc_stride), sink_size, window_size, h2o_size, keep_idx.data_ptr(),
                                               int(keep_stride), keep_count.data_ptr()))
 
-    def set_cascade(self, enable: bool) -> None:
-        """Shared-prefix decode (pairs of sequences read shared blocks once)."""
-        _abi.check(self.lib.pkv_set_cascade(self._h, 1 if enable else 0))
+    def set_cascade(self, mode) -> None:
+        """Shared-prefix decode: 0 / False off, 1 / True sequence pairs (the
+        default), 2 group prefixes through the multi-query kernel."""
+        mode = 1 if mode is True else 0 if mode is False else int(mode)
+        _abi.check(self.lib.pkv_set_cascade(self._h, mode))
 
     def seq_compact(self, seq_ids, counts, keep_idx=None, keep_stride: int = 0, acc=None, acc_stride: int = 0,
                     stream=None) -> None:

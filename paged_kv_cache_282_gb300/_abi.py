@@ -20,7 +20,7 @@ STATUS_NAMES = {
 KV_DTYPES = {"fp32": 0, "bf16": 1, "fp8": 2, "fp8_e4m3": 2, "int8": 3}
 MASKS = {"full": 0, "sliding": 1, "sink_window": 2}
 KERNELS = ["cow_copy", "append", "decode", "combine", "h2o_score", "h2o_select", "table_patch", "swap_copy",
-           "compact"]
+           "compact", "prefix_decode"]
 
 
 class PKVError(RuntimeError):

@@ -47,6 +47,18 @@ struct CombineItem {
   int32_t q_row, kv_head, first_partial, n_partials;
 };
 
+// Shared-prefix group work for the multi-query kernel: the logical blocks
+// [lblk_begin, lblk_end) of kv head kv_head, which every member sequence
+// holds as the same physical blocks (read through table_seq's table row),
+// attended by all members' query heads at once.  Each member writes one
+// partial record per item.
+struct PrefixItem {
+  int32_t kv_head, table_seq, lblk_begin, lblk_end, member_begin, n_members, pad0, pad1;
+};
+struct PrefixMember {
+  int32_t q_row, out_index, item, pad;  // item: the merge item of (q_row, kv_head)
+};
+
 // A (sequence, kv head) with an empty keep-set: out = 0, lse = -inf.
 struct EmptyItem {
   int32_t q_row, kv_head;
@@ -100,6 +112,9 @@ struct DecodeTCParams {
   int32_t* status;
   uint64_t wait_limit_ns;  // bound of every mbarrier wait
   int32_t starve_warp;     // >= 0: that warp arms its first stage but issues no copy (wait-expiry test)
+  const PrefixItem* prefix_items;  // the multi-query kernel's work (one CTA each)
+  const PrefixMember* prefix_members;
+  int32_t n_prefix_items;
 };
 
 struct DecodeF32Params {
@@ -127,6 +142,11 @@ struct DecodeF32Params {
 // Returns the launch error.
 cudaError_t launch_decode_tc(int kv_dtype, int G, int nq, const DecodeTCParams& p, int grid_ctas,
                              cudaStream_t stream);
+// Shared-prefix multi-query kernel (bf16 KV): one CTA per PrefixItem.
+cudaError_t launch_prefix_decode(int G, const DecodeTCParams& p, cudaStream_t stream);
+cudaError_t prefix_decode_prepare(int G);
+constexpr int kPrefixRowsPerCta = 128;  // 8 warps x 16 query rows
+
 // Decode kernel geometry: warps per CTA and dynamic shared memory bytes.
 int decode_tc_warps_per_cta(int kv_dtype, int nq);
 size_t decode_tc_smem_bytes(int kv_dtype, int nq);

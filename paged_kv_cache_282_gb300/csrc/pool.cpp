@@ -336,7 +336,7 @@ struct pkv_pool {
   int device_id = 0, num_sms = 0;
   int tc_warps_per_cta = 0, tc_ctas_per_sm = 0;    // one sequence per warp
   int tc2_warps_per_cta = 0, tc2_ctas_per_sm = 0;  // up to two sequences over shared blocks
-  bool cascade = true;                              // read shared prefixes once per sequence pair
+  int cascade = 1;  // 0: off; 1: sequence pairs; 2: group prefixes (multi-query kernel)
   size_t tc_smem = 0;
   CUtensorMap tmap_k{}, tmap_v{};
   bool tc_path = false;
@@ -548,6 +548,8 @@ struct Plan {
   int ctas = 0;
   int n_partials = 0;
   int nq = 1;  // 2: pieces may carry a second sequence (the two-sequence kernel)
+  std::vector<PrefixItem> prefix_items;  // the multi-query kernel's work (group prefixes)
+  std::vector<PrefixMember> prefix_members;
 };
 
 struct Seg {
@@ -592,32 +594,94 @@ size_t max_pieces(const pkv_pool* p, int32_t n_seqs, int32_t num_splits) {
   const size_t nbg = (size_t)n_seqs * p->cfg.n_kv_heads;
   const size_t a = 2 * nbg + (size_t)max_total_warps(p) + 1;
   const size_t b = nbg * (size_t)std::max(1, num_splits) + nbg + 1;
-  // shared-prefix plans: 3 segments per sequence pair and kv head, and a
-  // record for each sequence of a run
-  const size_t c = 2 * (2 * nbg + (size_t)max_total_warps(p, 2)) + 2;
+  // shared-prefix plans: 3 segments per sequence pair and kv head, a record
+  // for each sequence of a run, and up to kMaxPrefixSplit group-prefix records
+  const size_t c = 2 * (2 * nbg + (size_t)max_total_warps(p, 2)) + 4 * nbg + 2;
   return std::max(std::max(a, b), c);
 }
 
-// Shared-prefix pairing for decode over whole keep-sets.  Blocks are shared
+// Shared-prefix planning for decode over whole keep-sets.  Blocks are shared
 // only through forks and replaced only at the tail (append, copy-on-write,
 // truncate) or all at once (compaction), so two sequences that hold the same
-// physical block at logical index k share every block before it as well.
-// Pairs are formed first among sequences whose last full blocks coincide
-// (they share every full block), then among the rest that share their first
-// block; the shared length is then measured entry by entry.  Returns
-// (b0, b1, shared blocks) triples, or nothing when the pairs would save less
-// than an eighth of the batch's block reads.
+// physical block at logical index k share every block before it as well:
+// sharing is a prefix of the tables.
+
+// Leading full blocks that rows x and y share, among the first lim: the last
+// equal entry by bisection, checked by memcmp (a mismatch inside the found
+// prefix, never expected, falls back to the exact scan).
+int32_t shared_blocks(const int32_t* x, const int32_t* y, int32_t from, int32_t lim) {
+  if (lim <= from) return from;
+  int32_t c = from, hi = lim;
+  if (x[lim - 1] == y[lim - 1]) {
+    c = lim;
+  } else {
+    while (c < hi) {  // entries below c equal; entry hi - 1 differs (or hi = lim)
+      const int32_t mid = (c + hi) / 2;
+      if (x[mid] == y[mid]) c = mid + 1; else hi = mid;
+    }
+  }
+  if (c > 0 && (memcmp(x, y, (size_t)c * sizeof(int32_t)) != 0 || x[0] < 0))
+    c = (int32_t)(std::mismatch(x, x + c, y).first - x);
+  return c;
+}
+
+// Groups of at least kMinGroupMembers sequences sharing their first
+// kMinGroupBlocks (or more) full blocks: the group's common prefix is read
+// once per CTA by the multi-query kernel (BF16 pools).
+constexpr int kMinGroupMembers = 4, kMinGroupBlocks = 8;
+constexpr int kMaxPrefixSplit = 4;  // records per (sequence, kv head) from its group prefix
+
+struct PrefixGroup {
+  std::vector<int32_t> members;  // batch indices, ascending
+  int32_t shared;                // common full blocks
+};
+
+std::vector<PrefixGroup> find_prefix_groups(const pkv_pool* p, int32_t n, const int32_t* ids) {
+  std::vector<PrefixGroup> groups;
+  if (p->cfg.kv_dtype != PKV_KV_BF16) return groups;
+  const auto& A = p->alloc;
+  auto full = [&](int32_t b) { return A.len[ids[b]] / kBlock; };
+  auto row = [&](int32_t b) { return A.table[ids[b]].data(); };
+  std::vector<std::pair<int32_t, int32_t>> keyed;  // (first block, batch index)
+  for (int32_t b = 0; b < n; ++b)
+    if (full(b) >= kMinGroupBlocks && row(b)[0] >= 0) keyed.push_back({row(b)[0], b});
+  std::sort(keyed.begin(), keyed.end());
+  for (size_t i = 0; i < keyed.size();) {
+    size_t j = i;
+    while (j < keyed.size() && keyed[j].first == keyed[i].first) ++j;
+    if (j - i >= (size_t)kMinGroupMembers) {
+      PrefixGroup gr;
+      const int32_t x = keyed[i].second;
+      int32_t c = full(x);
+      for (size_t k = i; k < j; ++k) {
+        gr.members.push_back(keyed[k].second);
+        if (k > i) c = std::min(c, shared_blocks(row(x), row(keyed[k].second), 0, std::min(c, full(keyed[k].second))));
+      }
+      gr.shared = c;
+      if (c >= kMinGroupBlocks) groups.push_back(std::move(gr));
+    }
+    i = j;
+  }
+  return groups;
+}
+
+// Pairs of sequences that share blocks past their group prefix (base[b]
+// blocks, 0 outside groups): first those whose last full blocks coincide
+// (they share every full block), then those with the same first block past
+// the base.  Pairs form only between sequences with the same base.  Returns
+// (b0, b1, shared blocks) triples (shared counted from block 0).
 struct Pairing {
   int32_t b0, b1, shared;
 };
 
-std::vector<Pairing> pair_shared_prefixes(const pkv_pool* p, int32_t n, const int32_t* ids) {
+std::vector<Pairing> pair_shared_prefixes(const pkv_pool* p, int32_t n, const int32_t* ids,
+                                          const std::vector<int32_t>& base) {
   const auto& A = p->alloc;
   auto full = [&](int32_t b) { return A.len[ids[b]] / kBlock; };
   auto row = [&](int32_t b) { return A.table[ids[b]].data(); };
   std::vector<Pairing> pairs;
   std::vector<uint8_t> used(n, 0);
-  std::vector<std::pair<int64_t, int32_t>> keyed;
+  std::vector<std::pair<std::pair<int64_t, int32_t>, int32_t>> keyed;  // ((key, base), b)
   keyed.reserve(n);
   auto pair_adjacent = [&]() {
     std::sort(keyed.begin(), keyed.end());
@@ -627,22 +691,8 @@ std::vector<Pairing> pair_shared_prefixes(const pkv_pool* p, int32_t n, const in
         continue;
       }
       const int32_t x = keyed[i].second, y = keyed[i + 1].second;
-      const int32_t lim = std::min(full(x), full(y));
-      // shared blocks form a prefix: the last equal entry, by bisection
-      int32_t c = 0, hi = lim;
-      if (lim > 0 && row(x)[lim - 1] == row(y)[lim - 1]) {
-        c = lim;
-      } else {
-        while (c < hi) {  // invariant: entries below c equal, entry hi - 1 differs (or hi = lim)
-          const int32_t mid = (c + hi) / 2;
-          if (row(x)[mid] == row(y)[mid]) c = mid + 1; else hi = mid;
-        }
-      }
-      // the prefix property is what the tables guarantee; a mismatch inside
-      // the found prefix (never expected) falls back to the exact scan
-      if (c > 0 && memcmp(row(x), row(y), (size_t)c * sizeof(int32_t)) != 0)
-        c = (int32_t)(std::mismatch(row(x), row(x) + c, row(y)).first - row(x));
-      if (c > 0) {
+      const int32_t c = shared_blocks(row(x), row(y), 0, std::min(full(x), full(y)));
+      if (c > base[x]) {
         pairs.push_back({std::min(x, y), std::max(x, y), c});
         used[x] = used[y] = 1;
         i += 2;
@@ -651,19 +701,14 @@ std::vector<Pairing> pair_shared_prefixes(const pkv_pool* p, int32_t n, const in
       }
     }
   };
-  // (full-block count, last full block): identical full blocks
   for (int32_t b = 0; b < n; ++b)
-    if (full(b) > 0 && row(b)[full(b) - 1] >= 0) keyed.push_back({((int64_t)full(b) << 32) | row(b)[full(b) - 1], b});
+    if (full(b) > base[b] && row(b)[full(b) - 1] >= 0)
+      keyed.push_back({{((int64_t)full(b) << 32) | row(b)[full(b) - 1], base[b]}, b});
   pair_adjacent();
-  // the rest: a common first block
   keyed.clear();
   for (int32_t b = 0; b < n; ++b)
-    if (!used[b] && full(b) > 0 && row(b)[0] >= 0) keyed.push_back({row(b)[0], b});
+    if (!used[b] && full(b) > base[b] && row(b)[base[b]] >= 0) keyed.push_back({{row(b)[base[b]], base[b]}, b});
   pair_adjacent();
-  int64_t saved = 0, total = 0;
-  for (int32_t b = 0; b < n; ++b) total += ceil_div(A.len[ids[b]], kBlock);
-  for (const auto& pr : pairs) saved += pr.shared;
-  if (saved * 8 < total) pairs.clear();
   return pairs;
 }
 
@@ -680,12 +725,32 @@ Plan& build_plan(pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, in
   segs.clear();
   std::vector<int64_t>& bg_units = cache.bg_units;
   bg_units.assign((size_t)n * Hk, 0);
-  // whole keep-sets (no mask), automatic partition: shared prefixes are read
-  // once per sequence pair by the two-sequence kernel
+  // whole keep-sets (no mask), automatic partition: a prefix shared by a
+  // group is read once per CTA of the multi-query kernel; blocks shared by a
+  // pair past that are read once by the two-sequence kernel
   std::vector<Pairing> pairs;
-  if (p->cascade && mode == 0 && num_splits <= 0 && n >= 2) pairs = pair_shared_prefixes(p, n, ids);
+  std::vector<PrefixGroup> groups;
+  std::vector<int32_t> base(n, 0);
+  plan.prefix_items.clear();
+  plan.prefix_members.clear();
+  if (p->cascade && mode == 0 && num_splits <= 0 && n >= 2) {
+    if (p->cascade >= 2) groups = find_prefix_groups(p, n, ids);
+    for (const auto& gr : groups)
+      for (int32_t b : gr.members) base[b] = gr.shared;
+    // Pairs only where no group prefix was taken out: past a group prefix the
+    // blocks a pair shares come from DRAM, where the two-sequence kernel
+    // (8 warps per SM) is slower than two one-sequence reads, the second of
+    // which hits L2.
+    if (groups.empty()) pairs = pair_shared_prefixes(p, n, ids, base);
+    // pairing alone must save an eighth of the block reads to be worth the
+    // two-sequence kernel's lower occupancy
+    int64_t saved = 0, total = 0;
+    for (int32_t b = 0; b < n; ++b) total += ceil_div(A.len[ids[b]], kBlock);
+    for (const auto& pr : pairs) saved += pr.shared - base[pr.b0];
+    if (saved * 8 < total) pairs.clear();
+  }
   plan.nq = pairs.empty() ? 1 : 2;
-  if (!pairs.empty()) {
+  if (!pairs.empty() || !groups.empty()) {
     // each pair's shared segment is followed by the two remainders, so the
     // short remainder runs (and the merges they end with) spread over all
     // warps instead of piling up at the end of the unit list
@@ -694,15 +759,43 @@ Plan& build_plan(pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, in
     for (const auto& pr : pairs) {
       paired[pr.b0] = paired[pr.b1] = 1;
       for (int g = 0; g < Hk; ++g) {
-        segs.push_back({pr.b0, g, 0, pr.shared, pr.b1});
+        segs.push_back({pr.b0, g, base[pr.b0], pr.shared, pr.b1});
         if (pr.shared < nblk(pr.b0)) segs.push_back({pr.b0, g, pr.shared, nblk(pr.b0), -1});
         if (pr.shared < nblk(pr.b1)) segs.push_back({pr.b1, g, pr.shared, nblk(pr.b1), -1});
       }
     }
     for (int32_t b = 0; b < n; ++b) {
       for (int g = 0; g < Hk; ++g) {
-        if (!paired[b] && nblk(b) > 0) segs.push_back({b, g, 0, nblk(b), -1});
+        if (!paired[b] && nblk(b) > base[b]) segs.push_back({b, g, base[b], nblk(b), -1});
         bg_units[(size_t)b * Hk + g] = nblk(b);
+      }
+    }
+    // multi-query items: per group, kv head and tile of up to 128 query rows,
+    // the prefix cut into `split` block ranges so the grid covers the GPU
+    if (!groups.empty()) {
+      const int G = p->G, per_tile = kPrefixRowsPerCta / G;
+      int64_t tiles = 0;
+      for (const auto& gr : groups) tiles += (int64_t)Hk * ceil_div((int32_t)gr.members.size(), per_tile);
+      const int64_t want = 2LL * std::max(1, p->num_sms);
+      for (const auto& gr : groups) {
+        const int32_t split = (int32_t)std::max<int64_t>(
+            1, std::min<int64_t>({(want + tiles - 1) / tiles, (int64_t)kMaxPrefixSplit,
+                                  (int64_t)(gr.shared / kMinGroupBlocks)}));
+        const int32_t M = (int32_t)gr.members.size();
+        for (int g = 0; g < Hk; ++g)
+          for (int32_t t0 = 0; t0 < M; t0 += per_tile)
+            for (int32_t k = 0; k < split; ++k) {
+              PrefixItem it{};
+              it.kv_head = g;
+              it.table_seq = ids[gr.members[0]];
+              it.lblk_begin = (int32_t)((int64_t)gr.shared * k / split);
+              it.lblk_end = (int32_t)((int64_t)gr.shared * (k + 1) / split);
+              it.member_begin = (int32_t)plan.prefix_members.size();
+              it.n_members = std::min(per_tile, M - t0);
+              for (int32_t m = 0; m < it.n_members; ++m)
+                plan.prefix_members.push_back({gr.members[t0 + m], -1, g, 0});  // item field: kv head for now
+              plan.prefix_items.push_back(it);
+            }
       }
     }
   } else {
@@ -856,6 +949,7 @@ Plan& build_plan(pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, in
       units = 0;
     }
   }
+  for (const PrefixMember& pm : plan.prefix_members) ++n_part[(size_t)pm.q_row * Hk + pm.item];
   int next_partial = 0;
   for (size_t bg = 0; bg < (size_t)n * Hk; ++bg)
     if (n_part[bg] > 0) {
@@ -877,6 +971,11 @@ Plan& build_plan(pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, in
     }
   std::vector<int32_t>& cursor = cache.cursor;
   cursor = first_partial;
+  for (PrefixMember& pm : plan.prefix_members) {
+    const size_t bg = (size_t)pm.q_row * Hk + pm.item;
+    pm.out_index = cursor[bg]++;
+    pm.item = item_of[bg];
+  }
   for (const PlanRun& ru : runs) {
     const Piece& pc = plan.pieces[ru.end - 1];
     const size_t bg0 = (size_t)pc.q_row * Hk + pc.kv_head;
@@ -949,7 +1048,7 @@ pkv_status check_keep_blocks_present(const pkv_pool* p, int32_t n, const int32_t
 // Byte layout of an uploaded decode plan: [warp_begin][pieces][merge items]
 // [merge counters, zero][empty items], each part 32-byte aligned.
 struct PlanLayout {
-  size_t wb = 0, pieces = 0, combine = 0, counters = 0, empty = 0, bytes = 0;
+  size_t wb = 0, pieces = 0, combine = 0, counters = 0, empty = 0, pitems = 0, pmembers = 0, bytes = 0;
 };
 
 PlanLayout plan_layout(Plan& pl, int wpc, size_t base) {
@@ -965,7 +1064,9 @@ PlanLayout plan_layout(Plan& pl, int wpc, size_t base) {
   L.combine = up(L.pieces + pl.pieces.size() * sizeof(Piece));
   L.counters = up(L.combine + pl.combine.size() * sizeof(CombineItem));
   L.empty = up(L.counters + pl.combine.size() * sizeof(int32_t));
-  L.bytes = L.empty + pl.empty.size() * sizeof(EmptyItem);
+  L.pitems = up(L.empty + pl.empty.size() * sizeof(EmptyItem));
+  L.pmembers = up(L.pitems + pl.prefix_items.size() * sizeof(PrefixItem));
+  L.bytes = L.pmembers + pl.prefix_members.size() * sizeof(PrefixMember);
   return L;
 }
 
@@ -977,13 +1078,17 @@ void plan_write(const Plan& pl, const PlanLayout& L, char* host) {
     memset(host + L.counters, 0, pl.combine.size() * sizeof(int32_t));
   }
   if (!pl.empty.empty()) memcpy(host + L.empty, pl.empty.data(), pl.empty.size() * sizeof(EmptyItem));
+  if (!pl.prefix_items.empty()) {
+    memcpy(host + L.pitems, pl.prefix_items.data(), pl.prefix_items.size() * sizeof(PrefixItem));
+    memcpy(host + L.pmembers, pl.prefix_members.data(), pl.prefix_members.size() * sizeof(PrefixMember));
+  }
 }
 
 // Launches the tensor-core decode (with its fused merge) over an uploaded plan.
 pkv_status launch_tc_plan(pkv_pool* p, cudaStream_t st, const Plan& pl, const PlanLayout& L, const char* dev,
                           const void* q, float scale, int mode, int S, int W, void* out, float* lse, float* logits,
                           int64_t logits_stride, void* partials) {
-  if (pl.total_warps == 0) return PKV_OK;
+  if (pl.total_warps == 0 && pl.prefix_items.empty()) return PKV_OK;
   const auto& c = p->cfg;
   DecodeTCParams prm;
   prm.tmap_k = p->tmap_k;
@@ -1016,6 +1121,12 @@ pkv_status launch_tc_plan(pkv_pool* p, cudaStream_t st, const Plan& pl, const Pl
   prm.wait_limit_ns = p->wait_limit_ns;
   prm.starve_warp = p->starve_warp;
   p->starve_warp = -1;
+  prm.prefix_items = (const PrefixItem*)(dev + L.pitems);
+  prm.prefix_members = (const PrefixMember*)(dev + L.pmembers);
+  prm.n_prefix_items = (int32_t)pl.prefix_items.size();
+  if (prm.n_prefix_items > 0)
+    if (pkv_status r = launch(p, PKV_KERNEL_PREFIX, st, [&] { return launch_prefix_decode(p->G, prm, st); })) return r;
+  if (pl.total_warps == 0) return PKV_OK;
   return launch(p, PKV_KERNEL_DECODE, st,
                 [&] { return launch_decode_tc(c.kv_dtype, p->G, pl.nq, prm, pl.ctas, st); });
 }
@@ -1302,6 +1413,7 @@ pkv_status pkv_pool_create(const pkv_pool_config* cfg, const pkv_pool_buffers* b
       if (pkv_status r = make_tensor_map(&p->tmap_v, b.v_pool, p->cfg)) return fail_dev(r);
       e = decode_tc_prepare(cfg->kv_dtype, p->G, 1);
       if (e == cudaSuccess) e = decode_tc_prepare(cfg->kv_dtype, p->G, 2);
+      if (e == cudaSuccess && cfg->kv_dtype == PKV_KV_BF16) e = prefix_decode_prepare(p->G);
       int occ = 0, occ2 = 0;
       if (e == cudaSuccess) e = decode_tc_occupancy(cfg->kv_dtype, p->G, 1, &occ);
       if (e == cudaSuccess) e = decode_tc_occupancy(cfg->kv_dtype, p->G, 2, &occ2);
@@ -1959,9 +2071,10 @@ pkv_status pkv_set_wait_limit(pkv_pool* p, int64_t wait_limit_ns) {
   return PKV_OK;
 }
 
-pkv_status pkv_set_cascade(pkv_pool* p, int32_t enable) {
+pkv_status pkv_set_cascade(pkv_pool* p, int32_t mode) {
   if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
-  p->cascade = enable != 0;
+  if (mode < 0 || mode > 2) return fail(PKV_ERR_INVALID_ARG, "cascade mode %d not in {0, 1, 2}", mode);
+  p->cascade = mode;
   return PKV_OK;
 }
 

@@ -53,7 +53,7 @@ def _shared_batch(kv: str, n_heads: int, seed: int):
     return wl, tw, sorted(ids)
 
 
-def _decode_both(tw, wl, ids, cascade: bool, static: bool = False, logits: bool = False):
+def _decode_both(tw, wl, ids, cascade, static: bool = False, logits: bool = False):
     tw.cache.set_cascade(cascade)
     q = workloads.queries(wl, n=len(ids), step=2)
     stride = max(tw.alloc.length(s) for s in ids)
@@ -77,17 +77,40 @@ def _decode_both(tw, wl, ids, cascade: bool, static: bool = False, logits: bool 
 @pytest.mark.parametrize("kv", ["bf16", "fp8", "int8"])
 @pytest.mark.parametrize("n_heads", [64, 32, 16, 8])
 def test_cascade_matches_oracle(kv, n_heads):
+    """Mode 2: group prefixes (BF16) and pairs; mode 1: pairs only; 0: off."""
     wl, tw, ids = _shared_batch(kv, n_heads, seed=90 + n_heads)
-    on = _decode_both(tw, wl, ids, cascade=True)
-    off = _decode_both(tw, wl, ids, cascade=False)
-    assert max_err(on, off.float().cpu().numpy()) <= 2 * TOL[kv]
+    groups = _decode_both(tw, wl, ids, cascade=2)
+    pairs = _decode_both(tw, wl, ids, cascade=1)
+    off = _decode_both(tw, wl, ids, cascade=0)
+    for x in (groups, pairs):
+        assert max_err(x, off.float().cpu().numpy()) <= 2 * TOL[kv]
 
 
-def test_cascade_logits_and_static_entry():
-    wl, tw, ids = _shared_batch("bf16", 64, seed=97)
-    _decode_both(tw, wl, ids, cascade=True, logits=True)
-    _decode_both(tw, wl, ids, cascade=True, static=True)
-    tw.cache.set_cascade(True)
+@pytest.mark.parametrize("n_heads", [64, 32])
+def test_cascade_logits_and_static_entry(n_heads):
+    wl, tw, ids = _shared_batch("bf16", n_heads, seed=97)
+    _decode_both(tw, wl, ids, cascade=2, logits=True)
+    _decode_both(tw, wl, ids, cascade=2, static=True)
+    _decode_both(tw, wl, ids, cascade=1, logits=True)
+
+
+@pytest.mark.parametrize("n_heads", [64, 32, 16, 8])
+def test_group_prefix_only(n_heads):
+    """Forty sequences that are the same 700-token prefix plus one private
+    token each: the group prefix (43 full blocks) is the multi-query kernel's
+    whole work but for one block per sequence; 40 x G rows span several row
+    tiles for small G."""
+    wl = workloads.small("bf16", lens=(1,), n_heads=n_heads, seed=99)
+    tw = Twin(wl, 600, 48, 60, seed=5)
+    base = tw.add()
+    k, v = workloads.kv_rows(wl, 0, 0, 700)
+    tw.append([base], k[None], v[None])
+    ids = [tw.fork(base) for _ in range(40)]
+    tw.free(base)
+    k, v = workloads.new_tokens(wl, len(ids), 6)
+    tw.append(ids, k, v)
+    _decode_both(tw, wl, ids, cascade=2)
+    _decode_both(tw, wl, ids, cascade=2, logits=True)
 
 
 def test_cascade_identical_forks_share_everything():

@@ -103,7 +103,10 @@ def test_prefix_sharing_append_cow():
     for s in ids:
         assert np.array_equal(tw.cache.block_table(s), tw.alloc.table(s))
     pool_bytes_equal(tw, ids, every=9)
-    _decode_and_compare(tw, ids, wl, splits=0)
+    for mode in (1, 2, 0):  # sequence pairs, group prefixes (multi-query kernel), off
+        tw.cache.set_cascade(mode)
+        _decode_and_compare(tw, ids, wl, splits=0)
+    tw.cache.set_cascade(1)
 
 
 def test_prefix_sharing_literal_shapes_never_copy():
