@@ -235,6 +235,7 @@ __device__ int block_excl_scan(int v, int* excl, int* s_warp) {
 
 constexpr int kSelUnroll = 16;     // keys per thread per sweep (independent loads)
 constexpr int kSelCap = 16384;      // shared-memory candidates of the two-pass path
+constexpr int kSelSample = 4096;    // keys sampled to pick the one-pass threshold (<= kSelCap)
 
 struct SelShared {
   uint32_t hist[256];
@@ -403,7 +404,76 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
   }
   for (int j = threadIdx.x; j < lo; j += blockDim.x) out[j] = j;
   int n_heavy = 0;
-  if (keep > 0) {
+  // Gathers, in position order, the keys of [0, n) at or above thr into the
+  // shared candidate arrays (at most kSelCap written); returns how many keys
+  // qualified.  Each thread takes kSelUnroll consecutive positions a sweep
+  // (float4 loads when the row is 16-byte aligned).
+  auto gather = [&](uint32_t thr) {
+    const bool vec = ((reinterpret_cast<uintptr_t>(a)) & 15) == 0;
+    int filled = 0;
+    for (int base = 0; base < n; base += kSelUnroll * kSelThreads) {
+      const int j0 = base + kSelUnroll * threadIdx.x;
+      uint32_t key[kSelUnroll];
+      if (vec && j0 + kSelUnroll <= n) {
+#pragma unroll
+        for (int v = 0; v < kSelUnroll / 4; ++v) {
+          const float4 x = reinterpret_cast<const float4*>(a + j0)[v];
+          key[4 * v] = order_key(x.x);
+          key[4 * v + 1] = order_key(x.y);
+          key[4 * v + 2] = order_key(x.z);
+          key[4 * v + 3] = order_key(x.w);
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < kSelUnroll; ++u) key[u] = j0 + u < n ? order_key(a[j0 + u]) : 0u;
+      }
+      int c = 0;
+#pragma unroll
+      for (int u = 0; u < kSelUnroll; ++u) c += (j0 + u < n && key[u] >= thr);
+      int excl;
+      const int tot = block_excl_scan(c, &excl, sh.warp);
+      int w = filled + excl;
+#pragma unroll
+      for (int u = 0; u < kSelUnroll; ++u)
+        if (j0 + u < n && key[u] >= thr) {
+          if (w < kSelCap) {
+            c_key[w] = key[u];
+            c_pos[w] = j0 + u;
+          }
+          ++w;
+        }
+      filled += tot;
+    }
+    __syncthreads();
+    return filled;
+  };
+  auto smem_key = [c_key](int i) { return c_key[i]; };
+  auto smem_pos = [c_pos](int i) { return c_pos[i]; };
+  bool done = false;
+  if (keep > 0 && n > 4 * kSelSample) {
+    // Long rows: a strided sample of kSelSample keys gives a threshold a bit
+    // below the expected keep-th largest; one pass gathers every key at or
+    // above it.  When at least keep (and at most kSelCap) keys qualify, the
+    // keep-th largest is among them and the exact select runs on them alone;
+    // otherwise the two-pass path below runs.
+    for (int i = threadIdx.x; i < kSelSample; i += blockDim.x)
+      c_key[i] = order_key(a[(int)((int64_t)i * n / kSelSample)]);
+    __syncthreads();
+    const int64_t want = ((int64_t)keep * kSelSample + n - 1) / n * 5 / 4 + 8;
+    const int r = want < kSelSample ? (int)want : kSelSample;
+    radix_select(smem_key, kSelSample, r, sh);
+    const uint32_t thr = sh.prefix;
+    __syncthreads();
+    const int m = gather(thr);
+    if (m >= keep && m <= kSelCap) {
+      radix_select(smem_key, m, keep, sh);
+      const uint32_t T = sh.prefix;
+      const int need_eq = sh.k;
+      n_heavy = ordered_emit(smem_key, smem_pos, m, T, need_eq, lo, hi, out + lo, sh);
+      done = true;
+    }
+  }
+  if (keep > 0 && !done) {
     auto global_key = [a](int i) { return order_key(a[i]); };
     auto global_pos = [](int i) { return i; };
     // pass 1: top-byte histogram and the candidate bucket
@@ -421,31 +491,7 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
     const int m = sh.n_cand;
     if (m <= kSelCap) {
       // pass 2: gather the candidates in position order
-      int filled = 0;
-      for (int base = 0; base < n; base += kSelUnroll * kSelThreads) {
-        const int j0 = base + kSelUnroll * threadIdx.x;
-        uint32_t key[kSelUnroll];
-        int c = 0;
-#pragma unroll
-        for (int u = 0; u < kSelUnroll; ++u) {
-          key[u] = j0 + u < n ? order_key(a[j0 + u]) : 0u;
-          c += (j0 + u < n && key[u] >= lo_key);
-        }
-        int excl;
-        const int tot = block_excl_scan(c, &excl, sh.warp);
-        int w = filled + excl;
-#pragma unroll
-        for (int u = 0; u < kSelUnroll; ++u)
-          if (j0 + u < n && key[u] >= lo_key) {
-            c_key[w] = key[u];
-            c_pos[w] = j0 + u;
-            ++w;
-          }
-        filled += tot;
-      }
-      __syncthreads();
-      auto smem_key = [c_key](int i) { return c_key[i]; };
-      auto smem_pos = [c_pos](int i) { return c_pos[i]; };
+      gather(lo_key);
       radix_select(smem_key, m, keep, sh);
       const uint32_t T = sh.prefix;
       const int need_eq = sh.k;
