@@ -399,7 +399,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        return run_reference(args, wl)
+        return run_reference(args, wl, label)
 
     if ws > 1:
         import torch.distributed as dist
@@ -550,7 +550,7 @@ def main():
     print(json.dumps(line))
 
 
-def run_reference(args, wl):
+def run_reference(args, wl, label):
     """The CPU oracle as it stands, timed on this machine's cores, each step a
     bounded sample of the workload."""
     n = min(args.cpu_sample, wl.batch)

@@ -175,6 +175,8 @@ __global__ void h2o_score_kernel(const SeqRow* __restrict__ rows, int n_heads, i
   const int G = n_heads / n_kv_heads;
   float sum = 0.0f;
   if ((G & 3) == 0 && ((reinterpret_cast<uintptr_t>(logits) | (uintptr_t)(stride * G * 4)) & 15) == 0) {
+    // the kv heads' loads are independent: unrolled, they are all in flight at once
+#pragma unroll 8
     for (int g = 0; g < n_kv_heads; ++g) {
       const float4* lg = reinterpret_cast<const float4*>(logits + (((size_t)b * n_kv_heads + g) * stride + j) * G);
       for (int i = 0; i < G / 4; ++i) {
@@ -184,6 +186,7 @@ __global__ void h2o_score_kernel(const SeqRow* __restrict__ rows, int n_heads, i
       }
     }
   } else {
+#pragma unroll 8
     for (int g = 0; g < n_kv_heads; ++g) {
       const float* lg = logits + (((size_t)b * n_kv_heads + g) * stride + j) * G;
       for (int i = 0; i < G; ++i) sum += __expf(lg[i] - s_lse[g * G + i]);
