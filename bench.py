@@ -186,7 +186,10 @@ class Stepper:
         wl, dev = setup.wl, setup.dev
         self.s, self.wl, self.dev = setup, wl, dev
         self.cache = setup.cache
-        self.ids = setup.ids
+        # int32 arrays once, so the per-step calls marshal nothing
+        self.ids = np.asarray(setup.ids, dtype=np.int32)
+        self.lens = np.asarray(setup.lens, dtype=np.int32)
+        self.lens1 = self.lens + 1
         n = len(self.ids)
         self.num_splits = num_splits
         self.q = workloads.queries(wl, n).to(dev)
@@ -213,12 +216,11 @@ class Stepper:
                      logits_stride=self.stride, workspace=self.ws)
             c.h2o_scores(self.ids, self.logits, self.stride, self.lse, self.acc, self.stride, mask=wl.mask,
                          num_sinks=wl.num_sinks, window=wl.window)
-            lens = [L + 1 for L in self.s.lens]
-            c.h2o_select(lens, self.acc, self.stride, wl.budget, wl.recent, self.keep, wl.budget, self.keep_n)
+            c.h2o_select(self.lens1, self.acc, self.stride, wl.budget, wl.recent, self.keep, wl.budget, self.keep_n)
         else:
             c.decode(self.ids, self.q if q is None else q, scale=wl.scale, mask=wl.mask, num_sinks=wl.num_sinks,
                      window=wl.window, num_splits=self.num_splits, out=o, lse=self.lse, workspace=self.ws)
-        c.seq_truncate_many(self.ids, self.s.lens)  # roll the appended token back (host only)
+        c.seq_truncate_many(self.ids, self.lens)  # roll the appended token back (host only)
 
 
 # --------------------------------------------------------------------------

@@ -27,9 +27,9 @@
 //    with fp32 accumulation.  The path is HBM-bound (4 flop/byte for BF16,
 //    G = 4); the MMAs only keep instruction issue far below the memory time.
 //  - FP8 / INT8: codes are widened to fp16 in registers (exact); the per-token K
-//    scale multiplies the logit, and the per-token V scale is folded into the
-//    softmax weight through the exponent (b_j = a_j + log2 vs_j), so the fp16
-//    weights never exceed 1 and the running max stays consistent.
+//    scale multiplies the logit, and the per-token V scale multiplies the
+//    softmax weight before it is rounded to fp16 (the running max and the sum
+//    l are those of the unscaled weights).
 //  - Every wait is bounded: after about 4 s the warp sets the status word,
 //    drains its own copies in flight (bounded again) and returns.
 
@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(TC<KV, NQ>::kWarps * 32, 1)
       for (int t = 0; t < NQ; ++t)
 #pragma unroll
         for (int e = 0; e < 4; ++e) sa[t][e] = sb[t][e] = 0.f;
-      float ks_r = 1.f, ks_r8 = 1.f, lv_r = 0.f, lv_r8 = 0.f;
+      float ks_r = 1.f, ks_r8 = 1.f, vs_r = 1.f, vs_r8 = 1.f;
       if (KV == 1) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -550,8 +550,8 @@ __global__ void __launch_bounds__(TC<KV, NQ>::kWarps * 32, 1)
         const uint32_t sc = scl + (uint32_t)(st * C::kScaleBytes);
         ks_r = lds_f32(sc + 4 * r);
         ks_r8 = lds_f32(sc + 4 * (r + 8));
-        lv_r = fast_log2(lds_f32(sc + 64 + 4 * r));
-        lv_r8 = fast_log2(lds_f32(sc + 64 + 4 * (r + 8)));
+        vs_r = lds_f32(sc + 64 + 4 * r);
+        vs_r8 = lds_f32(sc + 64 + 4 * (r + 8));
       }
 
       // ---- mask (per token: the same for both sequences, whose shared
@@ -600,12 +600,7 @@ __global__ void __launch_bounds__(TC<KV, NQ>::kWarps * 32, 1)
         }
         const float a0 = k0 ? s0 * sl2 : -INFINITY, a1 = k0 ? s1 * sl2 : -INFINITY;
         const float a2 = k1 ? s2 * sl2 : -INFINITY, a3 = k1 ? s3 * sl2 : -INFINITY;
-        // a + log2(v scale): the exponent of the weight that multiplies V.  Slots
-        // of masked tokens may hold anything (unwritten memory), so neither their
-        // scale nor their V row may reach the arithmetic.
-        const float e0 = k0 ? a0 + lv_r : -INFINITY, e1 = k0 ? a1 + lv_r : -INFINITY;
-        const float e2 = k1 ? a2 + lv_r8 : -INFINITY, e3 = k1 ? a3 + lv_r8 : -INFINITY;
-        float bm0 = fmaxf(e0, e2), bm1 = fmaxf(e1, e3);
+        float bm0 = fmaxf(a0, a2), bm1 = fmaxf(a1, a3);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
           bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, off));
@@ -614,15 +609,10 @@ __global__ void __launch_bounds__(TC<KV, NQ>::kWarps * 32, 1)
         const float mn0 = fmaxf(m0[t], bm0), mn1 = fmaxf(m1[t], bm1);
         const float z0 = mn0 == -INFINITY ? 0.f : mn0, z1 = mn1 == -INFINITY ? 0.f : mn1;
         const float al0 = fast_exp2(m0[t] - z0), al1 = fast_exp2(m1[t] - z1);
-        const float p0 = fast_exp2(e0 - z0), p1 = fast_exp2(e1 - z1), p2 = fast_exp2(e2 - z0),
-                    p3 = fast_exp2(e3 - z1);
-        if (KV == 1) {
-          l0[t] = l0[t] * al0 + (p0 + p2);
-          l1[t] = l1[t] * al1 + (p1 + p3);
-        } else {
-          l0[t] = l0[t] * al0 + (fast_exp2(a0 - z0) + fast_exp2(a2 - z0));
-          l1[t] = l1[t] * al1 + (fast_exp2(a1 - z1) + fast_exp2(a3 - z1));
-        }
+        const float p0 = fast_exp2(a0 - z0), p1 = fast_exp2(a1 - z1), p2 = fast_exp2(a2 - z0),
+                    p3 = fast_exp2(a3 - z1);
+        l0[t] = l0[t] * al0 + (p0 + p2);
+        l1[t] = l1[t] * al1 + (p1 + p3);
         m0[t] = mn0;
         m1[t] = mn1;
         if (__any_sync(kFull, (al0 != 1.f) || (al1 != 1.f))) {
@@ -634,8 +624,17 @@ __global__ void __launch_bounds__(TC<KV, NQ>::kWarps * 32, 1)
             o[t][i][3] *= al1;
           }
         }
-        pb0[t] = movmatrix_t(KV == 1 ? pack_bf16(p0, p1) : pack_f16(p0, p1));
-        pb1[t] = movmatrix_t(KV == 1 ? pack_bf16(p2, p3) : pack_f16(p2, p3));
+        // FP8 / INT8: the weight multiplies the V code times the token's V
+        // scale.  Slots of masked tokens may hold anything (unwritten memory),
+        // so their scale must not reach the arithmetic (0 * NaN is NaN).
+        if (KV == 1) {
+          pb0[t] = movmatrix_t(pack_bf16(p0, p1));
+          pb1[t] = movmatrix_t(pack_bf16(p2, p3));
+        } else {
+          const float w0 = k0 ? vs_r : 0.f, w1 = k1 ? vs_r8 : 0.f;
+          pb0[t] = movmatrix_t(pack_f16(p0 * w0, p1 * w0));
+          pb1[t] = movmatrix_t(pack_f16(p2 * w1, p3 * w1));
+        }
       }
 
       // ---- O^T += V^T P : rows = head-dim, columns = query heads
