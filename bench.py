@@ -453,6 +453,21 @@ def main():
     setup.cache.sync_status()
     ms_max = reduce_max(ms, ws, dev)
 
+    # ---- per-step spread (separate from the timed region): events around
+    # each of up to 50 steps, for the median and the 10th / 90th percentiles
+    pct = None
+    if rank == 0:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(min(50, args.steps))]
+        for a0, a1 in evs:
+            a0.record(stream)
+            st.step()
+            a1.record(stream)
+        torch.cuda.synchronize(dev)
+        t = sorted(a0.elapsed_time(a1) for a0, a1 in evs)
+        q = lambda f: round(t[min(len(t) - 1, int(f * len(t)))], 5)
+        pct = {"steps": len(t), "p10": q(0.1), "p50": q(0.5), "p90": q(0.9)}
+
     # ---- end to end through host buffers ----
     e2e = None
     if not args.no_e2e:
@@ -521,6 +536,7 @@ def main():
         "steps": args.steps,
         "warmup": max(3, args.warmup),
         "ms_per_step": round(ms_step, 5),
+        "step_ms_percentiles": pct,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
