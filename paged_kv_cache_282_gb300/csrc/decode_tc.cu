@@ -97,6 +97,11 @@ constexpr size_t smem_bytes() {
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
+// Release / acquire fence at GPU scope: orders a warp's partial-record stores
+// before the arrival count that publishes them, and the count before the
+// merging warp's loads of the other warps' records.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t global_timer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -687,6 +692,9 @@ __global__ void __launch_bounds__(TC<KV, NQ>::kWarps * 32, 1)
 
     if (pc.flags & kPieceLastOfRun) {
       // ---- finalise the run: one output or partial record per sequence
+      int rec_items[NQ];  // merge item of each record written, or -1
+#pragma unroll
+      for (int t = 0; t < NQ; ++t) rec_items[t] = -1;
 #pragma unroll
       for (int t = 0; t < NQ; ++t) {
         if (t == 1 && !two) break;
@@ -739,14 +747,24 @@ __global__ void __launch_bounds__(TC<KV, NQ>::kWarps * 32, 1)
               rec[G * 128 + G + h1] = L1;
             }
           }
-          // publish the record, count it, and merge if it was the last one
-          __threadfence();
-          __syncwarp();
+          rec_items[t] = ci;
+        }
+      }
+      // publish the run's records (one release fence for both sequences of a
+      // pair), count them, and merge any (sequence, kv head) whose last
+      // record this was (acquire before reading the others' records)
+      if (rec_items[0] >= 0 || (NQ == 2 && rec_items[NQ - 1] >= 0)) {
+        fence_acq_rel_gpu();
+        __syncwarp();
+#pragma unroll
+        for (int t = 0; t < NQ; ++t) {
+          const int ci = rec_items[t];
+          if (ci < 0) continue;
           int last = 0;
           if (lane == 0) last = atomicAdd(p.counters + ci, 1) == p.combine[ci].n_partials - 1;
           last = __shfl_sync(kFull, last, 0);
           if (last) {
-            __threadfence();
+            fence_acq_rel_gpu();
             merge_partials<G>(p, p.combine[ci], lane);
           }
         }
@@ -1000,7 +1018,7 @@ __global__ void __launch_bounds__(kPWarps * 32, 1) prefix_decode_kernel(const __
       rec[G * 128 + G + h] = half ? l_r8 : l_r;
     }
   }
-  __threadfence();
+  fence_acq_rel_gpu();
   __syncwarp();
   for (int k = 0; k < MPW; ++k) {
     if (mbase + k >= it.n_members) break;
@@ -1009,7 +1027,7 @@ __global__ void __launch_bounds__(kPWarps * 32, 1) prefix_decode_kernel(const __
     if (lane == 0) last = atomicAdd(p.counters + mb.item, 1) == p.combine[mb.item].n_partials - 1;
     last = __shfl_sync(kFull, last, 0);
     if (last) {
-      __threadfence();
+      fence_acq_rel_gpu();
       merge_partials<G>(p, p.combine[mb.item], lane);
     }
   }
