@@ -460,6 +460,17 @@ __global__ void __launch_bounds__(TC<KV, NQ>::kWarps * 32, 1)
   for (int pi = pb; pi < pe; ++pi) {
     const Piece pc = p.pieces[pi];
     const int g = pc.kv_head, L = pc.ctx_len;
+    // blocks whose every token is kept: [wb0, wb1) (the tail of the keep-set)
+    // and [0, wsb) (blocks wholly inside the sinks); all other blocks test
+    // their tokens one by one
+    int wb0 = 0, wsb = 0;
+    const int wb1 = L / kBlock;
+    if (p.mask_mode == 1) {
+      wb0 = max(0, (L - 1 - p.window + kBlock - 1) / kBlock);
+    } else if (p.mask_mode == 2 && (long long)L > (long long)p.num_sinks + p.window) {
+      wb0 = (L - p.window + kBlock - 1) / kBlock;
+      wsb = p.num_sinks / kBlock;
+    }
     if (!run_open) {
       two = NQ == 2 && pc.q_row1 >= 0;
       // Q^T fragments (B operand): rows k = head-dim slots, column n = query head r
@@ -564,10 +575,7 @@ __global__ void __launch_bounds__(TC<KV, NQ>::kWarps * 32, 1)
       const int tok0 = lb * kBlock + r, tok1 = tok0 + 8;
       // most units lie wholly inside the keep-set: their first and last
       // token decide it, and the per-token test is skipped
-      const bool whole = kept(lb * kBlock, L, p.mask_mode, p.num_sinks, p.window) &&
-                         kept(lb * kBlock + kBlock - 1, L, p.mask_mode, p.num_sinks, p.window) &&
-                         (p.mask_mode != 2 || lb * kBlock + kBlock <= p.num_sinks ||
-                          lb * kBlock >= L - p.window || (long long)L <= (long long)p.num_sinks + p.window);
+      const bool whole = (lb >= wb0 && lb < wb1) || lb < wsb;
       const bool k0 = whole || kept(tok0, L, p.mask_mode, p.num_sinks, p.window);
       const bool k1 = whole || kept(tok1, L, p.mask_mode, p.num_sinks, p.window);
       const bool h0v = 2 * c < G, h1v = 2 * c + 1 < G;
