@@ -175,14 +175,27 @@ __global__ void h2o_score_kernel(const SeqRow* __restrict__ rows, int n_heads, i
   const int G = n_heads / n_kv_heads;
   float sum = 0.0f;
   if ((G & 3) == 0 && ((reinterpret_cast<uintptr_t>(logits) | (uintptr_t)(stride * G * 4)) & 15) == 0) {
-    // the kv heads' loads are independent: unrolled, they are all in flight at once
-#pragma unroll 8
-    for (int g = 0; g < n_kv_heads; ++g) {
-      const float4* lg = reinterpret_cast<const float4*>(logits + (((size_t)b * n_kv_heads + g) * stride + j) * G);
-      for (int i = 0; i < G / 4; ++i) {
-        const float4 x = lg[i];
-        const float* ls = s_lse + g * G + 4 * i;
-        sum += __expf(x.x - ls[0]) + __expf(x.y - ls[1]) + __expf(x.z - ls[2]) + __expf(x.w - ls[3]);
+    // heads in groups of four (one float4 each), visited in head order; a
+    // batch of 8 float4 loads is issued before any of them is used
+    const int q4 = G >> 2, nf = n_heads >> 2;
+    for (int f0 = 0; f0 < nf; f0 += 8) {
+      int g = f0 / q4, i = f0 - g * q4;
+      float4 x[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (f0 + u < nf)
+          x[u] = *reinterpret_cast<const float4*>(logits + (((size_t)b * n_kv_heads + g) * stride + j) * G + 4 * i);
+        if (++i == q4) {
+          i = 0;
+          ++g;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (f0 + u < nf) {
+          const float* ls = s_lse + 4 * (f0 + u);
+          sum += __expf(x[u].x - ls[0]) + __expf(x[u].y - ls[1]) + __expf(x[u].z - ls[2]) + __expf(x[u].w - ls[3]);
+        }
       }
     }
   } else {
@@ -237,35 +250,99 @@ __device__ int block_excl_scan(int v, int* excl, int* s_warp) {
 }
 
 constexpr int kSelUnroll = 16;     // keys per thread per sweep (independent loads)
-constexpr int kSelCap = 16384;      // shared-memory candidates of the two-pass path
+constexpr int kSelCap = 8192;       // candidates held in shared memory
 constexpr int kSelSample = 4096;    // keys sampled to pick the one-pass threshold (<= kSelCap)
+// The gather streams a row through a ring of bulk copies: kSelRing stages of
+// kSelChunk scores, one chunk per sweep (kSelChunk / kSelThreads per thread).
+constexpr int kSelChunk = 8192;
+constexpr int kSelRing = 4;
+constexpr size_t kSelSmem = (size_t)kSelCap * 8 + (size_t)kSelRing * kSelChunk * 4;
+static_assert(kSelSample % kSelThreads == 0 && kSelChunk % (4 * kSelThreads) == 0, "select geometry");
+static_assert(kSelSmem <= 200 * 1024, "select shared memory");
+
+template <int N>
+struct IntTag {
+  static constexpr int value = N;
+};
 
 struct SelShared {
+  unsigned long long bar[kSelRing];  // ring stage mbarriers (one arrival + the copy's bytes)
   uint32_t hist[256];
   int warp[32];
+  int tot[32];     // per-warp candidate counts of a sweep
   uint32_t prefix, mask;
-  int k, n_cand, top;
+  int k, n_cand, top, n_head;
 };
+
+__device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
+  return (uint32_t)__cvta_generic_to_shared(ptr);
+}
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_inval(uint32_t bar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for phase `parity` of an mbarrier, for at most limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+// 1-D bulk copy global -> shared; both addresses and the size 16-byte multiples.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
 
 // Histogram of digit (key >> shift) & 255 over the keys i < m whose bits under
 // `mask` equal `prefix`.  Scores are often equal (zero outside the keep-set,
 // or of one magnitude), so lanes of a warp holding the same digit are
 // grouped (match.any) and their leader adds the group's count: one shared
 // atomic per distinct digit per warp step instead of one per key.
-template <class KeyAt>
+// U keys per thread per sweep: few for the short candidate lists in shared
+// memory (every thread runs every slot of the sweep), kSelUnroll for rows
+// read from global memory.
+template <int U, class KeyAt>
 __device__ void digit_histogram(KeyAt key_at, int m, uint32_t prefix, uint32_t mask, int shift, SelShared& sh) {
   for (int i = threadIdx.x; i < 256; i += blockDim.x) sh.hist[i] = 0;
   __syncthreads();
   const int lane = threadIdx.x & 31;
-  for (int base = 0; base < m; base += kSelUnroll * kSelThreads) {
-    uint32_t key[kSelUnroll];
+  for (int base = 0; base < m; base += U * kSelThreads) {
+    uint32_t key[U];
 #pragma unroll
-    for (int u = 0; u < kSelUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int i = base + u * kSelThreads + threadIdx.x;
       key[u] = i < m ? key_at(i) : 0u;
     }
 #pragma unroll
-    for (int u = 0; u < kSelUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int i = base + u * kSelThreads + threadIdx.x;
       const bool in = i < m && (key[u] & mask) == prefix;
       if (!__any_sync(0xffffffffu, in)) continue;
@@ -310,7 +387,7 @@ __device__ void find_digit(SelShared& sh, int k, int* digit_out, int* k_out, int
 // Exact keep-th largest key among keys i < m (radix select, 8 bits a pass):
 // on return sh.prefix is that key and sh.k the number of keys equal to it
 // that belong to the selection (the lowest positions among them).
-template <class KeyAt>
+template <int U, class KeyAt>
 __device__ void radix_select(KeyAt key_at, int m, int keep, SelShared& sh) {
   if (threadIdx.x == 0) {
     sh.prefix = 0;
@@ -321,7 +398,7 @@ __device__ void radix_select(KeyAt key_at, int m, int keep, SelShared& sh) {
   for (int shift = 24; shift >= 0; shift -= 8) {
     const uint32_t prefix = sh.prefix, mask = sh.mask;
     const int k = sh.k;
-    digit_histogram(key_at, m, prefix, mask, shift, sh);
+    digit_histogram<U>(key_at, m, prefix, mask, shift, sh);
     __shared__ int s_digit, s_k;
     find_digit(sh, k, &s_digit, &s_k, nullptr);
     if (threadIdx.x == 0) {
@@ -338,16 +415,16 @@ __device__ void radix_select(KeyAt key_at, int m, int keep, SelShared& sh) {
 // to T (counted over all i, in or out of the range); keys are visited in the
 // order of i, which must be the order of positions.  Returns the number
 // written.
-template <class KeyAt, class PosAt>
+template <int U, class KeyAt, class PosAt>
 __device__ int ordered_emit(KeyAt key_at, PosAt pos_at, int m, uint32_t T, int need_eq, int emit_lo, int emit_hi,
                             int32_t* out, SelShared& sh) {
   int taken = 0, eq_seen = 0;
-  for (int base = 0; base < m; base += kSelUnroll * kSelThreads) {
-    const int i0 = base + kSelUnroll * threadIdx.x;
-    uint32_t key[kSelUnroll];
+  for (int base = 0; base < m; base += U * kSelThreads) {
+    const int i0 = base + U * threadIdx.x;
+    uint32_t key[U];
     int n_eq = 0;
 #pragma unroll
-    for (int u = 0; u < kSelUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
       key[u] = i0 + u < m ? key_at(i0 + u) : 0u;
       n_eq += (i0 + u < m && key[u] == T);
     }
@@ -356,7 +433,7 @@ __device__ int ordered_emit(KeyAt key_at, PosAt pos_at, int m, uint32_t T, int n
     int rank = eq_seen + eq_excl, n_sel = 0;
     uint32_t take = 0;  // bit u: key u is selected and inside the range
 #pragma unroll
-    for (int u = 0; u < kSelUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
       if (i0 + u >= m) continue;
       const bool sel = key[u] > T || (key[u] == T && rank++ < need_eq);
       const int p = pos_at(i0 + u);
@@ -369,12 +446,150 @@ __device__ int ordered_emit(KeyAt key_at, PosAt pos_at, int m, uint32_t T, int n
     const int sel_tot = block_excl_scan(n_sel, &sel_excl, sh.warp);
     int pos = taken + sel_excl;
 #pragma unroll
-    for (int u = 0; u < kSelUnroll; ++u)
+    for (int u = 0; u < U; ++u)
       if (take >> u & 1u) out[pos++] = pos_at(i0 + u);
     taken += sel_tot;
     eq_seen += eq_tot;
   }
   return taken;
+}
+
+// The ring's geometry for a row: the head (positions before the row's first
+// 128-byte boundary, fewer than 32, read directly) and the chunks after it.
+__device__ __forceinline__ int ring_head(const float* a, int n) {
+  return min(n, (int)(((128u - (uint32_t)(reinterpret_cast<uintptr_t>(a) & 127u)) & 127u) >> 2));
+}
+// Thread 0: chunk c of the row into stage c % kSelRing, one bulk copy from a
+// 128-byte aligned address (the ragged end, under 16 bytes, is read directly).
+__device__ __forceinline__ void ring_issue(const float* a, int n, int head, int c, float* ring, SelShared& sh) {
+  const int st = c % kSelRing, k0 = head + c * kSelChunk;
+  const int bulk = min(kSelChunk, n - k0) & ~3;
+  const uint32_t bar = smem_u32(&sh.bar[st]);
+  if (bulk > 0) {
+    mbar_expect_tx(bar, (uint32_t)bulk * 4u);
+    bulk_load(smem_u32(ring + (size_t)st * kSelChunk), a + k0, (uint32_t)bulk * 4u, bar);
+  } else {
+    mbar_arrive(bar);
+  }
+}
+// Thread 0: initialises the ring's barriers and issues its first chunks.  A
+// barrier of the whole block must separate this from the first wait.
+__device__ void ring_prime(const float* a, int n, float* ring, SelShared& sh) {
+  const int head = ring_head(a, n), nch = (n - head + kSelChunk - 1) / kSelChunk;
+  for (int i = 0; i < kSelRing; ++i) mbar_init(smem_u32(&sh.bar[i]), 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  for (int c = 0; c < min(nch, kSelRing); ++c) ring_issue(a, n, head, c, ring, sh);
+}
+
+// Streams the scores a[0, n) through the shared-memory ring and gathers, in
+// position order, the keys at or above thr into c_key / c_pos (at most
+// kSelCap stored).  The head is read directly by warp 0; the chunks arrive
+// kSelRing - 1 ahead of the sweep (primed: ring_prime already ran for this
+// row).  A sweep whose chunk holds no candidate costs one barrier (which also
+// hands its stage back to the copies); a sweep with candidates adds one more
+// to exchange the warps' counts.  Returns the number of qualifying keys, or
+// -1 when a copy did not complete within limit_ns (the copies still in flight
+// are waited for, within a bound, first).  Called by the whole block.
+__device__ int gather_ring(const float* __restrict__ a, int n, uint32_t thr, bool primed, float* ring,
+                           uint32_t* c_key, int32_t* c_pos, SelShared& sh, uint64_t limit_ns) {
+  constexpr int P = kSelChunk / kSelThreads;  // keys per thread per sweep
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const uint32_t lt = (1u << lane) - 1u;  // lanes below this one
+  // the float whose order key is thr: keys >= thr are exactly the non-NaN
+  // floats >= thr_f (-0 and +0 share one key)
+  const float thr_f = __uint_as_float((thr & 0x80000000u) ? (thr & 0x7fffffffu) : ~thr);
+  const int head = ring_head(a, n);
+  const int nch = (n - head + kSelChunk - 1) / kSelChunk;
+  if (t < 32) {
+    const uint32_t key = t < head ? order_key(a[t]) : 0u;
+    const uint32_t hb = __ballot_sync(kFull, t < head && key >= thr);
+    if ((hb >> lane) & 1u) {
+      c_key[__popc(hb & lt)] = key;
+      c_pos[__popc(hb & lt)] = t;
+    }
+    if (t == 0) {
+      sh.n_head = __popc(hb);
+      if (!primed) ring_prime(a, n, ring, sh);
+    }
+  }
+  __syncthreads();
+  int filled = sh.n_head;
+  for (int c = 0; c < nch; ++c) {
+    const int st = c % kSelRing, k0 = head + c * kSelChunk;
+    const int cnt = min(kSelChunk, n - k0), bulk = cnt & ~3;
+    const bool ok = mbar_wait(smem_u32(&sh.bar[st]), (uint32_t)((c / kSelRing) & 1), limit_ns);
+    const int i0 = P * t;
+    const float* src = ring + (size_t)st * kSelChunk;
+    float x[P];
+    if (ok && i0 + P <= bulk) {
+#pragma unroll
+      for (int v = 0; v < P / 4; ++v) {
+        const float4 y = reinterpret_cast<const float4*>(src + i0)[v];
+        x[4 * v] = y.x;
+        x[4 * v + 1] = y.y;
+        x[4 * v + 2] = y.z;
+        x[4 * v + 3] = y.w;
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < P; ++u) {
+        const int i = i0 + u;
+        x[u] = (!ok || i >= cnt) ? -INFINITY : (i < bulk ? src[i] : a[k0 + i]);
+      }
+    }
+    // Prefilter in float: !(x < thr_f) holds for every key at or above thr
+    // (and for NaN); the exact key test runs only in sweeps where it fires.
+    bool maybe = false;
+#pragma unroll
+    for (int u = 0; u < P; ++u) maybe |= !(x[u] < thr_f);
+    // every thread has read stage st; any candidate, or a copy that timed out?
+    const int flags = __syncthreads_or((maybe ? 1 : 0) | (ok ? 0 : 0x10000));
+    if (flags & 0x10000) {
+      if (t == 0)
+        for (int v = c; v < min(nch, c + kSelRing); ++v)
+          mbar_wait(smem_u32(&sh.bar[v % kSelRing]), (uint32_t)((v / kSelRing) & 1), limit_ns);
+      __syncthreads();
+      return -1;
+    }
+    if (t == 0 && c + kSelRing < nch) ring_issue(a, n, head, c + kSelRing, ring, sh);
+    if (flags == 0) continue;
+    uint32_t key[P], sel = 0;  // bit u: key u qualifies
+#pragma unroll
+    for (int u = 0; u < P; ++u) {
+      key[u] = order_key(x[u]);
+      sel |= (uint32_t)(i0 + u < cnt && key[u] >= thr) << u;
+    }
+    // candidates before this thread's within its warp, and the warp's count
+    int below = 0, wcount = 0;
+#pragma unroll
+    for (int u = 0; u < P; ++u) {
+      const uint32_t bu = __ballot_sync(kFull, (sel >> u) & 1u);
+      below += __popc(bu & lt);
+      wcount += __popc(bu);
+    }
+    if (lane == 0) sh.tot[w] = wcount;
+    __syncthreads();
+    const int tw = sh.tot[lane];
+    const int before = (int)__reduce_add_sync(kFull, (uint32_t)(lane < w ? tw : 0));
+    const int total = (int)__reduce_add_sync(kFull, (uint32_t)tw);
+    int pos = filled + before + below;
+#pragma unroll
+    for (int u = 0; u < P; ++u)
+      if ((sel >> u) & 1u) {
+        if (pos < kSelCap) {
+          c_key[pos] = key[u];
+          c_pos[pos] = k0 + i0 + u;
+        }
+        ++pos;
+      }
+    filled += total;
+  }
+  __syncthreads();
+  if (t == 0)
+    for (int i = 0; i < kSelRing; ++i) mbar_inval(smem_u32(&sh.bar[i]));
+  __syncthreads();
+  return filled;
 }
 
 // One CTA per sequence.  The kept set is [0, lo) (sinks), the selected
@@ -389,11 +604,13 @@ __device__ int ordered_emit(KeyAt key_at, PosAt pos_at, int m, uint32_t T, int n
 __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* __restrict__ rows,
                                                                  const float* __restrict__ acc, int64_t acc_stride,
                                                                  SelPolicy pol, int32_t* __restrict__ keep_idx,
-                                                                 int64_t keep_stride, int32_t* __restrict__ keep_count) {
+                                                                 int64_t keep_stride, int32_t* __restrict__ keep_count,
+                                                                 int32_t* __restrict__ status, uint64_t wait_limit_ns) {
   __shared__ SelShared sh;
-  extern __shared__ uint32_t cand[];  // kSelCap keys, then kSelCap positions
+  extern __shared__ uint32_t cand[];  // kSelCap keys, kSelCap positions, then the ring
   uint32_t* c_key = cand;
   int32_t* c_pos = reinterpret_cast<int32_t*>(cand + kSelCap);
+  float* ring = reinterpret_cast<float*>(cand + 2 * kSelCap);
   const SeqRow row = rows[blockIdx.x];
   const int b = row.q_row, L = row.ctx_len;
   const float* a = acc + (size_t)b * acc_stride;
@@ -409,70 +626,60 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
   int n_heavy = 0;
   // Gathers, in position order, the keys of [0, n) at or above thr into the
   // shared candidate arrays (at most kSelCap written); returns how many keys
-  // qualified.  Each thread takes kSelUnroll consecutive positions a sweep
-  // (float4 loads when the row is 16-byte aligned).
-  auto gather = [&](uint32_t thr) {
-    const bool vec = ((reinterpret_cast<uintptr_t>(a)) & 15) == 0;
-    int filled = 0;
-    for (int base = 0; base < n; base += kSelUnroll * kSelThreads) {
-      const int j0 = base + kSelUnroll * threadIdx.x;
-      uint32_t key[kSelUnroll];
-      if (vec && j0 + kSelUnroll <= n) {
-#pragma unroll
-        for (int v = 0; v < kSelUnroll / 4; ++v) {
-          const float4 x = reinterpret_cast<const float4*>(a + j0)[v];
-          key[4 * v] = order_key(x.x);
-          key[4 * v + 1] = order_key(x.y);
-          key[4 * v + 2] = order_key(x.z);
-          key[4 * v + 3] = order_key(x.w);
-        }
-      } else {
-#pragma unroll
-        for (int u = 0; u < kSelUnroll; ++u) key[u] = j0 + u < n ? order_key(a[j0 + u]) : 0u;
-      }
-      int c = 0;
-#pragma unroll
-      for (int u = 0; u < kSelUnroll; ++u) c += (j0 + u < n && key[u] >= thr);
-      int excl;
-      const int tot = block_excl_scan(c, &excl, sh.warp);
-      int w = filled + excl;
-#pragma unroll
-      for (int u = 0; u < kSelUnroll; ++u)
-        if (j0 + u < n && key[u] >= thr) {
-          if (w < kSelCap) {
-            c_key[w] = key[u];
-            c_pos[w] = j0 + u;
-          }
-          ++w;
-        }
-      filled += tot;
+  // qualified, or -1 when a copy timed out.
+  auto gather = [&](uint32_t thr, bool primed) {
+    return gather_ring(a, n, thr, primed, ring, c_key, c_pos, sh, wait_limit_ns);
+  };
+  auto timed_out = [&]() {
+    if (threadIdx.x == 0) {
+      atomicOr(status, kStatusTimeout);
+      keep_count[b] = 0;
     }
-    __syncthreads();
-    return filled;
   };
   auto smem_key = [c_key](int i) { return c_key[i]; };
   auto smem_pos = [c_pos](int i) { return c_pos[i]; };
+  // exact select and ordered output over the m (<= kSelCap) candidates in
+  // shared memory, with as few keys per thread as cover m in one sweep
+  auto select_candidates = [&](int m) {
+    auto run = [&](auto tag) {
+      constexpr int U = decltype(tag)::value;
+      radix_select<U>(smem_key, m, keep, sh);
+      const uint32_t T = sh.prefix;
+      const int need_eq = sh.k;
+      return ordered_emit<U>(smem_key, smem_pos, m, T, need_eq, lo, hi, out + lo, sh);
+    };
+    if (m <= 2 * kSelThreads) return run(IntTag<2>{});
+    if (m <= 4 * kSelThreads) return run(IntTag<4>{});
+    return run(IntTag<kSelCap / kSelThreads>{});
+  };
   bool done = false;
   if (keep > 0 && n > 4 * kSelSample) {
     // Long rows: a strided sample of kSelSample keys gives a threshold a bit
     // below the expected keep-th largest; one pass gathers every key at or
     // above it.  When at least keep (and at most kSelCap) keys qualify, the
     // keep-th largest is among them and the exact select runs on them alone;
-    // otherwise the two-pass path below runs.
-    for (int i = threadIdx.x; i < kSelSample; i += blockDim.x)
-      c_key[i] = order_key(a[(int)((int64_t)i * n / kSelSample)]);
+    // otherwise the two-pass path below runs.  The row's first chunks stream
+    // into the ring while the sample is read and ranked.
+    if (threadIdx.x == 0) ring_prime(a, n, ring, sh);
+    {
+      constexpr int U = kSelSample / kSelThreads;  // every load issued before the first store
+      uint32_t sk[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        sk[u] = order_key(a[(int)((int64_t)(threadIdx.x + u * kSelThreads) * n / kSelSample)]);
+#pragma unroll
+      for (int u = 0; u < U; ++u) c_key[threadIdx.x + u * kSelThreads] = sk[u];
+    }
     __syncthreads();
     const int64_t want = ((int64_t)keep * kSelSample + n - 1) / n * 5 / 4 + 8;
     const int r = want < kSelSample ? (int)want : kSelSample;
-    radix_select(smem_key, kSelSample, r, sh);
+    radix_select<kSelSample / kSelThreads>(smem_key, kSelSample, r, sh);
     const uint32_t thr = sh.prefix;
     __syncthreads();
-    const int m = gather(thr);
+    const int m = gather(thr, true);
+    if (m < 0) return timed_out();
     if (m >= keep && m <= kSelCap) {
-      radix_select(smem_key, m, keep, sh);
-      const uint32_t T = sh.prefix;
-      const int need_eq = sh.k;
-      n_heavy = ordered_emit(smem_key, smem_pos, m, T, need_eq, lo, hi, out + lo, sh);
+      n_heavy = select_candidates(m);
       done = true;
     }
   }
@@ -480,7 +687,7 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
     auto global_key = [a](int i) { return order_key(a[i]); };
     auto global_pos = [](int i) { return i; };
     // pass 1: top-byte histogram and the candidate bucket
-    digit_histogram(global_key, n, 0u, 0u, 24, sh);
+    digit_histogram<kSelUnroll>(global_key, n, 0u, 0u, 24, sh);
     {
       __shared__ int s_top, s_rest, s_cnt;
       find_digit(sh, keep, &s_top, &s_rest, &s_cnt);
@@ -494,16 +701,13 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
     const int m = sh.n_cand;
     if (m <= kSelCap) {
       // pass 2: gather the candidates in position order
-      gather(lo_key);
-      radix_select(smem_key, m, keep, sh);
-      const uint32_t T = sh.prefix;
-      const int need_eq = sh.k;
-      n_heavy = ordered_emit(smem_key, smem_pos, m, T, need_eq, lo, hi, out + lo, sh);
+      if (gather(lo_key, false) < 0) return timed_out();
+      n_heavy = select_candidates(m);
     } else {
-      radix_select(global_key, n, keep, sh);
+      radix_select<kSelUnroll>(global_key, n, keep, sh);
       const uint32_t T = sh.prefix;
       const int need_eq = sh.k;
-      n_heavy = ordered_emit(global_key, global_pos, n, T, need_eq, lo, hi, out + lo, sh);
+      n_heavy = ordered_emit<kSelUnroll>(global_key, global_pos, n, T, need_eq, lo, hi, out + lo, sh);
     }
   }
   for (int i = threadIdx.x; i < L - hi; i += blockDim.x) out[lo + n_heavy + i] = hi + i;
@@ -713,10 +917,10 @@ cudaError_t launch_compact_scores(const CompactSeq* seqs, int n, const int32_t* 
 
 cudaError_t launch_h2o_select(const SeqRow* rows, int n_seqs, const float* acc, int64_t acc_stride,
                               const SelPolicy& pol, int32_t* keep_idx, int64_t keep_stride, int32_t* keep_count,
-                              cudaStream_t st) {
+                              int32_t* status, uint64_t wait_limit_ns, cudaStream_t st) {
   if (n_seqs <= 0) return cudaSuccess;
   static std::atomic<uint64_t> attr_set{0};  // one bit per device
-  const int smem = kSelCap * 8;
+  const int smem = (int)kSelSmem;
   int dev = 0;
   if (cudaError_t e = cudaGetDevice(&dev)) return e;
   const uint64_t bit = dev < 64 ? uint64_t(1) << dev : 0;
@@ -725,7 +929,8 @@ cudaError_t launch_h2o_select(const SeqRow* rows, int n_seqs, const float* acc, 
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit);
   }
-  h2o_select_kernel<<<n_seqs, kSelThreads, smem, st>>>(rows, acc, acc_stride, pol, keep_idx, keep_stride, keep_count);
+  h2o_select_kernel<<<n_seqs, kSelThreads, smem, st>>>(rows, acc, acc_stride, pol, keep_idx, keep_stride, keep_count,
+                                                       status, wait_limit_ns);
   return cudaGetLastError();
 }
 

@@ -1996,7 +1996,7 @@ pkv_status select_keep(pkv_pool* p, void* stream, int32_t n, const int32_t* lens
   if (pkv_status r = Staging::upload(s, n * sizeof(SeqRow), st)) return r;
   if (pkv_status r = launch(p, PKV_KERNEL_H2O_SELECT, st, [&] {
         return launch_h2o_select((const SeqRow*)s->dev, n, acc, acc_stride, pol, keep_idx, keep_stride, keep_count,
-                                 st);
+                                 p->buf.status, p->wait_limit_ns, st);
       }))
     return r;
   return Staging::release(s, st);

@@ -255,6 +255,31 @@ def test_policy_select_bit_exact(sinks, window, heavy):
         assert np.array_equal(keep[b, : cnt[b]], ref), (b, L)
 
 
+@pytest.mark.parametrize("pad,offset", [(1, 0), (3, 1)])
+def test_select_rows_not_16_byte_aligned(pad, offset):
+    """Score rows that do not start on a 16-byte boundary (a row stride that
+    is not a multiple of four floats, a base pointer one float in) take the
+    plain-load gather instead of the bulk-copy ring: same keep-sets."""
+    lens = [3000, 20000, 70001, 131072]
+    stride = max(lens) + pad
+    base = workloads.h2o_scores_input(len(lens), stride, seed=11 + pad)
+    cache = Twin(workloads.small("bf16", lens=(1,)), 4, 1, 4).cache
+    flat = torch.zeros(offset + len(lens) * stride, dtype=torch.float32, device="cuda")
+    flat[offset:] = base.reshape(-1).cuda()
+    acc = flat[offset:].view(len(lens), stride)
+    for sinks, window, heavy in ((4, 512, 1536), (0, 0, 9000)):
+        width = sinks + window + heavy
+        keep = torch.full((len(lens), width), -7, dtype=torch.int32, device="cuda")
+        cnt = torch.full((len(lens),), -1, dtype=torch.int32, device="cuda")
+        cache.policy_select(lens, acc, stride, sinks, window, heavy, keep, width, cnt)
+        cache.sync_status()
+        k, c = keep.cpu().numpy(), cnt.cpu().numpy()
+        for b, L in enumerate(lens):
+            ref = oracle.policy_select(L, sinks, window, heavy, base[b, :L].double().numpy())
+            assert c[b] == ref.size, (b, L)
+            assert np.array_equal(k[b, : c[b]], ref), (b, L)
+
+
 def test_patches_and_cow_chains_in_one_flush():
     """Several host-side changes queued before one device call: a table entry
     set to -1 and back (truncate + re-append), and a copy-on-write whose source
