@@ -251,7 +251,8 @@ __device__ int block_excl_scan(int v, int* excl, int* s_warp) {
 
 constexpr int kSelUnroll = 16;     // keys per thread per sweep (independent loads)
 constexpr int kSelCap = 8192;       // candidates held in shared memory
-constexpr int kSelSample = 4096;    // keys sampled to pick the one-pass threshold (<= kSelCap)
+constexpr int kSelSample = 2048;    // keys sampled to pick the one-pass threshold (<= kSelCap)
+constexpr int kSelSampleMinRow = 16384;  // rows longer than this take the sampled one-pass path
 // The gather streams a row through a ring of bulk copies: kSelRing stages of
 // kSelChunk scores, one chunk per sweep (kSelChunk / kSelThreads per thread).
 constexpr int kSelChunk = 8192;
@@ -268,6 +269,7 @@ struct IntTag {
 struct SelShared {
   unsigned long long bar[kSelRing];  // ring stage mbarriers (one arrival + the copy's bytes)
   uint32_t hist[256];
+  uint32_t hist2[2][256];  // radix passes: one filled while the other is cleared
   int warp[32];
   int tot[32];     // per-warp candidate counts of a sweep
   uint32_t prefix, mask;
@@ -330,9 +332,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // memory (every thread runs every slot of the sweep), kSelUnroll for rows
 // read from global memory.
 template <int U, class KeyAt>
-__device__ void digit_histogram(KeyAt key_at, int m, uint32_t prefix, uint32_t mask, int shift, SelShared& sh) {
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) sh.hist[i] = 0;
-  __syncthreads();
+__device__ void accumulate_digits(KeyAt key_at, int m, uint32_t prefix, uint32_t mask, int shift, uint32_t* hist) {
   const int lane = threadIdx.x & 31;
   for (int base = 0; base < m; base += U * kSelThreads) {
     uint32_t key[U];
@@ -348,10 +348,49 @@ __device__ void digit_histogram(KeyAt key_at, int m, uint32_t prefix, uint32_t m
       if (!__any_sync(0xffffffffu, in)) continue;
       const uint32_t digit = in ? (key[u] >> shift) & 255u : 256u;
       const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-      if (in && lane == __ffs(peers) - 1) atomicAdd(&sh.hist[digit], (uint32_t)__popc(peers));
+      if (in && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(peers));
     }
   }
+}
+template <int U, class KeyAt>
+__device__ void digit_histogram(KeyAt key_at, int m, uint32_t prefix, uint32_t mask, int shift, SelShared& sh) {
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) sh.hist[i] = 0;
   __syncthreads();
+  accumulate_digits<U>(key_at, m, prefix, mask, shift, sh.hist);
+  __syncthreads();
+}
+
+// Warp 0 alone: the digit d of a 256-bin histogram whose bin holds the k-th
+// largest key, (keys in bins above d) < k <= (keys in bins d and above).  Lane
+// l scans bins 255 - 8l down to 248 - 8l.  The one lane that holds d returns
+// true with d, k minus the keys above d, and the keys in bins d and above.
+__device__ __forceinline__ bool find_digit_warp(const uint32_t* hist, int k, int* digit, int* k_rem, int* count) {
+  const int lane = threadIdx.x & 31;
+  int c[8], sum = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    c[j] = (int)hist[255 - 8 * lane - j];
+    sum += c[j];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  int above = incl - sum;
+  if (!(above < k && k <= incl)) return false;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (above < k && k <= above + c[j]) {
+      *digit = 255 - 8 * lane - j;
+      *k_rem = k - above;
+      *count = above + c[j];
+      return true;
+    }
+    above += c[j];
+  }
+  return false;
 }
 
 // Finds, in parallel over the 256 bins, the digit d whose bin holds the k-th
@@ -387,24 +426,32 @@ __device__ void find_digit(SelShared& sh, int k, int* digit_out, int* k_out, int
 // Exact keep-th largest key among keys i < m (radix select, 8 bits a pass):
 // on return sh.prefix is that key and sh.k the number of keys equal to it
 // that belong to the selection (the lowest positions among them).
+// With last_shift > 0 the passes stop after that digit: sh.prefix then holds
+// the keep-th largest key's top bits with the rest zero, a lower bound of it.
 template <int U, class KeyAt>
-__device__ void radix_select(KeyAt key_at, int m, int keep, SelShared& sh) {
+__device__ void radix_select(KeyAt key_at, int m, int keep, SelShared& sh, int last_shift = 0) {
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) sh.hist2[0][i] = 0;
   if (threadIdx.x == 0) {
     sh.prefix = 0;
     sh.mask = 0;
     sh.k = keep;
   }
   __syncthreads();
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  int pass = 0;
+  for (int shift = 24; shift >= last_shift; shift -= 8, ++pass) {
     const uint32_t prefix = sh.prefix, mask = sh.mask;
     const int k = sh.k;
-    digit_histogram<U>(key_at, m, prefix, mask, shift, sh);
-    __shared__ int s_digit, s_k;
-    find_digit(sh, k, &s_digit, &s_k, nullptr);
-    if (threadIdx.x == 0) {
-      sh.prefix = prefix | ((uint32_t)s_digit << shift);
-      sh.mask = mask | (255u << shift);
-      sh.k = s_k;
+    // the other buffer was last read before the previous pass's final barrier
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) sh.hist2[(pass + 1) & 1][i] = 0;
+    accumulate_digits<U>(key_at, m, prefix, mask, shift, sh.hist2[pass & 1]);
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      int d, kr, cnt;
+      if (find_digit_warp(sh.hist2[pass & 1], k, &d, &kr, &cnt)) {
+        sh.prefix = prefix | ((uint32_t)d << shift);
+        sh.mask = mask | (255u << shift);
+        sh.k = kr;
+      }
     }
     __syncthreads();
   }
@@ -508,21 +555,34 @@ __device__ int gather_ring(const float* __restrict__ a, int n, uint32_t thr, boo
       c_key[__popc(hb & lt)] = key;
       c_pos[__popc(hb & lt)] = t;
     }
-    if (t == 0) {
-      sh.n_head = __popc(hb);
-      if (!primed) ring_prime(a, n, ring, sh);
-    }
+    if (t == 0) sh.n_head = __popc(hb);
   }
-  __syncthreads();
+  // Thread 0 alone waits on the ring's barriers: for chunk c + 1 before the
+  // barrier that ends sweep c (chunk 0 before the first), so each sweep's
+  // chunk is resident once the previous barrier is passed.
+  bool ok = true;
+  if (t == 0) {
+    if (!primed) ring_prime(a, n, ring, sh);
+    if (nch > 0) ok = mbar_wait(smem_u32(&sh.bar[0]), 0u, limit_ns);
+  }
+  auto drain = [&](int first, int end) {  // thread 0: chunks [first, end) were issued, not consumed
+    if (t == 0)
+      for (int v = first; v < end; ++v)
+        mbar_wait(smem_u32(&sh.bar[v % kSelRing]), (uint32_t)((v / kSelRing) & 1), limit_ns);
+    __syncthreads();
+  };
+  if (__syncthreads_or(ok ? 0 : 1)) {
+    drain(0, min(nch, kSelRing));
+    return -1;
+  }
   int filled = sh.n_head;
   for (int c = 0; c < nch; ++c) {
     const int st = c % kSelRing, k0 = head + c * kSelChunk;
     const int cnt = min(kSelChunk, n - k0), bulk = cnt & ~3;
-    const bool ok = mbar_wait(smem_u32(&sh.bar[st]), (uint32_t)((c / kSelRing) & 1), limit_ns);
     const int i0 = P * t;
     const float* src = ring + (size_t)st * kSelChunk;
     float x[P];
-    if (ok && i0 + P <= bulk) {
+    if (i0 + P <= bulk) {
 #pragma unroll
       for (int v = 0; v < P / 4; ++v) {
         const float4 y = reinterpret_cast<const float4*>(src + i0)[v];
@@ -535,7 +595,7 @@ __device__ int gather_ring(const float* __restrict__ a, int n, uint32_t thr, boo
 #pragma unroll
       for (int u = 0; u < P; ++u) {
         const int i = i0 + u;
-        x[u] = (!ok || i >= cnt) ? -INFINITY : (i < bulk ? src[i] : a[k0 + i]);
+        x[u] = i >= cnt ? -INFINITY : (i < bulk ? src[i] : a[k0 + i]);
       }
     }
     // Prefilter in float: !(x < thr_f) holds for every key at or above thr
@@ -543,23 +603,19 @@ __device__ int gather_ring(const float* __restrict__ a, int n, uint32_t thr, boo
     bool maybe = false;
 #pragma unroll
     for (int u = 0; u < P; ++u) maybe |= !(x[u] < thr_f);
+    if (t == 0 && c + 1 < nch)
+      ok = mbar_wait(smem_u32(&sh.bar[(c + 1) % kSelRing]), (uint32_t)(((c + 1) / kSelRing) & 1), limit_ns);
     // every thread has read stage st; any candidate, or a copy that timed out?
     const int flags = __syncthreads_or((maybe ? 1 : 0) | (ok ? 0 : 0x10000));
     if (flags & 0x10000) {
-      if (t == 0)
-        for (int v = c; v < min(nch, c + kSelRing); ++v)
-          mbar_wait(smem_u32(&sh.bar[v % kSelRing]), (uint32_t)((v / kSelRing) & 1), limit_ns);
-      __syncthreads();
+      drain(c + 1, min(nch, c + kSelRing));
       return -1;
     }
     if (t == 0 && c + kSelRing < nch) ring_issue(a, n, head, c + kSelRing, ring, sh);
     if (flags == 0) continue;
-    uint32_t key[P], sel = 0;  // bit u: key u qualifies
+    uint32_t sel = 0;  // bit u: key u qualifies
 #pragma unroll
-    for (int u = 0; u < P; ++u) {
-      key[u] = order_key(x[u]);
-      sel |= (uint32_t)(i0 + u < cnt && key[u] >= thr) << u;
-    }
+    for (int u = 0; u < P; ++u) sel |= (uint32_t)(i0 + u < cnt && order_key(x[u]) >= thr) << u;
     // candidates before this thread's within its warp, and the warp's count
     int below = 0, wcount = 0;
 #pragma unroll
@@ -578,7 +634,7 @@ __device__ int gather_ring(const float* __restrict__ a, int n, uint32_t thr, boo
     for (int u = 0; u < P; ++u)
       if ((sel >> u) & 1u) {
         if (pos < kSelCap) {
-          c_key[pos] = key[u];
+          c_key[pos] = order_key(x[u]);
           c_pos[pos] = k0 + i0 + u;
         }
         ++pos;
@@ -653,7 +709,7 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
     return run(IntTag<kSelCap / kSelThreads>{});
   };
   bool done = false;
-  if (keep > 0 && n > 4 * kSelSample) {
+  if (keep > 0 && n > kSelSampleMinRow) {
     // Long rows: a strided sample of kSelSample keys gives a threshold a bit
     // below the expected keep-th largest; one pass gathers every key at or
     // above it.  When at least keep (and at most kSelCap) keys qualify, the
@@ -673,7 +729,8 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
     __syncthreads();
     const int64_t want = ((int64_t)keep * kSelSample + n - 1) / n * 5 / 4 + 8;
     const int r = want < kSelSample ? (int)want : kSelSample;
-    radix_select<kSelSample / kSelThreads>(smem_key, kSelSample, r, sh);
+    // the r-th largest sample's top 16 bits: a threshold at or below it
+    radix_select<kSelSample / kSelThreads>(smem_key, kSelSample, r, sh, 16);
     const uint32_t thr = sh.prefix;
     __syncthreads();
     const int m = gather(thr, true);
