@@ -173,6 +173,8 @@ __global__ void h2o_score_kernel(const SeqRow* __restrict__ rows, int n_heads, i
   if (k >= nk) return;
   const int j = keep_pos(k, L, mode, S, W);
   const int G = n_heads / n_kv_heads;
+  float* accj = acc + (size_t)b * acc_stride + j;
+  const float prev = *accj;  // in flight with the logit loads
   float sum = 0.0f;
   if ((G & 3) == 0 && ((reinterpret_cast<uintptr_t>(logits) | (uintptr_t)(stride * G * 4)) & 15) == 0) {
     // heads in groups of four (one float4 each), visited in head order; a
@@ -205,7 +207,7 @@ __global__ void h2o_score_kernel(const SeqRow* __restrict__ rows, int n_heads, i
       for (int i = 0; i < G; ++i) sum += __expf(lg[i] - s_lse[g * G + i]);
     }
   }
-  acc[(size_t)b * acc_stride + j] += sum / (float)n_heads;
+  *accj = prev + sum / (float)n_heads;
 }
 
 // ---------------------------------------------------------------------------

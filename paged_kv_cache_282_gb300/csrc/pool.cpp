@@ -1960,7 +1960,7 @@ pkv_status pkv_h2o_scores(pkv_pool* p, void* stream, int32_t n, const int32_t* i
   if (pkv_status r = p->staging.acquire(n * sizeof(SeqRow), &s)) return r;
   SeqRow* rows = (SeqRow*)s->host;
   for (int32_t i = 0; i < n; ++i) rows[i] = {ids[i], i, A.len[ids[i]], 0};
-  if (pkv_status r = Staging::upload(s, n * sizeof(SeqRow), st)) return r;
+  if (pkv_status r = p->staging.upload_overlapped(s, n * sizeof(SeqRow), st)) return r;
   const auto& c = p->cfg;
   if (pkv_status r = launch(p, PKV_KERNEL_H2O_SCORE, st, [&] {
         return launch_h2o_score((const SeqRow*)s->dev, n, c.n_heads, c.n_kv_heads, logits, logits_stride, lse, mode,
@@ -1993,7 +1993,7 @@ pkv_status select_keep(pkv_pool* p, void* stream, int32_t n, const int32_t* lens
   if (pkv_status r = p->staging.acquire(n * sizeof(SeqRow), &s)) return r;
   SeqRow* rows = (SeqRow*)s->host;
   for (int32_t i = 0; i < n; ++i) rows[i] = {-1, i, lens[i], 0};
-  if (pkv_status r = Staging::upload(s, n * sizeof(SeqRow), st)) return r;
+  if (pkv_status r = p->staging.upload_overlapped(s, n * sizeof(SeqRow), st)) return r;
   if (pkv_status r = launch(p, PKV_KERNEL_H2O_SELECT, st, [&] {
         return launch_h2o_select((const SeqRow*)s->dev, n, acc, acc_stride, pol, keep_idx, keep_stride, keep_count,
                                  p->buf.status, p->wait_limit_ns, st);
