@@ -278,6 +278,12 @@ struct SelShared {
   int k, n_cand, top, n_head;
 };
 
+// Slot of candidate i in the shared candidate arrays: the word index with its
+// low 3 bits XORed by bits 5-7.  A row of 32 consecutive candidates stays one
+// row (conflict-free linear reads), and a warp whose lanes write 8 consecutive
+// candidates each (stride 8) spreads over all 32 banks.
+__device__ __forceinline__ int cand_slot(int i) { return i ^ ((i >> 5) & 7); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
   return (uint32_t)__cvta_generic_to_shared(ptr);
 }
@@ -554,8 +560,8 @@ __device__ int gather_ring(const float* __restrict__ a, int n, uint32_t thr, boo
     const uint32_t key = t < head ? order_key(a[t]) : 0u;
     const uint32_t hb = __ballot_sync(kFull, t < head && key >= thr);
     if ((hb >> lane) & 1u) {
-      c_key[__popc(hb & lt)] = key;
-      c_pos[__popc(hb & lt)] = t;
+      c_key[cand_slot(__popc(hb & lt))] = key;
+      c_pos[cand_slot(__popc(hb & lt))] = t;
     }
     if (t == 0) sh.n_head = __popc(hb);
   }
@@ -616,15 +622,16 @@ __device__ int gather_ring(const float* __restrict__ a, int n, uint32_t thr, boo
     if (t == 0 && c + kSelRing < nch) ring_issue(a, n, head, c + kSelRing, ring, sh);
     if (flags == 0) continue;
     uint32_t sel = 0;  // bit u: key u qualifies
+    int below = 0, wcount = 0;  // candidates before this thread's within its warp, and the warp's count
+    if (__any_sync(kFull, maybe)) {
 #pragma unroll
-    for (int u = 0; u < P; ++u) sel |= (uint32_t)(i0 + u < cnt && order_key(x[u]) >= thr) << u;
-    // candidates before this thread's within its warp, and the warp's count
-    int below = 0, wcount = 0;
+      for (int u = 0; u < P; ++u) sel |= (uint32_t)(i0 + u < cnt && order_key(x[u]) >= thr) << u;
 #pragma unroll
-    for (int u = 0; u < P; ++u) {
-      const uint32_t bu = __ballot_sync(kFull, (sel >> u) & 1u);
-      below += __popc(bu & lt);
-      wcount += __popc(bu);
+      for (int u = 0; u < P; ++u) {
+        const uint32_t bu = __ballot_sync(kFull, (sel >> u) & 1u);
+        below += __popc(bu & lt);
+        wcount += __popc(bu);
+      }
     }
     if (lane == 0) sh.tot[w] = wcount;
     __syncthreads();
@@ -636,8 +643,8 @@ __device__ int gather_ring(const float* __restrict__ a, int n, uint32_t thr, boo
     for (int u = 0; u < P; ++u)
       if ((sel >> u) & 1u) {
         if (pos < kSelCap) {
-          c_key[pos] = order_key(x[u]);
-          c_pos[pos] = k0 + i0 + u;
+          c_key[cand_slot(pos)] = order_key(x[u]);
+          c_pos[cand_slot(pos)] = k0 + i0 + u;
         }
         ++pos;
       }
@@ -694,8 +701,8 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
       keep_count[b] = 0;
     }
   };
-  auto smem_key = [c_key](int i) { return c_key[i]; };
-  auto smem_pos = [c_pos](int i) { return c_pos[i]; };
+  auto smem_key = [c_key](int i) { return c_key[cand_slot(i)]; };
+  auto smem_pos = [c_pos](int i) { return c_pos[cand_slot(i)]; };
   // exact select and ordered output over the m (<= kSelCap) candidates in
   // shared memory, with as few keys per thread as cover m in one sweep
   auto select_candidates = [&](int m) {
@@ -726,7 +733,7 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
       for (int u = 0; u < U; ++u)
         sk[u] = order_key(a[(int)((int64_t)(threadIdx.x + u * kSelThreads) * n / kSelSample)]);
 #pragma unroll
-      for (int u = 0; u < U; ++u) c_key[threadIdx.x + u * kSelThreads] = sk[u];
+      for (int u = 0; u < U; ++u) c_key[cand_slot(threadIdx.x + u * kSelThreads)] = sk[u];
     }
     __syncthreads();
     const int64_t want = ((int64_t)keep * kSelSample + n - 1) / n * 5 / 4 + 8;
