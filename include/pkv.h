@@ -379,9 +379,11 @@ pkv_status pkv_timing_enable(pkv_pool* pool, int32_t kernel_mask);
 pkv_status pkv_timing_read(pkv_pool* pool, double* total_ms_out /* [PKV_KERNEL_COUNT] */,
                            int64_t* launches_out /* [PKV_KERNEL_COUNT] */);
 /* Bound (ns, within [1 ms, 60 s]; default 4 s) of every wait of the decode
- * kernel on its shared-memory stages.  A wait that runs out sets
- * PKV_ERR_TIMEOUT in the status word; the warp then drains its own copies in
- * flight (bounded again) and returns, leaving the context usable. */
+ * kernel on its shared-memory stages, and of the keep-set selection's waits
+ * on the score rows it streams into shared memory.  A wait that runs out sets
+ * PKV_ERR_TIMEOUT in the status word; the warp (decode) or block (selection;
+ * its keep_count is then 0) waits for its own copies in flight (bounded
+ * again) and returns, leaving the context usable. */
 pkv_status pkv_set_wait_limit(pkv_pool* pool, int64_t wait_limit_ns);
 /* Shared-prefix (cascade) decode ([PA] prefix sharing: a system prompt
  * reused by many requests, parallel sampling).  In decode over whole
@@ -404,6 +406,13 @@ pkv_status pkv_set_cascade(pkv_pool* pool, int32_t mode);
  * can only run out.  Outputs of that call are undefined; the status word
  * reports PKV_ERR_TIMEOUT. */
 pkv_status pkv_test_starve_next_decode(pkv_pool* pool, int32_t warp);
+/* Test hook for the same bound in the keep-set selection: in the next
+ * pkv_h2o_select / pkv_policy_select on this pool, the block of the first
+ * listed sequence never issues the first copy of its score row, so its wait
+ * can only run out (when that row is streamed at all: budget < length).
+ * That sequence's keep-set is undefined; the status word reports
+ * PKV_ERR_TIMEOUT. */
+pkv_status pkv_test_starve_next_select(pkv_pool* pool);
 
 /* Total kernel launches issued by this pool so far (all kernels). */
 pkv_status pkv_launch_count(const pkv_pool* pool, int64_t* out);

@@ -93,6 +93,7 @@ SIGNATURES = {
     "pkv_get_host_block_table": [c_void_p, c_int32, c_void_p, c_int32, c_void_p],
     "pkv_host_free_blocks": [c_void_p, c_void_p],
     "pkv_test_starve_next_decode": [c_void_p, c_int32],
+    "pkv_test_starve_next_select": [c_void_p],
     "pkv_last_error": [],
     "pkv_version": [],
 }

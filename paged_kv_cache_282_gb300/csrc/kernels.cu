@@ -276,6 +276,7 @@ struct SelShared {
   int tot[32];     // per-warp candidate counts of a sweep
   uint32_t prefix, mask;
   int k, n_cand, top, n_head;
+  int starve;  // test hook: the first chunk of this block's row is never issued
 };
 
 // Slot of candidate i in the shared candidate arrays: the word index with its
@@ -520,6 +521,7 @@ __device__ __forceinline__ void ring_issue(const float* a, int n, int head, int 
   const int st = c % kSelRing, k0 = head + c * kSelChunk;
   const int bulk = min(kSelChunk, n - k0) & ~3;
   const uint32_t bar = smem_u32(&sh.bar[st]);
+  if (c == 0 && sh.starve) return;  // test hook: this stage never completes
   if (bulk > 0) {
     mbar_expect_tx(bar, (uint32_t)bulk * 4u);
     bulk_load(smem_u32(ring + (size_t)st * kSelChunk), a + k0, (uint32_t)bulk * 4u, bar);
@@ -670,8 +672,10 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
                                                                  const float* __restrict__ acc, int64_t acc_stride,
                                                                  SelPolicy pol, int32_t* __restrict__ keep_idx,
                                                                  int64_t keep_stride, int32_t* __restrict__ keep_count,
-                                                                 int32_t* __restrict__ status, uint64_t wait_limit_ns) {
+                                                                 int32_t* __restrict__ status, uint64_t wait_limit_ns,
+                                                                 int starve_first) {
   __shared__ SelShared sh;
+  if (threadIdx.x == 0) sh.starve = starve_first && blockIdx.x == 0;
   extern __shared__ uint32_t cand[];  // kSelCap keys, kSelCap positions, then the ring
   uint32_t* c_key = cand;
   int32_t* c_pos = reinterpret_cast<int32_t*>(cand + kSelCap);
@@ -983,7 +987,7 @@ cudaError_t launch_compact_scores(const CompactSeq* seqs, int n, const int32_t* 
 
 cudaError_t launch_h2o_select(const SeqRow* rows, int n_seqs, const float* acc, int64_t acc_stride,
                               const SelPolicy& pol, int32_t* keep_idx, int64_t keep_stride, int32_t* keep_count,
-                              int32_t* status, uint64_t wait_limit_ns, cudaStream_t st) {
+                              int32_t* status, uint64_t wait_limit_ns, bool starve_first, cudaStream_t st) {
   if (n_seqs <= 0) return cudaSuccess;
   static std::atomic<uint64_t> attr_set{0};  // one bit per device
   const int smem = (int)kSelSmem;
@@ -996,7 +1000,7 @@ cudaError_t launch_h2o_select(const SeqRow* rows, int n_seqs, const float* acc, 
     attr_set.fetch_or(bit);
   }
   h2o_select_kernel<<<n_seqs, kSelThreads, smem, st>>>(rows, acc, acc_stride, pol, keep_idx, keep_stride, keep_count,
-                                                       status, wait_limit_ns);
+                                                       status, wait_limit_ns, starve_first ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -199,7 +199,7 @@ cudaError_t launch_compact_scores(const CompactSeq* seqs, int n, const int32_t* 
 
 cudaError_t launch_h2o_select(const SeqRow* rows, int n_seqs, const float* acc, int64_t acc_stride,
                               const SelPolicy& pol, int32_t* keep_idx, int64_t keep_stride, int32_t* keep_count,
-                              int32_t* status, uint64_t wait_limit_ns, cudaStream_t stream);
+                              int32_t* status, uint64_t wait_limit_ns, bool starve_first, cudaStream_t stream);
 
 }  // namespace pkv
 

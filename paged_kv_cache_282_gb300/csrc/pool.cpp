@@ -343,6 +343,7 @@ struct pkv_pool {
   int G = 1;
   uint64_t wait_limit_ns = 4000000000ull;  // bound of the decode kernel's waits
   int32_t starve_warp = -1;                // one-shot wait-expiry test hook
+  bool starve_select = false;              // one-shot wait-expiry test hook of the selection
   // Vectors reused by every decode plan: fresh ones each call would spend
   // most of the planning time faulting in new pages.
   std::unique_ptr<PlanCache, PlanCacheDeleter> plan_cache;
@@ -1994,9 +1995,11 @@ pkv_status select_keep(pkv_pool* p, void* stream, int32_t n, const int32_t* lens
   SeqRow* rows = (SeqRow*)s->host;
   for (int32_t i = 0; i < n; ++i) rows[i] = {-1, i, lens[i], 0};
   if (pkv_status r = p->staging.upload_overlapped(s, n * sizeof(SeqRow), st)) return r;
+  const bool starve = p->starve_select;
+  p->starve_select = false;
   if (pkv_status r = launch(p, PKV_KERNEL_H2O_SELECT, st, [&] {
         return launch_h2o_select((const SeqRow*)s->dev, n, acc, acc_stride, pol, keep_idx, keep_stride, keep_count,
-                                 p->buf.status, p->wait_limit_ns, st);
+                                 p->buf.status, p->wait_limit_ns, starve, st);
       }))
     return r;
   return Staging::release(s, st);
@@ -2082,6 +2085,12 @@ pkv_status pkv_test_starve_next_decode(pkv_pool* p, int32_t warp) {
   if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
   if (warp < 0) return fail(PKV_ERR_INVALID_ARG, "warp < 0");
   p->starve_warp = warp;
+  return PKV_OK;
+}
+
+pkv_status pkv_test_starve_next_select(pkv_pool* p) {
+  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  p->starve_select = true;
   return PKV_OK;
 }
 

@@ -337,6 +337,32 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     assert max_err(out, ref) <= TOL["bf16"] and lse_err(lse, ref_lse) <= 2e-3
 
 
+def test_select_bounded_wait_reports_timeout_and_context_survives():
+    """The first row's first streamed chunk is never copied: its bounded wait
+    runs out, the status word reports the expiry, that row's count is 0, and
+    the next selection on the same context is exact."""
+    lens = [40000, 3000, 70001]
+    stride = max(lens)
+    acc = workloads.h2o_scores_input(len(lens), stride, seed=21)
+    tw = Twin(workloads.small("bf16", lens=(1,)), 4, 1, 4)
+    cache = tw.cache
+    keep = torch.full((len(lens), 2048), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((len(lens),), -1, dtype=torch.int32, device="cuda")
+    _abi.check(cache.lib.pkv_set_wait_limit(cache.handle, 50_000_000))  # 50 ms
+    _abi.check(cache.lib.pkv_test_starve_next_select(cache.handle))
+    cache.h2o_select(lens, acc.cuda(), stride, 2048, 512, keep, 2048, cnt)
+    with pytest.raises(_abi.PKVError) as e:
+        cache.sync_status()
+    assert e.value.status == 6
+    assert int(cnt[0]) == 0
+    cache.h2o_select(lens, acc.cuda(), stride, 2048, 512, keep, 2048, cnt)
+    cache.sync_status()
+    k, c = keep.cpu().numpy(), cnt.cpu().numpy()
+    for b, L in enumerate(lens):
+        ref = oracle.h2o_select(L, 2048, 512, acc[b, :L].double().numpy())
+        assert c[b] == ref.size and np.array_equal(k[b, : c[b]], ref), b
+
+
 # --------------------------------------------------------------------------
 # H2O compaction: the keep-set becomes the whole sequence
 # --------------------------------------------------------------------------
