@@ -217,7 +217,9 @@ struct StagingSlot {
 };
 
 struct Staging {
-  static constexpr int kSlots = 4;
+  // Enough slots that a step's uploads (plan, per-sequence rows) reuse a slot
+  // only well after its kernel has run, so acquire does not stall the host.
+  static constexpr int kSlots = 16;
   StagingSlot slot[kSlots];
   int next = 0;
 
@@ -229,7 +231,7 @@ struct Staging {
       s.pending = false;
     }
     if (s.cap < bytes) {
-      size_t cap = std::max<size_t>(bytes, size_t(1) << 20);
+      size_t cap = std::max<size_t>(bytes, size_t(1) << 18);
       cap = (cap + 4095) & ~size_t(4095);
       if (s.host) PKV_CUDA(cudaFreeHost(s.host));
       if (s.dev) PKV_CUDA(cudaFree(s.dev));
@@ -572,6 +574,15 @@ struct PlanCache {
   std::vector<size_t> vstart;
   std::vector<Piece> ordered;
   std::vector<char> blob;
+  struct BgRecord {
+    int32_t vfirst, first_partial, flags;
+  };
+  struct WarpStartRec {
+    int64_t unit;
+    int32_t seg, seg_off;
+  };
+  std::vector<BgRecord> bg_rec;
+  std::vector<WarpStartRec> warp_start;
 };
 
 void destroy_plan_cache(PlanCache* c) { delete c; }
@@ -715,6 +726,118 @@ std::vector<Pairing> pair_shared_prefixes(const pkv_pool* p, int32_t n, const in
 
 // Fills plan = the pool's cached plan; the returned reference stays valid
 // until the next call.
+// The stream-K plan when every piece serves one sequence (no pairs, no group
+// prefixes, automatic partition), in one pass over the warps: the same plan
+// as the general path below, built without its intermediate piece lists.
+// Warp w takes the units [U w / TW, U (w + 1) / TW) of the segment list; a
+// (sequence, kv head) whose units span warps vfirst..vlast > vfirst writes
+// one partial record per warp, numbered in warp order from its first record;
+// each warp's pieces go straight to its physical slot.
+void plan_stream_k_single(pkv_pool* p, int32_t n, const int32_t* ids, PlanCache& cache, int TWmax) {
+  Plan& plan = cache.plan;
+  const int Hk = p->cfg.n_kv_heads;
+  const auto& A = p->alloc;
+  const std::vector<Seg>& segs = cache.segs;
+  const std::vector<int64_t>& bg_units = cache.bg_units;
+  const size_t nbg = (size_t)n * Hk;
+  int64_t U = 0;
+  for (const Seg& sg : segs) U += sg.hi - sg.lo;
+  const int TW = (int)std::min<int64_t>(TWmax, (U + kMinUnitsPerWarp - 1) / kMinUnitsPerWarp);
+  // per (sequence, kv head): its first warp, first record and merge item
+  // (flags: the merge item << 1, 0 when the output is written directly)
+  using BgRec = PlanCache::BgRecord;
+  std::vector<BgRec>& bgr = cache.bg_rec;
+  bgr.assign(nbg, BgRec{0, -1, 0});
+  auto warp_of = [&](int64_t u) { return (int32_t)(((u + 1) * TW - 1) / U); };
+  int next_partial = 0;
+  {
+    int64_t off = 0;
+    for (size_t bg = 0; bg < nbg; ++bg) {
+      const int64_t nu = bg_units[bg];
+      if (nu == 0) {
+        plan.empty.push_back({(int32_t)(bg / Hk), (int32_t)(bg % Hk)});
+        continue;
+      }
+      const int32_t v0 = warp_of(off), v1 = warp_of(off + nu - 1);
+      bgr[bg].vfirst = v0;
+      if (v1 > v0) {
+        bgr[bg].first_partial = next_partial;
+        bgr[bg].flags = (int32_t)plan.combine.size() << 1;
+        plan.combine.push_back({(int32_t)(bg / Hk), (int32_t)(bg % Hk), next_partial, v1 - v0 + 1});
+        next_partial += v1 - v0 + 1;
+      }
+      off += nu;
+    }
+  }
+  plan.n_partials = next_partial;
+  // each virtual warp's first unit, the segment holding it and its offset there
+  std::vector<PlanCache::WarpStartRec>& ws = cache.warp_start;
+  ws.resize(TW + 1);
+  {
+    size_t si = 0;
+    int64_t pos = 0;  // first unit of segment si
+    const int64_t q = U / TW, r = U % TW;
+    int64_t bound = 0, carry = 0;  // first unit of warp v: U v / TW, advanced without division
+    for (int v = 0; v <= TW; ++v) {
+      while (v < TW && si < segs.size() && pos + (segs[si].hi - segs[si].lo) <= bound) {
+        pos += segs[si].hi - segs[si].lo;
+        ++si;
+      }
+      ws[v] = {bound, (int32_t)si, (int32_t)(bound - pos)};
+      bound += q;
+      carry += r;
+      if (carry >= TW) {
+        carry -= TW;
+        ++bound;
+      }
+    }
+  }
+  // physical placement: virtual warp v runs in CTA v % C as its warp v / C
+  const int WPC = warps_per_cta(p, 1);
+  const int C = std::max(1, std::min(TW, TWmax / WPC));
+  const int slots = TW > 0 ? C * WPC : 0;
+  plan.pieces.clear();
+  plan.pieces.reserve(segs.size() + TW);
+  plan.warp_begin.assign(slots + 1, 0);
+  int phys = 0;
+  for (int cta = 0; cta < C; ++cta)
+    for (int wl = 0; wl < WPC; ++wl, ++phys) {
+      plan.warp_begin[phys] = (int32_t)plan.pieces.size();
+      const int v = wl * C + cta;
+      if (v >= TW) continue;
+      int64_t left = ws[v + 1].unit - ws[v].unit;
+      int32_t si = ws[v].seg;
+      int32_t lo = segs[si].lo + ws[v].seg_off;
+      while (left > 0) {
+        const Seg& sg = segs[si];
+        const int32_t hi = (int32_t)std::min<int64_t>(sg.hi, lo + left);
+        const BgRec& br = bgr[(size_t)sg.b * Hk + sg.g];
+        left -= hi - lo;
+        // the run ends with the warp's units or where the next segment is another (sequence, kv head)
+        const bool last = left == 0 || (size_t)si + 1 >= segs.size() || segs[si + 1].b != sg.b ||
+                          segs[si + 1].g != sg.g;
+        Piece pc;
+        pc.seq_slot = ids[sg.b];
+        pc.q_row = sg.b;
+        pc.kv_head = sg.g;
+        pc.lblk_begin = lo;
+        pc.lblk_end = hi;
+        pc.ctx_len = A.len[pc.seq_slot];
+        pc.out_index = br.first_partial >= 0 ? br.first_partial + (v - br.vfirst) : -1;
+        pc.flags = (last ? kPieceLastOfRun : 0) | br.flags;
+        pc.q_row1 = -1;
+        pc.out_index1 = -1;
+        pc.item1 = 0;
+        pc.pad = 0;
+        plan.pieces.push_back(pc);
+        if (left > 0) lo = segs[++si].lo;
+      }
+    }
+  plan.warp_begin[slots] = (int32_t)plan.pieces.size();
+  plan.total_warps = slots;
+  plan.ctas = TW > 0 ? C : 0;
+}
+
 Plan& build_plan(pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, int W, int num_splits) {
   const int Hk = p->cfg.n_kv_heads;
   const auto& A = p->alloc;
@@ -814,6 +937,16 @@ Plan& build_plan(pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, in
   plan.combine.clear();
   plan.warp_begin.clear();
   const int TWmax = max_total_warps(p, plan.nq);
+  if (num_splits <= 0 && plan.nq == 1 && plan.prefix_items.empty()) {
+    if (!segs.empty()) {
+      plan_stream_k_single(p, n, ids, cache, TWmax);
+    } else {  // nothing to read: every (sequence, kv head) has an empty keep-set
+      for (int32_t b = 0; b < n; ++b)
+        for (int g = 0; g < Hk; ++g) plan.empty.push_back({b, g});
+      plan.warp_begin.assign(1, 0);
+    }
+    return plan;
+  }
   auto piece_of = [&](const Seg& s, int32_t lo, int32_t hi) {
     Piece pc;
     pc.seq_slot = ids[s.b];
