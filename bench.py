@@ -477,24 +477,41 @@ def main():
     e2e = None
     if not args.no_e2e:
         n = len(setup.ids)
-        q_h = st.q.cpu().pin_memory()
-        k_h, v_h = st.k_new.cpu().pin_memory(), st.v_new.cpu().pin_memory()
+        # a step's inputs (queries, new K, new V) packed in one buffer: one copy each way
+        parts = (st.q, st.k_new, st.v_new)
+        assert all(t.dtype == st.q.dtype for t in parts)
+        sizes = [t.numel() for t in parts]
+
+        def packed(pin):
+            flat = torch.empty(sum(sizes), dtype=st.q.dtype, device="cpu" if pin else dev)
+            if pin:
+                flat = flat.pin_memory()
+            views, off = [], 0
+            for t, nel in zip(parts, sizes):
+                views.append(flat[off:off + nel].view(t.shape))
+                off += nel
+            return flat, views
+
+        in_h, (q_h, k_h, v_h) = packed(True)
+        q_h.copy_(st.q.cpu())
+        k_h.copy_(st.k_new.cpu())
+        v_h.copy_(st.v_new.cpu())
         out_h = [torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory() for _ in range(2)]
-        bufs = [(torch.empty_like(st.q), torch.empty_like(st.k_new), torch.empty_like(st.v_new),
-                 torch.empty_like(st.out)) for _ in range(2)]
+        bufs = []
+        for _ in range(2):
+            flat_d, (qd_, kd_, vd_) = packed(False)
+            bufs.append((flat_d, qd_, kd_, vd_, torch.empty_like(st.out)))
         cs, ds = torch.cuda.Stream(dev), torch.cuda.Stream(dev)  # uploads, downloads
         fetched = [torch.cuda.Event() for _ in range(2)]
         loaded = [torch.cuda.Event() for _ in range(2)]
         done = [torch.cuda.Event() for _ in range(2)]
 
         def upload(i):  # inputs of step i into buffer set i % 2, on the copy stream
-            qd, kd, vd, _ = bufs[i % 2]
+            flat_d = bufs[i % 2][0]
             with torch.cuda.stream(cs):
                 if i >= 2:
                     cs.wait_event(done[i % 2])  # step i - 2 read this set
-                qd.copy_(q_h, non_blocking=True)
-                kd.copy_(k_h, non_blocking=True)
-                vd.copy_(v_h, non_blocking=True)
+                flat_d.copy_(in_h, non_blocking=True)
                 loaded[i % 2].record(cs)
 
         def run(steps):
@@ -502,7 +519,7 @@ def main():
             for i in range(steps):
                 if i + 1 < steps:
                     upload(i + 1)
-                qd, kd, vd, od = bufs[i % 2]
+                _, qd, kd, vd, od = bufs[i % 2]
                 stream.wait_event(loaded[i % 2])
                 if i >= 2:
                     stream.wait_event(fetched[i % 2])  # step i - 2's output has left this buffer

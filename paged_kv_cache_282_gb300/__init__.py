@@ -26,8 +26,14 @@ def version() -> str:
 
 
 def _stream_ptr(stream) -> int:
+    """The CUDA stream handle for a call: `stream`, else torch's current stream
+    on the current device (read straight from torch's C layer when it offers
+    that, which costs far less per call than building a Stream object)."""
     import torch
     if stream is None:
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            return int(raw(torch._C._cuda_getDevice()))
         stream = torch.cuda.current_stream()
     return int(stream.cuda_stream)
 

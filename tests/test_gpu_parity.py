@@ -337,6 +337,17 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     assert max_err(out, ref) <= TOL["bf16"] and lse_err(lse, ref_lse) <= 2e-3
 
 
+def test_default_stream_is_torchs_current_stream():
+    """Calls without a stream argument run on torch's current stream,
+    including inside a torch.cuda.stream context."""
+    import paged_kv_cache_282_gb300 as pkv
+    side = torch.cuda.Stream()
+    assert pkv._stream_ptr(None) == torch.cuda.current_stream().cuda_stream
+    with torch.cuda.stream(side):
+        assert pkv._stream_ptr(None) == side.cuda_stream
+    assert pkv._stream_ptr(side) == side.cuda_stream
+
+
 def test_select_bounded_wait_reports_timeout_and_context_survives():
     """The first row's first streamed chunk is never copied: its bounded wait
     runs out, the status word reports the expiry, that row's count is 0, and
