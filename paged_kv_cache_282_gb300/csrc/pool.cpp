@@ -583,6 +583,10 @@ struct PlanCache {
   };
   std::vector<BgRecord> bg_rec;
   std::vector<WarpStartRec> warp_start;
+  struct SegRecord {
+    int32_t v0, runs, rec0, rec1;
+  };
+  std::vector<SegRecord> seg_rec;
 };
 
 void destroy_plan_cache(PlanCache* c) { delete c; }
@@ -838,6 +842,147 @@ void plan_stream_k_single(pkv_pool* p, int32_t n, const int32_t* ids, PlanCache&
   plan.ctas = TW > 0 ? C : 0;
 }
 
+// The same one-pass construction for plans with sequence pairs (whole
+// keep-sets, no group prefixes): every (sequence, kv head) has at most one
+// pair segment, shared with its partner, and one segment of its own (the
+// remainder past the shared blocks, or its whole context).  A segment spans
+// the warps v0 .. v0 + runs - 1, one run in each.  A pair segment's runs
+// write one record per sequence; a remainder's always do (it never holds
+// all of its sequence's units); an unpaired segment's only when it spans
+// several warps.  A sequence's records are its pair runs' and then its own
+// segment's, in warp order -- the order of the general path.
+void plan_stream_k_pairs(pkv_pool* p, int32_t n, const int32_t* ids, PlanCache& cache, int TWmax) {
+  Plan& plan = cache.plan;
+  const int Hk = p->cfg.n_kv_heads;
+  const auto& A = p->alloc;
+  const std::vector<Seg>& segs = cache.segs;
+  const std::vector<int64_t>& bg_units = cache.bg_units;
+  const size_t nbg = (size_t)n * Hk, ns = segs.size();
+  int64_t U = 0;
+  for (const Seg& sg : segs) U += sg.hi - sg.lo;
+  const int TW = (int)std::min<int64_t>(TWmax, (U + kMinUnitsPerWarp - 1) / kMinUnitsPerWarp);
+  auto warp_of = [&](int64_t u) { return (int32_t)(((u + 1) * TW - 1) / U); };
+  // per segment: first warp, number of runs, and its records' first index
+  // for the first and the second sequence
+  using SegRec = PlanCache::SegRecord;
+  std::vector<SegRec>& sr = cache.seg_rec;
+  sr.resize(ns);
+  std::vector<int32_t>& pair_runs = cache.cursor;  // per (sequence, kv head): runs of its pair segment
+  std::vector<int32_t>& own_runs = cache.n_part;   // runs of its own segment that write records
+  pair_runs.assign(nbg, 0);
+  own_runs.assign(nbg, 0);
+  {
+    int64_t off = 0;
+    for (size_t k = 0; k < ns; ++k) {
+      const Seg& sg = segs[k];
+      const int64_t len = sg.hi - sg.lo;
+      const int32_t v0 = warp_of(off), runs = warp_of(off + len - 1) - v0 + 1;
+      sr[k] = {v0, runs, -1, -1};
+      const size_t bg = (size_t)sg.b * Hk + sg.g;
+      if (sg.b1 >= 0) {
+        pair_runs[bg] = runs;
+        pair_runs[(size_t)sg.b1 * Hk + sg.g] = runs;
+      } else if (runs > 1 || len != bg_units[bg]) {
+        own_runs[bg] = runs;
+      }
+      off += len;
+    }
+  }
+  std::vector<int32_t>& first_partial = cache.first_partial;
+  std::vector<int32_t>& item_of = cache.item_of;
+  first_partial.assign(nbg, -1);
+  item_of.assign(nbg, -1);
+  int next_partial = 0;
+  for (size_t bg = 0; bg < nbg; ++bg) {
+    const int32_t np = pair_runs[bg] + own_runs[bg];
+    if (bg_units[bg] == 0) {
+      plan.empty.push_back({(int32_t)(bg / Hk), (int32_t)(bg % Hk)});
+    } else if (np > 0) {
+      first_partial[bg] = next_partial;
+      item_of[bg] = (int32_t)plan.combine.size();
+      plan.combine.push_back({(int32_t)(bg / Hk), (int32_t)(bg % Hk), next_partial, np});
+      next_partial += np;
+    }
+  }
+  plan.n_partials = next_partial;
+  for (size_t k = 0; k < ns; ++k) {
+    const Seg& sg = segs[k];
+    const size_t bg = (size_t)sg.b * Hk + sg.g;
+    if (sg.b1 >= 0) {
+      sr[k].rec0 = first_partial[bg];
+      sr[k].rec1 = first_partial[(size_t)sg.b1 * Hk + sg.g];
+    } else if (own_runs[bg] > 0) {
+      sr[k].rec0 = first_partial[bg] + pair_runs[bg];
+    }
+  }
+  // each virtual warp's first unit, the segment holding it and its offset there
+  std::vector<PlanCache::WarpStartRec>& ws = cache.warp_start;
+  ws.resize(TW + 1);
+  {
+    size_t si = 0;
+    int64_t pos = 0;
+    const int64_t q = U / TW, r = U % TW;
+    int64_t bound = 0, carry = 0;
+    for (int v = 0; v <= TW; ++v) {
+      while (v < TW && si < ns && pos + (segs[si].hi - segs[si].lo) <= bound) {
+        pos += segs[si].hi - segs[si].lo;
+        ++si;
+      }
+      ws[v] = {bound, (int32_t)si, (int32_t)(bound - pos)};
+      bound += q;
+      carry += r;
+      if (carry >= TW) {
+        carry -= TW;
+        ++bound;
+      }
+    }
+  }
+  const int WPC = warps_per_cta(p, 2);
+  const int C = std::max(1, std::min(TW, TWmax / WPC));
+  const int slots = TW > 0 ? C * WPC : 0;
+  plan.pieces.clear();
+  plan.pieces.reserve(ns + TW);
+  plan.warp_begin.assign(slots + 1, 0);
+  int phys = 0;
+  for (int cta = 0; cta < C; ++cta)
+    for (int wl = 0; wl < WPC; ++wl, ++phys) {
+      plan.warp_begin[phys] = (int32_t)plan.pieces.size();
+      const int v = wl * C + cta;
+      if (v >= TW) continue;
+      int64_t left = ws[v + 1].unit - ws[v].unit;
+      int32_t si = ws[v].seg;
+      int32_t lo = segs[si].lo + ws[v].seg_off;
+      while (left > 0) {
+        const Seg& sg = segs[si];
+        const SegRec& rc = sr[si];
+        const int32_t hi = (int32_t)std::min<int64_t>(sg.hi, lo + left);
+        const int32_t j = v - rc.v0;  // this warp's run of the segment
+        left -= hi - lo;
+        const bool last = left == 0 || (size_t)si + 1 >= ns || segs[si + 1].b != sg.b ||
+                          segs[si + 1].g != sg.g || segs[si + 1].b1 != sg.b1;
+        Piece pc;
+        pc.seq_slot = ids[sg.b];
+        pc.q_row = sg.b;
+        pc.kv_head = sg.g;
+        pc.lblk_begin = lo;
+        pc.lblk_end = hi;
+        pc.ctx_len = A.len[pc.seq_slot];
+        pc.out_index = rc.rec0 >= 0 ? rc.rec0 + j : -1;
+        pc.flags = (last ? kPieceLastOfRun : 0) |
+                   (rc.rec0 >= 0 ? item_of[(size_t)sg.b * Hk + sg.g] << 1 : 0);
+        pc.q_row1 = sg.b1;
+        pc.out_index1 = sg.b1 >= 0 ? rc.rec1 + j : -1;
+        pc.item1 = sg.b1 >= 0 ? item_of[(size_t)sg.b1 * Hk + sg.g] : 0;
+        pc.pad = 0;
+        plan.pieces.push_back(pc);
+        if (left > 0) lo = segs[++si].lo;
+      }
+    }
+  plan.warp_begin[slots] = (int32_t)plan.pieces.size();
+  plan.total_warps = slots;
+  plan.ctas = TW > 0 ? C : 0;
+}
+
 Plan& build_plan(pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, int W, int num_splits) {
   const int Hk = p->cfg.n_kv_heads;
   const auto& A = p->alloc;
@@ -937,6 +1082,10 @@ Plan& build_plan(pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, in
   plan.combine.clear();
   plan.warp_begin.clear();
   const int TWmax = max_total_warps(p, plan.nq);
+  if (num_splits <= 0 && plan.nq == 2 && plan.prefix_items.empty() && !segs.empty()) {
+    plan_stream_k_pairs(p, n, ids, cache, TWmax);
+    return plan;
+  }
   if (num_splits <= 0 && plan.nq == 1 && plan.prefix_items.empty()) {
     if (!segs.empty()) {
       plan_stream_k_single(p, n, ids, cache, TWmax);
