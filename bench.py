@@ -570,7 +570,8 @@ def main():
     dec_ms += ktimes["prefix_decode"][0]
     dec_avg = dec_ms / max(dec_n, 1)
     achieved = step_bytes / (dec_avg * 1e-3) / 1e9 if dec_n else None
-    traffic = profiled_traffic("decode_tc.cu", label)
+    # the captures in profiles/ ran with the default shared-prefix mode (1)
+    traffic = profiled_traffic("decode_tc.cu", label) if cascade == 1 else None
     decode_share = round(dec_ms / max(ms, 1e-9), 4)
     cpu = None
     if not args.no_cpu_baseline and ws == 1:
