@@ -413,6 +413,20 @@ pkv_status pkv_test_starve_next_decode(pkv_pool* pool, int32_t warp);
  * That sequence's keep-set is undefined; the status word reports
  * PKV_ERR_TIMEOUT. */
 pkv_status pkv_test_starve_next_select(pkv_pool* pool);
+/* Test hooks for the decode planner (host only, no device work).
+ * pkv_test_set_geometry: the launch geometry a host-only pool plans for --
+ * SMs, warps per CTA of the one-sequence and of the two-sequence kernel (one
+ * CTA per SM each) -- and the GQA group size.  pkv_test_plan_bytes: builds
+ * the plan of a decode call (the same arguments) and copies its uploaded
+ * bytes into `out` (cap bytes; *size gets the length) and into info[4] the
+ * physical warps, CTAs, partial records and sequences per warp; general != 0
+ * forces the general planner instead of the one-pass paths, which must give
+ * the same bytes. */
+pkv_status pkv_test_set_geometry(pkv_pool* pool, int32_t num_sms, int32_t warps_per_cta, int32_t pair_warps_per_cta,
+                                 int32_t group);
+pkv_status pkv_test_plan_bytes(pkv_pool* pool, int32_t n_seqs, const int32_t* seq_ids, int32_t mask_mode,
+                               int32_t num_sinks, int32_t window, int32_t num_splits, int32_t general, void* out,
+                               size_t cap, size_t* size, int32_t* info);
 
 /* Total kernel launches issued by this pool so far (all kernels). */
 pkv_status pkv_launch_count(const pkv_pool* pool, int64_t* out);

@@ -94,6 +94,9 @@ SIGNATURES = {
     "pkv_host_free_blocks": [c_void_p, c_void_p],
     "pkv_test_starve_next_decode": [c_void_p, c_int32],
     "pkv_test_starve_next_select": [c_void_p],
+    "pkv_test_set_geometry": [c_void_p, c_int32, c_int32, c_int32, c_int32],
+    "pkv_test_plan_bytes": [c_void_p, c_int32, c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p,
+                            c_size_t, c_void_p, c_void_p],
     "pkv_last_error": [],
     "pkv_version": [],
 }

@@ -346,6 +346,7 @@ struct pkv_pool {
   uint64_t wait_limit_ns = 4000000000ull;  // bound of the decode kernel's waits
   int32_t starve_warp = -1;                // one-shot wait-expiry test hook
   bool starve_select = false;              // one-shot wait-expiry test hook of the selection
+  bool general_plan = false;               // test hook: plan every decode on the general path
   // Vectors reused by every decode plan: fresh ones each call would spend
   // most of the planning time faulting in new pages.
   std::unique_ptr<PlanCache, PlanCacheDeleter> plan_cache;
@@ -1082,11 +1083,11 @@ Plan& build_plan(pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, in
   plan.combine.clear();
   plan.warp_begin.clear();
   const int TWmax = max_total_warps(p, plan.nq);
-  if (num_splits <= 0 && plan.nq == 2 && plan.prefix_items.empty() && !segs.empty()) {
+  if (!p->general_plan && num_splits <= 0 && plan.nq == 2 && plan.prefix_items.empty() && !segs.empty()) {
     plan_stream_k_pairs(p, n, ids, cache, TWmax);
     return plan;
   }
-  if (num_splits <= 0 && plan.nq == 1 && plan.prefix_items.empty()) {
+  if (!p->general_plan && num_splits <= 0 && plan.nq == 1 && plan.prefix_items.empty()) {
     if (!segs.empty()) {
       plan_stream_k_single(p, n, ids, cache, TWmax);
     } else {  // nothing to read: every (sequence, kv head) has an empty keep-set
@@ -2373,6 +2374,40 @@ pkv_status pkv_test_starve_next_decode(pkv_pool* p, int32_t warp) {
 pkv_status pkv_test_starve_next_select(pkv_pool* p) {
   if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
   p->starve_select = true;
+  return PKV_OK;
+}
+
+pkv_status pkv_test_set_geometry(pkv_pool* p, int32_t num_sms, int32_t wpc, int32_t wpc2, int32_t group) {
+  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  if (p->device) return fail(PKV_ERR_INVALID_ARG, "the geometry of a device pool is its GPU's");
+  if (num_sms < 1 || wpc < 1 || wpc2 < 1 || group < 1) return fail(PKV_ERR_INVALID_ARG, "geometry must be positive");
+  p->num_sms = num_sms;
+  p->tc_warps_per_cta = wpc;
+  p->tc2_warps_per_cta = wpc2;
+  p->tc_ctas_per_sm = p->tc2_ctas_per_sm = 1;
+  p->G = group;
+  return PKV_OK;
+}
+
+pkv_status pkv_test_plan_bytes(pkv_pool* p, int32_t n, const int32_t* ids, int32_t mode, int32_t S, int32_t W,
+                               int32_t num_splits, int32_t general, void* out, size_t cap, size_t* size,
+                               int32_t* info) {
+  if (!p || !size || !info) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  if (pkv_status r = check_seq_list(p, n, ids)) return r;
+  if (n < 1) return fail(PKV_ERR_INVALID_ARG, "no sequences");
+  if (!valid_mask(mode, S, W)) return fail(PKV_ERR_INVALID_ARG, "invalid mask %d (%d, %d)", mode, S, W);
+  if (num_splits < 0) return fail(PKV_ERR_INVALID_ARG, "num_splits < 0");
+  p->general_plan = general != 0;
+  Plan& plan = build_plan(p, n, ids, mode, S, W, num_splits);
+  p->general_plan = false;
+  const PlanLayout L = plan_layout(plan, warps_per_cta(p, plan.nq), 0);
+  *size = L.bytes;
+  info[0] = plan.total_warps;
+  info[1] = plan.ctas;
+  info[2] = plan.n_partials;
+  info[3] = plan.nq;
+  if (cap < L.bytes || !out) return fail(PKV_ERR_INVALID_ARG, "plan of %zu bytes > cap %zu", L.bytes, cap);
+  plan_write(plan, L, (char*)out);
   return PKV_OK;
 }
 

@@ -287,3 +287,51 @@ def test_compaction_refusals_leave_state_unchanged(pkv):
         assert (lib.block_table(a).tolist(), lib.block_table(b).tolist(), lib.stats()["free_blocks"]) == before
     lib.seq_compact([b], [17])
     assert lib.seq_len(b) == 17 and len(lib.block_table(b)) == 2
+
+
+def _plan(pkv, c, ids, mode, S, W, splits, general):
+    import ctypes
+    buf = ctypes.create_string_buffer(16 << 20)
+    size = ctypes.c_size_t()
+    info = (ctypes.c_int32 * 4)()
+    arr = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    pkv._abi.check(c.lib.pkv_test_plan_bytes(c._h, arr.size, arr.ctypes.data_as(ctypes.c_void_p), mode, S, W, splits,
+                                             general, buf, len(buf), ctypes.byref(size), info))
+    return buf.raw[: size.value], tuple(info)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_one_pass_planner_matches_general_planner(pkv, seed):
+    """The one-pass decode planner (one sequence per warp; sequence pairs)
+    writes the same plan bytes as the general planner: random batches with
+    empty and short sequences, forked pairs with private suffixes, every mask,
+    two GQA widths and both warp geometries."""
+    rng = random.Random(seed)
+    Hk = (2, 8)[seed % 2]
+    c = pkv.PagedKVCache(60000, Hk * 4, Hk, 128, 300, 1300, host_only=True, alloc_seed=seed)
+    pkv._abi.check(c.lib.pkv_test_set_geometry(c._h, 152, 16 if seed % 3 == 0 else 12, 12, 4))
+    ids = []
+    if seed % 2:  # parents forked once, then private suffixes on some of each
+        for _ in range(rng.randint(2, 40)):
+            s = c.seq_add()
+            c.reserve_slots([s], rng.randint(1, 3000))
+            f = c.seq_fork(s)
+            ids += [s, f]
+            for x in (s, f):
+                if rng.random() < 0.7:
+                    c.reserve_slots([x], rng.randint(1, 700))
+    else:
+        for _ in range(rng.randint(1, 150)):
+            s = c.seq_add()
+            L = 0 if rng.random() < 0.1 else rng.randint(1, 9000 if rng.random() < 0.8 else 40)
+            if L:
+                c.reserve_slots([s], L)
+            ids.append(s)
+    pairs_seen = False
+    for mode, S, W in [(0, 0, 0), (1, 0, rng.randint(0, 3000)), (2, rng.randint(0, 40), rng.randint(0, 3000)),
+                       (2, 0, 0)]:
+        fast, info = _plan(pkv, c, ids, mode, S, W, 0, 0)
+        general, ginfo = _plan(pkv, c, ids, mode, S, W, 0, 1)
+        assert info == ginfo and fast == general, (mode, S, W)
+        pairs_seen |= info[3] == 2
+    assert pairs_seen == bool(seed % 2)
