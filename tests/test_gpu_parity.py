@@ -337,6 +337,35 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     assert max_err(out, ref) <= TOL["bf16"] and lse_err(lse, ref_lse) <= 2e-3
 
 
+@pytest.mark.parametrize("pad", [0, 5])
+def test_select_chunk_boundaries(pad):
+    """Ranked lengths on and around the streamed gather's 8192-key chunks,
+    the last ragged chunk under 16 bytes, and the sampled path's 16384-key
+    threshold, on row starts aligned to 128 bytes (pad 0) and not (pad 5):
+    keep-sets exact for plain H2O and the combined rule."""
+    base = [16384, 16385, 16386, 24575, 24576, 24577, 24579, 32768 + 3, 40961, 65536]
+    lens = [L + 512 for L in base]  # ranked part [0, L - 512) hits the sizes above
+    stride = max(lens) + pad
+    acc = workloads.h2o_scores_input(len(lens), stride, seed=31 + pad)
+    cache = Twin(workloads.small("bf16", lens=(1,)), 4, 1, 4).cache
+    keep = torch.full((len(lens), 2048), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((len(lens),), -1, dtype=torch.int32, device="cuda")
+    cache.h2o_select(lens, acc.cuda(), stride, 2048, 512, keep, 2048, cnt)
+    cache.sync_status()
+    k, c = keep.cpu().numpy(), cnt.cpu().numpy()
+    for b, L in enumerate(lens):
+        ref = oracle.h2o_select(L, 2048, 512, acc[b, :L].double().numpy())
+        assert c[b] == ref.size and np.array_equal(k[b, : c[b]], ref), (b, L)
+    width = 4 + 256 + 4000
+    keep2 = torch.full((len(lens), width), -7, dtype=torch.int32, device="cuda")
+    cache.policy_select(lens, acc.cuda(), stride, 4, 256, 4000, keep2, width, cnt)
+    cache.sync_status()
+    k, c = keep2.cpu().numpy(), cnt.cpu().numpy()
+    for b, L in enumerate(lens):
+        ref = oracle.policy_select(L, 4, 256, 4000, acc[b, :L].double().numpy())
+        assert c[b] == ref.size and np.array_equal(k[b, : c[b]], ref), (b, L)
+
+
 def test_default_stream_is_torchs_current_stream():
     """Calls without a stream argument run on torch's current stream,
     including inside a torch.cuda.stream context."""
