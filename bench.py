@@ -281,14 +281,27 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+KERNEL_HEADERS = ("async_copy.cuh", "pkv_internal.h")
+
+
+def kernel_source_sha(kernel_file: str) -> str:
+    """sha256 of a kernel file followed by the library headers it includes."""
+    csrc = os.path.join(ROOT, "paged_kv_cache_282_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in (kernel_file,) + KERNEL_HEADERS:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def profiled_traffic(kernel_file: str, workload: str):
     """DRAM bytes per launch recorded from an ncu capture in profiles/, valid
-    only while the kernel source is unchanged (sha256 recorded beside it)."""
+    only while the kernel source is unchanged (its sha256, with the headers
+    it includes, recorded beside it)."""
     path = os.path.join(ROOT, "profiles", f"decode_tc_{workload}.md")
-    src = os.path.join(ROOT, "paged_kv_cache_282_gb300", "csrc", kernel_file)
     try:
         text = open(path).read()
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        sha = kernel_source_sha(kernel_file)
         m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
         m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
         if m_sha and m_tr and m_sha.group(1) == sha:

@@ -31,7 +31,8 @@ def nvcc() -> str:
 
 def _deps():
     files = [os.path.join(CSRC, s) for s in SOURCES]
-    files += [os.path.join(CSRC, "pkv_internal.h"), os.path.join(INCLUDE, "pkv.h"), __file__]
+    files += [os.path.join(CSRC, "pkv_internal.h"), os.path.join(CSRC, "async_copy.cuh"), os.path.join(INCLUDE, "pkv.h"),
+              __file__]
     return files
 
 

@@ -16,6 +16,7 @@
 #include <algorithm>
 #include <atomic>
 
+#include "async_copy.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -285,53 +286,6 @@ struct SelShared {
 // candidates each (stride 8) spreads over all 32 banks.
 __device__ __forceinline__ int cand_slot(int i) { return i ^ ((i >> 5) & 7); }
 
-__device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
-  return (uint32_t)__cvta_generic_to_shared(ptr);
-}
-__device__ __forceinline__ uint64_t global_timer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_inval(uint32_t bar) {
-  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Wait for phase `parity` of an mbarrier, for at most limit_ns.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63) == 0 && global_timer_ns() - t0 > limit_ns) return false;
-  }
-}
-// 1-D bulk copy global -> shared; both addresses and the size 16-byte multiples.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
-
 // Histogram of digit (key >> shift) & 255 over the keys i < m whose bits under
 // `mask` equal `prefix`.  Scores are often equal (zero outside the keep-set,
 // or of one magnitude), so lanes of a warp holding the same digit are
@@ -520,11 +474,11 @@ __device__ __forceinline__ int ring_head(const float* a, int n) {
 __device__ __forceinline__ void ring_issue(const float* a, int n, int head, int c, float* ring, SelShared& sh) {
   const int st = c % kSelRing, k0 = head + c * kSelChunk;
   const int bulk = min(kSelChunk, n - k0) & ~3;
-  const uint32_t bar = smem_u32(&sh.bar[st]);
+  const uint32_t bar = smem_addr(&sh.bar[st]);
   if (c == 0 && sh.starve) return;  // test hook: this stage never completes
   if (bulk > 0) {
     mbar_expect_tx(bar, (uint32_t)bulk * 4u);
-    bulk_load(smem_u32(ring + (size_t)st * kSelChunk), a + k0, (uint32_t)bulk * 4u, bar);
+    bulk_load(smem_addr(ring + (size_t)st * kSelChunk), a + k0, (uint32_t)bulk * 4u, bar);
   } else {
     mbar_arrive(bar);
   }
@@ -533,7 +487,7 @@ __device__ __forceinline__ void ring_issue(const float* a, int n, int head, int 
 // barrier of the whole block must separate this from the first wait.
 __device__ void ring_prime(const float* a, int n, float* ring, SelShared& sh) {
   const int head = ring_head(a, n), nch = (n - head + kSelChunk - 1) / kSelChunk;
-  for (int i = 0; i < kSelRing; ++i) mbar_init(smem_u32(&sh.bar[i]), 1);
+  for (int i = 0; i < kSelRing; ++i) mbar_init(smem_addr(&sh.bar[i]), 1);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   for (int c = 0; c < min(nch, kSelRing); ++c) ring_issue(a, n, head, c, ring, sh);
@@ -573,12 +527,12 @@ __device__ int gather_ring(const float* __restrict__ a, int n, uint32_t thr, boo
   bool ok = true;
   if (t == 0) {
     if (!primed) ring_prime(a, n, ring, sh);
-    if (nch > 0) ok = mbar_wait(smem_u32(&sh.bar[0]), 0u, limit_ns);
+    if (nch > 0) ok = mbar_wait(smem_addr(&sh.bar[0]), 0u, limit_ns);
   }
   auto drain = [&](int first, int end) {  // thread 0: chunks [first, end) were issued, not consumed
     if (t == 0)
       for (int v = first; v < end; ++v)
-        mbar_wait(smem_u32(&sh.bar[v % kSelRing]), (uint32_t)((v / kSelRing) & 1), limit_ns);
+        mbar_wait(smem_addr(&sh.bar[v % kSelRing]), (uint32_t)((v / kSelRing) & 1), limit_ns);
     __syncthreads();
   };
   if (__syncthreads_or(ok ? 0 : 1)) {
@@ -614,7 +568,7 @@ __device__ int gather_ring(const float* __restrict__ a, int n, uint32_t thr, boo
 #pragma unroll
     for (int u = 0; u < P; ++u) maybe |= !(x[u] < thr_f);
     if (t == 0 && c + 1 < nch)
-      ok = mbar_wait(smem_u32(&sh.bar[(c + 1) % kSelRing]), (uint32_t)(((c + 1) / kSelRing) & 1), limit_ns);
+      ok = mbar_wait(smem_addr(&sh.bar[(c + 1) % kSelRing]), (uint32_t)(((c + 1) / kSelRing) & 1), limit_ns);
     // every thread has read stage st; any candidate, or a copy that timed out?
     const int flags = __syncthreads_or((maybe ? 1 : 0) | (ok ? 0 : 0x10000));
     if (flags & 0x10000) {
@@ -654,7 +608,7 @@ __device__ int gather_ring(const float* __restrict__ a, int n, uint32_t thr, boo
   }
   __syncthreads();
   if (t == 0)
-    for (int i = 0; i < kSelRing; ++i) mbar_inval(smem_u32(&sh.bar[i]));
+    for (int i = 0; i < kSelRing; ++i) mbar_inval(smem_addr(&sh.bar[i]));
   __syncthreads();
   return filled;
 }
