@@ -24,8 +24,8 @@
  *   [SO]  "系统优化" (threethreeliu.top, knowledge-inference-optimization-
  *         memory): sliding window / StreamingLLM keep-set, H2O evict_tokens.
  *
- * Readings where the pages are silent or garbled are listed in the design doc and
- * restated next to the code that adopts them.
+ * Where the pages are silent or garbled, the reading taken is stated next to
+ * the code that adopts it.
  */
 #include <math.h>
 #include <pthread.h>

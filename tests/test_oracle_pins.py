@@ -59,7 +59,8 @@ def test_kv_bytes_per_token_llama3_8b():
 
 def test_kv_cache_gb_printouts_are_twice_the_formula():
     """The page's printed comments are exactly 2x what its own formula
-    returns; the formula is taken as authoritative (the design doc readings)."""
+    returns; the formula is taken as authoritative (the printouts are read as
+    a slip in the page)."""
     g = _read_golden_kv()
     f8k = oracle.kv_cache_gib(32, 8, 128, 8192)
     f128k = oracle.kv_cache_gib(32, 8, 128, 131072)
