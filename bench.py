@@ -70,10 +70,11 @@ class Setup:
     """Pool + sequences of one workload on one GPU, filled from the seeded
     generator through the library's own append path."""
 
-    def __init__(self, wl, dev, headroom_blocks: int | None = None):
+    def __init__(self, wl, dev, headroom_blocks: int | None = None, extra_seqs: int = 0):
         from paged_kv_cache_282_gb300 import PagedKVCache
         self.wl, self.dev = wl, dev
         self.extra = {}
+        self.extra_seqs = extra_seqs  # sequence ids left free (forks of the workload's sequences)
         name = wl.name
         if name == "prefix_append":
             self._setup_prefix(PagedKVCache)
@@ -130,8 +131,8 @@ class Setup:
         per_seq = 1 + (W + 15) // 16 + 2 + chunk // 16 + 2
         maxb = max((L + 15) // 16 for L in wl.lens) + 4
         self.cache = c = PagedKVCache(len(wl.lens) * per_seq + 64, wl.n_heads, wl.n_kv_heads, wl.head_dim,
-                                      len(wl.lens), maxb, kv_dtype=wl.kv_dtype, alloc_seed=wl.seed,
-                                      device=self.dev)
+                                      len(wl.lens) + self.extra_seqs, maxb, kv_dtype=wl.kv_dtype,
+                                      alloc_seed=wl.seed, device=self.dev)
         zeros = torch.zeros((1, chunk, wl.n_kv_heads, wl.head_dim), dtype=torch.bfloat16, device=self.dev)
         self.ids = []
         for b, L in enumerate(wl.lens):
@@ -400,6 +401,9 @@ def main():
                     help="shared-prefix decode: 0 off, 1 sequence pairs, 2 group prefixes (multi-query kernel)")
     ap.add_argument("--time-kernels", action="store_true",
                     help="bracket every kernel (not only decode) with events; adds gaps to the step")
+    ap.add_argument("--op", default="step", choices=["step", "compact", "swap"],
+                    help="step: the decode step (default); compact: H2O compaction of the streaming workload's "
+                         "sequences to their keep-sets; swap: every sequence to pinned host memory and back")
     args = ap.parse_args()
 
     wl = workloads.ALL[args.workload]()
@@ -423,6 +427,10 @@ def main():
     torch.cuda.set_device(dev)
     import paged_kv_cache_282_gb300 as pkv
     pkv.load()
+    if args.op != "step":
+        if ws > 1:
+            raise SystemExit("--op compact / swap run on one GPU")
+        return run_op(args, wl, label, dev)
 
     setup = Setup(wl, dev)
     cascade = 0 if args.no_cascade else args.cascade
@@ -627,6 +635,130 @@ def main():
         "cpu_baseline": cpu,
         "clocks": clk,
     }
+    print(json.dumps(line))
+
+
+def run_op(args, wl, label, dev):
+    """Throughput of the NEXT-row data movers on a workload-sized pool.
+
+    compact: the streaming workload's sequences are forked (sharing every
+    block) and each fork is compacted to its H2O keep-set (2048 positions
+    out of the sink + window set); per round the kept rows are read and
+    written once (K and V, + scales), algorithmic bytes = 2 x the kept rows'
+    bytes, against the HBM copy peak.  The forks are freed between rounds;
+    their score arrays are not compacted (no acc argument).  The timed call
+    includes the host's table rewrite (the dropped entries of a long, mostly
+    evicted sequence become -1) and its upload.
+    swap: every sequence of the workload moves to pinned host memory and
+    back; bytes per direction = the blocks' K/V (+ scales); the copies run
+    through the host pool's device-mapped address, so the bound is the
+    host link (no measured peak for it: peak null)."""
+    import torch
+    from paged_kv_cache_282_gb300 import BLOCK_SIZE
+    if args.op == "compact" and wl.name != "streaming_h2o":
+        wl = workloads.streaming_h2o()
+        label = wl.name
+    setup = Setup(wl, dev, extra_seqs=len(wl.lens) if args.op == "compact" else 0)
+    c = setup.cache
+    stream = torch.cuda.current_stream(dev)
+    rounds = max(3, min(args.steps, 50))
+    peak, peak_kind = hbm_peak()
+    row_bytes = wl.head_dim * BYTES[wl.kv_dtype] + (4 if wl.kv_dtype in ("fp8", "int8") else 0)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device())
+    time.sleep(0.3)
+    if args.op == "compact":
+        st = Stepper(setup, wl.num_splits)
+        for _ in range(max(3, args.warmup)):
+            st.step()  # decode + H2O scores accumulate into st.acc
+        n = len(setup.ids)
+        keep = torch.zeros((n, wl.budget), dtype=torch.int32, device=dev)
+        cnt = torch.zeros(n, dtype=torch.int32, device=dev)
+        c.h2o_select(st.lens, st.acc, st.stride, wl.budget, wl.recent, keep, wl.budget, cnt)
+        c.sync_status()
+        counts = cnt.cpu().numpy()
+        moved = int(counts.sum()) * wl.n_kv_heads * 2 * row_bytes  # K and V rows read (and as many written)
+
+        q0 = st.q[:0]
+
+        def one_round(timed):
+            forks = [c.seq_fork(s) for s in setup.ids]
+            c.decode([], q0)  # an empty call flushes the forks' queued table writes before the timed call
+            if timed:
+                e0.record(stream)
+            c.seq_compact(forks, counts, keep, wl.budget)
+            if timed:
+                e1.record(stream)
+            c.sync_status()
+            for f in forks:
+                c.seq_free(f)
+            return e0.elapsed_time(e1) if timed else 0.0
+
+        for _ in range(3):
+            one_round(False)
+        c.timing_enable(["compact"])
+        c.timing_read()
+        t_wall0 = time.time()
+        ms = [one_round(True) for _ in range(rounds)]
+        t_wall1 = time.time()
+        kt = c.timing_read()["compact"]
+        c.timing_enable(False)
+        algo = 2 * moved
+        call_ms = statistics.median(ms)
+        kern_ms = kt[0] / max(kt[1], 1)
+        line = {"metric": "H2O compaction GB/s (kept rows read + written, frac of HBM peak)",
+                "value": round(algo / (call_ms * 1e-3) / 1e9, 2), "unit": "GB/s", "op": "compact",
+                "n_gpus": 1, "steps": rounds, "warmup": max(3, args.warmup), "ms_per_op": round(call_ms, 5),
+                "higher_is_better": True, "dtype": wl.kv_dtype, "data": "synthetic",
+                "config": {"workload": label, "sequences": n, "kept_rows": int(counts.sum()),
+                           "bytes_per_op": algo},
+                "roofline": {"bound": "hbm", "kernel": "compact_gather_kernel",
+                             "achieved": round(algo / (kern_ms * 1e-3) / 1e9, 2), "peak": peak,
+                             "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s",
+                             "frac": round(algo / (kern_ms * 1e-3) / 1e9 / peak, 4),
+                             "avg_launch_ms": round(kern_ms, 5)}}
+    else:
+        blocks = 0
+        for s in setup.ids:
+            blocks += int((c.block_table(s) >= 0).sum())
+        c.swap_space(blocks + 16)
+        per_dir = blocks * wl.n_kv_heads * BLOCK_SIZE * 2 * row_bytes
+
+        def one_round(timed):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            ev[0].record(stream)
+            c.swap_out(setup.ids)
+            ev[1].record(stream)
+            c.swap_in(setup.ids)
+            ev[2].record(stream)
+            c.sync_status()
+            return (ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])) if timed else (0.0, 0.0)
+
+        for _ in range(3):
+            one_round(False)
+        c.timing_enable(["swap_copy"])
+        c.timing_read()
+        t_wall0 = time.time()
+        ms = [one_round(True) for _ in range(rounds)]
+        t_wall1 = time.time()
+        kt = c.timing_read()["swap_copy"]
+        c.timing_enable(False)
+        out_ms = statistics.median([a for a, _ in ms])
+        in_ms = statistics.median([b for _, b in ms])
+        kern_ms = kt[0] / max(kt[1], 1)
+        line = {"metric": "CPU swap GB/s per direction (device pool <-> pinned host pool)",
+                "value": round(2 * per_dir / ((out_ms + in_ms) * 1e-3) / 1e9, 2), "unit": "GB/s", "op": "swap",
+                "n_gpus": 1, "steps": rounds, "warmup": 3, "ms_per_op": round(out_ms + in_ms, 5),
+                "higher_is_better": True, "dtype": wl.kv_dtype, "data": "synthetic",
+                "config": {"workload": label, "sequences": len(setup.ids), "blocks": blocks,
+                           "bytes_per_direction": per_dir},
+                "swap_out_gbs": round(per_dir / (out_ms * 1e-3) / 1e9, 2),
+                "swap_in_gbs": round(per_dir / (in_ms * 1e-3) / 1e9, 2),
+                "roofline": {"bound": "host link", "kernel": "block_copy_kernel",
+                             "achieved": round(per_dir / (kern_ms * 1e-3) / 1e9, 2), "peak": None,
+                             "unit": "GB/s", "frac": None, "avg_launch_ms": round(kern_ms, 5)}}
+    clocks.stop()
+    line["clocks"] = clocks.summary(t_wall0, t_wall1)
     print(json.dumps(line))
 
 

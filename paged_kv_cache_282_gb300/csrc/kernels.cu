@@ -743,6 +743,15 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
 // (token, kv head) row: K, V and the FP8 / INT8 scales); the score array follows.
 // ---------------------------------------------------------------------------
 
+// Moves each kept (token, kv head) row -- its K and V row and, for one-byte
+// codes, the two scales -- from the sequence's current block to its fresh
+// block.  A task of 2 x row_bytes / 16 lanes (at most a warp) moves one row
+// pair in 16-byte chunks, K in the task's first half and V in its second;
+// tasks run head-major (consecutive tasks: consecutive kept tokens of one
+// kv head), so neighbouring lanes and warps read and write neighbouring rows.
+// Each lane serves kCompactTasks tasks, spaced a grid's worth of tasks
+// apart, and issues all their loads before its stores.
+constexpr int kCompactTasks = 2;
 __global__ void compact_gather_kernel(const CompactSeq* __restrict__ seqs, const int32_t* __restrict__ new_blocks,
                                       const int32_t* __restrict__ tables, int max_blocks, int num_blocks,
                                       const int32_t* __restrict__ keep_idx, int64_t keep_stride, int Hk, int row_bytes,
@@ -750,27 +759,47 @@ __global__ void compact_gather_kernel(const CompactSeq* __restrict__ seqs, const
                                       float* __restrict__ k_scale, float* __restrict__ v_scale,
                                       int32_t* __restrict__ status) {
   const CompactSeq sq = seqs[blockIdx.y];
-  const int lane = threadIdx.x & 31;
-  const int64_t rows = (int64_t)sq.count * Hk;
-  const int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-  if (w >= rows) return;
-  const int i = (int)(w / Hk), g = (int)(w - (int64_t)i * Hk);
-  const int src = keep_idx[(size_t)sq.q_row * keep_stride + i];
-  const int sb = (src >= 0 && src < sq.old_len) ? tables[(size_t)sq.seq_slot * max_blocks + src / kBlock] : -1;
-  if (sb < 0 || sb >= num_blocks) {
-    if (lane == 0) atomicOr(status, kStatusBadBlock);
-    return;
+  const int C = row_bytes / 16;          // chunks per row
+  const int per = min(32, 2 * C);        // lanes per task
+  const int lane = threadIdx.x & 31, sub = lane % per;
+  const int64_t tasks = (int64_t)sq.count * Hk;
+  const int64_t slot = ((int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5)) * (32 / per) + lane / per;
+  const int64_t span = (int64_t)gridDim.x * (blockDim.x / 32) * (32 / per);  // tasks one round of the grid covers
+  size_t srow[kCompactTasks], drow[kCompactTasks];
+  bool live[kCompactTasks];
+#pragma unroll
+  for (int u = 0; u < kCompactTasks; ++u) {
+    const int64_t t = slot + u * span;
+    live[u] = false;
+    if (t >= tasks) continue;
+    const int g = (int)(t / sq.count), i = (int)(t - (int64_t)g * sq.count);
+    const int src = keep_idx[(size_t)sq.q_row * keep_stride + i];
+    const int sb = (src >= 0 && src < sq.old_len) ? tables[(size_t)sq.seq_slot * max_blocks + src / kBlock] : -1;
+    if (sb < 0 || sb >= num_blocks) {
+      if (sub == 0) atomicOr(status, kStatusBadBlock);
+      continue;
+    }
+    const int db = new_blocks[sq.new_off + i / kBlock];
+    srow[u] = ((size_t)sb * Hk + g) * kBlock + (src & 15);
+    drow[u] = ((size_t)db * Hk + g) * kBlock + (i & 15);
+    live[u] = true;
   }
-  const int db = new_blocks[sq.new_off + i / kBlock];
-  const size_t srow = ((size_t)sb * Hk + g) * kBlock + (src & 15);
-  const size_t drow = ((size_t)db * Hk + g) * kBlock + (i & 15);
-  for (int ch = lane; ch < row_bytes / 16; ch += 32) {
-    reinterpret_cast<uint4*>(k_pool + drow * row_bytes)[ch] = reinterpret_cast<const uint4*>(k_pool + srow * row_bytes)[ch];
-    reinterpret_cast<uint4*>(v_pool + drow * row_bytes)[ch] = reinterpret_cast<const uint4*>(v_pool + srow * row_bytes)[ch];
+  for (int q = sub; q < 2 * C; q += per) {
+    char* pool = q < C ? k_pool : v_pool;
+    const int ch = q < C ? q : q - C;
+    uint4 x[kCompactTasks];
+#pragma unroll
+    for (int u = 0; u < kCompactTasks; ++u)
+      if (live[u]) x[u] = reinterpret_cast<const uint4*>(pool + srow[u] * row_bytes)[ch];
+#pragma unroll
+    for (int u = 0; u < kCompactTasks; ++u)
+      if (live[u]) reinterpret_cast<uint4*>(pool + drow[u] * row_bytes)[ch] = x[u];
   }
-  if (k_scale && lane == 0) {
-    k_scale[drow] = k_scale[srow];
-    v_scale[drow] = v_scale[srow];
+#pragma unroll
+  for (int u = 0; u < kCompactTasks; ++u) {
+    if (!live[u]) continue;
+    if (k_scale && sub == 0) k_scale[drow[u]] = k_scale[srow[u]];
+    if (v_scale && sub == per - 1) v_scale[drow[u]] = v_scale[srow[u]];
   }
 }
 
@@ -921,9 +950,10 @@ cudaError_t launch_compact_gather(const CompactSeq* seqs, int n, int max_count, 
                                   int64_t keep_stride, int Hk, int row_bytes, void* k_pool, void* v_pool, float* k_scale,
                                   float* v_scale, int32_t* status, cudaStream_t st) {
   if (n <= 0 || max_count <= 0) return cudaSuccess;
-  const int64_t rows = (int64_t)max_count * Hk;
+  const int tasks_per_warp = 32 / std::min(32, 2 * (row_bytes / 16)) * kCompactTasks;
+  const int64_t warps = ((int64_t)max_count * Hk + tasks_per_warp - 1) / tasks_per_warp;
   for (int first = 0; first < n; first += 65535) {  // grid.y limit
-    dim3 grid((unsigned)((rows + 7) / 8), (unsigned)std::min(65535, n - first));
+    dim3 grid((unsigned)((warps + 7) / 8), (unsigned)std::min(65535, n - first));
     compact_gather_kernel<<<grid, 256, 0, st>>>(seqs + first, new_blocks, tables, max_blocks, num_blocks, keep_idx,
                                                 keep_stride, Hk, row_bytes, (char*)k_pool, (char*)v_pool, k_scale,
                                                 v_scale, status);
