@@ -588,6 +588,12 @@ struct PlanCache {
     int32_t v0, runs, rec0, rec1;
   };
   std::vector<SegRecord> seg_rec;
+  struct SegPiece {
+    Piece piece;  // the fields every piece of the segment shares
+    int32_t first_partial, vfirst;
+    bool run_continues;
+  };
+  std::vector<SegPiece> seg_piece;
 };
 
 void destroy_plan_cache(PlanCache* c) { delete c; }
@@ -797,48 +803,64 @@ void plan_stream_k_single(pkv_pool* p, int32_t n, const int32_t* ids, PlanCache&
       }
     }
   }
-  // physical placement: virtual warp v runs in CTA v % C as its warp v / C
+  // per segment: its pieces' common fields, whether the next segment
+  // continues the same (sequence, kv head), and its records
+  std::vector<PlanCache::SegPiece>& tpl = cache.seg_piece;
+  tpl.resize(segs.size());
+  for (size_t k = 0; k < segs.size(); ++k) {
+    const Seg& sg = segs[k];
+    const BgRec& br = bgr[(size_t)sg.b * Hk + sg.g];
+    Piece& pc = tpl[k].piece;
+    pc.seq_slot = ids[sg.b];
+    pc.q_row = sg.b;
+    pc.kv_head = sg.g;
+    pc.lblk_begin = pc.lblk_end = 0;
+    pc.ctx_len = A.len[pc.seq_slot];
+    pc.out_index = -1;
+    pc.flags = br.flags;
+    pc.q_row1 = -1;
+    pc.out_index1 = -1;
+    pc.item1 = 0;
+    pc.pad = 0;
+    tpl[k].first_partial = br.first_partial;
+    tpl[k].vfirst = br.vfirst;
+    tpl[k].run_continues = k + 1 < segs.size() && segs[k + 1].b == sg.b && segs[k + 1].g == sg.g;
+  }
+  // physical placement: virtual warp v runs in CTA v % C as its warp v / C;
+  // pieces are written in place (at most one per segment plus one per warp)
   const int WPC = warps_per_cta(p, 1);
   const int C = std::max(1, std::min(TW, TWmax / WPC));
   const int slots = TW > 0 ? C * WPC : 0;
-  plan.pieces.clear();
-  plan.pieces.reserve(segs.size() + TW);
+  plan.pieces.resize(segs.size() + TW);
+  Piece* out = plan.pieces.data();
+  size_t np = 0;
   plan.warp_begin.assign(slots + 1, 0);
   int phys = 0;
   for (int cta = 0; cta < C; ++cta)
     for (int wl = 0; wl < WPC; ++wl, ++phys) {
-      plan.warp_begin[phys] = (int32_t)plan.pieces.size();
+      plan.warp_begin[phys] = (int32_t)np;
       const int v = wl * C + cta;
       if (v >= TW) continue;
       int64_t left = ws[v + 1].unit - ws[v].unit;
       int32_t si = ws[v].seg;
       int32_t lo = segs[si].lo + ws[v].seg_off;
       while (left > 0) {
-        const Seg& sg = segs[si];
-        const int32_t hi = (int32_t)std::min<int64_t>(sg.hi, lo + left);
-        const BgRec& br = bgr[(size_t)sg.b * Hk + sg.g];
+        const PlanCache::SegPiece& t = tpl[si];
+        const int32_t hi = (int32_t)std::min<int64_t>(segs[si].hi, lo + left);
         left -= hi - lo;
         // the run ends with the warp's units or where the next segment is another (sequence, kv head)
-        const bool last = left == 0 || (size_t)si + 1 >= segs.size() || segs[si + 1].b != sg.b ||
-                          segs[si + 1].g != sg.g;
-        Piece pc;
-        pc.seq_slot = ids[sg.b];
-        pc.q_row = sg.b;
-        pc.kv_head = sg.g;
+        const bool last = left == 0 || !t.run_continues;
+        Piece& pc = out[np++];
+        pc = t.piece;
         pc.lblk_begin = lo;
         pc.lblk_end = hi;
-        pc.ctx_len = A.len[pc.seq_slot];
-        pc.out_index = br.first_partial >= 0 ? br.first_partial + (v - br.vfirst) : -1;
-        pc.flags = (last ? kPieceLastOfRun : 0) | br.flags;
-        pc.q_row1 = -1;
-        pc.out_index1 = -1;
-        pc.item1 = 0;
-        pc.pad = 0;
-        plan.pieces.push_back(pc);
+        if (t.first_partial >= 0) pc.out_index = t.first_partial + (v - t.vfirst);
+        if (last) pc.flags |= kPieceLastOfRun;
         if (left > 0) lo = segs[++si].lo;
       }
     }
-  plan.warp_begin[slots] = (int32_t)plan.pieces.size();
+  plan.pieces.resize(np);
+  plan.warp_begin[slots] = (int32_t)np;
   plan.total_warps = slots;
   plan.ctas = TW > 0 ? C : 0;
 }
