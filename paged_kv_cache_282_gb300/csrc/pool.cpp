@@ -960,48 +960,64 @@ void plan_stream_k_pairs(pkv_pool* p, int32_t n, const int32_t* ids, PlanCache& 
       }
     }
   }
+  // per segment: its pieces' common fields and whether the next segment
+  // continues the same run key (sequence, kv head, second sequence)
+  std::vector<PlanCache::SegPiece>& tpl = cache.seg_piece;
+  tpl.resize(ns);
+  for (size_t k = 0; k < ns; ++k) {
+    const Seg& sg = segs[k];
+    const SegRec& rc = sr[k];
+    Piece& pc = tpl[k].piece;
+    pc.seq_slot = ids[sg.b];
+    pc.q_row = sg.b;
+    pc.kv_head = sg.g;
+    pc.lblk_begin = pc.lblk_end = 0;
+    pc.ctx_len = A.len[pc.seq_slot];
+    pc.out_index = -1;
+    pc.flags = rc.rec0 >= 0 ? item_of[(size_t)sg.b * Hk + sg.g] << 1 : 0;
+    pc.q_row1 = sg.b1;
+    pc.out_index1 = -1;
+    pc.item1 = sg.b1 >= 0 ? item_of[(size_t)sg.b1 * Hk + sg.g] : 0;
+    pc.pad = 0;
+    tpl[k].first_partial = rc.rec0;
+    tpl[k].vfirst = rc.v0;
+    tpl[k].run_continues =
+        k + 1 < ns && segs[k + 1].b == sg.b && segs[k + 1].g == sg.g && segs[k + 1].b1 == sg.b1;
+  }
   const int WPC = warps_per_cta(p, 2);
   const int C = std::max(1, std::min(TW, TWmax / WPC));
   const int slots = TW > 0 ? C * WPC : 0;
-  plan.pieces.clear();
-  plan.pieces.reserve(ns + TW);
+  plan.pieces.resize(ns + TW);
+  Piece* out = plan.pieces.data();
+  size_t np = 0;
   plan.warp_begin.assign(slots + 1, 0);
   int phys = 0;
   for (int cta = 0; cta < C; ++cta)
     for (int wl = 0; wl < WPC; ++wl, ++phys) {
-      plan.warp_begin[phys] = (int32_t)plan.pieces.size();
+      plan.warp_begin[phys] = (int32_t)np;
       const int v = wl * C + cta;
       if (v >= TW) continue;
       int64_t left = ws[v + 1].unit - ws[v].unit;
       int32_t si = ws[v].seg;
       int32_t lo = segs[si].lo + ws[v].seg_off;
       while (left > 0) {
-        const Seg& sg = segs[si];
-        const SegRec& rc = sr[si];
-        const int32_t hi = (int32_t)std::min<int64_t>(sg.hi, lo + left);
-        const int32_t j = v - rc.v0;  // this warp's run of the segment
+        const PlanCache::SegPiece& t = tpl[si];
+        const int32_t hi = (int32_t)std::min<int64_t>(segs[si].hi, lo + left);
+        const int32_t j = v - t.vfirst;  // this warp's run of the segment
         left -= hi - lo;
-        const bool last = left == 0 || (size_t)si + 1 >= ns || segs[si + 1].b != sg.b ||
-                          segs[si + 1].g != sg.g || segs[si + 1].b1 != sg.b1;
-        Piece pc;
-        pc.seq_slot = ids[sg.b];
-        pc.q_row = sg.b;
-        pc.kv_head = sg.g;
+        const bool last = left == 0 || !t.run_continues;
+        Piece& pc = out[np++];
+        pc = t.piece;
         pc.lblk_begin = lo;
         pc.lblk_end = hi;
-        pc.ctx_len = A.len[pc.seq_slot];
-        pc.out_index = rc.rec0 >= 0 ? rc.rec0 + j : -1;
-        pc.flags = (last ? kPieceLastOfRun : 0) |
-                   (rc.rec0 >= 0 ? item_of[(size_t)sg.b * Hk + sg.g] << 1 : 0);
-        pc.q_row1 = sg.b1;
-        pc.out_index1 = sg.b1 >= 0 ? rc.rec1 + j : -1;
-        pc.item1 = sg.b1 >= 0 ? item_of[(size_t)sg.b1 * Hk + sg.g] : 0;
-        pc.pad = 0;
-        plan.pieces.push_back(pc);
+        if (t.first_partial >= 0) pc.out_index = t.first_partial + j;
+        if (pc.q_row1 >= 0) pc.out_index1 = sr[si].rec1 + j;
+        if (last) pc.flags |= kPieceLastOfRun;
         if (left > 0) lo = segs[++si].lo;
       }
     }
-  plan.warp_begin[slots] = (int32_t)plan.pieces.size();
+  plan.pieces.resize(np);
+  plan.warp_begin[slots] = (int32_t)np;
   plan.total_warps = slots;
   plan.ctas = TW > 0 ? C : 0;
 }
