@@ -744,6 +744,27 @@ std::vector<Pairing> pair_shared_prefixes(const pkv_pool* p, int32_t n, const in
 // (sequence, kv head) whose units span warps vfirst..vlast > vfirst writes
 // one partial record per warp, numbered in warp order from its first record;
 // each warp's pieces go straight to its physical slot.
+// The warp that holds unit u (warp w holds [U w / TW, U (w + 1) / TW)), for
+// u that never decreases: the bounds advance by U / TW plus a carry of the
+// remainder, without division.
+struct WarpCursor {
+  int64_t q, r, TW, next, carry;  // next: first unit of warp v + 1
+  int32_t v = 0;
+  WarpCursor(int64_t U, int64_t tw) : q(U / tw), r(U % tw), TW(tw), next(U / tw), carry(U % tw) {}
+  int32_t at(int64_t u) {
+    while (next <= u) {
+      ++v;
+      next += q;
+      carry += r;
+      if (carry >= TW) {
+        carry -= TW;
+        ++next;
+      }
+    }
+    return v;
+  }
+};
+
 void plan_stream_k_single(pkv_pool* p, int32_t n, const int32_t* ids, PlanCache& cache, int TWmax) {
   Plan& plan = cache.plan;
   const int Hk = p->cfg.n_kv_heads;
@@ -759,7 +780,7 @@ void plan_stream_k_single(pkv_pool* p, int32_t n, const int32_t* ids, PlanCache&
   using BgRec = PlanCache::BgRecord;
   std::vector<BgRec>& bgr = cache.bg_rec;
   bgr.assign(nbg, BgRec{0, -1, 0});
-  auto warp_of = [&](int64_t u) { return (int32_t)(((u + 1) * TW - 1) / U); };
+  WarpCursor wc(U, TW);
   int next_partial = 0;
   {
     int64_t off = 0;
@@ -769,7 +790,7 @@ void plan_stream_k_single(pkv_pool* p, int32_t n, const int32_t* ids, PlanCache&
         plan.empty.push_back({(int32_t)(bg / Hk), (int32_t)(bg % Hk)});
         continue;
       }
-      const int32_t v0 = warp_of(off), v1 = warp_of(off + nu - 1);
+      const int32_t v0 = wc.at(off), v1 = wc.at(off + nu - 1);
       bgr[bg].vfirst = v0;
       if (v1 > v0) {
         bgr[bg].first_partial = next_partial;
@@ -884,7 +905,7 @@ void plan_stream_k_pairs(pkv_pool* p, int32_t n, const int32_t* ids, PlanCache& 
   int64_t U = 0;
   for (const Seg& sg : segs) U += sg.hi - sg.lo;
   const int TW = (int)std::min<int64_t>(TWmax, (U + kMinUnitsPerWarp - 1) / kMinUnitsPerWarp);
-  auto warp_of = [&](int64_t u) { return (int32_t)(((u + 1) * TW - 1) / U); };
+  WarpCursor wc(U, TW);
   // per segment: first warp, number of runs, and its records' first index
   // for the first and the second sequence
   using SegRec = PlanCache::SegRecord;
@@ -899,7 +920,7 @@ void plan_stream_k_pairs(pkv_pool* p, int32_t n, const int32_t* ids, PlanCache& 
     for (size_t k = 0; k < ns; ++k) {
       const Seg& sg = segs[k];
       const int64_t len = sg.hi - sg.lo;
-      const int32_t v0 = warp_of(off), runs = warp_of(off + len - 1) - v0 + 1;
+      const int32_t v0 = wc.at(off), runs = wc.at(off + len - 1) - v0 + 1;
       sr[k] = {v0, runs, -1, -1};
       const size_t bg = (size_t)sg.b * Hk + sg.g;
       if (sg.b1 >= 0) {
