@@ -1138,7 +1138,8 @@ Plan& build_plan(pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, in
         }
     }
   }
-  plan.pieces.clear();
+  // (the one-pass paths size the piece array themselves: clearing it first
+  // would make them zero-fill all of it again)
   plan.combine.clear();
   plan.warp_begin.clear();
   const int TWmax = max_total_warps(p, plan.nq);
@@ -1150,12 +1151,14 @@ Plan& build_plan(pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, in
     if (!segs.empty()) {
       plan_stream_k_single(p, n, ids, cache, TWmax);
     } else {  // nothing to read: every (sequence, kv head) has an empty keep-set
+      plan.pieces.clear();
       for (int32_t b = 0; b < n; ++b)
         for (int g = 0; g < Hk; ++g) plan.empty.push_back({b, g});
       plan.warp_begin.assign(1, 0);
     }
     return plan;
   }
+  plan.pieces.clear();
   auto piece_of = [&](const Seg& s, int32_t lo, int32_t hi) {
     Piece pc;
     pc.seq_slot = ids[s.b];
