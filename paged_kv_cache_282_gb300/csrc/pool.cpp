@@ -120,6 +120,54 @@ struct HostAllocator {
   // queued device-side effects
   std::vector<int32_t> pending_cow;  // (src, dst) pairs
   std::vector<TablePatch> pending_patch;
+  // duplicate checks of sequence lists: the check's epoch, per sequence id
+  std::vector<uint32_t> seen_mark;
+  uint32_t seen_epoch = 0;
+  // per-block counters of one append's dry run (valid for the current epoch)
+  std::vector<uint32_t> drop_mark;
+  std::vector<int32_t> drop_count;
+  uint32_t drop_epoch = 0;
+
+  // Starts a fresh set of per-block counters (all zero).
+  void begin_drops() {
+    if (drop_mark.size() != (size_t)NB) {
+      drop_mark.assign(NB, 0);
+      drop_count.assign(NB, 0);
+    }
+    if (++drop_epoch == 0) {
+      std::fill(drop_mark.begin(), drop_mark.end(), 0);
+      drop_epoch = 1;
+    }
+  }
+  int32_t& dropped(int32_t b) {
+    if (drop_mark[b] != drop_epoch) {
+      drop_mark[b] = drop_epoch;
+      drop_count[b] = 0;
+    }
+    return drop_count[b];
+  }
+  // per table entry: the position of its last queued patch (valid for the
+  // entries the queue names, rewritten on each collapse)
+  std::vector<int32_t> patch_last;
+  // per block: a member of the current wave of copies (current epoch)
+  std::vector<uint32_t> wave_mark;
+  uint32_t wave_epoch = 0;
+
+
+  // The first id that occurs twice in ids[0, n), or -1 (ids must already be
+  // valid sequence ids).  Linear in n.
+  int32_t first_repeat(int32_t n, const int32_t* ids) {
+    if (seen_mark.size() != (size_t)max_seqs) seen_mark.assign(max_seqs, 0);
+    if (++seen_epoch == 0) {
+      std::fill(seen_mark.begin(), seen_mark.end(), 0);
+      seen_epoch = 1;
+    }
+    for (int32_t i = 0; i < n; ++i) {
+      if (seen_mark[ids[i]] == seen_epoch) return ids[i];
+      seen_mark[ids[i]] = seen_epoch;
+    }
+    return -1;
+  }
 
   void init(int32_t nb, int32_t ms, int32_t mb, uint64_t seed, const int32_t* order) {
     NB = nb;
@@ -446,16 +494,46 @@ pkv_status make_tensor_map(CUtensorMap* m, void* base, const pkv_pool_config& c)
 }
 
 // Several queued changes of one table entry collapse to the last one (the
-// kernels that apply patches do so in parallel).
-std::vector<TablePatch> dedup_patches(const std::vector<TablePatch>& q) {
-  std::unordered_map<int32_t, size_t> last;
-  last.reserve(q.size() * 2);
-  for (size_t i = 0; i < q.size(); ++i) last[q[i].index] = i;
+// kernels that apply patches do so in parallel); the kept patches stay in
+// queue order.
+std::vector<TablePatch> dedup_patches(HostAllocator& A, const std::vector<TablePatch>& q) {
+  const size_t entries = (size_t)A.max_seqs * A.max_blocks;
+  if (A.patch_last.size() != entries) A.patch_last.assign(entries, 0);
+  for (size_t i = 0; i < q.size(); ++i) A.patch_last[q[i].index] = (int32_t)i;
   std::vector<TablePatch> out;
-  out.reserve(last.size());
+  out.reserve(q.size());
   for (size_t i = 0; i < q.size(); ++i)
-    if (last[q[i].index] == i) out.push_back(q[i]);
+    if (A.patch_last[q[i].index] == (int32_t)i) out.push_back(q[i]);
   return out;
+}
+
+// A queued copy whose source or destination is the destination of an earlier
+// copy in the queue must run after it, so the queue is cut into waves of
+// independent copies that run in order. Returns the first copy of each wave
+// and, last, the number of copies.
+std::vector<size_t> cow_waves(HostAllocator& A) {
+  const size_t ncow = A.pending_cow.size() / 2;
+  std::vector<size_t> start{0};
+  if (ncow) {
+    if (A.wave_mark.size() != (size_t)A.NB) A.wave_mark.assign(A.NB, 0);
+    auto next_wave = [&A]() {
+      if (++A.wave_epoch == 0) {
+        std::fill(A.wave_mark.begin(), A.wave_mark.end(), 0);
+        A.wave_epoch = 1;
+      }
+    };
+    next_wave();
+    for (size_t k = 0; k < ncow; ++k) {
+      const int32_t src = A.pending_cow[2 * k], dst = A.pending_cow[2 * k + 1];
+      if (A.wave_mark[src] == A.wave_epoch || A.wave_mark[dst] == A.wave_epoch) {
+        start.push_back(k);
+        next_wave();
+      }
+      A.wave_mark[dst] = A.wave_epoch;  // the destinations of the current wave
+    }
+  }
+  start.push_back(ncow);
+  return start;
 }
 
 // Flushes queued copy-on-write copies and, unless the caller applies them
@@ -466,24 +544,10 @@ pkv_status flush_pending(pkv_pool* p, cudaStream_t st, bool with_patches = true)
   // Table patches: several changes to one entry collapse to the last one (the
   // patch kernel applies its list in parallel).
   std::vector<TablePatch> patches;
-  if (with_patches) patches = dedup_patches(A.pending_patch);
-  // COW copies: a copy whose source or destination is the destination of an
-  // earlier copy in the list must run after it, so the list is cut into waves
-  // of independent copies that run in order.
-  std::vector<size_t> wave_start{0};
-  {
-    std::set<int32_t> dsts;
-    for (size_t k = 0; k < A.pending_cow.size() / 2; ++k) {
-      const int32_t src = A.pending_cow[2 * k], dst = A.pending_cow[2 * k + 1];
-      if (dsts.count(src) || dsts.count(dst)) {
-        wave_start.push_back(k);
-        dsts.clear();
-      }
-      dsts.insert(dst);
-    }
-  }
+  if (with_patches) patches = dedup_patches(A, A.pending_patch);
+  // COW copies in waves of independent copies
+  const std::vector<size_t> wave_start = cow_waves(A);
   const size_t ncow = A.pending_cow.size() / 2, npatch = patches.size();
-  wave_start.push_back(ncow);
   const size_t cow_bytes = ncow * 2 * sizeof(int32_t), patch_off = (cow_bytes + 255) & ~size_t(255);
   const size_t bytes = patch_off + npatch * sizeof(TablePatch);
   StagingSlot* s;
@@ -1510,26 +1574,9 @@ int pkv::decode_attn_into(pkv_pool* p, void* stream, int32_t n, const int32_t* i
   cudaStream_t st = (cudaStream_t)stream;
 
   // queued allocator effects: last value per table entry; copies in waves
-  std::vector<TablePatch> patches;
-  {
-    std::unordered_map<int32_t, size_t> last;
-    for (size_t i = 0; i < A.pending_patch.size(); ++i) last[A.pending_patch[i].index] = i;
-    for (size_t i = 0; i < A.pending_patch.size(); ++i)
-      if (last[A.pending_patch[i].index] == i) patches.push_back(A.pending_patch[i]);
-  }
+  const std::vector<TablePatch> patches = dedup_patches(A, A.pending_patch);
   const size_t ncow = A.pending_cow.size() / 2;
-  std::vector<size_t> waves{0};
-  {
-    std::set<int32_t> dsts;
-    for (size_t k = 0; k < ncow; ++k) {
-      if (dsts.count(A.pending_cow[2 * k]) || dsts.count(A.pending_cow[2 * k + 1])) {
-        waves.push_back(k);
-        dsts.clear();
-      }
-      dsts.insert(A.pending_cow[2 * k + 1]);
-    }
-    waves.push_back(ncow);
-  }
+  const std::vector<size_t> waves = cow_waves(A);
   Plan empty_plan;
   Plan& plan = n > 0 ? build_plan(p, n, ids, mode, S, W, num_splits) : empty_plan;
   const size_t pf = (size_t)partial_floats(p->G, c.head_dim) * sizeof(float);
@@ -1616,9 +1663,9 @@ pkv_status swap_move(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, b
     if (!A.valid_seq(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", s);
     if (A.swapped[s] != (out ? 0 : 1))
       return fail(PKV_ERR_INVALID_ARG, "sequence %d is already %s", s, out ? "swapped out" : "on the device");
-    for (int32_t j = 0; j < i; ++j)
-      if (ids[j] == s) return fail(PKV_ERR_INVALID_ARG, "sequence %d listed twice", s);
   }
+  if (const int32_t d = A.first_repeat(n, ids); d >= 0)
+    return fail(PKV_ERR_INVALID_ARG, "sequence %d listed twice", d);
   std::unordered_map<int32_t, int32_t> moved;  // source block -> destination block
   for (int32_t i = 0; i < n; ++i)
     for (int32_t b : out ? A.table[ids[i]] : A.host_table[ids[i]])
@@ -1839,9 +1886,9 @@ pkv_status pkv_seq_truncate_many(pkv_pool* p, int32_t n, const int32_t* ids, con
     if (L < 0 || L > A.len[s]) return fail(PKV_ERR_INVALID_ARG, "new_len %d outside [0, %d]", L, A.len[s]);
     if (L % kBlock && A.table[s][ceil_div(L, kBlock) - 1] < 0)
       return fail(PKV_ERR_INVALID_ARG, "the new last block of sequence %d was evicted", s);
-    for (int32_t j = 0; j < i; ++j)
-      if (ids[j] == s) return fail(PKV_ERR_INVALID_ARG, "sequence %d listed twice", s);
   }
+  if (const int32_t d = A.first_repeat(n, ids); d >= 0)
+    return fail(PKV_ERR_INVALID_ARG, "sequence %d listed twice", d);
   for (int32_t i = 0; i < n; ++i) {
     A.drop_from(ids[i], ceil_div(new_lens[i], kBlock));
     A.len[ids[i]] = new_lens[i];
@@ -1931,16 +1978,11 @@ pkv_status pkv_reserve_slots(pkv_pool* p, int32_t n, const int32_t* ids, int32_t
   if (T < 0) return fail(PKV_ERR_INVALID_ARG, "T < 0");
   if (pkv_status r = check_seq_list(p, n, ids)) return r;
   auto& A = p->alloc;
-  {
-    std::vector<int32_t> sorted(ids, ids + n);
-    std::sort(sorted.begin(), sorted.end());
-    if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end())
-      return fail(PKV_ERR_INVALID_ARG, "a sequence appears twice in one append");
-  }
+  if (A.first_repeat(n, ids) >= 0) return fail(PKV_ERR_INVALID_ARG, "a sequence appears twice in one append");
   // dry run: count the blocks needed, with the refcount drops earlier
   // copies in this call cause
   int64_t need = 0;
-  std::unordered_map<int32_t, int32_t> dropped;
+  A.begin_drops();
   for (int32_t i = 0; i < n; ++i) {
     const int32_t s = ids[i];
     if ((int64_t)A.len[s] + T > (int64_t)A.max_blocks * kBlock)
@@ -1952,9 +1994,9 @@ pkv_status pkv_reserve_slots(pkv_pool* p, int32_t n, const int32_t* ids, int32_t
       } else if (t == 0) {
         const int32_t b = A.table[s][pos / kBlock];
         if (b < 0) return fail(PKV_ERR_INVALID_ARG, "sequence %d: last block was evicted", s);
-        if (A.refcount[b] - dropped[b] > 1) {
+        if (A.refcount[b] - A.dropped(b) > 1) {
           ++need;
-          ++dropped[b];
+          ++A.dropped(b);
         }
       }
     }
@@ -2005,7 +2047,7 @@ pkv_status pkv_append(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, 
   cudaStream_t st = (cudaStream_t)stream;
   // copies first: the new rows of a copied block land in the copy
   if (pkv_status r = flush_pending(p, st, /*with_patches=*/false)) return r;
-  std::vector<TablePatch> patches = dedup_patches(p->alloc.pending_patch);
+  std::vector<TablePatch> patches = dedup_patches(p->alloc, p->alloc.pending_patch);
   p->alloc.pending_patch.clear();
   if (ntok == 0 && patches.empty()) return PKV_OK;
   const auto& c = p->cfg;
@@ -2068,9 +2110,9 @@ pkv_status pkv_seq_compact(pkv_pool* p, void* stream, int32_t n, const int32_t* 
   auto& A = p->alloc;
   int64_t need = 0;
   int32_t max_count = 0, max_len = 0;
+  if (const int32_t d = A.first_repeat(n, ids); d >= 0)
+    return fail(PKV_ERR_INVALID_ARG, "sequence %d listed twice", d);
   for (int32_t i = 0; i < n; ++i) {
-    for (int32_t j = 0; j < i; ++j)
-      if (ids[j] == ids[i]) return fail(PKV_ERR_INVALID_ARG, "sequence %d listed twice", ids[i]);
     if (counts[i] < 0 || counts[i] > A.len[ids[i]])
       return fail(PKV_ERR_INVALID_ARG, "count %d outside [0, %d]", counts[i], A.len[ids[i]]);
     need += ceil_div(counts[i], kBlock);
