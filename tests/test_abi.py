@@ -335,3 +335,43 @@ def test_one_pass_planner_matches_general_planner(pkv, seed):
         assert info == ginfo and fast == general, (mode, S, W)
         pairs_seen |= info[3] == 2
     assert pairs_seen == bool(seed % 2)
+
+
+@pytest.mark.parametrize("spare", [0, 1])
+def test_append_to_shared_block_needs_one_copy_fewer_than_sharers(pkv, spare):
+    """Four sequences share a part-filled block. When all four append in one
+    call, three copy it and the last one finds it its own: the call needs
+    three free blocks, not four. One block fewer refuses it, with nothing
+    changed; library and oracle agree either way."""
+    free_after_forks = 3 - 1 + spare          # 2 (refused) or 3 (fits)
+    nb = 2 + free_after_forks                 # 17 tokens take 2 blocks
+    lib = pkv.PagedKVCache(nb, 4, 2, 64, 8, 8, kv_dtype="fp32", alloc_seed=9, host_only=True)
+    ora = oracle.OracleAllocator(nb, 8, 8, seed=9)
+    a = lib.seq_add()
+    assert ora.seq_add() == a
+    lib.reserve_slots([a], 17)
+    ora.append([a], 17)
+    ids = [a]
+    for _ in range(3):
+        ids.append(lib.seq_fork(a))
+        assert ora.fork(a) == ids[-1]
+    assert lib.stats()["free_blocks"] == ora.num_free() == free_after_forks
+    tables = [lib.block_table(s).tolist() for s in ids]
+    if spare:
+        s1, c1 = lib.reserve_slots(ids, 1)
+        s2, c2 = ora.append(ids, 1)
+        assert np.array_equal(s1, s2) and np.array_equal(c1, c2) and len(c1) == 3
+        for s in ids:
+            assert np.array_equal(lib.block_table(s), ora.table(s))
+        assert lib.stats()["free_blocks"] == ora.num_free() == 0
+    else:
+        with pytest.raises(pkv.PKVError) as e:
+            lib.reserve_slots(ids, 1)
+        assert e.value.status == 3
+        with pytest.raises(MemoryError):
+            ora.append(ids, 1)
+        assert [lib.block_table(s).tolist() for s in ids] == tables
+        assert [lib.seq_len(s) for s in ids] == [17] * 4
+    with pytest.raises(pkv.PKVError) as e:  # a sequence listed twice
+        lib.reserve_slots([ids[1], ids[1]], 1)
+    assert e.value.status == 1
