@@ -42,8 +42,11 @@ def _i32_array(values) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(values, dtype=np.int32))
 
 
-def _ptr(arr: np.ndarray):
-    return arr.ctypes.data_as(ctypes.c_void_p)
+def _ptr(arr: np.ndarray) -> int:
+    """The address of a host array for a `void*` argument.  A plain integer
+    (cheaper than a ctypes pointer object), so the caller keeps `arr` alive
+    across the call: every caller passes an array held in a local name."""
+    return arr.ctypes.data
 
 
 # Raw C-ABI entry points, re-exported under their own names (marshalling is
@@ -72,7 +75,7 @@ class PagedKVCache:
         self._order = None if free_order is None else _i32_array(free_order)
         self.cfg = _abi.pkv_pool_config(num_blocks, BLOCK_SIZE, n_heads, n_kv_heads, head_dim, max_seqs,
                                         max_blocks_per_seq, KV_DTYPES[kv_dtype], alloc_seed & (2 ** 64 - 1),
-                                        None if self._order is None else _ptr(self._order).value)
+                                        None if self._order is None else _ptr(self._order))
         self._h = ctypes.c_void_p()
         self.host_only = host_only
         self._workspace = None
