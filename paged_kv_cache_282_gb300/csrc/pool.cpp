@@ -117,7 +117,9 @@ struct HostAllocator {
   std::vector<uint8_t> live, holes;
   std::set<int32_t> free_ids;
   int64_t cow_count = 0, n_alloc = 0, n_freed = 0;
-  // queued device-side effects
+  // queued device-side effects (device pools only: a host-only pool has no
+  // device table or blocks to update)
+  bool queue = false;
   std::vector<int32_t> pending_cow;  // (src, dst) pairs
   std::vector<TablePatch> pending_patch;
   // duplicate checks of sequence lists: the check's epoch, per sequence id
@@ -152,7 +154,6 @@ struct HostAllocator {
   // per block: a member of the current wave of copies (current epoch)
   std::vector<uint32_t> wave_mark;
   uint32_t wave_epoch = 0;
-
 
   // The first id that occurs twice in ids[0, n), or -1 (ids must already be
   // valid sequence ids).  Linear in n.
@@ -239,13 +240,13 @@ struct HostAllocator {
   void set_entry(int32_t s, int32_t lb, int32_t v) {
     if ((int32_t)table[s].size() <= lb) table[s].resize(lb + 1, -1);
     table[s][lb] = v;
-    pending_patch.push_back({s * max_blocks + lb, v});
+    if (queue) pending_patch.push_back({s * max_blocks + lb, v});
   }
   void drop_from(int32_t s, int32_t first_lb) {
     auto& t = table[s];
     for (int32_t lb = first_lb; lb < (int32_t)t.size(); ++lb) {
       if (t[lb] >= 0) release(t[lb]);
-      if (t[lb] != -1) pending_patch.push_back({s * max_blocks + lb, -1});
+      if (queue && t[lb] != -1) pending_patch.push_back({s * max_blocks + lb, -1});
     }
     if ((int32_t)t.size() > first_lb) t.resize(first_lb);
   }
@@ -418,7 +419,13 @@ pkv_status launch(pkv_pool* p, int kernel, cudaStream_t st, F&& fn) {
     PKV_CUDA(cudaEventRecord(a, st));
   }
   cudaError_t e = fn();
-  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "kernel %d launch failed: %s", kernel, cudaGetErrorString(e));
+  if (e != cudaSuccess) {
+    if (timed) {  // the pair goes back unused
+      p->timing.spare.push_back(a);
+      p->timing.spare.push_back(b);
+    }
+    return fail(PKV_ERR_CUDA, "kernel %d launch failed: %s", kernel, cudaGetErrorString(e));
+  }
   ++p->launches;
   if (timed) {
     PKV_CUDA(cudaEventRecord(b, st));
@@ -1717,10 +1724,7 @@ pkv_status swap_move(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, b
       A.swapped[s] = 0;
     }
   }
-  if (!p->device) {
-    A.pending_patch.clear();
-    return PKV_OK;
-  }
+  if (!p->device) return PKV_OK;
   const int npairs = (int)(pairs.size() / 2);
   if (npairs == 0) return PKV_OK;
   const auto& c = p->cfg;
@@ -1786,6 +1790,7 @@ pkv_status pkv_pool_create(const pkv_pool_config* cfg, const pkv_pool_buffers* b
       return fail(PKV_ERR_INVALID_ARG, "k_scale / v_scale must be 16-byte aligned");
     }
     p->device = true;
+    p->alloc.queue = true;
     p->buf = b;
     auto fail_dev = [&](pkv_status r) {
       p->staging.destroy();
@@ -2016,7 +2021,7 @@ pkv_status pkv_reserve_slots(pkv_pool* p, int32_t n, const int32_t* ids, int32_t
         const int32_t fresh = A.take();
         --A.refcount[old];
         A.set_entry(s, lb, fresh);
-        if (p->device) {
+        if (A.queue) {
           A.pending_cow.push_back(old);
           A.pending_cow.push_back(fresh);
         }
@@ -2031,7 +2036,6 @@ pkv_status pkv_reserve_slots(pkv_pool* p, int32_t n, const int32_t* ids, int32_t
       A.len[s] = pos + 1;
     }
   }
-  if (!p->device) A.pending_patch.clear();
   if (n_cow_out) *n_cow_out = ncow;
   return PKV_OK;
 }
@@ -2164,10 +2168,7 @@ pkv_status pkv_seq_compact(pkv_pool* p, void* stream, int32_t n, const int32_t* 
     A.len[ids[i]] = counts[i];
     A.holes[ids[i]] = 0;
   }
-  if (!p->device) {
-    A.pending_patch.clear();
-    return PKV_OK;
-  }
+  if (!p->device) return PKV_OK;
   if (pkv_status r = flush_pending(p, st)) return r;  // new tables, after the gather
   if (acc && n > 0)
     if (pkv_status r = launch(p, PKV_KERNEL_COMPACT, st, [&] {
