@@ -231,6 +231,13 @@ struct HostAllocator {
     ++n_alloc;
     return b;
   }
+  // Undoes the latest take() of b (blocks go back in the reverse order of
+  // their takes, which restores the free pool exactly).
+  void untake(int32_t b) {
+    refcount[b] = 0;
+    free_blocks.push_back(b);
+    --n_alloc;
+  }
   void release(int32_t b) {
     if (--refcount[b] == 0) {
       free_blocks.push_back(b);
@@ -2142,13 +2149,18 @@ pkv_status pkv_seq_compact(pkv_pool* p, void* stream, int32_t n, const int32_t* 
     seqs[i] = {ids[i], i, counts[i], (int32_t)fresh.size(), A.len[ids[i]], 0, 0, 0};
     for (int32_t k = 0; k < ceil_div(counts[i], kBlock); ++k) fresh.push_back(A.take());
   }
+  // a failure before the gather is queued gives the fresh blocks back
+  auto undo = [&](pkv_status r) {
+    for (size_t k = fresh.size(); k-- > 0;) A.untake(fresh[k]);
+    return r;
+  };
   StagingSlot* s = nullptr;
   if (p->device && n > 0) {
     const size_t seq_bytes = n * sizeof(CompactSeq), off = (seq_bytes + 255) & ~size_t(255);
-    if (pkv_status r = p->staging.acquire(off + fresh.size() * sizeof(int32_t) + 4, &s)) return r;
+    if (pkv_status r = p->staging.acquire(off + fresh.size() * sizeof(int32_t) + 4, &s)) return undo(r);
     memcpy(s->host, seqs.data(), seq_bytes);
     if (!fresh.empty()) memcpy(s->host + off, fresh.data(), fresh.size() * sizeof(int32_t));
-    if (pkv_status r = Staging::upload(s, off + fresh.size() * sizeof(int32_t), st)) return r;
+    if (pkv_status r = Staging::upload(s, off + fresh.size() * sizeof(int32_t), st)) return undo(r);
     const auto& c = p->cfg;
     const int row_bytes = c.head_dim * elem_bytes(c.kv_dtype);
     const bool fp8 = has_scales(c.kv_dtype);
@@ -2159,7 +2171,7 @@ pkv_status pkv_seq_compact(pkv_pool* p, void* stream, int32_t n, const int32_t* 
                                        fp8 ? p->buf.k_scale : nullptr, fp8 ? p->buf.v_scale : nullptr, p->buf.status,
                                        st);
         }))
-      return r;
+      return undo(r);
   }
   size_t pos = 0;
   for (int32_t i = 0; i < n; ++i) A.drop_from(ids[i], 0);  // old blocks, ascending, sequence by sequence
