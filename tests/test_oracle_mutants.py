@@ -44,20 +44,73 @@ MUTANTS = {
     "swap-in keeps the host blocks": ("        else\n          drop_host_block(a, from[lb]);", "        else\n          (void)0;"),
     "token slot shifted": ("    slot = j % ORACLE_BLOCK;\n    if (block < 0 || block >= jb->num_blocks) {",
                            "    slot = (j + 1) % ORACLE_BLOCK;\n    if (block < 0 || block >= jb->num_blocks) {"),
+    "H2O select: recent window one short": ("for (j = ncand; j < L; j++) chosen[j] = 1;",
+                                            "for (j = ncand + 1; j < L; j++) chosen[j] = 1;"),
+    "H2O select: one heavy hitter short": ("for (j = 0; j < keep; j++) chosen[c[j].pos] = 1;",
+                                           "for (j = 0; j + 1 < keep; j++) chosen[c[j].pos] = 1;"),
+    "H2O update reads head 0's lse": ("- lse[(size_t)b * H + h]);", "- lse[(size_t)b * H]);"),
+    "H2O update weighs masked positions": (
+        "      if (!oracle_keep(L, mask_mode, num_sinks, window, j)) continue;\n      for (h = 0; h < H; h++) {",
+        "      if (0) continue;\n      for (h = 0; h < H; h++) {"),
+    "decode ignores the softmax scale": ("s[j] = jb->scale * dot;", "s[j] = dot;"),
+    "decode averages values uniformly": ("    p = exp(s[j] - lse);\n", "    p = exp(s[j] - lse) * 0 + 1.0 / L;\n"),
+    "FP8 codes read without their scale": (
+        "return oracle_e4m3_decode(((const uint8_t*)pool)[i]) * (double)scl[si];",
+        "return oracle_e4m3_decode(((const uint8_t*)pool)[i]);"),
+    "bf16 query loses its low mantissa bits": ("  return bf16_bits_to_double(((const uint16_t*)jb->q)[i]);",
+                                               "  return bf16_bits_to_double(((const uint16_t*)jb->q)[i] & 0xFF00);"),
+    "e4m3 saturates at 240": ("if (a >= 448.0) return (uint8_t)(sign | 0x7E);", "if (a >= 240.0) return (uint8_t)(sign | 0x77);"),
+    "pool layout: slot outside kv head": ("return (((size_t)block * Hk + g) * ORACLE_BLOCK + slot) * D + d;",
+                                          "return (((size_t)block * ORACLE_BLOCK + slot) * Hk + g) * D + d;"),
+    "truncate frees one block too few": ("  for (lb = keep_blk; lb < nblk; lb++) {", "  for (lb = keep_blk + 1; lb < nblk; lb++) {"),
+    "eviction ignores a block's last token": ("for (j = lo; j < hi && j < L; j++)", "for (j = lo; j + 1 < hi && j < L; j++)"),
+    "combined rule: one sink short": ("const int is_sink = j < sinks,", "const int is_sink = j + 1 < sinks,"),
+    "sequence id: largest free": ("  for (s = 0; s < a->max_seqs; s++) {\n    if (!a->active[s]) {",
+                                  "  for (s = a->max_seqs - 1; s >= 0; s--) {\n    if (!a->active[s]) {"),
+    "freed block goes to the back of the pool": (
+        "  if (a->refcount[b] == 0) a->free_stack[a->free_top++] = b;",
+        "  if (a->refcount[b] == 0) {\n    memmove(a->free_stack + 1, a->free_stack, sizeof(int32_t) * a->free_top);\n"
+        "    a->free_stack[0] = b;\n    a->free_top++;\n  }"),
+    "swap copies in the wrong direction": ("        pairs_out[2 * npairs] = b;\n        pairs_out[2 * npairs + 1] = map[b];",
+                                           "        pairs_out[2 * npairs] = map[b];\n        pairs_out[2 * npairs + 1] = b;"),
+    "compaction takes no fresh blocks": (
+        "    for (k = 0; k < nb; k++) new_blocks[pos++] = take_block(w);\n  }\n  for (i = 0; i < n; i++) {",
+        "    for (k = 0; k < nb; k++) new_blocks[pos++] = 0;\n  }\n  for (i = 0; i < n; i++) {"),
 }
 
 
-@pytest.mark.parametrize("name", sorted(MUTANTS))
-def test_pins_catch_mutant(name, tmp_path):
+def _run_mutant(name, work):
+    """Builds the oracle with one planted mistake and runs the pins against
+    it; returns (pins failed?, the end of their output)."""
     old, new = MUTANTS[name]
     src = open(SRC).read()
-    assert src.count(old) == 1, f"mutation site not unique: {name}"
-    mutant_c = tmp_path / "mutant.c"
+    if src.count(old) != 1:
+        return None, f"mutation site not unique: {name}"
+    d = work / f"m{sorted(MUTANTS).index(name)}"
+    d.mkdir()
+    mutant_c, so = d / "mutant.c", d / "libmutant.so"
     mutant_c.write_text(src.replace(old, new))
-    so = tmp_path / "libmutant.so"
     subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math", "-ffp-contract=off", "-pthread",
                     str(mutant_c), "-o", str(so), "-lm"], check=True)
-    env = dict(os.environ, ORACLE_LIB=str(so))
+    env = dict(os.environ, ORACLE_LIB=str(so), OMP_NUM_THREADS="1")
     r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_oracle_pins.py"), "-x", "-q",
-                        "-p", "no:cacheprovider"], cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
-    assert r.returncode != 0, f"the pins did not catch: {name}\n{r.stdout[-2000:]}"
+                        "-p", "no:cacheprovider"], cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
+    return r.returncode != 0, r.stdout[-2000:]
+
+
+@pytest.fixture(scope="module")
+def mutant_results(tmp_path_factory):
+    """Every mutant's pin run, several at a time (each is an independent
+    process on its own copy of the oracle)."""
+    from concurrent.futures import ThreadPoolExecutor
+    work = tmp_path_factory.mktemp("mutants")
+    names = sorted(MUTANTS)
+    with ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
+        return dict(zip(names, ex.map(lambda n: _run_mutant(n, work), names)))
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, mutant_results):
+    caught, tail = mutant_results[name]
+    assert caught is not None, tail
+    assert caught, f"the pins did not catch: {name}\n{tail}"

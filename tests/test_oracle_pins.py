@@ -385,6 +385,37 @@ def test_h2o_update_matches_page_algorithm():
     assert np.allclose(acc[0, : ref.size], ref, rtol=1e-12, atol=1e-15)
 
 
+
+@pytest.mark.parametrize("mask,S,W", [("sliding", 0, 7), ("sink_window", 4, 9)])
+def test_h2o_update_gives_masked_positions_no_weight(mask, S, W):
+    """Under a mask, a position outside the keep-set gets no attention weight,
+    whatever the logits buffer holds there: the update adds nothing to it,
+    the step still adds exactly 1 in total, and the kept positions get the
+    masked softmax weights (mean over heads) of textbook attention."""
+    wl = workloads.small("fp32", lens=(40,), n_heads=4, n_kv_heads=2, head_dim=16)
+    L = 40
+    alloc, pool, ids, dense = _build_oracle_cache(wl, (L,), seed=11)
+    k, _ = dense[0]
+    mode = {"sliding": oracle.MASK_SLIDING, "sink_window": oracle.MASK_SINK_WINDOW}[mask]
+    q = workloads.queries(wl, 1, step=3)
+    _, lse, logits = oracle.decode(pool, alloc.tables_matrix(ids), [L], workloads.as_bits(q), oracle.KV_FP32,
+                                   wl.n_heads, wl.scale, mode, S, W, want_logits=True, logits_stride=64)
+    kept = torch.zeros(L, dtype=torch.bool)
+    kept[oracle.keep_set(L, mode, S, W)] = True
+    assert 0 < int(kept.sum()) < L
+    ref = _accumulate_h2o([_dense_attention_weights(q[0].double(), k[:L].double(), wl.scale, kept,
+                                                    wl.group)]).numpy()
+    dropped = ~kept.numpy()
+    for fill in (None, 0.0, 50.0):  # masked logits as the decode left them, or finite values
+        lg = logits.copy()
+        if fill is not None:
+            lg[:, :, :L][:, :, dropped] = fill
+        acc = np.zeros((1, 64))
+        oracle.h2o_update(acc, [L], lg, lse, mode, S, W)
+        assert np.all(acc[0, :L][dropped] == 0.0)
+        assert abs(acc.sum() - 1.0) < 1e-12
+        assert np.allclose(acc[0, :L], ref, rtol=1e-12, atol=1e-15)
+
 # --------------------------------------------------------------------------
 # Attention: closed forms, textbook attention (SDPA) and paging invariance.
 # --------------------------------------------------------------------------
@@ -548,6 +579,29 @@ def test_free_pool_initial_order():
     fl = b.free_list().tolist()
     assert sorted(fl) == list(range(50)) and fl != list(range(50))
 
+
+
+def test_smallest_free_sequence_id_and_last_freed_block_first():
+    """The allocator's determinism rules on tiny inputs: a new sequence takes
+    the smallest id not in use; freed blocks go back to the front of the free
+    pool in ascending logical order, so the last one freed is reused first."""
+    a = oracle.OracleAllocator(8, 4, 4, seed=0)
+    assert [a.seq_add() for _ in range(3)] == [0, 1, 2]
+    a.free(1)
+    assert a.seq_add() == 1
+    a.free(2)
+    a.free(0)
+    assert [a.seq_add(), a.seq_add(), a.seq_add()] == [0, 2, 3]
+    b = oracle.OracleAllocator(8, 4, 4, seed=0)  # identity order: block 0 at the front
+    x, y = b.seq_add(), b.seq_add()
+    b.append([x], 20)
+    b.append([y], 1)
+    assert b.table(x).tolist() == [0, 1] and b.table(y).tolist() == [2]
+    b.free(x)  # releases block 0, then block 1
+    assert b.free_list().tolist() == [1, 0, 3, 4, 5, 6, 7]
+    z = b.seq_add()
+    b.append([z], 17)
+    assert b.table(z).tolist() == [1, 0]
 
 def _check_invariants(a, live):
     NB = a.NB
