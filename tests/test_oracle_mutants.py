@@ -76,6 +76,48 @@ MUTANTS = {
     "compaction takes no fresh blocks": (
         "    for (k = 0; k < nb; k++) new_blocks[pos++] = take_block(w);\n  }\n  for (i = 0; i < n; i++) {",
         "    for (k = 0; k < nb; k++) new_blocks[pos++] = 0;\n  }\n  for (i = 0; i < n; i++) {"),
+    "FP8 quantiser's absmax ignores the sign": (
+        "    float v = fabsf(bf16_bits_to_float(x[d]));\n    if (v > amax) amax = v;\n  }\n"
+        "  s = (amax == 0.0f) ? 1.0f : amax / 448.0f;",
+        "    float v = bf16_bits_to_float(x[d]);\n    if (v > amax) amax = v;\n  }\n"
+        "  s = (amax == 0.0f) ? 1.0f : amax / 448.0f;"),
+    "INT8 quantiser's absmax ignores the sign": (
+        "    float v = fabsf(bf16_bits_to_float(x[d]));\n    if (v > amax) amax = v;\n  }\n"
+        "  s = (amax == 0.0f) ? 1.0f : amax / 127.0f;",
+        "    float v = bf16_bits_to_float(x[d]);\n    if (v > amax) amax = v;\n  }\n"
+        "  s = (amax == 0.0f) ? 1.0f : amax / 127.0f;"),
+    "INT8 codes lose their sign": ("return (int8_t)(x < 0.0f ? -n : n);", "return (int8_t)n;"),
+    "quantised scale stored at the neighbouring slot": (
+        "      size_t si = ((size_t)block * q->Hk + g) * ORACLE_BLOCK + slot;",
+        "      size_t si = ((size_t)block * q->Hk + g) * ORACLE_BLOCK + (slot ^ 1);"),
+    "scatter reverses the kv heads": ("      size_t s = (((size_t)t * Hk + g) * D) * (size_t)elem_bytes;",
+                                      "      size_t s = (((size_t)t * Hk + (Hk - 1 - g)) * D) * (size_t)elem_bytes;"),
+    "row copy leaves the K scale": (
+        "        k_scale[((size_t)db * Hk + g) * ORACLE_BLOCK + dso] = k_scale[((size_t)sb * Hk + g) * ORACLE_BLOCK + so];",
+        "        (void)0;"),
+    "block copy leaves V": (
+        "  memcpy((char*)v_pool + (size_t)dst * blk, (char*)v_pool + (size_t)src * blk, blk);\n"
+        "  if (k_scale && v_scale) {\n    size_t sb",
+        "  if (k_scale && v_scale) {\n    size_t sb"),
+    "block copy leaves the K scales": (
+        "    memcpy(k_scale + (size_t)dst * sb, k_scale + (size_t)src * sb, sb * sizeof(float));", "    (void)0;"),
+    "swap copy leaves the V scales": ("      memcpy(dst_vs + d * sb, src_vs + s * sb, sb * sizeof(float));", "      (void)0;"),
+    "e4m3 decode with exponent bias 8": ("    mag = ldexp((double)(8 + m), e - 10); /* (1 + m/8) * 2^(e-7) */",
+                                         "    mag = ldexp((double)(8 + m), e - 11);"),
+    "e4m3 encode loses negative zero": ("  sign = signbit(x) ? 0x80 : 0x00;", "  sign = (x < 0) ? 0x80 : 0x00;"),
+    "swap-in shares no device block": ("      } else {\n        a->refcount[map[b]] += 1;\n      }",
+                                       "      } else {\n        (void)0;\n      }"),
+    "swap never marks sequences": ("    a->swapped[s] = out ? 1 : 0;", "    a->swapped[s] = 0;"),
+    "fork shares full blocks only": (
+        "  nblk = (a->lens[src] + ORACLE_BLOCK - 1) / ORACLE_BLOCK;\n  for (lb = 0; lb < nblk; lb++) {\n"
+        "    int b = a->tables[(size_t)src",
+        "  nblk = a->lens[src] / ORACLE_BLOCK;\n  for (lb = 0; lb < nblk; lb++) {\n    int b = a->tables[(size_t)src"),
+    "softmax sum without the running max": (
+        "    if (oracle_keep(L, jb->mask_mode, jb->num_sinks, jb->window, j)) sum += exp(s[j] - m);",
+        "    if (oracle_keep(L, jb->mask_mode, jb->num_sinks, jb->window, j)) sum += exp(s[j]);"),
+    "combined rule ranks only positions before the window": (
+        "  qsort(c, (size_t)L, sizeof(scored_pos), cmp_desc_score_asc_pos);",
+        "  qsort(c, (size_t)(L > window ? L - window : 0), sizeof(scored_pos), cmp_desc_score_asc_pos);"),
 }
 
 

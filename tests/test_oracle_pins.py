@@ -206,6 +206,39 @@ def test_quantize_row_int8_per_token_scale():
     codes, s = oracle.quantize_row_int8(np.zeros(128, dtype=np.uint16))
     assert s == 1.0 and not codes.any()
 
+@pytest.mark.parametrize("kv", ["fp8", "int8"])
+def test_quantised_scatter_places_codes_and_scale_at_the_token_slot(kv):
+    """Each (token, kv head) row lands at the token's slot: the codes and the
+    scale stored there are the pinned per-token quantisation of that row,
+    and every slot nobody wrote stays zero."""
+    kvd = {"fp8": oracle.KV_FP8, "int8": oracle.KV_INT8}[kv]
+    quant = oracle.quantize_row_bf16 if kv == "fp8" else oracle.quantize_row_int8
+    rng = np.random.default_rng(21)
+    NB, Hk, D, T = 6, 3, 64, 37
+    pool = oracle.OraclePool(NB, Hk, D, kvd)
+    slots = rng.choice(NB * 16, size=T, replace=False)
+
+    def rows():
+        x = rng.standard_normal((T, Hk, D)) * 10 ** rng.uniform(-2, 2, (T, Hk, 1))
+        return workloads.as_bits(torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16))
+
+    kb, vb = rows(), rows()
+    pool.write(slots, kb, vb)
+    written = np.zeros((NB, 16), dtype=bool)
+    for t, sl in enumerate(slots):
+        b, o = divmod(int(sl), 16)
+        written[b, o] = True
+        for g in range(Hk):
+            for codes_arr, scale_arr, src in ((pool.k, pool.k_scale, kb), (pool.v, pool.v_scale, vb)):
+                codes, sc = quant(src[t, g])
+                assert np.array_equal(codes_arr[b, g, o], codes)
+                assert scale_arr[b, g, o] == np.float32(sc)
+    for arr in (pool.k, pool.v):
+        assert not arr.transpose(0, 2, 1, 3)[~written].any()
+    for arr in (pool.k_scale, pool.v_scale):
+        assert not arr.transpose(0, 2, 1)[~written].any()
+
+
 # --------------------------------------------------------------------------
 # Keep-sets versus the pages' own snippets, re-run literally on tiny inputs.
 # --------------------------------------------------------------------------
@@ -571,6 +604,54 @@ def test_page_physical_layout_example():
     b.append([s], L)
     assert b.table(s).tolist() == blocks
 
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8", "int8"])
+def test_block_row_and_swap_copies_move_every_array(kv):
+    """A copy-on-write block copy makes the destination block equal to the
+    source in K, V and both scale arrays and changes nothing else; a row copy
+    does the same for single token slots; swap copies move whole blocks
+    between the device and host pools in the direction asked."""
+    kvd = {"bf16": oracle.KV_BF16, "fp8": oracle.KV_FP8, "int8": oracle.KV_INT8}[kv]
+    rng = np.random.default_rng(5)
+    pool = oracle.OraclePool(5, 2, 32, kvd)
+
+    def arrays():
+        return [x for x in (pool.k, pool.v, pool.k_scale, pool.v_scale) if x is not None]
+
+    for a in arrays():
+        if a.dtype == np.float32:
+            a[...] = rng.standard_normal(a.shape)
+        else:
+            info = np.iinfo(a.dtype)
+            a[...] = rng.integers(info.min, info.max, a.shape, endpoint=True, dtype=a.dtype)
+    before = [a.copy() for a in arrays()]
+    pool.copy_block(1, 3)
+    for a, b0 in zip(arrays(), before):
+        want = b0.copy()
+        want[3] = b0[1]
+        assert np.array_equal(a, want)
+    before = [a.copy() for a in arrays()]
+    src, dst = [5, 17, 40], [70, 2, 33]
+    pool.copy_rows(src, dst)
+    for a, b0 in zip(arrays(), before):
+        want = b0.copy()
+        for s_, d_ in zip(src, dst):
+            want[d_ // 16, :, d_ % 16] = b0[s_ // 16, :, s_ % 16]
+        assert np.array_equal(a, want)
+    pool.add_host_pool(4)
+    host = [x for x in (pool.hk, pool.hv, pool.hk_scale, pool.hv_scale) if x is not None]
+    dev = [a.copy() for a in arrays()]
+    pool.swap_copy(np.array([[4, 2], [0, 1]]), out=True)
+    for h, d0 in zip(host, dev):
+        assert np.array_equal(h[2], d0[4]) and np.array_equal(h[1], d0[0])
+        assert not h[0].any() and not h[3].any()
+    assert all(np.array_equal(a, d0) for a, d0 in zip(arrays(), dev))
+    pool.swap_copy(np.array([[2, 3]]), out=False)
+    for a, d0 in zip(arrays(), dev):
+        want = d0.copy()
+        want[3] = d0[4]
+        assert np.array_equal(a, want)
 
 def test_free_pool_initial_order():
     a = oracle.OracleAllocator(50, 1, 4, seed=0)
