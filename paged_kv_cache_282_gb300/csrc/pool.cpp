@@ -148,9 +148,11 @@ struct HostAllocator {
     }
     return drop_count[b];
   }
-  // per table entry: the position of its last queued patch (valid for the
-  // entries the queue names, rewritten on each collapse)
-  std::vector<int32_t> patch_last;
+  // per table entry: the position of its last queued patch (valid only for
+  // the entries the queue names, which each collapse writes before reading,
+  // so the array is never cleared and its untouched pages are never mapped)
+  std::unique_ptr<int32_t[]> patch_last;
+  size_t patch_last_n = 0;
   // per block: a member of the current wave of copies (current epoch)
   std::vector<uint32_t> wave_mark;
   uint32_t wave_epoch = 0;
@@ -512,7 +514,10 @@ pkv_status make_tensor_map(CUtensorMap* m, void* base, const pkv_pool_config& c)
 // queue order.
 std::vector<TablePatch> dedup_patches(HostAllocator& A, const std::vector<TablePatch>& q) {
   const size_t entries = (size_t)A.max_seqs * A.max_blocks;
-  if (A.patch_last.size() != entries) A.patch_last.assign(entries, 0);
+  if (A.patch_last_n != entries) {
+    A.patch_last.reset(new int32_t[entries]);
+    A.patch_last_n = entries;
+  }
   for (size_t i = 0; i < q.size(); ++i) A.patch_last[q[i].index] = (int32_t)i;
   std::vector<TablePatch> out;
   out.reserve(q.size());
