@@ -418,10 +418,13 @@ pkv_status pkv_test_starve_next_select(pkv_pool* pool);
  * SMs, warps per CTA of the one-sequence and of the two-sequence kernel (one
  * CTA per SM each) -- and the GQA group size.  pkv_test_plan_bytes: builds
  * the plan of a decode call (the same arguments) and copies its uploaded
- * bytes into `out` (cap bytes; *size gets the length) and into info[4] the
- * physical warps, CTAs, partial records and sequences per warp; general != 0
- * forces the general planner instead of the one-pass paths, which must give
- * the same bytes. */
+ * bytes into `out` (cap bytes; *size gets the length) and into info[9] the
+ * physical warps, CTAs, partial records, sequences per warp, and the counts
+ * of pieces, merge items, empty items, group-prefix items and group-prefix
+ * members (the sections of the uploaded plan, in that order, each starting
+ * on a 32-byte boundary after the warp_begin array of warps + 1 entries);
+ * general != 0 forces the general planner instead of the one-pass paths,
+ * which must give the same bytes. */
 pkv_status pkv_test_set_geometry(pkv_pool* pool, int32_t num_sms, int32_t warps_per_cta, int32_t pair_warps_per_cta,
                                  int32_t group);
 pkv_status pkv_test_plan_bytes(pkv_pool* pool, int32_t n_seqs, const int32_t* seq_ids, int32_t mask_mode,

@@ -2528,6 +2528,11 @@ pkv_status pkv_test_plan_bytes(pkv_pool* p, int32_t n, const int32_t* ids, int32
   info[1] = plan.ctas;
   info[2] = plan.n_partials;
   info[3] = plan.nq;
+  info[4] = (int32_t)plan.pieces.size();
+  info[5] = (int32_t)plan.combine.size();
+  info[6] = (int32_t)plan.empty.size();
+  info[7] = (int32_t)plan.prefix_items.size();
+  info[8] = (int32_t)plan.prefix_members.size();
   if (cap < L.bytes || !out) return fail(PKV_ERR_INVALID_ARG, "plan of %zu bytes > cap %zu", L.bytes, cap);
   plan_write(plan, L, (char*)out);
   return PKV_OK;

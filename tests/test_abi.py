@@ -293,7 +293,7 @@ def _plan(pkv, c, ids, mode, S, W, splits, general):
     import ctypes
     buf = ctypes.create_string_buffer(16 << 20)
     size = ctypes.c_size_t()
-    info = (ctypes.c_int32 * 4)()
+    info = (ctypes.c_int32 * 9)()
     arr = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
     pkv._abi.check(c.lib.pkv_test_plan_bytes(c._h, arr.size, arr.ctypes.data_as(ctypes.c_void_p), mode, S, W, splits,
                                              general, buf, len(buf), ctypes.byref(size), info))
@@ -375,3 +375,159 @@ def test_append_to_shared_block_needs_one_copy_fewer_than_sharers(pkv, spare):
     with pytest.raises(pkv.PKVError) as e:  # a sequence listed twice
         lib.reserve_slots([ids[1], ids[1]], 1)
     assert e.value.status == 1
+
+
+# The uploaded plan's records, as laid out by the library (see the test
+# hook's declaration): int32 fields in declaration order.
+_PIECE = np.dtype([(f, "<i4") for f in ("seq_slot", "q_row", "kv_head", "lo", "hi", "ctx_len", "out_index", "flags",
+                                        "q_row1", "out_index1", "item1", "pad")])
+_COMBINE = np.dtype([(f, "<i4") for f in ("q_row", "kv_head", "first", "n")])
+_EMPTY = np.dtype([(f, "<i4") for f in ("q_row", "kv_head")])
+_PITEM = np.dtype([(f, "<i4") for f in ("kv_head", "table_seq", "lo", "hi", "member_begin", "n_members", "p0", "p1")])
+_PMEMBER = np.dtype([(f, "<i4") for f in ("q_row", "out_index", "item", "pad")])
+
+
+def _parse_plan(raw, info):
+    warps, _, _, _, n_pieces, n_combine, n_empty, n_items, n_members = info
+    up = lambda x: (x + 31) & ~31  # noqa: E731
+    off = {"wb": 0}
+    off["pieces"] = up(4 * (warps + 1))
+    off["combine"] = up(off["pieces"] + n_pieces * _PIECE.itemsize)
+    off["counters"] = up(off["combine"] + n_combine * _COMBINE.itemsize)
+    off["empty"] = up(off["counters"] + 4 * n_combine)
+    off["pitems"] = up(off["empty"] + n_empty * _EMPTY.itemsize)
+    off["pmembers"] = up(off["pitems"] + n_items * _PITEM.itemsize)
+    assert len(raw) == off["pmembers"] + n_members * _PMEMBER.itemsize
+    arr = lambda dt, key, cnt: np.frombuffer(raw, dtype=dt, count=cnt, offset=off[key])  # noqa: E731
+    return (arr("<i4", "wb", warps + 1), arr(_PIECE, "pieces", n_pieces), arr(_COMBINE, "combine", n_combine),
+            arr("<i4", "counters", n_combine), arr(_EMPTY, "empty", n_empty), arr(_PITEM, "pitems", n_items),
+            arr(_PMEMBER, "pmembers", n_members))
+
+
+def _check_plan(c, ids, Hk, mode, S, W, splits, raw, info, wpc):
+    """What any decode plan must satisfy, stated from the keep-sets alone:
+    every kept logical block of every (sequence, kv head) is read exactly
+    once (by a piece of the sequence, as the second sequence of a pair whose
+    table holds the same physical blocks, or by a group prefix all of whose
+    members hold them); each (sequence, kv head) either writes its output
+    directly from one run or has one merge item whose records are written
+    exactly once; runs end at warp ends; stream-K warps differ by at most one
+    block of work."""
+    wb, pieces, combine, counters, empty, pitems, pmembers = _parse_plan(raw, info)
+    n = len(ids)
+    lens = [c.seq_len(s) for s in ids]
+    tables = [c.block_table(s) for s in ids]
+    assert info[0] == len(wb) - 1 and (info[0] == 0 or info[0] == info[1] * wpc)
+    assert wb[0] == 0 and wb[-1] == len(pieces) and np.all(np.diff(wb) >= 0)
+    assert not counters.any()
+    item_of = {(int(ci["q_row"]), int(ci["kv_head"])): k for k, ci in enumerate(combine)}
+    assert len(item_of) == len(combine)
+    spans = sorted((int(ci["first"]), int(ci["n"])) for ci in combine)
+    assert all(nn >= 1 for _, nn in spans)
+    assert [f for f, _ in spans] == list(np.cumsum([0] + [nn for _, nn in spans])[:-1])
+    assert sum(nn for _, nn in spans) == info[2]
+    read = {(b, g): [] for b in range(n) for g in range(Hk)}
+    written = {(b, g): [] for b in range(n) for g in range(Hk)}
+    direct = {(b, g): 0 for b in range(n) for g in range(Hk)}
+    for w in range(len(wb) - 1):
+        run = []
+        units = 0
+        for pc in pieces[wb[w]:wb[w + 1]]:
+            b, g = int(pc["q_row"]), int(pc["kv_head"])
+            assert pc["seq_slot"] == ids[b] and pc["ctx_len"] == lens[b] and pc["lo"] < pc["hi"]
+            blocks = list(range(int(pc["lo"]), int(pc["hi"])))
+            units += len(blocks)
+            assert all(tables[b][blocks] >= 0)
+            read[(b, g)] += blocks
+            if pc["q_row1"] >= 0:
+                b1 = int(pc["q_row1"])
+                assert np.array_equal(tables[b1][blocks], tables[b][blocks])
+                read[(b1, g)] += blocks
+            run.append(pc)
+            if not pc["flags"] & 1:
+                continue
+            key = {(int(x["q_row"]), int(x["kv_head"]), int(x["q_row1"]), int(x["out_index"]), int(x["out_index1"]),
+                    int(x["flags"]) >> 1, int(x["item1"])) for x in run}
+            assert len(key) == 1, "a run's pieces share sequence, head and records"
+            if pc["out_index"] >= 0:
+                assert pc["flags"] >> 1 == item_of[(b, g)]
+                written[(b, g)].append(int(pc["out_index"]))
+            else:
+                direct[(b, g)] += 1
+            if pc["q_row1"] >= 0:
+                b1 = int(pc["q_row1"])
+                assert pc["out_index1"] >= 0 and pc["item1"] == item_of[(b1, g)]
+                written[(b1, g)].append(int(pc["out_index1"]))
+            run = []
+        assert not run, "a warp's last piece ends its run"
+    for it in pitems:
+        g, lo, hi = int(it["kv_head"]), int(it["lo"]), int(it["hi"])
+        members = pmembers[int(it["member_begin"]):int(it["member_begin"]) + int(it["n_members"])]
+        assert len(members) == it["n_members"] > 0 and lo < hi
+        ref = c.block_table(int(it["table_seq"]))[lo:hi]
+        for m in members:
+            b = int(m["q_row"])
+            assert np.array_equal(tables[b][lo:hi], ref) and all(ref >= 0)
+            assert m["item"] == item_of[(b, g)]
+            read[(b, g)] += list(range(lo, hi))
+            written[(b, g)].append(int(m["out_index"]))
+    empties = {(int(e["q_row"]), int(e["kv_head"])) for e in empty}
+    assert len(empties) == len(empty)
+    for b in range(n):
+        kept = sorted({j // 16 for j in oracle.keep_set(lens[b], mode, S, W)})
+        for g in range(Hk):
+            assert sorted(read[(b, g)]) == kept, (b, g)
+            assert ((b, g) in empties) == (not kept)
+            if (b, g) in item_of:
+                ci = combine[item_of[(b, g)]]
+                assert direct[(b, g)] == 0
+                assert sorted(written[(b, g)]) == list(range(int(ci["first"]), int(ci["first"]) + int(ci["n"])))
+                if splits > 0:
+                    assert ci["n"] == min(splits, len(kept))
+            elif kept:
+                assert direct[(b, g)] == 1 and not written[(b, g)]
+    if splits == 0 and not len(pitems):
+        per_warp = [sum(int(x["hi"] - x["lo"]) for x in pieces[wb[w]:wb[w + 1]]) for w in range(len(wb) - 1)]
+        busy = [u for u in per_warp if u]
+        assert not busy or max(busy) - min(busy) <= 1
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_decode_plans_read_every_kept_block_once(pkv, seed):
+    """Plans from both planner paths, checked against the keep-sets: random
+    batches (empty, short and long sequences; forks with private suffixes;
+    streaming eviction matching the mask), every mask, explicit splits,
+    sequence pairs and, on some seeds, group prefixes."""
+    rng = random.Random(100 + seed)
+    Hk = (2, 8)[seed % 2]
+    wpc, wpc2 = (16, 12) if seed % 3 == 0 else (12, 12)
+    c = pkv.PagedKVCache(60000, Hk * 4, Hk, 128, 300, 1300, kv_dtype="bf16", host_only=True, alloc_seed=seed)
+    pkv._abi.check(c.lib.pkv_test_set_geometry(c._h, 152 if seed % 4 else 7, wpc, wpc2, 4))
+    if seed % 5 == 4:
+        c.set_cascade(2)
+    ids = []
+    for _ in range(rng.randint(1, 30)):
+        s = c.seq_add()
+        L = 0 if rng.random() < 0.1 else rng.randint(1, 5000 if rng.random() < 0.8 else 40)
+        if L:
+            c.reserve_slots([s], L)
+        ids.append(s)
+        for _ in range(rng.choice([0, 0, 1, 5])):  # forks, some with private suffixes
+            f = c.seq_fork(s)
+            if rng.random() < 0.5:
+                c.reserve_slots([f], rng.randint(1, 300))
+            ids.append(f)
+    rng.shuffle(ids)
+    S, W = rng.randint(0, 40), rng.randint(1, 3000)
+    evicted = [s for s in ids if rng.random() < 0.2]
+    cases = [(0, 0, 0, 0), (0, 0, 0, rng.randint(1, 70)), (1, 0, rng.randint(0, 3000), 0), (1, 0, 500, 16),
+             (2, S, W, 0), (2, 0, 0, 0)]
+    for mode, s_, w_, splits in cases:
+        for general in (0, 1):
+            raw, info = _plan(pkv, c, ids, mode, s_, w_, splits, general)
+            _check_plan(c, ids, Hk, mode, s_, w_, splits, raw, info, wpc2 if info[3] == 2 else wpc)
+    for s in evicted:  # sink + window eviction: the same mask's plans skip the freed blocks
+        c.seq_evict(s, S, W)
+    for general in (0, 1):
+        raw, info = _plan(pkv, c, ids, 2, S, W, 0, general)
+        _check_plan(c, ids, Hk, 2, S, W, 0, raw, info, wpc)
