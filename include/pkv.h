@@ -250,7 +250,8 @@ pkv_status pkv_decode_attn_static(pkv_pool* pool, void* stream, int32_t n_seqs, 
  * and each kept key j, acc[b][j] += (1/n_heads) * sum_h exp(s_hj - lse_h),
  * the attention weight summed over the single decode query and averaged over
  * all query heads.  logits/lse as written by pkv_decode_attn with the same
- * sequences and keep-set.  acc: device [n_seqs][acc_stride] fp32. */
+ * sequences and keep-set.  acc: device [n_seqs][acc_stride] fp32.  At most
+ * 65535 sequences per call (PKV_ERR_UNSUPPORTED above that). */
 pkv_status pkv_h2o_scores(pkv_pool* pool, void* stream, int32_t n_seqs, const int32_t* seq_ids,
                           const float* logits, int64_t logits_stride, const float* lse,
                           int32_t mask_mode, int32_t num_sinks, int32_t window, float* acc,

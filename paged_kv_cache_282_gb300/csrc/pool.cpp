@@ -2348,6 +2348,7 @@ pkv_status pkv_h2o_scores(pkv_pool* p, void* stream, int32_t n, const int32_t* i
   if (pkv_status r = check_seq_list(p, n, ids)) return r;
   if (!valid_mask(mode, S, W)) return fail(PKV_ERR_INVALID_ARG, "invalid mask");
   if (n > 0 && (!logits || !lse || !acc)) return fail(PKV_ERR_INVALID_ARG, "NULL device array");
+  if (n > 65535) return fail(PKV_ERR_UNSUPPORTED, "%d sequences in one score update (at most 65535)", n);
   const auto& A = p->alloc;
   int32_t maxlen = 0, max_keep = 0;
   for (int32_t i = 0; i < n; ++i) {
