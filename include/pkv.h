@@ -24,7 +24,8 @@
  *        Cache 淘汰 (H2O), Flash Attention (tiled online softmax).
  *
  * Conventions
- *   - Every call returns a pkv_status; nothing throws across the ABI.
+ *   - Every call returns a pkv_status; nothing throws across the ABI (a
+ *     failed host allocation inside the library returns PKV_ERR_HOST_MEMORY).
  *     pkv_last_error() gives a message for the calling thread's last failure.
  *   - "device" pointers are CUDA device memory owned by the caller; the
  *     library never frees them.  "host" pointers are ordinary host memory.
@@ -68,7 +69,9 @@ typedef enum {
   PKV_ERR_TIMEOUT = 6,       /* a device-side bounded wait ran out */
   PKV_ERR_DEVICE_ASSERT = 7, /* a device-side range check failed */
   PKV_ERR_NO_DEVICE = 8,     /* device work requested on a host-only pool */
-  PKV_ERR_WORKSPACE = 9      /* workspace too small (see pkv_decode_workspace_size) */
+  PKV_ERR_WORKSPACE = 9,     /* workspace too small (see pkv_decode_workspace_size) */
+  PKV_ERR_HOST_MEMORY = 10   /* a host allocation failed; the pool may be part-way
+                                through the call and should be destroyed */
 } pkv_status;
 
 typedef enum { PKV_KV_FP32 = 0, PKV_KV_BF16 = 1, PKV_KV_FP8_E4M3 = 2, PKV_KV_INT8 = 3 } pkv_kv_dtype;

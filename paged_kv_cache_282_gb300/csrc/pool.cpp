@@ -14,6 +14,7 @@
 #include <cstdio>
 #include <cstring>
 #include <memory>
+#include <new>
 #include <numeric>
 #include <set>
 #include <string>
@@ -42,6 +43,27 @@ static pkv_status fail(pkv_status s, const char* fmt, ...) {
 }
 
 void pkv::set_error(const char* msg) { g_last_error = msg ? msg : ""; }
+
+// Runs an entry point's body; a C++ exception (a failed host allocation)
+// becomes a status instead of crossing the C ABI.
+template <class F>
+static pkv_status guarded(F&& body) noexcept {
+  const char* what = nullptr;
+  pkv_status st = PKV_ERR_HOST_MEMORY;
+  try {
+    return body();
+  } catch (const std::bad_alloc&) {
+    what = "host memory allocation failed";
+  } catch (...) {
+    what = "unexpected C++ exception";
+    st = PKV_ERR_INVALID_ARG;
+  }
+  try {
+    g_last_error = what;
+  } catch (...) {
+  }
+  return st;
+}
 
 #define PKV_CUDA(call)                                                                  \
   do {                                                                                  \
@@ -1571,77 +1593,79 @@ int pkv::decode_attn_into(pkv_pool* p, void* stream, int32_t n, const int32_t* i
                           int32_t mode, int32_t S, int32_t W, int32_t num_splits, void* out, float* lse,
                           float* logits, int64_t logits_stride, void* plan_dev, size_t plan_cap, void* partials_dev,
                           size_t partials_cap) {
-  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
-  if (!p->device) return fail(PKV_ERR_NO_DEVICE, "host-only pool");
-  if (p->cfg.kv_dtype == PKV_KV_FP32)
-    return fail(PKV_ERR_UNSUPPORTED, "static-scratch decode serves bf16 / fp8 / int8 pools");
-  {
-    int cur = -1;
-    if (cudaGetDevice(&cur) != cudaSuccess || cur != p->device_id)
-      return fail(PKV_ERR_INVALID_ARG, "the pool's device (%d) is not the current device (%d)", p->device_id, cur);
-  }
-  if (pkv_status r = check_seq_list(p, n, ids)) return r;
-  if (!valid_mask(mode, S, W)) return fail(PKV_ERR_INVALID_ARG, "invalid mask %d (%d, %d)", mode, S, W);
-  if (num_splits < 0) return fail(PKV_ERR_INVALID_ARG, "num_splits < 0");
-  if (n > 0 && (!q || !out)) return fail(PKV_ERR_INVALID_ARG, "q / out is NULL");
-  HostAllocator& A = p->alloc;
-  int32_t maxlen = 0;
-  for (int32_t i = 0; i < n; ++i) maxlen = std::max(maxlen, A.len[ids[i]]);
-  if (logits && logits_stride < maxlen) return fail(PKV_ERR_INVALID_ARG, "logits_stride < max length");
-  if (pkv_status r = check_keep_blocks_present(p, n, ids, mode, S, W)) return r;
-  const auto& c = p->cfg;
-  cudaStream_t st = (cudaStream_t)stream;
+  return guarded([&]() -> pkv_status {
+    if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    if (!p->device) return fail(PKV_ERR_NO_DEVICE, "host-only pool");
+    if (p->cfg.kv_dtype == PKV_KV_FP32)
+      return fail(PKV_ERR_UNSUPPORTED, "static-scratch decode serves bf16 / fp8 / int8 pools");
+    {
+      int cur = -1;
+      if (cudaGetDevice(&cur) != cudaSuccess || cur != p->device_id)
+        return fail(PKV_ERR_INVALID_ARG, "the pool's device (%d) is not the current device (%d)", p->device_id, cur);
+    }
+    if (pkv_status r = check_seq_list(p, n, ids)) return r;
+    if (!valid_mask(mode, S, W)) return fail(PKV_ERR_INVALID_ARG, "invalid mask %d (%d, %d)", mode, S, W);
+    if (num_splits < 0) return fail(PKV_ERR_INVALID_ARG, "num_splits < 0");
+    if (n > 0 && (!q || !out)) return fail(PKV_ERR_INVALID_ARG, "q / out is NULL");
+    HostAllocator& A = p->alloc;
+    int32_t maxlen = 0;
+    for (int32_t i = 0; i < n; ++i) maxlen = std::max(maxlen, A.len[ids[i]]);
+    if (logits && logits_stride < maxlen) return fail(PKV_ERR_INVALID_ARG, "logits_stride < max length");
+    if (pkv_status r = check_keep_blocks_present(p, n, ids, mode, S, W)) return r;
+    const auto& c = p->cfg;
+    cudaStream_t st = (cudaStream_t)stream;
 
-  // queued allocator effects: last value per table entry; copies in waves
-  const std::vector<TablePatch> patches = dedup_patches(A, A.pending_patch);
-  const size_t ncow = A.pending_cow.size() / 2;
-  const std::vector<size_t> waves = cow_waves(A);
-  Plan empty_plan;
-  Plan& plan = n > 0 ? build_plan(p, n, ids, mode, S, W, num_splits) : empty_plan;
-  const size_t pf = (size_t)partial_floats(p->G, c.head_dim) * sizeof(float);
-  if ((size_t)plan.n_partials * pf > partials_cap)
-    return fail(PKV_ERR_WORKSPACE, "needs %zu bytes of partial records, the static scratch holds %zu",
-                (size_t)plan.n_partials * pf, partials_cap);
+    // queued allocator effects: last value per table entry; copies in waves
+    const std::vector<TablePatch> patches = dedup_patches(A, A.pending_patch);
+    const size_t ncow = A.pending_cow.size() / 2;
+    const std::vector<size_t> waves = cow_waves(A);
+    Plan empty_plan;
+    Plan& plan = n > 0 ? build_plan(p, n, ids, mode, S, W, num_splits) : empty_plan;
+    const size_t pf = (size_t)partial_floats(p->G, c.head_dim) * sizeof(float);
+    if ((size_t)plan.n_partials * pf > partials_cap)
+      return fail(PKV_ERR_WORKSPACE, "needs %zu bytes of partial records, the static scratch holds %zu",
+                  (size_t)plan.n_partials * pf, partials_cap);
 
-  // one blob: [cow pairs][patches][plan]
-  auto up32 = [](size_t x) { return (x + 31) & ~size_t(31); };
-  const size_t cow_off = 0, patch_off = up32(ncow * 2 * sizeof(int32_t));
-  const PlanLayout L =
-      plan_layout(plan, warps_per_cta(p, plan.nq), patch_off + patches.size() * sizeof(TablePatch));
-  const size_t bytes = L.bytes;
-  if (bytes > plan_cap)
-    return fail(PKV_ERR_WORKSPACE, "needs %zu bytes of plan, the static scratch holds %zu", bytes, plan_cap);
-  std::vector<char>& blob = plan_cache(p).blob;
-  if (blob.size() < bytes) blob.resize(bytes);
-  if (ncow) memcpy(blob.data() + cow_off, A.pending_cow.data(), ncow * 2 * sizeof(int32_t));
-  if (!patches.empty()) memcpy(blob.data() + patch_off, patches.data(), patches.size() * sizeof(TablePatch));
-  plan_write(plan, L, blob.data());
-  char* dev = (char*)plan_dev;
-  if (bytes) PKV_CUDA(cudaMemcpyAsync(dev, blob.data(), bytes, cudaMemcpyHostToDevice, st));
+    // one blob: [cow pairs][patches][plan]
+    auto up32 = [](size_t x) { return (x + 31) & ~size_t(31); };
+    const size_t cow_off = 0, patch_off = up32(ncow * 2 * sizeof(int32_t));
+    const PlanLayout L =
+        plan_layout(plan, warps_per_cta(p, plan.nq), patch_off + patches.size() * sizeof(TablePatch));
+    const size_t bytes = L.bytes;
+    if (bytes > plan_cap)
+      return fail(PKV_ERR_WORKSPACE, "needs %zu bytes of plan, the static scratch holds %zu", bytes, plan_cap);
+    std::vector<char>& blob = plan_cache(p).blob;
+    if (blob.size() < bytes) blob.resize(bytes);
+    if (ncow) memcpy(blob.data() + cow_off, A.pending_cow.data(), ncow * 2 * sizeof(int32_t));
+    if (!patches.empty()) memcpy(blob.data() + patch_off, patches.data(), patches.size() * sizeof(TablePatch));
+    plan_write(plan, L, blob.data());
+    char* dev = (char*)plan_dev;
+    if (bytes) PKV_CUDA(cudaMemcpyAsync(dev, blob.data(), bytes, cudaMemcpyHostToDevice, st));
 
-  if (ncow) {
-    const size_t blk_bytes = (size_t)c.n_kv_heads * kBlock * c.head_dim * elem_bytes(c.kv_dtype);
-    const size_t scl = has_scales(c.kv_dtype) ? (size_t)c.n_kv_heads * kBlock : 0;
-    for (size_t w = 0; w + 1 < waves.size(); ++w) {
-      const size_t k0 = waves[w], k1 = waves[w + 1];
-      if (k1 == k0) continue;
-      if (pkv_status r = launch(p, PKV_KERNEL_COW_COPY, st, [&] {
-            return launch_cow_copy((const int32_t*)(dev + cow_off) + 2 * k0, (int)(k1 - k0), p->buf.k_pool,
-                                   p->buf.v_pool, p->buf.k_scale, p->buf.v_scale, blk_bytes, scl, st);
+    if (ncow) {
+      const size_t blk_bytes = (size_t)c.n_kv_heads * kBlock * c.head_dim * elem_bytes(c.kv_dtype);
+      const size_t scl = has_scales(c.kv_dtype) ? (size_t)c.n_kv_heads * kBlock : 0;
+      for (size_t w = 0; w + 1 < waves.size(); ++w) {
+        const size_t k0 = waves[w], k1 = waves[w + 1];
+        if (k1 == k0) continue;
+        if (pkv_status r = launch(p, PKV_KERNEL_COW_COPY, st, [&] {
+              return launch_cow_copy((const int32_t*)(dev + cow_off) + 2 * k0, (int)(k1 - k0), p->buf.k_pool,
+                                     p->buf.v_pool, p->buf.k_scale, p->buf.v_scale, blk_bytes, scl, st);
+            }))
+          return r;
+      }
+    }
+    if (!patches.empty()) {
+      if (pkv_status r = launch(p, PKV_KERNEL_TABLE_PATCH, st, [&] {
+            return launch_table_patch((const int32_t*)(dev + patch_off), (int)patches.size(), p->buf.block_tables, st);
           }))
         return r;
     }
-  }
-  if (!patches.empty()) {
-    if (pkv_status r = launch(p, PKV_KERNEL_TABLE_PATCH, st, [&] {
-          return launch_table_patch((const int32_t*)(dev + patch_off), (int)patches.size(), p->buf.block_tables, st);
-        }))
-      return r;
-  }
-  A.pending_cow.clear();
-  A.pending_patch.clear();
-  if (n == 0) return PKV_OK;
-  return launch_tc_plan(p, st, plan, L, dev, q, scale, mode, S, W, out, lse, logits, logits_stride, partials_dev);
+    A.pending_cow.clear();
+    A.pending_patch.clear();
+    if (n == 0) return PKV_OK;
+    return launch_tc_plan(p, st, plan, L, dev, q, scale, mode, S, W, out, lse, logits, logits_stride, partials_dev);
+  });
 }
 
 // ---------------------------------------------------------------------------
@@ -1767,76 +1791,80 @@ const char* pkv_last_error(void) { return g_last_error.c_str(); }
 const char* pkv_version(void) { return "pkv 0.1 (sm_103a)"; }
 
 pkv_status pkv_pool_required_bytes(const pkv_pool_config* cfg, pkv_buffer_sizes* out) {
-  if (pkv_status r = check_config(cfg)) return r;
-  if (!out) return fail(PKV_ERR_INVALID_ARG, "out is NULL");
-  const size_t rows = (size_t)cfg->num_blocks * cfg->n_kv_heads * kBlock;
-  out->k_pool = out->v_pool = rows * cfg->head_dim * elem_bytes(cfg->kv_dtype);
-  out->k_scale = out->v_scale = has_scales(cfg->kv_dtype) ? rows * sizeof(float) : 0;
-  out->block_tables = (size_t)cfg->max_seqs * cfg->max_blocks_per_seq * sizeof(int32_t);
-  out->status = 4 * sizeof(int32_t);
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    if (pkv_status r = check_config(cfg)) return r;
+    if (!out) return fail(PKV_ERR_INVALID_ARG, "out is NULL");
+    const size_t rows = (size_t)cfg->num_blocks * cfg->n_kv_heads * kBlock;
+    out->k_pool = out->v_pool = rows * cfg->head_dim * elem_bytes(cfg->kv_dtype);
+    out->k_scale = out->v_scale = has_scales(cfg->kv_dtype) ? rows * sizeof(float) : 0;
+    out->block_tables = (size_t)cfg->max_seqs * cfg->max_blocks_per_seq * sizeof(int32_t);
+    out->status = 4 * sizeof(int32_t);
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_pool_create(const pkv_pool_config* cfg, const pkv_pool_buffers* buffers, pkv_pool** out) {
-  if (!out) return fail(PKV_ERR_INVALID_ARG, "out is NULL");
-  *out = nullptr;
-  if (pkv_status r = check_config(cfg)) return r;
-  pkv_pool* p = new pkv_pool();
-  p->cfg = *cfg;
-  p->cfg.free_order = nullptr;
-  p->G = cfg->n_heads / cfg->n_kv_heads;
-  p->alloc.init(cfg->num_blocks, cfg->max_seqs, cfg->max_blocks_per_seq, cfg->alloc_seed, cfg->free_order);
-  if (buffers) {
-    const auto& b = *buffers;
-    const bool fp8 = has_scales(cfg->kv_dtype);
-    if (!b.k_pool || !b.v_pool || !b.block_tables || !b.status || (fp8 && (!b.k_scale || !b.v_scale))) {
-      delete p;
-      return fail(PKV_ERR_INVALID_ARG, "a required device buffer is NULL");
+  return guarded([&]() -> pkv_status {
+    if (!out) return fail(PKV_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (pkv_status r = check_config(cfg)) return r;
+    pkv_pool* p = new pkv_pool();
+    p->cfg = *cfg;
+    p->cfg.free_order = nullptr;
+    p->G = cfg->n_heads / cfg->n_kv_heads;
+    p->alloc.init(cfg->num_blocks, cfg->max_seqs, cfg->max_blocks_per_seq, cfg->alloc_seed, cfg->free_order);
+    if (buffers) {
+      const auto& b = *buffers;
+      const bool fp8 = has_scales(cfg->kv_dtype);
+      if (!b.k_pool || !b.v_pool || !b.block_tables || !b.status || (fp8 && (!b.k_scale || !b.v_scale))) {
+        delete p;
+        return fail(PKV_ERR_INVALID_ARG, "a required device buffer is NULL");
+      }
+      if (((uintptr_t)b.k_pool | (uintptr_t)b.v_pool) & 127) {
+        delete p;
+        return fail(PKV_ERR_INVALID_ARG, "k_pool / v_pool must be 128-byte aligned");
+      }
+      if (fp8 && (((uintptr_t)b.k_scale | (uintptr_t)b.v_scale) & 15)) {
+        delete p;
+        return fail(PKV_ERR_INVALID_ARG, "k_scale / v_scale must be 16-byte aligned");
+      }
+      p->device = true;
+      p->alloc.queue = true;
+      p->buf = b;
+      auto fail_dev = [&](pkv_status r) {
+        p->staging.destroy();
+        delete p;
+        return r;
+      };
+      cudaError_t e = cudaGetDevice(&p->device_id);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device_id);
+      if (e != cudaSuccess) return fail_dev(fail(PKV_ERR_CUDA, "device query failed: %s", cudaGetErrorString(e)));
+      const size_t tbytes = (size_t)cfg->max_seqs * cfg->max_blocks_per_seq * sizeof(int32_t);
+      e = cudaMemset(b.block_tables, 0xFF, tbytes);
+      if (e == cudaSuccess) e = cudaMemset(b.status, 0, 4 * sizeof(int32_t));
+      if (e == cudaSuccess) e = cudaDeviceSynchronize();
+      if (e != cudaSuccess) return fail_dev(fail(PKV_ERR_CUDA, "buffer init failed: %s", cudaGetErrorString(e)));
+      if (cfg->kv_dtype != PKV_KV_FP32) {
+        p->tc_path = true;
+        if (pkv_status r = make_tensor_map(&p->tmap_k, b.k_pool, p->cfg)) return fail_dev(r);
+        if (pkv_status r = make_tensor_map(&p->tmap_v, b.v_pool, p->cfg)) return fail_dev(r);
+        e = decode_tc_prepare(cfg->kv_dtype, p->G, 1);
+        if (e == cudaSuccess) e = decode_tc_prepare(cfg->kv_dtype, p->G, 2);
+        if (e == cudaSuccess && cfg->kv_dtype == PKV_KV_BF16) e = prefix_decode_prepare(p->G);
+        int occ = 0, occ2 = 0;
+        if (e == cudaSuccess) e = decode_tc_occupancy(cfg->kv_dtype, p->G, 1, &occ);
+        if (e == cudaSuccess) e = decode_tc_occupancy(cfg->kv_dtype, p->G, 2, &occ2);
+        if (e != cudaSuccess) return fail_dev(fail(PKV_ERR_CUDA, "decode kernel setup failed: %s", cudaGetErrorString(e)));
+        p->tc_ctas_per_sm = std::max(1, occ);
+        p->tc_warps_per_cta = decode_tc_warps_per_cta(cfg->kv_dtype, 1);
+        p->tc2_ctas_per_sm = std::max(1, occ2);
+        p->tc2_warps_per_cta = decode_tc_warps_per_cta(cfg->kv_dtype, 2);
+        p->tc_smem = decode_tc_smem_bytes(cfg->kv_dtype, 1);
+      }
     }
-    if (((uintptr_t)b.k_pool | (uintptr_t)b.v_pool) & 127) {
-      delete p;
-      return fail(PKV_ERR_INVALID_ARG, "k_pool / v_pool must be 128-byte aligned");
-    }
-    if (fp8 && (((uintptr_t)b.k_scale | (uintptr_t)b.v_scale) & 15)) {
-      delete p;
-      return fail(PKV_ERR_INVALID_ARG, "k_scale / v_scale must be 16-byte aligned");
-    }
-    p->device = true;
-    p->alloc.queue = true;
-    p->buf = b;
-    auto fail_dev = [&](pkv_status r) {
-      p->staging.destroy();
-      delete p;
-      return r;
-    };
-    cudaError_t e = cudaGetDevice(&p->device_id);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device_id);
-    if (e != cudaSuccess) return fail_dev(fail(PKV_ERR_CUDA, "device query failed: %s", cudaGetErrorString(e)));
-    const size_t tbytes = (size_t)cfg->max_seqs * cfg->max_blocks_per_seq * sizeof(int32_t);
-    e = cudaMemset(b.block_tables, 0xFF, tbytes);
-    if (e == cudaSuccess) e = cudaMemset(b.status, 0, 4 * sizeof(int32_t));
-    if (e == cudaSuccess) e = cudaDeviceSynchronize();
-    if (e != cudaSuccess) return fail_dev(fail(PKV_ERR_CUDA, "buffer init failed: %s", cudaGetErrorString(e)));
-    if (cfg->kv_dtype != PKV_KV_FP32) {
-      p->tc_path = true;
-      if (pkv_status r = make_tensor_map(&p->tmap_k, b.k_pool, p->cfg)) return fail_dev(r);
-      if (pkv_status r = make_tensor_map(&p->tmap_v, b.v_pool, p->cfg)) return fail_dev(r);
-      e = decode_tc_prepare(cfg->kv_dtype, p->G, 1);
-      if (e == cudaSuccess) e = decode_tc_prepare(cfg->kv_dtype, p->G, 2);
-      if (e == cudaSuccess && cfg->kv_dtype == PKV_KV_BF16) e = prefix_decode_prepare(p->G);
-      int occ = 0, occ2 = 0;
-      if (e == cudaSuccess) e = decode_tc_occupancy(cfg->kv_dtype, p->G, 1, &occ);
-      if (e == cudaSuccess) e = decode_tc_occupancy(cfg->kv_dtype, p->G, 2, &occ2);
-      if (e != cudaSuccess) return fail_dev(fail(PKV_ERR_CUDA, "decode kernel setup failed: %s", cudaGetErrorString(e)));
-      p->tc_ctas_per_sm = std::max(1, occ);
-      p->tc_warps_per_cta = decode_tc_warps_per_cta(cfg->kv_dtype, 1);
-      p->tc2_ctas_per_sm = std::max(1, occ2);
-      p->tc2_warps_per_cta = decode_tc_warps_per_cta(cfg->kv_dtype, 2);
-      p->tc_smem = decode_tc_smem_bytes(cfg->kv_dtype, 1);
-    }
-  }
-  *out = p;
-  return PKV_OK;
+    *out = p;
+    return PKV_OK;
+  });
 }
 
 void pkv_pool_destroy(pkv_pool* p) {
@@ -1849,532 +1877,574 @@ void pkv_pool_destroy(pkv_pool* p) {
 }
 
 pkv_status pkv_seq_add(pkv_pool* p, int32_t* seq_out) {
-  if (!p || !seq_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
-  auto& A = p->alloc;
-  if (A.free_ids.empty()) return fail(PKV_ERR_OUT_OF_SEQS, "all %d sequence ids are in use", A.max_seqs);
-  int32_t s = *A.free_ids.begin();
-  A.free_ids.erase(A.free_ids.begin());
-  A.live[s] = 1;
-  A.holes[s] = 0;
-  A.len[s] = 0;
-  A.table[s].clear();
-  *seq_out = s;
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    if (!p || !seq_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+    auto& A = p->alloc;
+    if (A.free_ids.empty()) return fail(PKV_ERR_OUT_OF_SEQS, "all %d sequence ids are in use", A.max_seqs);
+    int32_t s = *A.free_ids.begin();
+    A.free_ids.erase(A.free_ids.begin());
+    A.live[s] = 1;
+    A.holes[s] = 0;
+    A.len[s] = 0;
+    A.table[s].clear();
+    *seq_out = s;
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_seq_fork(pkv_pool* p, int32_t src, int32_t* dst_out) {
-  if (!p || !dst_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
-  auto& A = p->alloc;
-  if (!A.on_device(src)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live or is swapped out", src);
-  int32_t d;
-  if (pkv_status r = pkv_seq_add(p, &d)) return r;
-  const int32_t nblk = ceil_div(A.len[src], kBlock);
-  for (int32_t lb = 0; lb < nblk; ++lb) {
-    const int32_t b = A.table[src][lb];
-    if (b >= 0) ++A.refcount[b];
-    A.set_entry(d, lb, b);
-  }
-  A.len[d] = A.len[src];
-  A.holes[d] = A.holes[src];
-  *dst_out = d;
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    if (!p || !dst_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+    auto& A = p->alloc;
+    if (!A.on_device(src)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live or is swapped out", src);
+    int32_t d;
+    if (pkv_status r = pkv_seq_add(p, &d)) return r;
+    const int32_t nblk = ceil_div(A.len[src], kBlock);
+    for (int32_t lb = 0; lb < nblk; ++lb) {
+      const int32_t b = A.table[src][lb];
+      if (b >= 0) ++A.refcount[b];
+      A.set_entry(d, lb, b);
+    }
+    A.len[d] = A.len[src];
+    A.holes[d] = A.holes[src];
+    *dst_out = d;
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_seq_truncate(pkv_pool* p, int32_t s, int32_t new_len) {
-  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
-  auto& A = p->alloc;
-  if (!A.on_device(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live or is swapped out", s);
-  if (new_len < 0 || new_len > A.len[s]) return fail(PKV_ERR_INVALID_ARG, "new_len %d outside [0, %d]", new_len, A.len[s]);
-  const int32_t keep_blk = ceil_div(new_len, kBlock);
-  if (new_len % kBlock && A.table[s][keep_blk - 1] < 0)
-    return fail(PKV_ERR_INVALID_ARG, "the new last block of sequence %d was evicted", s);
-  A.drop_from(s, keep_blk);
-  A.len[s] = new_len;
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    auto& A = p->alloc;
+    if (!A.on_device(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live or is swapped out", s);
+    if (new_len < 0 || new_len > A.len[s]) return fail(PKV_ERR_INVALID_ARG, "new_len %d outside [0, %d]", new_len, A.len[s]);
+    const int32_t keep_blk = ceil_div(new_len, kBlock);
+    if (new_len % kBlock && A.table[s][keep_blk - 1] < 0)
+      return fail(PKV_ERR_INVALID_ARG, "the new last block of sequence %d was evicted", s);
+    A.drop_from(s, keep_blk);
+    A.len[s] = new_len;
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_seq_truncate_many(pkv_pool* p, int32_t n, const int32_t* ids, const int32_t* new_lens) {
-  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
-  if (n < 0 || (n > 0 && (!ids || !new_lens))) return fail(PKV_ERR_INVALID_ARG, "bad arrays");
-  auto& A = p->alloc;
-  for (int32_t i = 0; i < n; ++i) {  // validate everything before changing anything
-    const int32_t s = ids[i], L = new_lens[i];
-    if (!A.on_device(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live or is swapped out", s);
-    if (L < 0 || L > A.len[s]) return fail(PKV_ERR_INVALID_ARG, "new_len %d outside [0, %d]", L, A.len[s]);
-    if (L % kBlock && A.table[s][ceil_div(L, kBlock) - 1] < 0)
-      return fail(PKV_ERR_INVALID_ARG, "the new last block of sequence %d was evicted", s);
-  }
-  if (const int32_t d = A.first_repeat(n, ids); d >= 0)
-    return fail(PKV_ERR_INVALID_ARG, "sequence %d listed twice", d);
-  for (int32_t i = 0; i < n; ++i) {
-    A.drop_from(ids[i], ceil_div(new_lens[i], kBlock));
-    A.len[ids[i]] = new_lens[i];
-  }
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    if (n < 0 || (n > 0 && (!ids || !new_lens))) return fail(PKV_ERR_INVALID_ARG, "bad arrays");
+    auto& A = p->alloc;
+    for (int32_t i = 0; i < n; ++i) {  // validate everything before changing anything
+      const int32_t s = ids[i], L = new_lens[i];
+      if (!A.on_device(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live or is swapped out", s);
+      if (L < 0 || L > A.len[s]) return fail(PKV_ERR_INVALID_ARG, "new_len %d outside [0, %d]", L, A.len[s]);
+      if (L % kBlock && A.table[s][ceil_div(L, kBlock) - 1] < 0)
+        return fail(PKV_ERR_INVALID_ARG, "the new last block of sequence %d was evicted", s);
+    }
+    if (const int32_t d = A.first_repeat(n, ids); d >= 0)
+      return fail(PKV_ERR_INVALID_ARG, "sequence %d listed twice", d);
+    for (int32_t i = 0; i < n; ++i) {
+      A.drop_from(ids[i], ceil_div(new_lens[i], kBlock));
+      A.len[ids[i]] = new_lens[i];
+    }
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_seq_free(pkv_pool* p, int32_t s) {
-  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
-  auto& A = p->alloc;
-  if (A.valid_seq(s) && A.swapped[s]) {  // give back the host blocks, ascending
-    for (int32_t hb : A.host_table[s])
-      if (hb >= 0) A.release_host(hb);
-    A.host_table[s].clear();
-    A.table[s].clear();
-    A.swapped[s] = 0;
-    A.len[s] = 0;
-  } else if (pkv_status r = pkv_seq_truncate(p, s, 0)) {
-    return r;
-  }
-  A.live[s] = 0;
-  A.holes[s] = 0;
-  A.free_ids.insert(s);
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    auto& A = p->alloc;
+    if (A.valid_seq(s) && A.swapped[s]) {  // give back the host blocks, ascending
+      for (int32_t hb : A.host_table[s])
+        if (hb >= 0) A.release_host(hb);
+      A.host_table[s].clear();
+      A.table[s].clear();
+      A.swapped[s] = 0;
+      A.len[s] = 0;
+    } else if (pkv_status r = pkv_seq_truncate(p, s, 0)) {
+      return r;
+    }
+    A.live[s] = 0;
+    A.holes[s] = 0;
+    A.free_ids.insert(s);
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_seq_evict(pkv_pool* p, int32_t s, int32_t S, int32_t W) {
-  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
-  auto& A = p->alloc;
-  if (!A.valid_seq(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", s);
-  if (S < 0 || W < 1) return fail(PKV_ERR_INVALID_ARG, "need num_sinks >= 0 and window >= 1");
-  if (A.swapped[s]) return fail(PKV_ERR_INVALID_ARG, "sequence %d is swapped out", s);
-  const int32_t L = A.len[s];
-  if ((int64_t)L <= (int64_t)S + W) return PKV_OK;
-  const int32_t nblk = ceil_div(L, kBlock);
-  for (int32_t lb = 0; lb < nblk; ++lb) {
-    const int32_t b = A.table[s][lb];
-    if (b < 0) continue;
-    const int32_t lo = lb * kBlock, hi = std::min(L, lo + kBlock);  // tokens [lo, hi)
-    const bool touches_sinks = lo < S;
-    const bool touches_window = hi > L - W;
-    if (!touches_sinks && !touches_window) {
-      A.release(b);
-      A.set_entry(s, lb, -1);
-      A.holes[s] = 1;
+  return guarded([&]() -> pkv_status {
+    if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    auto& A = p->alloc;
+    if (!A.valid_seq(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", s);
+    if (S < 0 || W < 1) return fail(PKV_ERR_INVALID_ARG, "need num_sinks >= 0 and window >= 1");
+    if (A.swapped[s]) return fail(PKV_ERR_INVALID_ARG, "sequence %d is swapped out", s);
+    const int32_t L = A.len[s];
+    if ((int64_t)L <= (int64_t)S + W) return PKV_OK;
+    const int32_t nblk = ceil_div(L, kBlock);
+    for (int32_t lb = 0; lb < nblk; ++lb) {
+      const int32_t b = A.table[s][lb];
+      if (b < 0) continue;
+      const int32_t lo = lb * kBlock, hi = std::min(L, lo + kBlock);  // tokens [lo, hi)
+      const bool touches_sinks = lo < S;
+      const bool touches_window = hi > L - W;
+      if (!touches_sinks && !touches_window) {
+        A.release(b);
+        A.set_entry(s, lb, -1);
+        A.holes[s] = 1;
+      }
     }
-  }
-  return PKV_OK;
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_seq_len(const pkv_pool* p, int32_t s, int32_t* len_out) {
-  if (!p || !len_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
-  if (!p->alloc.valid_seq(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", s);
-  *len_out = p->alloc.len[s];
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    if (!p || !len_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+    if (!p->alloc.valid_seq(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", s);
+    *len_out = p->alloc.len[s];
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_get_block_table(const pkv_pool* p, int32_t s, int32_t* host_out, int32_t cap, int32_t* n_out) {
-  if (!p || !n_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
-  const auto& A = p->alloc;
-  if (!A.valid_seq(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", s);
-  const int32_t n = ceil_div(A.len[s], kBlock);
-  *n_out = n;
-  if (n > cap || (n > 0 && !host_out)) return fail(PKV_ERR_INVALID_ARG, "capacity %d < %d entries", cap, n);
-  for (int32_t i = 0; i < n; ++i) host_out[i] = A.table[s][i];
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    if (!p || !n_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+    const auto& A = p->alloc;
+    if (!A.valid_seq(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", s);
+    const int32_t n = ceil_div(A.len[s], kBlock);
+    *n_out = n;
+    if (n > cap || (n > 0 && !host_out)) return fail(PKV_ERR_INVALID_ARG, "capacity %d < %d entries", cap, n);
+    for (int32_t i = 0; i < n; ++i) host_out[i] = A.table[s][i];
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_pool_stats(const pkv_pool* p, pkv_stats* out) {
-  if (!p || !out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
-  const auto& A = p->alloc;
-  out->num_blocks = A.NB;
-  out->free_blocks = (int64_t)A.free_blocks.size();
-  out->used_blocks = A.NB - out->free_blocks;
-  out->shared_blocks = 0;
-  for (int32_t r : A.refcount) out->shared_blocks += r > 1;
-  out->active_seqs = A.max_seqs - (int64_t)A.free_ids.size();
-  out->cow_copies = A.cow_count;
-  out->blocks_allocated = A.n_alloc;
-  out->blocks_freed = A.n_freed;
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    if (!p || !out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+    const auto& A = p->alloc;
+    out->num_blocks = A.NB;
+    out->free_blocks = (int64_t)A.free_blocks.size();
+    out->used_blocks = A.NB - out->free_blocks;
+    out->shared_blocks = 0;
+    for (int32_t r : A.refcount) out->shared_blocks += r > 1;
+    out->active_seqs = A.max_seqs - (int64_t)A.free_ids.size();
+    out->cow_copies = A.cow_count;
+    out->blocks_allocated = A.n_alloc;
+    out->blocks_freed = A.n_freed;
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_reserve_slots(pkv_pool* p, int32_t n, const int32_t* ids, int32_t T, int64_t* slots_out,
                              int32_t* cow_out, int32_t cow_cap, int32_t* n_cow_out) {
-  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
-  if (T < 0) return fail(PKV_ERR_INVALID_ARG, "T < 0");
-  if (pkv_status r = check_seq_list(p, n, ids)) return r;
-  auto& A = p->alloc;
-  if (A.first_repeat(n, ids) >= 0) return fail(PKV_ERR_INVALID_ARG, "a sequence appears twice in one append");
-  // dry run: count the blocks needed, with the refcount drops earlier
-  // copies in this call cause
-  int64_t need = 0;
-  A.begin_drops();
-  for (int32_t i = 0; i < n; ++i) {
-    const int32_t s = ids[i];
-    if ((int64_t)A.len[s] + T > (int64_t)A.max_blocks * kBlock)
-      return fail(PKV_ERR_INVALID_ARG, "sequence %d would exceed max_blocks_per_seq", s);
-    for (int32_t t = 0; t < T; ++t) {
-      const int32_t pos = A.len[s] + t;
-      if (pos % kBlock == 0) {
-        ++need;
-      } else if (t == 0) {
-        const int32_t b = A.table[s][pos / kBlock];
-        if (b < 0) return fail(PKV_ERR_INVALID_ARG, "sequence %d: last block was evicted", s);
-        if (A.refcount[b] - A.dropped(b) > 1) {
+  return guarded([&]() -> pkv_status {
+    if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    if (T < 0) return fail(PKV_ERR_INVALID_ARG, "T < 0");
+    if (pkv_status r = check_seq_list(p, n, ids)) return r;
+    auto& A = p->alloc;
+    if (A.first_repeat(n, ids) >= 0) return fail(PKV_ERR_INVALID_ARG, "a sequence appears twice in one append");
+    // dry run: count the blocks needed, with the refcount drops earlier
+    // copies in this call cause
+    int64_t need = 0;
+    A.begin_drops();
+    for (int32_t i = 0; i < n; ++i) {
+      const int32_t s = ids[i];
+      if ((int64_t)A.len[s] + T > (int64_t)A.max_blocks * kBlock)
+        return fail(PKV_ERR_INVALID_ARG, "sequence %d would exceed max_blocks_per_seq", s);
+      for (int32_t t = 0; t < T; ++t) {
+        const int32_t pos = A.len[s] + t;
+        if (pos % kBlock == 0) {
           ++need;
-          ++A.dropped(b);
+        } else if (t == 0) {
+          const int32_t b = A.table[s][pos / kBlock];
+          if (b < 0) return fail(PKV_ERR_INVALID_ARG, "sequence %d: last block was evicted", s);
+          if (A.refcount[b] - A.dropped(b) > 1) {
+            ++need;
+            ++A.dropped(b);
+          }
         }
       }
     }
-  }
-  if (need > (int64_t)A.free_blocks.size())
-    return fail(PKV_ERR_OUT_OF_BLOCKS, "append needs %lld blocks, %zu free", (long long)need, A.free_blocks.size());
-  int32_t ncow = 0;
-  for (int32_t i = 0; i < n; ++i) {
-    const int32_t s = ids[i];
-    for (int32_t t = 0; t < T; ++t) {
-      const int32_t pos = A.len[s];
-      const int32_t lb = pos / kBlock;
-      if (pos % kBlock == 0) {
-        A.set_entry(s, lb, A.take());
-      } else if (A.refcount[A.table[s][lb]] > 1) {
-        const int32_t old = A.table[s][lb];
-        const int32_t fresh = A.take();
-        --A.refcount[old];
-        A.set_entry(s, lb, fresh);
-        if (A.queue) {
-          A.pending_cow.push_back(old);
-          A.pending_cow.push_back(fresh);
+    if (need > (int64_t)A.free_blocks.size())
+      return fail(PKV_ERR_OUT_OF_BLOCKS, "append needs %lld blocks, %zu free", (long long)need, A.free_blocks.size());
+    int32_t ncow = 0;
+    for (int32_t i = 0; i < n; ++i) {
+      const int32_t s = ids[i];
+      for (int32_t t = 0; t < T; ++t) {
+        const int32_t pos = A.len[s];
+        const int32_t lb = pos / kBlock;
+        if (pos % kBlock == 0) {
+          A.set_entry(s, lb, A.take());
+        } else if (A.refcount[A.table[s][lb]] > 1) {
+          const int32_t old = A.table[s][lb];
+          const int32_t fresh = A.take();
+          --A.refcount[old];
+          A.set_entry(s, lb, fresh);
+          if (A.queue) {
+            A.pending_cow.push_back(old);
+            A.pending_cow.push_back(fresh);
+          }
+          if (cow_out && ncow < cow_cap) {
+            cow_out[2 * ncow] = old;
+            cow_out[2 * ncow + 1] = fresh;
+          }
+          ++ncow;
+          ++A.cow_count;
         }
-        if (cow_out && ncow < cow_cap) {
-          cow_out[2 * ncow] = old;
-          cow_out[2 * ncow + 1] = fresh;
-        }
-        ++ncow;
-        ++A.cow_count;
+        if (slots_out) slots_out[(size_t)i * T + t] = (int64_t)A.table[s][lb] * kBlock + pos % kBlock;
+        A.len[s] = pos + 1;
       }
-      if (slots_out) slots_out[(size_t)i * T + t] = (int64_t)A.table[s][lb] * kBlock + pos % kBlock;
-      A.len[s] = pos + 1;
     }
-  }
-  if (n_cow_out) *n_cow_out = ncow;
-  return PKV_OK;
+    if (n_cow_out) *n_cow_out = ncow;
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_append(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, int32_t T, const void* k_new,
                       const void* v_new) {
-  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
-  if (!p->device) return fail(PKV_ERR_NO_DEVICE, "host-only pool");
-  if ((int64_t)n * T > 0 && (!k_new || !v_new)) return fail(PKV_ERR_INVALID_ARG, "k_new / v_new is NULL");
-  const size_t ntok = (size_t)n * (size_t)std::max(T, 0);
-  std::vector<int64_t> slots(ntok);
-  if (pkv_status r = pkv_reserve_slots(p, n, ids, T, slots.data(), nullptr, 0, nullptr)) return r;
-  cudaStream_t st = (cudaStream_t)stream;
-  // copies first: the new rows of a copied block land in the copy
-  if (pkv_status r = flush_pending(p, st, /*with_patches=*/false)) return r;
-  std::vector<TablePatch> patches = dedup_patches(p->alloc, p->alloc.pending_patch);
-  p->alloc.pending_patch.clear();
-  if (ntok == 0 && patches.empty()) return PKV_OK;
-  const auto& c = p->cfg;
-  const size_t row_bytes = (size_t)c.n_kv_heads * c.head_dim * (c.kv_dtype == PKV_KV_FP32 ? 4 : 2);
-  AppendArgs a;
-  a.kv_dtype = c.kv_dtype;
-  a.Hk = c.n_kv_heads;
-  a.D = c.head_dim;
-  a.k_pool = p->buf.k_pool;
-  a.v_pool = p->buf.v_pool;
-  a.k_scale = p->buf.k_scale;
-  a.v_scale = p->buf.v_scale;
-  a.tables = p->buf.block_tables;
-  if (ntok <= (size_t)kInlineAppend && patches.size() <= (size_t)kInlineAppend) {
-    // small (decode-step) append: slots and patches ride in the parameters
-    a.n_tokens = (int)ntok;
-    a.n_patches = (int)patches.size();
-    a.slots = nullptr;
-    a.patches = nullptr;
-    for (size_t i = 0; i < ntok; ++i) a.inline_slots[i] = slots[i];
-    for (size_t i = 0; i < patches.size(); ++i) {
-      a.inline_patches[2 * i] = patches[i].index;
-      a.inline_patches[2 * i + 1] = patches[i].value;
+  return guarded([&]() -> pkv_status {
+    if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    if (!p->device) return fail(PKV_ERR_NO_DEVICE, "host-only pool");
+    if ((int64_t)n * T > 0 && (!k_new || !v_new)) return fail(PKV_ERR_INVALID_ARG, "k_new / v_new is NULL");
+    const size_t ntok = (size_t)n * (size_t)std::max(T, 0);
+    std::vector<int64_t> slots(ntok);
+    if (pkv_status r = pkv_reserve_slots(p, n, ids, T, slots.data(), nullptr, 0, nullptr)) return r;
+    cudaStream_t st = (cudaStream_t)stream;
+    // copies first: the new rows of a copied block land in the copy
+    if (pkv_status r = flush_pending(p, st, /*with_patches=*/false)) return r;
+    std::vector<TablePatch> patches = dedup_patches(p->alloc, p->alloc.pending_patch);
+    p->alloc.pending_patch.clear();
+    if (ntok == 0 && patches.empty()) return PKV_OK;
+    const auto& c = p->cfg;
+    const size_t row_bytes = (size_t)c.n_kv_heads * c.head_dim * (c.kv_dtype == PKV_KV_FP32 ? 4 : 2);
+    AppendArgs a;
+    a.kv_dtype = c.kv_dtype;
+    a.Hk = c.n_kv_heads;
+    a.D = c.head_dim;
+    a.k_pool = p->buf.k_pool;
+    a.v_pool = p->buf.v_pool;
+    a.k_scale = p->buf.k_scale;
+    a.v_scale = p->buf.v_scale;
+    a.tables = p->buf.block_tables;
+    if (ntok <= (size_t)kInlineAppend && patches.size() <= (size_t)kInlineAppend) {
+      // small (decode-step) append: slots and patches ride in the parameters
+      a.n_tokens = (int)ntok;
+      a.n_patches = (int)patches.size();
+      a.slots = nullptr;
+      a.patches = nullptr;
+      for (size_t i = 0; i < ntok; ++i) a.inline_slots[i] = slots[i];
+      for (size_t i = 0; i < patches.size(); ++i) {
+        a.inline_patches[2 * i] = patches[i].index;
+        a.inline_patches[2 * i + 1] = patches[i].value;
+      }
+      a.k_new = k_new;
+      a.v_new = v_new;
+      return launch(p, PKV_KERNEL_APPEND, st, [&] { return launch_append(a, st); });
     }
-    a.k_new = k_new;
-    a.v_new = v_new;
-    return launch(p, PKV_KERNEL_APPEND, st, [&] { return launch_append(a, st); });
-  }
-  // large appends go through the staging ring in chunks of tokens; the first
-  // chunk carries the patches
-  const size_t chunk = size_t(1) << 20;
-  size_t t0 = 0;
-  do {
-    const size_t nt = std::min(chunk, ntok - t0);
-    const size_t np = t0 == 0 ? patches.size() : 0;
-    const size_t slot_off = (np * sizeof(TablePatch) + 255) & ~size_t(255);
-    StagingSlot* s;
-    if (pkv_status r = p->staging.acquire(slot_off + nt * sizeof(int64_t), &s)) return r;
-    if (np) memcpy(s->host, patches.data(), np * sizeof(TablePatch));
-    if (nt) memcpy(s->host + slot_off, slots.data() + t0, nt * sizeof(int64_t));
-    if (pkv_status r = Staging::upload(s, slot_off + nt * sizeof(int64_t), st)) return r;
-    a.n_tokens = (int)nt;
-    a.n_patches = (int)np;
-    a.patches = (const int32_t*)s->dev;
-    a.slots = (const int64_t*)(s->dev + slot_off);
-    a.k_new = (const char*)k_new + t0 * row_bytes;
-    a.v_new = (const char*)v_new + t0 * row_bytes;
-    if (pkv_status r = launch(p, PKV_KERNEL_APPEND, st, [&] { return launch_append(a, st); })) return r;
-    if (pkv_status r = Staging::release(s, st)) return r;
-    t0 += nt;
-  } while (t0 < ntok);
-  return PKV_OK;
+    // large appends go through the staging ring in chunks of tokens; the first
+    // chunk carries the patches
+    const size_t chunk = size_t(1) << 20;
+    size_t t0 = 0;
+    do {
+      const size_t nt = std::min(chunk, ntok - t0);
+      const size_t np = t0 == 0 ? patches.size() : 0;
+      const size_t slot_off = (np * sizeof(TablePatch) + 255) & ~size_t(255);
+      StagingSlot* s;
+      if (pkv_status r = p->staging.acquire(slot_off + nt * sizeof(int64_t), &s)) return r;
+      if (np) memcpy(s->host, patches.data(), np * sizeof(TablePatch));
+      if (nt) memcpy(s->host + slot_off, slots.data() + t0, nt * sizeof(int64_t));
+      if (pkv_status r = Staging::upload(s, slot_off + nt * sizeof(int64_t), st)) return r;
+      a.n_tokens = (int)nt;
+      a.n_patches = (int)np;
+      a.patches = (const int32_t*)s->dev;
+      a.slots = (const int64_t*)(s->dev + slot_off);
+      a.k_new = (const char*)k_new + t0 * row_bytes;
+      a.v_new = (const char*)v_new + t0 * row_bytes;
+      if (pkv_status r = launch(p, PKV_KERNEL_APPEND, st, [&] { return launch_append(a, st); })) return r;
+      if (pkv_status r = Staging::release(s, st)) return r;
+      t0 += nt;
+    } while (t0 < ntok);
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_seq_compact(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, const int32_t* keep_idx,
                            int64_t keep_stride, const int32_t* counts, float* acc, int64_t acc_stride) {
-  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
-  if (pkv_status r = check_seq_list(p, n, ids)) return r;
-  if (n > 0 && !counts) return fail(PKV_ERR_INVALID_ARG, "counts is NULL");
-  auto& A = p->alloc;
-  int64_t need = 0;
-  int32_t max_count = 0, max_len = 0;
-  if (const int32_t d = A.first_repeat(n, ids); d >= 0)
-    return fail(PKV_ERR_INVALID_ARG, "sequence %d listed twice", d);
-  for (int32_t i = 0; i < n; ++i) {
-    if (counts[i] < 0 || counts[i] > A.len[ids[i]])
-      return fail(PKV_ERR_INVALID_ARG, "count %d outside [0, %d]", counts[i], A.len[ids[i]]);
-    need += ceil_div(counts[i], kBlock);
-    max_count = std::max(max_count, counts[i]);
-    max_len = std::max(max_len, A.len[ids[i]]);
-  }
-  if (p->device) {
-    if (max_count > 0 && (!keep_idx || keep_stride < max_count))
-      return fail(PKV_ERR_INVALID_ARG, "keep_idx is NULL or keep_stride < largest count");
-    if (acc && acc_stride < max_len) return fail(PKV_ERR_INVALID_ARG, "acc_stride < length");
-  }
-  if (need > (int64_t)A.free_blocks.size())
-    return fail(PKV_ERR_OUT_OF_BLOCKS, "compaction needs %lld fresh blocks, %zu free", (long long)need,
-                A.free_blocks.size());
-  cudaStream_t st = (cudaStream_t)stream;
-  if (p->device)
-    if (pkv_status r = flush_pending(p, st)) return r;  // the gather reads the current device table
-  // fresh blocks for every sequence first, then release the old ones
-  std::vector<CompactSeq> seqs(n);
-  std::vector<int32_t> fresh;
-  fresh.reserve(need);
-  for (int32_t i = 0; i < n; ++i) {
-    seqs[i] = {ids[i], i, counts[i], (int32_t)fresh.size(), A.len[ids[i]], 0, 0, 0};
-    for (int32_t k = 0; k < ceil_div(counts[i], kBlock); ++k) fresh.push_back(A.take());
-  }
-  // a failure before the gather is queued gives the fresh blocks back
-  auto undo = [&](pkv_status r) {
-    for (size_t k = fresh.size(); k-- > 0;) A.untake(fresh[k]);
-    return r;
-  };
-  StagingSlot* s = nullptr;
-  if (p->device && n > 0) {
-    const size_t seq_bytes = n * sizeof(CompactSeq), off = (seq_bytes + 255) & ~size_t(255);
-    if (pkv_status r = p->staging.acquire(off + fresh.size() * sizeof(int32_t) + 4, &s)) return undo(r);
-    memcpy(s->host, seqs.data(), seq_bytes);
-    if (!fresh.empty()) memcpy(s->host + off, fresh.data(), fresh.size() * sizeof(int32_t));
-    if (pkv_status r = Staging::upload(s, off + fresh.size() * sizeof(int32_t), st)) return undo(r);
-    const auto& c = p->cfg;
-    const int row_bytes = c.head_dim * elem_bytes(c.kv_dtype);
-    const bool fp8 = has_scales(c.kv_dtype);
-    if (pkv_status r = launch(p, PKV_KERNEL_COMPACT, st, [&] {
-          return launch_compact_gather((const CompactSeq*)s->dev, n, max_count, (const int32_t*)(s->dev + off),
-                                       p->buf.block_tables, c.max_blocks_per_seq, c.num_blocks, keep_idx, keep_stride,
-                                       c.n_kv_heads, row_bytes, p->buf.k_pool, p->buf.v_pool,
-                                       fp8 ? p->buf.k_scale : nullptr, fp8 ? p->buf.v_scale : nullptr, p->buf.status,
-                                       st);
-        }))
-      return undo(r);
-  }
-  size_t pos = 0;
-  for (int32_t i = 0; i < n; ++i) A.drop_from(ids[i], 0);  // old blocks, ascending, sequence by sequence
-  for (int32_t i = 0; i < n; ++i) {
-    for (int32_t k = 0; k < ceil_div(counts[i], kBlock); ++k) A.set_entry(ids[i], k, fresh[pos++]);
-    A.len[ids[i]] = counts[i];
-    A.holes[ids[i]] = 0;
-  }
-  if (!p->device) return PKV_OK;
-  if (pkv_status r = flush_pending(p, st)) return r;  // new tables, after the gather
-  if (acc && n > 0)
-    if (pkv_status r = launch(p, PKV_KERNEL_COMPACT, st, [&] {
-          return launch_compact_scores((const CompactSeq*)s->dev, n, keep_idx, keep_stride, acc, acc_stride, st);
-        }))
+  return guarded([&]() -> pkv_status {
+    if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    if (pkv_status r = check_seq_list(p, n, ids)) return r;
+    if (n > 0 && !counts) return fail(PKV_ERR_INVALID_ARG, "counts is NULL");
+    auto& A = p->alloc;
+    int64_t need = 0;
+    int32_t max_count = 0, max_len = 0;
+    if (const int32_t d = A.first_repeat(n, ids); d >= 0)
+      return fail(PKV_ERR_INVALID_ARG, "sequence %d listed twice", d);
+    for (int32_t i = 0; i < n; ++i) {
+      if (counts[i] < 0 || counts[i] > A.len[ids[i]])
+        return fail(PKV_ERR_INVALID_ARG, "count %d outside [0, %d]", counts[i], A.len[ids[i]]);
+      need += ceil_div(counts[i], kBlock);
+      max_count = std::max(max_count, counts[i]);
+      max_len = std::max(max_len, A.len[ids[i]]);
+    }
+    if (p->device) {
+      if (max_count > 0 && (!keep_idx || keep_stride < max_count))
+        return fail(PKV_ERR_INVALID_ARG, "keep_idx is NULL or keep_stride < largest count");
+      if (acc && acc_stride < max_len) return fail(PKV_ERR_INVALID_ARG, "acc_stride < length");
+    }
+    if (need > (int64_t)A.free_blocks.size())
+      return fail(PKV_ERR_OUT_OF_BLOCKS, "compaction needs %lld fresh blocks, %zu free", (long long)need,
+                  A.free_blocks.size());
+    cudaStream_t st = (cudaStream_t)stream;
+    if (p->device)
+      if (pkv_status r = flush_pending(p, st)) return r;  // the gather reads the current device table
+    // fresh blocks for every sequence first, then release the old ones
+    std::vector<CompactSeq> seqs(n);
+    std::vector<int32_t> fresh;
+    fresh.reserve(need);
+    for (int32_t i = 0; i < n; ++i) {
+      seqs[i] = {ids[i], i, counts[i], (int32_t)fresh.size(), A.len[ids[i]], 0, 0, 0};
+      for (int32_t k = 0; k < ceil_div(counts[i], kBlock); ++k) fresh.push_back(A.take());
+    }
+    // a failure before the gather is queued gives the fresh blocks back
+    auto undo = [&](pkv_status r) {
+      for (size_t k = fresh.size(); k-- > 0;) A.untake(fresh[k]);
       return r;
-  return s ? Staging::release(s, st) : PKV_OK;
+    };
+    StagingSlot* s = nullptr;
+    if (p->device && n > 0) {
+      const size_t seq_bytes = n * sizeof(CompactSeq), off = (seq_bytes + 255) & ~size_t(255);
+      if (pkv_status r = p->staging.acquire(off + fresh.size() * sizeof(int32_t) + 4, &s)) return undo(r);
+      memcpy(s->host, seqs.data(), seq_bytes);
+      if (!fresh.empty()) memcpy(s->host + off, fresh.data(), fresh.size() * sizeof(int32_t));
+      if (pkv_status r = Staging::upload(s, off + fresh.size() * sizeof(int32_t), st)) return undo(r);
+      const auto& c = p->cfg;
+      const int row_bytes = c.head_dim * elem_bytes(c.kv_dtype);
+      const bool fp8 = has_scales(c.kv_dtype);
+      if (pkv_status r = launch(p, PKV_KERNEL_COMPACT, st, [&] {
+            return launch_compact_gather((const CompactSeq*)s->dev, n, max_count, (const int32_t*)(s->dev + off),
+                                         p->buf.block_tables, c.max_blocks_per_seq, c.num_blocks, keep_idx, keep_stride,
+                                         c.n_kv_heads, row_bytes, p->buf.k_pool, p->buf.v_pool,
+                                         fp8 ? p->buf.k_scale : nullptr, fp8 ? p->buf.v_scale : nullptr, p->buf.status,
+                                         st);
+          }))
+        return undo(r);
+    }
+    size_t pos = 0;
+    for (int32_t i = 0; i < n; ++i) A.drop_from(ids[i], 0);  // old blocks, ascending, sequence by sequence
+    for (int32_t i = 0; i < n; ++i) {
+      for (int32_t k = 0; k < ceil_div(counts[i], kBlock); ++k) A.set_entry(ids[i], k, fresh[pos++]);
+      A.len[ids[i]] = counts[i];
+      A.holes[ids[i]] = 0;
+    }
+    if (!p->device) return PKV_OK;
+    if (pkv_status r = flush_pending(p, st)) return r;  // new tables, after the gather
+    if (acc && n > 0)
+      if (pkv_status r = launch(p, PKV_KERNEL_COMPACT, st, [&] {
+            return launch_compact_scores((const CompactSeq*)s->dev, n, keep_idx, keep_stride, acc, acc_stride, st);
+          }))
+        return r;
+    return s ? Staging::release(s, st) : PKV_OK;
+  });
 }
 
 pkv_status pkv_swap_space_create(pkv_pool* p, int64_t nh, void* hk, void* hv, float* hks, float* hvs) {
-  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
-  auto& A = p->alloc;
-  if (nh < 0 || nh > INT32_MAX) return fail(PKV_ERR_INVALID_ARG, "num_host_blocks %lld out of range", (long long)nh);
-  for (int32_t s = 0; s < A.max_seqs; ++s)
-    if (A.swapped[s]) return fail(PKV_ERR_INVALID_ARG, "sequence %d is swapped out", s);
-  const bool scaled = has_scales(p->cfg.kv_dtype);
-  void *kd = nullptr, *vd = nullptr, *ksd = nullptr, *vsd = nullptr;
-  if (p->device) {
-    if (nh > 0 && (!hk || !hv || (scaled && (!hks || !hvs))))
-      return fail(PKV_ERR_INVALID_ARG, "a host buffer of the swap space is NULL");
-    if (pkv_status r = map_host(hk, &kd, "host_k")) return r;
-    if (pkv_status r = map_host(hv, &vd, "host_v")) return r;
-    if (scaled) {
-      if (pkv_status r = map_host(hks, &ksd, "host_k_scale")) return r;
-      if (pkv_status r = map_host(hvs, &vsd, "host_v_scale")) return r;
+  return guarded([&]() -> pkv_status {
+    if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    auto& A = p->alloc;
+    if (nh < 0 || nh > INT32_MAX) return fail(PKV_ERR_INVALID_ARG, "num_host_blocks %lld out of range", (long long)nh);
+    for (int32_t s = 0; s < A.max_seqs; ++s)
+      if (A.swapped[s]) return fail(PKV_ERR_INVALID_ARG, "sequence %d is swapped out", s);
+    const bool scaled = has_scales(p->cfg.kv_dtype);
+    void *kd = nullptr, *vd = nullptr, *ksd = nullptr, *vsd = nullptr;
+    if (p->device) {
+      if (nh > 0 && (!hk || !hv || (scaled && (!hks || !hvs))))
+        return fail(PKV_ERR_INVALID_ARG, "a host buffer of the swap space is NULL");
+      if (pkv_status r = map_host(hk, &kd, "host_k")) return r;
+      if (pkv_status r = map_host(hv, &vd, "host_v")) return r;
+      if (scaled) {
+        if (pkv_status r = map_host(hks, &ksd, "host_k_scale")) return r;
+        if (pkv_status r = map_host(hvs, &vsd, "host_v_scale")) return r;
+      }
+    } else if (hk || hv || hks || hvs) {
+      return fail(PKV_ERR_INVALID_ARG, "a host-only pool takes no swap buffers");
     }
-  } else if (hk || hv || hks || hvs) {
-    return fail(PKV_ERR_INVALID_ARG, "a host-only pool takes no swap buffers");
-  }
-  p->host_k = hk;
-  p->host_v = hv;
-  p->host_ks = scaled ? hks : nullptr;
-  p->host_vs = scaled ? hvs : nullptr;
-  p->host_k_dev = kd;
-  p->host_v_dev = vd;
-  p->host_ks_dev = (float*)ksd;
-  p->host_vs_dev = (float*)vsd;
-  A.set_swap_space((int32_t)nh);
-  p->swap_space = true;
-  return PKV_OK;
+    p->host_k = hk;
+    p->host_v = hv;
+    p->host_ks = scaled ? hks : nullptr;
+    p->host_vs = scaled ? hvs : nullptr;
+    p->host_k_dev = kd;
+    p->host_v_dev = vd;
+    p->host_ks_dev = (float*)ksd;
+    p->host_vs_dev = (float*)vsd;
+    A.set_swap_space((int32_t)nh);
+    p->swap_space = true;
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_swap_out(pkv_pool* p, void* stream, int32_t n, const int32_t* ids) {
-  return swap_move(p, stream, n, ids, true);
+  return guarded([&]() -> pkv_status {
+    return swap_move(p, stream, n, ids, true);
+  });
 }
 
 pkv_status pkv_swap_in(pkv_pool* p, void* stream, int32_t n, const int32_t* ids) {
-  return swap_move(p, stream, n, ids, false);
+  return guarded([&]() -> pkv_status {
+    return swap_move(p, stream, n, ids, false);
+  });
 }
 
 pkv_status pkv_seq_swapped(const pkv_pool* p, int32_t s, int32_t* swapped_out) {
-  if (!p || !swapped_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
-  if (!p->alloc.valid_seq(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", s);
-  *swapped_out = p->alloc.swapped[s];
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    if (!p || !swapped_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+    if (!p->alloc.valid_seq(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", s);
+    *swapped_out = p->alloc.swapped[s];
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_get_host_block_table(const pkv_pool* p, int32_t s, int32_t* host_out, int32_t cap, int32_t* n_out) {
-  if (!p || !n_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
-  const auto& A = p->alloc;
-  if (!A.valid_seq(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", s);
-  const int32_t n = A.swapped[s] ? ceil_div(A.len[s], kBlock) : 0;
-  *n_out = n;
-  if (n > cap || (n > 0 && !host_out)) return fail(PKV_ERR_INVALID_ARG, "capacity %d < %d entries", cap, n);
-  for (int32_t i = 0; i < n; ++i) host_out[i] = A.host_table[s][i];
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    if (!p || !n_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+    const auto& A = p->alloc;
+    if (!A.valid_seq(s)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live", s);
+    const int32_t n = A.swapped[s] ? ceil_div(A.len[s], kBlock) : 0;
+    *n_out = n;
+    if (n > cap || (n > 0 && !host_out)) return fail(PKV_ERR_INVALID_ARG, "capacity %d < %d entries", cap, n);
+    for (int32_t i = 0; i < n; ++i) host_out[i] = A.host_table[s][i];
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_host_free_blocks(const pkv_pool* p, int64_t* n_out) {
-  if (!p || !n_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
-  *n_out = (int64_t)p->alloc.host_free.size();
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    if (!p || !n_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+    *n_out = (int64_t)p->alloc.host_free.size();
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_decode_workspace_size(const pkv_pool* p, int32_t n, int32_t num_splits, size_t* bytes_out) {
-  if (!p || !bytes_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
-  if (n < 0 || num_splits < 0) return fail(PKV_ERR_INVALID_ARG, "negative size");
-  if (p->cfg.kv_dtype == PKV_KV_FP32) {
-    *bytes_out = 0;
+  return guarded([&]() -> pkv_status {
+    if (!p || !bytes_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+    if (n < 0 || num_splits < 0) return fail(PKV_ERR_INVALID_ARG, "negative size");
+    if (p->cfg.kv_dtype == PKV_KV_FP32) {
+      *bytes_out = 0;
+      return PKV_OK;
+    }
+    *bytes_out = max_pieces(p, n, num_splits) * partial_floats(p->G, p->cfg.head_dim) * sizeof(float);
     return PKV_OK;
-  }
-  *bytes_out = max_pieces(p, n, num_splits) * partial_floats(p->G, p->cfg.head_dim) * sizeof(float);
-  return PKV_OK;
+  });
 }
 
 pkv_status pkv_decode_attn(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, const void* q, float scale,
                            int32_t mode, int32_t S, int32_t W, int32_t num_splits, void* out, float* lse,
                            float* logits, int64_t logits_stride, void* workspace, size_t workspace_bytes) {
-  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
-  if (!p->device) return fail(PKV_ERR_NO_DEVICE, "host-only pool");
-  if (pkv_status r = check_seq_list(p, n, ids)) return r;
-  if (!valid_mask(mode, S, W)) return fail(PKV_ERR_INVALID_ARG, "invalid mask %d (%d, %d)", mode, S, W);
-  if (num_splits < 0) return fail(PKV_ERR_INVALID_ARG, "num_splits < 0");
-  if (n > 0 && (!q || !out)) return fail(PKV_ERR_INVALID_ARG, "q / out is NULL");
-  const auto& A = p->alloc;
-  int32_t maxlen = 0;
-  for (int32_t i = 0; i < n; ++i) maxlen = std::max(maxlen, A.len[ids[i]]);
-  if (logits && logits_stride < maxlen) return fail(PKV_ERR_INVALID_ARG, "logits_stride < max length");
-  if (pkv_status r = check_keep_blocks_present(p, n, ids, mode, S, W)) return r;
-  cudaStream_t st = (cudaStream_t)stream;
-  if (pkv_status r = flush_pending(p, st)) return r;
-  if (n == 0) return PKV_OK;
-  const auto& c = p->cfg;
+  return guarded([&]() -> pkv_status {
+    if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    if (!p->device) return fail(PKV_ERR_NO_DEVICE, "host-only pool");
+    if (pkv_status r = check_seq_list(p, n, ids)) return r;
+    if (!valid_mask(mode, S, W)) return fail(PKV_ERR_INVALID_ARG, "invalid mask %d (%d, %d)", mode, S, W);
+    if (num_splits < 0) return fail(PKV_ERR_INVALID_ARG, "num_splits < 0");
+    if (n > 0 && (!q || !out)) return fail(PKV_ERR_INVALID_ARG, "q / out is NULL");
+    const auto& A = p->alloc;
+    int32_t maxlen = 0;
+    for (int32_t i = 0; i < n; ++i) maxlen = std::max(maxlen, A.len[ids[i]]);
+    if (logits && logits_stride < maxlen) return fail(PKV_ERR_INVALID_ARG, "logits_stride < max length");
+    if (pkv_status r = check_keep_blocks_present(p, n, ids, mode, S, W)) return r;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (pkv_status r = flush_pending(p, st)) return r;
+    if (n == 0) return PKV_OK;
+    const auto& c = p->cfg;
 
-  if (c.kv_dtype == PKV_KV_FP32) {
+    if (c.kv_dtype == PKV_KV_FP32) {
+      StagingSlot* s;
+      if (pkv_status r = p->staging.acquire(n * sizeof(SeqRow), &s)) return r;
+      SeqRow* rows = (SeqRow*)s->host;
+      for (int32_t i = 0; i < n; ++i) rows[i] = {ids[i], i, A.len[ids[i]], 0};
+      if (pkv_status r = Staging::upload(s, n * sizeof(SeqRow), st)) return r;
+      DecodeF32Params prm;
+      prm.k_pool = (const float*)p->buf.k_pool;
+      prm.v_pool = (const float*)p->buf.v_pool;
+      prm.tables = p->buf.block_tables;
+      prm.max_blocks = c.max_blocks_per_seq;
+      prm.num_blocks = c.num_blocks;
+      prm.n_heads = c.n_heads;
+      prm.n_kv_heads = c.n_kv_heads;
+      prm.head_dim = c.head_dim;
+      prm.rows = (const SeqRow*)s->dev;
+      prm.n_seqs = n;
+      prm.q = (const float*)q;
+      prm.out = (float*)out;
+      prm.lse = lse;
+      prm.logits = logits;
+      prm.logits_stride = logits_stride;
+      prm.scale = scale;
+      prm.mask_mode = mode;
+      prm.num_sinks = S;
+      prm.window = W;
+      prm.status = p->buf.status;
+      if (pkv_status r = launch(p, PKV_KERNEL_DECODE, st, [&] { return launch_decode_f32(prm, st); })) return r;
+      return Staging::release(s, st);
+    }
+
+    size_t need = 0;
+    pkv_decode_workspace_size(p, n, num_splits, &need);
+    Plan& plan = build_plan(p, n, ids, mode, S, W, num_splits);
+    const size_t pf = (size_t)partial_floats(p->G, c.head_dim) * sizeof(float);
+    if (plan.n_partials > 0 && (!workspace || workspace_bytes < plan.n_partials * pf))
+      return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
+    if (plan.n_partials > 0 && ((uintptr_t)workspace & 15))
+      return fail(PKV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    const PlanLayout L = plan_layout(plan, warps_per_cta(p, plan.nq), 0);
     StagingSlot* s;
-    if (pkv_status r = p->staging.acquire(n * sizeof(SeqRow), &s)) return r;
-    SeqRow* rows = (SeqRow*)s->host;
-    for (int32_t i = 0; i < n; ++i) rows[i] = {ids[i], i, A.len[ids[i]], 0};
-    if (pkv_status r = Staging::upload(s, n * sizeof(SeqRow), st)) return r;
-    DecodeF32Params prm;
-    prm.k_pool = (const float*)p->buf.k_pool;
-    prm.v_pool = (const float*)p->buf.v_pool;
-    prm.tables = p->buf.block_tables;
-    prm.max_blocks = c.max_blocks_per_seq;
-    prm.num_blocks = c.num_blocks;
-    prm.n_heads = c.n_heads;
-    prm.n_kv_heads = c.n_kv_heads;
-    prm.head_dim = c.head_dim;
-    prm.rows = (const SeqRow*)s->dev;
-    prm.n_seqs = n;
-    prm.q = (const float*)q;
-    prm.out = (float*)out;
-    prm.lse = lse;
-    prm.logits = logits;
-    prm.logits_stride = logits_stride;
-    prm.scale = scale;
-    prm.mask_mode = mode;
-    prm.num_sinks = S;
-    prm.window = W;
-    prm.status = p->buf.status;
-    if (pkv_status r = launch(p, PKV_KERNEL_DECODE, st, [&] { return launch_decode_f32(prm, st); })) return r;
+    if (pkv_status r = p->staging.acquire(L.bytes, &s)) return r;
+    plan_write(plan, L, s->host);
+    if (pkv_status r = p->staging.upload_overlapped(s, L.bytes, st)) return r;
+    if (pkv_status r = launch_tc_plan(p, st, plan, L, s->dev, q, scale, mode, S, W, out, lse, logits, logits_stride,
+                                      workspace))
+      return r;
     return Staging::release(s, st);
-  }
-
-  size_t need = 0;
-  pkv_decode_workspace_size(p, n, num_splits, &need);
-  Plan& plan = build_plan(p, n, ids, mode, S, W, num_splits);
-  const size_t pf = (size_t)partial_floats(p->G, c.head_dim) * sizeof(float);
-  if (plan.n_partials > 0 && (!workspace || workspace_bytes < plan.n_partials * pf))
-    return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
-  if (plan.n_partials > 0 && ((uintptr_t)workspace & 15))
-    return fail(PKV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
-  const PlanLayout L = plan_layout(plan, warps_per_cta(p, plan.nq), 0);
-  StagingSlot* s;
-  if (pkv_status r = p->staging.acquire(L.bytes, &s)) return r;
-  plan_write(plan, L, s->host);
-  if (pkv_status r = p->staging.upload_overlapped(s, L.bytes, st)) return r;
-  if (pkv_status r = launch_tc_plan(p, st, plan, L, s->dev, q, scale, mode, S, W, out, lse, logits, logits_stride,
-                                    workspace))
-    return r;
-  return Staging::release(s, st);
+  });
 }
 
 pkv_status pkv_h2o_scores(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, const float* logits,
                           int64_t logits_stride, const float* lse, int32_t mode, int32_t S, int32_t W, float* acc,
                           int64_t acc_stride) {
-  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
-  if (!p->device) return fail(PKV_ERR_NO_DEVICE, "host-only pool");
-  if (pkv_status r = check_seq_list(p, n, ids)) return r;
-  if (!valid_mask(mode, S, W)) return fail(PKV_ERR_INVALID_ARG, "invalid mask");
-  if (n > 0 && (!logits || !lse || !acc)) return fail(PKV_ERR_INVALID_ARG, "NULL device array");
-  if (n > 65535) return fail(PKV_ERR_UNSUPPORTED, "%d sequences in one score update (at most 65535)", n);
-  const auto& A = p->alloc;
-  int32_t maxlen = 0, max_keep = 0;
-  for (int32_t i = 0; i < n; ++i) {
-    const int32_t L = A.len[ids[i]];
-    maxlen = std::max(maxlen, L);
-    int32_t k = L;
-    if (mode == PKV_MASK_SLIDING) k = std::min(L, W + 1);
-    if (mode == PKV_MASK_SINK_WINDOW && (int64_t)L > (int64_t)S + W) k = S + W;
-    max_keep = std::max(max_keep, k);
-  }
-  if (logits_stride < maxlen || acc_stride < maxlen) return fail(PKV_ERR_INVALID_ARG, "stride < max length");
-  cudaStream_t st = (cudaStream_t)stream;
-  if (pkv_status r = flush_pending(p, st)) return r;
-  if (n == 0 || max_keep == 0) return PKV_OK;
-  StagingSlot* s;
-  if (pkv_status r = p->staging.acquire(n * sizeof(SeqRow), &s)) return r;
-  SeqRow* rows = (SeqRow*)s->host;
-  for (int32_t i = 0; i < n; ++i) rows[i] = {ids[i], i, A.len[ids[i]], 0};
-  if (pkv_status r = p->staging.upload_overlapped(s, n * sizeof(SeqRow), st)) return r;
-  const auto& c = p->cfg;
-  if (pkv_status r = launch(p, PKV_KERNEL_H2O_SCORE, st, [&] {
-        return launch_h2o_score((const SeqRow*)s->dev, n, c.n_heads, c.n_kv_heads, logits, logits_stride, lse, mode,
-                                S, W, acc, acc_stride, max_keep, st);
-      }))
-    return r;
-  return Staging::release(s, st);
+  return guarded([&]() -> pkv_status {
+    if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    if (!p->device) return fail(PKV_ERR_NO_DEVICE, "host-only pool");
+    if (pkv_status r = check_seq_list(p, n, ids)) return r;
+    if (!valid_mask(mode, S, W)) return fail(PKV_ERR_INVALID_ARG, "invalid mask");
+    if (n > 0 && (!logits || !lse || !acc)) return fail(PKV_ERR_INVALID_ARG, "NULL device array");
+    if (n > 65535) return fail(PKV_ERR_UNSUPPORTED, "%d sequences in one score update (at most 65535)", n);
+    const auto& A = p->alloc;
+    int32_t maxlen = 0, max_keep = 0;
+    for (int32_t i = 0; i < n; ++i) {
+      const int32_t L = A.len[ids[i]];
+      maxlen = std::max(maxlen, L);
+      int32_t k = L;
+      if (mode == PKV_MASK_SLIDING) k = std::min(L, W + 1);
+      if (mode == PKV_MASK_SINK_WINDOW && (int64_t)L > (int64_t)S + W) k = S + W;
+      max_keep = std::max(max_keep, k);
+    }
+    if (logits_stride < maxlen || acc_stride < maxlen) return fail(PKV_ERR_INVALID_ARG, "stride < max length");
+    cudaStream_t st = (cudaStream_t)stream;
+    if (pkv_status r = flush_pending(p, st)) return r;
+    if (n == 0 || max_keep == 0) return PKV_OK;
+    StagingSlot* s;
+    if (pkv_status r = p->staging.acquire(n * sizeof(SeqRow), &s)) return r;
+    SeqRow* rows = (SeqRow*)s->host;
+    for (int32_t i = 0; i < n; ++i) rows[i] = {ids[i], i, A.len[ids[i]], 0};
+    if (pkv_status r = p->staging.upload_overlapped(s, n * sizeof(SeqRow), st)) return r;
+    const auto& c = p->cfg;
+    if (pkv_status r = launch(p, PKV_KERNEL_H2O_SCORE, st, [&] {
+          return launch_h2o_score((const SeqRow*)s->dev, n, c.n_heads, c.n_kv_heads, logits, logits_stride, lse, mode,
+                                  S, W, acc, acc_stride, max_keep, st);
+        }))
+      return r;
+    return Staging::release(s, st);
+  });
 }
 
 namespace {
@@ -2416,133 +2486,157 @@ pkv_status select_keep(pkv_pool* p, void* stream, int32_t n, const int32_t* lens
 pkv_status pkv_h2o_select(pkv_pool* p, void* stream, int32_t n, const int32_t* lens, const float* acc,
                           int64_t acc_stride, int32_t budget, int32_t recent, int32_t* keep_idx, int64_t keep_stride,
                           int32_t* keep_count) {
-  if (recent < 0 || budget < recent || budget < 1) return fail(PKV_ERR_INVALID_ARG, "need 0 <= recent <= budget, budget >= 1");
-  if (keep_stride < budget) return fail(PKV_ERR_INVALID_ARG, "keep_stride < budget");
-  return select_keep(p, stream, n, lens, acc, acc_stride, SelPolicy{0, recent, budget - recent, 0}, budget, keep_idx,
-                     keep_stride, keep_count);
+  return guarded([&]() -> pkv_status {
+    if (recent < 0 || budget < recent || budget < 1) return fail(PKV_ERR_INVALID_ARG, "need 0 <= recent <= budget, budget >= 1");
+    if (keep_stride < budget) return fail(PKV_ERR_INVALID_ARG, "keep_stride < budget");
+    return select_keep(p, stream, n, lens, acc, acc_stride, SelPolicy{0, recent, budget - recent, 0}, budget, keep_idx,
+                       keep_stride, keep_count);
+  });
 }
 
 pkv_status pkv_policy_select(pkv_pool* p, void* stream, int32_t n, const int32_t* lens, const float* acc,
                              int64_t acc_stride, int32_t sink_size, int32_t window_size, int32_t h2o_size,
                              int32_t* keep_idx, int64_t keep_stride, int32_t* keep_count) {
-  if (sink_size < 0 || window_size < 0 || h2o_size < 0)
-    return fail(PKV_ERR_INVALID_ARG, "sink_size, window_size and h2o_size must be >= 0");
-  return select_keep(p, stream, n, lens, acc, acc_stride, SelPolicy{sink_size, window_size, h2o_size, 1},
-                     (int64_t)sink_size + window_size + h2o_size, keep_idx, keep_stride, keep_count);
+  return guarded([&]() -> pkv_status {
+    if (sink_size < 0 || window_size < 0 || h2o_size < 0)
+      return fail(PKV_ERR_INVALID_ARG, "sink_size, window_size and h2o_size must be >= 0");
+    return select_keep(p, stream, n, lens, acc, acc_stride, SelPolicy{sink_size, window_size, h2o_size, 1},
+                       (int64_t)sink_size + window_size + h2o_size, keep_idx, keep_stride, keep_count);
+  });
 }
 
 pkv_status pkv_sync_status(pkv_pool* p, void* stream) {
-  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
-  if (!p->device) return fail(PKV_ERR_NO_DEVICE, "host-only pool");
-  cudaStream_t st = (cudaStream_t)stream;
-  PKV_CUDA(cudaStreamSynchronize(st));
-  int32_t w[4] = {0, 0, 0, 0};
-  PKV_CUDA(cudaMemcpy(w, p->buf.status, sizeof w, cudaMemcpyDeviceToHost));
-  if (w[0]) {
-    PKV_CUDA(cudaMemset(p->buf.status, 0, sizeof w));
-    PKV_CUDA(cudaDeviceSynchronize());
-    if (w[0] & kStatusTimeout) return fail(PKV_ERR_TIMEOUT, "a device wait timed out (info %d)", w[1]);
-    return fail(PKV_ERR_DEVICE_ASSERT, "device range check failed (info %d, %d)", w[1], w[2]);
-  }
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    if (!p->device) return fail(PKV_ERR_NO_DEVICE, "host-only pool");
+    cudaStream_t st = (cudaStream_t)stream;
+    PKV_CUDA(cudaStreamSynchronize(st));
+    int32_t w[4] = {0, 0, 0, 0};
+    PKV_CUDA(cudaMemcpy(w, p->buf.status, sizeof w, cudaMemcpyDeviceToHost));
+    if (w[0]) {
+      PKV_CUDA(cudaMemset(p->buf.status, 0, sizeof w));
+      PKV_CUDA(cudaDeviceSynchronize());
+      if (w[0] & kStatusTimeout) return fail(PKV_ERR_TIMEOUT, "a device wait timed out (info %d)", w[1]);
+      return fail(PKV_ERR_DEVICE_ASSERT, "device range check failed (info %d, %d)", w[1], w[2]);
+    }
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_timing_enable(pkv_pool* p, int32_t kernel_mask) {
-  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
-  p->timing.mask = p->device ? kernel_mask : 0;
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    p->timing.mask = p->device ? kernel_mask : 0;
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_timing_read(pkv_pool* p, double* total_ms, int64_t* launches) {
-  if (!p || !total_ms || !launches) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
-  for (int k = 0; k < PKV_KERNEL_COUNT; ++k) {
-    double sum = 0;
-    for (auto& pr : p->timing.marks[k]) {
-      PKV_CUDA(cudaEventSynchronize(pr.second));
-      float ms = 0;
-      PKV_CUDA(cudaEventElapsedTime(&ms, pr.first, pr.second));
-      sum += ms;
-      p->timing.spare.push_back(pr.first);
-      p->timing.spare.push_back(pr.second);
+  return guarded([&]() -> pkv_status {
+    if (!p || !total_ms || !launches) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+    for (int k = 0; k < PKV_KERNEL_COUNT; ++k) {
+      double sum = 0;
+      for (auto& pr : p->timing.marks[k]) {
+        PKV_CUDA(cudaEventSynchronize(pr.second));
+        float ms = 0;
+        PKV_CUDA(cudaEventElapsedTime(&ms, pr.first, pr.second));
+        sum += ms;
+        p->timing.spare.push_back(pr.first);
+        p->timing.spare.push_back(pr.second);
+      }
+      total_ms[k] = sum;
+      launches[k] = (int64_t)p->timing.marks[k].size();
+      p->timing.marks[k].clear();
     }
-    total_ms[k] = sum;
-    launches[k] = (int64_t)p->timing.marks[k].size();
-    p->timing.marks[k].clear();
-  }
-  return PKV_OK;
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_set_wait_limit(pkv_pool* p, int64_t wait_limit_ns) {
-  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
-  if (wait_limit_ns < 1000000 || wait_limit_ns > 60000000000LL)
-    return fail(PKV_ERR_INVALID_ARG, "wait limit must lie in [1 ms, 60 s]");
-  p->wait_limit_ns = (uint64_t)wait_limit_ns;
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    if (wait_limit_ns < 1000000 || wait_limit_ns > 60000000000LL)
+      return fail(PKV_ERR_INVALID_ARG, "wait limit must lie in [1 ms, 60 s]");
+    p->wait_limit_ns = (uint64_t)wait_limit_ns;
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_set_cascade(pkv_pool* p, int32_t mode) {
-  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
-  if (mode < 0 || mode > 2) return fail(PKV_ERR_INVALID_ARG, "cascade mode %d not in {0, 1, 2}", mode);
-  p->cascade = mode;
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    if (mode < 0 || mode > 2) return fail(PKV_ERR_INVALID_ARG, "cascade mode %d not in {0, 1, 2}", mode);
+    p->cascade = mode;
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_test_starve_next_decode(pkv_pool* p, int32_t warp) {
-  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
-  if (warp < 0) return fail(PKV_ERR_INVALID_ARG, "warp < 0");
-  p->starve_warp = warp;
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    if (warp < 0) return fail(PKV_ERR_INVALID_ARG, "warp < 0");
+    p->starve_warp = warp;
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_test_starve_next_select(pkv_pool* p) {
-  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
-  p->starve_select = true;
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    p->starve_select = true;
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_test_set_geometry(pkv_pool* p, int32_t num_sms, int32_t wpc, int32_t wpc2, int32_t group) {
-  if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
-  if (p->device) return fail(PKV_ERR_INVALID_ARG, "the geometry of a device pool is its GPU's");
-  if (num_sms < 1 || wpc < 1 || wpc2 < 1 || group < 1) return fail(PKV_ERR_INVALID_ARG, "geometry must be positive");
-  p->num_sms = num_sms;
-  p->tc_warps_per_cta = wpc;
-  p->tc2_warps_per_cta = wpc2;
-  p->tc_ctas_per_sm = p->tc2_ctas_per_sm = 1;
-  p->G = group;
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    if (p->device) return fail(PKV_ERR_INVALID_ARG, "the geometry of a device pool is its GPU's");
+    if (num_sms < 1 || wpc < 1 || wpc2 < 1 || group < 1) return fail(PKV_ERR_INVALID_ARG, "geometry must be positive");
+    p->num_sms = num_sms;
+    p->tc_warps_per_cta = wpc;
+    p->tc2_warps_per_cta = wpc2;
+    p->tc_ctas_per_sm = p->tc2_ctas_per_sm = 1;
+    p->G = group;
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_test_plan_bytes(pkv_pool* p, int32_t n, const int32_t* ids, int32_t mode, int32_t S, int32_t W,
                                int32_t num_splits, int32_t general, void* out, size_t cap, size_t* size,
                                int32_t* info) {
-  if (!p || !size || !info) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
-  if (pkv_status r = check_seq_list(p, n, ids)) return r;
-  if (n < 1) return fail(PKV_ERR_INVALID_ARG, "no sequences");
-  if (!valid_mask(mode, S, W)) return fail(PKV_ERR_INVALID_ARG, "invalid mask %d (%d, %d)", mode, S, W);
-  if (num_splits < 0) return fail(PKV_ERR_INVALID_ARG, "num_splits < 0");
-  p->general_plan = general != 0;
-  Plan& plan = build_plan(p, n, ids, mode, S, W, num_splits);
-  p->general_plan = false;
-  const PlanLayout L = plan_layout(plan, warps_per_cta(p, plan.nq), 0);
-  *size = L.bytes;
-  info[0] = plan.total_warps;
-  info[1] = plan.ctas;
-  info[2] = plan.n_partials;
-  info[3] = plan.nq;
-  info[4] = (int32_t)plan.pieces.size();
-  info[5] = (int32_t)plan.combine.size();
-  info[6] = (int32_t)plan.empty.size();
-  info[7] = (int32_t)plan.prefix_items.size();
-  info[8] = (int32_t)plan.prefix_members.size();
-  if (cap < L.bytes || !out) return fail(PKV_ERR_INVALID_ARG, "plan of %zu bytes > cap %zu", L.bytes, cap);
-  plan_write(plan, L, (char*)out);
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    if (!p || !size || !info) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+    if (pkv_status r = check_seq_list(p, n, ids)) return r;
+    if (n < 1) return fail(PKV_ERR_INVALID_ARG, "no sequences");
+    if (!valid_mask(mode, S, W)) return fail(PKV_ERR_INVALID_ARG, "invalid mask %d (%d, %d)", mode, S, W);
+    if (num_splits < 0) return fail(PKV_ERR_INVALID_ARG, "num_splits < 0");
+    p->general_plan = general != 0;
+    Plan& plan = build_plan(p, n, ids, mode, S, W, num_splits);
+    p->general_plan = false;
+    const PlanLayout L = plan_layout(plan, warps_per_cta(p, plan.nq), 0);
+    *size = L.bytes;
+    info[0] = plan.total_warps;
+    info[1] = plan.ctas;
+    info[2] = plan.n_partials;
+    info[3] = plan.nq;
+    info[4] = (int32_t)plan.pieces.size();
+    info[5] = (int32_t)plan.combine.size();
+    info[6] = (int32_t)plan.empty.size();
+    info[7] = (int32_t)plan.prefix_items.size();
+    info[8] = (int32_t)plan.prefix_members.size();
+    if (cap < L.bytes || !out) return fail(PKV_ERR_INVALID_ARG, "plan of %zu bytes > cap %zu", L.bytes, cap);
+    plan_write(plan, L, (char*)out);
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_launch_count(const pkv_pool* p, int64_t* out) {
-  if (!p || !out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
-  *out = p->launches;
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    if (!p || !out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+    *out = p->launches;
+    return PKV_OK;
+  });
 }
 
 }  // extern "C"
