@@ -435,6 +435,15 @@ pkv_status pkv_test_plan_bytes(pkv_pool* pool, int32_t n_seqs, const int32_t* se
                                int32_t num_sinks, int32_t window, int32_t num_splits, int32_t general, void* out,
                                size_t cap, size_t* size, int32_t* info);
 
+/* Test hook (host only): how the library would cut this list of queued
+ * block copies (src, dst pairs, host) into waves that run one after another
+ * (the copies inside a wave run in parallel).  starts_out (host, cap
+ * entries) receives the index of each wave's first copy and, last, n_pairs;
+ * *n_out gets the count (waves + 1; an empty list gives {0, 0}).  The
+ * pool's own queue is untouched. */
+pkv_status pkv_test_cow_waves(pkv_pool* pool, int32_t n_pairs, const int32_t* pairs, int32_t* starts_out,
+                              int32_t cap, int32_t* n_out);
+
 /* Total kernel launches issued by this pool so far (all kernels). */
 pkv_status pkv_launch_count(const pkv_pool* pool, int64_t* out);
 

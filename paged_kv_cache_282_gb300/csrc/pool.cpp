@@ -175,7 +175,8 @@ struct HostAllocator {
   // so the array is never cleared and its untouched pages are never mapped)
   std::unique_ptr<int32_t[]> patch_last;
   size_t patch_last_n = 0;
-  // per block: a member of the current wave of copies (current epoch)
+  // per block, for the current wave of copies: 2 * epoch when the block is a
+  // source in it, 2 * epoch + 1 when it is a destination
   std::vector<uint32_t> wave_mark;
   uint32_t wave_epoch = 0;
 
@@ -548,17 +549,21 @@ std::vector<TablePatch> dedup_patches(HostAllocator& A, const std::vector<TableP
   return out;
 }
 
-// A queued copy whose source or destination is the destination of an earlier
-// copy in the queue must run after it, so the queue is cut into waves of
-// independent copies that run in order. Returns the first copy of each wave
-// and, last, the number of copies.
+// The queued copies must give what running them one by one in queue order
+// gives, and the copies of one launch run in any order.  So the queue is cut
+// into waves that run in order, each free of conflicts: within a wave no
+// copy reads a block that another writes (a source that is an earlier
+// copy's destination, or a destination that is an earlier copy's source)
+// and no two copies write one block.  A block freed after it was queued as
+// a source can come back as a later copy's destination.  Returns the first
+// copy of each wave and, last, the number of copies.
 std::vector<size_t> cow_waves(HostAllocator& A) {
   const size_t ncow = A.pending_cow.size() / 2;
   std::vector<size_t> start{0};
   if (ncow) {
     if (A.wave_mark.size() != (size_t)A.NB) A.wave_mark.assign(A.NB, 0);
     auto next_wave = [&A]() {
-      if (++A.wave_epoch == 0) {
+      if (++A.wave_epoch >= (1u << 31)) {
         std::fill(A.wave_mark.begin(), A.wave_mark.end(), 0);
         A.wave_epoch = 1;
       }
@@ -566,11 +571,13 @@ std::vector<size_t> cow_waves(HostAllocator& A) {
     next_wave();
     for (size_t k = 0; k < ncow; ++k) {
       const int32_t src = A.pending_cow[2 * k], dst = A.pending_cow[2 * k + 1];
-      if (A.wave_mark[src] == A.wave_epoch || A.wave_mark[dst] == A.wave_epoch) {
+      const uint32_t as_src = 2 * A.wave_epoch, as_dst = as_src + 1;
+      if (A.wave_mark[src] == as_dst || A.wave_mark[dst] == as_src || A.wave_mark[dst] == as_dst) {
         start.push_back(k);
         next_wave();
       }
-      A.wave_mark[dst] = A.wave_epoch;  // the destinations of the current wave
+      A.wave_mark[src] = 2 * A.wave_epoch;
+      A.wave_mark[dst] = 2 * A.wave_epoch + 1;
     }
   }
   start.push_back(ncow);
@@ -2627,6 +2634,25 @@ pkv_status pkv_test_plan_bytes(pkv_pool* p, int32_t n, const int32_t* ids, int32
     info[8] = (int32_t)plan.prefix_members.size();
     if (cap < L.bytes || !out) return fail(PKV_ERR_INVALID_ARG, "plan of %zu bytes > cap %zu", L.bytes, cap);
     plan_write(plan, L, (char*)out);
+    return PKV_OK;
+  });
+}
+
+pkv_status pkv_test_cow_waves(pkv_pool* p, int32_t n_pairs, const int32_t* pairs, int32_t* starts_out, int32_t cap,
+                              int32_t* n_out) {
+  return guarded([&]() -> pkv_status {
+    if (!p || !n_out || n_pairs < 0 || (n_pairs > 0 && !pairs)) return fail(PKV_ERR_INVALID_ARG, "bad arguments");
+    auto& A = p->alloc;
+    for (int64_t i = 0; i < 2 * (int64_t)n_pairs; ++i)
+      if (pairs[i] < 0 || pairs[i] >= A.NB) return fail(PKV_ERR_INVALID_ARG, "block %d out of range", pairs[i]);
+    std::vector<int32_t> queued;
+    queued.swap(A.pending_cow);
+    A.pending_cow.assign(pairs, pairs + 2 * (size_t)n_pairs);
+    const std::vector<size_t> w = cow_waves(A);
+    A.pending_cow.swap(queued);
+    *n_out = (int32_t)w.size();
+    if ((int32_t)w.size() > cap || !starts_out) return fail(PKV_ERR_INVALID_ARG, "capacity %d < %zu", cap, w.size());
+    for (size_t i = 0; i < w.size(); ++i) starts_out[i] = (int32_t)w[i];
     return PKV_OK;
   });
 }

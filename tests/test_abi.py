@@ -531,3 +531,53 @@ def test_decode_plans_read_every_kept_block_once(pkv, seed):
     for general in (0, 1):
         raw, info = _plan(pkv, c, ids, 2, S, W, 0, general)
         _check_plan(c, ids, Hk, 2, S, W, 0, raw, info, wpc)
+
+
+def _cow_waves(pkv, c, pairs):
+    import ctypes
+    arr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1))
+    cap = len(pairs) + 2
+    out = np.zeros(cap, dtype=np.int32)
+    n = ctypes.c_int32()
+    pkv._abi.check(c.lib.pkv_test_cow_waves(c._h, len(pairs), arr.ctypes.data, out.ctypes.data, cap, ctypes.byref(n)))
+    return out[: n.value].tolist()
+
+
+def test_copy_waves_run_like_the_queue_in_order(pkv):
+    """The queued copy-on-write copies run in waves; the copies of a wave run
+    in parallel.  Each wave must be free of conflicts (no copy reads a block
+    another one writes, no two write the same block), so that any order
+    inside a wave gives what the queue gives one by one; and a wave ends only
+    where the next copy conflicts with it."""
+    c = pkv.PagedKVCache(12, 4, 2, 64, 4, 4, kv_dtype="fp32", host_only=True)
+    # a block freed after it was queued as a source comes back as a destination
+    assert _cow_waves(pkv, c, [(3, 5), (7, 3)]) == [0, 1, 2]
+    assert _cow_waves(pkv, c, [(3, 5), (5, 6)]) == [0, 1, 2]   # reads an earlier copy's result
+    assert _cow_waves(pkv, c, [(3, 5), (4, 5)]) == [0, 1, 2]   # writes an earlier copy's destination
+    assert _cow_waves(pkv, c, [(3, 5), (3, 6)]) == [0, 2]      # two reads of one block
+    assert _cow_waves(pkv, c, []) == [0, 0]  # one empty wave
+    rng = random.Random(7)
+    for trial in range(3000):
+        n = rng.randint(1, 14)
+        pairs = [(rng.randrange(12), rng.randrange(12)) for _ in range(n)]
+        pairs = [(a, b) for a, b in pairs if a != b] or [(0, 1)]
+        st = _cow_waves(pkv, c, pairs)
+        assert st[0] == 0 and st[-1] == len(pairs) and all(x < y for x, y in zip(st, st[1:]))
+        blocks = list(range(12))
+        for w in range(len(st) - 1):
+            wave = pairs[st[w]:st[w + 1]]
+            srcs, dsts = [a for a, _ in wave], [b for _, b in wave]
+            assert len(set(dsts)) == len(dsts) and not set(dsts) & set(srcs), (pairs, st)
+            if w + 1 < len(st) - 1:  # the next wave's first copy conflicts with this wave
+                a, b = pairs[st[w + 1]]
+                assert a in dsts or b in dsts or b in srcs, (pairs, st)
+            # a conflict-free wave: reading everything first, then writing,
+            # equals running its copies one by one
+            new = blocks.copy()
+            for a, b in wave:
+                new[b] = blocks[a]
+            seq = blocks.copy()
+            for a, b in wave:
+                seq[b] = seq[a]
+            assert new == seq
+            blocks = new

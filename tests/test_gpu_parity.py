@@ -317,6 +317,36 @@ def test_patches_and_cow_chains_in_one_flush():
     assert np.array_equal(d, tw.pool.k[dst, :, :4])
 
 
+
+def test_copy_into_a_block_freed_after_it_was_queued_as_a_source():
+    """A queued copy-on-write reads block A; A is then freed and, before any
+    device call, comes back as the destination of a second copy.  The device
+    must keep the queue's order: the first copy reads A before the second
+    one overwrites it."""
+    wl = workloads.small("bf16", lens=(20, 20), seed=74)
+    tw = Twin(wl, 16, 8, 8, seed=0)
+    a, b = fill_sequences(tw, wl.lens)
+    fb = tw.fork(b)  # b's part-filled last block A is shared
+    _, cow1 = tw.cache.reserve_slots([b], 1)
+    _, ocow1 = tw.alloc.append([b], 1)  # copy A -> B queued; fb still holds A
+    tw.free(fb)  # A goes back to the front of the free pool
+    fa = tw.fork(a)  # a's part-filled last block is shared
+    _, cow2 = tw.cache.reserve_slots([a], 1)
+    _, ocow2 = tw.alloc.append([a], 1)  # its copy lands in A
+    assert np.array_equal(cow1, ocow1) and np.array_equal(cow2, ocow2)
+    assert cow2[0, 1] == cow1[0, 0]
+    for src, dst in list(ocow1) + list(ocow2):
+        tw.pool.copy_block(int(src), int(dst))
+    q = workloads.queries(wl, 1)
+    tw.cache.decode([], q[:0].cuda())  # flushes everything queued
+    tw.cache.sync_status()
+    for s in (a, b, fa):
+        assert np.array_equal(tw.cache.block_table(s), tw.alloc.table(s))
+    for blk in (int(cow1[0, 1]), int(cow2[0, 1])):  # slots 0..3 hold tokens 16..19
+        for dev_pool, host_pool in ((tw.cache.k_pool, tw.pool.k), (tw.cache.v_pool, tw.pool.v)):
+            d = dev_pool.view(torch.int16)[blk, :, :4].cpu().numpy().view(np.uint16)
+            assert np.array_equal(d, host_pool[blk, :, :4]), blk
+
 def test_bounded_wait_reports_timeout_and_context_survives():
     """A stage whose copies are never issued makes its bounded wait run out:
     the kernel returns, the status word reports the expiry, and the next
