@@ -34,7 +34,11 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Device work is enqueued asynchronously on it; host arrays
  *     passed in are fully consumed before the call returns.
- *   - A pool is used from one host thread at a time.
+ *   - A pool is used from one host thread at a time, and its device work
+ *     must run in call order: pass one stream to every call, or order the
+ *     streams yourself.  (Blocks that one call frees on the host can be the
+ *     ones the next call's kernels write, while the first call's kernels may
+ *     still read them.)
  *   - Layouts (row-major, innermost last):
  *       k_pool, v_pool  [num_blocks][n_kv_heads][16][head_dim]  kv dtype
  *       k_scale,v_scale [num_blocks][n_kv_heads][16]            fp32 (FP8 / INT8 only)
