@@ -274,13 +274,28 @@ struct HostAllocator {
     table[s][lb] = v;
     if (queue) pending_patch.push_back({s * max_blocks + lb, v});
   }
+  // Releases the blocks of s from logical block first_lb on (ascending) and
+  // shortens its table there.  Runs of evicted entries (-1), which fill most
+  // of a long streaming sequence's table, are skipped eight at a time.
   void drop_from(int32_t s, int32_t first_lb) {
     auto& t = table[s];
-    for (int32_t lb = first_lb; lb < (int32_t)t.size(); ++lb) {
-      if (t[lb] >= 0) release(t[lb]);
-      if (queue && t[lb] != -1) pending_patch.push_back({s * max_blocks + lb, -1});
+    const int32_t n = (int32_t)t.size();
+    for (int32_t lb = first_lb; lb < n;) {
+      if (lb + 8 <= n) {
+        uint64_t w[4];
+        memcpy(w, t.data() + lb, sizeof w);
+        if ((w[0] & w[1] & w[2] & w[3]) == ~uint64_t(0)) {
+          lb += 8;
+          continue;
+        }
+      }
+      for (const int32_t e = std::min(n, lb + 8); lb < e; ++lb) {
+        const int32_t b = t[lb];
+        if (b >= 0) release(b);
+        if (queue && b != -1) pending_patch.push_back({s * max_blocks + lb, -1});
+      }
     }
-    if ((int32_t)t.size() > first_lb) t.resize(first_lb);
+    if (n > first_lb) t.resize(first_lb);
   }
 };
 
