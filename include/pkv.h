@@ -448,6 +448,13 @@ pkv_status pkv_test_plan_bytes(pkv_pool* pool, int32_t n_seqs, const int32_t* se
 pkv_status pkv_test_cow_waves(pkv_pool* pool, int32_t n_pairs, const int32_t* pairs, int32_t* starts_out,
                               int32_t cap, int32_t* n_out);
 
+/* Test hook (host-only pools): queue_patches != 0 makes the pool queue the
+ * block-table patches a device pool would send to its device table.  Each
+ * call moves the patches queued so far into out (host, (flat index, value)
+ * pairs in queue order, cap pairs), clears the queue (and the queued copies)
+ * and gives their count in *n_out. */
+pkv_status pkv_test_take_patches(pkv_pool* pool, int32_t queue_patches, int32_t* out, int32_t cap, int32_t* n_out);
+
 /* Total kernel launches issued by this pool so far (all kernels). */
 pkv_status pkv_launch_count(const pkv_pool* pool, int64_t* out);
 

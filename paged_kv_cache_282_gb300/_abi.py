@@ -98,6 +98,7 @@ SIGNATURES = {
     "pkv_test_plan_bytes": [c_void_p, c_int32, c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p,
                             c_size_t, c_void_p, c_void_p],
     "pkv_test_cow_waves": [c_void_p, c_int32, c_void_p, c_void_p, c_int32, _P(c_int32)],
+    "pkv_test_take_patches": [c_void_p, c_int32, c_void_p, c_int32, _P(c_int32)],
     "pkv_last_error": [],
     "pkv_version": [],
 }

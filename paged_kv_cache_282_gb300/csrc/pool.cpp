@@ -1921,11 +1921,16 @@ pkv_status pkv_seq_fork(pkv_pool* p, int32_t src, int32_t* dst_out) {
     if (!A.on_device(src)) return fail(PKV_ERR_INVALID_ARG, "sequence %d is not live or is swapped out", src);
     int32_t d;
     if (pkv_status r = pkv_seq_add(p, &d)) return r;
+    // The new id's device row is all -1 (every release of an entry queued a
+    // -1 for it), so only the blocks it shares need table patches.
     const int32_t nblk = ceil_div(A.len[src], kBlock);
+    const int32_t* from = A.table[src].data();
+    A.table[d].assign(from, from + nblk);
     for (int32_t lb = 0; lb < nblk; ++lb) {
-      const int32_t b = A.table[src][lb];
-      if (b >= 0) ++A.refcount[b];
-      A.set_entry(d, lb, b);
+      const int32_t b = from[lb];
+      if (b < 0) continue;
+      ++A.refcount[b];
+      if (A.queue) A.pending_patch.push_back({d * A.max_blocks + lb, b});
     }
     A.len[d] = A.len[src];
     A.holes[d] = A.holes[src];
@@ -2668,6 +2673,24 @@ pkv_status pkv_test_cow_waves(pkv_pool* p, int32_t n_pairs, const int32_t* pairs
     *n_out = (int32_t)w.size();
     if ((int32_t)w.size() > cap || !starts_out) return fail(PKV_ERR_INVALID_ARG, "capacity %d < %zu", cap, w.size());
     for (size_t i = 0; i < w.size(); ++i) starts_out[i] = (int32_t)w[i];
+    return PKV_OK;
+  });
+}
+
+pkv_status pkv_test_take_patches(pkv_pool* p, int32_t queue_patches, int32_t* out, int32_t cap, int32_t* n_out) {
+  return guarded([&]() -> pkv_status {
+    if (!p || !n_out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+    if (p->device) return fail(PKV_ERR_INVALID_ARG, "a device pool flushes its own queue");
+    auto& A = p->alloc;
+    A.queue = queue_patches != 0;
+    *n_out = (int32_t)A.pending_patch.size();
+    if (*n_out > cap || (*n_out > 0 && !out)) return fail(PKV_ERR_INVALID_ARG, "capacity %d < %d patches", cap, *n_out);
+    for (size_t i = 0; i < A.pending_patch.size(); ++i) {
+      out[2 * i] = A.pending_patch[i].index;
+      out[2 * i + 1] = A.pending_patch[i].value;
+    }
+    A.pending_patch.clear();
+    A.pending_cow.clear();
     return PKV_OK;
   });
 }

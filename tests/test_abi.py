@@ -581,3 +581,64 @@ def test_copy_waves_run_like_the_queue_in_order(pkv):
                 seq[b] = seq[a]
             assert new == seq
             blocks = new
+
+
+def _take_patches(pkv, c, queue=True):
+    import ctypes
+    cap = 1 << 16
+    out = np.zeros(2 * cap, dtype=np.int32)
+    n = ctypes.c_int32()
+    pkv._abi.check(c.lib.pkv_test_take_patches(c._h, int(queue), out.ctypes.data, cap, ctypes.byref(n)))
+    return out[: 2 * n.value].reshape(-1, 2)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_table_patches_keep_the_device_table_equal_to_the_host_tables(pkv, seed):
+    """The device block table is only ever changed by the queued patches.
+    Replaying them in order into a model of it after every allocator call
+    (adds, appends with copy-on-write, forks, frees, evictions, truncations,
+    compactions, swaps) must give the host tables: a live sequence's row
+    entry for entry up to its length and -1 past it; -1 everywhere in the
+    rows of free or swapped-out ids."""
+    rng = random.Random(seed)
+    S, MB = 12, 40
+    c = pkv.PagedKVCache(300, 8, 2, 128, S, MB, kv_dtype="bf16", alloc_seed=seed + 1, host_only=True)
+    c.swap_space(200)
+    _take_patches(pkv, c)
+    dev = np.full((S, MB), -1, dtype=np.int32)
+    live = []
+    for op in range(1500):
+        r = rng.random()
+        try:
+            if not live or r < 0.15:
+                live.append(c.seq_add())
+            elif r < 0.45:
+                s = rng.choice(live)
+                c.reserve_slots([s], rng.randint(1, 40))
+            elif r < 0.58:
+                live.append(c.seq_fork(rng.choice(live)))
+            elif r < 0.68:
+                s = rng.choice(live)
+                c.seq_free(s)
+                live.remove(s)
+            elif r < 0.76:
+                c.seq_evict(rng.choice(live), rng.randint(0, 20), rng.randint(1, 100))
+            elif r < 0.84:
+                s = rng.choice(live)
+                c.seq_truncate(s, rng.randint(0, c.seq_len(s)))
+            elif r < 0.90:
+                s = rng.choice(live)
+                c.seq_compact([s], [rng.randint(0, c.seq_len(s))])
+            else:
+                s = rng.choice(live)
+                (c.swap_in if c.swapped(s) else c.swap_out)([s])
+        except pkv.PKVError:
+            pass  # refused calls (out of blocks or ids, evicted last block, swapped-out sequence) change nothing
+        for idx, val in _take_patches(pkv, c):
+            dev.flat[idx] = val
+        for s in range(S):
+            want = np.full(MB, -1, dtype=np.int32)
+            if s in live and not c.swapped(s):
+                t = c.block_table(s)
+                want[: t.size] = t
+            assert np.array_equal(dev[s], want), (seed, op, s)
