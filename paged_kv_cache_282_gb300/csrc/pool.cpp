@@ -1765,8 +1765,11 @@ pkv_status swap_move(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, b
     }
     if (out) {
       A.host_table[s] = row;
-    } else {
-      for (int32_t lb = 0; lb < nb; ++lb) A.set_entry(s, lb, row[lb]);
+    } else {  // the device row is all -1 since the swap-out: patch the blocks only
+      A.table[s] = row;
+      if (A.queue)
+        for (int32_t lb = 0; lb < nb; ++lb)
+          if (row[lb] >= 0) A.pending_patch.push_back({s * A.max_blocks + lb, row[lb]});
     }
   }
   for (int32_t i = 0; i < n; ++i) {
