@@ -521,7 +521,7 @@ def test_decode_plans_read_every_kept_block_once(pkv, seed):
     S, W = rng.randint(0, 40), rng.randint(1, 3000)
     evicted = [s for s in ids if rng.random() < 0.2]
     cases = [(0, 0, 0, 0), (0, 0, 0, rng.randint(1, 70)), (1, 0, rng.randint(0, 3000), 0), (1, 0, 500, 16),
-             (2, S, W, 0), (2, 0, 0, 0)]
+             (1, 0, 0, 0), (2, S, W, 0), (2, 0, 0, 0), (2, 5, 0, 0), (2, 0, 7, 3), (2, 17, 15, 0)]
     for mode, s_, w_, splits in cases:
         for general in (0, 1):
             raw, info = _plan(pkv, c, ids, mode, s_, w_, splits, general)
