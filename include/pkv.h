@@ -181,7 +181,9 @@ pkv_status pkv_pool_stats(const pkv_pool* pool, pkv_stats* out);
  * (src, dst) pairs (host [cow_cap][2], may be NULL).  All or nothing:
  * PKV_ERR_OUT_OF_BLOCKS leaves the state unchanged.  On a device pool the
  * block copies and table updates are queued and run at the start of the next
- * call that takes a stream. */
+ * call that takes a stream, with the result of running them one by one in
+ * queue order (a block freed after it was queued as a copy's source may be
+ * the destination of a later copy). */
 pkv_status pkv_reserve_slots(pkv_pool* pool, int32_t n_seqs, const int32_t* seq_ids, int32_t T,
                              int64_t* slots_out, int32_t* cow_pairs_out, int32_t cow_cap,
                              int32_t* n_cow_out);
