@@ -276,8 +276,10 @@ struct HostAllocator {
   }
   // Releases the blocks of s from logical block first_lb on (ascending) and
   // shortens its table there.  Runs of evicted entries (-1), which fill most
-  // of a long streaming sequence's table, are skipped eight at a time.
-  void drop_from(int32_t s, int32_t first_lb) {
+  // of a long streaming sequence's table, are skipped eight at a time.  The
+  // released entries get -1 patches from logical block patch_from on (the
+  // caller sets the ones below it again).
+  void drop_from(int32_t s, int32_t first_lb, int32_t patch_from = 0) {
     auto& t = table[s];
     const int32_t n = (int32_t)t.size();
     for (int32_t lb = first_lb; lb < n;) {
@@ -292,7 +294,7 @@ struct HostAllocator {
       for (const int32_t e = std::min(n, lb + 8); lb < e; ++lb) {
         const int32_t b = t[lb];
         if (b >= 0) release(b);
-        if (queue && b != -1) pending_patch.push_back({s * max_blocks + lb, -1});
+        if (queue && b != -1 && lb >= patch_from) pending_patch.push_back({s * max_blocks + lb, -1});
       }
     }
     if (n > first_lb) t.resize(first_lb);
@@ -601,13 +603,15 @@ std::vector<size_t> cow_waves(HostAllocator& A) {
 
 // Flushes queued copy-on-write copies and, unless the caller applies them
 // itself (the append kernel does), the queued block-table patches.
-pkv_status flush_pending(pkv_pool* p, cudaStream_t st, bool with_patches = true) {
+// patches_unique: the caller knows no table entry is queued twice.
+pkv_status flush_pending(pkv_pool* p, cudaStream_t st, bool with_patches = true, bool patches_unique = false) {
   HostAllocator& A = p->alloc;
   if (A.pending_cow.empty() && (A.pending_patch.empty() || !with_patches)) return PKV_OK;
   // Table patches: several changes to one entry collapse to the last one (the
   // patch kernel applies its list in parallel).
-  std::vector<TablePatch> patches;
-  if (with_patches) patches = dedup_patches(A, A.pending_patch);
+  std::vector<TablePatch> collapsed;
+  if (with_patches && !patches_unique) collapsed = dedup_patches(A, A.pending_patch);
+  const std::vector<TablePatch>& patches = !with_patches || !patches_unique ? collapsed : A.pending_patch;
   // COW copies in waves of independent copies
   const std::vector<size_t> wave_start = cow_waves(A);
   const size_t ncow = A.pending_cow.size() / 2, npatch = patches.size();
@@ -2260,14 +2264,18 @@ pkv_status pkv_seq_compact(pkv_pool* p, void* stream, int32_t n, const int32_t* 
         return undo(r);
     }
     size_t pos = 0;
-    for (int32_t i = 0; i < n; ++i) A.drop_from(ids[i], 0);  // old blocks, ascending, sequence by sequence
+    // old blocks, ascending, sequence by sequence; each entry gets one patch
+    // (its fresh block below the new length, -1 past it)
+    for (int32_t i = 0; i < n; ++i) A.drop_from(ids[i], 0, ceil_div(counts[i], kBlock));
     for (int32_t i = 0; i < n; ++i) {
       for (int32_t k = 0; k < ceil_div(counts[i], kBlock); ++k) A.set_entry(ids[i], k, fresh[pos++]);
       A.len[ids[i]] = counts[i];
       A.holes[ids[i]] = 0;
     }
     if (!p->device) return PKV_OK;
-    if (pkv_status r = flush_pending(p, st)) return r;  // new tables, after the gather
+    // new tables, after the gather (the queue holds this call's patches only:
+    // the flush before the gather emptied it)
+    if (pkv_status r = flush_pending(p, st, true, true)) return r;
     if (acc && n > 0)
       if (pkv_status r = launch(p, PKV_KERNEL_COMPACT, st, [&] {
             return launch_compact_scores((const CompactSeq*)s->dev, n, keep_idx, keep_stride, acc, acc_stride, st);

@@ -599,7 +599,8 @@ def test_table_patches_keep_the_device_table_equal_to_the_host_tables(pkv, seed)
     (adds, appends with copy-on-write, forks, frees, evictions, truncations,
     compactions, swaps) must give the host tables: a live sequence's row
     entry for entry up to its length and -1 past it; -1 everywhere in the
-    rows of free or swapped-out ids."""
+    rows of free or swapped-out ids.  A compaction queues at most one patch
+    per entry (the library uploads them without collapsing)."""
     rng = random.Random(seed)
     S, MB = 12, 40
     c = pkv.PagedKVCache(300, 8, 2, 128, S, MB, kv_dtype="bf16", alloc_seed=seed + 1, host_only=True)
@@ -609,6 +610,7 @@ def test_table_patches_keep_the_device_table_equal_to_the_host_tables(pkv, seed)
     live = []
     for op in range(1500):
         r = rng.random()
+        compacted = False
         try:
             if not live or r < 0.15:
                 live.append(c.seq_add())
@@ -629,12 +631,16 @@ def test_table_patches_keep_the_device_table_equal_to_the_host_tables(pkv, seed)
             elif r < 0.90:
                 s = rng.choice(live)
                 c.seq_compact([s], [rng.randint(0, c.seq_len(s))])
+                compacted = True
             else:
                 s = rng.choice(live)
                 (c.swap_in if c.swapped(s) else c.swap_out)([s])
         except pkv.PKVError:
             pass  # refused calls (out of blocks or ids, evicted last block, swapped-out sequence) change nothing
-        for idx, val in _take_patches(pkv, c):
+        patches = _take_patches(pkv, c)
+        if compacted:
+            assert len(set(patches[:, 0].tolist())) == len(patches)
+        for idx, val in patches:
             dev.flat[idx] = val
         for s in range(S):
             want = np.full(MB, -1, dtype=np.int32)
