@@ -18,7 +18,6 @@
 #include <numeric>
 #include <set>
 #include <string>
-#include <unordered_map>
 #include <vector>
 
 #include "../../include/pkv.h"
@@ -175,6 +174,21 @@ struct HostAllocator {
   // so the array is never cleared and its untouched pages are never mapped)
   std::unique_ptr<int32_t[]> patch_last;
   size_t patch_last_n = 0;
+  // per source block of a swap (device or host block): its destination,
+  // valid where move_mark holds the current epoch
+  std::vector<uint32_t> move_mark;
+  std::vector<int32_t> move_dst;
+  uint32_t move_epoch = 0;
+  void begin_moves(size_t n_src) {
+    if (move_mark.size() < n_src) {
+      move_mark.assign(n_src, 0);
+      move_dst.assign(n_src, -1);
+    }
+    if (++move_epoch == 0) {
+      std::fill(move_mark.begin(), move_mark.end(), 0);
+      move_epoch = 1;
+    }
+  }
   // per block, for the current wave of copies: 2 * epoch when the block is a
   // source in it, 2 * epoch + 1 when it is a destination
   std::vector<uint32_t> wave_mark;
@@ -1735,19 +1749,26 @@ pkv_status swap_move(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, b
   }
   if (const int32_t d = A.first_repeat(n, ids); d >= 0)
     return fail(PKV_ERR_INVALID_ARG, "sequence %d listed twice", d);
-  std::unordered_map<int32_t, int32_t> moved;  // source block -> destination block
+  // each distinct source block moves once: its destination, once taken,
+  // serves every listed sequence that holds it
+  A.begin_moves(out ? (size_t)A.NB : (size_t)A.NH);
+  size_t need = 0;
   for (int32_t i = 0; i < n; ++i)
     for (int32_t b : out ? A.table[ids[i]] : A.host_table[ids[i]])
-      if (b >= 0) moved.emplace(b, -1);
+      if (b >= 0 && A.move_mark[b] != A.move_epoch) {
+        A.move_mark[b] = A.move_epoch;
+        A.move_dst[b] = -1;
+        ++need;
+      }
   const size_t avail = out ? A.host_free.size() : A.free_blocks.size();
-  if (moved.size() > avail)
-    return fail(PKV_ERR_OUT_OF_BLOCKS, "swap-%s needs %zu blocks, %zu free", out ? "out" : "in", moved.size(), avail);
+  if (need > avail)
+    return fail(PKV_ERR_OUT_OF_BLOCKS, "swap-%s needs %zu blocks, %zu free", out ? "out" : "in", need, avail);
   cudaStream_t st = (cudaStream_t)stream;
   // queued copies first: a pending copy-on-write must land before its blocks move
   if (p->device)
     if (pkv_status r = flush_pending(p, st)) return r;
   std::vector<int32_t> pairs;
-  pairs.reserve(2 * moved.size());
+  pairs.reserve(2 * need);
   for (int32_t i = 0; i < n; ++i) {
     const int32_t s = ids[i], nb = ceil_div(A.len[s], kBlock);
     std::vector<int32_t> row(nb, -1);
@@ -1755,7 +1776,7 @@ pkv_status swap_move(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, b
     for (int32_t lb = 0; lb < nb && lb < (int32_t)from.size(); ++lb) {
       const int32_t b = from[lb];
       if (b < 0) continue;
-      int32_t& m = moved[b];
+      int32_t& m = A.move_dst[b];
       if (m < 0) {
         m = out ? A.take_host() : A.take();
         pairs.push_back(b);
