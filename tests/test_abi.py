@@ -629,8 +629,8 @@ def test_table_patches_keep_the_device_table_equal_to_the_host_tables(pkv, seed)
                 s = rng.choice(live)
                 c.seq_truncate(s, rng.randint(0, c.seq_len(s)))
             elif r < 0.90:
-                s = rng.choice(live)
-                c.seq_compact([s], [rng.randint(0, c.seq_len(s))])
+                group = rng.sample(live, rng.randint(1, min(3, len(live))))
+                c.seq_compact(group, [rng.randint(0, c.seq_len(x)) for x in group])
                 compacted = True
             else:
                 s = rng.choice(live)
