@@ -217,7 +217,7 @@ class Stepper:
                      logits_stride=self.stride, workspace=self.ws)
             c.h2o_scores(self.ids, self.logits, self.stride, self.lse, self.acc, self.stride, mask=wl.mask,
                          num_sinks=wl.num_sinks, window=wl.window)
-            c.h2o_select(self.lens1, self.acc, self.stride, wl.budget, wl.recent, self.keep, wl.budget, self.keep_n)
+            c.h2o_select(self.ids, self.acc, self.stride, wl.budget, wl.recent, self.keep, wl.budget, self.keep_n)
         else:
             c.decode(self.ids, self.q if q is None else q, scale=wl.scale, mask=wl.mask, num_sinks=wl.num_sinks,
                      window=wl.window, num_splits=self.num_splits, out=o, lse=self.lse, workspace=self.ws)
@@ -674,7 +674,7 @@ def run_op(args, wl, label, dev):
         n = len(setup.ids)
         keep = torch.zeros((n, wl.budget), dtype=torch.int32, device=dev)
         cnt = torch.zeros(n, dtype=torch.int32, device=dev)
-        c.h2o_select(st.lens, st.acc, st.stride, wl.budget, wl.recent, keep, wl.budget, cnt)
+        c.h2o_select(st.ids, st.acc, st.stride, wl.budget, wl.recent, keep, wl.budget, cnt)
         c.sync_status()
         counts = cnt.cpu().numpy()
         moved = int(counts.sum()) * wl.n_kv_heads * 2 * row_bytes  # K and V rows read (and as many written)

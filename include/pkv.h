@@ -74,8 +74,13 @@ typedef enum {
   PKV_ERR_DEVICE_ASSERT = 7, /* a device-side range check failed */
   PKV_ERR_NO_DEVICE = 8,     /* device work requested on a host-only pool */
   PKV_ERR_WORKSPACE = 9,     /* workspace too small (see pkv_decode_workspace_size) */
-  PKV_ERR_HOST_MEMORY = 10   /* a host allocation failed; the pool may be part-way
+  PKV_ERR_HOST_MEMORY = 10,  /* a host allocation failed; the pool may be part-way
                                 through the call and should be destroyed */
+  PKV_ERR_UNDRAINED = 11     /* a device-side bounded wait ran out, and so did the
+                                wait for the copies the kernel had already issued:
+                                they may still land in shared memory after the
+                                kernel exits, so later work on this CUDA context
+                                is not reliable (recreate the context) */
 } pkv_status;
 
 typedef enum { PKV_KV_FP32 = 0, PKV_KV_BF16 = 1, PKV_KV_FP8_E4M3 = 2, PKV_KV_INT8 = 3 } pkv_kv_dtype;
@@ -90,7 +95,8 @@ typedef enum { PKV_KV_FP32 = 0, PKV_KV_BF16 = 1, PKV_KV_FP8_E4M3 = 2, PKV_KV_INT
 typedef enum { PKV_MASK_FULL = 0, PKV_MASK_SLIDING = 1, PKV_MASK_SINK_WINDOW = 2 } pkv_mask_mode;
 
 /* [PA] PagedAttention 的设计 / 三大运行时组件.  Shapes supported: block_size
- * 16; head_dim 128 for BF16/FP8/INT8 and 64 or 128 for FP32; G in {1, 2, 4, 8}. */
+ * 16; head_dim 64 or 128 (every kv dtype); G in {1, 2, 4, 8} ([LC] MHA / GQA /
+ * MQA head counts).  Anything else: PKV_ERR_UNSUPPORTED. */
 typedef struct {
   int32_t num_blocks;         /* physical blocks in the pool */
   int32_t block_size;         /* must be 16 */
@@ -212,7 +218,12 @@ pkv_status pkv_decode_workspace_size(const pkv_pool* pool, int32_t n_seqs, int32
  * (context length L_b, the current token included) and query head h:
  *   s_j = scale * q[b][h] . K_j   for kept keys j (FP8 / INT8: K_j = code_j * s_j)
  *   out[b][h] = sum_j softmax(s)_j V_j,   lse[b][h] = ln sum_j exp(s_j)
- * Empty keep-set: out = 0, lse = -inf.
+ * Empty keep-set: out = 0, lse = -inf.  Accumulation is fp32.  FP8 / INT8
+ * pools: the codes enter the tensor-core products exactly; q is rounded to
+ * fp16 after scaling each head by a power of two (so no element overflows),
+ * and the softmax weights, normalised by the largest weight times V scale,
+ * are rounded to fp16 -- valid for any magnitudes of q, K and V, with V
+ * scales above 2^-100.
  *   q, out      device [n_seqs][n_heads][head_dim] (fp32 for FP32 pools, else bf16)
  *   lse         device [n_seqs][n_heads] fp32, or NULL
  *   logits      device [n_seqs][n_kv_heads][logits_stride][G] fp32, or NULL:
@@ -240,13 +251,15 @@ pkv_status pkv_decode_attn(pkv_pool* pool, void* stream, int32_t n_seqs, const i
  * latency-critical loop where cudaMalloc / cudaFree would synchronise the
  * device.  It allocates no device or pinned memory (host-side planning uses
  * ordinary heap memory) and copies its plan from pageable memory.
- *   - bf16 and FP8 pools only (PKV_ERR_UNSUPPORTED for fp32); the pool's
+ *   - bf16, FP8 and INT8 pools (PKV_ERR_UNSUPPORTED for fp32); the pool's
  *     device must be the current device.
  *   - A call that needs more than the array holds fails with
  *     PKV_ERR_WORKSPACE and a message giving both sizes; nothing is launched.
  *   - The first call on a device looks up the array's device address (once per
- *     device, with that device current); make that first call before any
- *     stream capture.
+ *     device, with that device current) and keeps it for the life of the
+ *     process; make that first call before any stream capture.  After the
+ *     device's primary context is reset, the kept address is stale: do not
+ *     call this entry point again in that process.
  *   - Every device that runs this entry point keeps the 32 MiB until the
  *     process exits.  All calls share the array: calls whose work overlaps on
  *     the GPU (other streams, other pools on the same device) race on it. */
@@ -267,13 +280,15 @@ pkv_status pkv_h2o_scores(pkv_pool* pool, void* stream, int32_t n_seqs, const in
                           int64_t acc_stride);
 
 /* H2O keep-set ([LC] H2OEviction.select, [SO] evict_tokens with recent = 0):
- * with keep = budget - recent, the positions [L - recent, L) plus the keep
- * highest acc values among [0, L - recent) (ties to the lower position), in
- * ascending order; all of [0, L) when L <= budget.  lens: host [n_seqs].
- * acc: device [n_seqs][acc_stride] fp32 (>= 0).  keep_idx: device
+ * for each listed sequence (length L, the pool's own), with keep = budget -
+ * recent, the positions [L - recent, L) plus the keep highest acc values among
+ * [0, L - recent) (ties to the lower position), in ascending order; all of
+ * [0, L) when L <= budget.  seq_ids: host [n_seqs], live sequences on the
+ * device.  acc: device [n_seqs][acc_stride] fp32 (>= 0; row i belongs to
+ * seq_ids[i]; acc_stride >= every listed length).  keep_idx: device
  * [n_seqs][keep_stride] int32 (keep_stride >= budget); keep_count: device
  * [n_seqs] int32.  0 <= recent <= budget. */
-pkv_status pkv_h2o_select(pkv_pool* pool, void* stream, int32_t n_seqs, const int32_t* lens,
+pkv_status pkv_h2o_select(pkv_pool* pool, void* stream, int32_t n_seqs, const int32_t* seq_ids,
                           const float* acc, int64_t acc_stride, int32_t budget, int32_t recent,
                           int32_t* keep_idx, int64_t keep_stride, int32_t* keep_count);
 
@@ -286,9 +301,10 @@ pkv_status pkv_h2o_select(pkv_pool* pool, void* stream, int32_t n_seqs, const in
  * recent is kept once and the set may be smaller than the three sizes'
  * sum.  Output ascending in keep_idx (device [n_seqs][keep_stride], with
  * keep_stride >= min(sink_size + window_size + h2o_size, largest length)),
- * its size in keep_count (device [n_seqs]).  lens: host [n_seqs]; acc:
- * device [n_seqs][acc_stride] fp32 (>= 0). */
-pkv_status pkv_policy_select(pkv_pool* pool, void* stream, int32_t n_seqs, const int32_t* lens,
+ * its size in keep_count (device [n_seqs]).  seq_ids: host [n_seqs], live
+ * sequences on the device (L is each one's length in the pool); acc: device
+ * [n_seqs][acc_stride] fp32 (>= 0; acc_stride >= every listed length). */
+pkv_status pkv_policy_select(pkv_pool* pool, void* stream, int32_t n_seqs, const int32_t* seq_ids,
                              const float* acc, int64_t acc_stride, int32_t sink_size, int32_t window_size,
                              int32_t h2o_size, int32_t* keep_idx, int64_t keep_stride, int32_t* keep_count);
 
@@ -361,7 +377,7 @@ pkv_status pkv_get_host_block_table(const pkv_pool* pool, int32_t seq, int32_t* 
 pkv_status pkv_host_free_blocks(const pkv_pool* pool, int64_t* n_out);
 
 /* Synchronises `stream`, then reports and clears the device status word:
- * PKV_ERR_TIMEOUT, PKV_ERR_DEVICE_ASSERT or PKV_OK. */
+ * PKV_ERR_UNDRAINED, PKV_ERR_TIMEOUT, PKV_ERR_DEVICE_ASSERT or PKV_OK. */
 pkv_status pkv_sync_status(pkv_pool* pool, void* stream);
 
 /* ---- measurement -------------------------------------------------------- */
@@ -393,7 +409,9 @@ pkv_status pkv_timing_read(pkv_pool* pool, double* total_ms_out /* [PKV_KERNEL_C
  * on the score rows it streams into shared memory.  A wait that runs out sets
  * PKV_ERR_TIMEOUT in the status word; the warp (decode) or block (selection;
  * its keep_count is then 0) waits for its own copies in flight (bounded
- * again) and returns, leaving the context usable. */
+ * again: 50 ms) and returns.  When those copies landed, the context stays
+ * usable; when that second wait runs out too, the status word reports
+ * PKV_ERR_UNDRAINED instead, and the context is not to be trusted. */
 pkv_status pkv_set_wait_limit(pkv_pool* pool, int64_t wait_limit_ns);
 /* Shared-prefix (cascade) decode ([PA] prefix sharing: a system prompt
  * reused by many requests, parallel sampling).  In decode over whole

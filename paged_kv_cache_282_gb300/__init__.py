@@ -288,19 +288,22 @@ class PagedKVCache:
                                            int(logits_stride), lse.data_ptr(), MASKS[mask], num_sinks, window,
                                            acc.data_ptr(), int(acc_stride)))
 
-    def h2o_select(self, lens, acc, acc_stride: int, budget: int, recent: int, keep_idx, keep_stride: int,
+    def h2o_select(self, seq_ids, acc, acc_stride: int, budget: int, recent: int, keep_idx, keep_stride: int,
                    keep_count, stream=None) -> None:
-        ln = _i32_array(lens)
-        _abi.check(self.lib.pkv_h2o_select(self._h, _stream_ptr(stream), ln.size, _ptr(ln), acc.data_ptr(),
+        """H2O keep-sets of the listed sequences (lengths from the pool); acc
+        row i belongs to seq_ids[i]."""
+        ids = _i32_array(seq_ids)
+        _abi.check(self.lib.pkv_h2o_select(self._h, _stream_ptr(stream), ids.size, _ptr(ids), acc.data_ptr(),
                                            int(acc_stride), budget, recent, keep_idx.data_ptr(), int(keep_stride),
                                            keep_count.data_ptr()))
 
-    def policy_select(self, lens, acc, acc_stride: int, sink_size: int, window_size: int, h2o_size: int, keep_idx,
+    def policy_select(self, seq_ids, acc, acc_stride: int, sink_size: int, window_size: int, h2o_size: int, keep_idx,
                       keep_stride: int, keep_count, stream=None) -> None:
         """Combined keep rule: first sink_size positions, last window_size,
-        and the h2o_size highest scores over all positions."""
-        ln = _i32_array(lens)
-        _abi.check(self.lib.pkv_policy_select(self._h, _stream_ptr(stream), ln.size, _ptr(ln), acc.data_ptr(),
+        and the h2o_size highest scores over all positions (lengths from the
+        pool; acc row i belongs to seq_ids[i])."""
+        ids = _i32_array(seq_ids)
+        _abi.check(self.lib.pkv_policy_select(self._h, _stream_ptr(stream), ids.size, _ptr(ids), acc.data_ptr(),
                                               int(acc_stride), sink_size, window_size, h2o_size, keep_idx.data_ptr(),
                                               int(keep_stride), keep_count.data_ptr()))
 

@@ -15,7 +15,7 @@ PKV_OK = 0
 STATUS_NAMES = {
     0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_OUT_OF_BLOCKS",
     4: "PKV_ERR_OUT_OF_SEQS", 5: "PKV_ERR_CUDA", 6: "PKV_ERR_TIMEOUT", 7: "PKV_ERR_DEVICE_ASSERT",
-    8: "PKV_ERR_NO_DEVICE", 9: "PKV_ERR_WORKSPACE", 10: "PKV_ERR_HOST_MEMORY",
+    8: "PKV_ERR_NO_DEVICE", 9: "PKV_ERR_WORKSPACE", 10: "PKV_ERR_HOST_MEMORY", 11: "PKV_ERR_UNDRAINED",
 }
 KV_DTYPES = {"fp32": 0, "bf16": 1, "fp8": 2, "fp8_e4m3": 2, "int8": 3}
 MASKS = {"full": 0, "sliding": 1, "sink_window": 2}

@@ -1,0 +1,34 @@
+// decode_tc_64.cu -- the decode kernel of decode_tc.cuh instantiated for
+// head_dim 64 (BF16, FP8-E4M3 and INT8 KV; G in {1, 2, 4, 8}; one or two
+// sequences per warp), with its launch, shared-memory and occupancy dispatch.
+
+#include "decode_tc.cuh"
+
+namespace pkv {
+
+cudaError_t launch_decode_tc_d64(int kv_dtype, int G, int nq, const DecodeTCParams& p, int ctas, cudaStream_t st) {
+  if (ctas <= 0) return cudaSuccess;
+#define X(KV, GG, NQ) \
+  if (kv_dtype == KV && G == GG && nq == NQ) return launch_t<KV, GG, NQ, 64>(p, ctas, st);
+  PKV_FOR_VARIANTS(X)
+#undef X
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t decode_tc_prepare_d64(int kv_dtype, int G, int nq) {
+#define X(KV, GG, NQ) \
+  if (kv_dtype == KV && G == GG && nq == NQ) return prepare_t<KV, GG, NQ, 64>();
+  PKV_FOR_VARIANTS(X)
+#undef X
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t decode_tc_occupancy_d64(int kv_dtype, int G, int nq, int* n) {
+#define X(KV, GG, NQ) \
+  if (kv_dtype == KV && G == GG && nq == NQ) return occupancy_t<KV, GG, NQ, 64>(n);
+  PKV_FOR_VARIANTS(X)
+#undef X
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pkv

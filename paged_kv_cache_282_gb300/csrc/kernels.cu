@@ -81,15 +81,17 @@ __global__ void append_copy_kernel(const __grid_constant__ AppendArgs a, int row
   }
 }
 
-// FP8 / INT8: one warp per (token, kv head, K|V) row of 128 values.
+// FP8 / INT8: one warp per (token, kv head, K|V) row of D values (D / 32 per
+// lane).
 //   FP8:  s = absmax / 448, code = E4M3(x / s), round to nearest even,
 //         saturate to +-448
 //   INT8: s = absmax / 127, code = x / s rounded to the nearest integer
 //         (ties to even), clamped to +-127
 // (fp32, IEEE division; s = 1 when absmax is 0)
-template <int KV>
+template <int KV, int D>
 __global__ void append_quant_kernel(const __grid_constant__ AppendArgs a) {
   constexpr float kMaxCode = KV == 3 ? 127.0f : 448.0f;
+  constexpr int E = D / 32;  // values per lane: 4 or 2
   apply_patches(a);
   const int lane = threadIdx.x & 31;
   const int64_t rows = (int64_t)a.n_tokens * a.Hk;
@@ -99,18 +101,26 @@ __global__ void append_quant_kernel(const __grid_constant__ AppendArgs a) {
     const int64_t row = is_v ? w - rows : w;  // = t * Hk + g
     const int64_t t = row / a.Hk, g = row - t * a.Hk;
     const __nv_bfloat16* src =
-        static_cast<const __nv_bfloat16*>(is_v ? a.v_new : a.k_new) + row * 128 + lane * 4;
-    const uint2 raw = *reinterpret_cast<const uint2*>(src);
-    const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-    const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-    float x[4] = {__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi)};
-    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+        static_cast<const __nv_bfloat16*>(is_v ? a.v_new : a.k_new) + row * D + lane * E;
+    float x[E];
+    if constexpr (E == 4) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(src);
+      const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+      const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+      x[0] = __low2float(lo), x[1] = __high2float(lo), x[2] = __low2float(hi), x[3] = __high2float(hi);
+    } else {
+      const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(src);
+      x[0] = __low2float(v), x[1] = __high2float(v);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int k = 0; k < E; ++k) amax = fmaxf(amax, fabsf(x[k]));
 #pragma unroll
     for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
     const float s = amax == 0.0f ? 1.0f : __fdiv_rn(amax, kMaxCode);
     uint32_t packed = 0;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < E; ++k) {
       uint32_t code;
       if (KV == 3) {
         const int n = __float2int_rn(__fdiv_rn(x[k], s));
@@ -123,8 +133,11 @@ __global__ void append_quant_kernel(const __grid_constant__ AppendArgs a) {
     const int64_t slot = slot_of(a, t);
     const int64_t blk = slot >> 4, off = slot & 15;
     const int64_t srow = (blk * a.Hk + g) * kBlock + off;
-    uint8_t* dst = static_cast<uint8_t*>(is_v ? a.v_pool : a.k_pool) + srow * 128 + lane * 4;
-    *reinterpret_cast<uint32_t*>(dst) = packed;
+    uint8_t* dst = static_cast<uint8_t*>(is_v ? a.v_pool : a.k_pool) + srow * D + lane * E;
+    if constexpr (E == 4)
+      *reinterpret_cast<uint32_t*>(dst) = packed;
+    else
+      *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
     if (lane == 0) (is_v ? a.v_scale : a.k_scale)[srow] = s;
   }
 }
@@ -197,7 +210,7 @@ __global__ void h2o_score_kernel(const SeqRow* __restrict__ rows, int n_heads, i
       for (int u = 0; u < 8; ++u) {
         if (f0 + u < nf) {
           const float* ls = s_lse + 4 * (f0 + u);
-          sum += __expf(x[u].x - ls[0]) + __expf(x[u].y - ls[1]) + __expf(x[u].z - ls[2]) + __expf(x[u].w - ls[3]);
+          sum += expf(x[u].x - ls[0]) + expf(x[u].y - ls[1]) + expf(x[u].z - ls[2]) + expf(x[u].w - ls[3]);
         }
       }
     }
@@ -205,7 +218,7 @@ __global__ void h2o_score_kernel(const SeqRow* __restrict__ rows, int n_heads, i
 #pragma unroll 8
     for (int g = 0; g < n_kv_heads; ++g) {
       const float* lg = logits + (((size_t)b * n_kv_heads + g) * stride + j) * G;
-      for (int i = 0; i < G; ++i) sum += __expf(lg[i] - s_lse[g * G + i]);
+      for (int i = 0; i < G; ++i) sum += expf(lg[i] - s_lse[g * G + i]);
     }
   }
   *accj = prev + sum / (float)n_heads;
@@ -277,7 +290,8 @@ struct SelShared {
   int tot[32];     // per-warp candidate counts of a sweep
   uint32_t prefix, mask;
   int k, n_cand, top, n_head;
-  int starve;  // test hook: the first chunk of this block's row is never issued
+  int starve;     // test hook: the first chunk of this block's row is never issued
+  int undrained;  // a copy into the ring was still in flight when the drain gave up
 };
 
 // Slot of candidate i in the shared candidate arrays: the word index with its
@@ -532,7 +546,9 @@ __device__ int gather_ring(const float* __restrict__ a, int n, uint32_t thr, boo
   auto drain = [&](int first, int end) {  // thread 0: chunks [first, end) were issued, not consumed
     if (t == 0)
       for (int v = first; v < end; ++v)
-        mbar_wait(smem_addr(&sh.bar[v % kSelRing]), (uint32_t)((v / kSelRing) & 1), limit_ns);
+        if (!(v == 0 && sh.starve) &&  // the test hook's stage has no copy to wait for
+            !mbar_wait(smem_addr(&sh.bar[v % kSelRing]), (uint32_t)((v / kSelRing) & 1), limit_ns))
+          sh.undrained = 1;
     __syncthreads();
   };
   if (__syncthreads_or(ok ? 0 : 1)) {
@@ -629,7 +645,10 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
                                                                  int32_t* __restrict__ status, uint64_t wait_limit_ns,
                                                                  int starve_first) {
   __shared__ SelShared sh;
-  if (threadIdx.x == 0) sh.starve = starve_first && blockIdx.x == 0;
+  if (threadIdx.x == 0) {
+    sh.starve = starve_first && blockIdx.x == 0;
+    sh.undrained = 0;
+  }
   extern __shared__ uint32_t cand[];  // kSelCap keys, kSelCap positions, then the ring
   uint32_t* c_key = cand;
   int32_t* c_pos = reinterpret_cast<int32_t*>(cand + kSelCap);
@@ -655,7 +674,7 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SeqRow* _
   };
   auto timed_out = [&]() {
     if (threadIdx.x == 0) {
-      atomicOr(status, kStatusTimeout);
+      atomicOr(status, sh.undrained ? kStatusTimeout | kStatusUndrained : kStatusTimeout);
       keep_count[b] = 0;
     }
   };
@@ -895,10 +914,18 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t st) {
   if (a.kv_dtype == 2 || a.kv_dtype == 3) {
     const int64_t warps = 2LL * a.n_tokens * a.Hk;
     const int grid = grid_for(std::max<int64_t>(warps * 32, a.n_patches), 256);
-    if (a.kv_dtype == 3)
-      append_quant_kernel<3><<<grid, 256, 0, st>>>(a);
-    else
-      append_quant_kernel<2><<<grid, 256, 0, st>>>(a);
+    if (a.D != 64 && a.D != 128) return cudaErrorInvalidValue;
+    if (a.kv_dtype == 3) {
+      if (a.D == 64)
+        append_quant_kernel<3, 64><<<grid, 256, 0, st>>>(a);
+      else
+        append_quant_kernel<3, 128><<<grid, 256, 0, st>>>(a);
+    } else {
+      if (a.D == 64)
+        append_quant_kernel<2, 64><<<grid, 256, 0, st>>>(a);
+      else
+        append_quant_kernel<2, 128><<<grid, 256, 0, st>>>(a);
+    }
   } else {
     const int row_chunks = a.D * (a.kv_dtype == 0 ? 4 : 2) / 16;
     const int64_t work = 2LL * a.n_tokens * a.Hk * row_chunks;

@@ -9,10 +9,23 @@
 namespace pkv {
 
 constexpr int kBlock = 16;   // tokens per physical block
-constexpr int kHeadDimTC = 128;  // head_dim of the tensor-core decode path
 
-// Device status word bits (pool status buffer, element 0).
-enum : int32_t { kStatusTimeout = 1, kStatusBadBlock = 2 };
+// Device status word bits (pool status buffer, element 0).  kStatusUndrained:
+// after a wait ran out, copies the waiting warp or block had issued were
+// still in flight when it gave up waiting for them too.
+enum : int32_t { kStatusTimeout = 1, kStatusBadBlock = 2, kStatusUndrained = 4 };
+
+// Geometry of the tensor-core decode kernel for a kv dtype (1 bf16, 2 FP8,
+// 3 INT8), sequences per warp (nq) and head_dim D: warps per CTA (one CTA
+// per SM), stages of each warp's ring, and dynamic shared memory.
+constexpr int tc_warps(int kv, int nq, int D) {
+  return (D == 128 && (kv == 1 || nq == 2)) || (kv != 1 && nq == 2) ? 12 : 16;
+}
+constexpr int tc_stages(int kv, int nq, int D) { return kv != 1 && (nq == 2 || D == 64) ? 3 : 2; }
+constexpr size_t tc_smem_bytes(int kv, int nq, int D) {
+  return 1024 + (size_t)tc_warps(kv, nq, D) * tc_stages(kv, nq, D) *
+                    (size_t)(2 * kBlock * D * (kv == 1 ? 2 : 1) + (kv == 1 ? 0 : 128) + 8);
+}
 
 // One contiguous range of logical blocks of one (sequence, kv head), handled
 // by one warp of the decode kernel.  Consecutive pieces of the same
@@ -87,7 +100,7 @@ struct SeqRow {
 inline __host__ __device__ int partial_floats(int G, int D) { return G * D + ((2 * G + 3) & ~3); }
 
 struct DecodeTCParams {
-  CUtensorMap tmap_k;  // 2-D view [num_blocks * Hk * 16][D] of the K pool, 128B swizzle
+  CUtensorMap tmap_k;  // 2-D view of the K pool in 128-byte rows, 128B swizzle (see make_tensor_map)
   CUtensorMap tmap_v;
   const float* k_scale;  // FP8 only
   const float* v_scale;
@@ -137,21 +150,35 @@ struct DecodeF32Params {
 
 // ---- kernel launchers (defined in the .cu files) -------------------------
 
-// Tensor-core decode: kv_dtype 1 = bf16, 2 = FP8; nq = 1, or 2 for the
-// variant whose pieces may carry a second sequence over shared blocks.
-// Returns the launch error.
-cudaError_t launch_decode_tc(int kv_dtype, int G, int nq, const DecodeTCParams& p, int grid_ctas,
-                             cudaStream_t stream);
-// Shared-prefix multi-query kernel (bf16 KV): one CTA per PrefixItem.
+// Tensor-core decode: kv_dtype 1 = bf16, 2 = FP8, 3 = INT8; nq = 1, or 2 for
+// the variant whose pieces may carry a second sequence over shared blocks;
+// one set per head_dim (64, 128).  Return the launch / attribute error.
+cudaError_t launch_decode_tc_d64(int kv_dtype, int G, int nq, const DecodeTCParams& p, int grid_ctas,
+                                 cudaStream_t stream);
+cudaError_t launch_decode_tc_d128(int kv_dtype, int G, int nq, const DecodeTCParams& p, int grid_ctas,
+                                  cudaStream_t stream);
+cudaError_t decode_tc_prepare_d64(int kv_dtype, int G, int nq);
+cudaError_t decode_tc_prepare_d128(int kv_dtype, int G, int nq);
+cudaError_t decode_tc_occupancy_d64(int kv_dtype, int G, int nq, int* ctas_per_sm);
+cudaError_t decode_tc_occupancy_d128(int kv_dtype, int G, int nq, int* ctas_per_sm);
+inline cudaError_t launch_decode_tc(int kv_dtype, int G, int nq, int D, const DecodeTCParams& p, int grid_ctas,
+                                    cudaStream_t stream) {
+  return D == 64 ? launch_decode_tc_d64(kv_dtype, G, nq, p, grid_ctas, stream)
+                 : launch_decode_tc_d128(kv_dtype, G, nq, p, grid_ctas, stream);
+}
+// sets the dynamic shared-memory attribute
+inline cudaError_t decode_tc_prepare(int kv_dtype, int G, int nq, int D) {
+  return D == 64 ? decode_tc_prepare_d64(kv_dtype, G, nq) : decode_tc_prepare_d128(kv_dtype, G, nq);
+}
+inline cudaError_t decode_tc_occupancy(int kv_dtype, int G, int nq, int D, int* ctas_per_sm) {
+  return D == 64 ? decode_tc_occupancy_d64(kv_dtype, G, nq, ctas_per_sm)
+                 : decode_tc_occupancy_d128(kv_dtype, G, nq, ctas_per_sm);
+}
+// Shared-prefix multi-query kernel (bf16 KV, head_dim 128): one CTA per PrefixItem.
 cudaError_t launch_prefix_decode(int G, const DecodeTCParams& p, cudaStream_t stream);
 cudaError_t prefix_decode_prepare(int G);
 constexpr int kPrefixRowsPerCta = 128;  // 8 warps x 16 query rows
 
-// Decode kernel geometry: warps per CTA and dynamic shared memory bytes.
-int decode_tc_warps_per_cta(int kv_dtype, int nq);
-size_t decode_tc_smem_bytes(int kv_dtype, int nq);
-cudaError_t decode_tc_prepare(int kv_dtype, int G, int nq);  // sets the smem attribute
-cudaError_t decode_tc_occupancy(int kv_dtype, int G, int nq, int* ctas_per_sm);
 
 cudaError_t launch_decode_f32(const DecodeF32Params& p, cudaStream_t stream);
 

@@ -517,10 +517,8 @@ pkv_status check_config(const pkv_pool_config* c) {
   if (c->kv_dtype != PKV_KV_FP32 && c->kv_dtype != PKV_KV_BF16 && c->kv_dtype != PKV_KV_FP8_E4M3 &&
       c->kv_dtype != PKV_KV_INT8)
     return fail(PKV_ERR_INVALID_ARG, "unknown kv_dtype %d", c->kv_dtype);
-  if (c->kv_dtype == PKV_KV_FP32 && c->head_dim != 64 && c->head_dim != 128)
-    return fail(PKV_ERR_UNSUPPORTED, "fp32 pools support head_dim 64 or 128");
-  if (c->kv_dtype != PKV_KV_FP32 && c->head_dim != kHeadDimTC)
-    return fail(PKV_ERR_UNSUPPORTED, "bf16 / fp8 / int8 pools support head_dim 128");
+  if (c->head_dim != 64 && c->head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %d not in {64, 128}", c->head_dim);
   if ((int64_t)c->num_blocks * c->n_kv_heads * kBlock >= (int64_t(1) << 31))
     return fail(PKV_ERR_UNSUPPORTED, "pool too large for 32-bit row coordinates");
   if (c->free_order) {
@@ -550,11 +548,17 @@ pkv_status make_tensor_map(CUtensorMap* m, void* base, const pkv_pool_config& c)
   }
   const bool fp8 = elem_bytes(c.kv_dtype) == 1;  // FP8 or INT8 codes
   const int es = fp8 ? 1 : 2;
-  // 2-D view: rows = (block, kv head, slot), columns = head_dim elements.
-  cuuint64_t dims[2] = {(cuuint64_t)c.head_dim, (cuuint64_t)c.num_blocks * c.n_kv_heads * kBlock};
-  cuuint64_t strides[1] = {(cuuint64_t)c.head_dim * es};
-  // one box = 16 rows x 128 bytes (64 bf16 or 128 one-byte codes), 128-byte swizzle
-  cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)kBlock};
+  const uint64_t rows = (uint64_t)c.num_blocks * c.n_kv_heads * kBlock;
+  const int row_bytes = c.head_dim * es;
+  // 2-D view with 128-byte box rows and the 128-byte swizzle.  Rows of at
+  // least 128 bytes: rows = (block, kv head, slot), columns = head_dim
+  // elements, one box = 16 rows x 128 bytes (64 bf16 or 128 one-byte codes).
+  // 64-byte rows (one-byte codes, head_dim 64): two slots per 128-byte row,
+  // one box = the 8 rows of a (block, kv head) chunk.
+  const bool pair_rows = row_bytes < 128;
+  cuuint64_t dims[2] = {(cuuint64_t)(pair_rows ? 128 : c.head_dim), (cuuint64_t)(pair_rows ? rows / 2 : rows)};
+  cuuint64_t strides[1] = {(cuuint64_t)(pair_rows ? 128 : row_bytes)};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)(pair_rows ? kBlock / 2 : kBlock)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -806,7 +810,7 @@ struct PrefixGroup {
 
 std::vector<PrefixGroup> find_prefix_groups(const pkv_pool* p, int32_t n, const int32_t* ids) {
   std::vector<PrefixGroup> groups;
-  if (p->cfg.kv_dtype != PKV_KV_BF16) return groups;
+  if (p->cfg.kv_dtype != PKV_KV_BF16 || p->cfg.head_dim != 128) return groups;  // the multi-query kernel's shapes
   const auto& A = p->alloc;
   auto full = [&](int32_t b) { return A.len[ids[b]] / kBlock; };
   auto row = [&](int32_t b) { return A.table[ids[b]].data(); };
@@ -1619,7 +1623,7 @@ pkv_status launch_tc_plan(pkv_pool* p, cudaStream_t st, const Plan& pl, const Pl
     if (pkv_status r = launch(p, PKV_KERNEL_PREFIX, st, [&] { return launch_prefix_decode(p->G, prm, st); })) return r;
   if (pl.total_warps == 0) return PKV_OK;
   return launch(p, PKV_KERNEL_DECODE, st,
-                [&] { return launch_decode_tc(c.kv_dtype, p->G, pl.nq, prm, pl.ctas, st); });
+                [&] { return launch_decode_tc(c.kv_dtype, p->G, pl.nq, c.head_dim, prm, pl.ctas, st); });
 }
 
 }  // namespace
@@ -1898,18 +1902,19 @@ pkv_status pkv_pool_create(const pkv_pool_config* cfg, const pkv_pool_buffers* b
         p->tc_path = true;
         if (pkv_status r = make_tensor_map(&p->tmap_k, b.k_pool, p->cfg)) return fail_dev(r);
         if (pkv_status r = make_tensor_map(&p->tmap_v, b.v_pool, p->cfg)) return fail_dev(r);
-        e = decode_tc_prepare(cfg->kv_dtype, p->G, 1);
-        if (e == cudaSuccess) e = decode_tc_prepare(cfg->kv_dtype, p->G, 2);
-        if (e == cudaSuccess && cfg->kv_dtype == PKV_KV_BF16) e = prefix_decode_prepare(p->G);
+        const int D = cfg->head_dim;
+        e = decode_tc_prepare(cfg->kv_dtype, p->G, 1, D);
+        if (e == cudaSuccess) e = decode_tc_prepare(cfg->kv_dtype, p->G, 2, D);
+        if (e == cudaSuccess && cfg->kv_dtype == PKV_KV_BF16 && D == 128) e = prefix_decode_prepare(p->G);
         int occ = 0, occ2 = 0;
-        if (e == cudaSuccess) e = decode_tc_occupancy(cfg->kv_dtype, p->G, 1, &occ);
-        if (e == cudaSuccess) e = decode_tc_occupancy(cfg->kv_dtype, p->G, 2, &occ2);
+        if (e == cudaSuccess) e = decode_tc_occupancy(cfg->kv_dtype, p->G, 1, D, &occ);
+        if (e == cudaSuccess) e = decode_tc_occupancy(cfg->kv_dtype, p->G, 2, D, &occ2);
         if (e != cudaSuccess) return fail_dev(fail(PKV_ERR_CUDA, "decode kernel setup failed: %s", cudaGetErrorString(e)));
         p->tc_ctas_per_sm = std::max(1, occ);
-        p->tc_warps_per_cta = decode_tc_warps_per_cta(cfg->kv_dtype, 1);
+        p->tc_warps_per_cta = tc_warps(cfg->kv_dtype, 1, D);
         p->tc2_ctas_per_sm = std::max(1, occ2);
-        p->tc2_warps_per_cta = decode_tc_warps_per_cta(cfg->kv_dtype, 2);
-        p->tc_smem = decode_tc_smem_bytes(cfg->kv_dtype, 1);
+        p->tc2_warps_per_cta = tc_warps(cfg->kv_dtype, 2, D);
+        p->tc_smem = tc_smem_bytes(cfg->kv_dtype, 1, D);
       }
     }
     *out = p;
@@ -2508,18 +2513,18 @@ pkv_status pkv_h2o_scores(pkv_pool* p, void* stream, int32_t n, const int32_t* i
 
 namespace {
 
-pkv_status select_keep(pkv_pool* p, void* stream, int32_t n, const int32_t* lens, const float* acc,
+pkv_status select_keep(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, const float* acc,
                        int64_t acc_stride, const SelPolicy& pol, int64_t max_keep, int32_t* keep_idx,
                        int64_t keep_stride, int32_t* keep_count) {
   if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
   if (!p->device) return fail(PKV_ERR_NO_DEVICE, "host-only pool");
-  if (n < 0 || (n > 0 && !lens)) return fail(PKV_ERR_INVALID_ARG, "bad lens");
+  if (pkv_status r = check_seq_list(p, n, ids)) return r;
   if (n > 0 && (!acc || !keep_idx || !keep_count)) return fail(PKV_ERR_INVALID_ARG, "NULL device array");
+  const auto& A = p->alloc;
   int32_t max_len = 0;
-  for (int32_t i = 0; i < n; ++i) {
-    if (lens[i] < 0 || lens[i] > acc_stride) return fail(PKV_ERR_INVALID_ARG, "length %d outside [0, acc_stride]", lens[i]);
-    max_len = std::max(max_len, lens[i]);
-  }
+  for (int32_t i = 0; i < n; ++i) max_len = std::max(max_len, A.len[ids[i]]);
+  if (max_len > acc_stride) return fail(PKV_ERR_INVALID_ARG, "acc_stride %lld below the longest sequence (%d)",
+                                        (long long)acc_stride, max_len);
   if (keep_stride < std::min<int64_t>(max_keep, max_len))
     return fail(PKV_ERR_INVALID_ARG, "keep_stride %lld below the largest keep-set", (long long)keep_stride);
   cudaStream_t st = (cudaStream_t)stream;
@@ -2528,7 +2533,7 @@ pkv_status select_keep(pkv_pool* p, void* stream, int32_t n, const int32_t* lens
   StagingSlot* s;
   if (pkv_status r = p->staging.acquire(n * sizeof(SeqRow), &s)) return r;
   SeqRow* rows = (SeqRow*)s->host;
-  for (int32_t i = 0; i < n; ++i) rows[i] = {-1, i, lens[i], 0};
+  for (int32_t i = 0; i < n; ++i) rows[i] = {ids[i], i, A.len[ids[i]], 0};
   if (pkv_status r = p->staging.upload_overlapped(s, n * sizeof(SeqRow), st)) return r;
   const bool starve = p->starve_select;
   p->starve_select = false;
@@ -2542,24 +2547,24 @@ pkv_status select_keep(pkv_pool* p, void* stream, int32_t n, const int32_t* lens
 
 }  // namespace
 
-pkv_status pkv_h2o_select(pkv_pool* p, void* stream, int32_t n, const int32_t* lens, const float* acc,
+pkv_status pkv_h2o_select(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, const float* acc,
                           int64_t acc_stride, int32_t budget, int32_t recent, int32_t* keep_idx, int64_t keep_stride,
                           int32_t* keep_count) {
   return guarded([&]() -> pkv_status {
     if (recent < 0 || budget < recent || budget < 1) return fail(PKV_ERR_INVALID_ARG, "need 0 <= recent <= budget, budget >= 1");
     if (keep_stride < budget) return fail(PKV_ERR_INVALID_ARG, "keep_stride < budget");
-    return select_keep(p, stream, n, lens, acc, acc_stride, SelPolicy{0, recent, budget - recent, 0}, budget, keep_idx,
+    return select_keep(p, stream, n, ids, acc, acc_stride, SelPolicy{0, recent, budget - recent, 0}, budget, keep_idx,
                        keep_stride, keep_count);
   });
 }
 
-pkv_status pkv_policy_select(pkv_pool* p, void* stream, int32_t n, const int32_t* lens, const float* acc,
+pkv_status pkv_policy_select(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, const float* acc,
                              int64_t acc_stride, int32_t sink_size, int32_t window_size, int32_t h2o_size,
                              int32_t* keep_idx, int64_t keep_stride, int32_t* keep_count) {
   return guarded([&]() -> pkv_status {
     if (sink_size < 0 || window_size < 0 || h2o_size < 0)
       return fail(PKV_ERR_INVALID_ARG, "sink_size, window_size and h2o_size must be >= 0");
-    return select_keep(p, stream, n, lens, acc, acc_stride, SelPolicy{sink_size, window_size, h2o_size, 1},
+    return select_keep(p, stream, n, ids, acc, acc_stride, SelPolicy{sink_size, window_size, h2o_size, 1},
                        (int64_t)sink_size + window_size + h2o_size, keep_idx, keep_stride, keep_count);
   });
 }
@@ -2575,6 +2580,11 @@ pkv_status pkv_sync_status(pkv_pool* p, void* stream) {
     if (w[0]) {
       PKV_CUDA(cudaMemset(p->buf.status, 0, sizeof w));
       PKV_CUDA(cudaDeviceSynchronize());
+      if (w[0] & kStatusUndrained)
+        return fail(PKV_ERR_UNDRAINED,
+                    "a device wait timed out (info %d) and copies it had issued were still in flight when the "
+                    "kernel gave up on them; later results on this CUDA context are not reliable",
+                    w[1]);
       if (w[0] & kStatusTimeout) return fail(PKV_ERR_TIMEOUT, "a device wait timed out (info %d)", w[1]);
       return fail(PKV_ERR_DEVICE_ASSERT, "device range check failed (info %d, %d)", w[1], w[2]);
     }

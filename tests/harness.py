@@ -14,6 +14,11 @@ from paged_kv_cache_282_gb300 import PagedKVCache
 KV_CODE = {"fp32": oracle.KV_FP32, "bf16": oracle.KV_BF16, "fp8": oracle.KV_FP8, "int8": oracle.KV_INT8}
 MASK_CODE = {"full": oracle.MASK_FULL, "sliding": oracle.MASK_SLIDING, "sink_window": oracle.MASK_SINK_WINDOW}
 TOL = {"fp32": 1e-4, "bf16": 1e-2, "fp8": 2e-2, "int8": 2e-2}  # max abs error on N(0,1) inputs
+# Accumulated H2O scores against the oracle's fp64 ones: relative error.  Each
+# term exp(s - lse) is evaluated in fp32 from fp32 logits and lse, whose
+# absolute errors (a few ulp of |s| and |lse|, below 1e-6 for the unit-scale
+# logits of these inputs) become the term's relative error.
+H2O_RTOL = 1e-5
 
 
 class Twin:
@@ -125,6 +130,69 @@ def fill_sequences(tw: Twin, lens, data_keys=None, chunk: int = 8192):
             k, v = workloads.kv_rows(tw.wl, key, t0, n)
             tw.append([s], k[None], v[None])
     return ids
+
+
+def length_only_pool(lens, device="cuda"):
+    """A device pool whose sequences have the given lengths, placed by the
+    allocator alone (no K/V written): for the calls that read only lengths,
+    such as the keep-set selections.  Returns (cache, seq_ids)."""
+    nb = sum((L + 15) // 16 for L in lens) + 1
+    maxb = max([(L + 15) // 16 for L in lens] + [1])
+    cache = PagedKVCache(nb, 1, 1, 64, len(lens), maxb, kv_dtype="bf16", device=torch.device(device))
+    ids = []
+    for L in lens:
+        s = cache.seq_add()
+        ids.append(s)
+        if L:
+            cache.reserve_slots([s], L)
+    return cache, ids
+
+
+def dequantised(tw: "Twin", which: str) -> np.ndarray:
+    """The oracle pool's K or V as float64 [NB][Hk][16][D] (codes times
+    scales for FP8 / INT8; unwritten slots may hold anything)."""
+    x = tw.pool.k if which == "k" else tw.pool.v
+    sc = tw.pool.k_scale if which == "k" else tw.pool.v_scale
+    if tw.wl.kv_dtype == "fp8":
+        table = np.array([oracle.e4m3_decode(c) for c in range(256)], dtype=np.float64)
+        return table[x] * sc[..., None]
+    if tw.wl.kv_dtype == "int8":
+        return x.astype(np.float64) * sc[..., None]
+    if tw.wl.kv_dtype == "bf16":
+        return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).double().numpy()
+    return x.astype(np.float64)
+
+
+def output_bounds(tw: "Twin", ids, q: torch.Tensor, logits: np.ndarray, lse: np.ndarray, rel: float) -> np.ndarray:
+    """Error bound of every output row [n][H] against the fp64 oracle:
+    sum_j p_j max_d |V_j| (rel + 2 e_j) over the kept keys j, with p the
+    oracle's softmax weights exp(logit - lse).  rel covers the roundings of
+    the weights and of the output; e_j = 2^-18 (1 + scale sum_d |q_d K_jd|)
+    covers the fp32 evaluation of logit j, whose absolute error grows with
+    the logit's magnitude (a change e in a logit moves its weight by a
+    factor up to e^e, and the normalisation by as much again)."""
+    G, scale = tw.wl.group, tw.wl.scale
+    K = dequantised(tw, "k")
+    vmax = np.nan_to_num(np.abs(dequantised(tw, "v")).max(axis=-1), nan=0.0, posinf=0.0)
+    qa = np.abs(q.double().numpy())
+    out = np.zeros(lse.shape)
+    for b, s in enumerate(ids):
+        L = tw.alloc.length(s)
+        if L == 0:
+            continue
+        pos = np.arange(L)
+        blk = tw.alloc.table(s)[pos // 16]
+        for h in range(lse.shape[1]):
+            lg = logits[b, h, :L]
+            kept = ~np.isnan(lg)
+            if not kept.any():
+                continue
+            g = h // G
+            k_abs = np.abs(K[blk[kept], g, pos[kept] % 16])  # [kept][D]
+            e = 2.0 ** -18 * (1.0 + scale * (k_abs @ qa[b, h]))
+            p = np.exp(lg[kept] - lse[b, h])
+            out[b, h] = float((p * vmax[blk[kept], g, pos[kept] % 16] * (rel + 2.0 * e)).sum())
+    return out
 
 
 def max_err(a: torch.Tensor, b: np.ndarray) -> float:

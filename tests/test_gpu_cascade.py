@@ -13,13 +13,13 @@ from harness import TOL, Twin, lse_err, max_err
 pytestmark = pytest.mark.gpu
 
 
-def _shared_batch(kv: str, n_heads: int, seed: int):
+def _shared_batch(kv: str, n_heads: int, seed: int, head_dim: int = 128):
     """Three prefix groups (100, 37 and 512 tokens) forked into children
     with private suffixes; some children forked again with no new token
     (tables identical up to the partial last block); one unrelated sequence,
     one of 5 tokens and one empty.  Then one token is appended to every
     non-empty sequence, which copies each shared partial last block."""
-    wl = workloads.small(kv, lens=(1,), n_heads=n_heads, seed=seed)
+    wl = workloads.small(kv, lens=(1,), n_heads=n_heads, head_dim=head_dim, seed=seed)
     tw = Twin(wl, 900, 40, 80, seed=seed)
     rng = np.random.default_rng(seed)
     key = 0
@@ -74,11 +74,13 @@ def _decode_both(tw, wl, ids, cascade, static: bool = False, logits: bool = Fals
     return out
 
 
+@pytest.mark.parametrize("D", [128, 64])
 @pytest.mark.parametrize("kv", ["bf16", "fp8", "int8"])
 @pytest.mark.parametrize("n_heads", [64, 32, 16, 8])
-def test_cascade_matches_oracle(kv, n_heads):
-    """Mode 2: group prefixes (BF16) and pairs; mode 1: pairs only; 0: off."""
-    wl, tw, ids = _shared_batch(kv, n_heads, seed=90 + n_heads)
+def test_cascade_matches_oracle(kv, n_heads, D):
+    """Mode 2: group prefixes (BF16, head_dim 128) and pairs; mode 1: pairs
+    only; 0: off."""
+    wl, tw, ids = _shared_batch(kv, n_heads, seed=90 + n_heads, head_dim=D)
     groups = _decode_both(tw, wl, ids, cascade=2)
     pairs = _decode_both(tw, wl, ids, cascade=1)
     off = _decode_both(tw, wl, ids, cascade=0)

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import workloads
-from harness import TOL, Twin, fill_sequences, lse_err
+from harness import TOL, Twin, fill_sequences, lse_err, max_err
 from paged_kv_cache_282_gb300 import _abi
 
 pytestmark = pytest.mark.gpu
@@ -29,26 +29,44 @@ def _call_static(cache, ids, q, out, lse, num_splits, mask=0, S=0, W=0):
     _abi.check(st)
 
 
-@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8", "int8"])
 def test_static_scratch_matches_workspace_decode(kv):
-    lens = (1, 16, 17, 300, 1000, 2049, 4000)
+    lens = (1, 16, 20, 300, 1000, 2049, 4000)
     wl = workloads.small(kv, lens=lens, seed=90)
-    tw = Twin(wl, sum((L + 15) // 16 for L in lens) + 4, len(lens), 300, seed=6)
+    tw = Twin(wl, sum((L + 15) // 16 for L in lens) + 8, len(lens) + 4, 300, seed=6)
     ids = fill_sequences(tw, lens)
     cache = tw.cache
     # two calls in a row, with different queries, split counts and keep-sets
     for call, (splits, mask, S, W) in enumerate([(0, 0, 0, 0), (5, 2, 4, 700)]):
-        q = workloads.queries(wl, step=call).cuda()
-        ref_out, ref_lse = cache.decode(ids, q, mask=["full", "sliding", "sink_window"][mask], num_sinks=S,
-                                        window=W, num_splits=splits)
-        out = torch.full_like(q, float("nan"))
-        lse = torch.full((len(ids), wl.n_heads), float("nan"), device="cuda")
-        _call_static(cache, ids, q, out, lse, splits, mask, S, W)
+        # allocator work that waits in the queue for the next device call,
+        # which is the static one: a fork of a sequence whose last block is
+        # partial, a one-token reservation that copies the now shared block
+        # (copy-on-write), and a truncation back to the old length
+        parent = ids[2 + call]
+        n0 = tw.alloc.length(parent)
+        fork = tw.fork(parent)
+        _, cow = cache.reserve_slots([parent], 1)
+        _, ocow = tw.alloc.append([parent], 1)
+        assert len(cow) == 1 and np.array_equal(cow, ocow)
+        tw.pool.copy_block(int(ocow[0, 0]), int(ocow[0, 1]))
+        tw.truncate(parent, n0)
+        batch = ids + [fork]
+        mname = ["full", "sliding", "sink_window"][mask]
+        q = workloads.queries(wl, n=len(batch), step=call)
+        qd = q.cuda()
+        out = torch.full_like(qd, float("nan"))
+        lse = torch.full((len(batch), wl.n_heads), float("nan"), device="cuda")
+        _call_static(cache, batch, qd, out, lse, splits, mask, S, W)
         cache.sync_status()
         assert torch.isfinite(out.float()).all()
+        ref_out, ref_lse = cache.decode(batch, qd, mask=mname, num_sinks=S, window=W, num_splits=splits)
         err = (out.float() - ref_out.float()).abs().max().item()
         assert err <= TOL[kv], (call, err)
         assert lse_err(lse, ref_lse.cpu().numpy().astype(np.float64)) <= 2e-3
+        # and against the oracle, which replayed the same allocator steps
+        ref, o_lse, _ = tw.oracle_decode(batch, q, mname, S, W)
+        assert max_err(out, ref) <= TOL[kv], call
+        assert lse_err(lse, o_lse) <= 2e-3
 
 
 def test_static_scratch_rejects_oversized_request():

@@ -7,8 +7,9 @@ Both the CPU oracle and the CUDA library consume exactly these bytes.
 Shapes follow the model shapes the pages quote: Llama-3-8B (32 query heads,
 8 KV heads, head_dim 128) and Llama-2-70B (64 query heads, 8 KV heads,
 head_dim 128).  No public dataset is involved: every value is N(0, 1) drawn
-from a seeded CPU generator, and lengths are uniform integers from a seeded
-``random.Random``.
+from a seeded CPU generator (optionally with each row's magnitude spread over
+several decades, for range tests), and lengths are uniform integers from a
+seeded ``random.Random``.
 
 K/V rows are drawn per (sequence, 256-token chunk) from their own seed, so
 any position range of any sequence can be produced on its own and the oracle
@@ -129,8 +130,21 @@ def _chunk_seed(wl_seed: int, stream: int, seq: int, chunk: int) -> int:
     return (((wl_seed * 1_000_003 + stream) * 1_000_033 + seq) * 1_048_583 + chunk)
 
 
-def _normal(shape, seed: int, dtype: torch.dtype) -> torch.Tensor:
-    return torch.randn(shape, generator=_gen(seed), dtype=torch.float32).to(dtype)
+def _normal(shape, seed: int, dtype: torch.dtype, spread: float = 0.0) -> torch.Tensor:
+    """N(0, 1) values; with spread > 0 every row along the last axis is
+    multiplied by its own factor 10^U(-spread, spread) (drawn after the values
+    from the same generator), before the conversion to ``dtype``."""
+    g = _gen(seed)
+    x = torch.randn(shape, generator=g, dtype=torch.float32)
+    if spread > 0:
+        u = torch.rand(tuple(shape[:-1]) + (1,), generator=g, dtype=torch.float64)
+        x = x * (10.0 ** ((2.0 * u - 1.0) * spread)).to(torch.float32)
+    return x.to(dtype)
+
+
+def _spread(wl: Workload) -> float:
+    """Decades of magnitude spread of the workload's rows (0: plain N(0, 1))."""
+    return float(wl.extra.get("spread", 0.0))
 
 
 def kv_rows(wl: Workload, seq_key: int, start: int, count: int, stream: int = 0):
@@ -146,7 +160,7 @@ def kv_rows(wl: Workload, seq_key: int, start: int, count: int, stream: int = 0)
             lo = c * CHUNK
             hi = min(end, lo + CHUNK)
             full = _normal((CHUNK, wl.n_kv_heads, wl.head_dim),
-                           _chunk_seed(wl.seed, 2 * stream + which, seq_key, c), wl.input_dtype)
+                           _chunk_seed(wl.seed, 2 * stream + which, seq_key, c), wl.input_dtype, _spread(wl))
             parts.append(full[pos - lo: hi - lo])
             pos = hi
         if parts:
@@ -160,15 +174,15 @@ def queries(wl: Workload, n: int | None = None, step: int = 0) -> torch.Tensor:
     """Decode queries [n][H][D] of the input dtype (bf16 for bf16/FP8 KV)."""
     n = wl.batch if n is None else n
     return _normal((n, wl.n_heads, wl.head_dim), _chunk_seed(wl.seed, 100 + step, 0, 0),
-                   wl.input_dtype).contiguous()
+                   wl.input_dtype, _spread(wl)).contiguous()
 
 
 def new_tokens(wl: Workload, n: int, step: int):
     """One new K/V row per sequence for an append step: [n][1][Hk][D] each."""
     k = _normal((n, 1, wl.n_kv_heads, wl.head_dim), _chunk_seed(wl.seed, 200 + 2 * step, 0, 0),
-                wl.input_dtype)
+                wl.input_dtype, _spread(wl))
     v = _normal((n, 1, wl.n_kv_heads, wl.head_dim), _chunk_seed(wl.seed, 201 + 2 * step, 0, 0),
-                wl.input_dtype)
+                wl.input_dtype, _spread(wl))
     return k.contiguous(), v.contiguous()
 
 
