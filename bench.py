@@ -257,10 +257,25 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
+    @staticmethod
+    def _stats(rows):
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[4:8]) if v.lower().startswith("active")})
+        return sm, mx, reasons
+
     def summary(self, t0, t1):
-        rows = [r for (t, r) in self.samples if t0 <= t <= t1] or [r for (_, r) in self.samples[-3:]]
+        """Clocks of the samples taken inside [t0, t1].  A region shorter than
+        the sampling period may hold none: it is then reported as unsampled,
+        with the samples just before and after it listed apart."""
+        rows = [r for (t, r) in self.samples if t0 <= t <= t1]
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+            before = [r for (t, r) in self.samples if t < t0][-1:]
+            after = [r for (t, r) in self.samples if t > t1][:1]
+            sm, mx, reasons = self._stats(before + after)
+            return {"sm_mhz": None, "sm_max_mhz": max(mx) if mx else None, "reasons": ["unsampled"], "samples": 0,
+                    "adjacent": {"sm_mhz": sm, "reasons": reasons}}
         sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
         mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -283,26 +298,28 @@ def hbm_peak():
 
 
 KERNEL_HEADERS = ("async_copy.cuh", "pkv_internal.h")
+DECODE_SOURCES = ("decode_tc.cuh",)
 
 
-def kernel_source_sha(kernel_file: str) -> str:
-    """sha256 of a kernel file followed by the library headers it includes."""
+def kernel_source_sha(kernel_files=DECODE_SOURCES) -> str:
+    """sha256 of the kernel's source files followed by the library headers
+    they include."""
     csrc = os.path.join(ROOT, "paged_kv_cache_282_gb300", "csrc")
     h = hashlib.sha256()
-    for name in (kernel_file,) + KERNEL_HEADERS:
+    for name in tuple(kernel_files) + KERNEL_HEADERS:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def profiled_traffic(kernel_file: str, workload: str):
-    """DRAM bytes per launch recorded from an ncu capture in profiles/, valid
-    only while the kernel source is unchanged (its sha256, with the headers
-    it includes, recorded beside it)."""
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the decode kernel recorded from an ncu capture
+    in profiles/, valid only while the kernel source is unchanged (its sha256,
+    with the headers it includes, recorded beside it)."""
     path = os.path.join(ROOT, "profiles", f"decode_tc_{workload}.md")
     try:
         text = open(path).read()
-        sha = kernel_source_sha(kernel_file)
+        sha = kernel_source_sha()
         m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
         m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
         if m_sha and m_tr and m_sha.group(1) == sha:
@@ -381,59 +398,11 @@ def oracle_baseline(wl, n_sample: int, repeats: int = 1):
 # main
 # --------------------------------------------------------------------------
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
-    ap.add_argument("--workload", default="llama3_8b_b64", choices=sorted(workloads.ALL))
-    ap.add_argument("--num-splits", type=int, default=None)
-    ap.add_argument("--cpu-sample", type=int, default=16, help="sequences in the oracle baseline sample")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--profile-steps", type=int, default=0, help="run N untimed steps and exit (for ncu)")
-    ap.add_argument("--kv-dtype", default=None, choices=["bf16", "fp8", "int8"],
-                    help="run the workload with another KV storage type")
-    ap.add_argument("--no-cascade", action="store_true",
-                    help="every sequence reads its own blocks (no shared-prefix decode)")
-    ap.add_argument("--cascade", type=int, default=1, choices=[0, 1, 2],
-                    help="shared-prefix decode: 0 off, 1 sequence pairs, 2 group prefixes (multi-query kernel)")
-    ap.add_argument("--time-kernels", action="store_true",
-                    help="bracket every kernel (not only decode) with events; adds gaps to the step")
-    ap.add_argument("--op", default="step", choices=["step", "compact", "swap"],
-                    help="step: the decode step (default); compact: H2O compaction of the streaming workload's "
-                         "sequences to their keep-sets; swap: every sequence to pinned host memory and back")
-    args = ap.parse_args()
-
-    wl = workloads.ALL[args.workload]()
-    label = wl.name
-    if args.kv_dtype and args.kv_dtype != wl.kv_dtype:
-        import dataclasses
-        wl = dataclasses.replace(wl, kv_dtype=args.kv_dtype)
-        label = f"{wl.name}_{args.kv_dtype}"
-    splits = wl.num_splits if args.num_splits is None else args.num_splits
-    ws, rank, local = dist_info()
-
-    if args.impl == "reference":
-        if rank != 0:
-            return
-        return run_reference(args, wl, label)
-
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    import paged_kv_cache_282_gb300 as pkv
-    pkv.load()
-    if args.op != "step":
-        if ws > 1:
-            raise SystemExit("--op compact / swap run on one GPU")
-        return run_op(args, wl, label, dev)
-
+def measure(args, wl, label, splits, dev, ws, rank, cascade, headline=True):
+    """Times one workload's decode step (the timed region, per-step spread,
+    a sustained leg, end to end through host buffers) and returns its JSON
+    fields (rank 0; None elsewhere or in profile mode)."""
     setup = Setup(wl, dev)
-    cascade = 0 if args.no_cascade else args.cascade
     setup.cache.set_cascade(cascade)
     st = Stepper(setup, splits)
     stream = torch.cuda.current_stream(dev)
@@ -448,7 +417,7 @@ def main():
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize(dev)
         print(json.dumps({"profile_steps": args.profile_steps, "workload": wl.name}))
-        return
+        return None
 
     clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     time.sleep(0.3)
@@ -473,6 +442,33 @@ def main():
     setup.cache.timing_enable(False)
     setup.cache.sync_status()
     ms_max = reduce_max(ms, ws, dev)
+
+    # ---- sustained leg: the same step repeated for at least a second, in
+    # chunks of steps bracketed by events (per-step median from the chunks),
+    # with its own clock record
+    sus = None
+    if not args.no_sustained:
+        per = max(ms / max(args.steps, 1), 1e-3)
+        chunk = max(1, int(math.ceil(2.0 / per)))  # about 2 ms per chunk
+        n_chunks = max(20, int(math.ceil(args.sustain_s * 1e3 / (per * chunk))))
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_chunks + 1)]
+        barrier(ws)
+        torch.cuda.synchronize(dev)
+        s_wall0 = time.time()
+        evs[0].record(stream)
+        for i in range(n_chunks):
+            for _ in range(chunk):
+                st.step()
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        s_wall1 = time.time()
+        barrier(ws)
+        per_chunk = [evs[i].elapsed_time(evs[i + 1]) / chunk for i in range(n_chunks)]
+        sus_ms = reduce_max(evs[0].elapsed_time(evs[-1]), ws, dev) / (n_chunks * chunk)
+        sus = {"steps": n_chunks * chunk, "seconds": round(evs[0].elapsed_time(evs[-1]) * 1e-3, 3),
+               "ms_per_step": round(sus_ms, 5), "ms_per_step_p50": round(statistics.median(per_chunk), 5),
+               "sus_wall": (s_wall0, s_wall1)}
+        setup.cache.sync_status()
 
     # ---- per-step spread (separate from the timed region): events around
     # each of up to 50 steps, for the median and the 10th / 90th percentiles
@@ -577,14 +573,14 @@ def main():
     if clocks:
         clocks.stop()
     if rank != 0:
-        return
+        return None
 
+    peak, peak_kind = hbm_peak()
     lens_step = [L + 1 for L in setup.lens]
     logical = setup.algorithmic_bytes(lens_step)
     step_bytes = setup.kv_bytes_read_per_step()
     ms_step = ms_max / args.steps
     value = whole_job_rate(ws, step_bytes, ms_step)
-    peak, peak_kind = hbm_peak()
     # decode time per step: the main decode kernel plus, with shared-prefix
     # groups, the multi-query kernel that runs before it
     dec_ms, dec_n = ktimes["decode"]
@@ -592,12 +588,17 @@ def main():
     dec_avg = dec_ms / max(dec_n, 1)
     achieved = step_bytes / (dec_avg * 1e-3) / 1e9 if dec_n else None
     # the captures in profiles/ ran with the default shared-prefix mode (1)
-    traffic = profiled_traffic("decode_tc.cu", label) if cascade == 1 else None
+    traffic = profiled_traffic(label) if cascade == 1 else None
     decode_share = round(dec_ms / max(ms, 1e-9), 4)
     cpu = None
-    if not args.no_cpu_baseline and ws == 1:
+    if headline and not args.no_cpu_baseline and ws == 1:
         cpu = oracle_baseline(wl, min(args.cpu_sample, wl.batch))
     clk = clocks.summary(t_wall0, t_wall1) if clocks else None
+    if sus is not None:
+        w0, w1 = sus.pop("sus_wall")
+        sus["value"] = round(whole_job_rate(ws, step_bytes, sus["ms_per_step"]), 2)
+        sus["frac_of_hbm_peak"] = round(sus["value"] / ws / peak, 4)
+        sus["clocks"] = clocks.summary(w0, w1) if clocks else None
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -634,8 +635,96 @@ def main():
         "e2e": e2e,
         "cpu_baseline": cpu,
         "clocks": clk,
+        "sustained": sus,
     }
-    print(json.dumps(line))
+    if not headline:
+        keep = ("value", "unit", "ms_per_step", "step_ms_percentiles", "dtype", "config", "tokens_per_s",
+                "frac_of_hbm_peak", "roofline", "gpu_launches", "e2e", "clocks", "sustained")
+        line = {k: line[k] for k in keep}
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--workload", default="llama3_8b_b64", choices=sorted(workloads.ALL))
+    ap.add_argument("--num-splits", type=int, default=None)
+    ap.add_argument("--cpu-sample", type=int, default=16, help="sequences in the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--profile-steps", type=int, default=0, help="run N untimed steps and exit (for ncu)")
+    ap.add_argument("--kv-dtype", default=None, choices=["bf16", "fp8", "int8"],
+                    help="run the workload with another KV storage type")
+    ap.add_argument("--no-cascade", action="store_true",
+                    help="every sequence reads its own blocks (no shared-prefix decode)")
+    ap.add_argument("--cascade", type=int, default=1, choices=[0, 1, 2],
+                    help="shared-prefix decode: 0 off, 1 sequence pairs, 2 group prefixes (multi-query kernel)")
+    ap.add_argument("--time-kernels", action="store_true",
+                    help="bracket every kernel (not only decode) with events; adds gaps to the step")
+    ap.add_argument("--head-dim", type=int, default=None, choices=[64, 128],
+                    help="run the workload with another head_dim")
+    ap.add_argument("--max-len", type=int, default=None,
+                    help="cap every sequence's length (a smaller case of the workload, e.g. for profiling)")
+    ap.add_argument("--no-sustained", action="store_true", help="skip the sustained (>= 1 s) leg")
+    ap.add_argument("--sustain-s", type=float, default=1.0, help="seconds of the sustained leg")
+    ap.add_argument("--no-long-ctx", action="store_true",
+                    help="default workload only: skip the 128K FP8 leg reported inside the same line")
+    ap.add_argument("--op", default="step", choices=["step", "compact", "swap"],
+                    help="step: the decode step (default); compact: H2O compaction of the streaming workload's "
+                         "sequences to their keep-sets; swap: every sequence to pinned host memory and back")
+    args = ap.parse_args()
+
+    wl = workloads.ALL[args.workload]()
+    label = wl.name
+    if args.kv_dtype and args.kv_dtype != wl.kv_dtype:
+        import dataclasses
+        wl = dataclasses.replace(wl, kv_dtype=args.kv_dtype)
+        label = f"{wl.name}_{args.kv_dtype}"
+    if args.head_dim and args.head_dim != wl.head_dim:
+        import dataclasses
+        wl = dataclasses.replace(wl, head_dim=args.head_dim)
+        label = f"{label}_d{args.head_dim}"
+    if args.max_len:
+        import dataclasses
+        wl = dataclasses.replace(wl, lens=tuple(min(L, args.max_len) for L in wl.lens))
+        label = f"{label}_max{args.max_len}"
+    splits = wl.num_splits if args.num_splits is None else args.num_splits
+    ws, rank, local = dist_info()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        return run_reference(args, wl, label)
+
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import paged_kv_cache_282_gb300 as pkv
+    pkv.load()
+    if args.op != "step":
+        if ws > 1:
+            raise SystemExit("--op compact / swap run on one GPU")
+        return run_op(args, wl, label, dev)
+
+    cascade = 0 if args.no_cascade else args.cascade
+    line = measure(args, wl, label, splits, dev, ws, rank, cascade, headline=True)
+    if args.profile_steps:
+        return
+    # The second throughput target: the 128K-context FP8 batch (64 splits),
+    # measured in the same process (every rank) and reported inside the same line.
+    if (args.workload == "llama3_8b_b64" and not args.kv_dtype and not args.no_long_ctx and
+            args.num_splits is None and not args.head_dim and not args.max_len):
+        wl2 = workloads.long_context_fp8()
+        leg = measure(args, wl2, wl2.name, wl2.num_splits, dev, ws, rank, cascade, headline=False)
+        if line is not None and leg is not None:
+            line["long_ctx_fp8"] = leg
+    if rank == 0 and line is not None:
+        print(json.dumps(line))
 
 
 def run_op(args, wl, label, dev):

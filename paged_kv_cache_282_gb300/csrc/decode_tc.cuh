@@ -59,19 +59,24 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint64_t kDrainTimeoutNs = 50000000ull;
 
-template <int KV, int NQ, int D>
+// Geometry of a unit: one 16-token block of HG adjacent kv heads.
+template <int KV, int NQ, int D, int HG>
 struct TC {
   static constexpr int kEs = KV == 1 ? 2 : 1;          // bytes per element
   static constexpr int kRowBytes = D * kEs;            // one token of one kv head
-  static constexpr int kChunkBytes = 16 * kRowBytes;   // K (or V) of one unit
+  static constexpr int kHeadChunk = 16 * kRowBytes;    // K (or V) of one kv head of a block
+  static constexpr int kChunkBytes = HG * kHeadChunk;  // K (or V) of one unit, contiguous in HBM
   static constexpr int kStageBytes = 2 * kChunkBytes;  // K then V
-  static constexpr int kScaleBytes = KV == 1 ? 0 : 128;  // 16 K scales + 16 V scales
+  static constexpr int kScaleBytes = KV == 1 ? 0 : HG * 128;  // 16 K scales per head, then the V scales
   static constexpr uint32_t kTxBytes = kStageBytes + kScaleBytes;
-  static constexpr int kWarps = tc_warps(KV, NQ, D);
-  static constexpr int kStages = tc_stages(KV, NQ, D);
-  // TMA boxes per chunk: 16 rows x 128 bytes each, except one-byte codes with
-  // D = 64, whose chunk is viewed as 8 rows of 128 bytes (two tokens a row)
+  static constexpr int kWarps = tc_warps(KV, NQ, D, HG);
+  static constexpr int kTeams = kWarps / HG;  // each team shares one ring of stages
+  static constexpr int kStages = tc_stages(KV, NQ, D, HG);
+  // TMA boxes per chunk, each 128 bytes wide: two for bf16 rows of 256 bytes
+  // (HG = 1), one otherwise; one-byte codes with D = 64 are viewed as rows of
+  // two tokens
   static constexpr int kBoxes = kRowBytes > 128 ? kRowBytes / 128 : 1;
+  static constexpr int kBoxBytes = kChunkBytes / kBoxes;
   static constexpr bool kPairRows = kRowBytes < 128;
 };
 
@@ -236,8 +241,10 @@ __device__ __forceinline__ void advance(const Piece* __restrict__ P, int pe, int
   }
 }
 
-// Row coordinate (block * Hk + kv_head) * 16 of the unit `lane` positions past
-// the cursor, or -1 past the end.
+// Row coordinate (block * Hk + first kv head) * 16 of the unit `lane` positions
+// past the cursor, or -1 past the end (a piece's kv_head names its unit's
+// group of HG kv heads).
+template <int HG>
 __device__ __forceinline__ int unit_row(const DecodeTCParams& p, int pe, int ip, int il, int lane) {
   advance(p.pieces, pe, ip, il, lane);
   if (ip >= pe) return -1;
@@ -249,7 +256,7 @@ __device__ __forceinline__ int unit_row(const DecodeTCParams& p, int pe, int ip,
     p.status[2] = il;
     blk = 0;  // keep the copy in bounds; the status word reports the fault
   }
-  return (blk * p.n_kv_heads + pc.kv_head) * kBlock;
+  return (blk * p.n_kv_heads + pc.kv_head * HG) * kBlock;
 }
 
 // Log-sum-exp merge of the partial records of one (sequence, kv head) by one
@@ -328,17 +335,20 @@ __device__ void merge_partials(const DecodeTCParams& p, const CombineItem it, in
   }
 }
 
-// Reports a wait that ran out, waits (bounded again) for the copies this warp
-// still has in flight into its stages, and flags a drain that ran out too.
+// Reports a wait that ran out (the team's leader also waits, bounded again,
+// for the copies it has in flight into its team's stages, and flags a drain
+// that ran out too).
 template <int S>
-__device__ void fail_and_drain(const DecodeTCParams& p, uint32_t bars, int from, int issued, int gw, int lane) {
+__device__ void fail_and_drain(const DecodeTCParams& p, uint32_t full, int from, int issued, bool leader, int gw,
+                               int lane) {
   if (lane == 0) {
     atomicOr(p.status, kStatusTimeout);
     p.status[1] = gw;
   }
+  if (!leader) return;
   bool drained = true;
   for (int v = from; v < issued; ++v)
-    drained &= mbar_wait(bars + 8 * (v % S), (uint32_t)((v / S) & 1), kDrainTimeoutNs);
+    drained &= mbar_wait(full + 8 * (v % S), (uint32_t)((v / S) & 1), kDrainTimeoutNs);
   if (!drained && lane == 0) atomicOr(p.status, kStatusUndrained);
 }
 
@@ -346,24 +356,51 @@ __device__ void fail_and_drain(const DecodeTCParams& p, uint32_t bars, int from,
 // the kernel
 // ---------------------------------------------------------------------------
 
-template <int KV, int G, int NQ, int D>
-__global__ void __launch_bounds__(TC<KV, NQ, D>::kWarps * 32, 1)
+// GP: query heads per kv head.  HG: kv heads per unit = warps of a team.  A
+// team shares one ring of stages, each holding a unit (one block of HG
+// adjacent kv heads); its warp jh attends with kv head jh of every unit for
+// that head's GP query heads, so a unit's K and V arrive as two contiguous
+// pieces of HG chunks while every warp runs the one-head computation.  The
+// plan names teams ("warps" of the plan) and units of HG heads, whose records
+// hold GV = GP HG query heads.
+template <int KV, int GP, int HG, int NQ, int D>
+__global__ void __launch_bounds__(TC<KV, NQ, D, HG>::kWarps * 32, 1)
     decode_tc_kernel(const __grid_constant__ DecodeTCParams p) {
-  using C = TC<KV, NQ, D>;
+  using C = TC<KV, NQ, D, HG>;
   constexpr int S = C::kStages;
   constexpr int KT = D / 16;  // k16 steps of QK, m16 tiles of PV
+  constexpr int GV = GP * HG;
+  constexpr int T = C::kTeams;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
-  const int gw = blockIdx.x * C::kWarps + wl;
+  const int team = wl / HG, jh = wl % HG;
+  const bool leader = jh == 0;  // issues the team's copies
+  const int gw = blockIdx.x * T + team;
+
+  const uint32_t data = smem_addr(base) + (uint32_t)(team * S * C::kStageBytes);
+  const uint32_t scl = smem_addr(base) + (uint32_t)(T * S * C::kStageBytes + team * S * C::kScaleBytes);
+  const uint32_t full = smem_addr(base) + (uint32_t)(T * S * (C::kStageBytes + C::kScaleBytes) + team * S * 16);
+  const uint32_t empty = full + 8 * S;  // HG arrivals: every warp of the team is done with the stage
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < T * S; ++s) {
+      const uint32_t f = smem_addr(base) + (uint32_t)(T * S * (C::kStageBytes + C::kScaleBytes) + (s / S) * S * 16 +
+                                                     (s % S) * 8);
+      mbar_init(f, 1);
+      mbar_init(f + 8 * S, HG);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
   if (gw >= p.total_warps) return;
-  // (sequence, kv head) pairs with an empty keep-set: zeros and -inf
+  // (sequence, unit head group) pairs with an empty keep-set: zeros and -inf
   for (int e = gw; e < p.n_empty; e += p.total_warps) {
     const EmptyItem it = p.empty[e];
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-    for (int h = 0; h < G; ++h) {
-      const size_t row = ((size_t)it.q_row * p.n_heads + it.kv_head * G + h);
+    for (int h = 0; h < GP; ++h) {
+      const size_t row = ((size_t)it.q_row * p.n_heads + it.kv_head * GV + jh * GP + h);
       if (D == 128)
         *reinterpret_cast<uint2*>(out + row * D + lane * 4) = make_uint2(0u, 0u);
       else
@@ -374,66 +411,71 @@ __global__ void __launch_bounds__(TC<KV, NQ, D>::kWarps * 32, 1)
   const int pb = p.warp_begin[gw], pe = p.warp_begin[gw + 1];
   if (pb >= pe) return;
 
-  const uint32_t data = smem_addr(base) + (uint32_t)(wl * S * C::kStageBytes);
-  const uint32_t scl = smem_addr(base) + (uint32_t)(C::kWarps * S * C::kStageBytes + wl * S * C::kScaleBytes);
-  const uint32_t bars =
-      smem_addr(base) + (uint32_t)(C::kWarps * S * (C::kStageBytes + C::kScaleBytes) + wl * S * 8);
-  if (lane == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(bars + 8 * s, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  }
-  __syncwarp();
-
   const int r = lane >> 2, c = lane & 3;
   const int Hk = p.n_kv_heads, H = p.n_heads;
   const float sl2 = p.scale * kLog2e;
 
-  // total units of this warp
+  // total units of this team
   int n_units = 0;
   for (int k = pb; k < pe; ++k) n_units += p.pieces[k].lblk_end - p.pieces[k].lblk_begin;
 
-  // issue side: rows of the current and the next batch of 32 units
+  // issue side (the leader warp): rows of the current and the next batch of 32 units
   int bip = pb, bil = p.pieces[pb].lblk_begin;  // cursor at the current batch start
-  int cur_rows = unit_row(p, pe, bip, bil, lane);
-  int nip = bip, nil = bil;
-  advance(p.pieces, pe, nip, nil, 32);
-  int next_rows = unit_row(p, pe, nip, nil, lane);
+  int cur_rows = -1, next_rows = -1, nip = bip, nil = bil;
+  if (leader) {
+    cur_rows = unit_row<HG>(p, pe, bip, bil, lane);
+    advance(p.pieces, pe, nip, nil, 32);
+    next_rows = unit_row<HG>(p, pe, nip, nil, lane);
+  }
   int batch_base = 0;
-  int issued = 0;
+  int issued = 0, ist = 0;  // units issued; the stage the next one goes to
+  // parity of that stage's empty barrier to wait for: refill v waits for the
+  // consumption of unit v - S, phase (v / S - 1) of the barrier; the S first
+  // issues wait for nothing and wrap the stage index once, so start at 1
+  uint32_t iph = 1;
 
   // TMA y coordinate of a unit's chunk: token rows, or pairs of tokens
   auto ycoord = [](int row) { return C::kPairRows ? row >> 1 : row; };
-
-  auto issue = [&](int v) {  // all lanes; lane 0 issues the copies of unit v
+  // leader warp, all lanes; lane 0 issues the copies of unit v.  False when
+  // the wait for the team to release the stage ran out.
+  auto issue = [&](int v) -> bool {
     if (v - batch_base >= 32) {
       batch_base += 32;
       cur_rows = next_rows;
       advance(p.pieces, pe, nip, nil, 32);
-      next_rows = unit_row(p, pe, nip, nil, lane);
+      next_rows = unit_row<HG>(p, pe, nip, nil, lane);
     }
     const int row = __shfl_sync(kFull, cur_rows, v - batch_base);
+    const int st = ist;
+    bool ok = true;
+    if (HG > 1 && v >= S) ok = mbar_wait(empty + 8 * st, iph, p.wait_limit_ns);  // lanes agree
+    if (++ist == S) {
+      ist = 0;
+      iph ^= 1u;
+    }
+    if (!ok) return false;
     if (lane == 0) {
-      const int st = v % S;
-      const uint32_t bar = bars + 8 * st;
+      const uint32_t bar = full + 8 * st;
       const uint32_t dst = data + (uint32_t)(st * C::kStageBytes);
       mbar_expect_tx(bar, C::kTxBytes);
-      if (v == 0 && gw == p.starve_warp) return;  // test hook: this stage never completes
+      if (v == 0 && gw == p.starve_warp) return true;  // test hook: this stage never completes
       const int y = ycoord(row);
 #pragma unroll
       for (int b = 0; b < C::kBoxes; ++b) {
-        tma_load_2d(dst + 2048 * b, &p.tmap_k, 64 * b, y, bar);
-        tma_load_2d(dst + C::kChunkBytes + 2048 * b, &p.tmap_v, 64 * b, y, bar);
+        tma_load_2d(dst + C::kBoxBytes * b, &p.tmap_k, 64 * b, y, bar);
+        tma_load_2d(dst + C::kChunkBytes + C::kBoxBytes * b, &p.tmap_v, 64 * b, y, bar);
       }
       if (KV != 1) {
         const uint32_t sd = scl + (uint32_t)(st * C::kScaleBytes);
-        bulk_load(sd, p.k_scale + row, 64, bar);
-        bulk_load(sd + 64, p.v_scale + row, 64, bar);
+        bulk_load(sd, p.k_scale + row, HG * 64, bar);
+        bulk_load(sd + HG * 64, p.v_scale + row, HG * 64, bar);
       }
     }
+    return true;
   };
 
-  for (; issued < n_units && issued < S; ++issued) issue(issued);
+  if (leader)
+    for (; issued < n_units && issued < S; ++issued) issue(issued);
 
   // per-lane fragment address pieces
   const int mi = lane >> 3, rr = lane & 7;
@@ -443,6 +485,8 @@ __global__ void __launch_bounds__(TC<KV, NQ, D>::kWarps * 32, 1)
   // bf16 V (ldmatrix, transposed): matrices (d lo|hi 8) x (tok 0-7|8-15)
   const uint32_t v_row_off = (uint32_t)((rr + ((mi >> 1) << 3)) * 128);
   const int v_hi = mi & 1;
+  // this warp's kv head within each unit: its K / V chunks and scales
+  const uint32_t head_off = (uint32_t)(jh * C::kHeadChunk), head_scl = (uint32_t)(jh * 64);
 
   // Per sequence t of the piece (t = 1 only in the two-sequence variant):
   // Q^T fragments, O^T accumulators, the softmax state of columns 2c, 2c+1,
@@ -452,11 +496,12 @@ __global__ void __launch_bounds__(TC<KV, NQ, D>::kWarps * 32, 1)
   float m0[NQ], m1[NQ], l0[NQ], l1[NQ];
   float sl2c[NQ][2], lgc[NQ][2];
   bool run_open = false, two = false;
-  int u = 0;
+  int u = 0, cst = 0;  // units consumed; the stage of the next one
+  uint32_t cph = 0;    // the phase that stage completes next
 
   for (int pi = pb; pi < pe; ++pi) {
     const Piece pc = p.pieces[pi];
-    const int g = pc.kv_head, L = pc.ctx_len;
+    const int g = pc.kv_head * HG + jh, L = pc.ctx_len;  // this warp's kv head
     // blocks whose every token is kept: [wb0, wb1) (the tail of the keep-set)
     // and [0, wsb) (blocks wholly inside the sinks); all other blocks test
     // their tokens one by one
@@ -471,12 +516,12 @@ __global__ void __launch_bounds__(TC<KV, NQ, D>::kWarps * 32, 1)
     if (!run_open) {
       two = NQ == 2 && pc.q_row1 >= 0;
       // Q^T fragments (B operand): rows k = head-dim slots, column n = query head r
-      const int h = g * G + r;
+      const int h = g * GP + r;
 #pragma unroll
       for (int t = 0; t < NQ; ++t) {
         const int qr = t == 0 ? pc.q_row : pc.q_row1;
-        const bool valid = r < G && qr >= 0;
-        const __nv_bfloat16* qrow = reinterpret_cast<const __nv_bfloat16*>(p.q) + ((size_t)(valid ? qr : 0) * H + h) * D;
+        const bool valid = r < GP && qr >= 0;
+        const __nv_bfloat16* qrow = reinterpret_cast<const __nv_bfloat16*>(p.q) + ((size_t)(valid ? qr : 0) * H + (valid ? h : 0)) * D;
         if (KV == 1) {
 #pragma unroll
           for (int kk = 0; kk < KT; ++kk) {
@@ -529,13 +574,13 @@ __global__ void __launch_bounds__(TC<KV, NQ, D>::kWarps * 32, 1)
     }
 
     for (int lb = pc.lblk_begin; lb < pc.lblk_end; ++lb, ++u) {
-      const int st = u % S;
-      if (!mbar_wait(bars + 8 * st, (uint32_t)((u / S) & 1), p.wait_limit_ns)) {
-        fail_and_drain<S>(p, bars, u + 1, issued, gw, lane);
+      const int st = cst;
+      if (!mbar_wait(full + 8 * st, cph, p.wait_limit_ns)) {
+        fail_and_drain<S>(p, full, u + 1, issued, leader, gw, lane);
         return;
       }
-      const uint32_t kb = data + (uint32_t)(st * C::kStageBytes);
-      const uint32_t vb = kb + (uint32_t)C::kChunkBytes;
+      const uint32_t kb = data + (uint32_t)(st * C::kStageBytes) + head_off;
+      const uint32_t vb = data + (uint32_t)(st * C::kStageBytes + C::kChunkBytes) + head_off;
 
       // ---- S = K Q^T : rows = tokens, columns = query heads of the group
       float sa[NQ][4], sb[NQ][4];
@@ -549,7 +594,7 @@ __global__ void __launch_bounds__(TC<KV, NQ, D>::kWarps * 32, 1)
         for (int kk = 0; kk < KT; ++kk) {
           const int c16 = 2 * kk + k_hi;  // 16-byte chunk index across the row
           uint32_t a[4];
-          ldsm_x4(kb + (uint32_t)((c16 >> 3) * 2048) + k_row_off + (uint32_t)((((c16 & 7) ^ rr)) << 4), a);
+          ldsm_x4(kb + (uint32_t)((c16 >> 3) * C::kBoxBytes) + k_row_off + (uint32_t)((((c16 & 7) ^ rr)) << 4), a);
 #pragma unroll
           for (int t = 0; t < NQ; ++t) {
             if (t == 1 && !two) break;
@@ -583,11 +628,11 @@ __global__ void __launch_bounds__(TC<KV, NQ, D>::kWarps * 32, 1)
               mma_f16(sa[t], a, qf[t][kk][0], qf[t][kk][1]);
           }
         }
-        const uint32_t sc = scl + (uint32_t)(st * C::kScaleBytes);
+        const uint32_t sc = scl + (uint32_t)(st * C::kScaleBytes) + head_scl;
         ks_r = lds_f32(sc + 4 * r);
         ks_r8 = lds_f32(sc + 4 * (r + 8));
-        lv_r = lds_f32(sc + 64 + 4 * r);
-        lv_r8 = lds_f32(sc + 64 + 4 * (r + 8));
+        lv_r = lds_f32(sc + HG * 64 + 4 * r);
+        lv_r8 = lds_f32(sc + HG * 64 + 4 * (r + 8));
       }
 
       // ---- mask (per token: the same for both sequences, whose shared
@@ -598,7 +643,7 @@ __global__ void __launch_bounds__(TC<KV, NQ, D>::kWarps * 32, 1)
       const bool whole = (lb >= wb0 && lb < wb1) || lb < wsb;
       const bool k0 = whole || kept(tok0, L, p.mask_mode, p.num_sinks, p.window);
       const bool k1 = whole || kept(tok1, L, p.mask_mode, p.num_sinks, p.window);
-      const bool h0v = 2 * c < G, h1v = 2 * c + 1 < G;
+      const bool h0v = 2 * c < GP, h1v = 2 * c + 1 < GP;
       if (KV != 1) {
         // log2 of the V scales of tokens r, r + 8; a masked slot may hold
         // unwritten memory, so its scale never reaches the arithmetic
@@ -606,7 +651,7 @@ __global__ void __launch_bounds__(TC<KV, NQ, D>::kWarps * 32, 1)
         lv_r8 = k1 ? fast_log2(lv_r8) : 0.f;
       }
       if (!whole && __ballot_sync(kFull, !(k0 && k1))) {
-        // zero the V rows of masked tokens in this warp's stage (0 * NaN = NaN)
+        // zero this head's V rows of masked tokens in the stage (0 * NaN = NaN)
         constexpr int kPieces = C::kRowBytes / 16;  // 16-byte pieces per token row
         constexpr int kRowsPerPass = 32 / kPieces;
         const int k = lane % kPieces;
@@ -616,7 +661,7 @@ __global__ void __launch_bounds__(TC<KV, NQ, D>::kWarps * 32, 1)
           if (!kept(lb * kBlock + t, L, p.mask_mode, p.num_sinks, p.window)) {
             uint32_t addr;
             if (KV == 1)
-              addr = vb + (uint32_t)((k >> 3) * 2048 + t * 128 + (((k & 7) ^ (t & 7)) << 4));
+              addr = vb + (uint32_t)((k >> 3) * C::kBoxBytes + t * 128 + (((k & 7) ^ (t & 7)) << 4));
             else
               addr = vb + ob_off<D>(t, 16 * k);
             asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
@@ -634,11 +679,11 @@ __global__ void __launch_bounds__(TC<KV, NQ, D>::kWarps * 32, 1)
         const float s2 = (sa[t][2] + sb[t][2]) * ks_r8, s3 = (sa[t][3] + sb[t][3]) * ks_r8;
         if (p.logits != nullptr) {
           const int qr = t == 0 ? pc.q_row : pc.q_row1;
-          float* lg = p.logits + ((size_t)qr * Hk + g) * p.logits_stride * G;
-          if (k0 && h0v) lg[(size_t)tok0 * G + 2 * c] = s0 * lgc[t][0];
-          if (k0 && h1v) lg[(size_t)tok0 * G + 2 * c + 1] = s1 * lgc[t][1];
-          if (k1 && h0v) lg[(size_t)tok1 * G + 2 * c] = s2 * lgc[t][0];
-          if (k1 && h1v) lg[(size_t)tok1 * G + 2 * c + 1] = s3 * lgc[t][1];
+          float* lg = p.logits + ((size_t)qr * Hk + g) * p.logits_stride * GP;
+          if (k0 && h0v) lg[(size_t)tok0 * GP + 2 * c] = s0 * lgc[t][0];
+          if (k0 && h1v) lg[(size_t)tok0 * GP + 2 * c + 1] = s1 * lgc[t][1];
+          if (k1 && h0v) lg[(size_t)tok1 * GP + 2 * c] = s2 * lgc[t][0];
+          if (k1 && h1v) lg[(size_t)tok1 * GP + 2 * c + 1] = s3 * lgc[t][1];
         }
         const float a0 = k0 ? s0 * sl2c[t][0] : -INFINITY, a1 = k0 ? s1 * sl2c[t][1] : -INFINITY;
         const float a2 = k1 ? s2 * sl2c[t][0] : -INFINITY, a3 = k1 ? s3 * sl2c[t][1] : -INFINITY;
@@ -693,7 +738,7 @@ __global__ void __launch_bounds__(TC<KV, NQ, D>::kWarps * 32, 1)
         for (int i = 0; i < KT; ++i) {
           const int c16 = 2 * i + v_hi;
           uint32_t a[4];
-          ldsm_x4_t(vb + (uint32_t)((c16 >> 3) * 2048) + v_row_off + (uint32_t)((((c16 & 7) ^ rr)) << 4), a);
+          ldsm_x4_t(vb + (uint32_t)((c16 >> 3) * C::kBoxBytes) + v_row_off + (uint32_t)((((c16 & 7) ^ rr)) << 4), a);
 #pragma unroll
           for (int t = 0; t < NQ; ++t) {
             if (t == 1 && !two) break;
@@ -730,14 +775,23 @@ __global__ void __launch_bounds__(TC<KV, NQ, D>::kWarps * 32, 1)
         }
       }
       __syncwarp();
-      if (issued < n_units) {
-        issue(issued);
+      if (HG > 1 && lane == 0) mbar_arrive(empty + 8 * st);  // this warp is done with the stage
+      if (++cst == S) {
+        cst = 0;
+        cph ^= 1u;
+      }
+      if (leader && issued < n_units) {
+        if (!issue(issued)) {
+          fail_and_drain<S>(p, full, u + 1, issued, true, gw, lane);
+          return;
+        }
         ++issued;
       }
     }
 
     if (pc.flags & kPieceLastOfRun) {
-      // ---- finalise the run: one output or partial record per sequence
+      // ---- finalise the run: this warp's GP rows of the output or of the
+      // unit's partial record, per sequence
       int rec_items[NQ];  // merge item of each record written, or -1
 #pragma unroll
       for (int t = 0; t < NQ; ++t) rec_items[t] = -1;
@@ -760,47 +814,50 @@ __global__ void __launch_bounds__(TC<KV, NQ, D>::kWarps * 32, 1)
         if (oi < 0) {
           __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
           const float inv0 = L0 > 0.f ? 1.f / L0 : 0.f, inv1 = L1 > 0.f ? 1.f / L1 : 0.f;
-          const size_t row0 = ((size_t)qr * H + g * G + h0) * D;
+          const size_t row0 = ((size_t)qr * H + g * GP + h0) * D;
           const size_t row1 = row0 + D;
 #pragma unroll
           for (int i = 0; i < KT; ++i)
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               const int d = dpos(i, half);
-              if (h0 < G) out[row0 + d] = __float2bfloat16(o[t][i][2 * half] * inv0);
-              if (h1 < G) out[row1 + d] = __float2bfloat16(o[t][i][2 * half + 1] * inv1);
+              if (h0 < GP) out[row0 + d] = __float2bfloat16(o[t][i][2 * half] * inv0);
+              if (h1 < GP) out[row1 + d] = __float2bfloat16(o[t][i][2 * half + 1] * inv1);
             }
           if (r == 0 && p.lse != nullptr) {
-            const size_t li = (size_t)qr * H + g * G;
-            if (h0 < G) p.lse[li + h0] = L0 > 0.f ? (m0[t] + log2f(L0)) * kLn2 : -INFINITY;
-            if (h1 < G) p.lse[li + h1] = L1 > 0.f ? (m1[t] + log2f(L1)) * kLn2 : -INFINITY;
+            const size_t li = (size_t)qr * H + g * GP;
+            if (h0 < GP) p.lse[li + h0] = L0 > 0.f ? (m0[t] + log2f(L0)) * kLn2 : -INFINITY;
+            if (h1 < GP) p.lse[li + h1] = L1 > 0.f ? (m1[t] + log2f(L1)) * kLn2 : -INFINITY;
           }
         } else {
-          float* rec = p.partials + (size_t)oi * partial_floats(G, D);
+          // record rows of this warp's heads: jh GP + h of the unit's GV
+          float* rec = p.partials + (size_t)oi * partial_floats(GV, D);
+          const int rh0 = jh * GP + h0, rh1 = jh * GP + h1;
 #pragma unroll
           for (int i = 0; i < KT; ++i)
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               const int d = dpos(i, half);
-              if (h0 < G) rec[h0 * D + d] = o[t][i][2 * half];
-              if (h1 < G) rec[h1 * D + d] = o[t][i][2 * half + 1];
+              if (h0 < GP) rec[rh0 * D + d] = o[t][i][2 * half];
+              if (h1 < GP) rec[rh1 * D + d] = o[t][i][2 * half + 1];
             }
           if (r == 0) {
-            if (h0 < G) {
-              rec[G * D + h0] = m0[t];
-              rec[G * D + G + h0] = L0;
+            if (h0 < GP) {
+              rec[GV * D + rh0] = m0[t];
+              rec[GV * D + GV + rh0] = L0;
             }
-            if (h1 < G) {
-              rec[G * D + h1] = m1[t];
-              rec[G * D + G + h1] = L1;
+            if (h1 < GP) {
+              rec[GV * D + rh1] = m1[t];
+              rec[GV * D + GV + rh1] = L1;
             }
           }
           rec_items[t] = ci;
         }
       }
       // publish the run's records (one release fence for both sequences of a
-      // pair), count them, and merge any (sequence, kv head) whose last
-      // record this was (acquire before reading the others' records)
+      // pair) and count them -- every warp of the team counts its part, so an
+      // item is complete after n_partials x HG arrivals; the warp that brings
+      // the last one merges the (sequence, unit) (acquire before reading)
       if (rec_items[0] >= 0 || (NQ == 2 && rec_items[NQ - 1] >= 0)) {
         fence_acq_rel_gpu();
         __syncwarp();
@@ -809,11 +866,11 @@ __global__ void __launch_bounds__(TC<KV, NQ, D>::kWarps * 32, 1)
           const int ci = rec_items[t];
           if (ci < 0) continue;
           int last = 0;
-          if (lane == 0) last = atomicAdd(p.counters + ci, 1) == p.combine[ci].n_partials - 1;
+          if (lane == 0) last = atomicAdd(p.counters + ci, 1) == p.combine[ci].n_partials * HG - 1;
           last = __shfl_sync(kFull, last, 0);
           if (last) {
             fence_acq_rel_gpu();
-            merge_partials<G, D>(p, p.combine[ci], lane);
+            merge_partials<GV, D>(p, p.combine[ci], lane);
           }
         }
       }
@@ -822,25 +879,27 @@ __global__ void __launch_bounds__(TC<KV, NQ, D>::kWarps * 32, 1)
   }
 }
 
-template <int KV, int G, int NQ, int D>
+// GP: query heads per kv head; HG: kv heads per unit (warps per team).
+template <int KV, int GP, int HG, int NQ, int D>
 cudaError_t launch_t(const DecodeTCParams& p, int ctas, cudaStream_t st) {
-  decode_tc_kernel<KV, G, NQ, D><<<ctas, TC<KV, NQ, D>::kWarps * 32, tc_smem_bytes(KV, NQ, D), st>>>(p);
+  decode_tc_kernel<KV, GP, HG, NQ, D><<<ctas, TC<KV, NQ, D, HG>::kWarps * 32, tc_smem_bytes(KV, NQ, D, HG), st>>>(p);
   return cudaGetLastError();
 }
 
-template <int KV, int G, int NQ, int D>
+template <int KV, int GP, int HG, int NQ, int D>
 cudaError_t prepare_t() {
-  return cudaFuncSetAttribute(decode_tc_kernel<KV, G, NQ, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)tc_smem_bytes(KV, NQ, D));
+  return cudaFuncSetAttribute(decode_tc_kernel<KV, GP, HG, NQ, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)tc_smem_bytes(KV, NQ, D, HG));
 }
 
-template <int KV, int G, int NQ, int D>
+template <int KV, int GP, int HG, int NQ, int D>
 cudaError_t occupancy_t(int* n) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_tc_kernel<KV, G, NQ, D>, TC<KV, NQ, D>::kWarps * 32,
-                                                       tc_smem_bytes(KV, NQ, D));
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_tc_kernel<KV, GP, HG, NQ, D>,
+                                                       TC<KV, NQ, D, HG>::kWarps * 32, tc_smem_bytes(KV, NQ, D, HG));
 }
 
-// Expands X(KV, G, NQ) for every compiled (dtype, group, sequences per warp).
+// Expands X(KV, G, NQ) for every compiled (dtype, group, sequences per warp);
+// each is built with units of one kv head and of tc_head_group heads.
 #define PKV_FOR_VARIANTS(X)                                                                 \
   X(1, 1, 1) X(1, 2, 1) X(1, 4, 1) X(1, 8, 1) X(2, 1, 1) X(2, 2, 1) X(2, 4, 1) X(2, 8, 1)          \
   X(3, 1, 1) X(3, 2, 1) X(3, 4, 1) X(3, 8, 1) X(1, 1, 2) X(1, 2, 2) X(1, 4, 2) X(1, 8, 2)          \

@@ -15,16 +15,70 @@ constexpr int kBlock = 16;   // tokens per physical block
 // still in flight when it gave up waiting for them too.
 enum : int32_t { kStatusTimeout = 1, kStatusBadBlock = 2, kStatusUndrained = 4 };
 
-// Geometry of the tensor-core decode kernel for a kv dtype (1 bf16, 2 FP8,
-// 3 INT8), sequences per warp (nq) and head_dim D: warps per CTA (one CTA
-// per SM), stages of each warp's ring, and dynamic shared memory.
-constexpr int tc_warps(int kv, int nq, int D) {
-  return (D == 128 && (kv == 1 || nq == 2)) || (kv != 1 && nq == 2) ? 12 : 16;
+// Kv heads per unit of the tensor-core decode kernel (kv dtype 1 bf16, 2 FP8,
+// 3 INT8; group size G; head_dim D).  A unit is one 16-token block of HG
+// adjacent kv heads, which lie next to each other in the pool: HG is chosen
+// so that a unit's K (and V) is one contiguous piece of at least 4 KB (DRAM
+// serves small scattered pieces markedly slower), while its query heads, HG x
+// G, still fit the 8 columns of one MMA tile.  The planner then sees n_kv_heads
+// / HG kv heads of HG x G query heads each (the query heads of adjacent kv
+// heads are adjacent too).  Pools whose n_kv_heads HG does not divide use 1.
+#ifndef PKV_MAX_HEAD_GROUP
+#define PKV_MAX_HEAD_GROUP 1
+#endif
+constexpr int tc_head_group(int kv, int G, int D) {
+  const int chunk = kBlock * D * (kv == 1 ? 2 : 1);  // bytes of one head's K in a block
+  int hg = chunk >= 4096 ? 1 : 4096 / chunk;
+  while (hg > 1 && (hg * G > 8 || hg > PKV_MAX_HEAD_GROUP)) hg >>= 1;
+  return hg;
 }
-constexpr int tc_stages(int kv, int nq, int D) { return kv != 1 && (nq == 2 || D == 64) ? 3 : 2; }
-constexpr size_t tc_smem_bytes(int kv, int nq, int D) {
-  return 1024 + (size_t)tc_warps(kv, nq, D) * tc_stages(kv, nq, D) *
-                    (size_t)(2 * kBlock * D * (kv == 1 ? 2 : 1) + (kv == 1 ? 0 : 128) + 8);
+
+// Geometry of the tensor-core decode kernel for a kv dtype, sequences per
+// warp (nq), head_dim D and kv heads per unit (hg): warps per CTA (one CTA per
+// SM), teams (hg warps sharing a ring of stages; the plan's "warps"), stages
+// of each ring and dynamic shared memory.  One-head units keep a ring per
+// warp (12 warps x 2 stages of 8 KB for bf16 head_dim 128, 16 warps
+// otherwise); units of several heads fill about 200 KB with stages.
+constexpr int tc_stage_bytes(int kv, int D, int hg) {
+  return 2 * hg * kBlock * D * (kv == 1 ? 2 : 1) + (kv == 1 ? 0 : hg * 128);
+}
+#ifndef PKV_TEAM_WARPS
+#define PKV_TEAM_WARPS 16  // warps per CTA of several-head units, one sequence per warp
+#endif
+#ifndef PKV_OB_WARPS  // one-head units of one-byte codes at head_dim 128, one sequence per warp
+#define PKV_OB_WARPS 16
+#endif
+#ifndef PKV_OB_STAGES
+#define PKV_OB_STAGES 2
+#endif
+#ifndef PKV_BF_WARPS  // one-head units of bf16 at head_dim 128, one sequence per warp
+#define PKV_BF_WARPS 12
+#endif
+#ifndef PKV_BF_STAGES
+#define PKV_BF_STAGES 2
+#endif
+constexpr int tc_warps(int kv, int nq, int D, int hg) {
+  return hg > 1                               ? (nq == 2 ? 12 : PKV_TEAM_WARPS / hg * hg)
+         : nq == 1 && D == 128 && kv != 1     ? PKV_OB_WARPS
+         : nq == 1 && D == 128 && kv == 1     ? PKV_BF_WARPS
+         : (D == 128 && (kv == 1 || nq == 2)) || (kv != 1 && nq == 2) ? 12
+                                                                     : 16;
+}
+constexpr int tc_teams(int kv, int nq, int D, int hg) { return tc_warps(kv, nq, D, hg) / hg; }
+#ifndef PKV_TEAM_STAGES
+#define PKV_TEAM_STAGES 0  // 0: fill about 200 KB
+#endif
+constexpr int tc_stages(int kv, int nq, int D, int hg) {
+  return hg == 1 ? (nq == 1 && D == 128 ? (kv != 1 ? PKV_OB_STAGES : PKV_BF_STAGES)
+                  : kv != 1 && (nq == 2 || D == 64) ? 3 : 2)
+         : PKV_TEAM_STAGES > 0 ? PKV_TEAM_STAGES
+         : 204800 / (tc_teams(kv, nq, D, hg) * (tc_stage_bytes(kv, D, hg) + 16)) < 2 ? 2
+         : 204800 / (tc_teams(kv, nq, D, hg) * (tc_stage_bytes(kv, D, hg) + 16)) > 6
+             ? 6
+             : 204800 / (tc_teams(kv, nq, D, hg) * (tc_stage_bytes(kv, D, hg) + 16));
+}
+constexpr size_t tc_smem_bytes(int kv, int nq, int D, int hg) {
+  return 1024 + (size_t)tc_teams(kv, nq, D, hg) * tc_stages(kv, nq, D, hg) * (size_t)(tc_stage_bytes(kv, D, hg) + 16);
 }
 
 // One contiguous range of logical blocks of one (sequence, kv head), handled
@@ -153,26 +207,27 @@ struct DecodeF32Params {
 // Tensor-core decode: kv_dtype 1 = bf16, 2 = FP8, 3 = INT8; nq = 1, or 2 for
 // the variant whose pieces may carry a second sequence over shared blocks;
 // one set per head_dim (64, 128).  Return the launch / attribute error.
-cudaError_t launch_decode_tc_d64(int kv_dtype, int G, int nq, const DecodeTCParams& p, int grid_ctas,
+// G is the kv head's group size; hg (1 or tc_head_group) the kv heads per unit.
+cudaError_t launch_decode_tc_d64(int kv_dtype, int G, int hg, int nq, const DecodeTCParams& p, int grid_ctas,
                                  cudaStream_t stream);
-cudaError_t launch_decode_tc_d128(int kv_dtype, int G, int nq, const DecodeTCParams& p, int grid_ctas,
+cudaError_t launch_decode_tc_d128(int kv_dtype, int G, int hg, int nq, const DecodeTCParams& p, int grid_ctas,
                                   cudaStream_t stream);
-cudaError_t decode_tc_prepare_d64(int kv_dtype, int G, int nq);
-cudaError_t decode_tc_prepare_d128(int kv_dtype, int G, int nq);
-cudaError_t decode_tc_occupancy_d64(int kv_dtype, int G, int nq, int* ctas_per_sm);
-cudaError_t decode_tc_occupancy_d128(int kv_dtype, int G, int nq, int* ctas_per_sm);
-inline cudaError_t launch_decode_tc(int kv_dtype, int G, int nq, int D, const DecodeTCParams& p, int grid_ctas,
-                                    cudaStream_t stream) {
-  return D == 64 ? launch_decode_tc_d64(kv_dtype, G, nq, p, grid_ctas, stream)
-                 : launch_decode_tc_d128(kv_dtype, G, nq, p, grid_ctas, stream);
+cudaError_t decode_tc_prepare_d64(int kv_dtype, int G, int hg, int nq);
+cudaError_t decode_tc_prepare_d128(int kv_dtype, int G, int hg, int nq);
+cudaError_t decode_tc_occupancy_d64(int kv_dtype, int G, int hg, int nq, int* ctas_per_sm);
+cudaError_t decode_tc_occupancy_d128(int kv_dtype, int G, int hg, int nq, int* ctas_per_sm);
+inline cudaError_t launch_decode_tc(int kv_dtype, int G, int hg, int nq, int D, const DecodeTCParams& p,
+                                    int grid_ctas, cudaStream_t stream) {
+  return D == 64 ? launch_decode_tc_d64(kv_dtype, G, hg, nq, p, grid_ctas, stream)
+                 : launch_decode_tc_d128(kv_dtype, G, hg, nq, p, grid_ctas, stream);
 }
 // sets the dynamic shared-memory attribute
-inline cudaError_t decode_tc_prepare(int kv_dtype, int G, int nq, int D) {
-  return D == 64 ? decode_tc_prepare_d64(kv_dtype, G, nq) : decode_tc_prepare_d128(kv_dtype, G, nq);
+inline cudaError_t decode_tc_prepare(int kv_dtype, int G, int hg, int nq, int D) {
+  return D == 64 ? decode_tc_prepare_d64(kv_dtype, G, hg, nq) : decode_tc_prepare_d128(kv_dtype, G, hg, nq);
 }
-inline cudaError_t decode_tc_occupancy(int kv_dtype, int G, int nq, int D, int* ctas_per_sm) {
-  return D == 64 ? decode_tc_occupancy_d64(kv_dtype, G, nq, ctas_per_sm)
-                 : decode_tc_occupancy_d128(kv_dtype, G, nq, ctas_per_sm);
+inline cudaError_t decode_tc_occupancy(int kv_dtype, int G, int hg, int nq, int D, int* ctas_per_sm) {
+  return D == 64 ? decode_tc_occupancy_d64(kv_dtype, G, hg, nq, ctas_per_sm)
+                 : decode_tc_occupancy_d128(kv_dtype, G, hg, nq, ctas_per_sm);
 }
 // Shared-prefix multi-query kernel (bf16 KV, head_dim 128): one CTA per PrefixItem.
 cudaError_t launch_prefix_decode(int G, const DecodeTCParams& p, cudaStream_t stream);

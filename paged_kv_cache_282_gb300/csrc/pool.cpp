@@ -454,7 +454,8 @@ struct pkv_pool {
   size_t tc_smem = 0;
   CUtensorMap tmap_k{}, tmap_v{};
   bool tc_path = false;
-  int G = 1;
+  int G = 1;   // query heads per kv head
+  int HG = 1;  // kv heads per unit of the tensor-core decode (the planner's kv heads hold HG each)
   uint64_t wait_limit_ns = 4000000000ull;  // bound of the decode kernel's waits
   int32_t starve_warp = -1;                // one-shot wait-expiry test hook
   bool starve_select = false;              // one-shot wait-expiry test hook of the selection
@@ -537,7 +538,15 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
                                    CUtensorMapFloatOOBfill);
 
-pkv_status make_tensor_map(CUtensorMap* m, void* base, const pkv_pool_config& c) {
+// kv heads per unit of the tensor-core decode for this pool (1 unless the
+// pool's kv heads split evenly into tc_head_group-sized units).
+int unit_heads(const pkv_pool_config& c, int G) {
+  if (c.kv_dtype == PKV_KV_FP32) return 1;
+  const int hg = tc_head_group(c.kv_dtype, G, c.head_dim);
+  return hg > 1 && c.n_kv_heads % hg == 0 ? hg : 1;
+}
+
+pkv_status make_tensor_map(CUtensorMap* m, void* base, const pkv_pool_config& c, int hg) {
   static EncodeTiledFn fn = nullptr;
   if (!fn) {
     cudaDriverEntryPointQueryResult q;
@@ -554,11 +563,12 @@ pkv_status make_tensor_map(CUtensorMap* m, void* base, const pkv_pool_config& c)
   // least 128 bytes: rows = (block, kv head, slot), columns = head_dim
   // elements, one box = 16 rows x 128 bytes (64 bf16 or 128 one-byte codes).
   // 64-byte rows (one-byte codes, head_dim 64): two slots per 128-byte row,
-  // one box = the 8 rows of a (block, kv head) chunk.
+  // one box = the 8 rows of a (block, kv head) chunk.  A decode unit of hg
+  // adjacent kv heads takes hg chunks in one box.
   const bool pair_rows = row_bytes < 128;
   cuuint64_t dims[2] = {(cuuint64_t)(pair_rows ? 128 : c.head_dim), (cuuint64_t)(pair_rows ? rows / 2 : rows)};
   cuuint64_t strides[1] = {(cuuint64_t)(pair_rows ? 128 : row_bytes)};
-  cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)(pair_rows ? kBlock / 2 : kBlock)};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)((pair_rows ? kBlock / 2 : kBlock) * hg)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -763,7 +773,7 @@ int max_total_warps(const pkv_pool* p, int nq = 1) {
 
 // Upper bound of partial records (and pieces) of one decode call.
 size_t max_pieces(const pkv_pool* p, int32_t n_seqs, int32_t num_splits) {
-  const size_t nbg = (size_t)n_seqs * p->cfg.n_kv_heads;
+  const size_t nbg = (size_t)n_seqs * (p->cfg.n_kv_heads / p->HG);
   const size_t a = 2 * nbg + (size_t)max_total_warps(p) + 1;
   const size_t b = nbg * (size_t)std::max(1, num_splits) + nbg + 1;
   // shared-prefix plans: 3 segments per sequence pair and kv head, a record
@@ -916,7 +926,7 @@ struct WarpCursor {
 
 void plan_stream_k_single(pkv_pool* p, int32_t n, const int32_t* ids, PlanCache& cache, int TWmax) {
   Plan& plan = cache.plan;
-  const int Hk = p->cfg.n_kv_heads;
+  const int Hk = p->cfg.n_kv_heads / p->HG;  // units of HG kv heads
   const auto& A = p->alloc;
   const std::vector<Seg>& segs = cache.segs;
   const std::vector<int64_t>& bg_units = cache.bg_units;
@@ -1046,7 +1056,7 @@ void plan_stream_k_single(pkv_pool* p, int32_t n, const int32_t* ids, PlanCache&
 // segment's, in warp order -- the order of the general path.
 void plan_stream_k_pairs(pkv_pool* p, int32_t n, const int32_t* ids, PlanCache& cache, int TWmax) {
   Plan& plan = cache.plan;
-  const int Hk = p->cfg.n_kv_heads;
+  const int Hk = p->cfg.n_kv_heads / p->HG;  // units of HG kv heads
   const auto& A = p->alloc;
   const std::vector<Seg>& segs = cache.segs;
   const std::vector<int64_t>& bg_units = cache.bg_units;
@@ -1193,7 +1203,7 @@ void plan_stream_k_pairs(pkv_pool* p, int32_t n, const int32_t* ids, PlanCache& 
 }
 
 Plan& build_plan(pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, int W, int num_splits) {
-  const int Hk = p->cfg.n_kv_heads;
+  const int Hk = p->cfg.n_kv_heads / p->HG;  // units of HG kv heads
   const auto& A = p->alloc;
   PlanCache& cache = plan_cache(p);
   Plan& plan = cache.plan;
@@ -1623,7 +1633,7 @@ pkv_status launch_tc_plan(pkv_pool* p, cudaStream_t st, const Plan& pl, const Pl
     if (pkv_status r = launch(p, PKV_KERNEL_PREFIX, st, [&] { return launch_prefix_decode(p->G, prm, st); })) return r;
   if (pl.total_warps == 0) return PKV_OK;
   return launch(p, PKV_KERNEL_DECODE, st,
-                [&] { return launch_decode_tc(c.kv_dtype, p->G, pl.nq, c.head_dim, prm, pl.ctas, st); });
+                [&] { return launch_decode_tc(c.kv_dtype, p->G, p->HG, pl.nq, c.head_dim, prm, pl.ctas, st); });
 }
 
 }  // namespace
@@ -1665,7 +1675,7 @@ int pkv::decode_attn_into(pkv_pool* p, void* stream, int32_t n, const int32_t* i
     const std::vector<size_t> waves = cow_waves(A);
     Plan empty_plan;
     Plan& plan = n > 0 ? build_plan(p, n, ids, mode, S, W, num_splits) : empty_plan;
-    const size_t pf = (size_t)partial_floats(p->G, c.head_dim) * sizeof(float);
+    const size_t pf = (size_t)partial_floats(p->G * p->HG, c.head_dim) * sizeof(float);
     if ((size_t)plan.n_partials * pf > partials_cap)
       return fail(PKV_ERR_WORKSPACE, "needs %zu bytes of partial records, the static scratch holds %zu",
                   (size_t)plan.n_partials * pf, partials_cap);
@@ -1866,6 +1876,7 @@ pkv_status pkv_pool_create(const pkv_pool_config* cfg, const pkv_pool_buffers* b
     p->cfg = *cfg;
     p->cfg.free_order = nullptr;
     p->G = cfg->n_heads / cfg->n_kv_heads;
+    p->HG = unit_heads(*cfg, p->G);
     p->alloc.init(cfg->num_blocks, cfg->max_seqs, cfg->max_blocks_per_seq, cfg->alloc_seed, cfg->free_order);
     if (buffers) {
       const auto& b = *buffers;
@@ -1900,21 +1911,22 @@ pkv_status pkv_pool_create(const pkv_pool_config* cfg, const pkv_pool_buffers* b
       if (e != cudaSuccess) return fail_dev(fail(PKV_ERR_CUDA, "buffer init failed: %s", cudaGetErrorString(e)));
       if (cfg->kv_dtype != PKV_KV_FP32) {
         p->tc_path = true;
-        if (pkv_status r = make_tensor_map(&p->tmap_k, b.k_pool, p->cfg)) return fail_dev(r);
-        if (pkv_status r = make_tensor_map(&p->tmap_v, b.v_pool, p->cfg)) return fail_dev(r);
-        const int D = cfg->head_dim;
-        e = decode_tc_prepare(cfg->kv_dtype, p->G, 1, D);
-        if (e == cudaSuccess) e = decode_tc_prepare(cfg->kv_dtype, p->G, 2, D);
+        const int D = cfg->head_dim, hg = p->HG;
+        if (pkv_status r = make_tensor_map(&p->tmap_k, b.k_pool, p->cfg, hg)) return fail_dev(r);
+        if (pkv_status r = make_tensor_map(&p->tmap_v, b.v_pool, p->cfg, hg)) return fail_dev(r);
+        e = decode_tc_prepare(cfg->kv_dtype, p->G, hg, 1, D);
+        if (e == cudaSuccess) e = decode_tc_prepare(cfg->kv_dtype, p->G, hg, 2, D);
         if (e == cudaSuccess && cfg->kv_dtype == PKV_KV_BF16 && D == 128) e = prefix_decode_prepare(p->G);
         int occ = 0, occ2 = 0;
-        if (e == cudaSuccess) e = decode_tc_occupancy(cfg->kv_dtype, p->G, 1, D, &occ);
-        if (e == cudaSuccess) e = decode_tc_occupancy(cfg->kv_dtype, p->G, 2, D, &occ2);
+        if (e == cudaSuccess) e = decode_tc_occupancy(cfg->kv_dtype, p->G, hg, 1, D, &occ);
+        if (e == cudaSuccess) e = decode_tc_occupancy(cfg->kv_dtype, p->G, hg, 2, D, &occ2);
         if (e != cudaSuccess) return fail_dev(fail(PKV_ERR_CUDA, "decode kernel setup failed: %s", cudaGetErrorString(e)));
+        // the plan's warps are the kernel's teams (hg warps each)
         p->tc_ctas_per_sm = std::max(1, occ);
-        p->tc_warps_per_cta = tc_warps(cfg->kv_dtype, 1, D);
+        p->tc_warps_per_cta = tc_teams(cfg->kv_dtype, 1, D, hg);
         p->tc2_ctas_per_sm = std::max(1, occ2);
-        p->tc2_warps_per_cta = tc_warps(cfg->kv_dtype, 2, D);
-        p->tc_smem = tc_smem_bytes(cfg->kv_dtype, 1, D);
+        p->tc2_warps_per_cta = tc_teams(cfg->kv_dtype, 2, D, hg);
+        p->tc_smem = tc_smem_bytes(cfg->kv_dtype, 1, D, hg);
       }
     }
     *out = p;
@@ -2396,7 +2408,7 @@ pkv_status pkv_decode_workspace_size(const pkv_pool* p, int32_t n, int32_t num_s
       *bytes_out = 0;
       return PKV_OK;
     }
-    *bytes_out = max_pieces(p, n, num_splits) * partial_floats(p->G, p->cfg.head_dim) * sizeof(float);
+    *bytes_out = max_pieces(p, n, num_splits) * partial_floats(p->G * p->HG, p->cfg.head_dim) * sizeof(float);
     return PKV_OK;
   });
 }
@@ -2455,7 +2467,7 @@ pkv_status pkv_decode_attn(pkv_pool* p, void* stream, int32_t n, const int32_t* 
     size_t need = 0;
     pkv_decode_workspace_size(p, n, num_splits, &need);
     Plan& plan = build_plan(p, n, ids, mode, S, W, num_splits);
-    const size_t pf = (size_t)partial_floats(p->G, c.head_dim) * sizeof(float);
+    const size_t pf = (size_t)partial_floats(p->G * p->HG, c.head_dim) * sizeof(float);
     if (plan.n_partials > 0 && (!workspace || workspace_bytes < plan.n_partials * pf))
       return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
     if (plan.n_partials > 0 && ((uintptr_t)workspace & 15))
@@ -2667,6 +2679,7 @@ pkv_status pkv_test_set_geometry(pkv_pool* p, int32_t num_sms, int32_t wpc, int3
     p->tc2_warps_per_cta = wpc2;
     p->tc_ctas_per_sm = p->tc2_ctas_per_sm = 1;
     p->G = group;
+    p->HG = unit_heads(p->cfg, group);
     return PKV_OK;
   });
 }
