@@ -70,9 +70,10 @@ class Setup:
     """Pool + sequences of one workload on one GPU, filled from the seeded
     generator through the library's own append path."""
 
-    def __init__(self, wl, dev, headroom_blocks: int | None = None, extra_seqs: int = 0):
+    def __init__(self, wl, dev, headroom_blocks: int | None = None, extra_seqs: int = 0, channel_scales=False):
         from paged_kv_cache_282_gb300 import PagedKVCache
         self.wl, self.dev = wl, dev
+        self.channel_scales = channel_scales
         self.extra = {}
         self.extra_seqs = extra_seqs  # sequence ids left free (forks of the workload's sequences)
         name = wl.name
@@ -87,6 +88,7 @@ class Setup:
             maxb = max((L + 15) // 16 for L in lens) + 4
             self.cache = PagedKVCache(need + hb, wl.n_heads, wl.n_kv_heads, wl.head_dim, len(lens), maxb,
                                       kv_dtype=wl.kv_dtype, alloc_seed=wl.seed, device=dev)
+            self._set_channel_scales()
             self.ids = []
             for b, L in enumerate(lens):
                 s = self.cache.seq_add()
@@ -97,6 +99,18 @@ class Setup:
                     self.cache.append([s], k[None].to(dev), v[None].to(dev))
         torch.cuda.synchronize(dev)
         self.lens = [self.cache.seq_len(s) for s in self.ids]
+
+    def _set_channel_scales(self):
+        """Per-channel scales (FP8 / INT8 pools, when asked for): seeded powers
+        of two 2^-2 .. 2^2 per (kv head, channel), standing in for calibrated
+        ones."""
+        if not self.channel_scales:
+            return
+        wl = self.wl
+        g = torch.Generator().manual_seed(wl.seed + 7)
+        kc, vc = (2.0 ** torch.randint(-2, 3, (wl.n_kv_heads, wl.head_dim), generator=g).float() for _ in range(2))
+        self.k_channel, self.v_channel = kc.to(self.dev), vc.to(self.dev)
+        self.cache.set_channel_scales(self.k_channel, self.v_channel)
 
     def _setup_prefix(self, PagedKVCache):
         wl = self.wl
@@ -402,7 +416,7 @@ def measure(args, wl, label, splits, dev, ws, rank, cascade, headline=True):
     """Times one workload's decode step (the timed region, per-step spread,
     a sustained leg, end to end through host buffers) and returns its JSON
     fields (rank 0; None elsewhere or in profile mode)."""
-    setup = Setup(wl, dev)
+    setup = Setup(wl, dev, channel_scales=args.channel_scales)
     setup.cache.set_cascade(cascade)
     st = Stepper(setup, splits)
     stream = torch.cuda.current_stream(dev)
@@ -615,6 +629,7 @@ def measure(args, wl, label, splits, dev, ws, rank, cascade, headline=True):
         "data": "synthetic (seeded N(0,1) K/V/Q; seeded uniform lengths)",
         "config": {"workload": label, "batch": len(setup.ids), "n_heads": wl.n_heads,
                    "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim, "kv_dtype": wl.kv_dtype,
+                   "channel_scales": bool(args.channel_scales),
                    "mask": wl.mask, "num_splits": splits, "cascade": cascade,
                    "context_tokens": sum(lens_step),
                    "kv_bytes_per_step": step_bytes, "l2": "KV pool larger than L2 (no flush needed)",
@@ -668,6 +683,8 @@ def main():
                     help="run the workload with another head_dim")
     ap.add_argument("--max-len", type=int, default=None,
                     help="cap every sequence's length (a smaller case of the workload, e.g. for profiling)")
+    ap.add_argument("--channel-scales", action="store_true",
+                    help="FP8 / INT8: per-channel scales on top of the per-token ones")
     ap.add_argument("--no-sustained", action="store_true", help="skip the sustained (>= 1 s) leg")
     ap.add_argument("--sustain-s", type=float, default=1.0, help="seconds of the sustained leg")
     ap.add_argument("--no-long-ctx", action="store_true",
@@ -687,6 +704,10 @@ def main():
         import dataclasses
         wl = dataclasses.replace(wl, head_dim=args.head_dim)
         label = f"{label}_d{args.head_dim}"
+    if args.channel_scales:
+        if wl.kv_dtype not in ("fp8", "int8"):
+            raise SystemExit("--channel-scales needs an FP8 or INT8 workload (--kv-dtype)")
+        label = f"{label}_channel"
     if args.max_len:
         import dataclasses
         wl = dataclasses.replace(wl, lens=tuple(min(L, args.max_len) for L in wl.lens))
@@ -718,7 +739,7 @@ def main():
     # The second throughput target: the 128K-context FP8 batch (64 splits),
     # measured in the same process (every rank) and reported inside the same line.
     if (args.workload == "llama3_8b_b64" and not args.kv_dtype and not args.no_long_ctx and
-            args.num_splits is None and not args.head_dim and not args.max_len):
+            args.num_splits is None and not args.head_dim and not args.max_len and not args.channel_scales):
         wl2 = workloads.long_context_fp8()
         leg = measure(args, wl2, wl2.name, wl2.num_splits, dev, ws, rank, cascade, headline=False)
         if line is not None and leg is not None:

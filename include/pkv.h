@@ -7,7 +7,8 @@
  * shared between sequences with reference counts and are copied on the first
  * write to a shared block.  Decode attends one query token per sequence over
  * its cached tokens, with grouped-query heads, optional FP8-E4M3 or INT8
- * storage with per-token scales, optional sliding-window or sink + window
+ * storage with per-token scales (and optional per-channel scales), optional
+ * sliding-window or sink + window
  * keep-sets, and
  * optional H2O accumulated-score output and keep-set selection.
  *
@@ -429,6 +430,27 @@ pkv_status pkv_set_wait_limit(pkv_pool* pool, int64_t wait_limit_ns);
  *   - mode 0: every sequence reads its own blocks.
  * All parts are merged by log-sum-exp like any split. */
 pkv_status pkv_set_cascade(pkv_pool* pool, int32_t mode);
+/* Per-channel scales ([PA] 量化原理 names per-channel and per-token scaling;
+ * FP8 / INT8 pools).  Each (kv head, channel d) gets a fixed scale c_d, a
+ * power of two (one exponent per channel, as in the OCP microscaling
+ * formats), set by the caller -- from calibration data rounded to powers of
+ * two, for instance -- while the pool holds no token; the per-token scales
+ * stay on top of them.  An appended row x is divided by its channel scales
+ * first, y_d = x_d / c_d (exact), and y is quantised per token as pkv_append
+ * describes; the value stored is code_d * s * c_d.  Decode folds the K
+ * scales into q once per (sequence, kv head) and the V scales into the
+ * output, so it reads no extra bytes; with powers of two both products are
+ * exact, and the numerics are those of plain per-token scaling.
+ * Compaction, copy-on-write and CPU swap move codes and per-token scales as
+ * before.
+ *   k_channel, v_channel  device [n_kv_heads][head_dim] fp32, borrowed: they
+ *                         must stay valid and unchanged while the pool is
+ *                         used; both NULL returns to plain per-token scales.
+ * Errors: PKV_ERR_UNSUPPORTED (a BF16 / FP32 pool); PKV_ERR_INVALID_ARG (a
+ * sequence holds tokens, only one array given, or a scale that is not a
+ * power of two in [2^-126, 2^127] -- checked with a synchronous copy to the
+ * host); PKV_ERR_NO_DEVICE (a host-only pool). */
+pkv_status pkv_set_channel_scales(pkv_pool* pool, const float* k_channel, const float* v_channel);
 /* Test hook for the bound above: in the next decode on this pool, warp `warp`
  * of the grid arms its first stage without issuing the copies, so that wait
  * can only run out.  Outputs of that call are undefined; the status word

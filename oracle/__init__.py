@@ -67,14 +67,15 @@ def _load():
         lib.oracle_keep.argtypes = [c_int] * 5
         lib.oracle_keep.restype = c_int
         lib.oracle_scatter.argtypes = [vp, c_int, c_int, c_int, vp, c_int, vp]
-        lib.oracle_quantize_scatter.argtypes = [vp, vp, c_int, c_int, vp, c_int, vp, c_int]
+        lib.oracle_quantize_scatter.argtypes = [vp, vp, c_int, c_int, vp, c_int, vp, c_int, vp]
+        lib.oracle_quantize_row_channel.argtypes = [vp, c_int, vp, c_int, vp, vp]
         lib.oracle_int8_encode.argtypes = [ctypes.c_float]
         lib.oracle_int8_encode.restype = ctypes.c_int8
         lib.oracle_quantize_row_int8.argtypes = [vp, c_int, vp, vp]
         lib.oracle_copy_block.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int]
         lib.oracle_decode.argtypes = [c_int, c_int, c_int, c_int, c_int, vp, vp, vp, vp, c_int,
                                       vp, c_int, vp, c_int, vp, c_dbl, c_int, c_int, c_int,
-                                      vp, vp, vp, c_int, c_int]
+                                      vp, vp, vp, c_int, c_int, vp, vp]
         lib.oracle_decode.restype = c_int
         lib.oracle_h2o_update.argtypes = [c_int, c_int, vp, vp, c_int, vp, c_int, c_int, c_int,
                                           vp, c_int]
@@ -191,6 +192,18 @@ def quantize_row_int8(row_bits: np.ndarray):
     return codes, float(scale[0])
 
 
+def quantize_row_channel(row_bits: np.ndarray, channel, kv_dtype: int):
+    """Per-channel + per-token quantisation of one row: row_bits uint16 bf16
+    bit patterns [D], channel fp32 [D] (or None) -> (codes [D], scale fp32)."""
+    lib = _load()
+    row_bits = _c(row_bits, np.uint16)
+    ch = None if channel is None else _c(channel, np.float32)
+    codes = np.empty(row_bits.size, dtype=np.int8 if kv_dtype == KV_INT8 else np.uint8)
+    scale = np.zeros(1, dtype=np.float32)
+    lib.oracle_quantize_row_channel(_ptr(row_bits), row_bits.size, _ptr(ch), kv_dtype, _ptr(codes), _ptr(scale))
+    return codes, float(scale[0])
+
+
 def quantize_row_bf16(row_bits: np.ndarray):
     """row_bits: uint16 bf16 bit patterns [D] -> (codes uint8 [D], scale fp32)."""
     lib = _load()
@@ -222,6 +235,7 @@ class OraclePool:
 
     def __init__(self, num_blocks: int, n_kv_heads: int, head_dim: int, kv_dtype: int):
         self.NB, self.Hk, self.D, self.kv_dtype = num_blocks, n_kv_heads, head_dim, kv_dtype
+        self.k_channel = self.v_channel = None  # per-channel scales [Hk][D] (FP8 / INT8), or None
         dt = {KV_FP32: np.float32, KV_BF16: np.uint16, KV_FP8: np.uint8, KV_INT8: np.int8}[kv_dtype]
         shape = (num_blocks, n_kv_heads, BLOCK, head_dim)
         self.k = np.zeros(shape, dtype=dt)
@@ -241,15 +255,24 @@ class OraclePool:
         if self.kv_dtype in (KV_FP8, KV_INT8):
             kb, vb = _c(k_rows, np.uint16), _c(v_rows, np.uint16)
             lib.oracle_quantize_scatter(_ptr(self.k), _ptr(self.k_scale), self.Hk, self.D,
-                                        _ptr(slots), T, _ptr(kb), self.kv_dtype)
+                                        _ptr(slots), T, _ptr(kb), self.kv_dtype, _ptr(self.k_channel))
             lib.oracle_quantize_scatter(_ptr(self.v), _ptr(self.v_scale), self.Hk, self.D,
-                                        _ptr(slots), T, _ptr(vb), self.kv_dtype)
+                                        _ptr(slots), T, _ptr(vb), self.kv_dtype, _ptr(self.v_channel))
         else:
             dt = np.float32 if self.kv_dtype == KV_FP32 else np.uint16
             kb, vb = _c(k_rows, dt), _c(v_rows, dt)
             es = 4 if self.kv_dtype == KV_FP32 else 2
             lib.oracle_scatter(_ptr(self.k), self.Hk, self.D, es, _ptr(slots), T, _ptr(kb))
             lib.oracle_scatter(_ptr(self.v), self.Hk, self.D, es, _ptr(slots), T, _ptr(vb))
+
+    def set_channel_scales(self, k_channel, v_channel) -> None:
+        """Per-channel scales [Hk][D] fp32 for K and V (FP8 / INT8 pools), or
+        None for both: the per-token scheme."""
+        if k_channel is None:
+            self.k_channel = self.v_channel = None
+            return
+        self.k_channel = _c(k_channel, np.float32).reshape(self.Hk, self.D)
+        self.v_channel = _c(v_channel, np.float32).reshape(self.Hk, self.D)
 
     def copy_rows(self, src_slots, dst_slots) -> None:
         es = {KV_FP32: 4, KV_BF16: 2, KV_FP8: 1, KV_INT8: 1}[self.kv_dtype]
@@ -311,7 +334,7 @@ def decode(pool: OraclePool, tables: np.ndarray, lens: np.ndarray, q: np.ndarray
                             _ptr(pool.k_scale), _ptr(pool.v_scale), pool.NB, _ptr(tables),
                             max_blocks, _ptr(lens), q_dtype, _ptr(q), float(scale), mask_mode,
                             num_sinks, window, _ptr(out), _ptr(lse), _ptr(logits),
-                            int(logits_stride or 0), threads)
+                            int(logits_stride or 0), threads, _ptr(pool.k_channel), _ptr(pool.v_channel))
     if bad:
         raise ValueError("a kept token maps to an invalid physical block")
     return out, lse, logits

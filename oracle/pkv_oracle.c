@@ -20,7 +20,7 @@
  *   [PA]  "KV Cache 与 PagedAttention：显存复用与长上下文推理" (plumephp.com,
  *         ai-kv-cache-paged-attention): 16-token blocks, global free pool,
  *         per-request block table, Block{bid, refcount} + copy_on_write,
- *         FP8 (E4M3) KV with per-token scaling.
+ *         FP8 (E4M3) / INT8 KV with per-token or per-channel scaling.
  *   [SO]  "系统优化" (threethreeliu.top, knowledge-inference-optimization-
  *         memory): sliding window / StreamingLLM keep-set, H2O evict_tokens.
  *
@@ -165,6 +165,33 @@ void oracle_quantize_row_int8(const uint16_t* x, int D, int8_t* codes, float* sc
   *scale = s;
 }
 
+/* Per-channel scaling ([PA] KV quantisation: "per-channel / per-token"
+ * scaling).  Reading adopted: every (kv head, channel d) has a fixed scale
+ * c_d > 0 chosen by the caller, and the per-token scale is kept on top of
+ * it: the row is first divided by its channel scales, y_d = x_d / c_d in
+ * fp32, then quantised per token exactly as above (s = absmax(y) / qmax,
+ * code_d = Q(y_d / s)).  The value a code stands for is code_d * s * c_d.
+ * c = NULL means c_d = 1 (y = x exactly: the per-token scheme). */
+void oracle_quantize_row_channel(const uint16_t* x, int D, const float* c, int kv_dtype, void* codes,
+                                 float* scale) {
+  float amax = 0.0f, s, y;
+  const float qmax = kv_dtype == KV_INT8 ? 127.0f : 448.0f;
+  int d;
+  for (d = 0; d < D; d++) {
+    const float v = c ? bf16_bits_to_float(x[d]) / c[d] : bf16_bits_to_float(x[d]);
+    if (fabsf(v) > amax) amax = fabsf(v);
+  }
+  s = (amax == 0.0f) ? 1.0f : amax / qmax;
+  for (d = 0; d < D; d++) {
+    y = c ? bf16_bits_to_float(x[d]) / c[d] : bf16_bits_to_float(x[d]);
+    if (kv_dtype == KV_INT8)
+      ((int8_t*)codes)[d] = oracle_int8_encode(y / s);
+    else
+      ((uint8_t*)codes)[d] = oracle_e4m3_encode(y / s);
+  }
+  *scale = s;
+}
+
 /* ------------------------------------------------------------------------- */
 /* Keep-set predicates.                                                       */
 /*   FULL:         every j in [0, L).                                         */
@@ -216,14 +243,16 @@ void oracle_scatter(void* pool, int Hk, int D, int elem_bytes, const int64_t* sl
 
 /* Quantised variants (FP8 E4M3 or INT8): quantise each (token, kv_head) row
  * of bf16 and scatter codes and the per-token scale (scale pool layout
- * [block][kv_head][slot]).  Tokens are independent (distinct slots), so they
- * are spread over the host's cores. */
+ * [block][kv_head][slot]); channel (NULL or [Hk][D]) gives the per-channel
+ * scales.  Tokens are independent (distinct slots), so they are spread over
+ * the host's cores. */
 typedef struct {
   uint8_t* pool;
   float* scale_pool;
   int Hk, D, T, thread_id, n_threads, kv_dtype;
   const int64_t* slots;
   const uint16_t* src;
+  const float* channel;
 } quantize_job;
 
 static void* quantize_worker(void* arg) {
@@ -234,19 +263,21 @@ static void* quantize_worker(void* arg) {
     for (g = 0; g < q->Hk; g++) {
       size_t di = pool_index(block, q->Hk, g, slot, q->D, 0);
       size_t si = ((size_t)block * q->Hk + g) * ORACLE_BLOCK + slot;
-      if (q->kv_dtype == KV_INT8)
-        oracle_quantize_row_int8(q->src + ((size_t)t * q->Hk + g) * q->D, q->D, (int8_t*)(q->pool + di),
-                                 q->scale_pool + si);
+      const uint16_t* row = q->src + ((size_t)t * q->Hk + g) * q->D;
+      if (q->channel)
+        oracle_quantize_row_channel(row, q->D, q->channel + (size_t)g * q->D, q->kv_dtype, q->pool + di,
+                                    q->scale_pool + si);
+      else if (q->kv_dtype == KV_INT8)
+        oracle_quantize_row_int8(row, q->D, (int8_t*)(q->pool + di), q->scale_pool + si);
       else
-        oracle_quantize_row_bf16(q->src + ((size_t)t * q->Hk + g) * q->D, q->D, q->pool + di,
-                                 q->scale_pool + si);
+        oracle_quantize_row_bf16(row, q->D, q->pool + di, q->scale_pool + si);
     }
   }
   return NULL;
 }
 
 void oracle_quantize_scatter(uint8_t* pool, float* scale_pool, int Hk, int D, const int64_t* slots, int T,
-                             const uint16_t* src, int kv_dtype) {
+                             const uint16_t* src, int kv_dtype, const float* channel) {
   long ncpu = sysconf(_SC_NPROCESSORS_ONLN);
   int n = (int)(ncpu > 0 ? ncpu : 1), i;
   quantize_job* jobs;
@@ -266,6 +297,7 @@ void oracle_quantize_scatter(uint8_t* pool, float* scale_pool, int Hk, int D, co
     jobs[i].slots = slots;
     jobs[i].src = src;
     jobs[i].kv_dtype = kv_dtype;
+    jobs[i].channel = channel;
     pthread_create(&th[i], NULL, quantize_worker, &jobs[i]);
   }
   for (i = 0; i < n; i++) pthread_join(th[i], NULL);
@@ -320,6 +352,7 @@ typedef struct {
   int n_seqs, H, Hk, D, kv_dtype, q_dtype;
   const void *k_pool, *v_pool;
   const float *k_scale, *v_scale;
+  const float *k_channel, *v_channel; /* per-channel scales [Hk][D], or NULL */
   const int32_t* tables;
   int max_blocks;
   const int32_t* lens;
@@ -333,15 +366,18 @@ typedef struct {
   int num_blocks;
 } decode_job;
 
-static double kv_value(const decode_job* jb, const void* pool, const float* scl, int block, int g,
-                       int slot, int d) {
+/* The value element d of a pool slot stands for: FP8 / INT8 code times the
+ * token's scale (times the channel's scale when the pool has them). */
+static double kv_value(const decode_job* jb, const void* pool, const float* scl, const float* channel,
+                       int block, int g, int slot, int d) {
   size_t i = pool_index(block, jb->Hk, g, slot, jb->D, d);
   if (jb->kv_dtype == KV_FP32) return (double)((const float*)pool)[i];
   if (jb->kv_dtype == KV_BF16) return bf16_bits_to_double(((const uint16_t*)pool)[i]);
   {
     size_t si = ((size_t)block * jb->Hk + g) * ORACLE_BLOCK + slot;
-    if (jb->kv_dtype == KV_INT8) return (double)((const int8_t*)pool)[i] * (double)scl[si];
-    return oracle_e4m3_decode(((const uint8_t*)pool)[i]) * (double)scl[si];
+    double c = channel ? (double)channel[(size_t)g * jb->D + d] : 1.0;
+    if (jb->kv_dtype == KV_INT8) return (double)((const int8_t*)pool)[i] * (double)scl[si] * c;
+    return oracle_e4m3_decode(((const uint8_t*)pool)[i]) * (double)scl[si] * c;
   }
 }
 
@@ -370,7 +406,7 @@ static void decode_one(decode_job* jb, int b, int h) {
       continue;
     }
     for (d = 0; d < D; d++)
-      dot += q_value(jb, b, h, d) * kv_value(jb, jb->k_pool, jb->k_scale, block, g, slot, d);
+      dot += q_value(jb, b, h, d) * kv_value(jb, jb->k_pool, jb->k_scale, jb->k_channel, block, g, slot, d);
     s[j] = jb->scale * dot;
     if (jb->logits) jb->logits[((size_t)b * jb->H + h) * jb->logits_stride + j] = s[j];
     if (s[j] > m) m = s[j];
@@ -394,7 +430,7 @@ static void decode_one(decode_job* jb, int b, int h) {
     if (block < 0 || block >= jb->num_blocks) continue;
     p = exp(s[j] - lse);
     for (d = 0; d < D; d++)
-      o[d] += p * kv_value(jb, jb->v_pool, jb->v_scale, block, g, slot, d);
+      o[d] += p * kv_value(jb, jb->v_pool, jb->v_scale, jb->v_channel, block, g, slot, d);
   }
   free(s);
 }
@@ -406,12 +442,15 @@ static void* decode_worker(void* arg) {
   return NULL;
 }
 
-/* Returns 0, or 1 when some kept token pointed at an invalid block. */
+/* Returns 0, or 1 when some kept token pointed at an invalid block.
+ * k_channel / v_channel: per-channel scales [Hk][D] of an FP8 / INT8 pool, or
+ * NULL. */
 int oracle_decode(int n_seqs, int H, int Hk, int D, int kv_dtype, const void* k_pool,
                   const void* v_pool, const float* k_scale, const float* v_scale, int num_blocks,
                   const int32_t* tables, int max_blocks, const int32_t* lens, int q_dtype,
                   const void* q, double scale, int mask_mode, int num_sinks, int window,
-                  double* out, double* lse, double* logits, int logits_stride, int n_threads) {
+                  double* out, double* lse, double* logits, int logits_stride, int n_threads,
+                  const float* k_channel, const float* v_channel) {
   decode_job base, *jobs;
   pthread_t* th;
   int t, bad = 0;
@@ -426,6 +465,8 @@ int oracle_decode(int n_seqs, int H, int Hk, int D, int kv_dtype, const void* k_
   base.v_pool = v_pool;
   base.k_scale = k_scale;
   base.v_scale = v_scale;
+  base.k_channel = k_channel;
+  base.v_channel = v_channel;
   base.tables = tables;
   base.max_blocks = max_blocks;
   base.lens = lens;

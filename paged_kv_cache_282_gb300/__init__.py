@@ -307,6 +307,17 @@ class PagedKVCache:
                                               int(acc_stride), sink_size, window_size, h2o_size, keep_idx.data_ptr(),
                                               int(keep_stride), keep_count.data_ptr()))
 
+    def set_channel_scales(self, k_channel=None, v_channel=None) -> None:
+        """Per-channel scales (FP8 / INT8 pools): device fp32 tensors
+        [n_kv_heads][head_dim] for K and V, or None for both.  Set while the
+        pool holds no token; the pool keeps references to them."""
+        if k_channel is not None:
+            assert k_channel.is_contiguous() and v_channel.is_contiguous()
+        self._channel = (k_channel, v_channel)
+        _abi.check(self.lib.pkv_set_channel_scales(
+            self._h, k_channel.data_ptr() if k_channel is not None else None,
+            v_channel.data_ptr() if v_channel is not None else None))
+
     def set_cascade(self, mode) -> None:
         """Shared-prefix decode: 0 / False off, 1 / True sequence pairs (the
         default), 2 group prefixes through the multi-query kernel."""

@@ -86,6 +86,7 @@ SIGNATURES = {
     "pkv_launch_count": [c_void_p, _P(c_int64)],
     "pkv_set_wait_limit": [c_void_p, c_int64],
     "pkv_set_cascade": [c_void_p, c_int32],
+    "pkv_set_channel_scales": [c_void_p, c_void_p, c_void_p],
     "pkv_swap_space_create": [c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_void_p],
     "pkv_swap_out": [c_void_p, c_void_p, c_int32, c_void_p],
     "pkv_swap_in": [c_void_p, c_void_p, c_int32, c_void_p],

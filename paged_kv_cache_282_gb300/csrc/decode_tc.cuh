@@ -39,6 +39,10 @@
 //    codes by, and l sums 2^(logit - m).  So the fp16 weights never overflow,
 //    and a weight flushes to zero only when its V-scaled value is below 2^-24
 //    of the largest one, whatever the magnitudes of q, K and V.
+//  - Per-channel scales (FP8 / INT8 pools that have them; powers of two, so
+//    the products are exact): the K channel scales multiply q once per run,
+//    the V channel scales multiply the output; neither touches the per-unit
+//    work.
 //  - Every wait is bounded: after the limit the warp sets the status word,
 //    drains its own copies in flight (bounded again; a drain that also runs
 //    out sets a second bit) and returns.
@@ -266,7 +270,9 @@ __device__ __forceinline__ int unit_row(const DecodeTCParams& p, int pe, int ip,
 // the scalars of record j, head h, so every head is merged at once and all
 // loads of a chunk are independent.  Each lane owns D/32 consecutive output
 // columns.  Records written by other SMs are read through L2 (ld.global.cg).
-template <int G, int D>
+// HG: kv heads of the item's unit (its row h belongs to kv head
+// kv_head * HG + h / (G / HG)), for the per-channel V scales.
+template <int G, int D, int HG = 1>
 __device__ void merge_partials(const DecodeTCParams& p, const CombineItem it, int lane) {
   constexpr int PF = G * D + ((2 * G + 3) & ~3);
   constexpr int RPC = 32 / G;  // records per chunk
@@ -323,13 +329,18 @@ __device__ void merge_partials(const DecodeTCParams& p, const CombineItem it, in
     const float Mh = __shfl_sync(kFull, M, h);
     const float inv = l > 0.f ? 1.f / l : 0.f;
     const size_t row = (size_t)it.q_row * p.n_heads + it.kv_head * G + h;
+    float cv[NV];  // per-channel V scales of this lane's columns (1 without them)
+#pragma unroll
+    for (int e = 0; e < NV; ++e)
+      cv[e] = p.v_channel != nullptr ? p.v_channel[(size_t)(it.kv_head * HG + h / (G / HG)) * D + lane * NV + e] : 1.f;
     if (NV == 4) {
       uint2 packed;
-      packed.x = pack_bf16(acc[h][0] * inv, acc[h][1] * inv);
-      packed.y = pack_bf16(acc[h][2] * inv, acc[h][3] * inv);
+      packed.x = pack_bf16(acc[h][0] * inv * cv[0], acc[h][1] * inv * cv[1]);
+      packed.y = pack_bf16(acc[h][2] * inv * cv[2], acc[h][3] * inv * cv[3]);
       *reinterpret_cast<uint2*>(out + row * D + lane * 4) = packed;
     } else {
-      *reinterpret_cast<uint32_t*>(out + row * D + lane * 2) = pack_bf16(acc[h][0] * inv, acc[h][1] * inv);
+      *reinterpret_cast<uint32_t*>(out + row * D + lane * 2) =
+          pack_bf16(acc[h][0] * inv * cv[0], acc[h][1] * inv * cv[1]);
     }
     if (lane == 0 && p.lse != nullptr) p.lse[row] = l > 0.f ? (Mh + log2f(l)) * kLn2 : -INFINITY;
   }
@@ -533,15 +544,20 @@ __global__ void __launch_bounds__(TC<KV, NQ, D, HG>::kWarps * 32, 1)
         } else {
           // one-byte codes: k-slot 2c+e <-> d = (D/4)c + 4kk + e, slot 2c+8+e <-> d + 2;
           // q scaled by 2^eq so that max |q| lies in [2^14, 2^15), then rounded to fp16
+          // (per-channel K scales c: the code products need q * c, formed in fp32)
           uint2 raw[KT];
+          const float* kch = p.k_channel != nullptr ? p.k_channel + (size_t)g * D + (D / 4) * c : nullptr;
+          auto qval = [&](int kk, int e) {  // element (D/4)c + 4kk + e of q (times c)
+            const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(e < 2 ? &raw[kk].x : &raw[kk].y);
+            const float v = (e & 1) ? __high2float(x) : __low2float(x);
+            return kch != nullptr ? v * __ldg(kch + 4 * kk + e) : v;
+          };
           float mx = 0.f;
 #pragma unroll
           for (int kk = 0; kk < KT; ++kk) {
             raw[kk] = valid ? *reinterpret_cast<const uint2*>(qrow + (D / 4) * c + 4 * kk) : make_uint2(0u, 0u);
-            const __nv_bfloat162 x01 = *reinterpret_cast<const __nv_bfloat162*>(&raw[kk].x);
-            const __nv_bfloat162 x23 = *reinterpret_cast<const __nv_bfloat162*>(&raw[kk].y);
-            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(__low2float(x01)), fabsf(__high2float(x01))),
-                                 fmaxf(fabsf(__low2float(x23)), fabsf(__high2float(x23)))));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mx = fmaxf(mx, fabsf(qval(kk, e)));
           }
           mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
           mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
@@ -551,10 +567,8 @@ __global__ void __launch_bounds__(TC<KV, NQ, D, HG>::kWarps * 32, 1)
           const float qs = __uint_as_float((uint32_t)(eq + 127) << 23);
 #pragma unroll
           for (int kk = 0; kk < KT; ++kk) {
-            const __nv_bfloat162 x01 = *reinterpret_cast<const __nv_bfloat162*>(&raw[kk].x);
-            const __nv_bfloat162 x23 = *reinterpret_cast<const __nv_bfloat162*>(&raw[kk].y);
-            qf[t][kk][0] = pack_f16(__low2float(x01) * qs, __high2float(x01) * qs);
-            qf[t][kk][1] = pack_f16(__low2float(x23) * qs, __high2float(x23) * qs);
+            qf[t][kk][0] = pack_f16(qval(kk, 0) * qs, qval(kk, 1) * qs);
+            qf[t][kk][1] = pack_f16(qval(kk, 2) * qs, qval(kk, 3) * qs);
           }
           // columns 2c, 2c+1 are the heads of lanes 8c and 8c + 4
           const int eq0 = __shfl_sync(kFull, eq, 8 * c), eq1 = __shfl_sync(kFull, eq, 8 * c + 4);
@@ -816,13 +830,15 @@ __global__ void __launch_bounds__(TC<KV, NQ, D, HG>::kWarps * 32, 1)
           const float inv0 = L0 > 0.f ? 1.f / L0 : 0.f, inv1 = L1 > 0.f ? 1.f / L1 : 0.f;
           const size_t row0 = ((size_t)qr * H + g * GP + h0) * D;
           const size_t row1 = row0 + D;
+          const float* vch = p.v_channel != nullptr ? p.v_channel + (size_t)g * D : nullptr;
 #pragma unroll
           for (int i = 0; i < KT; ++i)
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               const int d = dpos(i, half);
-              if (h0 < GP) out[row0 + d] = __float2bfloat16(o[t][i][2 * half] * inv0);
-              if (h1 < GP) out[row1 + d] = __float2bfloat16(o[t][i][2 * half + 1] * inv1);
+              const float cv = vch != nullptr ? __ldg(vch + d) : 1.f;  // per-channel V scale
+              if (h0 < GP) out[row0 + d] = __float2bfloat16(o[t][i][2 * half] * inv0 * cv);
+              if (h1 < GP) out[row1 + d] = __float2bfloat16(o[t][i][2 * half + 1] * inv1 * cv);
             }
           if (r == 0 && p.lse != nullptr) {
             const size_t li = (size_t)qr * H + g * GP;
@@ -870,7 +886,7 @@ __global__ void __launch_bounds__(TC<KV, NQ, D, HG>::kWarps * 32, 1)
           last = __shfl_sync(kFull, last, 0);
           if (last) {
             fence_acq_rel_gpu();
-            merge_partials<GV, D>(p, p.combine[ci], lane);
+            merge_partials<GV, D, HG>(p, p.combine[ci], lane);
           }
         }
       }

@@ -82,7 +82,8 @@ __global__ void append_copy_kernel(const __grid_constant__ AppendArgs a, int row
 }
 
 // FP8 / INT8: one warp per (token, kv head, K|V) row of D values (D / 32 per
-// lane).
+// lane).  With per-channel scales c the row is divided by them first
+// (y = x / c), and y is what is quantised per token.
 //   FP8:  s = absmax / 448, code = E4M3(x / s), round to nearest even,
 //         saturate to +-448
 //   INT8: s = absmax / 127, code = x / s rounded to the nearest integer
@@ -111,6 +112,11 @@ __global__ void append_quant_kernel(const __grid_constant__ AppendArgs a) {
     } else {
       const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(src);
       x[0] = __low2float(v), x[1] = __high2float(v);
+    }
+    if (a.k_channel != nullptr) {  // per-channel scales: y = x / c first (IEEE division)
+      const float* ch = (is_v ? a.v_channel : a.k_channel) + g * D + lane * E;
+#pragma unroll
+      for (int k = 0; k < E; ++k) x[k] = __fdiv_rn(x[k], ch[k]);
     }
     float amax = 0.0f;
 #pragma unroll

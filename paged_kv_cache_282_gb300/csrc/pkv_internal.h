@@ -182,6 +182,8 @@ struct DecodeTCParams {
   const PrefixItem* prefix_items;  // the multi-query kernel's work (one CTA each)
   const PrefixMember* prefix_members;
   int32_t n_prefix_items;
+  const float* k_channel;  // per-channel scales [Hk][D] of an FP8 / INT8 pool, or nullptr
+  const float* v_channel;
 };
 
 struct DecodeF32Params {
@@ -261,6 +263,8 @@ struct AppendArgs {
   void* v_pool;
   float* k_scale;
   float* v_scale;
+  const float* k_channel;  // per-channel scales [Hk][D] (FP8 / INT8), or nullptr
+  const float* v_channel;
   int32_t* tables;
   int64_t inline_slots[kInlineAppend];
   int32_t inline_patches[2 * kInlineAppend];

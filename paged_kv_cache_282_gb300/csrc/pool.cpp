@@ -10,6 +10,7 @@
 // fixed here so that tests can replay them exactly.
 
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -454,6 +455,8 @@ struct pkv_pool {
   size_t tc_smem = 0;
   CUtensorMap tmap_k{}, tmap_v{};
   bool tc_path = false;
+  const float* k_channel = nullptr;  // per-channel scales [Hk][D] (device, borrowed), FP8 / INT8 only
+  const float* v_channel = nullptr;
   int G = 1;   // query heads per kv head
   int HG = 1;  // kv heads per unit of the tensor-core decode (the planner's kv heads hold HG each)
   uint64_t wait_limit_ns = 4000000000ull;  // bound of the decode kernel's waits
@@ -1629,6 +1632,8 @@ pkv_status launch_tc_plan(pkv_pool* p, cudaStream_t st, const Plan& pl, const Pl
   prm.prefix_items = (const PrefixItem*)(dev + L.pitems);
   prm.prefix_members = (const PrefixMember*)(dev + L.pmembers);
   prm.n_prefix_items = (int32_t)pl.prefix_items.size();
+  prm.k_channel = p->k_channel;
+  prm.v_channel = p->v_channel;
   if (prm.n_prefix_items > 0)
     if (pkv_status r = launch(p, PKV_KERNEL_PREFIX, st, [&] { return launch_prefix_decode(p->G, prm, st); })) return r;
   if (pl.total_warps == 0) return PKV_OK;
@@ -2197,6 +2202,8 @@ pkv_status pkv_append(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, 
     a.v_pool = p->buf.v_pool;
     a.k_scale = p->buf.k_scale;
     a.v_scale = p->buf.v_scale;
+    a.k_channel = p->k_channel;
+    a.v_channel = p->v_channel;
     a.tables = p->buf.block_tables;
     if (ntok <= (size_t)kInlineAppend && patches.size() <= (size_t)kInlineAppend) {
       // small (decode-step) append: slots and patches ride in the parameters
@@ -2639,6 +2646,38 @@ pkv_status pkv_set_wait_limit(pkv_pool* p, int64_t wait_limit_ns) {
     if (wait_limit_ns < 1000000 || wait_limit_ns > 60000000000LL)
       return fail(PKV_ERR_INVALID_ARG, "wait limit must lie in [1 ms, 60 s]");
     p->wait_limit_ns = (uint64_t)wait_limit_ns;
+    return PKV_OK;
+  });
+}
+
+pkv_status pkv_set_channel_scales(pkv_pool* p, const float* k_channel, const float* v_channel) {
+  return guarded([&]() -> pkv_status {
+    if (!p) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    if (!p->device) return fail(PKV_ERR_NO_DEVICE, "host-only pool");
+    if (!has_scales(p->cfg.kv_dtype)) return fail(PKV_ERR_UNSUPPORTED, "channel scales need an FP8 or INT8 pool");
+    if ((k_channel == nullptr) != (v_channel == nullptr))
+      return fail(PKV_ERR_INVALID_ARG, "give both channel scale arrays or neither");
+    const auto& A = p->alloc;
+    for (int32_t s = 0; s < A.max_seqs; ++s)
+      if (A.live[s] && A.len[s] > 0)
+        return fail(PKV_ERR_INVALID_ARG, "channel scales change only while the pool holds no token (sequence %d)", s);
+    if (k_channel) {
+      const size_t n = (size_t)p->cfg.n_kv_heads * p->cfg.head_dim;
+      std::vector<float> h(2 * n);
+      PKV_CUDA(cudaMemcpy(h.data(), k_channel, n * sizeof(float), cudaMemcpyDeviceToHost));
+      PKV_CUDA(cudaMemcpy(h.data() + n, v_channel, n * sizeof(float), cudaMemcpyDeviceToHost));
+      for (size_t i = 0; i < 2 * n; ++i) {
+        uint32_t bits;
+        memcpy(&bits, &h[i], sizeof bits);
+        const uint32_t ex = (bits >> 23) & 0xFF;
+        // a power of two, 2^-126 .. 2^127: sign 0, mantissa 0, a normal exponent
+        if ((bits & 0x807FFFFFu) != 0 || ex == 0 || ex == 0xFF)
+          return fail(PKV_ERR_INVALID_ARG, "channel scale %zu of %s (%g) is not a positive power of two", i % n,
+                      i < n ? "K" : "V", (double)h[i]);
+      }
+    }
+    p->k_channel = k_channel;
+    p->v_channel = v_channel;
     return PKV_OK;
   });
 }

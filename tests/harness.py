@@ -33,6 +33,12 @@ class Twin:
         self.alloc = oracle.OracleAllocator(num_blocks, max_seqs, max_blocks, seed=seed, order=free_order)
         self.pool = oracle.OraclePool(num_blocks, wl.n_kv_heads, wl.head_dim, KV_CODE[wl.kv_dtype])
 
+    def set_channel_scales(self, k_channel: np.ndarray, v_channel: np.ndarray) -> None:
+        """Per-channel scales [Hk][D] on both sides (before any token)."""
+        self.cache.set_channel_scales(torch.from_numpy(np.ascontiguousarray(k_channel, np.float32)).to(self.dev),
+                                      torch.from_numpy(np.ascontiguousarray(v_channel, np.float32)).to(self.dev))
+        self.pool.set_channel_scales(k_channel, v_channel)
+
     def add(self) -> int:
         a, b = self.cache.seq_add(), self.alloc.seq_add()
         assert a == b
@@ -150,14 +156,17 @@ def length_only_pool(lens, device="cuda"):
 
 def dequantised(tw: "Twin", which: str) -> np.ndarray:
     """The oracle pool's K or V as float64 [NB][Hk][16][D] (codes times
-    scales for FP8 / INT8; unwritten slots may hold anything)."""
+    token and channel scales for FP8 / INT8; unwritten slots may hold
+    anything)."""
     x = tw.pool.k if which == "k" else tw.pool.v
     sc = tw.pool.k_scale if which == "k" else tw.pool.v_scale
+    ch = tw.pool.k_channel if which == "k" else tw.pool.v_channel
+    ch = 1.0 if ch is None else ch.astype(np.float64)[None, :, None, :]  # per-channel scales [Hk][D]
     if tw.wl.kv_dtype == "fp8":
         table = np.array([oracle.e4m3_decode(c) for c in range(256)], dtype=np.float64)
-        return table[x] * sc[..., None]
+        return table[x] * sc[..., None] * ch
     if tw.wl.kv_dtype == "int8":
-        return x.astype(np.float64) * sc[..., None]
+        return x.astype(np.float64) * sc[..., None] * ch
     if tw.wl.kv_dtype == "bf16":
         return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).double().numpy()
     return x.astype(np.float64)
@@ -165,13 +174,15 @@ def dequantised(tw: "Twin", which: str) -> np.ndarray:
 
 def output_bounds(tw: "Twin", ids, q: torch.Tensor, logits: np.ndarray, lse: np.ndarray, rel: float) -> np.ndarray:
     """Error bound of every output row [n][H] against the fp64 oracle:
-    sum_j p_j max_d |V_j| (rel + 2 e_j) over the kept keys j, with p the
-    oracle's softmax weights exp(logit - lse).  rel covers the roundings of
-    the weights and of the output; e_j = 2^-18 (1 + scale sum_d |q_d K_jd|)
-    covers the fp32 evaluation of logit j, whose absolute error grows with
-    the logit's magnitude (a change e in a logit moves its weight by a
-    factor up to e^e, and the normalisation by as much again)."""
+    sum_j p_j max_d |V_j| (rel + expm1(e_j + ebar)) over the kept keys j,
+    with p the oracle's softmax weights exp(logit - lse) and ebar =
+    sum_k p_k e_k.  rel covers the roundings of the weights and of the
+    output; e_j = 2^-18 (1 + scale sum_d |q_d K_jd|) bounds the error of
+    logit j, an fp32 sum of exact products, which grows with the logit's
+    magnitude.  Errors e_k in the logits move weight j by a factor within
+    exp(+-(e_j + ebar)) (its own term and the normalisation's)."""
     G, scale = tw.wl.group, tw.wl.scale
+    r = 2.0 ** -18
     K = dequantised(tw, "k")
     vmax = np.nan_to_num(np.abs(dequantised(tw, "v")).max(axis=-1), nan=0.0, posinf=0.0)
     qa = np.abs(q.double().numpy())
@@ -189,9 +200,10 @@ def output_bounds(tw: "Twin", ids, q: torch.Tensor, logits: np.ndarray, lse: np.
                 continue
             g = h // G
             k_abs = np.abs(K[blk[kept], g, pos[kept] % 16])  # [kept][D]
-            e = 2.0 ** -18 * (1.0 + scale * (k_abs @ qa[b, h]))
+            e = r * (1.0 + scale * (k_abs @ qa[b, h]))
             p = np.exp(lg[kept] - lse[b, h])
-            out[b, h] = float((p * vmax[blk[kept], g, pos[kept] % 16] * (rel + 2.0 * e)).sum())
+            ebar = float((p * e).sum())
+            out[b, h] = float((p * vmax[blk[kept], g, pos[kept] % 16] * (rel + np.expm1(e + ebar))).sum())
     return out
 
 

@@ -129,6 +129,10 @@ def test_wide_magnitudes(kv, D):
     lens = (1, 2, 17, 200, 517, 1000, 2049)
     wl = workloads.small(kv, lens=lens, head_dim=D, seed=95 + D, extra={"spread": 3.0})
     tw = Twin(wl, sum((L + 15) // 16 for L in lens) + 4, len(lens), 160, seed=8)
+    if kv != "bf16" and D == 64:  # per-channel scales 2^-7 .. 2^7 as well
+        rng = np.random.default_rng(12)
+        tw.set_channel_scales((2.0 ** rng.integers(-7, 8, (8, D))).astype(np.float32),
+                              (2.0 ** rng.integers(-7, 8, (8, D))).astype(np.float32))
     ids = fill_sequences(tw, lens)
     stride = max(lens)
     for step in (0, 1):
@@ -143,6 +147,51 @@ def test_wide_magnitudes(kv, D):
             assert bad.size == 0, (step, splits, bad[:4].tolist(), err[tuple(bad[0])], bound[tuple(bad[0])])
             got_lse = lse.cpu().numpy().astype(np.float64)
             assert np.all(np.abs(got_lse - ref_lse) <= 2e-5 * (1.0 + np.abs(ref_lse))), (step, splits)
+
+
+@pytest.mark.parametrize("D", [128, 64])
+@pytest.mark.parametrize("kv", ["fp8", "int8"])
+def test_channel_scales(kv, D):
+    """Per-channel scales (one power of two per kv head and channel, 2^-4 ..
+    2^4) on top of the per-token ones: stored codes and token scales
+    bit-exact against the oracle's quantiser with the same channel scales;
+    decode within the dtype's bound for several keep-sets and splits and
+    through the static-scratch entry; logits within 2e-3; lse within 2e-3.
+    Scales that are not powers of two, and changing the scales while tokens
+    are stored, are refused."""
+    wl = workloads.small(kv, lens=LENS, head_dim=D, seed=71)
+    tw = Twin(wl, sum((L + 15) // 16 for L in LENS) + 4, len(LENS), 160, seed=3)
+    rng = np.random.default_rng(D + (kv == "int8"))
+    kc = (2.0 ** rng.integers(-4, 5, (wl.n_kv_heads, D))).astype(np.float32)
+    vc = (2.0 ** rng.integers(-4, 5, (wl.n_kv_heads, D))).astype(np.float32)
+    bad = kc.copy()
+    bad[1, 3] = 3.0
+    with pytest.raises(_abi.PKVError) as e:
+        tw.cache.set_channel_scales(torch.from_numpy(bad).cuda(), torch.from_numpy(vc).cuda())
+    assert e.value.status == 1
+    tw.set_channel_scales(kc, vc)
+    ids = fill_sequences(tw, LENS)
+    _pool_bytes_equal(tw, ids)
+    q = workloads.queries(wl)
+    stride = max(LENS)
+    for mask, S, W, splits in (("full", 0, 0, 0), ("full", 0, 0, 3), ("sink_window", 4, 100, 0), ("sliding", 0, 37, 2)):
+        ref, ref_lse, ref_lg = tw.oracle_decode(ids, q, mask, S, W, want_logits=True, logits_stride=stride)
+        lg = torch.full((len(ids), wl.n_kv_heads, stride, wl.group), float("nan"), device="cuda")
+        out, lse = tw.cache.decode(ids, q.cuda(), scale=wl.scale, mask=mask, num_sinks=S, window=W,
+                                   num_splits=splits, logits=lg, logits_stride=stride)
+        tw.cache.sync_status()
+        assert max_err(out, ref) <= TOL[kv], (mask, splits, max_err(out, ref))
+        assert lse_err(lse, ref_lse) <= 2e-3
+        got = lg.permute(0, 1, 3, 2).reshape(len(ids), wl.n_heads, stride).cpu().numpy()
+        kept = ~np.isnan(ref_lg)
+        assert np.array_equal(kept, ~np.isnan(got)) and np.abs(got[kept] - ref_lg[kept]).max() <= 2e-3
+    out, lse = tw.cache.decode_static(ids, q.cuda(), scale=wl.scale)
+    tw.cache.sync_status()
+    ref, ref_lse, _ = tw.oracle_decode(ids, q)
+    assert max_err(out, ref) <= TOL[kv] and lse_err(lse, ref_lse) <= 2e-3
+    with pytest.raises(_abi.PKVError) as e:
+        tw.cache.set_channel_scales(None, None)
+    assert e.value.status == 1
 
 
 @pytest.mark.parametrize("kv", ["bf16", "fp8", "int8"])

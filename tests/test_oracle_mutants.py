@@ -18,8 +18,8 @@ MUTANTS = {
     "streaming window off by one": ("return j < num_sinks || j >= L - window;", "return j < num_sinks || j > L - window;"),
     "GQA maps head modulo kv heads": ("int G = jb->H / jb->Hk, g = h / G,", "int G = jb->H / jb->Hk, g = h % jb->Hk,"),
     "softmax not normalised": ("p = exp(s[j] - lse);", "p = exp(s[j] - m);"),
-    "values read from the key pool": ("o[d] += p * kv_value(jb, jb->v_pool, jb->v_scale, block, g, slot, d);",
-                                      "o[d] += p * kv_value(jb, jb->k_pool, jb->k_scale, block, g, slot, d);"),
+    "values read from the key pool": ("o[d] += p * kv_value(jb, jb->v_pool, jb->v_scale, jb->v_channel, block, g, slot, d);",
+                                      "o[d] += p * kv_value(jb, jb->k_pool, jb->k_scale, jb->k_channel, block, g, slot, d);"),
     "lse off by a constant": ("lse = m + log(sum);", "lse = m + log(sum) + 1e-6;"),
     "H2O sum instead of mean over heads": ("acc[(size_t)b * acc_stride + j] += cur / (double)H;",
                                            "acc[(size_t)b * acc_stride + j] += cur;"),
@@ -37,8 +37,8 @@ MUTANTS = {
     "int8 quantiser divides by 128": ("s = (amax == 0.0f) ? 1.0f : amax / 127.0f;",
                                       "s = (amax == 0.0f) ? 1.0f : amax / 128.0f;"),
     "int8 codes truncate": ("  n = round_half_even(a);\n  if (n > 127) n = 127;", "  n = (int)a;\n  if (n > 127) n = 127;"),
-    "int8 codes read unsigned": ("if (jb->kv_dtype == KV_INT8) return (double)((const int8_t*)pool)[i] * (double)scl[si];",
-                                 "if (jb->kv_dtype == KV_INT8) return (double)((const uint8_t*)pool)[i] * (double)scl[si];"),
+    "int8 codes read unsigned": ("if (jb->kv_dtype == KV_INT8) return (double)((const int8_t*)pool)[i] * (double)scl[si] * c;",
+                                 "if (jb->kv_dtype == KV_INT8) return (double)((const uint8_t*)pool)[i] * (double)scl[si] * c;"),
     "swap-out shares no host block": ("      } else if (out) {\n        a->host_refcount[map[b]] += 1;",
                                       "      } else if (0) {\n        a->host_refcount[map[b]] += 1;"),
     "swap-in keeps the host blocks": ("        else\n          drop_host_block(a, from[lb]);", "        else\n          (void)0;"),
@@ -55,8 +55,22 @@ MUTANTS = {
     "decode ignores the softmax scale": ("s[j] = jb->scale * dot;", "s[j] = dot;"),
     "decode averages values uniformly": ("    p = exp(s[j] - lse);\n", "    p = exp(s[j] - lse) * 0 + 1.0 / L;\n"),
     "FP8 codes read without their scale": (
-        "return oracle_e4m3_decode(((const uint8_t*)pool)[i]) * (double)scl[si];",
-        "return oracle_e4m3_decode(((const uint8_t*)pool)[i]);"),
+        "return oracle_e4m3_decode(((const uint8_t*)pool)[i]) * (double)scl[si] * c;",
+        "return oracle_e4m3_decode(((const uint8_t*)pool)[i]) * c;"),
+    "channel quantiser multiplies by the channel scale": (
+        "    y = c ? bf16_bits_to_float(x[d]) / c[d] : bf16_bits_to_float(x[d]);",
+        "    y = c ? bf16_bits_to_float(x[d]) * c[d] : bf16_bits_to_float(x[d]);"),
+    "channel quantiser's absmax ignores the channel scales": (
+        "    const float v = c ? bf16_bits_to_float(x[d]) / c[d] : bf16_bits_to_float(x[d]);",
+        "    const float v = bf16_bits_to_float(x[d]);"),
+    "dequantisation ignores the channel scale": (
+        "    double c = channel ? (double)channel[(size_t)g * jb->D + d] : 1.0;", "    double c = 1.0;"),
+    "dequantisation takes kv head 0's channel scales": (
+        "    double c = channel ? (double)channel[(size_t)g * jb->D + d] : 1.0;",
+        "    double c = channel ? (double)channel[d] : 1.0;"),
+    "quantiser takes kv head 0's channel scales": (
+        "oracle_quantize_row_channel(row, q->D, q->channel + (size_t)g * q->D, q->kv_dtype, q->pool + di,",
+        "oracle_quantize_row_channel(row, q->D, q->channel, q->kv_dtype, q->pool + di,"),
     "bf16 query loses its low mantissa bits": ("  return bf16_bits_to_double(((const uint16_t*)jb->q)[i]);",
                                                "  return bf16_bits_to_double(((const uint16_t*)jb->q)[i] & 0xFF00);"),
     "e4m3 saturates at 240": ("if (a >= 448.0) return (uint8_t)(sign | 0x7E);", "if (a >= 240.0) return (uint8_t)(sign | 0x77);"),

@@ -169,6 +169,82 @@ def test_quantize_row_per_token_scale():
     assert s == 1.0 and not codes.any()
 
 
+def _channel_restatement(xf, c, kv):
+    """Per-channel + per-token quantisation written again with numpy float32
+    arithmetic (IEEE division) and the library codecs: y = x / c, s =
+    absmax(y) / qmax, code = Q(y / s)."""
+    qmax = np.float32(127.0 if kv == "int8" else 448.0)
+    y = np.asarray(xf, np.float32) / np.asarray(c, np.float32)
+    amax = np.float32(np.max(np.abs(y)))
+    s = np.float32(1.0) if amax == 0 else np.float32(amax / qmax)
+    z = (y / s).astype(np.float32)
+    if kv == "int8":
+        return np.clip(np.rint(z.astype(np.float64)), -127, 127).astype(np.int8), float(s)
+    return _torch_e4m3_code(z), float(s)
+
+
+@pytest.mark.parametrize("kv", ["fp8", "int8"])
+def test_quantize_row_channel_scales(kv):
+    """Per-channel scaling ([PA] KV quantisation names per-channel and
+    per-token scaling): codes and scale equal an independent restatement;
+    unit channel scales (or none) reproduce the per-token quantiser byte for
+    byte; dequantisation code * s * c lies within half a step of x."""
+    rng = np.random.default_rng(5 if kv == "fp8" else 6)
+    kvc = oracle.KV_INT8 if kv == "int8" else oracle.KV_FP8
+    per_token = oracle.quantize_row_int8 if kv == "int8" else oracle.quantize_row_bf16
+    for trial in range(200):
+        D = 128 if trial % 2 else 64
+        x = torch.from_numpy(rng.standard_normal(D).astype(np.float32) * 10 ** rng.uniform(-2, 2))
+        bits = workloads.as_bits(x.to(torch.bfloat16))
+        xf = x.to(torch.bfloat16).float().numpy()
+        c = (10.0 ** rng.uniform(-1.5, 1.5, D)).astype(np.float32)
+        if trial % 3 == 0:
+            c = (2.0 ** rng.integers(-4, 5, D)).astype(np.float32)  # exact powers of two
+        codes, s = oracle.quantize_row_channel(bits, c, kvc)
+        want, ws = _channel_restatement(xf, c, kv)
+        assert s == ws and np.array_equal(codes, want), trial
+        # no channel scales, or all ones: the per-token scheme exactly
+        pc, ps = per_token(bits)
+        for cc in (None, np.ones(D, np.float32)):
+            c1, s1 = oracle.quantize_row_channel(bits, cc, kvc)
+            assert s1 == ps and np.array_equal(c1, pc)
+        # dequantisation within half a step (times the channel scale)
+        if kv == "int8":
+            deq = codes.astype(np.float64) * s * c
+            tol = 0.5 * s * c.astype(np.float64) * (1 + 1e-6)
+        else:
+            deq = np.array([oracle.e4m3_decode(int(v)) for v in codes]) * s * c
+            y = np.abs(xf.astype(np.float64) / c)
+            tol = np.maximum(y * 2.0 ** -4, s * 2.0 ** -10) * c * (1 + 1e-6)
+        assert np.all(np.abs(deq - xf) <= tol + 1e-30), trial
+
+
+@pytest.mark.parametrize("kv,ratio", [("int8", 100.0), ("fp8", 1e5)])
+def test_channel_scales_tame_outlier_channels(kv, ratio):
+    """What per-channel scales are for: keys with a few outlier channels lose
+    the small channels under per-token scaling (INT8's uniform steps already
+    at 100x; FP8's floating steps only once the small channels fall into its
+    subnormal range); dividing each channel by its own magnitude first keeps
+    their precision."""
+    rng = np.random.default_rng(9)
+    D, T = 128, 64
+    mag = np.ones(D, np.float32)
+    mag[[3, 40, 77, 120]] = ratio
+    x = rng.standard_normal((T, D)).astype(np.float32) * mag
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    xf = xb.float().numpy()
+    kvc = oracle.KV_INT8 if kv == "int8" else oracle.KV_FP8
+    err_tok, err_ch = [], []
+    for t in range(T):
+        bits = workloads.as_bits(xb[t])
+        for c, errs in ((None, err_tok), (mag, err_ch)):
+            codes, s = oracle.quantize_row_channel(bits, c, kvc)
+            vals = codes.astype(np.float64) if kv == "int8" else np.array([oracle.e4m3_decode(int(v)) for v in codes])
+            deq = vals * s * (1.0 if c is None else c)
+            errs.append(np.abs(deq - xf[t])[mag == 1.0].mean())
+    assert np.mean(err_ch) < 0.2 * np.mean(err_tok)
+
+
 def test_int8_encode_rounds_half_to_even_and_clamps():
     for x, want in ((0.5, 0), (1.5, 2), (2.5, 2), (-2.5, -2), (-3.5, -4), (126.5, 126), (0.49999997, 0),
                     (127.0, 127), (127.4, 127), (127.6, 127), (300.0, 127), (-1e9, -127), (float("inf"), 127),
@@ -479,6 +555,46 @@ def _dequant_dense(wl, pool, alloc, sid, L):
         ks.append(kc * torch.from_numpy(pool.k_scale[b, :, o].astype(np.float64))[:, None])
         vs.append(vc * torch.from_numpy(pool.v_scale[b, :, o].astype(np.float64))[:, None])
     return torch.stack(ks), torch.stack(vs)
+
+
+@pytest.mark.parametrize("kv", ["fp8", "int8"])
+def test_decode_with_channel_scales_matches_library_attention(kv):
+    """FP8 / INT8 pools with per-channel scales (different per kv head): the
+    oracle's decode equals library attention on the dense layout dequantised
+    here as code * token scale * channel scale, and the stored codes equal the
+    per-row quantiser's."""
+    lens = (1, 17, 50, 97)
+    wl = workloads.small(kv, lens=lens, n_heads=8, n_kv_heads=2, head_dim=32, seed=23)
+    rng = np.random.default_rng(41)
+    kc = (10.0 ** rng.uniform(-1, 1, (2, 32))).astype(np.float32)
+    vc = (10.0 ** rng.uniform(-1, 1, (2, 32))).astype(np.float32)
+    nb = sum((L + 15) // 16 for L in lens) + 2
+    alloc = oracle.OracleAllocator(nb, len(lens), 8, seed=4)
+    kvc = oracle.KV_INT8 if kv == "int8" else oracle.KV_FP8
+    pool = oracle.OraclePool(nb, 2, 32, kvc)
+    pool.set_channel_scales(kc, vc)
+    ids = [alloc.seq_add() for _ in lens]
+    for b, L in enumerate(lens):
+        k, v = workloads.kv_rows(wl, b, 0, L)
+        slots, _ = alloc.append([ids[b]], L)
+        pool.write(slots, workloads.as_bits(k), workloads.as_bits(v))
+        # codes at the slots equal the per-row quantiser with the same channel scales
+        j = L - 1
+        blk, off = int(slots[j] // 16), int(slots[j] % 16)
+        for g in range(2):
+            ck, sk = oracle.quantize_row_channel(workloads.as_bits(k[j, g]), kc[g], kvc)
+            assert np.array_equal(pool.k[blk, g, off], ck) and pool.k_scale[blk, g, off] == sk
+    q = workloads.queries(wl)
+    qd = q.float().double()
+    out, lse, _ = oracle.decode(pool, alloc.tables_matrix(ids), lens, workloads.as_bits(q), oracle.KV_BF16,
+                                wl.n_heads, wl.scale)
+    for b, L in enumerate(lens):
+        K, V = _dequant_dense(wl, pool, alloc, ids[b], L)
+        K = K * torch.from_numpy(kc.astype(np.float64))[None]
+        V = V * torch.from_numpy(vc.astype(np.float64))[None]
+        keep = torch.ones(L, dtype=torch.bool)
+        ref = _sdpa(qd[b], K, V, wl.group, keep, wl.scale)
+        assert torch.allclose(torch.from_numpy(out[b]), ref, rtol=1e-10, atol=1e-12), (b, L)
 
 
 @pytest.mark.parametrize("kv", ["fp32", "bf16", "fp8", "int8"])
