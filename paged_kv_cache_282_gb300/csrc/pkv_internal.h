@@ -57,12 +57,19 @@ constexpr int tc_stage_bytes(int kv, int D, int hg) {
 #ifndef PKV_BF_STAGES
 #define PKV_BF_STAGES 2
 #endif
+#ifndef PKV_PAIR_WARPS  // two sequences per warp (shared-prefix pairs)
+#define PKV_PAIR_WARPS 12
+#endif
+#ifndef PKV_PAIR_STAGES
+#define PKV_PAIR_STAGES 0  // 0: 2 for bf16, 3 for one-byte codes
+#endif
 constexpr int tc_warps(int kv, int nq, int D, int hg) {
   return hg > 1                               ? (nq == 2 ? 12 : PKV_TEAM_WARPS / hg * hg)
+         : nq == 2 && (D == 128 || kv != 1)   ? PKV_PAIR_WARPS
          : nq == 1 && D == 128 && kv != 1     ? PKV_OB_WARPS
          : nq == 1 && D == 128 && kv == 1     ? PKV_BF_WARPS
-         : (D == 128 && (kv == 1 || nq == 2)) || (kv != 1 && nq == 2) ? 12
-                                                                     : 16;
+         : D == 128 && kv == 1                ? 12
+                                              : 16;
 }
 constexpr int tc_teams(int kv, int nq, int D, int hg) { return tc_warps(kv, nq, D, hg) / hg; }
 #ifndef PKV_TEAM_STAGES
@@ -70,6 +77,7 @@ constexpr int tc_teams(int kv, int nq, int D, int hg) { return tc_warps(kv, nq, 
 #endif
 constexpr int tc_stages(int kv, int nq, int D, int hg) {
   return hg == 1 ? (nq == 1 && D == 128 ? (kv != 1 ? PKV_OB_STAGES : PKV_BF_STAGES)
+                  : nq == 2 && PKV_PAIR_STAGES > 0 ? PKV_PAIR_STAGES
                   : kv != 1 && (nq == 2 || D == 64) ? 3 : 2)
          : PKV_TEAM_STAGES > 0 ? PKV_TEAM_STAGES
          : 204800 / (tc_teams(kv, nq, D, hg) * (tc_stage_bytes(kv, D, hg) + 16)) < 2 ? 2
