@@ -70,9 +70,12 @@ struct TC {
   static constexpr int kRowBytes = D * kEs;            // one token of one kv head
   static constexpr int kHeadChunk = 16 * kRowBytes;    // K (or V) of one kv head of a block
   static constexpr int kChunkBytes = HG * kHeadChunk;  // K (or V) of one unit, contiguous in HBM
-  static constexpr int kStageBytes = 2 * kChunkBytes;  // K then V
-  static constexpr int kScaleBytes = KV == 1 ? 0 : HG * 128;  // 16 K scales per head, then the V scales
-  static constexpr uint32_t kTxBytes = kStageBytes + kScaleBytes;
+  static constexpr int kUPS = tc_ups(KV, NQ, D, HG);             // units per stage
+  static constexpr int kUnitBytes = 2 * kChunkBytes;              // K then V of one unit
+  static constexpr int kStageBytes = kUPS * kUnitBytes;
+  static constexpr int kUnitScaleBytes = KV == 1 ? 0 : HG * 128;  // 16 K scales per head, then the V scales
+  static constexpr int kScaleBytes = kUPS * kUnitScaleBytes;      // per stage
+  static constexpr uint32_t kUnitTxBytes = kUnitBytes + kUnitScaleBytes;
   static constexpr int kWarps = tc_warps(KV, NQ, D, HG);
   static constexpr int kTeams = kWarps / HG;  // each team shares one ring of stages
   static constexpr int kStages = tc_stages(KV, NQ, D, HG);
@@ -347,8 +350,8 @@ __device__ void merge_partials(const DecodeTCParams& p, const CombineItem it, in
 }
 
 // Reports a wait that ran out (the team's leader also waits, bounded again,
-// for the copies it has in flight into its team's stages, and flags a drain
-// that ran out too).
+// for the copies it has in flight into its team's stages -- the stages from
+// `from` to `issued` in ring order -- and flags a drain that ran out too).
 template <int S>
 __device__ void fail_and_drain(const DecodeTCParams& p, uint32_t full, int from, int issued, bool leader, int gw,
                                int lane) {
@@ -439,54 +442,74 @@ __global__ void __launch_bounds__(TC<KV, NQ, D, HG>::kWarps * 32, 1)
     next_rows = unit_row<HG>(p, pe, nip, nil, lane);
   }
   int batch_base = 0;
-  int issued = 0, ist = 0;  // units issued; the stage the next one goes to
-  // parity of that stage's empty barrier to wait for: refill v waits for the
-  // consumption of unit v - S, phase (v / S - 1) of the barrier; the S first
-  // issues wait for nothing and wrap the stage index once, so start at 1
+  int issued = 0, ist = 0;  // units issued; the stage the next stage of units goes to
+  // parity of that stage's empty barrier to wait for: refill v (teams: one
+  // unit per stage) waits for the consumption of unit v - S, phase (v / S - 1)
+  // of the barrier; the S first issues wait for nothing and wrap the stage
+  // index once, so start at 1
   uint32_t iph = 1;
 
   // TMA y coordinate of a unit's chunk: token rows, or pairs of tokens
   auto ycoord = [](int row) { return C::kPairRows ? row >> 1 : row; };
-  // leader warp, all lanes; lane 0 issues the copies of unit v.  False when
-  // the wait for the team to release the stage ran out.
-  auto issue = [&](int v) -> bool {
-    if (v - batch_base >= 32) {
-      batch_base += 32;
-      cur_rows = next_rows;
-      advance(p.pieces, pe, nip, nil, 32);
-      next_rows = unit_row<HG>(p, pe, nip, nil, lane);
-    }
-    const int row = __shfl_sync(kFull, cur_rows, v - batch_base);
+  // leader warp, all lanes: fills the next stage with the next (up to) kUPS
+  // units of the stream; lane 0 issues the copies.  Returns the units issued
+  // (0 past the end of the stream) or -1 when the wait for the team to
+  // release the stage ran out.
+  auto issue = [&]() -> int {
+    const int v0 = issued;
+    if (v0 >= n_units) return 0;
+    const int nu = min(C::kUPS, n_units - v0);
     const int st = ist;
     bool ok = true;
-    if (HG > 1 && v >= S) ok = mbar_wait(empty + 8 * st, iph, p.wait_limit_ns);  // lanes agree
+    if (HG > 1 && v0 >= S) ok = mbar_wait(empty + 8 * st, iph, p.wait_limit_ns);  // lanes agree
     if (++ist == S) {
       ist = 0;
       iph ^= 1u;
     }
-    if (!ok) return false;
-    if (lane == 0) {
-      const uint32_t bar = full + 8 * st;
-      const uint32_t dst = data + (uint32_t)(st * C::kStageBytes);
-      mbar_expect_tx(bar, C::kTxBytes);
-      if (v == 0 && gw == p.starve_warp) return true;  // test hook: this stage never completes
-      const int y = ycoord(row);
+    if (!ok) return -1;
+    int rows[C::kUPS];
 #pragma unroll
-      for (int b = 0; b < C::kBoxes; ++b) {
-        tma_load_2d(dst + C::kBoxBytes * b, &p.tmap_k, 64 * b, y, bar);
-        tma_load_2d(dst + C::kChunkBytes + C::kBoxBytes * b, &p.tmap_v, 64 * b, y, bar);
-      }
-      if (KV != 1) {
-        const uint32_t sd = scl + (uint32_t)(st * C::kScaleBytes);
-        bulk_load(sd, p.k_scale + row, HG * 64, bar);
-        bulk_load(sd + HG * 64, p.v_scale + row, HG * 64, bar);
+    for (int j = 0; j < C::kUPS; ++j) {
+      rows[j] = -1;
+      if (j < nu) {
+        const int v = v0 + j;
+        if (v - batch_base >= 32) {
+          batch_base += 32;
+          cur_rows = next_rows;
+          advance(p.pieces, pe, nip, nil, 32);
+          next_rows = unit_row<HG>(p, pe, nip, nil, lane);
+        }
+        rows[j] = __shfl_sync(kFull, cur_rows, v - batch_base);
       }
     }
-    return true;
+    issued = v0 + nu;
+    if (lane == 0) {
+      const uint32_t bar = full + 8 * st;
+      mbar_expect_tx(bar, (uint32_t)nu * C::kUnitTxBytes);
+      if (v0 == 0 && gw == p.starve_warp) return nu;  // test hook: this stage never completes
+#pragma unroll
+      for (int j = 0; j < C::kUPS; ++j) {
+        if (j >= nu) break;
+        const uint32_t dst = data + (uint32_t)(st * C::kStageBytes + j * C::kUnitBytes);
+        const int y = ycoord(rows[j]);
+#pragma unroll
+        for (int b = 0; b < C::kBoxes; ++b) {
+          tma_load_2d(dst + C::kBoxBytes * b, &p.tmap_k, 64 * b, y, bar);
+          tma_load_2d(dst + C::kChunkBytes + C::kBoxBytes * b, &p.tmap_v, 64 * b, y, bar);
+        }
+        if (KV != 1) {
+          const uint32_t sd = scl + (uint32_t)(st * C::kScaleBytes + j * C::kUnitScaleBytes);
+          bulk_load(sd, p.k_scale + rows[j], HG * 64, bar);
+          bulk_load(sd + HG * 64, p.v_scale + rows[j], HG * 64, bar);
+        }
+      }
+    }
+    return nu;
   };
 
   if (leader)
-    for (; issued < n_units && issued < S; ++issued) issue(issued);
+    for (int s0 = 0; s0 < S; ++s0)
+      if (issue() <= 0) break;
 
   // per-lane fragment address pieces
   const int mi = lane >> 3, rr = lane & 7;
@@ -589,12 +612,13 @@ __global__ void __launch_bounds__(TC<KV, NQ, D, HG>::kWarps * 32, 1)
 
     for (int lb = pc.lblk_begin; lb < pc.lblk_end; ++lb, ++u) {
       const int st = cst;
-      if (!mbar_wait(full + 8 * st, cph, p.wait_limit_ns)) {
-        fail_and_drain<S>(p, full, u + 1, issued, leader, gw, lane);
+      const int slot = C::kUPS == 1 ? 0 : u % C::kUPS;  // the unit's place in its stage
+      if (slot == 0 && !mbar_wait(full + 8 * st, cph, p.wait_limit_ns)) {
+        fail_and_drain<S>(p, full, u / C::kUPS + 1, (issued + C::kUPS - 1) / C::kUPS, leader, gw, lane);
         return;
       }
-      const uint32_t kb = data + (uint32_t)(st * C::kStageBytes) + head_off;
-      const uint32_t vb = data + (uint32_t)(st * C::kStageBytes + C::kChunkBytes) + head_off;
+      const uint32_t kb = data + (uint32_t)(st * C::kStageBytes + slot * C::kUnitBytes) + head_off;
+      const uint32_t vb = data + (uint32_t)(st * C::kStageBytes + slot * C::kUnitBytes + C::kChunkBytes) + head_off;
 
       // ---- S = K Q^T : rows = tokens, columns = query heads of the group
       float sa[NQ][4], sb[NQ][4];
@@ -642,7 +666,7 @@ __global__ void __launch_bounds__(TC<KV, NQ, D, HG>::kWarps * 32, 1)
               mma_f16(sa[t], a, qf[t][kk][0], qf[t][kk][1]);
           }
         }
-        const uint32_t sc = scl + (uint32_t)(st * C::kScaleBytes) + head_scl;
+        const uint32_t sc = scl + (uint32_t)(st * C::kScaleBytes + slot * C::kUnitScaleBytes) + head_scl;
         ks_r = lds_f32(sc + 4 * r);
         ks_r8 = lds_f32(sc + 4 * (r + 8));
         lv_r = lds_f32(sc + HG * 64 + 4 * r);
@@ -788,18 +812,17 @@ __global__ void __launch_bounds__(TC<KV, NQ, D, HG>::kWarps * 32, 1)
           }
         }
       }
-      __syncwarp();
-      if (HG > 1 && lane == 0) mbar_arrive(empty + 8 * st);  // this warp is done with the stage
-      if (++cst == S) {
-        cst = 0;
-        cph ^= 1u;
-      }
-      if (leader && issued < n_units) {
-        if (!issue(issued)) {
-          fail_and_drain<S>(p, full, u + 1, issued, true, gw, lane);
+      if (slot == C::kUPS - 1 || u + 1 == n_units) {  // the stage is consumed
+        __syncwarp();
+        if (HG > 1 && lane == 0) mbar_arrive(empty + 8 * st);  // this warp is done with the stage
+        if (++cst == S) {
+          cst = 0;
+          cph ^= 1u;
+        }
+        if (leader && issue() < 0) {
+          fail_and_drain<S>(p, full, u / C::kUPS + 1, (issued + C::kUPS - 1) / C::kUPS, true, gw, lane);
           return;
         }
-        ++issued;
       }
     }
 

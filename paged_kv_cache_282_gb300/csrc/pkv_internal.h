@@ -37,9 +37,12 @@ constexpr int tc_head_group(int kv, int G, int D) {
 // warp (nq), head_dim D and kv heads per unit (hg): warps per CTA (one CTA per
 // SM), teams (hg warps sharing a ring of stages; the plan's "warps"), stages
 // of each ring and dynamic shared memory.  One-head units keep a ring per
-// warp (12 warps x 2 stages of 8 KB for bf16 head_dim 128, 16 warps
-// otherwise); units of several heads fill about 200 KB with stages.
-constexpr int tc_stage_bytes(int kv, int D, int hg) {
+// warp (7 warps x 2 stages of 8 KB for bf16 head_dim 128: fewer, longer
+// runs per SM stream faster than 12 x 2; 16 warps for one-byte codes, which
+// the 64-split batch needs; 12 or 16 otherwise); units of several heads fill
+// about 200 KB with stages.
+// Bytes of one unit in a stage: K then V of hg heads (+ their scales).
+constexpr int tc_unit_bytes(int kv, int D, int hg) {
   return 2 * hg * kBlock * D * (kv == 1 ? 2 : 1) + (kv == 1 ? 0 : hg * 128);
 }
 #ifndef PKV_TEAM_WARPS
@@ -51,11 +54,26 @@ constexpr int tc_stage_bytes(int kv, int D, int hg) {
 #ifndef PKV_OB_STAGES
 #define PKV_OB_STAGES 2
 #endif
+#ifndef PKV_OB_UPS  // units per stage
+#define PKV_OB_UPS 1
+#endif
 #ifndef PKV_BF_WARPS  // one-head units of bf16 at head_dim 128, one sequence per warp
-#define PKV_BF_WARPS 12
+#define PKV_BF_WARPS 7
 #endif
 #ifndef PKV_BF_STAGES
 #define PKV_BF_STAGES 2
+#endif
+#ifndef PKV_BF_UPS
+#define PKV_BF_UPS 1
+#endif
+#ifndef PKV_D64_WARPS  // one-head units at head_dim 64, one sequence per warp
+#define PKV_D64_WARPS 16
+#endif
+#ifndef PKV_D64_STAGES
+#define PKV_D64_STAGES 0  // 0: 2 for bf16, 3 for one-byte codes
+#endif
+#ifndef PKV_D64_UPS
+#define PKV_D64_UPS 1
 #endif
 #ifndef PKV_PAIR_WARPS  // two sequences per warp (shared-prefix pairs)
 #define PKV_PAIR_WARPS 12
@@ -68,25 +86,33 @@ constexpr int tc_warps(int kv, int nq, int D, int hg) {
          : nq == 2 && (D == 128 || kv != 1)   ? PKV_PAIR_WARPS
          : nq == 1 && D == 128 && kv != 1     ? PKV_OB_WARPS
          : nq == 1 && D == 128 && kv == 1     ? PKV_BF_WARPS
+         : nq == 1                            ? PKV_D64_WARPS
          : D == 128 && kv == 1                ? 12
                                               : 16;
 }
+// Units per stage: a stage holds that many consecutive units of its ring's
+// stream under one barrier (one-sequence rings only).
+constexpr int tc_ups(int kv, int nq, int D, int hg) {
+  return hg > 1 || nq == 2 ? 1 : D == 64 ? PKV_D64_UPS : kv != 1 ? PKV_OB_UPS : PKV_BF_UPS;
+}
+constexpr int tc_stage_bytes(int kv, int nq, int D, int hg) { return tc_ups(kv, nq, D, hg) * tc_unit_bytes(kv, D, hg); }
 constexpr int tc_teams(int kv, int nq, int D, int hg) { return tc_warps(kv, nq, D, hg) / hg; }
 #ifndef PKV_TEAM_STAGES
 #define PKV_TEAM_STAGES 0  // 0: fill about 200 KB
 #endif
 constexpr int tc_stages(int kv, int nq, int D, int hg) {
   return hg == 1 ? (nq == 1 && D == 128 ? (kv != 1 ? PKV_OB_STAGES : PKV_BF_STAGES)
+                  : nq == 1 && PKV_D64_STAGES > 0 ? PKV_D64_STAGES
                   : nq == 2 && PKV_PAIR_STAGES > 0 ? PKV_PAIR_STAGES
                   : kv != 1 && (nq == 2 || D == 64) ? 3 : 2)
          : PKV_TEAM_STAGES > 0 ? PKV_TEAM_STAGES
-         : 204800 / (tc_teams(kv, nq, D, hg) * (tc_stage_bytes(kv, D, hg) + 16)) < 2 ? 2
-         : 204800 / (tc_teams(kv, nq, D, hg) * (tc_stage_bytes(kv, D, hg) + 16)) > 6
+         : 204800 / (tc_teams(kv, nq, D, hg) * (tc_stage_bytes(kv, nq, D, hg) + 16)) < 2 ? 2
+         : 204800 / (tc_teams(kv, nq, D, hg) * (tc_stage_bytes(kv, nq, D, hg) + 16)) > 6
              ? 6
-             : 204800 / (tc_teams(kv, nq, D, hg) * (tc_stage_bytes(kv, D, hg) + 16));
+             : 204800 / (tc_teams(kv, nq, D, hg) * (tc_stage_bytes(kv, nq, D, hg) + 16));
 }
 constexpr size_t tc_smem_bytes(int kv, int nq, int D, int hg) {
-  return 1024 + (size_t)tc_teams(kv, nq, D, hg) * tc_stages(kv, nq, D, hg) * (size_t)(tc_stage_bytes(kv, D, hg) + 16);
+  return 1024 + (size_t)tc_teams(kv, nq, D, hg) * tc_stages(kv, nq, D, hg) * (size_t)(tc_stage_bytes(kv, nq, D, hg) + 16);
 }
 
 // One contiguous range of logical blocks of one (sequence, kv head), handled
