@@ -180,13 +180,26 @@ __global__ void table_patch_kernel(const int32_t* __restrict__ patches, int n, i
 // H2O score: acc[b][j] += mean over query heads of exp(s_hj - lse_h)
 // ---------------------------------------------------------------------------
 
+// Each term is 2^(s log2(e) - lse log2(e)) on the hardware ex2: the exponent
+// comes from one fused multiply-add of the fp32 logit against lse log2(e)
+// staged in shared memory, so its absolute error is about |s - lse| 2^-24
+// plus half an ulp of lse log2(e); with the instruction's own relative error
+// (about 2^-22) a term is within 2e-6 of exp(s - lse) for |s - lse| < 20,
+// and terms below that weigh nothing at the scores' 1e-5 relative bound.
+// The accurate expf spent most of this kernel's time in instructions.
+__device__ __forceinline__ float h2o_term(float s, float lse2) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(fmaf(s, 1.4426950408889634f, -lse2)));
+  return y;
+}
+
 __global__ void h2o_score_kernel(const SeqRow* __restrict__ rows, int n_heads, int n_kv_heads,
                                  const float* __restrict__ logits, int64_t stride, const float* __restrict__ lse,
                                  int mode, int S, int W, float* __restrict__ acc, int64_t acc_stride) {
-  extern __shared__ float s_lse[];
+  extern __shared__ float s_lse[];  // lse log2(e) per query head
   const SeqRow row = rows[blockIdx.y];
   const int b = row.q_row, L = row.ctx_len;
-  for (int h = threadIdx.x; h < n_heads; h += blockDim.x) s_lse[h] = lse[(size_t)b * n_heads + h];
+  for (int h = threadIdx.x; h < n_heads; h += blockDim.x) s_lse[h] = lse[(size_t)b * n_heads + h] * 1.4426950408889634f;
   __syncthreads();
   const int nk = keep_count_of(L, mode, S, W);
   const int k = blockIdx.x * blockDim.x + threadIdx.x;
@@ -216,7 +229,8 @@ __global__ void h2o_score_kernel(const SeqRow* __restrict__ rows, int n_heads, i
       for (int u = 0; u < 8; ++u) {
         if (f0 + u < nf) {
           const float* ls = s_lse + 4 * (f0 + u);
-          sum += expf(x[u].x - ls[0]) + expf(x[u].y - ls[1]) + expf(x[u].z - ls[2]) + expf(x[u].w - ls[3]);
+          sum += h2o_term(x[u].x, ls[0]) + h2o_term(x[u].y, ls[1]) + h2o_term(x[u].z, ls[2]) +
+                 h2o_term(x[u].w, ls[3]);
         }
       }
     }
@@ -224,7 +238,7 @@ __global__ void h2o_score_kernel(const SeqRow* __restrict__ rows, int n_heads, i
 #pragma unroll 8
     for (int g = 0; g < n_kv_heads; ++g) {
       const float* lg = logits + (((size_t)b * n_kv_heads + g) * stride + j) * G;
-      for (int i = 0; i < G; ++i) sum += expf(lg[i] - s_lse[g * G + i]);
+      for (int i = 0; i < G; ++i) sum += h2o_term(lg[i], s_lse[g * G + i]);
     }
   }
   *accj = prev + sum / (float)n_heads;

@@ -15,9 +15,11 @@ KV_CODE = {"fp32": oracle.KV_FP32, "bf16": oracle.KV_BF16, "fp8": oracle.KV_FP8,
 MASK_CODE = {"full": oracle.MASK_FULL, "sliding": oracle.MASK_SLIDING, "sink_window": oracle.MASK_SINK_WINDOW}
 TOL = {"fp32": 1e-4, "bf16": 1e-2, "fp8": 2e-2, "int8": 2e-2}  # max abs error on N(0,1) inputs
 # Accumulated H2O scores against the oracle's fp64 ones: relative error.  Each
-# term exp(s - lse) is evaluated in fp32 from fp32 logits and lse, whose
-# absolute errors (a few ulp of |s| and |lse|, below 1e-6 for the unit-scale
-# logits of these inputs) become the term's relative error.
+# term exp(s - lse) is evaluated from fp32 logits and lse, whose absolute
+# errors (a few ulp of |s| and |lse|, below 1e-6 for the unit-scale logits of
+# these inputs) become the term's relative error, as does the rounding of its
+# exponent (about |s - lse| 2^-24, taken base 2) and the exponential's own
+# (about 2^-22 relative): a few 1e-6 at most.
 H2O_RTOL = 1e-5
 
 
