@@ -449,6 +449,7 @@ __global__ void __launch_bounds__(TC<KV, NQ, D, HG>::kWarps * 32, 1)
   // index once, so start at 1
   uint32_t iph = 1;
 
+  const uint64_t kv_policy = l2_evict_first_policy();
   // TMA y coordinate of a unit's chunk: token rows, or pairs of tokens
   auto ycoord = [](int row) { return C::kPairRows ? row >> 1 : row; };
   // leader warp, all lanes: fills the next stage with the next (up to) kUPS
@@ -494,8 +495,13 @@ __global__ void __launch_bounds__(TC<KV, NQ, D, HG>::kWarps * 32, 1)
         const int y = ycoord(rows[j]);
 #pragma unroll
         for (int b = 0; b < C::kBoxes; ++b) {
-          tma_load_2d(dst + C::kBoxBytes * b, &p.tmap_k, 64 * b, y, bar);
-          tma_load_2d(dst + C::kChunkBytes + C::kBoxBytes * b, &p.tmap_v, 64 * b, y, bar);
+          if (p.kv_evict_first) {
+            tma_load_2d_hint(dst + C::kBoxBytes * b, &p.tmap_k, 64 * b, y, bar, kv_policy);
+            tma_load_2d_hint(dst + C::kChunkBytes + C::kBoxBytes * b, &p.tmap_v, 64 * b, y, bar, kv_policy);
+          } else {
+            tma_load_2d(dst + C::kBoxBytes * b, &p.tmap_k, 64 * b, y, bar);
+            tma_load_2d(dst + C::kChunkBytes + C::kBoxBytes * b, &p.tmap_v, 64 * b, y, bar);
+          }
         }
         if (KV != 1) {
           const uint32_t sd = scl + (uint32_t)(st * C::kScaleBytes + j * C::kUnitScaleBytes);

@@ -75,6 +75,9 @@ constexpr int tc_unit_bytes(int kv, int D, int hg) {
 #ifndef PKV_D64_UPS
 #define PKV_D64_UPS 1
 #endif
+#ifndef PKV_KV_EVICT_FIRST  // allows the L2 evict-first policy on K / V copies read once per call
+#define PKV_KV_EVICT_FIRST 1
+#endif
 #ifndef PKV_PAIR_WARPS  // two sequences per warp (shared-prefix pairs)
 #define PKV_PAIR_WARPS 12
 #endif
@@ -218,6 +221,7 @@ struct DecodeTCParams {
   int32_t n_prefix_items;
   const float* k_channel;  // per-channel scales [Hk][D] of an FP8 / INT8 pool, or nullptr
   const float* v_channel;
+  int32_t kv_evict_first;  // nonzero: K / V tensor copies with an L2 evict-first policy
 };
 
 struct DecodeF32Params {

@@ -139,6 +139,7 @@ struct HostAllocator {
   std::vector<uint8_t> live, holes;
   std::set<int32_t> free_ids;
   int64_t cow_count = 0, n_alloc = 0, n_freed = 0;
+  int64_t n_multi = 0;  // blocks held more than once (refcount > 1)
   // queued device-side effects (device pools only: a host-only pool has no
   // device table or blocks to update)
   bool queue = false;
@@ -215,6 +216,7 @@ struct HostAllocator {
     max_seqs = ms;
     max_blocks = mb;
     refcount.assign(nb, 0);
+    n_multi = 0;
     std::vector<int32_t> front_first(nb);
     if (order) {
       std::copy(order, order + nb, front_first.begin());
@@ -279,10 +281,14 @@ struct HostAllocator {
     --n_alloc;
   }
   void release(int32_t b) {
+    if (refcount[b] == 2) --n_multi;
     if (--refcount[b] == 0) {
       free_blocks.push_back(b);
       ++n_freed;
     }
+  }
+  void add_ref(int32_t b) {
+    if (++refcount[b] == 2) ++n_multi;
   }
   void set_entry(int32_t s, int32_t lb, int32_t v) {
     if ((int32_t)table[s].size() <= lb) table[s].resize(lb + 1, -1);
@@ -1634,6 +1640,10 @@ pkv_status launch_tc_plan(pkv_pool* p, cudaStream_t st, const Plan& pl, const Pl
   prm.n_prefix_items = (int32_t)pl.prefix_items.size();
   prm.k_channel = p->k_channel;
   prm.v_channel = p->v_channel;
+  // K / V read once per call (no block held twice in the pool, no pairs):
+  // their copies may leave L2 first; shared blocks keep the default policy,
+  // since sequences that share them reread them from L2
+  prm.kv_evict_first = PKV_KV_EVICT_FIRST && pl.nq == 1 && p->alloc.n_multi == 0 ? 1 : 0;
   if (prm.n_prefix_items > 0)
     if (pkv_status r = launch(p, PKV_KERNEL_PREFIX, st, [&] { return launch_prefix_decode(p->G, prm, st); })) return r;
   if (pl.total_warps == 0) return PKV_OK;
@@ -1803,7 +1813,7 @@ pkv_status swap_move(pkv_pool* p, void* stream, int32_t n, const int32_t* ids, b
       } else if (out) {
         ++A.host_refcount[m];
       } else {
-        ++A.refcount[m];
+        A.add_ref(m);
       }
       row[lb] = m;
     }
@@ -1979,7 +1989,7 @@ pkv_status pkv_seq_fork(pkv_pool* p, int32_t src, int32_t* dst_out) {
     for (int32_t lb = 0; lb < nblk; ++lb) {
       const int32_t b = from[lb];
       if (b < 0) continue;
-      ++A.refcount[b];
+      A.add_ref(b);
       if (A.queue) A.pending_patch.push_back({d * A.max_blocks + lb, b});
     }
     A.len[d] = A.len[src];
@@ -2102,8 +2112,7 @@ pkv_status pkv_pool_stats(const pkv_pool* p, pkv_stats* out) {
     out->num_blocks = A.NB;
     out->free_blocks = (int64_t)A.free_blocks.size();
     out->used_blocks = A.NB - out->free_blocks;
-    out->shared_blocks = 0;
-    for (int32_t r : A.refcount) out->shared_blocks += r > 1;
+    out->shared_blocks = A.n_multi;
     out->active_seqs = A.max_seqs - (int64_t)A.free_ids.size();
     out->cow_copies = A.cow_count;
     out->blocks_allocated = A.n_alloc;
@@ -2155,7 +2164,7 @@ pkv_status pkv_reserve_slots(pkv_pool* p, int32_t n, const int32_t* ids, int32_t
         } else if (A.refcount[A.table[s][lb]] > 1) {
           const int32_t old = A.table[s][lb];
           const int32_t fresh = A.take();
-          --A.refcount[old];
+          A.release(old);  // still held by another sequence
           A.set_entry(s, lb, fresh);
           if (A.queue) {
             A.pending_cow.push_back(old);
