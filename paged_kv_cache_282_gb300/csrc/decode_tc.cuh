@@ -248,10 +248,11 @@ __device__ __forceinline__ void advance(const Piece* __restrict__ P, int pe, int
   }
 }
 
-// Row coordinate (block * Hk + first kv head) * 16 of the unit `lane` positions
-// past the cursor, or -1 past the end (a piece's kv_head names its unit's
-// group of HG kv heads).
-template <int HG>
+// Row coordinate r = (block * Hk + first kv head) * 16 of the unit `lane`
+// positions past the cursor (a piece's kv_head names its unit's group of HG
+// kv heads), or -1 past the end.  Two-sequence rings (PER_UNIT) return r when
+// the unit is read once (Piece::stream_from) and -r - 2 otherwise.
+template <int HG, bool PER_UNIT>
 __device__ __forceinline__ int unit_row(const DecodeTCParams& p, int pe, int ip, int il, int lane) {
   advance(p.pieces, pe, ip, il, lane);
   if (ip >= pe) return -1;
@@ -263,7 +264,9 @@ __device__ __forceinline__ int unit_row(const DecodeTCParams& p, int pe, int ip,
     p.status[2] = il;
     blk = 0;  // keep the copy in bounds; the status word reports the fault
   }
-  return (blk * p.n_kv_heads + pc.kv_head * HG) * kBlock;
+  const int row = (blk * p.n_kv_heads + pc.kv_head * HG) * kBlock;
+  if (!PER_UNIT) return row;
+  return il >= pc.stream_from ? row : -row - 2;
 }
 
 // Log-sum-exp merge of the partial records of one (sequence, kv head) by one
@@ -437,9 +440,9 @@ __global__ void __launch_bounds__(TC<KV, NQ, D, HG>::kWarps * 32, 1)
   int bip = pb, bil = p.pieces[pb].lblk_begin;  // cursor at the current batch start
   int cur_rows = -1, next_rows = -1, nip = bip, nil = bil;
   if (leader) {
-    cur_rows = unit_row<HG>(p, pe, bip, bil, lane);
+    cur_rows = unit_row<HG, NQ == 2>(p, pe, bip, bil, lane);
     advance(p.pieces, pe, nip, nil, 32);
-    next_rows = unit_row<HG>(p, pe, nip, nil, lane);
+    next_rows = unit_row<HG, NQ == 2>(p, pe, nip, nil, lane);
   }
   int batch_base = 0;
   int issued = 0, ist = 0;  // units issued; the stage the next stage of units goes to
@@ -478,9 +481,9 @@ __global__ void __launch_bounds__(TC<KV, NQ, D, HG>::kWarps * 32, 1)
           batch_base += 32;
           cur_rows = next_rows;
           advance(p.pieces, pe, nip, nil, 32);
-          next_rows = unit_row<HG>(p, pe, nip, nil, lane);
+          next_rows = unit_row<HG, NQ == 2>(p, pe, nip, nil, lane);
         }
-        rows[j] = __shfl_sync(kFull, cur_rows, v - batch_base);
+        rows[j] = __shfl_sync(kFull, cur_rows, v - batch_base);  // encoded as unit_row returns it
       }
     }
     issued = v0 + nu;
@@ -491,11 +494,15 @@ __global__ void __launch_bounds__(TC<KV, NQ, D, HG>::kWarps * 32, 1)
 #pragma unroll
       for (int j = 0; j < C::kUPS; ++j) {
         if (j >= nu) break;
+        // read once by this call: the copies may leave L2 first (the pair
+        // rings decide per unit, the one-sequence rings per call)
+        const bool once = NQ == 2 ? rows[j] >= 0 : p.kv_evict_first != 0;
+        const int row = NQ == 2 && rows[j] < 0 ? -rows[j] - 2 : rows[j];
         const uint32_t dst = data + (uint32_t)(st * C::kStageBytes + j * C::kUnitBytes);
-        const int y = ycoord(rows[j]);
+        const int y = ycoord(row);
 #pragma unroll
         for (int b = 0; b < C::kBoxes; ++b) {
-          if (p.kv_evict_first) {
+          if (once) {
             tma_load_2d_hint(dst + C::kBoxBytes * b, &p.tmap_k, 64 * b, y, bar, kv_policy);
             tma_load_2d_hint(dst + C::kChunkBytes + C::kBoxBytes * b, &p.tmap_v, 64 * b, y, bar, kv_policy);
           } else {
@@ -505,8 +512,8 @@ __global__ void __launch_bounds__(TC<KV, NQ, D, HG>::kWarps * 32, 1)
         }
         if (KV != 1) {
           const uint32_t sd = scl + (uint32_t)(st * C::kScaleBytes + j * C::kUnitScaleBytes);
-          bulk_load(sd, p.k_scale + rows[j], HG * 64, bar);
-          bulk_load(sd + HG * 64, p.v_scale + rows[j], HG * 64, bar);
+          bulk_load(sd, p.k_scale + row, HG * 64, bar);
+          bulk_load(sd + HG * 64, p.v_scale + row, HG * 64, bar);
         }
       }
     }

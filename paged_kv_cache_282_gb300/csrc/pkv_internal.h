@@ -140,7 +140,11 @@ struct Piece {
   int32_t q_row1;
   int32_t out_index1;
   int32_t item1;
-  int32_t pad;
+  // Logical blocks from this one on are read once by this call (no other
+  // sequence holds them, or only the pair itself): their copies may leave L2
+  // first.  lblk_end or more: none.  Read by the two-sequence rings; the
+  // one-sequence rings take DecodeTCParams::kv_evict_first.
+  int32_t stream_from;
 };
 static_assert(sizeof(Piece) == 48, "Piece layout");
 
@@ -221,7 +225,7 @@ struct DecodeTCParams {
   int32_t n_prefix_items;
   const float* k_channel;  // per-channel scales [Hk][D] of an FP8 / INT8 pool, or nullptr
   const float* v_channel;
-  int32_t kv_evict_first;  // nonzero: K / V tensor copies with an L2 evict-first policy
+  int32_t kv_evict_first;  // one-sequence rings: K / V copies with an L2 evict-first policy
 };
 
 struct DecodeF32Params {

@@ -727,6 +727,7 @@ struct Plan {
 struct Seg {
   int32_t b, g, lo, hi;  // batch index, kv head, logical blocks [lo, hi)
   int32_t b1;            // >= 0: a second sequence over the same physical blocks
+  int32_t stream_from;   // blocks from this one on are read once (Piece::stream_from)
 };
 
 struct PlanRun {
@@ -1010,7 +1011,7 @@ void plan_stream_k_single(pkv_pool* p, int32_t n, const int32_t* ids, PlanCache&
     pc.q_row1 = -1;
     pc.out_index1 = -1;
     pc.item1 = 0;
-    pc.pad = 0;
+    pc.stream_from = sg.stream_from;
     tpl[k].first_partial = br.first_partial;
     tpl[k].vfirst = br.vfirst;
     tpl[k].run_continues = k + 1 < segs.size() && segs[k + 1].b == sg.b && segs[k + 1].g == sg.g;
@@ -1167,7 +1168,7 @@ void plan_stream_k_pairs(pkv_pool* p, int32_t n, const int32_t* ids, PlanCache& 
     pc.q_row1 = sg.b1;
     pc.out_index1 = -1;
     pc.item1 = sg.b1 >= 0 ? item_of[(size_t)sg.b1 * Hk + sg.g] : 0;
-    pc.pad = 0;
+    pc.stream_from = sg.stream_from;
     tpl[k].first_partial = rc.rec0;
     tpl[k].vfirst = rc.v0;
     tpl[k].run_continues =
@@ -1209,6 +1210,23 @@ void plan_stream_k_pairs(pkv_pool* p, int32_t n, const int32_t* ids, PlanCache& 
   plan.warp_begin[slots] = (int32_t)np;
   plan.total_warps = slots;
   plan.ctas = TW > 0 ? C : 0;
+}
+
+// The start of the longest tail [x, hi) of the logical blocks [lo, hi) of
+// sequence slot s whose every block at most `limit` sequences hold (lo when
+// no block of the pool is held twice).  The call reads those blocks once
+// (limit 2: a pair's shared blocks, read once for both), so their copies may
+// leave L2 first.  Without eviction, sharing is a prefix of the tables and
+// this is every such block; an evicted sibling can leave its window blocks
+// shared behind blocks that are not, which then keep the default policy.
+int32_t stream_from(const pkv_pool* p, int32_t s, int32_t lo, int32_t hi, int32_t limit) {
+  if (!PKV_KV_EVICT_FIRST) return INT32_MAX;
+  const auto& A = p->alloc;
+  if (A.n_multi == 0) return lo;
+  const int32_t* t = A.table[s].data();
+  int32_t x = hi;
+  while (x > lo && (t[x - 1] < 0 || A.refcount[t[x - 1]] <= limit)) --x;
+  return x;
 }
 
 Plan& build_plan(pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, int W, int num_splits) {
@@ -1255,15 +1273,20 @@ Plan& build_plan(pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, in
     auto nblk = [&](int32_t b) { return ceil_div(A.len[ids[b]], kBlock); };
     for (const auto& pr : pairs) {
       paired[pr.b0] = paired[pr.b1] = 1;
+      // the pair's shared blocks stream where only the pair holds them
+      const int32_t sf_pair = stream_from(p, ids[pr.b0], base[pr.b0], pr.shared, 2);
+      const int32_t sf0 = stream_from(p, ids[pr.b0], pr.shared, nblk(pr.b0), 1);
+      const int32_t sf1 = stream_from(p, ids[pr.b1], pr.shared, nblk(pr.b1), 1);
       for (int g = 0; g < Hk; ++g) {
-        segs.push_back({pr.b0, g, base[pr.b0], pr.shared, pr.b1});
-        if (pr.shared < nblk(pr.b0)) segs.push_back({pr.b0, g, pr.shared, nblk(pr.b0), -1});
-        if (pr.shared < nblk(pr.b1)) segs.push_back({pr.b1, g, pr.shared, nblk(pr.b1), -1});
+        segs.push_back({pr.b0, g, base[pr.b0], pr.shared, pr.b1, sf_pair});
+        if (pr.shared < nblk(pr.b0)) segs.push_back({pr.b0, g, pr.shared, nblk(pr.b0), -1, sf0});
+        if (pr.shared < nblk(pr.b1)) segs.push_back({pr.b1, g, pr.shared, nblk(pr.b1), -1, sf1});
       }
     }
     for (int32_t b = 0; b < n; ++b) {
+      const int32_t sf = paired[b] ? 0 : stream_from(p, ids[b], base[b], nblk(b), 1);
       for (int g = 0; g < Hk; ++g) {
-        if (!paired[b] && nblk(b) > base[b]) segs.push_back({b, g, base[b], nblk(b), -1});
+        if (!paired[b] && nblk(b) > base[b]) segs.push_back({b, g, base[b], nblk(b), -1, sf});
         bg_units[(size_t)b * Hk + g] = nblk(b);
       }
     }
@@ -1299,9 +1322,11 @@ Plan& build_plan(pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, in
     for (int32_t b = 0; b < n; ++b) {
       BlockRange r[2];
       const int nr = keep_ranges(A.len[ids[b]], mode, S, W, r);
+      int32_t sf[2];
+      for (int k = 0; k < nr; ++k) sf[k] = stream_from(p, ids[b], r[k].lo, r[k].hi, 1);
       for (int g = 0; g < Hk; ++g)
         for (int k = 0; k < nr; ++k) {
-          segs.push_back({b, g, r[k].lo, r[k].hi, -1});
+          segs.push_back({b, g, r[k].lo, r[k].hi, -1, sf[k]});
           bg_units[(size_t)b * Hk + g] += r[k].hi - r[k].lo;
         }
     }
@@ -1340,7 +1365,7 @@ Plan& build_plan(pkv_pool* p, int32_t n, const int32_t* ids, int mode, int S, in
     pc.q_row1 = s.b1;
     pc.out_index1 = -1;
     pc.item1 = 0;
-    pc.pad = 0;
+    pc.stream_from = s.stream_from;
     return pc;
   };
   std::vector<int32_t>& piece_warp = cache.piece_warp;  // warp of each piece
@@ -1640,9 +1665,9 @@ pkv_status launch_tc_plan(pkv_pool* p, cudaStream_t st, const Plan& pl, const Pl
   prm.n_prefix_items = (int32_t)pl.prefix_items.size();
   prm.k_channel = p->k_channel;
   prm.v_channel = p->v_channel;
-  // K / V read once per call (no block held twice in the pool, no pairs):
-  // their copies may leave L2 first; shared blocks keep the default policy,
-  // since sequences that share them reread them from L2
+  // one-sequence rings: evict-first when no block of the pool is held twice
+  // (deciding per unit, as the pair rings do, costs those rings about a
+  // quarter more instructions)
   prm.kv_evict_first = PKV_KV_EVICT_FIRST && pl.nq == 1 && p->alloc.n_multi == 0 ? 1 : 0;
   if (prm.n_prefix_items > 0)
     if (pkv_status r = launch(p, PKV_KERNEL_PREFIX, st, [&] { return launch_prefix_decode(p->G, prm, st); })) return r;

@@ -380,7 +380,7 @@ def test_append_to_shared_block_needs_one_copy_fewer_than_sharers(pkv, spare):
 # The uploaded plan's records, as laid out by the library (see the test
 # hook's declaration): int32 fields in declaration order.
 _PIECE = np.dtype([(f, "<i4") for f in ("seq_slot", "q_row", "kv_head", "lo", "hi", "ctx_len", "out_index", "flags",
-                                        "q_row1", "out_index1", "item1", "pad")])
+                                        "q_row1", "out_index1", "item1", "stream_from")])
 _COMBINE = np.dtype([(f, "<i4") for f in ("q_row", "kv_head", "first", "n")])
 _EMPTY = np.dtype([(f, "<i4") for f in ("q_row", "kv_head")])
 _PITEM = np.dtype([(f, "<i4") for f in ("kv_head", "table_seq", "lo", "hi", "member_begin", "n_members", "p0", "p1")])
@@ -426,6 +426,26 @@ def _check_plan(c, ids, Hk, mode, S, W, splits, raw, info, wpc):
     assert all(nn >= 1 for _, nn in spans)
     assert [f for f, _ in spans] == list(np.cumsum([0] + [nn for _, nn in spans])[:-1])
     assert sum(nn for _, nn in spans) == info[2]
+    # blocks read once by the call (no other holder, or only the pair): a
+    # piece's stream_from starts the longest tail of its segment held by at
+    # most that many sequences, counted over the listed sequences' tables
+    # (every live sequence is listed); with no block held twice it is the
+    # segment's start
+    holders = {}
+    for t in tables:
+        for blk in t[t >= 0].tolist():
+            holders[blk] = holders.get(blk, 0) + 1
+    any_shared = any(v > 1 for v in holders.values())
+    for pc in pieces:
+        limit = 2 if pc["q_row1"] >= 0 else 1
+        row = tables[int(pc["q_row"])]
+        sf = int(pc["stream_from"])
+        for lb in range(max(sf, int(pc["lo"])), int(pc["hi"])):
+            assert holders[int(row[lb])] <= limit, (lb, sf)
+        if any_shared and int(pc["lo"]) <= sf - 1 < int(pc["hi"]):
+            assert holders[int(row[sf - 1])] > limit, (sf, int(pc["lo"]))
+        if not any_shared:
+            assert sf <= int(pc["lo"])
     read = {(b, g): [] for b in range(n) for g in range(Hk)}
     written = {(b, g): [] for b in range(n) for g in range(Hk)}
     direct = {(b, g): 0 for b in range(n) for g in range(Hk)}
