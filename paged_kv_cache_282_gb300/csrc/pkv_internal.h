@@ -39,8 +39,8 @@ constexpr int tc_head_group(int kv, int G, int D) {
 // of each ring and dynamic shared memory.  One-head units keep a ring per
 // warp (7 warps x 2 stages of 8 KB for bf16 head_dim 128: fewer, longer
 // runs per SM stream faster than 12 x 2; 16 warps for one-byte codes, which
-// the 64-split batch needs; 12 or 16 otherwise); units of several heads fill
-// about 200 KB with stages.
+// the 64-split batch needs; 12 for bf16 at head_dim 64, 12 or 16
+// otherwise); units of several heads fill about 200 KB with stages.
 // Bytes of one unit in a stage: K then V of hg heads (+ their scales).
 constexpr int tc_unit_bytes(int kv, int D, int hg) {
   return 2 * hg * kBlock * D * (kv == 1 ? 2 : 1) + (kv == 1 ? 0 : hg * 128);
@@ -66,8 +66,11 @@ constexpr int tc_unit_bytes(int kv, int D, int hg) {
 #ifndef PKV_BF_UPS
 #define PKV_BF_UPS 1
 #endif
-#ifndef PKV_D64_WARPS  // one-head units at head_dim 64, one sequence per warp
-#define PKV_D64_WARPS 16
+#ifndef PKV_D64_BF_WARPS  // one-head units at head_dim 64, one sequence per warp: bf16
+#define PKV_D64_BF_WARPS 12
+#endif
+#ifndef PKV_D64_OB_WARPS  // ... and one-byte codes
+#define PKV_D64_OB_WARPS 16
 #endif
 #ifndef PKV_D64_STAGES
 #define PKV_D64_STAGES 0  // 0: 2 for bf16, 3 for one-byte codes
@@ -89,7 +92,7 @@ constexpr int tc_warps(int kv, int nq, int D, int hg) {
          : nq == 2 && (D == 128 || kv != 1)   ? PKV_PAIR_WARPS
          : nq == 1 && D == 128 && kv != 1     ? PKV_OB_WARPS
          : nq == 1 && D == 128 && kv == 1     ? PKV_BF_WARPS
-         : nq == 1                            ? PKV_D64_WARPS
+         : nq == 1                            ? (kv == 1 ? PKV_D64_BF_WARPS : PKV_D64_OB_WARPS)
          : D == 128 && kv == 1                ? 12
                                               : 16;
 }
