@@ -291,11 +291,16 @@ constexpr int kSelSample = 2048;    // keys sampled to pick the one-pass thresho
 constexpr int kSelSampleMinRow = 16384;  // rows longer than this take the sampled one-pass path
 // The gather streams a row through a ring of bulk copies: kSelRing stages of
 // kSelChunk scores, one chunk per sweep (kSelChunk / kSelThreads per thread).
-constexpr int kSelChunk = 8192;
-constexpr int kSelRing = 4;
+#ifndef PKV_SEL_CHUNK
+#define PKV_SEL_CHUNK 8192
+#endif
+#ifndef PKV_SEL_RING
+#define PKV_SEL_RING 4
+#endif
+constexpr int kSelChunk = PKV_SEL_CHUNK;
+constexpr int kSelRing = PKV_SEL_RING;
 constexpr size_t kSelSmem = (size_t)kSelCap * 8 + (size_t)kSelRing * kSelChunk * 4;
 static_assert(kSelSample % kSelThreads == 0 && kSelChunk % (4 * kSelThreads) == 0, "select geometry");
-static_assert(kSelSmem <= 200 * 1024, "select shared memory");
 
 template <int N>
 struct IntTag {
@@ -313,6 +318,7 @@ struct SelShared {
   int starve;     // test hook: the first chunk of this block's row is never issued
   int undrained;  // a copy into the ring was still in flight when the drain gave up
 };
+static_assert(kSelSmem + sizeof(SelShared) <= 227 * 1024, "select shared memory");
 
 // Slot of candidate i in the shared candidate arrays: the word index with its
 // low 3 bits XORed by bits 5-7.  A row of 32 consecutive candidates stays one
