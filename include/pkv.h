@@ -258,9 +258,8 @@ pkv_status pkv_decode_attn(pkv_pool* pool, void* stream, int32_t n_seqs, const i
  *     PKV_ERR_WORKSPACE and a message giving both sizes; nothing is launched.
  *   - The first call on a device looks up the array's device address (once per
  *     device, with that device current) and keeps it for the life of the
- *     process; make that first call before any stream capture.  After the
- *     device's primary context is reset, the kept address is stale: do not
- *     call this entry point again in that process.
+ *     process.  After the device's primary context is reset, the kept
+ *     address is stale: do not call this entry point again in that process.
  *   - Every device that runs this entry point keeps the 32 MiB until the
  *     process exits.  All calls share the array: calls whose work overlaps on
  *     the GPU (other streams, other pools on the same device) race on it. */
