@@ -380,7 +380,9 @@ __device__ void fail_and_drain(const DecodeTCParams& p, uint32_t full, int from,
 // pieces of HG chunks while every warp runs the one-head computation.  The
 // plan names teams ("warps" of the plan) and units of HG heads, whose records
 // hold GV = GP HG query heads.
-template <int KV, int GP, int HG, int NQ, int D>
+// EF: one-sequence rings whose K / V copies all take the L2 evict-first
+// policy (chosen per call on the host, DecodeTCParams::kv_evict_first).
+template <int KV, int GP, int HG, int NQ, int D, bool EF = false>
 __global__ void __launch_bounds__(TC<KV, NQ, D, HG>::kWarps * 32, 1)
     decode_tc_kernel(const __grid_constant__ DecodeTCParams p) {
   using C = TC<KV, NQ, D, HG>;
@@ -495,8 +497,8 @@ __global__ void __launch_bounds__(TC<KV, NQ, D, HG>::kWarps * 32, 1)
       for (int j = 0; j < C::kUPS; ++j) {
         if (j >= nu) break;
         // read once by this call: the copies may leave L2 first (the pair
-        // rings decide per unit, the one-sequence rings per call)
-        const bool once = NQ == 2 ? rows[j] >= 0 : p.kv_evict_first != 0;
+        // rings decide per unit, the one-sequence rings per call, as EF)
+        const bool once = NQ == 2 ? rows[j] >= 0 : EF;
         const int row = NQ == 2 && rows[j] < 0 ? -rows[j] - 2 : rows[j];
         const uint32_t dst = data + (uint32_t)(st * C::kStageBytes + j * C::kUnitBytes);
         const int y = ycoord(row);
@@ -934,14 +936,27 @@ __global__ void __launch_bounds__(TC<KV, NQ, D, HG>::kWarps * 32, 1)
 // GP: query heads per kv head; HG: kv heads per unit (warps per team).
 template <int KV, int GP, int HG, int NQ, int D>
 cudaError_t launch_t(const DecodeTCParams& p, int ctas, cudaStream_t st) {
-  decode_tc_kernel<KV, GP, HG, NQ, D><<<ctas, TC<KV, NQ, D, HG>::kWarps * 32, tc_smem_bytes(KV, NQ, D, HG), st>>>(p);
+  constexpr int threads = TC<KV, NQ, D, HG>::kWarps * 32;
+  constexpr size_t smem = tc_smem_bytes(KV, NQ, D, HG);
+  if constexpr (NQ == 1 && HG == 1) {
+    if (p.kv_evict_first) {
+      decode_tc_kernel<KV, GP, HG, NQ, D, true><<<ctas, threads, smem, st>>>(p);
+      return cudaGetLastError();
+    }
+  }
+  decode_tc_kernel<KV, GP, HG, NQ, D><<<ctas, threads, smem, st>>>(p);
   return cudaGetLastError();
 }
 
 template <int KV, int GP, int HG, int NQ, int D>
 cudaError_t prepare_t() {
-  return cudaFuncSetAttribute(decode_tc_kernel<KV, GP, HG, NQ, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)tc_smem_bytes(KV, NQ, D, HG));
+  const int smem = (int)tc_smem_bytes(KV, NQ, D, HG);
+  if constexpr (NQ == 1 && HG == 1) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(decode_tc_kernel<KV, GP, HG, NQ, D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaFuncSetAttribute(decode_tc_kernel<KV, GP, HG, NQ, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
 template <int KV, int GP, int HG, int NQ, int D>

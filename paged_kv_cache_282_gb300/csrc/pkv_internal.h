@@ -228,7 +228,7 @@ struct DecodeTCParams {
   int32_t n_prefix_items;
   const float* k_channel;  // per-channel scales [Hk][D] of an FP8 / INT8 pool, or nullptr
   const float* v_channel;
-  int32_t kv_evict_first;  // one-sequence rings: K / V copies with an L2 evict-first policy
+  int32_t kv_evict_first;  // one-sequence rings: launch the variant whose K / V copies are evict-first in L2
 };
 
 struct DecodeF32Params {
