@@ -23,7 +23,10 @@
 //    swizzle, so the fragment loads below are bank-conflict free) and
 //    completed through mbarrier transaction counts.  Lane 0 refills a stage as
 //    soon as the warp has consumed it; physical block ids for the next 32
-//    units are fetched one batch ahead.
+//    units are fetched one batch ahead.  K / V that the call reads only once
+//    are copied with an L2 evict-first policy, so they do not push the block
+//    tables, plans, records and shared prefixes out of L2 (one-sequence rings:
+//    a launch variant chosen per call; pair rings: per piece).
 //  - Every K/V byte is read once per GQA group: the G query heads are the N
 //    dimension of m16n8k16 tensor-core MMAs (S = K Q^T, then O^T = V^T P),
 //    with fp32 accumulation.  The path is HBM-bound (4 flop/byte for BF16,
